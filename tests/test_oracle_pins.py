@@ -1,0 +1,430 @@
+"""Pins of the CPU oracle to facts outside itself (no GPU needed).
+
+Each test names the passage it follows.  The oracle is test infrastructure;
+these tests are what make it trustworthy as the parity reference.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+from conftest import golden_lines
+
+
+# ---------------------------------------------------------------- Philox
+
+def test_philox_known_answers(oracle):
+    """Random123 known-answer vectors for Philox4x32-10 (Salmon et al., SC'11)."""
+    rows = golden_lines("philox4x32_10_kat.txt")
+    assert len(rows) == 3
+    for ln in rows:
+        lhs, rhs = ln.split("->")
+        vals = [int(x, 16) for x in lhs.split()]
+        want = [int(x, 16) for x in rhs.split()]
+        assert oracle.philox4x32_10(vals[:4], vals[4:6]) == want
+
+
+def test_uniform_mapping(oracle):
+    """u_accept uses the top 24 bits of word 0, u_sample the top 53 bits of
+    (w0:w1); counter = (b, k, draw, 0), key = (lo32(seed), hi32(seed))."""
+    seed = 0x0123456789ABCDEF
+    for b, k in [(0, 0), (5, 3), (511, 15), (2**31, 7)]:
+        w = oracle.philox4x32_10([b, k, 0, 0], [seed & 0xFFFFFFFF, seed >> 32])
+        assert oracle.u_accept(seed, b, k) == (w[0] >> 8) / 2.0**24
+        w = oracle.philox4x32_10([b, k, 1, 0], [seed & 0xFFFFFFFF, seed >> 32])
+        assert oracle.u_sample(seed, b, k) == (((w[0] << 32) | w[1]) >> 11) / 2.0**53
+    us = [oracle.u_accept(7, b, 0) for b in range(2000)]
+    assert 0.0 <= min(us) and max(us) < 1.0
+    assert abs(np.mean(us) - 0.5) < 0.03
+
+
+# ---------------------------------------------------------------- hand rule
+
+def _logp(p):
+    p = np.asarray(p, dtype=np.float64)
+    with np.errstate(divide="ignore"):
+        return np.where(p > 0, np.log(np.where(p > 0, p, 1.0)), -np.inf)
+
+
+def test_hand_rule_4_tokens(oracle):
+    """'Правило проверки' (kiosknews.app, 'Немного теории'), worked by hand."""
+    rows = golden_lines("hand_rule_4tok.txt")
+    assert len(rows) >= 8
+    for ln in rows:
+        name, p, q, x, ua, acc, us, tok = [f.strip() for f in ln.split("|")]
+        p = [float(v) for v in p.split()]
+        q = [float(v) for v in q.split()]
+        x, acc, tok = int(x), int(acc), int(tok)
+        ua, us = float(ua), float(us)
+        target = np.stack([_logp(p), np.zeros(4)])       # row 1: bonus row (uniform)
+        draft = _logp(q)[None, :]
+        out, a = oracle.verify_request_u(target, draft, [x], 1, 1.0, [ua], us)
+        assert a == acc, name
+        if acc:
+            assert out[0] == x, name
+        else:
+            assert out[0] == tok, name
+        assert out[1] == (-1 if not acc else out[1]), name
+
+
+def test_hand_bonus_token(oracle):
+    """All drafts accepted -> one more token from the target row K+1 (braintools.ru,
+    'Как это работает': 'ещё один следующий токен – итого шесть')."""
+    p1 = [0.1, 0.2, 0.3, 0.4]  # bonus row
+    target = np.stack([_logp([0.25] * 4), _logp(p1)])
+    draft = _logp([0.25] * 4)[None, :]
+    # C = (.1,.3,.6,1.0)
+    for u, want in [(0.0, 0), (0.05, 0), (0.15, 1), (0.35, 2), (0.7, 3), (0.999, 3)]:
+        out, a = oracle.verify_request_u(target, draft, [2], 1, 1.0, [0.5], u)
+        assert a == 1 and out[0] == 2 and out[1] == want
+
+
+def test_inverse_cdf_edges(oracle):
+    assert oracle.inverse_cdf([0.0, 0.0, 1.0, 0.0], 0.0)[0] == 2
+    assert oracle.inverse_cdf([0.0, 0.0, 1.0, 0.0], 0.999999)[0] == 2
+    assert oracle.inverse_cdf([1.0, 1.0], 0.5)[0] == 1       # C_0 = 1 is not > 1
+    assert oracle.inverse_cdf([1.0, 1.0], 0.4999)[0] == 0
+    # residual with Z == 0 falls back to p
+    t, _ = oracle.sample_residual([0.5, 0.5], [0.5, 0.5], 0.75)
+    assert t == 1
+
+
+# ---------------------------------------------------------------- exact law
+
+def _tables(rng, V, K, spread=1.0):
+    """Context-dependent target P(.|prefix) for prefixes of length 0..K and
+    draft Q(.|prefix) for lengths 0..K-1, as dicts keyed by prefix tuples."""
+    P, Q = {}, {}
+    for n in range(K + 1):
+        for pre in itertools.product(range(V), repeat=n):
+            P[pre] = rng.dirichlet(np.full(V, spread))
+            if n < K:
+                Q[pre] = rng.dirichlet(np.full(V, spread))
+    return P, Q
+
+
+def _bisect(f, lo=0.0, hi=1.0, iters=60):
+    """Largest u in [lo,hi) with f(u) True assuming f is True then False."""
+    for _ in range(iters):
+        mid = 0.5 * (lo + hi)
+        if f(mid):
+            lo = mid
+        else:
+            hi = mid
+    return lo
+
+
+def _emitted_law(oracle, P, Q, V, K, T):
+    """Exact output law of the oracle for every draft sequence, integrating
+    the acceptance and sampling uniforms by bisection on the oracle's own
+    decisions (which are monotone in u).  Returns {emitted tuple: prob}."""
+    law = {}
+    one = 1.0 - 2.0**-40
+    T = float(np.float32(T))  # the oracle reads T as float32
+    for x in itertools.product(range(V), repeat=K):
+        wx = 1.0
+        for k in range(K):
+            wx *= Q[x[:k]][x[k]]
+        tgt = np.stack([np.log(P[x[:k]]) * T for k in range(K + 1)])
+        drf = np.stack([np.log(Q[x[:k]]) * T for k in range(K)])
+
+        def run(ua, us):
+            return oracle.verify_request_u(tgt, drf, x, K, T, ua, us)
+
+        # acceptance probability at each position, positions before it forced
+        # to accept (u = 0 accepts since every p > 0)
+        acc = []
+        for k in range(K):
+            def accepted(u, k=k):
+                ua = [0.0] * K
+                ua[k] = u
+                return run(ua, 0.5)[1] > k
+            if accepted(one):
+                acc.append(1.0)
+            else:
+                acc.append(_bisect(accepted))
+        reach = 1.0
+        for a in range(K + 1):
+            if a < K:
+                pr_stop = reach * (1.0 - acc[a])
+            else:
+                pr_stop = reach
+            if pr_stop > 0.0:
+                ua = [0.0] * K
+                if a < K:
+                    ua[a] = one
+                # token(u) is non-decreasing in u: find each boundary
+                prev = 0.0
+                for v in range(V):
+                    if v < V - 1:
+                        bnd = _bisect(lambda u: run(ua, u)[0][a] <= v)
+                        if run(ua, 0.0)[0][a] > v:
+                            bnd = 0.0
+                    else:
+                        bnd = 1.0
+                    pv = max(0.0, bnd - prev)
+                    prev = max(prev, bnd)
+                    if pv > 0.0:
+                        e = tuple(x[:a]) + (v,)
+                        law[e] = law.get(e, 0.0) + wx * pr_stop * pv
+            if a < K:
+                reach *= acc[a]
+    return law
+
+
+@pytest.mark.parametrize("V,K,T,seed", [(4, 3, 1.0, 1), (5, 2, 0.7, 2), (8, 2, 1.3, 3)])
+def test_lossless_exact_enumeration(oracle, V, K, T, seed):
+    """'Утверждение 1' (kiosknews.app): the emitted tokens follow the target
+    law exactly, whatever q.  Continuing with target sampling after the
+    emitted prefix must reproduce P_target for every length-(K+1) sequence."""
+    rng = np.random.default_rng(seed)
+    P, Q = _tables(rng, V, K)
+    law = _emitted_law(oracle, P, Q, V, K, T)
+    assert abs(sum(law.values()) - 1.0) < 1e-12
+    worst = 0.0
+    for s in itertools.product(range(V), repeat=K + 1):
+        want = 1.0
+        for j in range(K + 1):
+            want *= P[s[:j]][s[j]]
+        got = 0.0
+        for n in range(1, K + 2):
+            e = s[:n]
+            if e in law:
+                cont = 1.0
+                for j in range(n, K + 1):
+                    cont *= P[s[:j]][s[j]]
+                got += law[e] * cont
+        worst = max(worst, abs(got - want))
+    assert worst < 1e-12
+    # first emitted token ~ p_0
+    first = np.zeros(V)
+    for e, pr in law.items():
+        first[e[0]] += pr
+    assert np.max(np.abs(first - P[()])) < 1e-12
+
+
+MUTANTS = {
+    # the acceptance ratio inverted: accept with min(1, q/p)
+    "inverted_ratio": ("return u * q_x < p_x;", "return u * p_x < q_x;"),
+    # residual of the wrong sign: max(0, q - p)
+    "residual_sign": ("double d = p[v] - q[v];", "double d = q[v] - p[v];"),
+    # after a rejection sample from p instead of the residual
+    "resample_from_p": ("return svo_inverse_cdf(r_scratch, V, u, margin);",
+                        "return svo_inverse_cdf(p, V, u, margin);"),
+    # bonus token taken from the last draft row's target row instead of row K
+    "bonus_row": ("svo_row_softmax(svo_row(tgt, dtype, (size_t)a, V), dtype, V, Td, p, NULL, NULL);",
+                  "svo_row_softmax(svo_row(tgt, dtype, (size_t)(a > 0 ? a - 1 : 0), V), dtype, V, Td, p, NULL, NULL);"),
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_exact_enumeration_catches_planted_mistakes(oracle, mutant, tmp_path):
+    """The enumeration check is sensitive: a copy of the oracle with one
+    planted mistake (compiled on the CPU into a temporary library) breaks the
+    lossless identity."""
+    import ctypes
+    import os
+    import subprocess
+    import oracle.build as ob
+    src = open(ob.SRC).read()
+    old, new = MUTANTS[mutant]
+    assert src.count(old) == 1, mutant
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(old, new))
+    so = str(tmp_path / "libmutant.so")
+    subprocess.check_call(["gcc", *ob.CFLAGS, str(path), "-o", so, "-lm", "-lpthread"])
+    good = oracle.lib()
+    mut = ctypes.CDLL(so)
+    mut.svo_verify_request_u.argtypes = good.svo_verify_request_u.argtypes
+    rng = np.random.default_rng(5)
+    V, K = 4, 2
+    P, Q = _tables(rng, V, K)
+    oracle._lib = mut
+    try:
+        law = _emitted_law(oracle, P, Q, V, K, 1.0)
+    finally:
+        oracle._lib = good
+    worst = 0.0
+    for s in itertools.product(range(V), repeat=K + 1):
+        want = 1.0
+        for j in range(K + 1):
+            want *= P[s[:j]][s[j]]
+        got = 0.0
+        for n in range(1, K + 2):
+            e = s[:n]
+            if e in law:
+                cont = 1.0
+                for j in range(n, K + 1):
+                    cont *= P[s[:j]][s[j]]
+                got += law[e] * cont
+        worst = max(worst, abs(got - want))
+    assert worst > 1e-4, mutant
+
+
+# ---------------------------------------------------------------- greedy
+
+def test_greedy_equals_argmax_decoding(oracle):
+    """braintools.ru, 'Почему ответ не портится': at temperature 0 the check is
+    an argmax comparison, so the output equals autoregressive argmax decoding
+    for accept_len + 1 steps; ties go to the lowest index."""
+    rng = np.random.default_rng(11)
+    V, K = 5, 3
+    P = {}
+    for n in range(K + 1):
+        for pre in itertools.product(range(V), repeat=n):
+            z = rng.integers(-3, 3, size=V).astype(np.float32)  # integer logits: many ties
+            P[pre] = z
+    for x in itertools.product(range(V), repeat=K):
+        tgt = np.stack([P[x[:k]] for k in range(K + 1)])
+        for T in (0.0, -1.0, float("nan"), 1e-45):  # all greedy
+            out, a = oracle.verify_request_u(tgt, None, x, K, T, [0.5] * K, 0.5)
+            g = []
+            for j in range(K + 1):
+                pre = tuple(g)
+                z = P[pre]
+                g.append(int(np.flatnonzero(z == z.max())[0]))
+                if j < K and x[j] != g[-1]:
+                    break
+            assert a == len(g) - 1
+            assert list(out[:a + 1]) == g
+            assert all(v == -1 for v in out[a + 1:])
+
+
+def test_greedy_bf16_ties_lowest_index(oracle):
+    bits = np.array([0x3F80, 0x4000, 0x4000, 0x3F80], dtype=np.uint16)  # 1, 2, 2, 1
+    assert oracle.row_argmax(bits) == 1
+    assert oracle.row_argmax(np.array([-np.inf, -np.inf, 3.0, 3.0], np.float32)) == 2
+
+
+# ---------------------------------------------------------------- statistics
+
+def test_chi_square_first_token(oracle):
+    """10^6 seeded oracle trials (its own Philox): the first emitted token is
+    distributed as p_0 ('Утверждение 1'); chi-square p-value > 0.01."""
+    stats = pytest.importorskip("scipy.stats")
+    rng = np.random.default_rng(20261202)
+    V, K, T, N = 16, 3, 0.9, 1_000_000
+    tgt = rng.normal(0, 1.5, size=(1, K + 1, V)).astype(np.float32)
+    drf = (tgt[:, :K] + rng.normal(0, 1.0, size=(1, K, V))).astype(np.float32)
+    q = np.stack([oracle.row_softmax(drf[0, k], T)[0] for k in range(K)])
+    p0 = oracle.row_softmax(tgt[0, 0], T)[0]
+    toks = np.stack([rng.choice(V, size=N, p=q[k] / q[k].sum()) for k in range(K)], axis=1)
+    res = oracle.verify(tgt, drf, toks.astype(np.int32), None, np.full(N, T, np.float32),
+                        seed=99, nthreads=oracle.cpu_count(), broadcast_rows=True)
+    counts = np.bincount(res["out_tokens"][:, 0], minlength=V).astype(np.float64)
+    exp = p0 * N
+    order = np.argsort(exp)
+    obs_m, exp_m, acc_o, acc_e = [], [], 0.0, 0.0
+    for i in order:  # merge small bins until expected >= 5
+        acc_o += counts[i]
+        acc_e += exp[i]
+        if acc_e >= 5:
+            obs_m.append(acc_o)
+            exp_m.append(acc_e)
+            acc_o = acc_e = 0.0
+    if acc_e > 0:
+        obs_m[-1] += acc_o
+        exp_m[-1] += acc_e
+    exp_m = np.array(exp_m) * (N / np.sum(exp_m))
+    pval = stats.chisquare(obs_m, exp_m).pvalue
+    assert pval > 0.01, pval
+    # the draft is poor on purpose: many rejections were exercised
+    assert np.mean(res["accept_len"]) < 2.0
+
+
+def test_mean_accept_length_closed_form(oracle):
+    """'Утверждение 2' (kiosknews.app): E[A] = sum_k P(A >= k); with x_k ~ q_k
+    drawn independently, P(A >= j) = prod_{k<j} beta_k, beta_k = sum min(p_k, q_k)."""
+    from oracle import tau
+    rng = np.random.default_rng(3)
+    V, K, T, N = 12, 4, 1.0, 200_000
+    tgt = rng.normal(0, 1.0, size=(1, K + 1, V)).astype(np.float32)
+    drf = (tgt[:, :K] + rng.normal(0, 0.6, size=(1, K, V))).astype(np.float32)
+    p = np.stack([oracle.row_softmax(tgt[0, k], T)[0] for k in range(K)])
+    q = np.stack([oracle.row_softmax(drf[0, k], T)[0] for k in range(K)])
+    beta = np.minimum(p, q).sum(axis=1)
+    toks = np.stack([rng.choice(V, size=N, p=q[k] / q[k].sum()) for k in range(K)], axis=1)
+    res = oracle.verify(tgt, drf, toks.astype(np.int32), None, np.full(N, T, np.float32),
+                        seed=5, nthreads=oracle.cpu_count(), broadcast_rows=True)
+    a = res["accept_len"].astype(np.float64)
+    want = tau.mean_accept_len(beta)
+    assert abs(a.mean() - want) < 4.0 * a.std() / math.sqrt(N)
+    # survival profile matches position by position
+    for j in range(1, K + 1):
+        pj = np.prod(beta[:j])
+        got = np.mean(a >= j)
+        assert abs(got - pj) < 4.0 * math.sqrt(pj * (1 - pj) / N) + 1e-12
+
+
+# ---------------------------------------------------------------- tau helpers
+
+def test_tau_helpers_match_printed_values():
+    """Numbers printed by braintools.ru ('Сколько это даёт') and the DFlash 2
+    survival profile and table of kiosknews.app ('Утверждение 2')."""
+    from oracle import tau
+    for ln in golden_lines("tau_values.txt"):
+        lhs, rhs = ln.split("=")
+        f = lhs.split()
+        kind, args = f[0], [float(v) for v in f[1:]]
+        vals = [float(v) for v in rhs.split()]
+        tol = vals[-1]
+        if kind == "expected_tokens":
+            assert abs(tau.expected_tokens(args[0], int(args[1])) - vals[0]) < tol
+        elif kind == "speedup":
+            assert abs(tau.speedup(args[0], int(args[1]), args[2]) - vals[0]) < tol
+        elif kind == "best_gamma":
+            g, s = tau.best_gamma(args[0], args[1])
+            assert g == int(vals[0]) and abs(s - vals[1]) < tol
+        elif kind == "best_speedup":
+            assert abs(tau.best_gamma(args[0], args[1])[1] - vals[0]) < tol
+        elif kind == "survival":
+            assert abs(tau.tau_from_survival(args) - vals[0]) < tol
+        else:
+            raise AssertionError(kind)
+
+
+# ---------------------------------------------------------------- schedule
+
+def test_schedule_hand_cases(oracle):
+    """DSpark (iitog.ru): verify length from the survival probability of the
+    draft prefix, read as the running product of draft max-probabilities."""
+    mp = np.array([[0.9, 0.8, 0.5],
+                   [0.9, 0.8, 0.5],
+                   [0.2, 0.9, 0.9],
+                   [1.0, 1.0, 1.0],
+                   [0.9, float("nan"), 1.0]], dtype=np.float32)
+    thr = [0.3, 0.4, 0.3, 0.3, 0.3]
+    # products 0.9, 0.72, 0.36: all >= 0.3 -> 3; 0.36 < 0.4 -> 2; 0.2 < 0.3 -> 0
+    want = [3, 2, 0, 3, 1]
+    for b in range(5):
+        assert oracle.schedule_len(mp[b:b + 1], thr[b])[0] == want[b]
+    assert list(oracle.schedule_len(mp, 0.3)) == [3, 3, 0, 3, 1]
+    assert oracle.schedule_len(np.array([[0.5, 0.5]], np.float32), 0.25)[0] == 2  # 0.25 >= 0.25
+    assert oracle.schedule_len(np.array([[0.5]], np.float32), 1.5)[0] == 0
+    # float32 rounding of the running product decides: 0.1f*0.1f*... vs threshold
+    c = np.float32(0.7)
+    prods = np.cumprod(np.full(6, c, dtype=np.float32), dtype=np.float32)
+    thr6 = prods[3]  # exactly the 4th float32 product
+    assert oracle.schedule_len(np.full((1, 6), c, np.float32), thr6)[0] == 4
+
+
+# ---------------------------------------------------------------- validation
+
+def test_length_clamp_and_bad_tokens(oracle):
+    rng = np.random.default_rng(0)
+    V, K = 6, 3
+    tgt = rng.normal(size=(4, K + 1, V)).astype(np.float32)
+    drf = rng.normal(size=(4, K, V)).astype(np.float32)
+    toks = np.array([[1, 2, 3], [1, 9, 3], [-1, 2, 3], [0, 0, 0]], np.int32)
+    vl = np.array([5, 3, 2, -2], np.int32)
+    res = oracle.verify(tgt, drf, toks, vl, np.zeros(4, np.float32), seed=1)
+    st = res["status"]
+    assert st[0] == oracle.BAD_LEN            # 5 > K
+    assert st[1] == oracle.BAD_TOKEN          # token 9 >= V at position 1
+    assert res["accept_len"][1] <= 1
+    assert st[2] == oracle.BAD_TOKEN and res["accept_len"][2] == 0
+    assert st[3] == oracle.BAD_LEN and res["accept_len"][3] == 0
+    for b in range(4):
+        a = res["accept_len"][b]
+        assert all(v == -1 for v in res["out_tokens"][b, a + 1:])
