@@ -1,0 +1,437 @@
+"""Benchmark of the verification step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one batch of synthetic inputs
+already resident in HBM: spec_schedule_len (for the confidence-scheduled
+workload c3) and spec_verify.  Default workload: c1 (B=32, K=8, V=151936,
+bf16).  L2 is flushed (a 512 MiB write) before every timed step, outside the
+step's CUDA events.
+
+Printed JSON line (rank 0):
+  value     verified draft positions per second (sum of verify lengths / time)
+  e2e       the same metric through the public API with the step's inputs copied
+            from pinned host memory and the outputs read back, every step
+  roofline  achieved HBM GB/s of the dominant kernel (algorithmic bytes per
+            launch / its CUDA-event duration) against the measured copy peak
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+
+Multi-GPU: replicas only.  Each rank verifies its own batch (seeded by rank);
+value = all ranks' positions / the max over ranks of the timed region.
+--impl reference times the CPU oracle (the only reference implementation: the
+pages publish no code) on the host cores, on the same workload.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+HBM_NOMINAL_GBS = 8000.0
+FALLBACK_PEAK_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_PEAK_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "speculative_decoding_verification_69_gb300", "csrc")
+    for fn in sorted(os.listdir(d)):
+        with open(os.path.join(d, fn), "rb") as f:
+            h.update(fn.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, only if it was taken on the current kernel sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t.get(workload)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return e.get("dram_bytes_per_launch"), e
+    except Exception:
+        pass
+    return None, None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda") if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda") if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample(inp, max_seconds=12.0, min_requests=2):
+    """Time the CPU oracle on a bounded sample of the workload's requests (all
+    host cores, rows-parallel over requests).  Returns (positions/s, cores,
+    sample description, seconds)."""
+    import oracle
+    h_t = workloads.to_numpy_logits(inp["target"])
+    h_d = workloads.to_numpy_logits(inp["draft"])
+    tok = inp["tokens"].cpu().numpy()
+    vl = inp["verify_len"].cpu().numpy() if inp["verify_len"] is not None else None
+    T = inp["temperature"].cpu().numpy()
+    B, K = tok.shape
+    cores = oracle.cpu_count()
+    # probe one request to size the sample
+    t0 = time.perf_counter()
+    oracle.verify(h_t, h_d, tok, vl, T, inp["seed"], b0=0, b1=1, nthreads=1)
+    one = max(time.perf_counter() - t0, 1e-4)
+    n = int(max(min_requests, min(B, max_seconds * cores / one)))
+    n = min(B, max(n, min(cores, B)))
+    t0 = time.perf_counter()
+    r = oracle.verify(h_t, h_d, tok, vl, T, inp["seed"], b0=0, b1=n, nthreads=min(cores, n))
+    dt = time.perf_counter() - t0
+    pos = int(vl[:n].clip(0, K).sum()) if vl is not None else n * K
+    return pos / dt, min(cores, n), "first %d of %d requests (%d verified positions)" % (n, B, pos), dt, r
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def prepare(cfg, rank, device):
+    inp = workloads.make_inputs(cfg, rep=rank, device=device)
+    if "draft_maxprob" in inp:
+        import speculative_decoding_verification_69_gb300 as sv
+        inp["verify_len"] = sv.schedule_len(inp["draft_maxprob"], inp["threshold"])
+    return inp
+
+
+def run_ours(args, world, rank, local):
+    import speculative_decoding_verification_69_gb300 as sv
+    sv.load_library()
+    dev = torch.device("cuda", local)
+    cfg = args.config
+    inp = prepare(cfg, rank, dev)
+    B, K1, V = inp["target"].shape
+    K = K1 - 1
+    esz = inp["target"].element_size()
+    scheduled = "draft_maxprob" in inp
+    verifier = sv.Verifier()
+    out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    vlen = torch.empty((B,), dtype=torch.int32, device=dev) if scheduled else inp["verify_len"]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        if scheduled:
+            sv.schedule_len(inp["draft_maxprob"], inp["threshold"], out=vlen)
+        verifier(inp["target"], inp["draft"], inp["tokens"], vlen, inp["temperature"],
+                 inp["seed"], out_tokens=out_tokens, accept_len=accept_len)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    positions = workloads.verified_positions(vlen)
+    alg_bytes = workloads.algorithmic_bytes(inp["temperature"], vlen, V, esz)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        sv.profile_events(*kev[i])
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    sv.profile_events(None, None)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    total_s = sum(step_ms) / 1e3
+    total_s_max = max_over_ranks(total_s, world)
+    all_pos = sum_over_ranks(positions * args.steps, world)
+    value = all_pos / total_s_max
+    kern_avg_s = sum(kern_ms) / len(kern_ms) / 1e3
+
+    # end to end through the public API: pinned host inputs -> device -> verify -> host
+    host = {k: inp[k].cpu().pin_memory() for k in ("target", "draft", "tokens", "temperature")}
+    if scheduled:
+        host["draft_maxprob"] = inp["draft_maxprob"].cpu().pin_memory()
+    elif inp["verify_len"] is not None:
+        host["verify_len"] = inp["verify_len"].cpu().pin_memory()
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    h_out = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    h_acc = torch.empty((B,), dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = h_out.numel() * 4 + h_acc.numel() * 4
+
+    def e2e_step():
+        for k, v in host.items():
+            dbuf[k].copy_(v, non_blocking=True)
+        vl = sv.schedule_len(dbuf["draft_maxprob"], inp["threshold"], out=vlen) if scheduled \
+            else dbuf.get("verify_len")
+        o, a = verifier(dbuf["target"], dbuf["draft"], dbuf["tokens"], vl, dbuf["temperature"],
+                        inp["seed"], out_tokens=out_tokens, accept_len=accept_len)
+        h_out.copy_(o, non_blocking=True)
+        h_acc.copy_(a, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    barrier(world)
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        e2e_step()
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev) / 1e3, world)
+    e2e_value = all_pos / e2e_s
+
+    peak, peak_kind = measured_peak()
+    achieved = alg_bytes / kern_avg_s / 1e9
+    traffic, _ = recorded_traffic("c%d" % cfg)
+    launches = (sv.kernels_per_verify() + (1 if scheduled else 0)) * args.steps
+
+    result = {
+        "metric": "verified draft positions/s",
+        "value": value,
+        "unit": "positions/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_s_max * 1e3 / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if inp["target"].dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded logits; no datasets or trained weights)",
+        "config": {
+            "workload": workloads.NAMES[cfg],
+            "B": B, "K": K, "V": V,
+            "verified_positions_per_step": positions,
+            "logit_bytes_per_step": alg_bytes,
+            "logits_GBps": alg_bytes * args.steps / total_s / 1e9,
+            "logits_frac_of_8TBps": alg_bytes * args.steps / total_s / 1e9 / HBM_NOMINAL_GBS,
+            "l2": "flushed before every timed step (512 MiB write, outside the step events)",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "sv_rowstats",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_source": peak_kind,
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "frac_of_8TBps": achieved / HBM_NOMINAL_GBS,
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": alg_bytes,
+            "kernel_ms": kern_avg_s * 1e3,
+        },
+        "e2e": {"value": e2e_value, "unit": "positions/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "wall_s": t_wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pps, cores, sample, dt, _ = oracle_sample(inp, max_seconds=args.cpu_seconds)
+        result["cpu_baseline"] = {"value": pps, "unit": "positions/s", "cores": cores,
+                                  "kind": "oracle", "sample": sample, "seconds": dt}
+    return result
+
+
+def run_reference(args, world, rank, local):
+    """The CPU oracle on the machine's host cores, same workload and metric."""
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    inp = workloads.make_inputs(args.config, rep=0, device=dev)
+    if "draft_maxprob" in inp:
+        import oracle
+        vl = oracle.schedule_len(inp["draft_maxprob"].cpu().numpy(), inp["threshold"])
+        inp["verify_len"] = torch.from_numpy(vl)
+    budget = max(2.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(inp, max_seconds=budget)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        pps, cores, sample, dt, _ = oracle_sample(inp, max_seconds=budget)
+        vals.append(pps)
+        secs.append(dt)
+    value = statistics.median(vals)
+    B, K1, V = inp["target"].shape
+    return {
+        "impl": "reference",
+        "metric": "verified draft positions/s",
+        "value": value,
+        "unit": "positions/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": statistics.median(secs) * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded logits; no datasets or trained weights)",
+        "config": {"workload": workloads.NAMES[args.config], "B": B, "K": K1 - 1, "V": V},
+        "cpu_baseline": {"value": value, "unit": "positions/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        # the CPU oracle: rank 0 alone runs it; other ranks exit without work
+        if int(os.environ.get("RANK", "0")) == 0:
+            local = int(os.environ.get("LOCAL_RANK", "0"))
+            if torch.cuda.is_available():
+                torch.cuda.set_device(local)
+            world = int(os.environ.get("WORLD_SIZE", "1"))
+            print(json.dumps(run_reference(args, world, 0, local)), flush=True)
+        return 0
+    world, rank, local = dist_setup(args.gpus)
+    res = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

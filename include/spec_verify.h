@@ -1,0 +1,183 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) speculative-decoding
+ * verification library (libspecverify.so).
+ *
+ * The operation.  A target model has scored a block of K draft tokens in one
+ * pass, giving logits for K+1 positions; the verifier accepts the longest valid
+ * draft prefix and emits one more token of the target's own:
+ *   - "Спекулятивный декодинг в проде" (kiosknews.app), opening section
+ *     ("Откуда взялся спекулятивный декодинг"): the model accepts the longest
+ *     correct prefix of the draft and places its own token at the first error;
+ *     section "Немного теории", "Правило проверки": a drafted token x is
+ *     accepted with probability min(1, p(x)/q(x)), p the target distribution
+ *     after temperature and q the draft distribution; after a rejection the
+ *     new token is sampled from the normalised residual max(0, p - q);
+ *     "Утверждение 1": the emitted token is then distributed exactly as p.
+ *   - "speculative decoding от черновика до проверки" (braintools.ru), "Как
+ *     это работает", step 3 and the six-token remark: drafts are checked left
+ *     to right, and when all K are accepted one more (bonus) token comes from
+ *     position K+1 of the same pass; "Почему ответ не портится": at
+ *     temperature 0 the check is a comparison with the target argmax.
+ *   - "DSpark: ... верификацией по уверенности" (iitog.ru): the verify length
+ *     of each request is chosen from the estimated survival probability of the
+ *     draft prefix (spec_schedule_len below).
+ *
+ * Conventions (all entry points):
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise; the
+ *     caller owns every buffer.  The calls never allocate or free memory and
+ *     never synchronise the device or the stream; all work is enqueued on
+ *     `stream` (a cudaStream_t passed as void*, NULL = legacy default stream).
+ *   - Host-detectable errors (null required pointers, sizes out of range,
+ *     misaligned buffers, a workspace that is too small, an unknown dtype) are
+ *     returned synchronously and nothing is launched.
+ *   - Data-dependent problems never trap the GPU: they are clamped and
+ *     reported through the optional device status word (SPEC_DEV_* bits,
+ *     OR-ed into *dev_status; the caller zeroes it).
+ *   - Identical inputs and seed give bit-identical outputs.  The random key is
+ *     (seed, request index b, position k, draw); vary `seed` per decoding step.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1, /* null pointer, size out of range, misalignment */
+    SPEC_ERR_UNSUPPORTED = 2, /* dtype or shape this build does not handle */
+    SPEC_ERR_CUDA = 3,        /* a CUDA runtime call (launch) failed */
+    SPEC_ERR_WORKSPACE = 4    /* workspace missing or smaller than required */
+} spec_status_t;
+
+typedef enum {
+    SPEC_DTYPE_F32 = 0, /* IEEE float32 logits */
+    SPEC_DTYPE_BF16 = 1 /* bfloat16 logits */
+} spec_dtype_t;
+
+/* Device status bits (OR-ed into *dev_status when dev_status != NULL). */
+#define SPEC_DEV_BAD_TOKEN 1u /* a draft token outside [0, V): that request's verify
+                                 length is cut to the first such position */
+#define SPEC_DEV_BAD_LEN 2u   /* verify_len outside [0, K]: clamped */
+#define SPEC_DEV_TIMEOUT 4u   /* a bounded device-side wait gave up; outputs of the
+                                 affected request are undefined */
+
+#define SPEC_MAX_K 32          /* largest supported draft length K */
+#define SPEC_MAX_V 0x40000000  /* largest supported vocabulary V (2^30) */
+
+/*
+ * Workspace size in bytes that spec_verify / spec_verify_debug need for the
+ * given problem (0 on invalid sizes).  The workspace is scratch device memory
+ * owned by the caller; it must be 256-byte aligned, need not be initialised,
+ * and must not be shared by calls that may run concurrently.
+ */
+size_t spec_verify_workspace_bytes(int B, int K, int V, spec_dtype_t dtype);
+
+/*
+ * spec_verify -- one verification step for a batch of B independent requests.
+ *
+ *   target_logits [B, K+1, V]  dtype, row-major contiguous.  Row k of request b
+ *                              scores draft token k (k < K) or the bonus
+ *                              position (k = verify length).
+ *   draft_logits  [B, K, V]    dtype, row-major contiguous (never NULL; greedy
+ *                              requests do not read it).
+ *   draft_tokens  [B, K]       int32 drafted tokens x_k.
+ *   verify_len    [B]          int32 number of drafts to verify per request,
+ *                              L_b in [0, K]; NULL means K for every request.
+ *                              Out-of-range values are clamped (SPEC_DEV_BAD_LEN).
+ *   temperature   [B]          float32 per-request temperature T_b.  A request
+ *                              is GREEDY when T_b is not a positive normal
+ *                              float (T <= 0, NaN, inf, or below FLT_MIN):
+ *                              draft token k is accepted iff it equals the
+ *                              target argmax of row k (ties: lowest index),
+ *                              and the emitted token is that argmax.
+ *                              Otherwise SAMPLED: p = softmax(z/T) of the
+ *                              target row, q = softmax(z'/T) of the draft row
+ *                              (the same T), accept x_k iff u_k * q(x_k) <
+ *                              p(x_k) with u_k a Philox uniform on a 2^-24
+ *                              grid; at the first rejection a the emitted token
+ *                              is drawn from max(0, p_a - q_a) (from p_a if that
+ *                              mass is zero); if all L_b drafts are accepted it
+ *                              is drawn from p at row L_b.  Draws are by
+ *                              inverse CDF in ascending token order with a
+ *                              Philox uniform on a 2^-53 grid.
+ *   seed                       64-bit key of the Philox4x32-10 generator.
+ *   B, K, V                    1 <= B < 2^24, 1 <= K <= SPEC_MAX_K,
+ *                              2 <= V <= SPEC_MAX_V.
+ *   out_tokens    [B, K+1]     int32, written: x_0..x_{a-1}, the emitted token
+ *                              at position a, -1 after it.
+ *   accept_len    [B]          int32, written: a (number of accepted drafts).
+ *   workspace, workspace_bytes scratch of at least
+ *                              spec_verify_workspace_bytes(B, K, V, dtype).
+ *   dev_status                 nullable device uint32, see SPEC_DEV_*.
+ *   stream                     cudaStream_t (as void*).
+ *
+ * Alignment: logits base pointers must be 16-byte aligned; rows whose byte
+ * length V*sizeof(dtype) is not a multiple of 16 take a slower scalar path.
+ * Logit values: -inf is legal (probability 0); NaN and +inf are not supported
+ * (results unspecified, no fault); every row must hold a finite logit.
+ */
+spec_status_t spec_verify(const void *target_logits, const void *draft_logits,
+                          spec_dtype_t dtype, const int32_t *draft_tokens,
+                          const int32_t *verify_len, const float *temperature, uint64_t seed,
+                          int B, int K, int V, int32_t *out_tokens, int32_t *accept_len,
+                          void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                          void *stream);
+
+/*
+ * spec_verify_debug -- spec_verify plus the intermediates used for parity:
+ *   row_stats [B, 2K+1, 2] float64: for target rows k = 0..K (index k) and draft
+ *             rows k = 0..K-1 (index K+1+k): { max_v z_v/T, log sum_v exp(z_v/T - max) }.
+ *             Rows the step did not read (beyond the verify length, draft rows of
+ *             greedy requests, all rows of greedy requests) hold NaN.
+ *   probs     [B, K, 2] float64: { p_k(x_k), q_k(x_k) } for sampled requests and
+ *             k < L_b; NaN elsewhere.
+ * Either pointer may be NULL.  Same contract otherwise.
+ */
+spec_status_t spec_verify_debug(const void *target_logits, const void *draft_logits,
+                                spec_dtype_t dtype, const int32_t *draft_tokens,
+                                const int32_t *verify_len, const float *temperature,
+                                uint64_t seed, int B, int K, int V, int32_t *out_tokens,
+                                int32_t *accept_len, void *workspace, size_t workspace_bytes,
+                                uint32_t *dev_status, double *row_stats, double *probs,
+                                void *stream);
+
+/*
+ * spec_schedule_len -- confidence-scheduled verify length (DSpark, iitog.ru):
+ *   verify_len[b] = number of leading positions k whose running product
+ *   prod_{j<=k} draft_maxprob[b, j] stays >= threshold, the product taken left
+ *   to right in float32 with every step rounded to nearest (no fused
+ *   multiply-add).  The empty product is 1, so verify_len[b] >= 0; NaN stops
+ *   the scan.
+ *   draft_maxprob [B, K] float32 device, verify_len [B] int32 device (written).
+ *   1 <= B < 2^24, 1 <= K <= SPEC_MAX_K.
+ */
+spec_status_t spec_schedule_len(const float *draft_maxprob, float threshold, int B, int K,
+                                int32_t *verify_len, void *stream);
+
+/*
+ * spec_profile_events -- measurement hook.  When both events are non-NULL
+ * (cudaEvent_t values passed as void*), every later spec_verify /
+ * spec_verify_debug call records ev_start immediately before and ev_end
+ * immediately after the launch of its dominant (logit-streaming) kernel, on
+ * the call's stream, so a caller can time that kernel alone.  Pass NULL, NULL
+ * to switch it off.  Process-global, not thread-safe; the events stay owned by
+ * the caller.
+ */
+void spec_profile_events(void *ev_start, void *ev_end);
+
+/* Number of kernels one spec_verify call launches (for launch accounting). */
+int spec_verify_kernel_count(void);
+
+/* Static description of a status code. */
+const char *spec_status_str(spec_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

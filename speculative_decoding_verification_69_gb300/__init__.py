@@ -1,0 +1,202 @@
+"""GB300-native verification step of speculative decoding.
+
+Thin Python binding (ctypes) over the C ABI of libspecverify.so
+(include/spec_verify.h).  The binding only marshals arguments: tensors are
+passed as raw device pointers with torch's current CUDA stream; every step of
+the verification runs in the library's sm_103a kernels.  There is no CPU or
+PyTorch fallback: if the library is missing or fails to load, every call
+raises.
+
+    out_tokens, accept_len = verify(target, draft, tokens, verify_len, temperature, seed)
+    verify_len = schedule_len(draft_maxprob, threshold)
+"""
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+SPEC_OK = 0
+DTYPE_F32, DTYPE_BF16 = 0, 1
+DEV_BAD_TOKEN, DEV_BAD_LEN, DEV_TIMEOUT = 1, 2, 4
+MAX_K = 32
+
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library():
+    """Load libspecverify.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if _build.stale():
+        _build.build()
+    if not os.path.exists(path):
+        raise SpecVerifyError("libspecverify.so is not built: run __graft_entry__.build()")
+    L = ctypes.CDLL(path)
+    vp, i32p, f32p, u32p, f64p = (ctypes.c_void_p,) * 5
+    L.spec_verify_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    L.spec_verify_workspace_bytes.restype = ctypes.c_size_t
+    common = [vp, vp, ctypes.c_int, i32p, i32p, f32p, ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
+              ctypes.c_int, i32p, i32p, vp, ctypes.c_size_t, u32p]
+    L.spec_verify.argtypes = common + [vp]
+    L.spec_verify.restype = ctypes.c_int
+    L.spec_verify_debug.argtypes = common + [f64p, f64p, vp]
+    L.spec_verify_debug.restype = ctypes.c_int
+    L.spec_schedule_len.argtypes = [f32p, ctypes.c_float, ctypes.c_int, ctypes.c_int, i32p, vp]
+    L.spec_schedule_len.restype = ctypes.c_int
+    L.spec_profile_events.argtypes = [vp, vp]
+    L.spec_profile_events.restype = None
+    L.spec_verify_kernel_count.argtypes = []
+    L.spec_verify_kernel_count.restype = ctypes.c_int
+    L.spec_status_str.argtypes = [ctypes.c_int]
+    L.spec_status_str.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def exported_symbols():
+    return ["spec_verify_workspace_bytes", "spec_verify", "spec_verify_debug",
+            "spec_schedule_len", "spec_profile_events", "spec_verify_kernel_count",
+            "spec_status_str"]
+
+
+def profile_events(start=None, end=None):
+    """Record torch.cuda.Event pairs around the dominant kernel of later calls
+    (None, None switches it off)."""
+    L = load_library()
+    if start is None or end is None:
+        L.spec_profile_events(None, None)
+    else:
+        L.spec_profile_events(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(end.cuda_event))
+
+
+def kernels_per_verify() -> int:
+    return int(load_library().spec_verify_kernel_count())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    raise TypeError("logits must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _check(status: int):
+    if status != SPEC_OK:
+        msg = load_library().spec_status_str(status).decode()
+        raise SpecVerifyError("spec_verify failed: %s (%d)" % (msg, status))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def workspace_bytes(B: int, K: int, V: int, dtype=torch.bfloat16) -> int:
+    code = DTYPE_BF16 if dtype == torch.bfloat16 else DTYPE_F32
+    return int(load_library().spec_verify_workspace_bytes(B, K, V, code))
+
+
+def _prepare(target, draft, tokens, verify_len, temperature):
+    if target.dim() != 3:
+        raise ValueError("target must be [B, K+1, V]")
+    B, K1, V = target.shape
+    K = K1 - 1
+    if draft.shape != (B, K, V) or draft.dtype != target.dtype:
+        raise ValueError("draft must be [B, K, V] with the target's dtype")
+    if tokens.shape != (B, K) or tokens.dtype != torch.int32:
+        raise ValueError("tokens must be int32 [B, K]")
+    if verify_len is not None and (verify_len.shape != (B,) or verify_len.dtype != torch.int32):
+        raise ValueError("verify_len must be int32 [B] or None")
+    if temperature.shape != (B,) or temperature.dtype != torch.float32:
+        raise ValueError("temperature must be float32 [B]")
+    for t in (target, draft, tokens, temperature) + ((verify_len,) if verify_len is not None else ()):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    return B, K, V
+
+
+class Verifier:
+    """Reusable verifier: owns the workspace so repeated calls allocate nothing."""
+
+    def __init__(self):
+        self._ws = None
+
+    def workspace(self, B, K, V, dtype, device):
+        n = workspace_bytes(B, K, V, dtype)
+        if self._ws is None or self._ws.numel() < n or self._ws.device != device:
+            self._ws = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+        return self._ws, n
+
+    def __call__(self, target, draft, tokens, verify_len, temperature, seed, *, out_tokens=None,
+                 accept_len=None, dev_status=None, stream=None, row_stats=None, probs=None):
+        L = load_library()
+        B, K, V = _prepare(target, draft, tokens, verify_len, temperature)
+        dev = target.device
+        if out_tokens is None:
+            out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+        if accept_len is None:
+            accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+        ws, n = self.workspace(B, K, V, target.dtype, dev)
+        args = [_ptr(target), _ptr(draft), _dtype_code(target), _ptr(tokens), _ptr(verify_len),
+                _ptr(temperature), int(seed) & 0xFFFFFFFFFFFFFFFF, B, K, V, _ptr(out_tokens),
+                _ptr(accept_len), _ptr(ws), ws.numel(), _ptr(dev_status)]
+        if row_stats is not None or probs is not None:
+            st = L.spec_verify_debug(*args, _ptr(row_stats), _ptr(probs), _stream(stream))
+        else:
+            st = L.spec_verify(*args, _stream(stream))
+        _check(st)
+        return out_tokens, accept_len
+
+
+_default = None
+
+
+def verify(target, draft, tokens, verify_len, temperature, seed, **kw):
+    """One verification step; see include/spec_verify.h for the semantics.
+    Returns (out_tokens [B, K+1] int32, accept_len [B] int32) on the device."""
+    global _default
+    if _default is None:
+        _default = Verifier()
+    return _default(target, draft, tokens, verify_len, temperature, seed, **kw)
+
+
+def verify_debug(target, draft, tokens, verify_len, temperature, seed, **kw):
+    """verify() plus intermediates: returns (out_tokens, accept_len, row_stats
+    [B, 2K+1, 2] float64, probs [B, K, 2] float64)."""
+    B, K1, V = target.shape
+    K = K1 - 1
+    rs = torch.empty((B, 2 * K + 1, 2), dtype=torch.float64, device=target.device)
+    pr = torch.empty((B, K, 2), dtype=torch.float64, device=target.device)
+    o, a = verify(target, draft, tokens, verify_len, temperature, seed, row_stats=rs, probs=pr, **kw)
+    return o, a, rs, pr
+
+
+def schedule_len(draft_maxprob, threshold, out=None, stream=None):
+    """Confidence-scheduled verify lengths (float32 running product >= threshold)."""
+    L = load_library()
+    if draft_maxprob.dim() != 2 or draft_maxprob.dtype != torch.float32 or not draft_maxprob.is_cuda:
+        raise ValueError("draft_maxprob must be a float32 CUDA tensor [B, K]")
+    draft_maxprob = draft_maxprob.contiguous()
+    B, K = draft_maxprob.shape
+    if out is None:
+        out = torch.empty((B,), dtype=torch.int32, device=draft_maxprob.device)
+    _check(L.spec_schedule_len(_ptr(draft_maxprob), float(threshold), B, K, _ptr(out), _stream(stream)))
+    return out

@@ -1,0 +1,305 @@
+// sv_common.cuh -- device building blocks shared by the verification kernels.
+//
+// Numerics contract (what makes the sampler reproduce the statistics pass bit
+// for bit):
+//   * a logit row is cut into tiles of TE elements; every tile keeps its own
+//     reference m_t = exact max of the raw logits in the tile;
+//   * the weight of element v of tile t is
+//         e_v = ex2.approx( fma(d, c_hi, d * c_lo) ),  d = z_v - m_t,
+//     with (c_hi, c_lo) a two-float split of log2(e)/T (c_hi rounded toward
+//     zero, c_lo >= FLT_MIN > 0 so that d = -inf gives -inf, never NaN);
+//   * every kernel evaluates that expression with the same explicitly rounded
+//     intrinsics (no contraction), so e_v is identical wherever it is formed;
+//   * tile sums use Fast2Sum against a biased accumulator (exact error terms),
+//     and cross-thread sums use two-float arithmetic, so the row normaliser
+//     S = sum_t S_t * 2^((m_t - m) c) is accurate to ~1e-12 relative and
+//     consistent with the e_v that the residual sampler re-forms.
+#pragma once
+#include <cstdint>
+#include <cfloat>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace sv {
+
+constexpr int kThreads = 256;   // threads per CTA of the row-tile kernels
+constexpr int kWarps = kThreads / 32;
+constexpr int kVecPerThread = 8; // 16-byte vectors per thread per tile
+
+enum { kF32 = 0, kBF16 = 1 };
+
+template <int DT> struct Fmt;
+template <> struct Fmt<kBF16> {
+    static constexpr int kEPV = 8;  // elements per 16-byte vector
+    static constexpr int kESZ = 2;
+    static constexpr uint32_t kNegInfWord = 0xFF80FF80u;
+};
+template <> struct Fmt<kF32> {
+    static constexpr int kEPV = 4;
+    static constexpr int kESZ = 4;
+    static constexpr uint32_t kNegInfWord = 0xFF800000u;
+};
+
+template <int DT> __host__ __device__ constexpr int tile_elems() {
+    return kThreads * kVecPerThread * Fmt<DT>::kEPV;
+}
+
+// ------------------------------------------------------------------ loads
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// One 16-byte vector of elements [e0, e0+EPV) of a row; elements at or past V
+// read as -inf.  VEC: the row is 16-byte aligned and V is a multiple of EPV.
+template <int DT, bool VEC>
+__device__ __forceinline__ uint4 load_vec(const char *row, long long e0, int V) {
+    constexpr int EPV = Fmt<DT>::kEPV;
+    const uint32_t ni = Fmt<DT>::kNegInfWord;
+    if (VEC) {
+        if (e0 < V) return ld_stream_v4(row + e0 * Fmt<DT>::kESZ);
+        return make_uint4(ni, ni, ni, ni);
+    } else {
+        uint32_t w[4] = {ni, ni, ni, ni};
+        if (DT == kBF16) {
+            const uint16_t *r = reinterpret_cast<const uint16_t *>(row);
+#pragma unroll
+            for (int i = 0; i < EPV; ++i) {
+                long long e = e0 + i;
+                uint32_t h = e < V ? (uint32_t)__ldg(r + e) : 0xFF80u;
+                if (i & 1) w[i >> 1] = (w[i >> 1] & 0x0000FFFFu) | (h << 16);
+                else w[i >> 1] = (w[i >> 1] & 0xFFFF0000u) | h;
+            }
+        } else {
+            const uint32_t *r = reinterpret_cast<const uint32_t *>(row);
+#pragma unroll
+            for (int i = 0; i < EPV; ++i) {
+                long long e = e0 + i;
+                w[i] = e < V ? __ldg(r + e) : ni;
+            }
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// Element i of a vector as float (exact).
+template <int DT> __device__ __forceinline__ float elem(const uint4 &v, int i) {
+    const uint32_t *w = &v.x;
+    if (DT == kBF16) {
+        uint32_t x = w[i >> 1];
+        return __uint_as_float((i & 1) ? (x & 0xFFFF0000u) : (x << 16));
+    } else {
+        return __uint_as_float(w[i]);
+    }
+}
+
+// Maximum element of a vector (exact).
+template <int DT> __device__ __forceinline__ float vec_max(const uint4 &v) {
+    if (DT == kBF16) {
+        __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&v.x);
+        __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&v.y);
+        __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162 *>(&v.z);
+        __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162 *>(&v.w);
+        __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
+        return fmaxf(__low2float(m), __high2float(m));
+    } else {
+        return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                     fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+    }
+}
+
+// ------------------------------------------------------------------ f32x2
+
+__device__ __forceinline__ unsigned long long f2u(float2 a) {
+    return *reinterpret_cast<unsigned long long *>(&a);
+}
+__device__ __forceinline__ float2 u2f(unsigned long long a) {
+    return *reinterpret_cast<float2 *>(&a);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
+    return u2f(d);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
+    return u2f(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
+    return u2f(d);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)), "l"(f2u(c)));
+    return u2f(d);
+}
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Weights of an element pair: 2^((z - m) * c) with c = c_hi + c_lo.
+__device__ __forceinline__ float2 weight2(float2 z, float2 m2, float2 chi2, float2 clo2) {
+    float2 d = sub2(z, m2);
+    float2 lo = mul2(d, clo2);
+    float2 t = fma2(d, chi2, lo);
+    return make_float2(ex2(t.x), ex2(t.y));
+}
+
+// ------------------------------------------------------------------ two-float
+
+struct FF {
+    float hi, lo;
+};
+
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+    float s = __fadd_rn(a.hi, b.hi);
+    float bb = __fsub_rn(s, a.hi);
+    float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(b.hi, bb));
+    e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+    float hi = __fadd_rn(s, e);
+    float lo = __fsub_rn(e, __fsub_rn(hi, s));
+    return FF{hi, lo};
+}
+
+__device__ __forceinline__ FF ff_shfl_xor(FF a, int m) {
+    return FF{__shfl_xor_sync(0xFFFFFFFFu, a.hi, m), __shfl_xor_sync(0xFFFFFFFFu, a.lo, m)};
+}
+
+__device__ __forceinline__ FF ff_from_double(double x) {
+    float hi = __double2float_rn(x);
+    float lo = __double2float_rn(x - (double)hi);
+    return FF{hi, lo};
+}
+
+__device__ __forceinline__ double ff_to_double(FF a) { return (double)a.hi + (double)a.lo; }
+
+// Per-thread accumulator of non-negative terms <= bias: Fast2Sum against a
+// biased high part keeps every rounding error exactly in the low part.
+struct BiasAcc2 {
+    float2 h, l;
+    float bias;
+    __device__ __forceinline__ void init(float b) {
+        bias = b;
+        h = make_float2(b, b);
+        l = make_float2(0.f, 0.f);
+    }
+    __device__ __forceinline__ void add(float2 e) {
+        float2 s = add2(h, e);
+        float2 z = sub2(s, h);
+        float2 err = sub2(e, z);
+        l = add2(l, err);
+        h = s;
+    }
+    __device__ __forceinline__ FF total() const {
+        FF a{__fsub_rn(h.x, bias), l.x};
+        FF b{__fsub_rn(h.y, bias), l.y};
+        return ff_add(a, b);
+    }
+};
+
+// ------------------------------------------------------------------ CTA reductions
+
+// CTA-wide max; every thread gets the result.  `red` holds kWarps floats.
+__device__ __forceinline__ float cta_max(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int i = 1; i < kWarps; ++i) r = fmaxf(r, red[i]);
+    return r;
+}
+
+// CTA-wide two-float sum; valid in every thread.  `red` holds 2*kWarps floats.
+__device__ __forceinline__ FF cta_sum_ff(FF v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = ff_add(v, ff_shfl_xor(v, o));
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) {
+        red[2 * w] = v.hi;
+        red[2 * w + 1] = v.lo;
+    }
+    __syncthreads();
+    FF r{red[0], red[1]};
+#pragma unroll
+    for (int i = 1; i < kWarps; ++i) r = ff_add(r, FF{red[2 * i], red[2 * i + 1]});
+    return r;
+}
+
+// CTA-wide (max value, lowest index) pair; valid in every thread.
+__device__ __forceinline__ void cta_argmax(float &v, int &idx, float *redv, int *redi) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float ov = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        int oi = __shfl_xor_sync(0xFFFFFFFFu, idx, o);
+        if (ov > v || (ov == v && oi < idx)) {
+            v = ov;
+            idx = oi;
+        }
+    }
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) {
+        redv[w] = v;
+        redi[w] = idx;
+    }
+    __syncthreads();
+    v = redv[0];
+    idx = redi[0];
+#pragma unroll
+    for (int i = 1; i < kWarps; ++i) {
+        float ov = redv[i];
+        int oi = redi[i];
+        if (ov > v || (ov == v && oi < idx)) {
+            v = ov;
+            idx = oi;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ Philox4x32-10
+
+// Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, SC'11): each round
+// multiplies words 0 and 2 by the two round constants, swaps and xors the
+// high halves with the other words and the key; the key advances by the two
+// Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t a = c.x, b = c.z;
+        const uint32_t hi_a = __umulhi(0xD2511F53u, a), lo_a = 0xD2511F53u * a;
+        const uint32_t hi_b = __umulhi(0xCD9E8D57u, b), lo_b = 0xCD9E8D57u * b;
+        c = make_uint4(hi_b ^ c.y ^ k0, lo_b, hi_a ^ c.w ^ k1, lo_a);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// Acceptance uniform (draw 0): 24 bits -> [0,1) exactly representable.
+__device__ __forceinline__ double uniform_accept(unsigned long long seed, uint32_t b, uint32_t k) {
+    uint4 w = philox4x32_10(make_uint4(b, k, 0u, 0u), (uint32_t)seed, (uint32_t)(seed >> 32));
+    return (double)(w.x >> 8) * 0x1p-24;
+}
+
+// Sampling uniform (draw 1): 53 bits of (w0:w1) -> [0,1).
+__device__ __forceinline__ double uniform_sample(unsigned long long seed, uint32_t b, uint32_t k) {
+    uint4 w = philox4x32_10(make_uint4(b, k, 1u, 0u), (uint32_t)seed, (uint32_t)(seed >> 32));
+    unsigned long long v = ((unsigned long long)w.x << 32) | (unsigned long long)w.y;
+    return (double)(v >> 11) * 0x1p-53;
+}
+
+} // namespace sv

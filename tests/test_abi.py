@@ -1,0 +1,84 @@
+"""C-ABI checks that need no GPU: the library builds for sm_103a, loads, and
+exports every function include/*.h declares; host-side argument validation
+returns errors before anything is launched."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(spec_\w+)\s*\(", src, flags=re.M):
+            names.append(m.group(1))
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import speculative_decoding_verification_69_gb300 as sv
+    return sv.load_library()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("spec_verify", "spec_verify_debug", "spec_verify_workspace_bytes",
+              "spec_schedule_len", "spec_status_str"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in _declared_functions():
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_workspace_bytes(lib):
+    import speculative_decoding_verification_69_gb300 as sv
+    assert lib.spec_verify_workspace_bytes(0, 4, 100, 0) == 0
+    assert lib.spec_verify_workspace_bytes(1, 33, 100, 0) == 0
+    assert lib.spec_verify_workspace_bytes(1, 4, 1, 0) == 0
+    assert lib.spec_verify_workspace_bytes(1, 4, 100, 7) == 0
+    n1 = lib.spec_verify_workspace_bytes(32, 8, 151936, sv.DTYPE_BF16)
+    n2 = lib.spec_verify_workspace_bytes(64, 8, 151936, sv.DTYPE_BF16)
+    assert 0 < n1 < n2 and n1 % 256 == 0
+    # small compared with the logits themselves
+    assert n1 < 0.05 * 32 * 17 * 151936 * 2
+
+
+def test_host_validation_without_gpu(lib):
+    """Invalid sizes, null pointers and bad workspaces are rejected on the host,
+    before any CUDA call (safe on a machine without a GPU)."""
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    i32 = ctypes.c_void_p(0x10000)
+    base = dict(t=fake, d=fake, dt=1, tok=i32, vl=None, T=fake, seed=1, B=2, K=4, V=100,
+                o=i32, a=i32, ws=ctypes.c_void_p(0x10000), wsb=1 << 30, st=None)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return lib.spec_verify(a["t"], a["d"], a["dt"], a["tok"], a["vl"], a["T"], a["seed"],
+                               a["B"], a["K"], a["V"], a["o"], a["a"], a["ws"], a["wsb"],
+                               a["st"], None)
+
+    assert call(B=0) == 1
+    assert call(K=0) == 1 and call(K=33) == 1
+    assert call(V=1) == 1
+    assert call(dt=5) == 2
+    assert call(t=None) == 1 and call(d=None) == 1 and call(tok=None) == 1
+    assert call(T=None) == 1 and call(o=None) == 1 and call(a=None) == 1
+    assert call(t=ctypes.c_void_p(0x10008)) == 1          # logits not 16-byte aligned
+    assert call(ws=None) == 4
+    assert call(wsb=16) == 4
+    assert call(ws=ctypes.c_void_p(0x10010)) == 4          # workspace not 256-byte aligned
+    assert lib.spec_schedule_len(None, 0.3, 4, 4, i32, None) == 1
+    assert lib.spec_schedule_len(fake, 0.3, 0, 4, i32, None) == 1
+    assert lib.spec_schedule_len(fake, 0.3, 4, 40, i32, None) == 1
+    assert lib.spec_status_str(0) == b"ok"
+    assert b"workspace" in lib.spec_status_str(4)

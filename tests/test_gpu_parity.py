@@ -1,0 +1,285 @@
+"""GPU parity: the sm_103a path against the CPU oracle on the same seeded inputs.
+
+Greedy tokens and accept lengths must be bit-exact.  Sampled ones may differ
+only in near-tie requests (the oracle's uniform within 1e-6 of p/q or of a
+normalised CDF boundary), and such differences must stay rare.  Intermediates
+(row max, log-sum, p(x_k), q(x_k)) agree within 1e-5 relative.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_helpers import (REL_TOL, check_intermediates, compare, gpu_run, host_inputs,
+                         oracle_run)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import speculative_decoding_verification_69_gb300 as sv
+    sv.load_library()
+    yield
+
+
+def _schedule(inp):
+    import speculative_decoding_verification_69_gb300 as sv
+    if "draft_maxprob" in inp:
+        inp["verify_len"] = sv.schedule_len(inp["draft_maxprob"], inp["threshold"])
+    return inp
+
+
+def _check_all(inp, idx, debug=True, max_rows=64):
+    gpu = gpu_run(inp, debug=debug)
+    h = host_inputs(inp)
+    orc = oracle_run(h, idx)
+    ng, ns, nu, nsamp, nflag = compare(gpu, orc, h, idx)
+    assert ng == 0, "greedy mismatch"
+    assert nu == 0, "sampled mismatch outside the near-tie window"
+    assert ns <= max(1, int(1e-4 * max(nsamp, 1))), (ns, nsamp)
+    if debug:
+        worst = check_intermediates(gpu, h, idx, max_rows=max_rows)
+        assert worst < REL_TOL, worst
+    return gpu, orc, h
+
+
+# ---------------------------------------------------------------- c0 (small, full)
+
+@pytest.mark.parametrize("greedy", [False, True])
+def test_c0_full(greedy):
+    inp = workloads.make_inputs(0, greedy=greedy)
+    _check_all(inp, [0])
+
+
+def test_c0_shapes_many_requests():
+    """c0's shapes (V=32000 fp32) over 256 requests and 4 seeds: several tiles
+    per row and a ragged tail tile."""
+    for rep in range(4):
+        inp = workloads.make_inputs(0, rep=rep, B=256)
+        _check_all(inp, list(range(256)), max_rows=200)
+
+
+# ---------------------------------------------------------------- c1..c4 full size
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4])
+def test_full_size_sampled_requests(cfg):
+    """Full-size inputs in the launch configuration the benchmark times; the
+    oracle checks a sample of requests one by one."""
+    inp = _schedule(workloads.make_inputs(cfg))
+    B = inp["target"].shape[0]
+    rng = np.random.default_rng(cfg)
+    idx = sorted(set(rng.choice(B, size=min(B, 12), replace=False).tolist()) | {0, B - 1})
+    gpu, orc, h = _check_all(inp, idx, max_rows=40)
+    # whole-batch invariants at any size
+    K = h["tokens"].shape[1]
+    a = gpu["accept_len"]
+    for b in range(B):
+        L = K if h["verify_len"] is None else int(h["verify_len"][b])
+        assert 0 <= a[b] <= L
+        assert np.array_equal(gpu["out_tokens"][b, :a[b]], h["tokens"][b, :a[b]])
+        assert 0 <= gpu["out_tokens"][b, a[b]] < h["target"].shape[2]
+        assert np.all(gpu["out_tokens"][b, a[b] + 1:] == -1)
+
+
+def test_c4_greedy_rows_bitexact_all():
+    """Every greedy request of c4 (128 of 512) is bit-exact: argmax with a
+    lowest-index tie-break is recomputed on the host for all of them."""
+    inp = workloads.make_inputs(4)
+    gpu = gpu_run(inp)
+    h = host_inputs(inp)
+    greedy = [b for b in range(512) if oracle.is_greedy(h["temperature"][b])]
+    assert len(greedy) == 128
+    orc = oracle_run(h, greedy)
+    for b in greedy:
+        assert gpu["accept_len"][b] == orc["accept_len"][b]
+        assert np.array_equal(gpu["out_tokens"][b], orc["out_tokens"][b])
+
+
+# ---------------------------------------------------------------- many sampled rows
+
+@pytest.mark.parametrize("cfg,B", [(1, 384), (3, 256)])
+def test_sampled_mismatch_budget(cfg, B):
+    """Hundreds of sampled requests at large V: every mismatch must be a
+    near-tie and mismatches must stay under 0.01% of rows (at most one here)."""
+    inp = _schedule(workloads.make_inputs(cfg, rep=7, B=B))
+    gpu = gpu_run(inp)
+    h = host_inputs(inp)
+    idx = list(range(B))
+    orc = oracle_run(h, idx)
+    ng, ns, nu, nsamp, nflag = compare(gpu, orc, h, idx)
+    assert ng == 0 and nu == 0
+    assert ns <= 1, (ns, nsamp, nflag)
+
+
+# ---------------------------------------------------------------- schedule
+
+def test_schedule_len_bitexact():
+    import speculative_decoding_verification_69_gb300 as sv
+    inp = workloads.make_inputs(3)
+    mp = inp["draft_maxprob"]
+    L = sv.schedule_len(mp, 0.3).cpu().numpy()
+    assert np.array_equal(L, oracle.schedule_len(mp.cpu().numpy(), 0.3))
+    assert L.min() >= 0 and L.max() <= 16 and len(set(L.tolist())) > 3  # ragged
+    rng = np.random.default_rng(1)
+    x = rng.random((4096, 32)).astype(np.float32) ** 0.05
+    x[::7, 3] = np.nan
+    for thr in (0.3, 0.5, np.float32(0.9) ** 5):
+        got = sv.schedule_len(torch.from_numpy(x).cuda(), float(thr)).cpu().numpy()
+        assert np.array_equal(got, oracle.schedule_len(x, float(thr)))
+
+
+# ---------------------------------------------------------------- edge cases
+
+def _rand_inputs(B, K, V, dtype, seed, T, L=None, device="cuda"):
+    g = torch.Generator(device=device).manual_seed(seed)
+    tgt = (torch.randn((B, K + 1, V), generator=g, device=device) * 2.0).to(dtype)
+    drf = (tgt[:, :K].float() + 0.5 * torch.randn((B, K, V), generator=g, device=device)).to(dtype)
+    T = torch.as_tensor(T, dtype=torch.float32, device=device).expand(B).contiguous()
+    tok = torch.empty((B, K), dtype=torch.int32, device=device)
+    for b in range(B):
+        t = float(T[b])
+        if t > 0 and math.isfinite(t) and t >= 1.1754944e-38:
+            pr = torch.softmax(drf[b].float() / t, dim=-1)
+            tok[b] = torch.multinomial(pr, 1, generator=g).view(K).to(torch.int32)
+        else:
+            tok[b] = drf[b].float().argmax(dim=-1).to(torch.int32)
+    vl = None if L is None else torch.as_tensor(L, dtype=torch.int32, device=device).contiguous()
+    return dict(target=tgt.contiguous(), draft=drf.contiguous(), tokens=tok, temperature=T,
+                verify_len=vl, seed=seed)
+
+
+@pytest.mark.parametrize("B,K,V,dtype", [
+    (3, 1, 2, torch.bfloat16),          # smallest vocabulary, K = 1
+    (5, 3, 1001, torch.bfloat16),       # V*2 not a multiple of 16: scalar path
+    (4, 5, 999, torch.float32),         # scalar path, fp32
+    (2, 32, 3000, torch.bfloat16),      # K = SPEC_MAX_K
+    (6, 4, 16384 + 8, torch.bfloat16),  # one full tile plus an 8-element tail tile
+    (6, 4, 3 * 8192 + 4, torch.float32),
+])
+def test_shapes_sampled_and_greedy(B, K, V, dtype):
+    for T in (0.9, 0.0):
+        inp = _rand_inputs(B, K, V, dtype, seed=B * 1000 + K + V, T=T)
+        _check_all(inp, list(range(B)))
+
+
+def test_ragged_verify_len_and_mixed_modes():
+    B, K, V = 16, 6, 4096
+    L = [0, 1, 2, 3, 4, 5, 6, 6, 0, 3, 6, 1, 2, 5, 4, 0]
+    T = [0.0 if b % 4 == 0 else 0.5 + 0.1 * b for b in range(B)]
+    inp = _rand_inputs(B, K, V, torch.bfloat16, seed=77, T=T, L=L)
+    gpu, orc, h = _check_all(inp, list(range(B)))
+    assert all(gpu["accept_len"][b] <= L[b] for b in range(B))
+
+
+def test_special_temperatures_are_greedy():
+    B, K, V = 6, 3, 512
+    T = [0.0, -1.0, float("nan"), float("inf"), 1e-40, 1e-30]  # last: tiny but sampled
+    inp = _rand_inputs(B, K, V, torch.bfloat16, seed=5, T=T)
+    gpu, orc, h = _check_all(inp, list(range(B)))
+
+
+def test_neg_inf_logits():
+    B, K, V = 4, 3, 2048
+    inp = _rand_inputs(B, K, V, torch.bfloat16, seed=9, T=1.0)
+    tgt, drf = inp["target"], inp["draft"]
+    tgt[:, :, ::3] = float("-inf")
+    drf[:, :, 1::5] = float("-inf")
+    tgt[1, :, :1024] = float("-inf")  # a whole first tile region of a row
+    g = torch.Generator(device="cuda").manual_seed(3)
+    for b in range(B):
+        pr = torch.softmax(drf[b].float(), dim=-1)
+        inp["tokens"][b] = torch.multinomial(pr, 1, generator=g).view(K).to(torch.int32)
+    for T in (1.0, 0.0):
+        inp["temperature"].fill_(T)
+        _check_all(inp, list(range(B)))
+
+
+def test_invalid_lengths_and_tokens_status():
+    import speculative_decoding_verification_69_gb300 as sv
+    B, K, V = 4, 3, 300
+    inp = _rand_inputs(B, K, V, torch.bfloat16, seed=2, T=0.8, L=[5, 3, -1, 2])
+    inp["tokens"][1, 1] = V + 4
+    gpu, orc, h = _check_all(inp, list(range(B)))
+    assert gpu["status"] & sv.DEV_BAD_LEN and gpu["status"] & sv.DEV_BAD_TOKEN
+    assert gpu["accept_len"][1] <= 1 and gpu["accept_len"][2] == 0
+
+
+def test_ties_lowest_index():
+    """bf16 logits with many exact ties at the maximum: greedy picks the lowest index."""
+    B, K, V = 8, 4, 5000
+    g = torch.Generator(device="cuda").manual_seed(4)
+    tgt = torch.randint(-3, 3, (B, K + 1, V), generator=g, device="cuda").to(torch.bfloat16)
+    drf = torch.randint(-3, 3, (B, K, V), generator=g, device="cuda").to(torch.bfloat16)
+    tok = tgt[:, :K].float().argmax(dim=-1).to(torch.int32).contiguous()  # first max: all accepted
+    tok[::2, 2] = 7
+    inp = dict(target=tgt.contiguous(), draft=drf.contiguous(), tokens=tok,
+               temperature=torch.zeros(B, device="cuda"), verify_len=None, seed=1)
+    gpu, orc, h = _check_all(inp, list(range(B)))
+    assert (gpu["accept_len"][1::2] == K).all()
+
+
+def test_deterministic_and_seed_sensitive():
+    inp = workloads.make_inputs(1, B=8)
+    a = gpu_run(inp)
+    b = gpu_run(inp)
+    assert np.array_equal(a["out_tokens"], b["out_tokens"])
+    inp["seed"] += 1
+    c = gpu_run(inp)
+    assert not np.array_equal(a["out_tokens"], c["out_tokens"]) or not np.array_equal(
+        a["accept_len"], c["accept_len"])
+
+
+# ---------------------------------------------------------------- statistics on the GPU
+
+def test_gpu_first_token_chi_square():
+    """'Утверждение 1': over 10^6 GPU verifications of one row set with fresh
+    draft tokens, the first emitted token is distributed as p_0."""
+    stats = pytest.importorskip("scipy.stats")
+    import speculative_decoding_verification_69_gb300 as sv
+    V, K, N, T = 16, 3, 1_000_000, 0.9
+    rng = np.random.default_rng(20261202)
+    tgt1 = rng.normal(0, 1.5, size=(1, K + 1, V)).astype(np.float32)
+    drf1 = (tgt1[:, :K] + rng.normal(0, 1.0, size=(1, K, V))).astype(np.float32)
+    q = np.stack([oracle.row_softmax(drf1[0, k], T)[0] for k in range(K)])
+    p0 = oracle.row_softmax(tgt1[0, 0], T)[0]
+    toks = np.stack([rng.choice(V, size=N, p=q[k] / q[k].sum()) for k in range(K)], axis=1)
+    tgt = torch.from_numpy(tgt1).cuda().expand(N, K + 1, V).contiguous()
+    drf = torch.from_numpy(drf1).cuda().expand(N, K, V).contiguous()
+    o, a = sv.verify(tgt, drf, torch.from_numpy(toks.astype(np.int32)).cuda(), None,
+                     torch.full((N,), T, device="cuda"), 4242)
+    first = o[:, 0].cpu().numpy()
+    counts = np.bincount(first, minlength=V).astype(np.float64)
+    exp = p0 * N
+    keep = exp >= 5
+    obs_m = np.append(counts[keep], counts[~keep].sum())
+    exp_m = np.append(exp[keep], exp[~keep].sum())
+    if exp_m[-1] < 5:
+        obs_m[-2] += obs_m[-1]; exp_m[-2] += exp_m[-1]
+        obs_m, exp_m = obs_m[:-1], exp_m[:-1]
+    exp_m *= N / exp_m.sum()
+    assert stats.chisquare(obs_m, exp_m).pvalue > 0.01
+
+
+def test_gpu_mean_accept_length_closed_form():
+    """'Утверждение 2': mean accept length = sum_j prod_{k<j} beta_k."""
+    import speculative_decoding_verification_69_gb300 as sv
+    from oracle import tau
+    V, K, N, T = 64, 6, 400_000, 1.0
+    rng = np.random.default_rng(8)
+    tgt1 = rng.normal(0, 1.2, size=(1, K + 1, V)).astype(np.float32)
+    drf1 = (tgt1[:, :K] + rng.normal(0, 0.5, size=(1, K, V))).astype(np.float32)
+    p = np.stack([oracle.row_softmax(tgt1[0, k], T)[0] for k in range(K)])
+    q = np.stack([oracle.row_softmax(drf1[0, k], T)[0] for k in range(K)])
+    beta = np.minimum(p, q).sum(axis=1)
+    toks = np.stack([rng.choice(V, size=N, p=q[k] / q[k].sum()) for k in range(K)], axis=1)
+    tgt = torch.from_numpy(tgt1).cuda().expand(N, K + 1, V).contiguous()
+    drf = torch.from_numpy(drf1).cuda().expand(N, K, V).contiguous()
+    o, a = sv.verify(tgt, drf, torch.from_numpy(toks.astype(np.int32)).cuda(), None,
+                     torch.full((N,), T, device="cuda"), 99)
+    a = a.cpu().numpy().astype(np.float64)
+    assert abs(a.mean() - tau.mean_accept_len(beta)) < 4.0 * a.std() / math.sqrt(N)

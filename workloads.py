@@ -1,0 +1,160 @@
+"""Seeded synthetic inputs for the verification step (shared by tests, bench, smoke).
+
+This module holds no arithmetic of the verification method: it only draws
+logits, draft tokens, temperatures and draft confidences.  Both the CUDA path
+and the CPU oracle consume exactly these tensors.
+
+The pages measure on production sessions and public suites (MATH-500, HumanEval,
+Spec-Bench) with trained models; none of that is available, so these synthetic
+logits stand in for them, using the vocabulary sizes of the model families the
+pages name (Qwen3 151936, Llama 3.x 128256, gpt-oss 201088).
+
+Workloads (sigma is a standard deviation):
+  c0  B=1,   K=4,  V=32000,  float32; target ~ N(0, 2); draft = target + N(0, 0.5);
+      tokens drawn from the draft softmax at T=1; run sampled (T=1) and greedy (T=0).
+  c1  B=32,  K=8,  V=151936, bf16; target ~ N(0, 2.5); draft = target + N(0, 0.7); T=1;
+      verify_len = 8.
+  c2  B=128, K=16, V=151936, bf16; target ~ N(0, 2.5); draft row k = target + N(0, 0.3+0.1k)
+      (k 0-based, a suffix-decay stand-in); T=0.8; verify_len = 16.
+  c3  B=256, K=16, V=128256, bf16; target ~ N(0, 2) plus one confidence spike per row
+      (one uniformly drawn token raised by U(10, 20)); draft = target + N(0, 0.6); T=0.7;
+      verify_len from the confidence schedule of the draft max-probabilities, threshold 0.3.
+  c4  B=512, K=8,  V=201088, bf16; target ~ N(0, 3); draft = target + N(0, 0.5);
+      exactly 128 requests (a seeded random choice) greedy (T=0), the others T ~ U(0, 1.2];
+      verify_len = 8.
+Draft tokens: multinomial draws from softmax(draft/T) of the (rounded) draft logits;
+argmax of the draft for greedy requests.
+"""
+import math
+
+import torch
+
+BASE_SEED = 20261202
+
+CONFIGS = {
+    0: dict(B=1, K=4, V=32000, dtype=torch.float32, sigma=2.0, noise=0.5, T=1.0),
+    1: dict(B=32, K=8, V=151936, dtype=torch.bfloat16, sigma=2.5, noise=0.7, T=1.0),
+    2: dict(B=128, K=16, V=151936, dtype=torch.bfloat16, sigma=2.5, noise="decay", T=0.8),
+    3: dict(B=256, K=16, V=128256, dtype=torch.bfloat16, sigma=2.0, noise=0.6, T=0.7,
+            spike=(10.0, 20.0), threshold=0.3),
+    4: dict(B=512, K=8, V=201088, dtype=torch.bfloat16, sigma=3.0, noise=0.5, T="mixed",
+            n_greedy=128, t_max=1.2),
+}
+
+NAMES = {
+    0: "c0: B=1 K=4 V=32000 fp32, sampled and greedy",
+    1: "c1: B=32 K=8 V=151936 bf16, T=1, verify_len 8",
+    2: "c2: B=128 K=16 V=151936 bf16, T=0.8, draft noise 0.3+0.1k",
+    3: "c3: B=256 K=16 V=128256 bf16, T=0.7, confidence-scheduled verify_len (threshold 0.3)",
+    4: "c4: B=512 K=8 V=201088 bf16, 25% greedy, T~U(0,1.2]",
+}
+
+
+def seed_for(cfg: int, rep: int = 0) -> int:
+    return BASE_SEED + 1000 * cfg + rep
+
+
+def make_inputs(cfg: int, rep: int = 0, device="cuda", B=None, V=None, K=None, greedy=None,
+                T=None):
+    """Inputs of workload `cfg` (optionally shrunk: B, V, K overrides).
+
+    Returns dict(target [B,K+1,V], draft [B,K,V], tokens int32 [B,K], temperature float32 [B],
+    verify_len int32 [B] or None, draft_maxprob float32 [B,K] (c3 only), threshold (c3 only),
+    seed).  greedy=True forces T=0 everywhere (c0's second mode); T overrides the temperature."""
+    c = dict(CONFIGS[cfg])
+    B = B or c["B"]
+    V = V or c["V"]
+    K = K or c["K"]
+    seed = seed_for(cfg, rep)
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+
+    target = torch.randn((B, K + 1, V), generator=g, device=dev, dtype=torch.float32)
+    target.mul_(c["sigma"])
+    if "spike" in c:
+        lo, hi = c["spike"]
+        idx = torch.randint(0, V, (B, K + 1, 1), generator=g, device=dev)
+        delta = lo + (hi - lo) * torch.rand((B, K + 1, 1), generator=g, device=dev)
+        target.scatter_add_(2, idx, delta)
+    noise = torch.randn((B, K, V), generator=g, device=dev, dtype=torch.float32)
+    if c["noise"] == "decay":
+        sig = 0.3 + 0.1 * torch.arange(K, device=dev, dtype=torch.float32)
+        noise.mul_(sig.view(1, K, 1))
+    else:
+        noise.mul_(c["noise"])
+    draft = noise.add_(target[:, :K])
+    target = target.to(c["dtype"])
+    draft = draft.to(c["dtype"])
+
+    # temperatures
+    if c["T"] == "mixed":
+        temp = c["t_max"] * (1.0 - torch.rand((B,), generator=g, device=dev))  # (0, t_max]
+        n_greedy = max(0, min(B, round(c["n_greedy"] * B / c["B"])))
+        perm = torch.randperm(B, generator=g, device=dev)
+        temp[perm[:n_greedy]] = 0.0
+    else:
+        temp = torch.full((B,), float(c["T"]), device=dev)
+    if T is not None:
+        temp.fill_(float(T))
+    if greedy:
+        temp.zero_()
+    temp = temp.to(torch.float32).contiguous()
+
+    # draft tokens from the draft softmax at each request's temperature
+    tokens = torch.empty((B, K), dtype=torch.int64, device=dev)
+    maxprob = torch.empty((B, K), dtype=torch.float32, device=dev)
+    chunk = max(1, (1 << 26) // (K * V))
+    for b0 in range(0, B, chunk):
+        b1 = min(B, b0 + chunk)
+        d = draft[b0:b1].float()
+        tb = temp[b0:b1].view(-1, 1, 1)
+        sampled = tb > 0
+        probs = torch.softmax(d / torch.where(sampled, tb, torch.ones_like(tb)), dim=-1)
+        maxprob[b0:b1] = probs.max(dim=-1).values
+        draws = torch.multinomial(probs.view(-1, V), 1, generator=g).view(b1 - b0, K)
+        amax = d.argmax(dim=-1)
+        tokens[b0:b1] = torch.where(sampled.view(-1, 1), draws, amax)
+    out = dict(target=target.contiguous(), draft=draft.contiguous(),
+               tokens=tokens.to(torch.int32).contiguous(), temperature=temp,
+               verify_len=None, seed=seed)
+    if cfg in (1, 2, 4):
+        out["verify_len"] = torch.full((B,), K, dtype=torch.int32, device=dev)
+    if "threshold" in c:
+        out["draft_maxprob"] = maxprob.contiguous()
+        out["threshold"] = c["threshold"]
+    return out
+
+
+def algorithmic_bytes(temperature, verify_len, V, esize):
+    """Bytes the step must read, each needed row once: (2L+1) rows of V logits
+    for a sampled request, (L+1) for a greedy one."""
+    t = temperature.detach().float().cpu()
+    L = verify_len.detach().cpu().long()
+    sampled = (t > 0) & torch.isfinite(t) & (t >= torch.finfo(torch.float32).tiny)
+    rows = torch.where(sampled, 2 * L + 1, L + 1)
+    return int(rows.sum().item()) * V * esize
+
+
+def verified_positions(verify_len):
+    return int(verify_len.detach().cpu().long().sum().item())
+
+
+def to_numpy_logits(t):
+    """Host copy of logits in the oracle's layout (bf16 as uint16 bit patterns)."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view("uint16")
+    return t.numpy()
+
+
+def human(cfg):
+    return NAMES[cfg]
+
+
+def mib(x):
+    return x / 2**20
+
+
+__all__ = ["CONFIGS", "NAMES", "make_inputs", "seed_for", "algorithmic_bytes",
+           "verified_positions", "to_numpy_logits", "math"]
