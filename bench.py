@@ -87,22 +87,29 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self.thread = None
+        self.window = (0.0, float("inf"))
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        t0 = time.perf_counter()
+        while not self.lines and time.perf_counter() - t0 < 3.0:  # wait for the first sample
+            time.sleep(0.01)
 
     def _read(self):
         for ln in self.proc.stdout:
-            self.lines.append(ln.strip())
+            self.lines.append((time.perf_counter(), ln.strip()))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
@@ -116,7 +123,10 @@ class ClockSampler:
             self.thread.join(timeout=2)
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lo, hi = self.window
+        for ts, ln in self.lines:
+            if ts < lo or ts > hi:
+                continue
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -189,17 +199,26 @@ def oracle_sample(inp, max_seconds=12.0, min_requests=2):
     T = inp["temperature"].cpu().numpy()
     B, K = tok.shape
     cores = oracle.cpu_count()
-    # probe one request to size the sample
+    nthreads = min(cores, B)
     t0 = time.perf_counter()
     oracle.verify(h_t, h_d, tok, vl, T, inp["seed"], b0=0, b1=1, nthreads=1)
-    one = max(time.perf_counter() - t0, 1e-4)
-    n = int(max(min_requests, min(B, max_seconds * cores / one)))
-    n = min(B, max(n, min(cores, B)))
-    t0 = time.perf_counter()
-    r = oracle.verify(h_t, h_d, tok, vl, T, inp["seed"], b0=0, b1=n, nthreads=min(cores, n))
-    dt = time.perf_counter() - t0
-    pos = int(vl[:n].clip(0, K).sum()) if vl is not None else n * K
-    return pos / dt, min(cores, n), "first %d of %d requests (%d verified positions)" % (n, B, pos), dt, r
+    t_one = max(time.perf_counter() - t0, 1e-6)
+    n = B
+    if t_one * B / nthreads > max_seconds:  # a prefix of the batch fits the budget
+        n = int(min(B, max(nthreads, max_seconds * nthreads / t_one)))
+        nthreads = min(nthreads, n)
+    pos_per_pass = int(vl[:n].clip(0, K).sum()) if vl is not None else n * K
+    # the sample, repeated until the time budget is spent (at least once)
+    reps, dt, r = 0, 0.0, None
+    while reps == 0 or dt < max_seconds:
+        t0 = time.perf_counter()
+        r = oracle.verify(h_t, h_d, tok, vl, T, inp["seed"], b0=0, b1=n, nthreads=nthreads)
+        dt += time.perf_counter() - t0
+        reps += 1
+    pos = pos_per_pass * reps
+    return (pos / dt, nthreads,
+            "requests 0..%d of %d x %d passes (%d verified positions), %d threads"
+            % (n - 1, B, reps, pos, nthreads), dt, r)
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -246,6 +265,10 @@ def run_ours(args, world, rank, local):
           for _ in range(args.steps)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
+    for a, b in kev:  # torch creates the CUDA event on first record
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
@@ -260,7 +283,9 @@ def run_ours(args, world, rank, local):
     sv.profile_events(None, None)
     torch.cuda.synchronize()
     barrier(world)
-    t_wall = time.perf_counter() - t_wall0
+    t_wall1 = time.perf_counter()
+    t_wall = t_wall1 - t_wall0
+    clocks.mark(t_wall0, t_wall1 + 0.05)
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     kern_ms = [a.elapsed_time(b) for a, b in kev]
@@ -370,7 +395,7 @@ def run_reference(args, world, rank, local):
         import oracle
         vl = oracle.schedule_len(inp["draft_maxprob"].cpu().numpy(), inp["threshold"])
         inp["verify_len"] = torch.from_numpy(vl)
-    budget = max(2.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    budget = min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_sample(inp, max_seconds=budget)
     vals, secs = [], []
@@ -405,7 +430,7 @@ def run_reference(args, world, rank, local):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -1,19 +1,20 @@
-// sv_common.cuh -- device building blocks shared by the verification kernels.
+// sv_common.cuh -- device building blocks shared by the verification kernels:
+// element access for bf16 / fp32 logit vectors, packed f32x2 arithmetic,
+// two-float (double-single) sums, warp / CTA reductions, bulk-copy and
+// mbarrier primitives with bounded waits, and Philox4x32-10.
 //
-// Numerics contract (what makes the sampler reproduce the statistics pass bit
-// for bit):
-//   * a logit row is cut into tiles of TE elements; every tile keeps its own
-//     reference m_t = exact max of the raw logits in the tile;
-//   * the weight of element v of tile t is
-//         e_v = ex2.approx( fma(d, c_hi, d * c_lo) ),  d = z_v - m_t,
-//     with (c_hi, c_lo) a two-float split of log2(e)/T (c_hi rounded toward
-//     zero, c_lo >= FLT_MIN > 0 so that d = -inf gives -inf, never NaN);
-//   * every kernel evaluates that expression with the same explicitly rounded
-//     intrinsics (no contraction), so e_v is identical wherever it is formed;
-//   * tile sums use Fast2Sum against a biased accumulator (exact error terms),
-//     and cross-thread sums use two-float arithmetic, so the row normaliser
-//     S = sum_t S_t * 2^((m_t - m) c) is accurate to ~1e-12 relative and
-//     consistent with the e_v that the residual sampler re-forms.
+// Numerics contract.
+//   * The streaming statistics pass needs only float accuracy (~1e-7): per
+//     chunk the exact max m_c and s_c = sum_v 2^((z_v - m_c) * c), c = log2(e)/T
+//     as a float, formed as ex2.approx((z - m_c) * c) and summed in float.
+//   * The sampler re-forms the weights of the one row (pair) it draws from with
+//     the row max m and a two-float c = c_hi + c_lo:
+//         e_v = ex2.approx(fma(d, c_hi, d * c_lo)),  d = z_v - m,
+//     and sums them exactly (Fast2Sum against a biased accumulator), so its
+//     normaliser carries no coherent error; every kernel that re-forms e_v uses
+//     the same explicitly rounded intrinsics, so the values agree bit for bit.
+//   * c_hi is rounded toward zero and c_lo >= FLT_MIN > 0, so d = -inf gives
+//     -inf (weight 0), never NaN.
 #pragma once
 #include <cstdint>
 #include <cfloat>
@@ -22,9 +23,10 @@
 
 namespace sv {
 
-constexpr int kThreads = 256;   // threads per CTA of the row-tile kernels
+constexpr int kThreads = 256;   // threads per CTA of the per-request kernels
 constexpr int kWarps = kThreads / 32;
-constexpr int kVecPerThread = 8; // 16-byte vectors per thread per tile
+constexpr int kChunkBytes = 4096;                 // logits one warp handles per item
+constexpr int kVecPerLane = kChunkBytes / 16 / 32; // 16-byte vectors per lane per item
 
 enum { kF32 = 0, kBF16 = 1 };
 
@@ -40,8 +42,8 @@ template <> struct Fmt<kF32> {
     static constexpr uint32_t kNegInfWord = 0xFF800000u;
 };
 
-template <int DT> __host__ __device__ constexpr int tile_elems() {
-    return kThreads * kVecPerThread * Fmt<DT>::kEPV;
+template <int DT> __host__ __device__ constexpr int chunk_elems() {
+    return kChunkBytes / Fmt<DT>::kESZ;
 }
 
 // ------------------------------------------------------------------ loads
@@ -267,6 +269,90 @@ __device__ __forceinline__ void cta_argmax(float &v, int &idx, float *redv, int 
             v = ov;
             idx = oi;
         }
+    }
+}
+
+// ------------------------------------------------------------------ warp reductions
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+__device__ __forceinline__ int warp_min_int(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+__device__ __forceinline__ FF warp_sum_ff(FF v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = ff_add(v, ff_shfl_xor(v, o));
+    return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// ------------------------------------------------------------------ bulk copies
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// Orders this thread's earlier shared-memory accesses before later bulk
+// (async-proxy) writes into the same buffer.
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+// Bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16),
+// completion signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for phase `parity` of `bar`, giving up after `limit_ns` nanoseconds.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0 && global_ns() - t0 > limit_ns) return false;
     }
 }
 

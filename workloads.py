@@ -25,8 +25,6 @@ Workloads (sigma is a standard deviation):
 Draft tokens: multinomial draws from softmax(draft/T) of the (rounded) draft logits;
 argmax of the draft for greedy requests.
 """
-import math
-
 import torch
 
 BASE_SEED = 20261202
@@ -118,7 +116,7 @@ def make_inputs(cfg: int, rep: int = 0, device="cuda", B=None, V=None, K=None, g
     out = dict(target=target.contiguous(), draft=draft.contiguous(),
                tokens=tokens.to(torch.int32).contiguous(), temperature=temp,
                verify_len=None, seed=seed)
-    if cfg in (1, 2, 4):
+    if cfg != 3:
         out["verify_len"] = torch.full((B,), K, dtype=torch.int32, device=dev)
     if "threshold" in c:
         out["draft_maxprob"] = maxprob.contiguous()
@@ -148,13 +146,3 @@ def to_numpy_logits(t):
     return t.numpy()
 
 
-def human(cfg):
-    return NAMES[cfg]
-
-
-def mib(x):
-    return x / 2**20
-
-
-__all__ = ["CONFIGS", "NAMES", "make_inputs", "seed_for", "algorithmic_bytes",
-           "verified_positions", "to_numpy_logits", "math"]
