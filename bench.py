@@ -363,7 +363,7 @@ def run_ours(args, world, rank, local):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "sv_rowstats",
+            "kernel": "sv_fused",
             "achieved": achieved,
             "peak": peak,
             "peak_source": peak_kind,
