@@ -247,13 +247,9 @@ __device__ void decide_request(const Params &P, int b, int lane) {
         else if (k == a && greedy) v = __float_as_int(ra.z);
         out[k] = v;
     }
-    if (P.dbg_probs) {
-        for (int k = lane; k < K; k += 32) {
-            const double pk = __shfl_sync(0xFFFFFFFFu, p, k & 31);
-            const double qk = __shfl_sync(0xFFFFFFFFu, q, k & 31);
-            P.dbg_probs[((size_t)b * K + k) * 2 + 0] = (!greedy && k < L) ? pk : NAN;
-            P.dbg_probs[((size_t)b * K + k) * 2 + 1] = (!greedy && k < L) ? qk : NAN;
-        }
+    if (P.dbg_probs && lane < K) {  // lane k holds position k (K <= 32)
+        P.dbg_probs[((size_t)b * K + lane) * 2 + 0] = (!greedy && lane < L) ? p : NAN;
+        P.dbg_probs[((size_t)b * K + lane) * 2 + 1] = (!greedy && lane < L) ? q : NAN;
     }
     if (P.dbg_rows) {
         const int nslot = 2 * K + 1;
@@ -583,6 +579,7 @@ __device__ void stream_producer(const Params &P, FusedShared &sh, int lane) {
                 d.nvec = (int)(jbytes / 16); d.cval = jcv; d.greedy = jg; d.pad = 0;
                 sh.desc[s] = d;
                 uint64_t *fb = reinterpret_cast<uint64_t *>(&sh.full[s]);
+                fence_proxy_async();
                 mbar_expect_tx(fb, jbytes);
                 bulk_g2s(sh.buf[s], row_ptr(P, jb, js, ESZ) + (size_t)jc * CE8 * ESZ, jbytes, fb);
                 prod_unlock(sh);
@@ -641,6 +638,7 @@ __device__ void task_producer_dt_dispatch(const Params &P, FusedShared &sh, int 
             d.nvec = (int)(bytes / 16); d.cval = 0.f; d.greedy = 0; d.pad = 0;
             sh.desc[s] = d;
             uint64_t *fb = reinterpret_cast<uint64_t *>(&sh.full[s]);
+            fence_proxy_async();
             mbar_expect_tx(fb, si.mode == 1 ? 2u * bytes : bytes);
             bulk_g2s(sh.buf[s], row_ptr(P, b, si.slot_t, esz) + (size_t)e0 * esz, bytes, fb);
             if (si.mode == 1)
