@@ -579,7 +579,6 @@ __device__ void stream_producer(const Params &P, FusedShared &sh, int lane) {
                 d.nvec = (int)(jbytes / 16); d.cval = jcv; d.greedy = jg; d.pad = 0;
                 sh.desc[s] = d;
                 uint64_t *fb = reinterpret_cast<uint64_t *>(&sh.full[s]);
-                fence_proxy_async();
                 mbar_expect_tx(fb, jbytes);
                 bulk_g2s(sh.buf[s], row_ptr(P, jb, js, ESZ) + (size_t)jc * CE8 * ESZ, jbytes, fb);
                 prod_unlock(sh);
@@ -638,7 +637,6 @@ __device__ void task_producer_dt_dispatch(const Params &P, FusedShared &sh, int 
             d.nvec = (int)(bytes / 16); d.cval = 0.f; d.greedy = 0; d.pad = 0;
             sh.desc[s] = d;
             uint64_t *fb = reinterpret_cast<uint64_t *>(&sh.full[s]);
-            fence_proxy_async();
             mbar_expect_tx(fb, si.mode == 1 ? 2u * bytes : bytes);
             bulk_g2s(sh.buf[s], row_ptr(P, b, si.slot_t, esz) + (size_t)e0 * esz, bytes, fb);
             if (si.mode == 1)
@@ -650,12 +648,135 @@ __device__ void task_producer_dt_dispatch(const Params &P, FusedShared &sh, int 
     producer_done(P, sh);
 }
 
+// ------------------------------------------------------------------ consumers
+
+// Completion counts a consumer warp has not published yet: finished stream
+// items of one row, finished sampler tasks of one request.  Counts are
+// published (GPU fence + atomic add) when the warp moves to another row or
+// request and before it blocks on a stage that is not ready, so a count never
+// waits on a warp that is itself waiting.
+struct Pending {
+    int row, cnt;   // stream items of row (b * nslot + slot)
+    int req, scnt;  // sampler tasks of request b
+};
+
+template <int DT>
+__device__ void flush_rows(const Params &P, Pending &pd, int lane) {
+    if (pd.cnt == 0) return;
+    const int row = pd.row, cnt = pd.cnt;
+    pd.cnt = 0;
+    int last = 0;
+    if (lane == 0) {
+        __threadfence();
+        last = atomicAdd(&P.row_cnt[row], cnt) + cnt == P.nchunk8;
+    }
+    if (!__shfl_sync(0xFFFFFFFFu, last, 0)) return;
+    __threadfence();
+    const int b = row / P.nslot, slot = row - b * P.nslot;
+    const ReqInfo rq = P.req[b];
+    const float4 rsv = combine_row(P, b, slot, rq.greedy != 0, rq.c, lane);
+    const int nrows = rq.greedy ? rq.L + 1 : 2 * rq.L + 1;
+    if (lane == 0) {
+        P.rowstat[row] = rsv;
+        __threadfence();
+        last = atomicAdd(&P.req_cnt[b], 1) == nrows - 1;
+    }
+    if (!__shfl_sync(0xFFFFFFFFu, last, 0)) return;
+    __threadfence();
+    decide_request<DT>(P, b, lane);
+}
+
+template <int DT>
+__device__ void flush_samples(const Params &P, Pending &pd, int lane) {
+    if (pd.scnt == 0) return;
+    const int b = pd.req, cnt = pd.scnt;
+    pd.scnt = 0;
+    int last = 0;
+    if (lane == 0) {
+        __threadfence();
+        last = atomicAdd(&P.samp_cnt[b], cnt) + cnt == P.nsub;
+    }
+    if (!__shfl_sync(0xFFFFFFFFu, last, 0)) return;
+    __threadfence();
+    find_request<DT>(P, b, lane);
+}
+
+template <int DT>
+__device__ void consumer_loop(const Params &P, FusedShared &sh, int cw, int lane) {
+    constexpr int ESZ = Fmt<DT>::kESZ;
+    constexpr int CE8 = kStageBytes / ESZ;
+    Pending pd{-1, 0, -1, 0};
+    for (uint32_t k = (uint32_t)cw;; k += (uint32_t)kFC) {
+        const int s = (int)(k % kFStages);
+        uint64_t *fb = reinterpret_cast<uint64_t *>(&sh.full[s]);
+        const uint32_t par = (k / kFStages) & 1u;
+        int ready = 0;
+        if (lane == 0) ready = mbar_try_wait(fb, par);
+        if (!__shfl_sync(0xFFFFFFFFu, ready, 0)) {
+            flush_rows<DT>(P, pd, lane);
+            flush_samples<DT>(P, pd, lane);
+            if (!mbar_wait_bounded(fb, par, kWaitLimitNs)) {
+                if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
+                return;
+            }
+        } else {
+            mbar_wait_bounded(fb, par, kWaitLimitNs);  // completes at once: every lane observes it
+        }
+        const Desc d = sh.desc[s];
+        if (d.kind == kKindEnd) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.empty[s]);
+            flush_rows<DT>(P, pd, lane);
+            flush_samples<DT>(P, pd, lane);
+            return;
+        }
+        if (d.kind == kKindStream) {
+            uint4 v[kStreamVec];
+#pragma unroll
+            for (int i = 0; i < kStreamVec; ++i) v[i] = sh.buf[s][i * 32 + lane];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.empty[s]);
+            const float4 part = stream_partial<DT>(v, d.nvec, d.greedy != 0, d.cval, d.c * CE8, lane);
+            const int row = d.b * P.nslot + d.slot;
+            if (lane == 0) P.part[(size_t)row * P.nchunk8 + d.c] = part;
+            if (row != pd.row) {
+                flush_rows<DT>(P, pd, lane);
+                pd.row = row;
+            }
+            ++pd.cnt;
+        } else {
+            uint4 vt[kSubVec], vd[kSubVec];
+            const uint32_t ni = Fmt<DT>::kNegInfWord;
+            const bool resid = d.slot == 1;
+#pragma unroll
+            for (int i = 0; i < kSubVec; ++i) {
+                vt[i] = sh.buf[s][i * 32 + lane];
+                vd[i] = resid ? sh.buf[s][kSubBytes / 16 + i * 32 + lane] : make_uint4(ni, ni, ni, ni);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.empty[s]);
+            const SampInfo si = load_samp(P, d.b);
+            float A, Bs, W;
+            FF st, sd;
+            sample_masses<DT>(vt, vd, d.nvec, si, A, Bs, W, st, sd, lane);
+            if (lane == 0) {
+                P.sub[(size_t)d.b * P.nsub + d.c] = make_float4(A, Bs, W, 0.f);
+                P.sexact[(size_t)d.b * P.nsub + d.c] = make_float4(st.hi, st.lo, sd.hi, sd.lo);
+            }
+            if (d.b != pd.req) {
+                flush_samples<DT>(P, pd, lane);
+                pd.req = d.b;
+            }
+            ++pd.scnt;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ the kernel
 
 template <int DT>
-__global__ void __launch_bounds__(kFThreads) sv_fused(Params P) {
+__global__ void __launch_bounds__(kFThreads, 3) sv_fused(Params P) {
     constexpr int ESZ = Fmt<DT>::kESZ;
-    constexpr int CE8 = kStageBytes / ESZ;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     FusedShared &sh = *reinterpret_cast<FusedShared *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -683,74 +804,7 @@ __global__ void __launch_bounds__(kFThreads) sv_fused(Params P) {
     }
 
     // -------------------------------------------------------------- consumers
-    const int cw = warp - kFProd;
-    for (uint32_t k = (uint32_t)cw;; k += (uint32_t)kFC) {
-        const int s = (int)(k % kFStages);
-        if (!mbar_wait_bounded(reinterpret_cast<uint64_t *>(&sh.full[s]), (k / kFStages) & 1u,
-                               kWaitLimitNs)) {
-            if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
-            return;
-        }
-        const Desc d = sh.desc[s];
-        if (d.kind == kKindEnd) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.empty[s]);
-            return;
-        }
-        if (d.kind == kKindStream) {
-            uint4 v[kStreamVec];
-#pragma unroll
-            for (int i = 0; i < kStreamVec; ++i) v[i] = sh.buf[s][i * 32 + lane];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.empty[s]);
-            const float4 part = stream_partial<DT>(v, d.nvec, d.greedy != 0, d.cval, d.c * CE8, lane);
-            const int row = d.b * P.nslot + d.slot;
-            int last = 0;
-            if (lane == 0) {
-                P.part[(size_t)row * P.nchunk8 + d.c] = part;
-                __threadfence();
-                last = atomicAdd(&P.row_cnt[row], 1) == P.nchunk8 - 1;
-            }
-            if (!__shfl_sync(0xFFFFFFFFu, last, 0)) continue;
-            __threadfence();
-            const float4 rsv = combine_row(P, d.b, d.slot, d.greedy != 0, d.cval, lane);
-            const ReqInfo rq = P.req[d.b];
-            const int nrows = rq.greedy ? rq.L + 1 : 2 * rq.L + 1;
-            if (lane == 0) {
-                P.rowstat[row] = rsv;
-                __threadfence();
-                last = atomicAdd(&P.req_cnt[d.b], 1) == nrows - 1;
-            }
-            if (!__shfl_sync(0xFFFFFFFFu, last, 0)) continue;
-            __threadfence();
-            decide_request<DT>(P, d.b, lane);
-        } else {
-            uint4 vt[kSubVec], vd[kSubVec];
-            const uint32_t ni = Fmt<DT>::kNegInfWord;
-            const bool resid = d.slot == 1;
-#pragma unroll
-            for (int i = 0; i < kSubVec; ++i) {
-                vt[i] = sh.buf[s][i * 32 + lane];
-                vd[i] = resid ? sh.buf[s][kSubBytes / 16 + i * 32 + lane] : make_uint4(ni, ni, ni, ni);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.empty[s]);
-            const SampInfo si = load_samp(P, d.b);
-            float A, Bs, W;
-            FF st, sd;
-            sample_masses<DT>(vt, vd, d.nvec, si, A, Bs, W, st, sd, lane);
-            int last = 0;
-            if (lane == 0) {
-                P.sub[(size_t)d.b * P.nsub + d.c] = make_float4(A, Bs, W, 0.f);
-                P.sexact[(size_t)d.b * P.nsub + d.c] = make_float4(st.hi, st.lo, sd.hi, sd.lo);
-                __threadfence();
-                last = atomicAdd(&P.samp_cnt[d.b], 1) == P.nsub - 1;
-            }
-            if (!__shfl_sync(0xFFFFFFFFu, last, 0)) continue;
-            __threadfence();
-            find_request<DT>(P, d.b, lane);
-        }
-    }
+    consumer_loop<DT>(P, sh, warp - kFProd, lane);
 }
 
 } // namespace sv
