@@ -12,9 +12,9 @@
 //   metadata across its lanes and      chunk of a row combines the row; the last
 //   bulk-copies each 8 KiB item        row of a request decides it (acceptance
 //   into the next free stage           rule, first rejection, outputs) and
-//   warp 1: claims published           publishes its sampler tasks
-//   sampler tasks (batches, compare-   sampler task -> residual / target masses
-//   and-swap) and copies each 4 KiB    of a 4 KiB chunk of the row (pair); the
+//   warp 1: claims sampler tasks in    publishes its sampler tasks
+//   batches (atomic add), waits for    sampler task -> residual / target masses
+//   their request, copies each 4 KiB   of a 4 KiB chunk of the row (pair); the
 //   chunk of the row (pair)            last task of a request draws the token
 //   both allocate stages from one      (inverse CDF)
 //   shared sequence counter
@@ -589,34 +589,41 @@ __device__ void stream_producer(const Params &P, FusedShared &sh, int lane) {
     if (lane == 0) producer_done(P, sh);
 }
 
-__device__ void task_producer_dt_dispatch(const Params &P, FusedShared &sh, int esz) {
+// Sampler tasks: request entry e (publication order) owns task indices
+// [e * nsub_pad, (e + 1) * nsub_pad), nsub_pad = nsub rounded up to kTaskBatch,
+// so a claimed batch never straddles two requests.  Batches are claimed with
+// one atomic add (no retries); a batch whose request is not published yet is
+// waited for (bounded), which never blocks stream items: they have their own
+// producer warp.
+__device__ void task_producer(const Params &P, FusedShared &sh, int esz) {
     const int ce4 = kSubBytes / esz;
-    const unsigned long long total =
-        (unsigned long long)(*P.n_sampled) * (unsigned long long)P.nsub;
-    unsigned long long idle_since = 0;
+    const unsigned long long nsub_pad =
+        (unsigned long long)((P.nsub + kTaskBatch - 1) / kTaskBatch) * kTaskBatch;
+    const unsigned long long total = (unsigned long long)(*P.n_sampled) * nsub_pad;
     for (;;) {
-        unsigned long long h = *reinterpret_cast<volatile unsigned long long *>(P.q_head);
+        const unsigned long long h = atomicAdd(P.q_head, (unsigned long long)kTaskBatch);
         if (h >= total) break;
-        const unsigned long long e = h / (unsigned long long)P.nsub;
-        if (ld_volatile_int(&P.q_entries[e]) == 0) {
-            const unsigned long long now = global_ns();
-            if (idle_since == 0) idle_since = now;
-            if (now - idle_since > kWaitLimitNs) {
+        const unsigned long long e = h / nsub_pad;
+        const int c0 = (int)(h - e * nsub_pad);
+        int bp1 = ld_volatile_int(&P.q_entries[e]);
+        if (bp1 == 0) {
+            const unsigned long long t0 = global_ns();
+            unsigned int nap = 128;
+            while ((bp1 = ld_volatile_int(&P.q_entries[e])) == 0) {
+                if (global_ns() - t0 > kWaitLimitNs) break;
+                __nanosleep(nap);
+                if (nap < 2048) nap <<= 1;
+            }
+            if (bp1 == 0) {
                 if (P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
                 break;
             }
-            __nanosleep(200);
-            continue;
         }
-        idle_since = 0;
-        const unsigned long long end_e = (e + 1) * (unsigned long long)P.nsub;
-        const unsigned long long n = min((unsigned long long)kTaskBatch, end_e - h);
-        if (atomicCAS(P.q_head, h, h + n) != h) continue;
-        const int b = ld_volatile_int(&P.q_entries[e]) - 1;
+        const int b = bp1 - 1;
         __threadfence();
         const SampInfo si = load_samp(P, b);
-        for (unsigned long long t = h; t < h + n; ++t) {
-            const int c = (int)(t - e * (unsigned long long)P.nsub);
+        const int c1 = min(c0 + kTaskBatch, P.nsub);
+        for (int c = c0; c < c1; ++c) {
             const uint32_t e0 = (uint32_t)c * (uint32_t)ce4;
             const uint32_t bytes = min((uint32_t)ce4, (uint32_t)P.V - e0) * (uint32_t)esz;
             uint32_t k;
@@ -731,6 +738,7 @@ __device__ void consumer_loop(const Params &P, FusedShared &sh, int cw, int lane
             return;
         }
         if (d.kind == kKindStream) {
+            flush_samples<DT>(P, pd, lane);  // publish finished sampler tasks at once
             uint4 v[kStreamVec];
 #pragma unroll
             for (int i = 0; i < kStreamVec; ++i) v[i] = sh.buf[s][i * 32 + lane];
@@ -755,6 +763,7 @@ __device__ void consumer_loop(const Params &P, FusedShared &sh, int cw, int lane
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.empty[s]);
+            flush_rows<DT>(P, pd, lane);  // publish finished rows at once
             const SampInfo si = load_samp(P, d.b);
             float A, Bs, W;
             FF st, sd;
@@ -799,7 +808,7 @@ __global__ void __launch_bounds__(kFThreads, 3) sv_fused(Params P) {
         return;
     }
     if (warp == 1) {
-        if (lane == 0) task_producer_dt_dispatch(P, sh, ESZ);
+        if (lane == 0) task_producer(P, sh, ESZ);
         return;
     }
 
