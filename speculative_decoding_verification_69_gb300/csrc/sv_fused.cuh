@@ -206,7 +206,7 @@ __device__ __forceinline__ float4 combine_row(const Params &P, int b, int slot, 
 
 // Acceptance decision of request b by one warp (lane k = draft position k).
 template <int DT>
-__device__ void decide_request(const Params &P, int b, int lane) {
+__device__ __noinline__ void decide_request(const Params &P, int b, int lane) {
     const int K = P.K;
     const ReqInfo rq = P.req[b];
     const int L = rq.L;
@@ -336,7 +336,7 @@ __device__ __forceinline__ void sample_masses(const uint4 (&vt)[kSubVec], const 
 // ------------------------------------------------------------------ inverse CDF (one warp)
 
 template <int DT>
-__device__ void find_request(const Params &P, int b, int lane) {
+__device__ __noinline__ void find_request(const Params &P, int b, int lane) {
     constexpr int EPV = Fmt<DT>::kEPV;
     constexpr int ESZ = Fmt<DT>::kESZ;
     constexpr int CE = kSubBytes / ESZ;
@@ -521,11 +521,46 @@ __device__ __forceinline__ void producer_done(const Params &P, FusedShared &sh) 
     prod_unlock(sh);
 }
 
-constexpr int kStreamBatch = 32;  // stream items claimed per global atomic
-constexpr int kTaskBatch = 16;    // sampler tasks claimed per compare-and-swap
+constexpr int kStreamBatch = 32;  // stream items claimed per global atomic (one per lane)
+constexpr int kTaskBatch = 16;    // sampler tasks claimed per global atomic (one per lane)
+constexpr int kIssueGroup = 8;    // stages acquired per lock hold (<= kFStages)
+static_assert(kIssueGroup <= kFStages, "issue group larger than the ring");
+
+// Lane 0 takes the lock, allocates `nn` consecutive sequence numbers and waits,
+// in order, until each of their stages has been released; the lock is then
+// held until the group is issued (`group_end`).  Returns the first sequence
+// number, or ~0u on timeout (lock released).
+__device__ __forceinline__ uint32_t group_begin(FusedShared &sh, int nn, int lane) {
+    uint32_t k0 = 0;
+    int ok = 1;
+    if (lane == 0) {
+        ok = prod_lock(sh);
+        if (ok) {
+            volatile unsigned int *seq = &sh.prod_seq;
+            k0 = *seq;
+            *seq = k0 + (uint32_t)nn;
+            for (int i = 0; i < nn && ok; ++i) {
+                const uint32_t k = k0 + (uint32_t)i;
+                if (k >= (uint32_t)kFStages &&
+                    !mbar_wait_bounded(reinterpret_cast<uint64_t *>(&sh.empty[k % kFStages]),
+                                       ((k / kFStages) - 1u) & 1u, kWaitLimitNs))
+                    ok = 0;
+            }
+            if (!ok) prod_unlock(sh);
+        }
+    }
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    k0 = __shfl_sync(0xFFFFFFFFu, k0, 0);
+    return ok ? k0 : ~0u;
+}
+
+__device__ __forceinline__ void group_end(FusedShared &sh, int lane) {
+    __syncwarp();
+    if (lane == 0) prod_unlock(sh);
+}
 
 template <int DT>
-__device__ void stream_producer(const Params &P, FusedShared &sh, int lane) {
+__device__ __noinline__ void stream_producer(const Params &P, FusedShared &sh, int lane) {
     constexpr int ESZ = Fmt<DT>::kESZ;
     constexpr int CE8 = kStageBytes / ESZ;
     const uint32_t n_stream = (uint32_t)(*P.row_count) * (uint32_t)P.nchunk8;
@@ -536,54 +571,38 @@ __device__ void stream_producer(const Params &P, FusedShared &sh, int lane) {
         if (base >= n_stream) break;
         // metadata of the batch, one item per lane
         const uint32_t item = base + (uint32_t)lane;
-        int b = 0, slot = 0, greedy = 0;
-        uint32_t c = 0, bytes = 0;
-        float cval = 0.f;
+        Desc d;
+        d.kind = kKindStream; d.b = 0; d.slot = 0; d.c = 0; d.nvec = 0; d.cval = 0.f;
+        d.greedy = 0; d.pad = 0;
+        const char *src = nullptr;
+        uint32_t bytes = 0;
         if (item < n_stream) {
             const uint32_t ri = item / (uint32_t)P.nchunk8;
-            c = item - ri * (uint32_t)P.nchunk8;
+            const uint32_t c = item - ri * (uint32_t)P.nchunk8;
             const int2 bs = P.rows[ri];
-            b = bs.x;
-            slot = bs.y;
-            const ReqInfo rq = P.req[b];
-            greedy = rq.greedy;
-            cval = rq.c;
+            const ReqInfo rq = P.req[bs.x];
             bytes = min((uint32_t)CE8, (uint32_t)P.V - c * CE8) * ESZ;
+            d.b = bs.x; d.slot = bs.y; d.c = (int)c; d.nvec = (int)(bytes / 16);
+            d.cval = rq.c; d.greedy = rq.greedy;
+            src = row_ptr(P, bs.x, bs.y, ESZ) + (size_t)c * CE8 * ESZ;
         }
         const int n = (int)min((uint32_t)kStreamBatch, n_stream - base);
-        for (int j = 0; j < n; ++j) {
-            const int jb = __shfl_sync(0xFFFFFFFFu, b, j);
-            const int js = __shfl_sync(0xFFFFFFFFu, slot, j);
-            const int jg = __shfl_sync(0xFFFFFFFFu, greedy, j);
-            const uint32_t jc = __shfl_sync(0xFFFFFFFFu, c, j);
-            const uint32_t jbytes = __shfl_sync(0xFFFFFFFFu, bytes, j);
-            const float jcv = __shfl_sync(0xFFFFFFFFu, cval, j);
-            int ok = 1;
-            uint32_t k = 0;
-            if (lane == 0) {
-                ok = prod_lock(sh);
-                if (ok && !acquire_stage(sh, k)) {
-                    prod_unlock(sh);
-                    ok = 0;
-                }
-            }
-            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+        for (int j0 = 0; j0 < n; j0 += kIssueGroup) {
+            const int nn = min(kIssueGroup, n - j0);
+            const uint32_t k0 = group_begin(sh, nn, lane);
+            if (k0 == ~0u) {
                 if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
                 if (lane == 0) producer_done(P, sh);
                 return;
             }
-            if (lane == 0) {
-                const int s = (int)(k % kFStages);
-                Desc d;
-                d.kind = kKindStream; d.b = jb; d.slot = js; d.c = (int)jc;
-                d.nvec = (int)(jbytes / 16); d.cval = jcv; d.greedy = jg; d.pad = 0;
+            if (lane >= j0 && lane < j0 + nn) {
+                const int s = (int)((k0 + (uint32_t)(lane - j0)) % kFStages);
                 sh.desc[s] = d;
                 uint64_t *fb = reinterpret_cast<uint64_t *>(&sh.full[s]);
-                mbar_expect_tx(fb, jbytes);
-                bulk_g2s(sh.buf[s], row_ptr(P, jb, js, ESZ) + (size_t)jc * CE8 * ESZ, jbytes, fb);
-                prod_unlock(sh);
+                mbar_expect_tx(fb, bytes);
+                bulk_g2s(sh.buf[s], src, bytes, fb);
             }
-            __syncwarp();
+            group_end(sh, lane);
         }
     }
     if (lane == 0) producer_done(P, sh);
@@ -594,65 +613,69 @@ __device__ void stream_producer(const Params &P, FusedShared &sh, int lane) {
 // so a claimed batch never straddles two requests.  Batches are claimed with
 // one atomic add (no retries); a batch whose request is not published yet is
 // waited for (bounded), which never blocks stream items: they have their own
-// producer warp.
-__device__ void task_producer(const Params &P, FusedShared &sh, int esz) {
+// producer warp.  Lane i issues task c0 + i.
+__device__ __noinline__ void task_producer(const Params &P, FusedShared &sh, int esz, int lane) {
     const int ce4 = kSubBytes / esz;
     const unsigned long long nsub_pad =
         (unsigned long long)((P.nsub + kTaskBatch - 1) / kTaskBatch) * kTaskBatch;
     const unsigned long long total = (unsigned long long)(*P.n_sampled) * nsub_pad;
     for (;;) {
-        const unsigned long long h = atomicAdd(P.q_head, (unsigned long long)kTaskBatch);
+        unsigned long long h = 0;
+        if (lane == 0) h = atomicAdd(P.q_head, (unsigned long long)kTaskBatch);
+        h = __shfl_sync(0xFFFFFFFFu, h, 0);
         if (h >= total) break;
         const unsigned long long e = h / nsub_pad;
         const int c0 = (int)(h - e * nsub_pad);
-        int bp1 = ld_volatile_int(&P.q_entries[e]);
-        if (bp1 == 0) {
-            const unsigned long long t0 = global_ns();
-            unsigned int nap = 128;
-            while ((bp1 = ld_volatile_int(&P.q_entries[e])) == 0) {
-                if (global_ns() - t0 > kWaitLimitNs) break;
-                __nanosleep(nap);
-                if (nap < 2048) nap <<= 1;
-            }
+        int bp1 = 0;
+        if (lane == 0) {
+            bp1 = ld_volatile_int(&P.q_entries[e]);
             if (bp1 == 0) {
-                if (P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
-                break;
+                const unsigned long long t0 = global_ns();
+                unsigned int nap = 128;
+                while ((bp1 = ld_volatile_int(&P.q_entries[e])) == 0) {
+                    if (global_ns() - t0 > kWaitLimitNs) break;
+                    __nanosleep(nap);
+                    if (nap < 2048) nap <<= 1;
+                }
             }
+            __threadfence();
+        }
+        bp1 = __shfl_sync(0xFFFFFFFFu, bp1, 0);
+        if (bp1 == 0) {
+            if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
+            break;
         }
         const int b = bp1 - 1;
-        __threadfence();
         const SampInfo si = load_samp(P, b);
-        const int c1 = min(c0 + kTaskBatch, P.nsub);
-        for (int c = c0; c < c1; ++c) {
-            const uint32_t e0 = (uint32_t)c * (uint32_t)ce4;
-            const uint32_t bytes = min((uint32_t)ce4, (uint32_t)P.V - e0) * (uint32_t)esz;
-            uint32_t k;
-            if (!prod_lock(sh)) {
-                if (P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
-                producer_done(P, sh);
+        const int n = min(kTaskBatch, P.nsub - c0);
+        for (int j0 = 0; j0 < n; j0 += kIssueGroup) {
+            const int nn = min(kIssueGroup, n - j0);
+            const uint32_t k0 = group_begin(sh, nn, lane);
+            if (k0 == ~0u) {
+                if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
+                if (lane == 0) producer_done(P, sh);
                 return;
             }
-            if (!acquire_stage(sh, k)) {
-                prod_unlock(sh);
-                if (P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
-                producer_done(P, sh);
-                return;
+            if (lane >= j0 && lane < j0 + nn) {
+                const int c = c0 + lane;
+                const uint32_t e0 = (uint32_t)c * (uint32_t)ce4;
+                const uint32_t bytes = min((uint32_t)ce4, (uint32_t)P.V - e0) * (uint32_t)esz;
+                const int s = (int)((k0 + (uint32_t)(lane - j0)) % kFStages);
+                Desc d;
+                d.kind = kKindSample; d.b = b; d.slot = si.mode; d.c = c;
+                d.nvec = (int)(bytes / 16); d.cval = 0.f; d.greedy = 0; d.pad = 0;
+                sh.desc[s] = d;
+                uint64_t *fb = reinterpret_cast<uint64_t *>(&sh.full[s]);
+                mbar_expect_tx(fb, si.mode == 1 ? 2u * bytes : bytes);
+                bulk_g2s(sh.buf[s], row_ptr(P, b, si.slot_t, esz) + (size_t)e0 * esz, bytes, fb);
+                if (si.mode == 1)
+                    bulk_g2s(sh.buf[s] + kSubBytes / 16,
+                             row_ptr(P, b, si.slot_d, esz) + (size_t)e0 * esz, bytes, fb);
             }
-            const int s = (int)(k % kFStages);
-            Desc d;
-            d.kind = kKindSample; d.b = b; d.slot = si.mode; d.c = c;
-            d.nvec = (int)(bytes / 16); d.cval = 0.f; d.greedy = 0; d.pad = 0;
-            sh.desc[s] = d;
-            uint64_t *fb = reinterpret_cast<uint64_t *>(&sh.full[s]);
-            mbar_expect_tx(fb, si.mode == 1 ? 2u * bytes : bytes);
-            bulk_g2s(sh.buf[s], row_ptr(P, b, si.slot_t, esz) + (size_t)e0 * esz, bytes, fb);
-            if (si.mode == 1)
-                bulk_g2s(sh.buf[s] + kSubBytes / 16, row_ptr(P, b, si.slot_d, esz) + (size_t)e0 * esz,
-                         bytes, fb);
-            prod_unlock(sh);
+            group_end(sh, lane);
         }
     }
-    producer_done(P, sh);
+    if (lane == 0) producer_done(P, sh);
 }
 
 // ------------------------------------------------------------------ consumers
@@ -808,7 +831,7 @@ __global__ void __launch_bounds__(kFThreads, 3) sv_fused(Params P) {
         return;
     }
     if (warp == 1) {
-        if (lane == 0) task_producer(P, sh, ESZ);
+        task_producer(P, sh, ESZ, lane);
         return;
     }
 
