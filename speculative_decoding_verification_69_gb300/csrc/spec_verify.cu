@@ -69,7 +69,7 @@ struct Params {
     const float *temperature;
     unsigned long long seed;
     int B, K, V, nchunk, nslot;
-    int nchunk8;  // 8 KiB stream items per row (fused kernel)
+    int nchunk8;  // 4 KiB stream items per row (fused kernel)
     int nsub;     // 4 KiB sampler chunks per row (fused kernel)
     int32_t *out_tokens;
     int32_t *accept_len;
@@ -749,7 +749,7 @@ static bool items_fit(int B, int K, int V, spec_dtype_t dt) {
 }
 
 static size_t nchunk8_for(int V, spec_dtype_t dt) {
-    const int ce = kStageBytes / (dt == SPEC_DTYPE_BF16 ? 2 : 4);
+    const int ce = kStageBytes / (dt == SPEC_DTYPE_BF16 ? 2 : 4);  // stream items per row
     return (size_t)((V + ce - 1) / ce);
 }
 

@@ -2,46 +2,39 @@
 //
 // One launch streams every needed logit row once and finishes every request
 // inside the same grid, so the row (pair) a rejected request samples from is
-// re-read while it is still resident in L2:
+// re-read while it is still resident in L2.  Every warp works on its own:
 //
-//   producer warps (two per CTA)     consumer warps (kFC per CTA)
-//   ------------------------------   ---------------------------------------------
-//   warp 0: claims stream items in   claim the next stage, wait for its bytes,
-//   batches of 32 from a global      copy it to registers, release it, then:
-//   counter, gathers their row         stream item  -> chunk partial; the last
-//   metadata across its lanes and      chunk of a row combines the row; the last
-//   bulk-copies each 8 KiB item        row of a request decides it (acceptance
-//   into the next free stage           rule, first rejection, outputs) and
-//   warp 1: claims sampler tasks in    publishes its sampler tasks
-//   batches (atomic add), waits for    sampler task -> residual / target masses
-//   their request, copies each 4 KiB   of a 4 KiB chunk of the row (pair); the
-//   chunk of the row (pair)            last task of a request draws the token
-//   both allocate stages from one      (inverse CDF)
-//   shared sequence counter
+//   * stream items (4 KiB of one needed row) are claimed in small batches from a
+//     global counter; the batch's row metadata is gathered across the lanes and
+//     each item is bulk-copied into the warp's own ring of kRing stages of
+//     shared memory, refilled as soon as a stage has been read into registers;
+//   * per item the warp computes a chunk partial (max and either the lowest
+//     argmax or the sum of 2^((z - max) log2(e)/T)); the last chunk of a row
+//     combines the row, the last row of a request decides it (acceptance rule,
+//     first rejection, outputs) and publishes its sampler tasks;
+//   * sampler tasks (4 KiB chunks of the row, or row pair, to draw from) are
+//     claimed by compare-and-swap only once published, read with plain loads
+//     (the rows are still in L2) and reduced to exact residual / target masses;
+//     the last task of a request draws the token (inverse CDF).
 //
-// Work order is request-major, so the rows of a request are read within a short
-// window and a request's sampler tasks find its rows in L2.  Every wait is
-// bounded (SPEC_DEV_TIMEOUT is raised on expiry).  Work is claimed from global
-// counters, never owned in advance, so CTAs that are not resident yet hold no
-// work that resident ones wait for.
+// Completion counts are published (GPU fence + atomic add) when a warp moves
+// to another row or request and before it waits, so no count waits on a
+// waiting warp.  Work is claimed, never owned in advance: CTAs that are not
+// resident hold no work.  Every wait is bounded (SPEC_DEV_TIMEOUT on expiry).
 #pragma once
 #include "sv_common.cuh"
 
 namespace sv {
 
-constexpr int kFC = 4;                         // consumer warps per CTA
-constexpr int kFProd = 2;                      // producer warps per CTA
-constexpr int kFThreads = (kFC + kFProd) * 32;
-constexpr int kFStages = 2 * kFC;              // shared-memory stages per CTA
-// Stage sequence number k goes to stage k % kFStages and to consumer warp
-// k % kFC, so every stage is consumed in order by one warp and filled in order
-// under the producers' lock: no barrier is ever more than one phase away from
-// the phase its waiter names (1-bit parity waits stay unambiguous).
-static_assert(kFStages % kFC == 0, "stages must be a multiple of the consumers");
-constexpr int kStageBytes = 8192;              // one stream item / one sampler task
-constexpr int kStreamVec = kStageBytes / 16 / 32;  // 16 vectors per lane
+constexpr int kFWarps = 8;                     // warps per CTA
+constexpr int kFThreads = kFWarps * 32;
+constexpr int kRing = 3;                       // bulk-copy stages per warp
+constexpr int kStageBytes = 4096;              // one stream item
+constexpr int kStreamVec = kStageBytes / 16 / 32;  // 8 vectors per lane
 constexpr int kSubBytes = 4096;                // per row of a sampler task
 constexpr int kSubVec = kSubBytes / 16 / 32;   // 8 vectors per lane
+constexpr int kStreamBatch = 16;               // stream items per claim (one per lane)
+constexpr int kTaskClaim = 4;                  // sampler tasks per claim
 
 enum { kKindStream = 0, kKindSample = 1, kKindEnd = 2 };
 
@@ -53,14 +46,17 @@ struct Desc {
     int pad;
 };
 
+// One warp's ring.  Item k (the warp's k-th issued item) uses stage k % kRing
+// and phase (k / kRing) & 1 of its barrier: one warp issues and consumes in
+// order, so a waiter is never more than one phase away.
+struct WarpRing {
+    uint4 buf[kRing][kStageBytes / 16];
+    Desc desc[kRing];
+    unsigned long long full[kRing];
+};
+
 struct FusedShared {
-    uint4 buf[kFStages][kStageBytes / 16];
-    Desc desc[kFStages];
-    unsigned long long full[kFStages];
-    unsigned long long empty[kFStages];
-    unsigned int prod_seq;  // producer stage sequence (under prod_lock)
-    unsigned int prod_done; // producers finished
-    int prod_lock;          // serialises stage allocation + fill between producers
+    WarpRing ring[kFWarps];
 };
 
 __device__ __forceinline__ void mbar_arrive(unsigned long long *bar) {
@@ -466,225 +462,10 @@ __device__ __noinline__ void find_request(const Params &P, int b, int lane) {
     if (lane == 0) P.out_tokens[(size_t)b * (P.K + 1) + si.a] = found;
 }
 
-// ------------------------------------------------------------------ producer helpers
+// ------------------------------------------------------------------ completion counts
 
-// Producer lock: stage allocation, the wait for the stage's release and the
-// fill happen in sequence order.  Bounded; returns false on timeout.
-__device__ __forceinline__ bool prod_lock(FusedShared &sh) {
-    if (atomicCAS(&sh.prod_lock, 0, 1) == 0) {
-        __threadfence_block();
-        return true;
-    }
-    const unsigned long long t0 = global_ns();
-    for (;;) {
-        __nanosleep(64);
-        if (atomicCAS(&sh.prod_lock, 0, 1) == 0) {
-            __threadfence_block();
-            return true;
-        }
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-__device__ __forceinline__ void prod_unlock(FusedShared &sh) {
-    __threadfence_block();
-    atomicExch(&sh.prod_lock, 0);
-}
-
-// Next stage for a producer (caller holds the lock): allocate a sequence number
-// and wait until the stage's previous contents have been released.
-__device__ __forceinline__ bool acquire_stage(FusedShared &sh, uint32_t &k) {
-    volatile unsigned int *seq = &sh.prod_seq;
-    k = *seq;
-    *seq = k + 1u;
-    if (k < (uint32_t)kFStages) return true;
-    return mbar_wait_bounded(reinterpret_cast<uint64_t *>(&sh.empty[k % kFStages]),
-                             ((k / kFStages) - 1u) & 1u, kWaitLimitNs);
-}
-
-// The last producer to finish writes one end marker per consumer warp (kFC
-// consecutive sequence numbers: one per consumer).
-__device__ __forceinline__ void producer_done(const Params &P, FusedShared &sh) {
-    if (atomicAdd(&sh.prod_done, 1u) != (unsigned)(kFProd - 1)) return;
-    if (!prod_lock(sh)) {
-        if (P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
-        return;
-    }
-    for (int j = 0; j < kFC; ++j) {
-        uint32_t k;
-        if (!acquire_stage(sh, k) && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
-        const int s = (int)(k % kFStages);
-        Desc d;
-        d.kind = kKindEnd; d.b = d.slot = d.c = d.nvec = d.greedy = d.pad = 0; d.cval = 0.f;
-        sh.desc[s] = d;
-        mbar_arrive(&sh.full[s]);
-    }
-    prod_unlock(sh);
-}
-
-constexpr int kStreamBatch = 32;  // stream items claimed per global atomic (one per lane)
-constexpr int kTaskBatch = 16;    // sampler tasks claimed per global atomic (one per lane)
-constexpr int kIssueGroup = 8;    // stages acquired per lock hold (<= kFStages)
-static_assert(kIssueGroup <= kFStages, "issue group larger than the ring");
-
-// Lane 0 takes the lock, allocates `nn` consecutive sequence numbers and waits,
-// in order, until each of their stages has been released; the lock is then
-// held until the group is issued (`group_end`).  Returns the first sequence
-// number, or ~0u on timeout (lock released).
-__device__ __forceinline__ uint32_t group_begin(FusedShared &sh, int nn, int lane) {
-    uint32_t k0 = 0;
-    int ok = 1;
-    if (lane == 0) {
-        ok = prod_lock(sh);
-        if (ok) {
-            volatile unsigned int *seq = &sh.prod_seq;
-            k0 = *seq;
-            *seq = k0 + (uint32_t)nn;
-            for (int i = 0; i < nn && ok; ++i) {
-                const uint32_t k = k0 + (uint32_t)i;
-                if (k >= (uint32_t)kFStages &&
-                    !mbar_wait_bounded(reinterpret_cast<uint64_t *>(&sh.empty[k % kFStages]),
-                                       ((k / kFStages) - 1u) & 1u, kWaitLimitNs))
-                    ok = 0;
-            }
-            if (!ok) prod_unlock(sh);
-        }
-    }
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    k0 = __shfl_sync(0xFFFFFFFFu, k0, 0);
-    return ok ? k0 : ~0u;
-}
-
-__device__ __forceinline__ void group_end(FusedShared &sh, int lane) {
-    __syncwarp();
-    if (lane == 0) prod_unlock(sh);
-}
-
-template <int DT>
-__device__ __noinline__ void stream_producer(const Params &P, FusedShared &sh, int lane) {
-    constexpr int ESZ = Fmt<DT>::kESZ;
-    constexpr int CE8 = kStageBytes / ESZ;
-    const uint32_t n_stream = (uint32_t)(*P.row_count) * (uint32_t)P.nchunk8;
-    for (;;) {
-        uint32_t base = 0;
-        if (lane == 0) base = atomicAdd(P.stream_head, (unsigned)kStreamBatch);
-        base = __shfl_sync(0xFFFFFFFFu, base, 0);
-        if (base >= n_stream) break;
-        // metadata of the batch, one item per lane
-        const uint32_t item = base + (uint32_t)lane;
-        Desc d;
-        d.kind = kKindStream; d.b = 0; d.slot = 0; d.c = 0; d.nvec = 0; d.cval = 0.f;
-        d.greedy = 0; d.pad = 0;
-        const char *src = nullptr;
-        uint32_t bytes = 0;
-        if (item < n_stream) {
-            const uint32_t ri = item / (uint32_t)P.nchunk8;
-            const uint32_t c = item - ri * (uint32_t)P.nchunk8;
-            const int2 bs = P.rows[ri];
-            const ReqInfo rq = P.req[bs.x];
-            bytes = min((uint32_t)CE8, (uint32_t)P.V - c * CE8) * ESZ;
-            d.b = bs.x; d.slot = bs.y; d.c = (int)c; d.nvec = (int)(bytes / 16);
-            d.cval = rq.c; d.greedy = rq.greedy;
-            src = row_ptr(P, bs.x, bs.y, ESZ) + (size_t)c * CE8 * ESZ;
-        }
-        const int n = (int)min((uint32_t)kStreamBatch, n_stream - base);
-        for (int j0 = 0; j0 < n; j0 += kIssueGroup) {
-            const int nn = min(kIssueGroup, n - j0);
-            const uint32_t k0 = group_begin(sh, nn, lane);
-            if (k0 == ~0u) {
-                if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
-                if (lane == 0) producer_done(P, sh);
-                return;
-            }
-            if (lane >= j0 && lane < j0 + nn) {
-                const int s = (int)((k0 + (uint32_t)(lane - j0)) % kFStages);
-                sh.desc[s] = d;
-                uint64_t *fb = reinterpret_cast<uint64_t *>(&sh.full[s]);
-                mbar_expect_tx(fb, bytes);
-                bulk_g2s(sh.buf[s], src, bytes, fb);
-            }
-            group_end(sh, lane);
-        }
-    }
-    if (lane == 0) producer_done(P, sh);
-}
-
-// Sampler tasks: request entry e (publication order) owns task indices
-// [e * nsub_pad, (e + 1) * nsub_pad), nsub_pad = nsub rounded up to kTaskBatch,
-// so a claimed batch never straddles two requests.  Batches are claimed with
-// one atomic add (no retries); a batch whose request is not published yet is
-// waited for (bounded), which never blocks stream items: they have their own
-// producer warp.  Lane i issues task c0 + i.
-__device__ __noinline__ void task_producer(const Params &P, FusedShared &sh, int esz, int lane) {
-    const int ce4 = kSubBytes / esz;
-    const unsigned long long nsub_pad =
-        (unsigned long long)((P.nsub + kTaskBatch - 1) / kTaskBatch) * kTaskBatch;
-    const unsigned long long total = (unsigned long long)(*P.n_sampled) * nsub_pad;
-    for (;;) {
-        unsigned long long h = 0;
-        if (lane == 0) h = atomicAdd(P.q_head, (unsigned long long)kTaskBatch);
-        h = __shfl_sync(0xFFFFFFFFu, h, 0);
-        if (h >= total) break;
-        const unsigned long long e = h / nsub_pad;
-        const int c0 = (int)(h - e * nsub_pad);
-        int bp1 = 0;
-        if (lane == 0) {
-            bp1 = ld_volatile_int(&P.q_entries[e]);
-            if (bp1 == 0) {
-                const unsigned long long t0 = global_ns();
-                unsigned int nap = 128;
-                while ((bp1 = ld_volatile_int(&P.q_entries[e])) == 0) {
-                    if (global_ns() - t0 > kWaitLimitNs) break;
-                    __nanosleep(nap);
-                    if (nap < 2048) nap <<= 1;
-                }
-            }
-            __threadfence();
-        }
-        bp1 = __shfl_sync(0xFFFFFFFFu, bp1, 0);
-        if (bp1 == 0) {
-            if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
-            break;
-        }
-        const int b = bp1 - 1;
-        const SampInfo si = load_samp(P, b);
-        const int n = min(kTaskBatch, P.nsub - c0);
-        for (int j0 = 0; j0 < n; j0 += kIssueGroup) {
-            const int nn = min(kIssueGroup, n - j0);
-            const uint32_t k0 = group_begin(sh, nn, lane);
-            if (k0 == ~0u) {
-                if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
-                if (lane == 0) producer_done(P, sh);
-                return;
-            }
-            if (lane >= j0 && lane < j0 + nn) {
-                const int c = c0 + lane;
-                const uint32_t e0 = (uint32_t)c * (uint32_t)ce4;
-                const uint32_t bytes = min((uint32_t)ce4, (uint32_t)P.V - e0) * (uint32_t)esz;
-                const int s = (int)((k0 + (uint32_t)(lane - j0)) % kFStages);
-                Desc d;
-                d.kind = kKindSample; d.b = b; d.slot = si.mode; d.c = c;
-                d.nvec = (int)(bytes / 16); d.cval = 0.f; d.greedy = 0; d.pad = 0;
-                sh.desc[s] = d;
-                uint64_t *fb = reinterpret_cast<uint64_t *>(&sh.full[s]);
-                mbar_expect_tx(fb, si.mode == 1 ? 2u * bytes : bytes);
-                bulk_g2s(sh.buf[s], row_ptr(P, b, si.slot_t, esz) + (size_t)e0 * esz, bytes, fb);
-                if (si.mode == 1)
-                    bulk_g2s(sh.buf[s] + kSubBytes / 16,
-                             row_ptr(P, b, si.slot_d, esz) + (size_t)e0 * esz, bytes, fb);
-            }
-            group_end(sh, lane);
-        }
-    }
-    if (lane == 0) producer_done(P, sh);
-}
-
-// ------------------------------------------------------------------ consumers
-
-// Completion counts a consumer warp has not published yet: finished stream
-// items of one row, finished sampler tasks of one request.  Counts are
-// published (GPU fence + atomic add) when the warp moves to another row or
-// request and before it blocks on a stage that is not ready, so a count never
-// waits on a warp that is itself waiting.
+// Completion counts a warp has not published yet: finished stream items of one
+// row, finished sampler tasks of one request.
 struct Pending {
     int row, cnt;   // stream items of row (b * nslot + slot)
     int req, scnt;  // sampler tasks of request b
@@ -731,112 +512,218 @@ __device__ void flush_samples(const Params &P, Pending &pd, int lane) {
     find_request<DT>(P, b, lane);
 }
 
+// ------------------------------------------------------------------ sampler tasks
+
+// Request entry e (publication order) owns task indices [e * nsub_pad,
+// (e + 1) * nsub_pad), nsub_pad = nsub rounded up to kTaskClaim.  Claims are
+// compare-and-swap on published entries only, so a claim never waits.
+// Returns the first claimed task index, or ~0ull.
+__device__ __forceinline__ unsigned long long claim_tasks(const Params &P, unsigned long long total,
+                                                          unsigned long long nsub_pad, int lane) {
+    unsigned long long got = ~0ull;
+    if (lane == 0) {
+        unsigned long long h = *reinterpret_cast<volatile unsigned long long *>(P.q_head);
+        for (int tries = 0; tries < 8 && h < total; ++tries) {
+            if (ld_volatile_int(&P.q_entries[h / nsub_pad]) == 0) break;
+            const unsigned long long old = atomicCAS(P.q_head, h, h + kTaskClaim);
+            if (old == h) {
+                got = h;
+                break;
+            }
+            h = old;
+        }
+        if (got != ~0ull) __threadfence();
+    }
+    return __shfl_sync(0xFFFFFFFFu, got, 0);
+}
+
+// Process the (up to kTaskClaim) sampler tasks starting at task index h.
 template <int DT>
-__device__ void consumer_loop(const Params &P, FusedShared &sh, int cw, int lane) {
+__device__ void run_tasks(const Params &P, unsigned long long h, unsigned long long nsub_pad,
+                          Pending &pd, int lane) {
+    constexpr int EPV = Fmt<DT>::kEPV;
     constexpr int ESZ = Fmt<DT>::kESZ;
-    constexpr int CE8 = kStageBytes / ESZ;
-    Pending pd{-1, 0, -1, 0};
-    for (uint32_t k = (uint32_t)cw;; k += (uint32_t)kFC) {
-        const int s = (int)(k % kFStages);
-        uint64_t *fb = reinterpret_cast<uint64_t *>(&sh.full[s]);
-        const uint32_t par = (k / kFStages) & 1u;
-        int ready = 0;
-        if (lane == 0) ready = mbar_try_wait(fb, par);
-        if (!__shfl_sync(0xFFFFFFFFu, ready, 0)) {
-            flush_rows<DT>(P, pd, lane);
-            flush_samples<DT>(P, pd, lane);
-            if (!mbar_wait_bounded(fb, par, kWaitLimitNs)) {
-                if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
-                return;
-            }
-        } else {
-            mbar_wait_bounded(fb, par, kWaitLimitNs);  // completes at once: every lane observes it
-        }
-        const Desc d = sh.desc[s];
-        if (d.kind == kKindEnd) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.empty[s]);
-            flush_rows<DT>(P, pd, lane);
-            flush_samples<DT>(P, pd, lane);
-            return;
-        }
-        if (d.kind == kKindStream) {
-            flush_samples<DT>(P, pd, lane);  // publish finished sampler tasks at once
-            uint4 v[kStreamVec];
+    constexpr int CE4 = kSubBytes / ESZ;
+    const unsigned long long e = h / nsub_pad;
+    const int c0 = (int)(h - e * nsub_pad);
+    const int b = ld_volatile_int(&P.q_entries[e]) - 1;
+    const SampInfo si = load_samp(P, b);
+    const bool resid = si.mode == 1;
+    const char *rowt = row_ptr(P, b, si.slot_t, ESZ);
+    const char *rowd = resid ? row_ptr(P, b, si.slot_d, ESZ) : rowt;
+    const uint32_t ni = Fmt<DT>::kNegInfWord;
+    if (b != pd.req) {
+        flush_samples<DT>(P, pd, lane);
+        pd.req = b;
+    }
+    const int c1 = min(c0 + kTaskClaim, P.nsub);
+    for (int c = c0; c < c1; ++c) {
+        const long long e0 = (long long)c * CE4;
+        const int nvec = (int)((min((long long)CE4, (long long)P.V - e0) + EPV - 1) / EPV);
+        uint4 vt[kSubVec], vd[kSubVec];
 #pragma unroll
-            for (int i = 0; i < kStreamVec; ++i) v[i] = sh.buf[s][i * 32 + lane];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.empty[s]);
-            const float4 part = stream_partial<DT>(v, d.nvec, d.greedy != 0, d.cval, d.c * CE8, lane);
-            const int row = d.b * P.nslot + d.slot;
-            if (lane == 0) P.part[(size_t)row * P.nchunk8 + d.c] = part;
-            if (row != pd.row) {
-                flush_rows<DT>(P, pd, lane);
-                pd.row = row;
-            }
-            ++pd.cnt;
-        } else {
-            uint4 vt[kSubVec], vd[kSubVec];
-            const uint32_t ni = Fmt<DT>::kNegInfWord;
-            const bool resid = d.slot == 1;
-#pragma unroll
-            for (int i = 0; i < kSubVec; ++i) {
-                vt[i] = sh.buf[s][i * 32 + lane];
-                vd[i] = resid ? sh.buf[s][kSubBytes / 16 + i * 32 + lane] : make_uint4(ni, ni, ni, ni);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.empty[s]);
-            flush_rows<DT>(P, pd, lane);  // publish finished rows at once
-            const SampInfo si = load_samp(P, d.b);
-            float A, Bs, W;
-            FF st, sd;
-            sample_masses<DT>(vt, vd, d.nvec, si, A, Bs, W, st, sd, lane);
-            if (lane == 0) {
-                P.sub[(size_t)d.b * P.nsub + d.c] = make_float4(A, Bs, W, 0.f);
-                P.sexact[(size_t)d.b * P.nsub + d.c] = make_float4(st.hi, st.lo, sd.hi, sd.lo);
-            }
-            if (d.b != pd.req) {
-                flush_samples<DT>(P, pd, lane);
-                pd.req = d.b;
-            }
-            ++pd.scnt;
+        for (int i = 0; i < kSubVec; ++i) {
+            const long long q = e0 + (long long)(i * 32 + lane) * EPV;
+            vt[i] = load_vec<DT, true>(rowt, q, P.V);
+            vd[i] = resid ? load_vec<DT, true>(rowd, q, P.V) : make_uint4(ni, ni, ni, ni);
         }
+        float A, Bs, W;
+        FF st, sd;
+        sample_masses<DT>(vt, vd, nvec, si, A, Bs, W, st, sd, lane);
+        if (lane == 0) {
+            P.sub[(size_t)b * P.nsub + c] = make_float4(A, Bs, W, 0.f);
+            P.sexact[(size_t)b * P.nsub + c] = make_float4(st.hi, st.lo, sd.hi, sd.lo);
+        }
+        ++pd.scnt;
     }
 }
 
 // ------------------------------------------------------------------ the kernel
 
 template <int DT>
-__global__ void __launch_bounds__(kFThreads, 3) sv_fused(Params P) {
+__global__ void __launch_bounds__(kFThreads, 2) sv_fused(Params P) {
     constexpr int ESZ = Fmt<DT>::kESZ;
+    constexpr int CE = kStageBytes / ESZ;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     FusedShared &sh = *reinterpret_cast<FusedShared *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kFStages; ++s) {
-            mbar_init(reinterpret_cast<uint64_t *>(&sh.full[s]), 1);
-            mbar_init(reinterpret_cast<uint64_t *>(&sh.empty[s]), 1);
-        }
-        sh.prod_seq = 0u;
-        sh.prod_done = 0u;
-        sh.prod_lock = 0;
+    WarpRing &rg = sh.ring[warp];
+    if (lane == 0) {
+        for (int s = 0; s < kRing; ++s) mbar_init(reinterpret_cast<uint64_t *>(&rg.full[s]), 1);
         fence_mbar_init();
     }
-    __syncthreads();
+    __syncwarp();
     // the outputs of sv_prep (row list, counters) are read below
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    if (warp == 0) {
-        stream_producer<DT>(P, sh, lane);
-        return;
-    }
-    if (warp == 1) {
-        task_producer(P, sh, ESZ, lane);
-        return;
-    }
+    const uint32_t n_stream = (uint32_t)(*P.row_count) * (uint32_t)P.nchunk8;
+    const unsigned long long nsub_pad =
+        (unsigned long long)((P.nsub + kTaskClaim - 1) / kTaskClaim) * kTaskClaim;
+    const unsigned long long total_tasks = (unsigned long long)(*P.n_sampled) * nsub_pad;
 
-    // -------------------------------------------------------------- consumers
-    consumer_loop<DT>(P, sh, warp - kFProd, lane);
+    Pending pd{-1, 0, -1, 0};
+    uint32_t k_iss = 0, k_cons = 0;  // issued / consumed items of this warp
+    int bcount = 0, bnext = 0;       // items in the current claimed batch, next to issue
+    bool stream_left = true;
+    // per-lane metadata of item (batch base + lane)
+    Desc my;
+    my.kind = kKindStream; my.b = my.slot = my.c = my.nvec = my.greedy = my.pad = 0; my.cval = 0.f;
+    const char *my_src = nullptr;
+    uint32_t my_bytes = 0;
+
+    // Issue the next stream item into stage k_iss % kRing (free by construction).
+    auto refill = [&]() -> bool {
+        if (bnext == bcount) {
+            if (!stream_left) return false;
+            uint32_t base = 0;
+            if (lane == 0) base = atomicAdd(P.stream_head, (unsigned)kStreamBatch);
+            base = __shfl_sync(0xFFFFFFFFu, base, 0);
+            if (base >= n_stream) {
+                stream_left = false;
+                return false;
+            }
+            bcount = (int)min((uint32_t)kStreamBatch, n_stream - base);
+            bnext = 0;
+            const uint32_t item = base + (uint32_t)lane;
+            if (lane < bcount) {
+                const uint32_t ri = item / (uint32_t)P.nchunk8;
+                const uint32_t c = item - ri * (uint32_t)P.nchunk8;
+                const int2 bs = P.rows[ri];
+                const ReqInfo rq = P.req[bs.x];
+                my_bytes = min((uint32_t)CE, (uint32_t)P.V - c * CE) * ESZ;
+                my.b = bs.x; my.slot = bs.y; my.c = (int)c; my.nvec = (int)(my_bytes / 16);
+                my.cval = rq.c; my.greedy = rq.greedy;
+                my_src = row_ptr(P, bs.x, bs.y, ESZ) + (size_t)c * CE * ESZ;
+            }
+        }
+        const int j = bnext++;
+        const int s = (int)(k_iss % kRing);
+        if (lane == j) {
+            fence_proxy_async();  // the stage's previous contents were read by this warp
+            rg.desc[s] = my;
+            uint64_t *fb = reinterpret_cast<uint64_t *>(&rg.full[s]);
+            mbar_expect_tx(fb, my_bytes);
+            bulk_g2s(rg.buf[s], my_src, my_bytes, fb);
+        }
+        __syncwarp();
+        ++k_iss;
+        return true;
+    };
+
+    for (int i = 0; i < kRing; ++i)
+        if (!refill()) break;
+    bool failed = false;
+    while (k_cons != k_iss) {
+        const int s = (int)(k_cons % kRing);
+        uint64_t *fb = reinterpret_cast<uint64_t *>(&rg.full[s]);
+        const uint32_t par = (k_cons / kRing) & 1u;
+        int ready = 0;
+        if (lane == 0) ready = mbar_try_wait(fb, par);
+        if (!__shfl_sync(0xFFFFFFFFu, ready, 0)) flush_rows<DT>(P, pd, lane);  // publish before waiting
+        if (!mbar_wait_bounded(fb, par, kWaitLimitNs)) {
+            failed = true;
+            break;
+        }
+        const Desc d = rg.desc[s];
+        uint4 v[kStreamVec];
+#pragma unroll
+        for (int i = 0; i < kStreamVec; ++i) v[i] = rg.buf[s][i * 32 + lane];
+        __syncwarp();
+        ++k_cons;
+        const bool claimed_before = bnext == bcount;
+        refill();
+        const float4 part = stream_partial<DT>(v, d.nvec, d.greedy != 0, d.cval, d.c * CE, lane);
+        const int row = d.b * P.nslot + d.slot;
+        if (lane == 0) P.part[(size_t)row * P.nchunk8 + d.c] = part;
+        if (row != pd.row) {
+            flush_rows<DT>(P, pd, lane);
+            pd.row = row;
+        }
+        ++pd.cnt;
+        if (claimed_before) {
+            // once per stream batch: take published sampler tasks first
+            const unsigned long long h = claim_tasks(P, total_tasks, nsub_pad, lane);
+            if (h != ~0ull) {
+                flush_rows<DT>(P, pd, lane);
+                run_tasks<DT>(P, h, nsub_pad, pd, lane);
+                flush_samples<DT>(P, pd, lane);
+            }
+        }
+    }
+    if (failed) {
+        if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
+        for (uint32_t k = k_cons + 1; k < k_iss; ++k)  // let this warp's copies land
+            mbar_wait_bounded(reinterpret_cast<uint64_t *>(&rg.full[k % kRing]), (k / kRing) & 1u,
+                              kWaitLimitNs);
+        return;
+    }
+    // stream exhausted: sampler tasks until every task is claimed
+    flush_rows<DT>(P, pd, lane);
+    unsigned long long idle_since = 0;
+    unsigned int nap = 128;
+    for (;;) {
+        const unsigned long long h = claim_tasks(P, total_tasks, nsub_pad, lane);
+        if (h != ~0ull) {
+            run_tasks<DT>(P, h, nsub_pad, pd, lane);
+            flush_samples<DT>(P, pd, lane);
+            idle_since = 0;
+            nap = 128;
+            continue;
+        }
+        unsigned long long head = 0;
+        if (lane == 0) head = *reinterpret_cast<volatile unsigned long long *>(P.q_head);
+        head = __shfl_sync(0xFFFFFFFFu, head, 0);
+        if (head >= total_tasks) break;
+        const unsigned long long now = global_ns();
+        if (idle_since == 0) idle_since = now;
+        if (now - idle_since > kWaitLimitNs) {
+            if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
+            break;
+        }
+        __nanosleep(nap);
+        if (nap < 4096) nap <<= 1;
+    }
+    flush_samples<DT>(P, pd, lane);
 }
 
 } // namespace sv
