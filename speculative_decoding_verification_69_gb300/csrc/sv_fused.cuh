@@ -18,8 +18,8 @@
 //     the last task of a request draws the token (inverse CDF).
 //
 // Completion counts are published (GPU fence + atomic add) when a warp moves
-// to another row or request and before it waits, so no count waits on a
-// waiting warp.  Work is claimed, never owned in advance: CTAs that are not
+// to another row or request and before it waits for other warps' work (task
+// publication), so no count is held by a warp that waits on it.  Work is claimed, never owned in advance: CTAs that are not
 // resident hold no work.  Every wait is bounded (SPEC_DEV_TIMEOUT on expiry).
 #pragma once
 #include "sv_common.cuh"
@@ -657,9 +657,7 @@ __global__ void __launch_bounds__(kFThreads, 2) sv_fused(Params P) {
         const int s = (int)(k_cons % kRing);
         uint64_t *fb = reinterpret_cast<uint64_t *>(&rg.full[s]);
         const uint32_t par = (k_cons / kRing) & 1u;
-        int ready = 0;
-        if (lane == 0) ready = mbar_try_wait(fb, par);
-        if (!__shfl_sync(0xFFFFFFFFu, ready, 0)) flush_rows<DT>(P, pd, lane);  // publish before waiting
+        // this wait depends on nothing but the warp's own copies: pending counts may stay pending
         if (!mbar_wait_bounded(fb, par, kWaitLimitNs)) {
             failed = true;
             break;
