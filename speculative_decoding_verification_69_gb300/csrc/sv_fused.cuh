@@ -34,7 +34,7 @@ constexpr int kStreamVec = kStageBytes / 16 / 32;  // 8 vectors per lane
 constexpr int kSubBytes = 4096;                // per row of a sampler task
 constexpr int kSubVec = kSubBytes / 16 / 32;   // 8 vectors per lane
 constexpr int kStreamBatch = 16;               // stream items per claim (one per lane)
-constexpr int kTaskClaim = 4;                  // sampler tasks per claim
+constexpr int kTaskClaim = 8;                  // sampler tasks per claim
 
 enum { kKindStream = 0, kKindSample = 1, kKindEnd = 2 };
 
@@ -515,15 +515,18 @@ __device__ void flush_samples(const Params &P, Pending &pd, int lane) {
 // ------------------------------------------------------------------ sampler tasks
 
 // Request entry e (publication order) owns task indices [e * nsub_pad,
-// (e + 1) * nsub_pad), nsub_pad = nsub rounded up to kTaskClaim.  Claims are
-// compare-and-swap on published entries only, so a claim never waits.
-// Returns the first claimed task index, or ~0ull.
-__device__ __forceinline__ unsigned long long claim_tasks(const Params &P, unsigned long long total,
-                                                          unsigned long long nsub_pad, int lane) {
+// (e + 1) * nsub_pad), nsub_pad = nsub rounded up to kTaskClaim.
+//
+// While streaming, a warp takes tasks only if they are already published
+// (compare-and-swap, at most two tries per stream batch), so a claim never
+// stops it.  Returns the first claimed task index, or ~0ull.
+__device__ __forceinline__ unsigned long long claim_published(const Params &P,
+                                                              unsigned long long total,
+                                                              unsigned long long nsub_pad, int lane) {
     unsigned long long got = ~0ull;
     if (lane == 0) {
         unsigned long long h = *reinterpret_cast<volatile unsigned long long *>(P.q_head);
-        for (int tries = 0; tries < 8 && h < total; ++tries) {
+        for (int tries = 0; tries < 2 && h < total; ++tries) {
             if (ld_volatile_int(&P.q_entries[h / nsub_pad]) == 0) break;
             const unsigned long long old = atomicCAS(P.q_head, h, h + kTaskClaim);
             if (old == h) {
@@ -533,6 +536,37 @@ __device__ __forceinline__ unsigned long long claim_tasks(const Params &P, unsig
             h = old;
         }
         if (got != ~0ull) __threadfence();
+    }
+    return __shfl_sync(0xFFFFFFFFu, got, 0);
+}
+
+// After streaming, a warp claims the next tasks with one atomic add and waits
+// (bounded) until their request is published; it has nothing else to do, and
+// publication depends only on stream items other warps already hold.
+// Returns the first claimed task index, ~0ull when all are claimed, or ~1ull
+// on timeout.
+__device__ __forceinline__ unsigned long long claim_next(const Params &P, unsigned long long total,
+                                                         unsigned long long nsub_pad, int lane) {
+    unsigned long long got = ~0ull;
+    if (lane == 0) {
+        const unsigned long long h = atomicAdd(P.q_head, (unsigned long long)kTaskClaim);
+        if (h < total) {
+            got = h;
+            const int *flag = &P.q_entries[h / nsub_pad];
+            if (ld_volatile_int(flag) == 0) {
+                const unsigned long long t0 = global_ns();
+                unsigned int nap = 64;
+                while (ld_volatile_int(flag) == 0) {
+                    if (global_ns() - t0 > kWaitLimitNs) {
+                        got = ~1ull;
+                        break;
+                    }
+                    __nanosleep(nap);
+                    if (nap < 1024) nap <<= 1;
+                }
+            }
+            __threadfence();
+        }
     }
     return __shfl_sync(0xFFFFFFFFu, got, 0);
 }
@@ -680,7 +714,7 @@ __global__ void __launch_bounds__(kFThreads, 2) sv_fused(Params P) {
         ++pd.cnt;
         if (claimed_before) {
             // once per stream batch: take published sampler tasks first
-            const unsigned long long h = claim_tasks(P, total_tasks, nsub_pad, lane);
+            const unsigned long long h = claim_published(P, total_tasks, nsub_pad, lane);
             if (h != ~0ull) {
                 flush_rows<DT>(P, pd, lane);
                 run_tasks<DT>(P, h, nsub_pad, pd, lane);
@@ -697,29 +731,15 @@ __global__ void __launch_bounds__(kFThreads, 2) sv_fused(Params P) {
     }
     // stream exhausted: sampler tasks until every task is claimed
     flush_rows<DT>(P, pd, lane);
-    unsigned long long idle_since = 0;
-    unsigned int nap = 128;
     for (;;) {
-        const unsigned long long h = claim_tasks(P, total_tasks, nsub_pad, lane);
-        if (h != ~0ull) {
-            run_tasks<DT>(P, h, nsub_pad, pd, lane);
-            flush_samples<DT>(P, pd, lane);
-            idle_since = 0;
-            nap = 128;
-            continue;
-        }
-        unsigned long long head = 0;
-        if (lane == 0) head = *reinterpret_cast<volatile unsigned long long *>(P.q_head);
-        head = __shfl_sync(0xFFFFFFFFu, head, 0);
-        if (head >= total_tasks) break;
-        const unsigned long long now = global_ns();
-        if (idle_since == 0) idle_since = now;
-        if (now - idle_since > kWaitLimitNs) {
+        const unsigned long long h = claim_next(P, total_tasks, nsub_pad, lane);
+        if (h == ~0ull) break;
+        if (h == ~1ull) {
             if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
             break;
         }
-        __nanosleep(nap);
-        if (nap < 4096) nap <<= 1;
+        run_tasks<DT>(P, h, nsub_pad, pd, lane);
+        flush_samples<DT>(P, pd, lane);
     }
     flush_samples<DT>(P, pd, lane);
 }
