@@ -34,7 +34,7 @@ constexpr int kStreamVec = kStageBytes / 16 / 32;  // 8 vectors per lane
 constexpr int kSubBytes = 4096;                // per row of a sampler task
 constexpr int kSubVec = kSubBytes / 16 / 32;   // 8 vectors per lane
 constexpr int kStreamBatch = 16;               // stream items per claim (one per lane)
-constexpr int kTaskClaim = 8;                  // sampler tasks per claim
+constexpr int kTaskClaim = 2;                  // sampler tasks per claim
 
 enum { kKindStream = 0, kKindSample = 1, kKindEnd = 2 };
 
