@@ -175,27 +175,49 @@ __device__ __forceinline__ float4 stream_partial(const uint4 (&v)[kStreamVec], i
 
 // Row statistics from its chunk partials (one warp): {max, S (sampled) or 0,
 // lowest argmax (greedy) as int bits, -}.
+constexpr int kPerLane = 4;  // chunk records held in registers per lane (128 per warp)
+
 __device__ __forceinline__ float4 combine_row(const Params &P, int b, int slot, bool greedy,
                                               float c, int lane) {
     const float4 *pp = P.part + ((size_t)b * P.nslot + slot) * P.nchunk8;
-    float m = -INFINITY;
-    for (int i = lane; i < P.nchunk8; i += 32) m = fmaxf(m, __ldcg(&pp[i].x));
-    m = warp_max(m);
-    if (greedy) {
-        int amax = INT_MAX;
-        for (int i = lane; i < P.nchunk8; i += 32) {
-            const float4 q = __ldcg(&pp[i]);
-            if (q.x == m) amax = min(amax, __float_as_int(q.w));
+    const int n = P.nchunk8;
+    float m = -INFINITY, S = 0.f;
+    int amax = INT_MAX;
+    // all loads of a round are issued before any is used
+    for (int base = 0; base < n; base += 32 * kPerLane) {
+        float4 q[kPerLane];
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int ci = base + i * 32 + lane;
+            q[i] = ci < n ? __ldcg(&pp[ci]) : make_float4(-INFINITY, 0.f, 0.f, __int_as_float(INT_MAX));
         }
-        return make_float4(m, 0.f, __int_as_float(warp_min_int(amax)), 0.f);
+        float mr = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) mr = fmaxf(mr, q[i].x);
+        mr = warp_max(mr);
+        if (greedy) {
+            int ar = INT_MAX;
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i)
+                if (q[i].x == mr) ar = min(ar, __float_as_int(q[i].w));
+            ar = warp_min_int(ar);
+            if (mr > m || (mr == m && ar < amax)) amax = ar;
+            m = fmaxf(m, mr);
+        } else {
+            const float mn = fmaxf(m, mr);
+            float Sr = 0.f;
+            if (mn > -INFINITY) {
+#pragma unroll
+                for (int i = 0; i < kPerLane; ++i)
+                    if (q[i].x > -INFINITY) Sr += q[i].y * ex2((q[i].x - mn) * c);
+                if (m > -INFINITY) S *= ex2((m - mn) * c);
+            }
+            S += warp_sum(Sr);
+            m = mn;
+        }
     }
-    float S = 0.f;
-    if (m > -INFINITY)
-        for (int i = lane; i < P.nchunk8; i += 32) {
-            const float4 q = __ldcg(&pp[i]);
-            if (q.x > -INFINITY) S += q.y * ex2((q.x - m) * c);
-        }
-    return make_float4(m, warp_sum(S), __int_as_float(-1), 0.f);
+    if (greedy) return make_float4(m, 0.f, __int_as_float(amax), 0.f);
+    return make_float4(m, S, __int_as_float(-1), 0.f);
 }
 
 // ------------------------------------------------------------------ decide
@@ -341,29 +363,56 @@ __device__ __noinline__ void find_request(const Params &P, int b, int lane) {
     const int nch = P.nsub;
     const float4 *sub = P.sub + (size_t)b * nch;
     const float4 *sex = P.sexact + (size_t)b * nch;
-    double st = 0.0, sd = 0.0, zw = 0.0;
-    for (int c = lane; c < nch; c += 32) {
-        const float4 e = __ldcg(&sex[c]);
-        st += (double)e.x + (double)e.y;
-        sd += (double)e.z + (double)e.w;
+    // each lane owns a contiguous block of chunks; records are loaded at once
+    const int per = (nch + 31) / 32;
+    const int c0 = lane * per, c1 = min(nch, c0 + per);
+    float4 q[kPerLane], e[kPerLane];
+    const bool held = per <= kPerLane;
+    double st = 0.0, sd = 0.0;
+    if (held) {
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int c = c0 + i;
+            q[i] = c < c1 ? __ldcg(&sub[c]) : make_float4(0.f, 0.f, 0.f, 0.f);
+            e[i] = c < c1 ? __ldcg(&sex[c]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            st += (double)e[i].x + (double)e[i].y;
+            sd += (double)e[i].z + (double)e[i].w;
+        }
+    } else {
+        for (int c = c0; c < c1; ++c) {
+            const float4 x = __ldcg(&sex[c]);
+            st += (double)x.x + (double)x.y;
+            sd += (double)x.z + (double)x.w;
+        }
     }
     st = warp_sum_d(st);
     sd = warp_sum_d(sd);
     const double kt = resid ? 1.0 / ((double)si.rho_t * st) : 1.0;
     const double kd = resid ? 1.0 / ((double)si.rho_d * sd) : 0.0;
-    // contiguous block of chunks per lane
-    const int per = (nch + 31) / 32;
-    const int c0 = lane * per, c1 = min(nch, c0 + per);
-    double zr = 0.0;
-    for (int c = c0; c < c1; ++c) {
-        const float4 q = __ldcg(&sub[c]);
-        zr += resid ? fmax(0.0, kt * (double)q.x - kd * (double)q.y) : (double)q.z;
-        zw += (double)q.z;
+    auto mass_r = [&](const float4 &x) {
+        return resid ? fmax(0.0, kt * (double)x.x - kd * (double)x.y) : (double)x.z;
+    };
+    double zr = 0.0, zw = 0.0;
+    if (held) {
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i)
+            if (c0 + i < c1) {
+                zr += mass_r(q[i]);
+                zw += (double)q[i].z;
+            }
+    } else {
+        for (int c = c0; c < c1; ++c) {
+            const float4 x = __ldcg(&sub[c]);
+            zr += mass_r(x);
+            zw += (double)x.z;
+        }
     }
     const double Zr = warp_sum_d(zr), Zw = warp_sum_d(zw);
     const bool use_w = !resid || !(Zr > 0.0);
-    const double Z = use_w ? Zw : Zr;
-    const double theta = si.u * Z;
+    const double theta = si.u * (use_w ? Zw : Zr);
     const double mine = use_w ? zw : zr;
     double incl = mine;
 #pragma unroll
@@ -372,16 +421,17 @@ __device__ __noinline__ void find_request(const Params &P, int b, int lane) {
         if (lane >= o) incl += u;
     }
     double base = incl - mine;
-    int my_c = INT_MAX;
+    int my_c = INT_MAX, my_last = -1;
     double my_base = 0.0;
-    if (base <= theta && base + mine > theta) {
-        for (int c = c0; c < c1; ++c) {
-            const float4 q = __ldcg(&sub[c]);
-            const double v = use_w ? (double)q.z : fmax(0.0, kt * (double)q.x - kd * (double)q.y);
+    const bool mine_crosses = base <= theta && base + mine > theta;
+    for (int c = c0; c < c1; ++c) {
+        const float4 x = held ? q[(c - c0) & (kPerLane - 1)] : __ldcg(&sub[c]);
+        const double v = use_w ? (double)x.z : mass_r(x);
+        if (v > 0.0) my_last = c;
+        if (mine_crosses && my_c == INT_MAX) {
             if (base + v > theta) {
                 my_c = c;
                 my_base = base;
-                break;
             }
             base += v;
         }
@@ -395,45 +445,49 @@ __device__ __noinline__ void find_request(const Params &P, int b, int lane) {
         th_local = theta - __shfl_sync(0xFFFFFFFFu, my_base, owner);
     } else {
         // rounding left no crossing: the last chunk with positive mass
-        int last = -1;
-        for (int c = c0; c < c1; ++c) {
-            const float4 q = __ldcg(&sub[c]);
-            const double v = use_w ? (double)q.z : fmax(0.0, kt * (double)q.x - kd * (double)q.y);
-            if (v > 0.0) last = c;
-        }
+        int last = my_last;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xFFFFFFFFu, last, o));
         ch = last >= 0 ? last : nch - 1;
         th_local = INFINITY;
     }
+    // the chosen chunk: all vectors loaded at once, then scanned in order
     const char *rowt = row_ptr(P, b, si.slot_t, ESZ);
     const char *rowd = resid ? row_ptr(P, b, si.slot_d, ESZ) : rowt;
     const long long e0 = (long long)ch * CE;
     const uint32_t ni = Fmt<DT>::kNegInfWord;
+    const bool two = resid && !use_w;
+    uint4 vt[kSubVec], vd[kSubVec];
+#pragma unroll
+    for (int i = 0; i < kSubVec; ++i) {
+        const long long q0 = e0 + (long long)(i * 32 + lane) * EPV;
+        vt[i] = load_vec<DT, true>(rowt, q0, P.V);
+        vd[i] = two ? load_vec<DT, true>(rowd, q0, P.V) : make_uint4(ni, ni, ni, ni);
+    }
     const float2 m2 = make_float2(si.m_t, si.m_d);
     const float2 chi2 = make_float2(si.c_hi, si.c_hi), clo2 = make_float2(si.c_lo, si.c_lo);
-    const float2 rho2 = (resid && !use_w) ? make_float2(si.rho_t, si.rho_d) : make_float2(si.rho_t, 0.f);
+    const float2 rho2 = two ? make_float2(si.rho_t, si.rho_d) : make_float2(si.rho_t, 0.f);
     const float dkt = (float)(kt - 1.0), dkd = (float)(kd - 1.0);
     double run = 0.0;
     int found = INT_MAX, last_pos = -1;
-    for (int i = 0; i < kSubVec && found == INT_MAX; ++i) {
+#pragma unroll
+    for (int i = 0; i < kSubVec; ++i) {
+        if (found != INT_MAX) break;
         const long long q0 = e0 + (long long)(i * 32 + lane) * EPV;
-        const uint4 vt = load_vec<DT, true>(rowt, q0, P.V);
-        const uint4 vd = (resid && !use_w) ? load_vec<DT, true>(rowd, q0, P.V) : make_uint4(ni, ni, ni, ni);
         float w[EPV];
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-            const float2 ee = weight2(make_float2(elem<DT>(vt, e), elem<DT>(vd, e)), m2, chi2, clo2);
+        for (int k = 0; k < EPV; ++k) {
+            const float2 ee = weight2(make_float2(elem<DT>(vt[i], k), elem<DT>(vd[i], k)), m2, chi2, clo2);
             const float2 ab = mul2(ee, rho2);
             float wv;
             if (use_w) wv = ab.x;
             else wv = ab.x > ab.y ? fmaxf(__fsub_rn(__fmaf_rn(ab.x, dkt, ab.x), __fmaf_rn(ab.y, dkd, ab.y)), 0.f) : 0.f;
-            w[e] = wv;
-            if (wv > 0.f && q0 + e < P.V) last_pos = (int)(q0 + e);
+            w[k] = wv;
+            if (wv > 0.f && q0 + k < P.V) last_pos = (int)(q0 + k);
         }
         float vs = w[0];
 #pragma unroll
-        for (int e = 1; e < EPV; ++e) vs = __fadd_rn(vs, w[e]);
+        for (int k = 1; k < EPV; ++k) vs = __fadd_rn(vs, w[k]);
         float inc = vs;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -445,9 +499,9 @@ __device__ __noinline__ void find_request(const Params &P, int b, int lane) {
         if (lo_edge <= th_local && lo_edge + (double)vs > th_local) {
             float ps = 0.f;
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-                ps = e == 0 ? w[0] : __fadd_rn(ps, w[e]);
-                if (tok == INT_MAX && lo_edge + (double)ps > th_local) tok = (int)(q0 + e);
+            for (int k = 0; k < EPV; ++k) {
+                ps = k == 0 ? w[0] : __fadd_rn(ps, w[k]);
+                if (tok == INT_MAX && lo_edge + (double)ps > th_local) tok = (int)(q0 + k);
             }
         }
         found = warp_min_int(tok);
@@ -472,7 +526,10 @@ struct Pending {
 };
 
 template <int DT>
-__device__ void flush_rows(const Params &P, Pending &pd, int lane) {
+__device__ __noinline__ void row_complete(const Params &P, int row, int lane);
+
+template <int DT>
+__device__ __forceinline__ void flush_rows(const Params &P, Pending &pd, int lane) {
     if (pd.cnt == 0) return;
     const int row = pd.row, cnt = pd.cnt;
     pd.cnt = 0;
@@ -481,7 +538,14 @@ __device__ void flush_rows(const Params &P, Pending &pd, int lane) {
         __threadfence();
         last = atomicAdd(&P.row_cnt[row], cnt) + cnt == P.nchunk8;
     }
-    if (!__shfl_sync(0xFFFFFFFFu, last, 0)) return;
+    if (__shfl_sync(0xFFFFFFFFu, last, 0)) row_complete<DT>(P, row, lane);
+}
+
+// The last chunk of a row: combine the row, and decide the request if this was
+// its last row.
+template <int DT>
+__device__ __noinline__ void row_complete(const Params &P, int row, int lane) {
+    int last = 0;
     __threadfence();
     const int b = row / P.nslot, slot = row - b * P.nslot;
     const ReqInfo rq = P.req[b];
@@ -573,8 +637,8 @@ __device__ __forceinline__ unsigned long long claim_next(const Params &P, unsign
 
 // Process the (up to kTaskClaim) sampler tasks starting at task index h.
 template <int DT>
-__device__ void run_tasks(const Params &P, unsigned long long h, unsigned long long nsub_pad,
-                          Pending &pd, int lane) {
+__device__ __noinline__ void run_tasks(const Params &P, unsigned long long h,
+                                       unsigned long long nsub_pad, Pending &pd, int lane) {
     constexpr int EPV = Fmt<DT>::kEPV;
     constexpr int ESZ = Fmt<DT>::kESZ;
     constexpr int CE4 = kSubBytes / ESZ;
