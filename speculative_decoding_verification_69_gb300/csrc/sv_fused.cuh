@@ -637,8 +637,8 @@ __device__ __forceinline__ unsigned long long claim_next(const Params &P, unsign
 
 // Process the (up to kTaskClaim) sampler tasks starting at task index h.
 template <int DT>
-__device__ __noinline__ void run_tasks(const Params &P, unsigned long long h,
-                                       unsigned long long nsub_pad, Pending &pd, int lane) {
+__device__ void run_tasks(const Params &P, unsigned long long h, unsigned long long nsub_pad,
+                          Pending &pd, int lane) {
     constexpr int EPV = Fmt<DT>::kEPV;
     constexpr int ESZ = Fmt<DT>::kESZ;
     constexpr int CE4 = kSubBytes / ESZ;
