@@ -49,9 +49,17 @@ struct Desc {
 // One warp's ring.  Item k (the warp's k-th issued item) uses stage k % kRing
 // and phase (k / kRing) & 1 of its barrier: one warp issues and consumes in
 // order, so a waiter is never more than one phase away.
+struct ItemMeta {
+    Desc d;
+    const char *src;
+    uint32_t bytes;
+    uint32_t pad;
+};
+
 struct WarpRing {
     uint4 buf[kRing][kStageBytes / 16];
     Desc desc[kRing];
+    ItemMeta meta[kStreamBatch];  // the claimed batch, one entry per lane
     unsigned long long full[kRing];
 };
 
@@ -61,6 +69,17 @@ struct FusedShared {
 
 __device__ __forceinline__ void mbar_arrive(unsigned long long *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Atomic add with release semantics: this thread's earlier stores are visible
+// before the add; the result is only needed later, so the warp keeps going.
+__device__ __forceinline__ int atom_add_release(int *p, int v) {
+    int old;
+    asm volatile("atom.add.release.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
 __device__ __forceinline__ int ld_volatile_int(const int *p) {
@@ -305,10 +324,9 @@ __device__ __noinline__ void decide_request(const Params &P, int b, int lane) {
             si.u = uniform_sample(P.seed, (uint32_t)b, (uint32_t)a);
             si.pad2 = 0.0;
             P.samp[b] = si;
-            __threadfence();
             const int e = atomicAdd(P.q_alloc, 1);
+            fence_acq_rel_gpu();  // the sampler state is visible before the entry
             *reinterpret_cast<volatile int *>(&P.q_entries[e]) = b + 1;
-            __threadfence();
         }
     }
     __syncwarp();
@@ -523,22 +541,36 @@ __device__ __noinline__ void find_request(const Params &P, int b, int lane) {
 struct Pending {
     int row, cnt;   // stream items of row (b * nslot + slot)
     int req, scnt;  // sampler tasks of request b
+    // a posted row count whose result (the counter's previous value, lane 0)
+    // is examined at the next flush point
+    int post_row, post_cnt, post_old;
 };
 
 template <int DT>
 __device__ __noinline__ void row_complete(const Params &P, int row, int lane);
 
+// Examine the posted count: if it completed its row, finish the row.
+template <int DT>
+__device__ __forceinline__ void resolve_rows(const Params &P, Pending &pd, int lane) {
+    if (pd.post_cnt == 0) return;
+    const int last = __shfl_sync(0xFFFFFFFFu, pd.post_old + pd.post_cnt == P.nchunk8, 0);
+    const int row = pd.post_row;
+    pd.post_cnt = 0;
+    if (last) row_complete<DT>(P, row, lane);
+}
+
+// Publish the pending count of the current row (release add, result examined
+// at the next flush point or by resolve_rows).
 template <int DT>
 __device__ __forceinline__ void flush_rows(const Params &P, Pending &pd, int lane) {
+    resolve_rows<DT>(P, pd, lane);
     if (pd.cnt == 0) return;
-    const int row = pd.row, cnt = pd.cnt;
+    int old = 0;
+    if (lane == 0) old = atom_add_release(&P.row_cnt[pd.row], pd.cnt);
+    pd.post_row = pd.row;
+    pd.post_cnt = pd.cnt;
+    pd.post_old = old;
     pd.cnt = 0;
-    int last = 0;
-    if (lane == 0) {
-        __threadfence();
-        last = atomicAdd(&P.row_cnt[row], cnt) + cnt == P.nchunk8;
-    }
-    if (__shfl_sync(0xFFFFFFFFu, last, 0)) row_complete<DT>(P, row, lane);
 }
 
 // The last chunk of a row: combine the row, and decide the request if this was
@@ -546,18 +578,17 @@ __device__ __forceinline__ void flush_rows(const Params &P, Pending &pd, int lan
 template <int DT>
 __device__ __noinline__ void row_complete(const Params &P, int row, int lane) {
     int last = 0;
-    __threadfence();
+    fence_acq_rel_gpu();
     const int b = row / P.nslot, slot = row - b * P.nslot;
     const ReqInfo rq = P.req[b];
     const float4 rsv = combine_row(P, b, slot, rq.greedy != 0, rq.c, lane);
     const int nrows = rq.greedy ? rq.L + 1 : 2 * rq.L + 1;
     if (lane == 0) {
         P.rowstat[row] = rsv;
-        __threadfence();
-        last = atomicAdd(&P.req_cnt[b], 1) == nrows - 1;
+        last = atom_add_release(&P.req_cnt[b], 1) == nrows - 1;
     }
     if (!__shfl_sync(0xFFFFFFFFu, last, 0)) return;
-    __threadfence();
+    fence_acq_rel_gpu();
     decide_request<DT>(P, b, lane);
 }
 
@@ -567,12 +598,9 @@ __device__ void flush_samples(const Params &P, Pending &pd, int lane) {
     const int b = pd.req, cnt = pd.scnt;
     pd.scnt = 0;
     int last = 0;
-    if (lane == 0) {
-        __threadfence();
-        last = atomicAdd(&P.samp_cnt[b], cnt) + cnt == P.nsub;
-    }
+    if (lane == 0) last = atom_add_release(&P.samp_cnt[b], cnt) + cnt == P.nsub;
     if (!__shfl_sync(0xFFFFFFFFu, last, 0)) return;
-    __threadfence();
+    fence_acq_rel_gpu();
     find_request<DT>(P, b, lane);
 }
 
@@ -699,28 +727,28 @@ __global__ void __launch_bounds__(kFThreads, 2) sv_fused(Params P) {
         (unsigned long long)((P.nsub + kTaskClaim - 1) / kTaskClaim) * kTaskClaim;
     const unsigned long long total_tasks = (unsigned long long)(*P.n_sampled) * nsub_pad;
 
-    Pending pd{-1, 0, -1, 0};
+    Pending pd{-1, 0, -1, 0, -1, 0, 0};
     uint32_t k_iss = 0, k_cons = 0;  // issued / consumed items of this warp
     int bcount = 0, bnext = 0;       // items in the current claimed batch, next to issue
     bool stream_left = true;
-    // per-lane metadata of item (batch base + lane)
-    Desc my;
-    my.kind = kKindStream; my.b = my.slot = my.c = my.nvec = my.greedy = my.pad = 0; my.cval = 0.f;
-    const char *my_src = nullptr;
-    uint32_t my_bytes = 0;
+    const uint32_t total_warps = gridDim.x * kFWarps;
+    uint32_t claim = max(1u, min((uint32_t)kStreamBatch, n_stream / (2u * total_warps)));
 
     // Issue the next stream item into stage k_iss % kRing (free by construction).
     auto refill = [&]() -> bool {
         if (bnext == bcount) {
             if (!stream_left) return false;
             uint32_t base = 0;
-            if (lane == 0) base = atomicAdd(P.stream_head, (unsigned)kStreamBatch);
+            if (lane == 0) base = atomicAdd(P.stream_head, claim);
             base = __shfl_sync(0xFFFFFFFFu, base, 0);
             if (base >= n_stream) {
                 stream_left = false;
                 return false;
             }
-            bcount = (int)min((uint32_t)kStreamBatch, n_stream - base);
+            bcount = (int)min(claim, n_stream - base);
+            // smaller claims near the end keep the warps' finishing times together
+            const uint32_t left = n_stream - base - (uint32_t)bcount;
+            claim = max(1u, min((uint32_t)kStreamBatch, left / (2u * total_warps)));
             bnext = 0;
             const uint32_t item = base + (uint32_t)lane;
             if (lane < bcount) {
@@ -728,20 +756,25 @@ __global__ void __launch_bounds__(kFThreads, 2) sv_fused(Params P) {
                 const uint32_t c = item - ri * (uint32_t)P.nchunk8;
                 const int2 bs = P.rows[ri];
                 const ReqInfo rq = P.req[bs.x];
-                my_bytes = min((uint32_t)CE, (uint32_t)P.V - c * CE) * ESZ;
-                my.b = bs.x; my.slot = bs.y; my.c = (int)c; my.nvec = (int)(my_bytes / 16);
-                my.cval = rq.c; my.greedy = rq.greedy;
-                my_src = row_ptr(P, bs.x, bs.y, ESZ) + (size_t)c * CE * ESZ;
+                ItemMeta m;
+                m.bytes = min((uint32_t)CE, (uint32_t)P.V - c * CE) * ESZ;
+                m.d.kind = kKindStream; m.d.b = bs.x; m.d.slot = bs.y; m.d.c = (int)c;
+                m.d.nvec = (int)(m.bytes / 16); m.d.cval = rq.c; m.d.greedy = rq.greedy; m.d.pad = 0;
+                m.src = row_ptr(P, bs.x, bs.y, ESZ) + (size_t)c * CE * ESZ;
+                m.pad = 0;
+                rg.meta[lane] = m;
             }
+            __syncwarp();
         }
         const int j = bnext++;
         const int s = (int)(k_iss % kRing);
-        if (lane == j) {
+        if (lane == 0) {
+            const ItemMeta m = rg.meta[j];
             fence_proxy_async();  // the stage's previous contents were read by this warp
-            rg.desc[s] = my;
+            rg.desc[s] = m.d;
             uint64_t *fb = reinterpret_cast<uint64_t *>(&rg.full[s]);
-            mbar_expect_tx(fb, my_bytes);
-            bulk_g2s(rg.buf[s], my_src, my_bytes, fb);
+            mbar_expect_tx(fb, m.bytes);
+            bulk_g2s(rg.buf[s], m.src, m.bytes, fb);
         }
         __syncwarp();
         ++k_iss;
@@ -781,6 +814,7 @@ __global__ void __launch_bounds__(kFThreads, 2) sv_fused(Params P) {
             const unsigned long long h = claim_published(P, total_tasks, nsub_pad, lane);
             if (h != ~0ull) {
                 flush_rows<DT>(P, pd, lane);
+                resolve_rows<DT>(P, pd, lane);
                 run_tasks<DT>(P, h, nsub_pad, pd, lane);
                 flush_samples<DT>(P, pd, lane);
             }
@@ -795,6 +829,7 @@ __global__ void __launch_bounds__(kFThreads, 2) sv_fused(Params P) {
     }
     // stream exhausted: sampler tasks until every task is claimed
     flush_rows<DT>(P, pd, lane);
+    resolve_rows<DT>(P, pd, lane);
     for (;;) {
         const unsigned long long h = claim_next(P, total_tasks, nsub_pad, lane);
         if (h == ~0ull) break;
