@@ -79,7 +79,8 @@ struct Params {
     // workspace
     ReqInfo *req;
     int *row_count;
-    int2 *rows;        // (b, slot) of every needed row, request-major
+    int4 *rows;        // (b, slot, greedy, log2(e)/T float bits) of every needed row, request-major
+    unsigned int epoch;  // per-call tag of the fused kernel's chunk partials
     float4 *part;      // [B, nslot, nchunk]: statistics-pass partials
     SampInfo *samp;    // [B]
     float4 *sub;       // [B, nchunk or nsub]: sampler chunk masses A, B, W
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
     for (int base = 0; base < P.B; base += kPrepThreads) {
         const int b = base + tid;
         int n = 0, L = 0, greedy = 1;
+        float cval = 0.f;
         if (b < P.B) {
             uint32_t st = 0;
             L = P.verify_len ? P.verify_len[b] : P.K;
@@ -169,6 +171,7 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
             }
             ri.pad = 0.f;
             P.req[b] = ri;
+            cval = ri.c;
             if (st && P.dev_status) atomicOr(P.dev_status, st);
             if (!greedy) atomicAdd(&n_samp_s, 1);
             n = L + 1 + (greedy ? 0 : L);
@@ -190,7 +193,7 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
         if (b < P.B) {
             for (int r = 0; r < n; ++r) {
                 int slot = r <= L ? r : (P.K + 1 + (r - L - 1));
-                P.rows[off + r] = make_int2(b, slot);
+                P.rows[off + r] = make_int4(b, slot, greedy, __float_as_int(cval));
             }
         }
         __syncthreads();
@@ -218,7 +221,7 @@ __device__ __forceinline__ void p1_issue(const Params &P, uint32_t item, uint4 *
                                          unsigned long long *bar, int esz) {
     const uint32_t ri = item / (uint32_t)P.nchunk;
     const uint32_t c = item - ri * (uint32_t)P.nchunk;
-    const int2 bs = P.rows[ri];
+    const int4 bs = P.rows[ri];
     const char *row = row_ptr(P, bs.x, bs.y, esz);
     const uint32_t ce = kChunkBytes / esz;
     const uint32_t e0 = c * ce;
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(kP1Warps * 32) sv_pass1(Params P) {
         const uint32_t par = (k / kStages) & 1u;
         const uint32_t ri = item / (uint32_t)P.nchunk;
         const uint32_t c = item - ri * (uint32_t)P.nchunk;
-        const int2 bs = P.rows[ri];
+        const int4 bs = P.rows[ri];
         const int b = bs.x, slot = bs.y;
         const uint32_t e0 = c * CE;
         const int nvec = (int)((min((uint32_t)CE, (uint32_t)P.V - e0) + EPV - 1) / EPV);
@@ -790,7 +793,7 @@ static Layout layout(int B, int K, int V, spec_dtype_t dt) {
     size_t off = 0;
     L.req = off; off = align256(off + sizeof(ReqInfo) * (size_t)B);
     L.row_count = off; off = align256(off + sizeof(int));
-    L.rows = off; off = align256(off + sizeof(int2) * (size_t)B * nslot);
+    L.rows = off; off = align256(off + sizeof(int4) * (size_t)B * nslot);
     L.part = off; off = align256(off + sizeof(float4) * (size_t)B * nslot * npart);
     L.samp = off; off = align256(off + sizeof(SampInfo) * (size_t)B);
     L.sub = off; off = align256(off + sizeof(float4) * (size_t)B * nsamp);
@@ -935,13 +938,16 @@ static spec_status_t verify_impl(const void *target_logits, const void *draft_lo
     char *ws = static_cast<char *>(workspace);
     P.req = reinterpret_cast<ReqInfo *>(ws + L.req);
     P.row_count = reinterpret_cast<int *>(ws + L.row_count);
-    P.rows = reinterpret_cast<int2 *>(ws + L.rows);
+    P.rows = reinterpret_cast<int4 *>(ws + L.rows);
     P.part = reinterpret_cast<float4 *>(ws + L.part);
     P.samp = reinterpret_cast<SampInfo *>(ws + L.samp);
     P.sub = reinterpret_cast<float4 *>(ws + L.sub);
     P.sexact = reinterpret_cast<float4 *>(ws + L.sexact);
     P.nchunk8 = (int)nchunk8_for(V, dtype);
     P.nsub = (int)nsub_for(V, dtype);
+    static unsigned int call_epoch = 0;
+    P.epoch = ++call_epoch;  // never 0: zeroed workspace never matches
+    if (P.epoch == 0) P.epoch = ++call_epoch;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (vec) {
         const Counters cn = counters(B, K);

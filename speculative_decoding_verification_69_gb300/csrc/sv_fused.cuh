@@ -33,7 +33,7 @@ constexpr int kStageBytes = 4096;              // one stream item
 constexpr int kStreamVec = kStageBytes / 16 / 32;  // 8 vectors per lane
 constexpr int kSubBytes = 4096;                // per row of a sampler task
 constexpr int kSubVec = kSubBytes / 16 / 32;   // 8 vectors per lane
-constexpr int kStreamBatch = 16;               // stream items per claim (one per lane)
+constexpr int kStreamBatch = 32;               // stream items per claim (one per lane)
 constexpr int kTaskClaim = 2;                  // sampler tasks per claim
 
 enum { kKindStream = 0, kKindSample = 1, kKindEnd = 2 };
@@ -49,17 +49,10 @@ struct Desc {
 // One warp's ring.  Item k (the warp's k-th issued item) uses stage k % kRing
 // and phase (k / kRing) & 1 of its barrier: one warp issues and consumes in
 // order, so a waiter is never more than one phase away.
-struct ItemMeta {
-    Desc d;
-    const char *src;
-    uint32_t bytes;
-    uint32_t pad;
-};
-
 struct WarpRing {
     uint4 buf[kRing][kStageBytes / 16];
     Desc desc[kRing];
-    ItemMeta meta[kStreamBatch];  // the claimed batch, one entry per lane
+    Desc meta[kStreamBatch];      // the claimed batch, one entry per lane
     unsigned long long full[kRing];
 };
 
@@ -130,8 +123,9 @@ __device__ __forceinline__ SampInfo load_samp(const Params &P, int b) {
 // ------------------------------------------------------------------ stream item
 
 // Chunk partial of one stream item held in registers (lane's vector i is
-// vector i*32 + lane of the chunk): greedy rows {max, -, -, lowest argmax},
-// sampled rows {max, sum 2^((z - max) c), -, -1}.
+// vector i*32 + lane of the chunk): greedy rows {max, -, lowest argmax, -},
+// sampled rows {max, sum 2^((z - max) c), -1, -}; the caller stores the call's
+// epoch in .w.
 template <int DT>
 __device__ __forceinline__ float4 stream_partial(const uint4 (&v)[kStreamVec], int nvec, bool greedy,
                                                  float c, int e0, int lane) {
@@ -164,7 +158,7 @@ __device__ __forceinline__ float4 stream_partial(const uint4 (&v)[kStreamVec], i
                 }
             }
         }
-        return make_float4(m, 0.f, 0.f, __int_as_float(warp_min_int(idx)));
+        return make_float4(m, 0.f, __int_as_float(warp_min_int(idx)), 0.f);
     }
     float s = 0.f;
     if (m > -INFINITY) {
@@ -187,7 +181,7 @@ __device__ __forceinline__ float4 stream_partial(const uint4 (&v)[kStreamVec], i
         const float2 t = add2(u2f(a0), u2f(a1));
         s = t.x + t.y;
     }
-    return make_float4(m, warp_sum(s), 0.f, __int_as_float(-1));
+    return make_float4(m, warp_sum(s), __int_as_float(-1), 0.f);
 }
 
 // ------------------------------------------------------------------ row combine
@@ -196,19 +190,43 @@ __device__ __forceinline__ float4 stream_partial(const uint4 (&v)[kStreamVec], i
 // lowest argmax (greedy) as int bits, -}.
 constexpr int kPerLane = 4;  // chunk records held in registers per lane (128 per warp)
 
+// A chunk partial of this call: its .w holds the call's epoch.  Partials are
+// published with relaxed counters, so the combining warp re-reads (bounded) a
+// record until its tag shows it; a 16-byte record is written in one store.
+__device__ __forceinline__ float4 load_partial(const float4 *p, unsigned int epoch, bool &ok) {
+    float4 q = __ldcg(p);
+    if (__float_as_uint(q.w) == epoch) return q;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        __nanosleep(32);
+        q = __ldcg(p);
+        if (__float_as_uint(q.w) == epoch) return q;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            ok = false;
+            return q;
+        }
+    }
+}
+
 __device__ __forceinline__ float4 combine_row(const Params &P, int b, int slot, bool greedy,
                                               float c, int lane) {
     const float4 *pp = P.part + ((size_t)b * P.nslot + slot) * P.nchunk8;
     const int n = P.nchunk8;
     float m = -INFINITY, S = 0.f;
     int amax = INT_MAX;
+    bool ok = true;
     // all loads of a round are issued before any is used
     for (int base = 0; base < n; base += 32 * kPerLane) {
         float4 q[kPerLane];
 #pragma unroll
         for (int i = 0; i < kPerLane; ++i) {
             const int ci = base + i * 32 + lane;
-            q[i] = ci < n ? __ldcg(&pp[ci]) : make_float4(-INFINITY, 0.f, 0.f, __int_as_float(INT_MAX));
+            q[i] = ci < n ? __ldcg(&pp[ci]) : make_float4(-INFINITY, 0.f, __int_as_float(INT_MAX), 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int ci = base + i * 32 + lane;
+            if (ci < n && __float_as_uint(q[i].w) != P.epoch) q[i] = load_partial(&pp[ci], P.epoch, ok);
         }
         float mr = -INFINITY;
 #pragma unroll
@@ -218,7 +236,7 @@ __device__ __forceinline__ float4 combine_row(const Params &P, int b, int slot, 
             int ar = INT_MAX;
 #pragma unroll
             for (int i = 0; i < kPerLane; ++i)
-                if (q[i].x == mr) ar = min(ar, __float_as_int(q[i].w));
+                if (q[i].x == mr) ar = min(ar, __float_as_int(q[i].z));
             ar = warp_min_int(ar);
             if (mr > m || (mr == m && ar < amax)) amax = ar;
             m = fmaxf(m, mr);
@@ -235,6 +253,8 @@ __device__ __forceinline__ float4 combine_row(const Params &P, int b, int slot, 
             m = mn;
         }
     }
+    if (__any_sync(0xFFFFFFFFu, !ok) && lane == 0 && P.dev_status)
+        atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
     if (greedy) return make_float4(m, 0.f, __int_as_float(amax), 0.f);
     return make_float4(m, S, __int_as_float(-1), 0.f);
 }
@@ -559,14 +579,15 @@ __device__ __forceinline__ void resolve_rows(const Params &P, Pending &pd, int l
     if (last) row_complete<DT>(P, row, lane);
 }
 
-// Publish the pending count of the current row (release add, result examined
-// at the next flush point or by resolve_rows).
+// Publish the pending count of the current row (relaxed add: the combining
+// warp validates the partials' tags; the result is examined at the next flush
+// point or by resolve_rows, so the warp does not wait for it).
 template <int DT>
 __device__ __forceinline__ void flush_rows(const Params &P, Pending &pd, int lane) {
     resolve_rows<DT>(P, pd, lane);
     if (pd.cnt == 0) return;
     int old = 0;
-    if (lane == 0) old = atom_add_release(&P.row_cnt[pd.row], pd.cnt);
+    if (lane == 0) old = atomicAdd(&P.row_cnt[pd.row], pd.cnt);  // partials carry tags: relaxed
     pd.post_row = pd.row;
     pd.post_cnt = pd.cnt;
     pd.post_old = old;
@@ -726,55 +747,66 @@ __global__ void __launch_bounds__(kFThreads, 2) sv_fused(Params P) {
     const unsigned long long nsub_pad =
         (unsigned long long)((P.nsub + kTaskClaim - 1) / kTaskClaim) * kTaskClaim;
     const unsigned long long total_tasks = (unsigned long long)(*P.n_sampled) * nsub_pad;
+    const uint32_t total_warps = gridDim.x * kFWarps;
 
     Pending pd{-1, 0, -1, 0, -1, 0, 0};
     uint32_t k_iss = 0, k_cons = 0;  // issued / consumed items of this warp
-    int bcount = 0, bnext = 0;       // items in the current claimed batch, next to issue
+    int bcount = 0, bnext = 0;       // items in the current batch (metadata in rg.meta), next to issue
     bool stream_left = true;
-    const uint32_t total_warps = gridDim.x * kFWarps;
+    // the next batch is claimed one batch ahead; lane 0 holds the claim's result
     uint32_t claim = max(1u, min((uint32_t)kStreamBatch, n_stream / (2u * total_warps)));
+    uint32_t ahead_base = 0, ahead_claim = claim;
+    if (lane == 0) ahead_base = atomicAdd(P.stream_head, claim);
+    // task-queue state read one batch ahead (lane 0)
+    unsigned long long pf_head = 0;
+    int pf_alloc = 0;
+
+    // Switch to the batch claimed ahead and claim the following one.
+    auto next_batch = [&]() -> bool {
+        const uint32_t base = __shfl_sync(0xFFFFFFFFu, ahead_base, 0);
+        if (base >= n_stream) {
+            stream_left = false;
+            return false;
+        }
+        bcount = (int)min(ahead_claim, n_stream - base);
+        bnext = 0;
+        if (lane < bcount) {
+            const uint32_t item = base + (uint32_t)lane;
+            const uint32_t ri = item / (uint32_t)P.nchunk8;
+            const uint32_t c = item - ri * (uint32_t)P.nchunk8;
+            const int4 r = P.rows[ri];
+            Desc m;
+            m.kind = kKindStream; m.b = r.x; m.slot = r.y; m.c = (int)c;
+            m.nvec = (int)(min((uint32_t)CE, (uint32_t)P.V - c * CE) * ESZ / 16);
+            m.cval = __int_as_float(r.w); m.greedy = r.z; m.pad = 0;
+            rg.meta[lane] = m;
+        }
+        // smaller claims near the end keep the warps' finishing times together
+        const uint32_t left = n_stream - base - (uint32_t)bcount;
+        claim = max(1u, min((uint32_t)kStreamBatch, left / (2u * total_warps)));
+        ahead_claim = claim;
+        if (lane == 0) {
+            ahead_base = atomicAdd(P.stream_head, claim);
+            pf_head = *reinterpret_cast<volatile unsigned long long *>(P.q_head);
+            pf_alloc = ld_volatile_int(P.q_alloc);
+        }
+        __syncwarp();
+        return true;
+    };
 
     // Issue the next stream item into stage k_iss % kRing (free by construction).
     auto refill = [&]() -> bool {
-        if (bnext == bcount) {
-            if (!stream_left) return false;
-            uint32_t base = 0;
-            if (lane == 0) base = atomicAdd(P.stream_head, claim);
-            base = __shfl_sync(0xFFFFFFFFu, base, 0);
-            if (base >= n_stream) {
-                stream_left = false;
-                return false;
-            }
-            bcount = (int)min(claim, n_stream - base);
-            // smaller claims near the end keep the warps' finishing times together
-            const uint32_t left = n_stream - base - (uint32_t)bcount;
-            claim = max(1u, min((uint32_t)kStreamBatch, left / (2u * total_warps)));
-            bnext = 0;
-            const uint32_t item = base + (uint32_t)lane;
-            if (lane < bcount) {
-                const uint32_t ri = item / (uint32_t)P.nchunk8;
-                const uint32_t c = item - ri * (uint32_t)P.nchunk8;
-                const int2 bs = P.rows[ri];
-                const ReqInfo rq = P.req[bs.x];
-                ItemMeta m;
-                m.bytes = min((uint32_t)CE, (uint32_t)P.V - c * CE) * ESZ;
-                m.d.kind = kKindStream; m.d.b = bs.x; m.d.slot = bs.y; m.d.c = (int)c;
-                m.d.nvec = (int)(m.bytes / 16); m.d.cval = rq.c; m.d.greedy = rq.greedy; m.d.pad = 0;
-                m.src = row_ptr(P, bs.x, bs.y, ESZ) + (size_t)c * CE * ESZ;
-                m.pad = 0;
-                rg.meta[lane] = m;
-            }
-            __syncwarp();
-        }
+        if (bnext == bcount && (!stream_left || !next_batch())) return false;
         const int j = bnext++;
         const int s = (int)(k_iss % kRing);
         if (lane == 0) {
-            const ItemMeta m = rg.meta[j];
+            const Desc m = rg.meta[j];
+            const uint32_t bytes = (uint32_t)m.nvec * 16u;
             fence_proxy_async();  // the stage's previous contents were read by this warp
-            rg.desc[s] = m.d;
+            rg.desc[s] = m;
             uint64_t *fb = reinterpret_cast<uint64_t *>(&rg.full[s]);
-            mbar_expect_tx(fb, m.bytes);
-            bulk_g2s(rg.buf[s], m.src, m.bytes, fb);
+            mbar_expect_tx(fb, bytes);
+            bulk_g2s(rg.buf[s], row_ptr(P, m.b, m.slot, ESZ) + (size_t)m.c * CE * ESZ, bytes, fb);
         }
         __syncwarp();
         ++k_iss;
@@ -799,9 +831,13 @@ __global__ void __launch_bounds__(kFThreads, 2) sv_fused(Params P) {
         for (int i = 0; i < kStreamVec; ++i) v[i] = rg.buf[s][i * 32 + lane];
         __syncwarp();
         ++k_cons;
-        const bool claimed_before = bnext == bcount;
+        // task-queue state prefetched at the previous batch switch
+        const int tasks_hint =
+            __shfl_sync(0xFFFFFFFFu, (int)(pf_head < (unsigned long long)pf_alloc * nsub_pad), 0);
+        const bool switching = bnext == bcount;
         refill();
-        const float4 part = stream_partial<DT>(v, d.nvec, d.greedy != 0, d.cval, d.c * CE, lane);
+        float4 part = stream_partial<DT>(v, d.nvec, d.greedy != 0, d.cval, d.c * CE, lane);
+        part.w = __uint_as_float(P.epoch);
         const int row = d.b * P.nslot + d.slot;
         if (lane == 0) P.part[(size_t)row * P.nchunk8 + d.c] = part;
         if (row != pd.row) {
@@ -809,8 +845,8 @@ __global__ void __launch_bounds__(kFThreads, 2) sv_fused(Params P) {
             pd.row = row;
         }
         ++pd.cnt;
-        if (claimed_before) {
-            // once per stream batch: take published sampler tasks first
+        if (switching && tasks_hint) {
+            // published sampler tasks were waiting at the last batch switch: take some
             const unsigned long long h = claim_published(P, total_tasks, nsub_pad, lane);
             if (h != ~0ull) {
                 flush_rows<DT>(P, pd, lane);
