@@ -363,7 +363,7 @@ def run_ours(args, world, rank, local):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "sv_fused",
+            "kernel": "sv_pass1",
             "achieved": achieved,
             "peak": peak,
             "peak_source": peak_kind,

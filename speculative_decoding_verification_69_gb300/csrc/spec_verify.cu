@@ -69,8 +69,6 @@ struct Params {
     const float *temperature;
     unsigned long long seed;
     int B, K, V, nchunk, nslot;
-    int nchunk8;  // 4 KiB stream items per row (fused kernel)
-    int nsub;     // 4 KiB sampler chunks per row (fused kernel)
     int32_t *out_tokens;
     int32_t *accept_len;
     uint32_t *dev_status;
@@ -80,21 +78,10 @@ struct Params {
     ReqInfo *req;
     int *row_count;
     int4 *rows;        // (b, slot, greedy, log2(e)/T float bits) of every needed row, request-major
-    unsigned int epoch;  // per-call tag of the fused kernel's chunk partials
     float4 *part;      // [B, nslot, nchunk]: statistics-pass partials
     SampInfo *samp;    // [B]
-    float4 *sub;       // [B, nchunk or nsub]: sampler chunk masses A, B, W
-    float4 *sexact;    // [B, nchunk or nsub]: exact sums of e (hi, lo) and e' (hi, lo)
-    // fused kernel only
-    float4 *rowstat;   // [B, nslot]: row max, S, argmax bits
-    int *row_cnt;      // [B, nslot] finished stream items per row
-    int *req_cnt;      // [B] finished rows per request
-    int *samp_cnt;     // [B] finished sampler tasks per request
-    int *q_entries;    // [B] published requests (b + 1), in publication order
-    int *q_alloc;      // next queue slot
-    int *n_sampled;    // number of sampled requests
-    unsigned long long *q_head;     // next sampler task
-    unsigned int *stream_head;      // next stream item
+    float4 *sub;       // [B, nchunk]: sampler chunk masses A, B, W
+    float4 *sexact;    // [B, nchunk]: exact sums of e (hi, lo) and e' (hi, lo)
 };
 
 __device__ __forceinline__ const char *row_ptr(const Params &P, int b, int slot, int esz) {
@@ -118,25 +105,8 @@ constexpr int kPrepThreads = 1024;
 __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
     __shared__ int warp_tot[kPrepThreads / 32];
     __shared__ int carry_s;
-    __shared__ int n_samp_s;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    if (tid == 0) {
-        carry_s = 0;
-        n_samp_s = 0;
-    }
-    if (P.row_cnt) {
-        for (int i = tid; i < P.B * P.nslot; i += kPrepThreads) P.row_cnt[i] = 0;
-        for (int i = tid; i < P.B; i += kPrepThreads) {
-            P.req_cnt[i] = 0;
-            P.samp_cnt[i] = 0;
-            P.q_entries[i] = 0;
-        }
-        if (tid == 0) {
-            *P.q_alloc = 0;
-            *P.q_head = 0ull;
-            *P.stream_head = 0u;
-        }
-    }
+    if (tid == 0) carry_s = 0;
     __syncthreads();
     for (int base = 0; base < P.B; base += kPrepThreads) {
         const int b = base + tid;
@@ -173,7 +143,6 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
             P.req[b] = ri;
             cval = ri.c;
             if (st && P.dev_status) atomicOr(P.dev_status, st);
-            if (!greedy) atomicAdd(&n_samp_s, 1);
             n = L + 1 + (greedy ? 0 : L);
         }
         // block exclusive scan of n
@@ -200,10 +169,7 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
         if (tid == 0) carry_s += block_tot;
         __syncthreads();
     }
-    if (tid == 0) {
-        *P.row_count = carry_s;
-        if (P.n_sampled) *P.n_sampled = n_samp_s;
-    }
+    if (tid == 0) *P.row_count = carry_s;
 }
 
 // ------------------------------------------------------------------ 2. statistics pass
@@ -720,16 +686,10 @@ __global__ void sv_schedule(const float *__restrict__ mp, float thr, int B, int 
     out[b] = L;
 }
 
-} // namespace sv
-
-#include "sv_fused.cuh"
-
-namespace sv {
-
 // ------------------------------------------------------------------ host side
 
 struct Layout {
-    size_t req, row_count, rows, part, samp, sub, sexact, rowstat, counters, total;
+    size_t req, row_count, rows, part, samp, sub, sexact, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -751,55 +711,18 @@ static bool items_fit(int B, int K, int V, spec_dtype_t dt) {
     return (size_t)B * (size_t)(2 * K + 1) * nchunk_for(V, dt) < ((size_t)1 << 31);
 }
 
-static size_t nchunk8_for(int V, spec_dtype_t dt) {
-    const int ce = kStageBytes / (dt == SPEC_DTYPE_BF16 ? 2 : 4);  // stream items per row
-    return (size_t)((V + ce - 1) / ce);
-}
-
-static size_t nsub_for(int V, spec_dtype_t dt) {
-    const int ce = kSubBytes / (dt == SPEC_DTYPE_BF16 ? 2 : 4);
-    return (size_t)((V + ce - 1) / ce);
-}
-
-// Counter block of the fused kernel (ints unless noted).
-struct Counters {
-    size_t row_cnt, req_cnt, samp_cnt, q_entries, q_alloc, n_sampled, q_head, stream_head, total;
-};
-
-static Counters counters(int B, int K) {
-    Counters c{};
-    const size_t nslot = (size_t)(2 * K + 1);
-    size_t off = 0;
-    c.q_head = off; off += 8;  // 64-bit first: aligned
-    c.row_cnt = off; off += 4 * (size_t)B * nslot;
-    c.req_cnt = off; off += 4 * (size_t)B;
-    c.samp_cnt = off; off += 4 * (size_t)B;
-    c.q_entries = off; off += 4 * (size_t)B;
-    c.q_alloc = off; off += 4;
-    c.n_sampled = off; off += 4;
-    c.stream_head = off; off += 4;
-    c.total = off;
-    return c;
-}
-
 static Layout layout(int B, int K, int V, spec_dtype_t dt) {
     Layout L{};
     const size_t nchunk = nchunk_for(V, dt);
-    const size_t nchunk8 = nchunk8_for(V, dt);
-    const size_t nsub = nsub_for(V, dt);
-    const size_t npart = nchunk > nchunk8 ? nchunk : nchunk8;
-    const size_t nsamp = nchunk > nsub ? nchunk : nsub;
     const size_t nslot = (size_t)(2 * K + 1);
     size_t off = 0;
     L.req = off; off = align256(off + sizeof(ReqInfo) * (size_t)B);
     L.row_count = off; off = align256(off + sizeof(int));
     L.rows = off; off = align256(off + sizeof(int4) * (size_t)B * nslot);
-    L.part = off; off = align256(off + sizeof(float4) * (size_t)B * nslot * npart);
+    L.part = off; off = align256(off + sizeof(float4) * (size_t)B * nslot * nchunk);
     L.samp = off; off = align256(off + sizeof(SampInfo) * (size_t)B);
-    L.sub = off; off = align256(off + sizeof(float4) * (size_t)B * nsamp);
-    L.sexact = off; off = align256(off + sizeof(float4) * (size_t)B * nsamp);
-    L.rowstat = off; off = align256(off + sizeof(float4) * (size_t)B * nslot);
-    L.counters = off; off = align256(off + counters(B, K).total);
+    L.sub = off; off = align256(off + sizeof(float4) * (size_t)B * nchunk);
+    L.sexact = off; off = align256(off + sizeof(float4) * (size_t)B * nchunk);
     L.total = off;
     return L;
 }
@@ -808,7 +731,6 @@ struct DevInfo {
     int sms = 0;
     int occ_p1[2][2] = {{0, 0}, {0, 0}};
     int occ_sample[2][2] = {{0, 0}, {0, 0}};
-    int occ_fused[2] = {0, 0};
     bool ok = false;
 };
 
@@ -833,21 +755,6 @@ static bool setup_kernels(DevInfo &d) {
     return true;
 }
 
-constexpr size_t kFusedSmem = sizeof(FusedShared);
-
-template <int DT>
-static bool setup_fused(DevInfo &d) {
-    if (cudaFuncSetAttribute(sv_fused<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kFusedSmem) != cudaSuccess)
-        return false;
-    int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sv_fused<DT>, kFThreads, kFusedSmem) !=
-        cudaSuccess)
-        return false;
-    d.occ_fused[DT] = o > 0 ? o : 1;
-    return true;
-}
-
 static const DevInfo *dev_info() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
@@ -857,8 +764,7 @@ static const DevInfo *dev_info() {
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return nullptr;
         if (!setup_kernels<kF32, false>(d) || !setup_kernels<kF32, true>(d) ||
-            !setup_kernels<kBF16, false>(d) || !setup_kernels<kBF16, true>(d) ||
-            !setup_fused<kF32>(d) || !setup_fused<kBF16>(d))
+            !setup_kernels<kBF16, false>(d) || !setup_kernels<kBF16, true>(d))
             return nullptr;
         d.sms = sms;
         d.ok = true;
@@ -867,19 +773,8 @@ static const DevInfo *dev_info() {
 }
 
 static cudaEvent_t g_prof_start = nullptr, g_prof_end = nullptr;
-constexpr int kKernelsPerVerify = 2;  // aligned rows: sv_prep + sv_fused
+constexpr int kKernelsPerVerify = 5;
 
-// 16-byte aligned rows: prep + the fused kernel.
-template <int DT>
-static void launch_fused(const Params &P, const DevInfo &d, cudaStream_t s) {
-    sv_prep<<<1, kPrepThreads, 0, s>>>(P);
-    const int g = d.sms * d.occ_fused[DT];
-    if (g_prof_start) cudaEventRecord(g_prof_start, s);
-    sv_fused<DT><<<g, kFThreads, kFusedSmem, s>>>(P);
-    if (g_prof_end) cudaEventRecord(g_prof_end, s);
-}
-
-// Rows that are not 16-byte aligned: five kernels with plain loads.
 template <int DT, bool VEC>
 static void launch_all(const Params &P, const DevInfo &d, cudaStream_t s) {
     sv_prep<<<1, kPrepThreads, 0, s>>>(P);
@@ -943,30 +838,13 @@ static spec_status_t verify_impl(const void *target_logits, const void *draft_lo
     P.samp = reinterpret_cast<SampInfo *>(ws + L.samp);
     P.sub = reinterpret_cast<float4 *>(ws + L.sub);
     P.sexact = reinterpret_cast<float4 *>(ws + L.sexact);
-    P.nchunk8 = (int)nchunk8_for(V, dtype);
-    P.nsub = (int)nsub_for(V, dtype);
-    static unsigned int call_epoch = 0;
-    P.epoch = ++call_epoch;  // never 0: zeroed workspace never matches
-    if (P.epoch == 0) P.epoch = ++call_epoch;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (vec) {
-        const Counters cn = counters(B, K);
-        char *cb = ws + L.counters;
-        P.rowstat = reinterpret_cast<float4 *>(ws + L.rowstat);
-        P.q_head = reinterpret_cast<unsigned long long *>(cb + cn.q_head);
-        P.row_cnt = reinterpret_cast<int *>(cb + cn.row_cnt);
-        P.req_cnt = reinterpret_cast<int *>(cb + cn.req_cnt);
-        P.samp_cnt = reinterpret_cast<int *>(cb + cn.samp_cnt);
-        P.q_entries = reinterpret_cast<int *>(cb + cn.q_entries);
-        P.q_alloc = reinterpret_cast<int *>(cb + cn.q_alloc);
-        P.n_sampled = reinterpret_cast<int *>(cb + cn.n_sampled);
-        P.stream_head = reinterpret_cast<unsigned int *>(cb + cn.stream_head);
-        if (dtype == SPEC_DTYPE_BF16) launch_fused<kBF16>(P, *d, s);
-        else launch_fused<kF32>(P, *d, s);
-    } else if (dtype == SPEC_DTYPE_BF16) {
-        launch_all<kBF16, false>(P, *d, s);
+    if (dtype == SPEC_DTYPE_BF16) {
+        if (vec) launch_all<kBF16, true>(P, *d, s);
+        else launch_all<kBF16, false>(P, *d, s);
     } else {
-        launch_all<kF32, false>(P, *d, s);
+        if (vec) launch_all<kF32, true>(P, *d, s);
+        else launch_all<kF32, false>(P, *d, s);
     }
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
