@@ -173,6 +173,34 @@ void spec_profile_events(void *ev_start, void *ev_end);
 /* Number of kernels one spec_verify call launches (for launch accounting). */
 int spec_verify_kernel_count(void);
 
+/*
+ * spec_verify_noalloc -- spec_verify without a caller-provided workspace, for
+ * callers that cannot allocate device memory at the call site: code that runs
+ * under a no-allocation rule (latency-critical serving loops, where cudaMalloc
+ * can synchronise the device), plugins of frameworks that own every device
+ * allocation, or callers that simply have no scratch buffer to hand.  The
+ * pages have no counterpart to this entry point; it is a deployment aid.
+ *
+ * The scratch is a library-owned static device array of
+ * SPEC_NOALLOC_SCRATCH_BYTES, resident on every GPU that loads the library
+ * until the process exits.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.  The call itself allocates nothing
+ * and frees nothing.  Problems whose workspace (spec_verify_workspace_bytes)
+ * exceeds SPEC_NOALLOC_SCRATCH_BYTES are rejected with SPEC_ERR_WORKSPACE
+ * before anything is launched.  Every call on a device shares the one array
+ * and it keeps the last call's contents (no field needs to start at zero):
+ * calls that may overlap on the GPU (different streams, no ordering) race and
+ * must be serialised by the caller.  Arguments and results are otherwise those
+ * of spec_verify.
+ */
+#define SPEC_NOALLOC_SCRATCH_BYTES (32u << 20)
+spec_status_t spec_verify_noalloc(const void *target_logits, const void *draft_logits,
+                                  spec_dtype_t dtype, const int32_t *draft_tokens,
+                                  const int32_t *verify_len, const float *temperature,
+                                  uint64_t seed, int B, int K, int V, int32_t *out_tokens,
+                                  int32_t *accept_len, uint32_t *dev_status, void *stream);
+
 /* Static description of a status code. */
 const char *spec_status_str(spec_status_t status);
 

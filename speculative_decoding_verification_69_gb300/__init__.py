@@ -55,6 +55,8 @@ def load_library():
     L.spec_verify_debug.restype = ctypes.c_int
     L.spec_schedule_len.argtypes = [f32p, ctypes.c_float, ctypes.c_int, ctypes.c_int, i32p, vp]
     L.spec_schedule_len.restype = ctypes.c_int
+    L.spec_verify_noalloc.argtypes = common[:12] + [u32p, vp]
+    L.spec_verify_noalloc.restype = ctypes.c_int
     L.spec_profile_events.argtypes = [vp, vp]
     L.spec_profile_events.restype = None
     L.spec_verify_kernel_count.argtypes = []
@@ -67,8 +69,31 @@ def load_library():
 
 def exported_symbols():
     return ["spec_verify_workspace_bytes", "spec_verify", "spec_verify_debug",
-            "spec_schedule_len", "spec_profile_events", "spec_verify_kernel_count",
-            "spec_status_str"]
+            "spec_schedule_len", "spec_verify_noalloc", "spec_profile_events",
+            "spec_verify_kernel_count", "spec_status_str"]
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def verify_noalloc(target, draft, tokens, verify_len, temperature, seed, *, out_tokens=None,
+                   accept_len=None, dev_status=None, stream=None):
+    """verify() on the library's static scratch (no workspace): for callers that
+    cannot allocate device memory at the call site.  Pass preallocated
+    out_tokens / accept_len to allocate nothing at all.  Calls on one device
+    share the scratch and must not overlap on the GPU."""
+    L = load_library()
+    B, K, V = _prepare(target, draft, tokens, verify_len, temperature)
+    dev = target.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if accept_len is None:
+        accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    _check(L.spec_verify_noalloc(_ptr(target), _ptr(draft), _dtype_code(target), _ptr(tokens),
+                                 _ptr(verify_len), _ptr(temperature),
+                                 int(seed) & 0xFFFFFFFFFFFFFFFF, B, K, V, _ptr(out_tokens),
+                                 _ptr(accept_len), _ptr(dev_status), _stream(stream)))
+    return out_tokens, accept_len
 
 
 def profile_events(start=None, end=None):

@@ -892,6 +892,36 @@ spec_status_t spec_schedule_len(const float *draft_maxprob, float threshold, int
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- no-allocation entry
+// Library-owned scratch for callers that cannot allocate (see the header).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SPEC_NOALLOC_SCRATCH_BYTES];
+static void *g_noalloc_ptr[64];  // device address of the array, per device
+
+spec_status_t spec_verify_noalloc(const void *target_logits, const void *draft_logits,
+                                  spec_dtype_t dtype, const int32_t *draft_tokens,
+                                  const int32_t *verify_len, const float *temperature,
+                                  uint64_t seed, int B, int K, int V, int32_t *out_tokens,
+                                  int32_t *accept_len, uint32_t *dev_status, void *stream) {
+    const size_t need = spec_verify_workspace_bytes(B, K, V, dtype);
+    if (need == 0) {
+        if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
+        return SPEC_ERR_INVALID_ARG;
+    }
+    if (need > (size_t)SPEC_NOALLOC_SCRATCH_BYTES) return SPEC_ERR_WORKSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPEC_ERR_CUDA;
+    if (!g_noalloc_ptr[dev]) {  // first call on this device: look up the array's address
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+            return SPEC_ERR_CUDA;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    return sv::verify_impl(target_logits, draft_logits, dtype, draft_tokens, verify_len,
+                           temperature, seed, B, K, V, out_tokens, accept_len,
+                           g_noalloc_ptr[dev], (size_t)SPEC_NOALLOC_SCRATCH_BYTES, dev_status,
+                           nullptr, nullptr, stream);
+}
+
 void spec_profile_events(void *ev_start, void *ev_end) {
     if (ev_start && ev_end) {
         sv::g_prof_start = static_cast<cudaEvent_t>(ev_start);
