@@ -82,6 +82,8 @@ struct Params {
     SampInfo *samp;    // [B]
     float4 *sub;       // [B, nchunk]: sampler chunk masses A, B, W
     float4 *sexact;    // [B, nchunk]: exact sums of e (hi, lo) and e' (hi, lo)
+    int *samp_list;    // [B] sampled requests (order of decision)
+    int *samp_count;   // number of entries in samp_list
 };
 
 __device__ __forceinline__ const char *row_ptr(const Params &P, int b, int slot, int esz) {
@@ -101,13 +103,18 @@ __device__ __forceinline__ float load_logit(const char *row, int dt, int x) {
 // ------------------------------------------------------------------ 1. prep
 
 constexpr int kPrepThreads = 1024;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded wait: 2 s
 
 __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
     __shared__ int warp_tot[kPrepThreads / 32];
     __shared__ int carry_s;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    if (tid == 0) carry_s = 0;
+    if (tid == 0) {
+        carry_s = 0;
+        *P.samp_count = 0;
+    }
     __syncthreads();
+    pdl_trigger();
     for (int base = 0; base < P.B; base += kPrepThreads) {
         const int b = base + tid;
         int n = 0, L = 0, greedy = 1;
@@ -115,13 +122,18 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
         if (b < P.B) {
             uint32_t st = 0;
             L = P.verify_len ? P.verify_len[b] : P.K;
+            const float T = P.temperature[b];
             if (L < 0) { L = 0; st |= SPEC_DEV_BAD_LEN; }
             if (L > P.K) { L = P.K; st |= SPEC_DEV_BAD_LEN; }
-            for (int k = 0; k < L; ++k) {
-                int x = P.tokens[(size_t)b * P.K + k];
-                if (x < 0 || x >= P.V) { L = k; st |= SPEC_DEV_BAD_TOKEN; break; }
-            }
-            const float T = P.temperature[b];
+            // all token loads issued before any is checked
+            int tok[SPEC_MAX_K];
+#pragma unroll
+            for (int k = 0; k < SPEC_MAX_K; ++k) tok[k] = k < L ? P.tokens[(size_t)b * P.K + k] : 0;
+            int Lv = L;
+#pragma unroll
+            for (int k = SPEC_MAX_K - 1; k >= 0; --k)
+                if (k < L && (tok[k] < 0 || tok[k] >= P.V)) Lv = k;
+            if (Lv < L) { L = Lv; st |= SPEC_DEV_BAD_TOKEN; }
             greedy = !(isfinite(T) && T >= FLT_MIN);
             ReqInfo ri;
             ri.L = L;
@@ -176,32 +188,86 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
 
 constexpr int kP1Warps = 8;  // warps per CTA; every warp runs its own copy pipeline
 constexpr int kStages = 3;   // bulk-copy stages per warp
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded wait: 2 s
+
+// What the issuing lane learned about a stage's item (the consumer reads it
+// from shared memory instead of global metadata).
+struct StageDesc {
+    int b, slot, c, nvec;
+    float cval;
+    int greedy;
+    int pad0, pad1;
+};
 
 struct P1Shared {
     uint4 buf[kP1Warps][kStages][kChunkBytes / 16];
+    StageDesc desc[kP1Warps][kStages];
     unsigned long long bar[kP1Warps][kStages];
 };
 
-__device__ __forceinline__ void p1_issue(const Params &P, uint32_t item, uint4 *dst,
-                                         unsigned long long *bar, int esz) {
-    const uint32_t ri = item / (uint32_t)P.nchunk;
-    const uint32_t c = item - ri * (uint32_t)P.nchunk;
-    const int4 bs = P.rows[ri];
-    const char *row = row_ptr(P, bs.x, bs.y, esz);
-    const uint32_t ce = kChunkBytes / esz;
-    const uint32_t e0 = c * ce;
-    const uint32_t n = min(ce, (uint32_t)P.V - e0);
-    const uint32_t bytes = n * (uint32_t)esz;
-    mbar_expect_tx(reinterpret_cast<uint64_t *>(bar), bytes);
-    bulk_g2s(dst, row + (size_t)e0 * esz, bytes, reinterpret_cast<uint64_t *>(bar));
+// Chunk partial of one 4 KiB item held in registers (lane's vector i is vector
+// i*32 + lane of the chunk): greedy rows {max, -, lowest argmax, -}; sampled
+// rows {max, sum 2^((z - max) c), -1, -}.
+template <int DT>
+__device__ __forceinline__ float4 chunk_partial(const uint4 (&v)[kVecPerLane], int nvec, bool greedy,
+                                                float c, int e0, int lane) {
+    constexpr int EPV = Fmt<DT>::kEPV;
+    float lm = -INFINITY;
+    if (DT == kBF16) {
+        uint32_t run = 0xFF80FF80u;
+#pragma unroll
+        for (int i = 0; i < kVecPerLane; ++i)
+            if (i * 32 + lane < nvec)
+                run = bf16x2_max(run, bf16x2_max(bf16x2_max(v[i].x, v[i].y), bf16x2_max(v[i].z, v[i].w)));
+        lm = fmaxf(__uint_as_float(run << 16), __uint_as_float(run & 0xFFFF0000u));
+    } else {
+#pragma unroll
+        for (int i = 0; i < kVecPerLane; ++i)
+            if (i * 32 + lane < nvec) lm = fmaxf(lm, vec_max<DT>(v[i]));
+    }
+    const float m = warp_max(lm);
+    if (greedy) {
+        int idx = INT_MAX;
+        if (lm == m) {
+#pragma unroll
+            for (int i = 0; i < kVecPerLane; ++i) {
+                if (i * 32 + lane < nvec) {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e)
+                        if (idx == INT_MAX && elem<DT>(v[i], e) == m) idx = e0 + (i * 32 + lane) * EPV + e;
+                }
+            }
+        }
+        return make_float4(m, 0.f, __int_as_float(warp_min_int(idx)), 0.f);
+    }
+    float s = 0.f;
+    if (m > -INFINITY) {
+        const unsigned long long m2 = f2u(make_float2(m, m)), c2 = f2u(make_float2(c, c));
+        unsigned long long a0 = 0ull, a1 = 0ull;
+#pragma unroll
+        for (int i = 0; i < kVecPerLane; ++i) {
+            if (i * 32 + lane < nvec) {
+                if (DT == kBF16) {
+                    bf16x2_exp_acc(v[i].x, m2, c2, a0);
+                    bf16x2_exp_acc(v[i].y, m2, c2, a1);
+                    bf16x2_exp_acc(v[i].z, m2, c2, a0);
+                    bf16x2_exp_acc(v[i].w, m2, c2, a1);
+                } else {
+                    f32x2_exp_acc(v[i].x, v[i].y, m2, c2, a0);
+                    f32x2_exp_acc(v[i].z, v[i].w, m2, c2, a1);
+                }
+            }
+        }
+        const float2 t = add2(u2f(a0), u2f(a1));
+        s = t.x + t.y;
+    }
+    return make_float4(m, warp_sum(s), __int_as_float(-1), 0.f);
 }
 
-// One item = 4 KiB of one needed logit row.  Warps are independent: each keeps
-// kStages bulk copies in flight into its own shared-memory ring, reads a stage
-// into registers, and writes one partial per item:
-//   greedy rows:  { m_c = max z, -, -, lowest index of m_c }
-//   sampled rows: { m_c = max z, s_c = sum 2^((z - m_c) c), -, -1 }
+// One item = 4 KiB of one needed logit row; item k of a warp is
+// first + k * total_warps (request-major order across the grid).  Each warp
+// keeps kStages bulk copies in flight into its own shared-memory ring; the row
+// metadata of 32 items at a time is gathered across the lanes, so neither the
+// issue nor the consumption of an item waits on a global load.
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kP1Warps * 32) sv_pass1(Params P) {
     constexpr int EPV = Fmt<DT>::kEPV;
@@ -210,174 +276,212 @@ __global__ void __launch_bounds__(kP1Warps * 32) sv_pass1(Params P) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     P1Shared &sh = *reinterpret_cast<P1Shared *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint4(*buf)[kChunkBytes / 16] = sh.buf[warp];
+    StageDesc *desc = sh.desc[warp];
+    unsigned long long *bar = sh.bar[warp];
+    if (VEC && lane == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(reinterpret_cast<uint64_t *>(&bar[s]), 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    pdl_wait();  // the row list comes from sv_prep
+    pdl_trigger();
     const uint32_t nitems = (uint32_t)(*P.row_count) * (uint32_t)P.nchunk;
     const uint32_t first = blockIdx.x * kP1Warps + warp;
     const uint32_t stride = gridDim.x * kP1Warps;
-    uint4(*buf)[kChunkBytes / 16] = sh.buf[warp];
-    unsigned long long *bar = sh.bar[warp];
     const uint32_t ni = Fmt<DT>::kNegInfWord;
     const uint4 neg_inf = make_uint4(ni, ni, ni, ni);
-    if (VEC) {
-        if (lane == 0) {
-            for (int s = 0; s < kStages; ++s) mbar_init(reinterpret_cast<uint64_t *>(&bar[s]), 1);
-            fence_mbar_init();
-            for (int s = 0; s < kStages; ++s) {
-                const uint32_t it = first + (uint32_t)s * stride;
-                if (it < nitems) p1_issue(P, it, buf[s], &bar[s], ESZ);
+
+    // per-lane metadata of the warp's items [mk0, mk0 + 32)
+    int4 mrow = make_int4(0, 0, 0, 0);
+    uint32_t mc = 0;
+    uint32_t mk0 = 0x80000000u;  // no window yet (item counts stay below 2^31)
+    auto meta = [&](uint32_t k, int4 &r, uint32_t &c) {
+        if (k - mk0 >= 32u) {  // gather the next 32 items' metadata
+            mk0 = k & ~31u;
+            const uint32_t item = first + (mk0 + (uint32_t)lane) * stride;
+            if (item < nitems) {
+                const uint32_t ri = item / (uint32_t)P.nchunk;
+                mc = item - ri * (uint32_t)P.nchunk;
+                mrow = P.rows[ri];
             }
         }
+        const int j = (int)(k - mk0);
+        r.x = __shfl_sync(0xFFFFFFFFu, mrow.x, j);
+        r.y = __shfl_sync(0xFFFFFFFFu, mrow.y, j);
+        r.z = __shfl_sync(0xFFFFFFFFu, mrow.z, j);
+        r.w = __shfl_sync(0xFFFFFFFFu, mrow.w, j);
+        c = __shfl_sync(0xFFFFFFFFu, mc, j);
+    };
+    auto nitems_of_warp = (nitems > first) ? (nitems - first + stride - 1) / stride : 0u;
+
+    // issue item k of this warp into stage k % kStages
+    auto issue = [&](uint32_t k) {
+        int4 r;
+        uint32_t c;
+        meta(k, r, c);
+        if (lane == 0) {
+            const int s = (int)(k % kStages);
+            const uint32_t e0 = c * CE;
+            const uint32_t bytes = min((uint32_t)CE, (uint32_t)P.V - e0) * ESZ;
+            StageDesc d;
+            d.b = r.x; d.slot = r.y; d.c = (int)c; d.nvec = (int)(bytes / 16);
+            d.cval = __int_as_float(r.w); d.greedy = r.z; d.pad0 = d.pad1 = 0;
+            desc[s] = d;
+            fence_proxy_async();  // the stage's previous contents were read by this warp
+            mbar_expect_tx(reinterpret_cast<uint64_t *>(&bar[s]), bytes);
+            bulk_g2s(buf[s], row_ptr(P, r.x, r.y, ESZ) + (size_t)e0 * ESZ, bytes,
+                     reinterpret_cast<uint64_t *>(&bar[s]));
+        }
         __syncwarp();
+    };
+
+    if (VEC) {
+        for (uint32_t k = 0; k < (uint32_t)kStages && k < nitems_of_warp; ++k) issue(k);
     }
     uint32_t k = 0;
     bool failed = false;
-    for (uint32_t item = first; item < nitems; item += stride, ++k) {
-        const int s = (int)(k % kStages);
-        const uint32_t par = (k / kStages) & 1u;
-        const uint32_t ri = item / (uint32_t)P.nchunk;
-        const uint32_t c = item - ri * (uint32_t)P.nchunk;
-        const int4 bs = P.rows[ri];
-        const int b = bs.x, slot = bs.y;
-        const uint32_t e0 = c * CE;
-        const int nvec = (int)((min((uint32_t)CE, (uint32_t)P.V - e0) + EPV - 1) / EPV);
+    for (; k < nitems_of_warp; ++k) {
         uint4 v[kVecPerLane];
+        StageDesc d;
         if (VEC) {
-            if (!mbar_wait_bounded(reinterpret_cast<uint64_t *>(&bar[s]), par, kWaitLimitNs)) {
+            const int s = (int)(k % kStages);
+            if (!mbar_wait_bounded(reinterpret_cast<uint64_t *>(&bar[s]), (k / kStages) & 1u,
+                                   kWaitLimitNs)) {
                 failed = true;
                 break;
             }
+            d = desc[s];
 #pragma unroll
             for (int i = 0; i < kVecPerLane; ++i) {
                 const int q = i * 32 + lane;
-                v[i] = q < nvec ? buf[s][q] : neg_inf;
+                v[i] = q < d.nvec ? buf[s][q] : neg_inf;
             }
             __syncwarp();
-            if (lane == 0) {
-                const uint32_t nx = item + (uint32_t)kStages * stride;
-                if (nx < nitems) {
-                    fence_proxy_async();
-                    p1_issue(P, nx, buf[s], &bar[s], ESZ);
-                }
-            }
+            if (k + kStages < nitems_of_warp) issue(k + kStages);
         } else {
-            const char *row = row_ptr(P, b, slot, ESZ);
+            int4 r;
+            uint32_t c;
+            meta(k, r, c);
+            d.b = r.x; d.slot = r.y; d.c = (int)c; d.cval = __int_as_float(r.w); d.greedy = r.z;
+            const uint32_t e0 = c * CE;
+            d.nvec = (int)((min((uint32_t)CE, (uint32_t)P.V - e0) + EPV - 1) / EPV);
+            const char *row = row_ptr(P, r.x, r.y, ESZ);
 #pragma unroll
             for (int i = 0; i < kVecPerLane; ++i)
                 v[i] = load_vec<DT, false>(row, (long long)e0 + (long long)(i * 32 + lane) * EPV, P.V);
         }
-        const ReqInfo rq = P.req[b];
-        float lm = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kVecPerLane; ++i) lm = fmaxf(lm, vec_max<DT>(v[i]));
-        const float m = warp_max(lm);
-        float4 out;
-        if (rq.greedy) {
-            int idx = INT_MAX;
-            if (lm == m) {
-#pragma unroll
-                for (int i = 0; i < kVecPerLane; ++i)
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e)
-                        if (idx == INT_MAX && elem<DT>(v[i], e) == m)
-                            idx = (int)e0 + (i * 32 + lane) * EPV + e;
-            }
-            idx = warp_min_int(idx);
-            out = make_float4(m, 0.f, 0.f, __int_as_float(idx));
-        } else {
-            float ssum = 0.f;
-            if (m > -INFINITY) {
-                const float2 m2 = make_float2(m, m), c2 = make_float2(rq.c, rq.c);
-                float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int i = 0; i < kVecPerLane; ++i) {
-#pragma unroll
-                    for (int e = 0; e < EPV; e += 4) {
-                        const float2 t0 = mul2(sub2(make_float2(elem<DT>(v[i], e), elem<DT>(v[i], e + 1)), m2), c2);
-                        a0 = add2(a0, make_float2(ex2(t0.x), ex2(t0.y)));
-                        const float2 t1 = mul2(sub2(make_float2(elem<DT>(v[i], e + 2), elem<DT>(v[i], e + 3)), m2), c2);
-                        a1 = add2(a1, make_float2(ex2(t1.x), ex2(t1.y)));
-                    }
-                }
-                const float2 a = add2(a0, a1);
-                ssum = a.x + a.y;
-            }
-            ssum = warp_sum(ssum);
-            out = make_float4(m, ssum, 0.f, __int_as_float(-1));
-        }
-        if (lane == 0) P.part[((size_t)b * P.nslot + slot) * P.nchunk + c] = out;
+        const float4 out = chunk_partial<DT>(v, d.nvec, d.greedy != 0, d.cval, d.c * CE, lane);
+        if (lane == 0) P.part[((size_t)d.b * P.nslot + d.slot) * P.nchunk + d.c] = out;
     }
     if (VEC && failed) {
         // report, then let every copy this warp still has in flight land
         if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
-        for (uint32_t kk = k; kk < k + kStages; ++kk) {
-            if (first + kk * stride >= nitems) break;
+        for (uint32_t kk = k; kk < k + kStages && kk < nitems_of_warp; ++kk)
             mbar_wait_bounded(reinterpret_cast<uint64_t *>(&bar[kk % kStages]), (kk / kStages) & 1u,
                               kWaitLimitNs);
-        }
     }
 }
 
 // ------------------------------------------------------------------ 3. decide
 
+constexpr int kPerLane = 4;  // chunk records held in registers per lane (128 per warp)
+
+// Row statistics from its chunk partials (one warp; loads issued up front):
+// {max, S (sampled rows), lowest argmax bits (greedy rows), -}.
+__device__ __forceinline__ float4 combine_row(const Params &P, int b, int slot, bool greedy,
+                                              float c, int lane) {
+    const float4 *pp = P.part + ((size_t)b * P.nslot + slot) * P.nchunk;
+    const int n = P.nchunk;
+    float m = -INFINITY, S = 0.f;
+    int amax = INT_MAX;
+    for (int base = 0; base < n; base += 32 * kPerLane) {
+        float4 q[kPerLane];
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int ci = base + i * 32 + lane;
+            q[i] = ci < n ? pp[ci] : make_float4(-INFINITY, 0.f, __int_as_float(INT_MAX), 0.f);
+        }
+        float mr = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) mr = fmaxf(mr, q[i].x);
+        mr = warp_max(mr);
+        if (greedy) {
+            int ar = INT_MAX;
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i)
+                if (q[i].x == mr) ar = min(ar, __float_as_int(q[i].z));
+            ar = warp_min_int(ar);
+            if (mr > m || (mr == m && ar < amax)) amax = ar;
+            m = fmaxf(m, mr);
+        } else {
+            const float mn = fmaxf(m, mr);
+            float Sr = 0.f;
+            if (mn > -INFINITY) {
+#pragma unroll
+                for (int i = 0; i < kPerLane; ++i)
+                    if (q[i].x > -INFINITY) Sr += q[i].y * ex2((q[i].x - mn) * c);
+                if (m > -INFINITY) S *= ex2((m - mn) * c);
+            }
+            S += warp_sum(Sr);
+            m = mn;
+        }
+    }
+    if (greedy) return make_float4(m, 0.f, __int_as_float(amax), 0.f);
+    return make_float4(m, S, __int_as_float(-1), 0.f);
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
     const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int K = P.K;
-    const ReqInfo rq = P.req[b];
-    const int L = rq.L;
-    const bool greedy = rq.greedy != 0;
     __shared__ float s_m[2 * SPEC_MAX_K + 1];
     __shared__ float s_S[2 * SPEC_MAX_K + 1];
     __shared__ int s_amax[SPEC_MAX_K + 1];
     __shared__ int s_a;
+    // inputs and sv_prep's results (two kernels back) may be read before the wait
+    const ReqInfo rq = P.req[b];
+    const int L = rq.L;
+    const bool greedy = rq.greedy != 0;
+    int x = 0;
+    float g = 0.f, gd = 0.f;
+    if (warp == 0 && lane < L) {
+        x = P.tokens[(size_t)b * K + lane];
+        if (!greedy) {
+            g = load_logit(row_ptr(P, b, lane, Fmt<DT>::kESZ), DT, x);
+            gd = load_logit(row_ptr(P, b, K + 1 + lane, Fmt<DT>::kESZ), DT, x);
+        }
+    }
+    pdl_wait();  // chunk partials come from sv_pass1
+    pdl_trigger();
     const int nrows = greedy ? L + 1 : 2 * L + 1;
-    // row statistics: one warp per row, lanes over the row's chunk partials
     for (int r = warp; r < nrows; r += kWarps) {
         const int slot = r <= L ? r : K + 1 + (r - L - 1);
-        const float4 *pp = P.part + ((size_t)b * P.nslot + slot) * P.nchunk;
-        float m = -INFINITY;
-        for (int c = lane; c < P.nchunk; c += 32) m = fmaxf(m, pp[c].x);
-        m = warp_max(m);
-        float S = 0.f;
-        int amax = INT_MAX;
-        if (greedy) {
-            for (int c = lane; c < P.nchunk; c += 32) {
-                const float4 q = pp[c];
-                if (q.x == m) amax = min(amax, __float_as_int(q.w));
-            }
-            amax = warp_min_int(amax);
-        } else if (m > -INFINITY) {
-            for (int c = lane; c < P.nchunk; c += 32) {
-                const float4 q = pp[c];
-                if (q.x > -INFINITY) S += q.y * ex2((q.x - m) * rq.c);
-            }
-            S = warp_sum(S);
-        }
+        const float4 rs = combine_row(P, b, slot, greedy, rq.c, lane);
         if (lane == 0) {
-            s_m[slot] = m;
-            s_S[slot] = S;
-            if (slot <= K) s_amax[slot] = amax;
+            s_m[slot] = rs.x;
+            s_S[slot] = rs.y;
+            if (slot <= K) s_amax[slot] = __float_as_int(rs.z);
         }
     }
     __syncthreads();
     if (warp == 0) {
         bool acc = true;
+        double p = NAN, q = NAN;
         if (lane < L) {
-            const int x = P.tokens[(size_t)b * K + lane];
             if (greedy) {
                 acc = (x == s_amax[lane]);
             } else {
-                const float g = load_logit(row_ptr(P, b, lane, Fmt<DT>::kESZ), DT, x);
-                const float gd = load_logit(row_ptr(P, b, K + 1 + lane, Fmt<DT>::kESZ), DT, x);
                 const float St = s_S[lane], Sd = s_S[K + 1 + lane];
-                const double p = St > 0.f ? exp2(((double)g - (double)s_m[lane]) * rq.cd) / (double)St : 0.0;
-                const double q = Sd > 0.f ? exp2(((double)gd - (double)s_m[K + 1 + lane]) * rq.cd) / (double)Sd : 0.0;
+                p = St > 0.f ? exp2(((double)g - (double)s_m[lane]) * rq.cd) / (double)St : 0.0;
+                q = Sd > 0.f ? exp2(((double)gd - (double)s_m[K + 1 + lane]) * rq.cd) / (double)Sd : 0.0;
                 const double u = uniform_accept(P.seed, (uint32_t)b, (uint32_t)lane);
                 acc = u * q < p;
-                if (P.dbg_probs) {
-                    P.dbg_probs[((size_t)b * K + lane) * 2 + 0] = p;
-                    P.dbg_probs[((size_t)b * K + lane) * 2 + 1] = q;
-                }
             }
+        }
+        if (P.dbg_probs && lane < K) {
+            P.dbg_probs[((size_t)b * K + lane) * 2 + 0] = (!greedy && lane < L) ? p : NAN;
+            P.dbg_probs[((size_t)b * K + lane) * 2 + 1] = (!greedy && lane < L) ? q : NAN;
         }
         const unsigned rej = ~__ballot_sync(0xFFFFFFFFu, acc);
         const int a = rej ? min(__ffs(rej) - 1, L) : L;
@@ -394,97 +498,71 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
     }
     if (tid == 0) {
         P.accept_len[b] = a;
-        SampInfo si;
-        si.mode = greedy ? 0 : (a < L ? 1 : 2);
-        si.a = a;
-        si.slot_t = a;
-        si.slot_d = K + 1 + a;
-        si.m_t = s_m[a];
-        si.rho_t = 1.f;
-        si.m_d = 0.f;
-        si.rho_d = 0.f;
-        if (si.mode == 1) {
-            si.rho_t = 1.f / s_S[a];
-            si.m_d = s_m[K + 1 + a];
-            si.rho_d = 1.f / s_S[K + 1 + a];
+        if (!greedy) {
+            SampInfo si;
+            si.mode = a < L ? 1 : 2;
+            si.a = a;
+            si.slot_t = a;
+            si.slot_d = K + 1 + a;
+            si.m_t = s_m[a];
+            si.rho_t = 1.f;
+            si.m_d = 0.f;
+            si.rho_d = 0.f;
+            if (si.mode == 1) {
+                si.rho_t = 1.f / s_S[a];
+                si.m_d = s_m[K + 1 + a];
+                si.rho_d = 1.f / s_S[K + 1 + a];
+            }
+            si.c_hi = rq.c_hi;
+            si.c_lo = rq.c_lo;
+            si.pad0 = si.pad1 = 0;
+            si.u = uniform_sample(P.seed, (uint32_t)b, (uint32_t)a);
+            si.pad2 = 0.0;
+            P.samp[b] = si;
+            P.samp_list[atomicAdd(P.samp_count, 1)] = b;  // order is irrelevant to the results
         }
-        si.c_hi = rq.c_hi;
-        si.c_lo = rq.c_lo;
-        si.u = greedy ? 0.0 : uniform_sample(P.seed, (uint32_t)b, (uint32_t)a);
-        P.samp[b] = si;
     }
     if (P.dbg_rows) {
         const int nslot = 2 * K + 1;
         for (int sl = tid; sl < nslot; sl += kThreads) {
             double m = NAN, ls = NAN;
-            const bool read = !greedy && (sl <= L || (sl >= K + 1 && sl - K - 1 < L));
-            if (read) {
+            if (!greedy && (sl <= L || (sl >= K + 1 && sl - K - 1 < L))) {
                 m = (double)s_m[sl] * rq.inv_t;
                 ls = log((double)s_S[sl]);
             }
             P.dbg_rows[((size_t)b * nslot + sl) * 2 + 0] = m;
             P.dbg_rows[((size_t)b * nslot + sl) * 2 + 1] = ls;
         }
-        if (P.dbg_probs)
-            for (int k = (greedy ? 0 : L) + tid; k < K; k += kThreads) {
-                P.dbg_probs[((size_t)b * K + k) * 2 + 0] = NAN;
-                P.dbg_probs[((size_t)b * K + k) * 2 + 1] = NAN;
-            }
     }
 }
 
 // ------------------------------------------------------------------ 4. sampler pass
 
-// Per element pair (target z, draft z') of the sampled row (pair):
-//   e = 2^((z - m) c), e' = 2^((z' - m') c) with the row maxima and two-float c;
-//   a = e * rho, b = e' * rho' with rho = 1/S from the statistics pass.
-// Per chunk: A = sum of a over {a > b}, B = sum of b over {a > b}, W = sum of a,
-// and the exact sums of e and e'.  The residual mass of a chunk is then
-// kappa A - kappa' B with kappa = 1 / (rho * sum e) (exact normaliser).
+// Masses of one 4 KiB chunk of the sampled row (pair).  Per element pair
+// (target z, draft z'): e = 2^((z - m) c), e' = 2^((z' - m') c) with the row
+// maxima and the two-float c; a = e * rho, b = e' * rho' with rho = 1/S from
+// the statistics pass.  A = sum of a over {a > b}, B = sum of b over {a > b},
+// W = sum of a, and the exact sums of e and e' (Fast2Sum).  The residual mass
+// of a chunk is then kappa A - kappa' B, kappa = 1 / (rho * sum e).
 template <int DT>
-__device__ __forceinline__ void pair_weights(float zt, float zd, float2 m2, float2 chi2,
-                                             float2 clo2, float2 rho2, float2 &ee, float2 &ab) {
-    ee = weight2(make_float2(zt, zd), m2, chi2, clo2);
-    ab = mul2(ee, rho2);
-}
-
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(kThreads) sv_sample(Params P) {
+__device__ __forceinline__ void sample_masses(const uint4 (&vt)[kVecPerLane],
+                                              const uint4 (&vd)[kVecPerLane], int nvec,
+                                              const SampInfo &si, float &A, float &Bs, float &W,
+                                              FF &st, FF &sd, int lane) {
     constexpr int EPV = Fmt<DT>::kEPV;
-    constexpr int ESZ = Fmt<DT>::kESZ;
-    constexpr int CE = chunk_elems<DT>();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t nitems = (uint32_t)P.B * (uint32_t)P.nchunk;
-    const uint32_t stride = gridDim.x * kWarps;
-    const uint32_t ni = Fmt<DT>::kNegInfWord;
-    for (uint32_t item = blockIdx.x * kWarps + warp; item < nitems; item += stride) {
-        const uint32_t b = item / (uint32_t)P.nchunk;
-        const uint32_t c = item - b * (uint32_t)P.nchunk;
-        const SampInfo si = P.samp[b];
-        if (si.mode == 0) continue;
-        const bool resid = si.mode == 1;
-        const char *rowt = row_ptr(P, (int)b, si.slot_t, ESZ);
-        const char *rowd = resid ? row_ptr(P, (int)b, si.slot_d, ESZ) : rowt;
-        const long long e0 = (long long)c * CE;
-        uint4 vt[kVecPerLane], vd[kVecPerLane];
+    const float2 m2 = make_float2(si.m_t, si.m_d);
+    const float2 chi2 = make_float2(si.c_hi, si.c_hi), clo2 = make_float2(si.c_lo, si.c_lo);
+    const float2 rho2 = make_float2(si.rho_t, si.rho_d);
+    BiasAcc2 acc;
+    acc.init(1.0f);
+    A = 0.f; Bs = 0.f; W = 0.f;
 #pragma unroll
-        for (int i = 0; i < kVecPerLane; ++i) {
-            const long long q = e0 + (long long)(i * 32 + lane) * EPV;
-            vt[i] = load_vec<DT, VEC>(rowt, q, P.V);
-            vd[i] = resid ? load_vec<DT, VEC>(rowd, q, P.V) : make_uint4(ni, ni, ni, ni);
-        }
-        const float2 m2 = make_float2(si.m_t, si.m_d);
-        const float2 chi2 = make_float2(si.c_hi, si.c_hi), clo2 = make_float2(si.c_lo, si.c_lo);
-        const float2 rho2 = make_float2(si.rho_t, si.rho_d);
-        BiasAcc2 acc;
-        acc.init(1.0f);
-        float A = 0.f, Bs = 0.f, W = 0.f;
-#pragma unroll
-        for (int i = 0; i < kVecPerLane; ++i) {
+    for (int i = 0; i < kVecPerLane; ++i) {
+        if (i * 32 + lane < nvec) {
 #pragma unroll
             for (int e = 0; e < EPV; ++e) {
-                float2 ee, ab;
-                pair_weights<DT>(elem<DT>(vt[i], e), elem<DT>(vd[i], e), m2, chi2, clo2, rho2, ee, ab);
+                const float2 ee = weight2(make_float2(elem<DT>(vt[i], e), elem<DT>(vd[i], e)), m2, chi2, clo2);
+                const float2 ab = mul2(ee, rho2);
                 acc.add(ee);
                 W = __fadd_rn(W, ab.x);
                 if (ab.x > ab.y) {
@@ -493,79 +571,211 @@ __global__ void __launch_bounds__(kThreads) sv_sample(Params P) {
                 }
             }
         }
-        A = warp_sum(A);
-        Bs = warp_sum(Bs);
-        W = warp_sum(W);
-        FF st = warp_sum_ff(ff_add(FF{__fsub_rn(acc.h.x, 1.0f), acc.l.x}, FF{0.f, 0.f}));
-        FF sd = warp_sum_ff(ff_add(FF{__fsub_rn(acc.h.y, 1.0f), acc.l.y}, FF{0.f, 0.f}));
+    }
+    A = warp_sum(A);
+    Bs = warp_sum(Bs);
+    W = warp_sum(W);
+    st = warp_sum_ff(ff_add(FF{__fsub_rn(acc.h.x, 1.0f), acc.l.x}, FF{0.f, 0.f}));
+    sd = warp_sum_ff(ff_add(FF{__fsub_rn(acc.h.y, 1.0f), acc.l.y}, FF{0.f, 0.f}));
+}
+
+constexpr int kSWarps = 4;   // warps per CTA of the sampler pass
+constexpr int kSStages = 3;  // stages per warp; a stage holds a target and a draft chunk
+
+struct SShared {
+    uint4 buf[kSWarps][kSStages][2 * kChunkBytes / 16];
+    SampInfo info[kSWarps][kSStages];
+    int item_b[kSWarps][kSStages], item_c[kSWarps][kSStages], item_nvec[kSWarps][kSStages];
+    unsigned long long bar[kSWarps][kSStages];
+};
+
+// Items = (sampled request, 4 KiB chunk) over the list sv_decide built; item k
+// of a warp is first + k * total_warps.  Same per-warp ring as sv_pass1.
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kSWarps * 32) sv_sample(Params P) {
+    constexpr int EPV = Fmt<DT>::kEPV;
+    constexpr int ESZ = Fmt<DT>::kESZ;
+    constexpr int CE = chunk_elems<DT>();
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    SShared &sh = *reinterpret_cast<SShared *>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned long long *bar = sh.bar[warp];
+    if (VEC && lane == 0) {
+        for (int s = 0; s < kSStages; ++s) mbar_init(reinterpret_cast<uint64_t *>(&bar[s]), 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    pdl_wait();  // the sampled-request list and SampInfo come from sv_decide
+    pdl_trigger();
+    const uint32_t nitems = (uint32_t)(*P.samp_count) * (uint32_t)P.nchunk;
+    const uint32_t first = blockIdx.x * kSWarps + warp;
+    const uint32_t stride = gridDim.x * kSWarps;
+    const uint32_t nk = nitems > first ? (nitems - first + stride - 1) / stride : 0u;
+    const uint32_t ni = Fmt<DT>::kNegInfWord;
+    const uint4 neg_inf = make_uint4(ni, ni, ni, ni);
+
+    auto item_of = [&](uint32_t k, int &b, uint32_t &c) {
+        const uint32_t item = first + k * stride;
+        const uint32_t li = item / (uint32_t)P.nchunk;
+        c = item - li * (uint32_t)P.nchunk;
+        b = P.samp_list[li];
+    };
+    auto issue = [&](uint32_t k) {
+        if (lane == 0) {
+            int b;
+            uint32_t c;
+            item_of(k, b, c);
+            const SampInfo si = P.samp[b];
+            const int s = (int)(k % kSStages);
+            const uint32_t e0 = c * CE;
+            const uint32_t bytes = min((uint32_t)CE, (uint32_t)P.V - e0) * ESZ;
+            sh.info[warp][s] = si;
+            sh.item_b[warp][s] = b;
+            sh.item_c[warp][s] = (int)c;
+            sh.item_nvec[warp][s] = (int)(bytes / 16);
+            fence_proxy_async();
+            uint64_t *fb = reinterpret_cast<uint64_t *>(&bar[s]);
+            mbar_expect_tx(fb, si.mode == 1 ? 2u * bytes : bytes);
+            bulk_g2s(sh.buf[warp][s], row_ptr(P, b, si.slot_t, ESZ) + (size_t)e0 * ESZ, bytes, fb);
+            if (si.mode == 1)
+                bulk_g2s(sh.buf[warp][s] + kChunkBytes / 16,
+                         row_ptr(P, b, si.slot_d, ESZ) + (size_t)e0 * ESZ, bytes, fb);
+        }
+        __syncwarp();
+    };
+    if (VEC)
+        for (uint32_t k = 0; k < (uint32_t)kSStages && k < nk; ++k) issue(k);
+    uint32_t k = 0;
+    bool failed = false;
+    for (; k < nk; ++k) {
+        uint4 vt[kVecPerLane], vd[kVecPerLane];
+        SampInfo si;
+        int b, c, nvec;
+        if (VEC) {
+            const int s = (int)(k % kSStages);
+            if (!mbar_wait_bounded(reinterpret_cast<uint64_t *>(&bar[s]), (k / kSStages) & 1u,
+                                   kWaitLimitNs)) {
+                failed = true;
+                break;
+            }
+            si = sh.info[warp][s];
+            b = sh.item_b[warp][s];
+            c = sh.item_c[warp][s];
+            nvec = sh.item_nvec[warp][s];
+            const bool resid = si.mode == 1;
+#pragma unroll
+            for (int i = 0; i < kVecPerLane; ++i) {
+                const int q = i * 32 + lane;
+                vt[i] = q < nvec ? sh.buf[warp][s][q] : neg_inf;
+                vd[i] = (resid && q < nvec) ? sh.buf[warp][s][kChunkBytes / 16 + q] : neg_inf;
+            }
+            __syncwarp();
+            if (k + kSStages < nk) issue(k + kSStages);
+        } else {
+            uint32_t cu;
+            item_of(k, b, cu);
+            c = (int)cu;
+            si = P.samp[b];
+            const long long e0 = (long long)c * CE;
+            nvec = (int)((min((long long)CE, (long long)P.V - e0) + EPV - 1) / EPV);
+            const bool resid = si.mode == 1;
+            const char *rowt = row_ptr(P, b, si.slot_t, ESZ);
+            const char *rowd = resid ? row_ptr(P, b, si.slot_d, ESZ) : rowt;
+#pragma unroll
+            for (int i = 0; i < kVecPerLane; ++i) {
+                const long long q = e0 + (long long)(i * 32 + lane) * EPV;
+                vt[i] = load_vec<DT, false>(rowt, q, P.V);
+                vd[i] = resid ? load_vec<DT, false>(rowd, q, P.V) : neg_inf;
+            }
+        }
+        float A, Bs, W;
+        FF st, sd;
+        sample_masses<DT>(vt, vd, nvec, si, A, Bs, W, st, sd, lane);
         if (lane == 0) {
             P.sub[(size_t)b * P.nchunk + c] = make_float4(A, Bs, W, 0.f);
             P.sexact[(size_t)b * P.nchunk + c] = make_float4(st.hi, st.lo, sd.hi, sd.lo);
         }
     }
+    if (VEC && failed) {
+        if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
+        for (uint32_t kk = k; kk < k + kSStages && kk < nk; ++kk)
+            mbar_wait_bounded(reinterpret_cast<uint64_t *>(&bar[kk % kSStages]), (kk / kSStages) & 1u,
+                              kWaitLimitNs);
+    }
 }
 
 // ------------------------------------------------------------------ 5. inverse CDF
 
+constexpr int kFindWarps = 8;  // one warp per sampled request
+
+// Token of one sampled request (one warp): exact normalisers, prefix over the
+// chunk masses (each lane owns a contiguous block of chunks, loaded at once),
+// then the chosen chunk's vectors (loaded at once) scanned in order.
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kThreads) sv_find(Params P) {
+__global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
     constexpr int EPV = Fmt<DT>::kEPV;
     constexpr int ESZ = Fmt<DT>::kESZ;
     constexpr int CE = chunk_elems<DT>();
-    __shared__ double red_d[kWarps];
-    __shared__ double s_tot[4];
-    __shared__ int s_chunk;
-    __shared__ double s_base;
-    __shared__ int s_tok;
-    const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();  // chunk masses come from sv_sample
+    pdl_trigger();
+    const int li = blockIdx.x * kFindWarps + warp;
+    if (li >= *P.samp_count) return;
+    const int b = P.samp_list[li];
     const SampInfo si = P.samp[b];
-    if (si.mode == 0) return;
     const bool resid = si.mode == 1;
     const int nch = P.nchunk;
     const float4 *sub = P.sub + (size_t)b * nch;
     const float4 *sex = P.sexact + (size_t)b * nch;
-    // exact normalisers and residual / target masses
-    double st = 0.0, sd = 0.0, zr = 0.0, zw = 0.0;
-    for (int c = tid; c < nch; c += kThreads) {
-        const float4 e = sex[c];
-        st += (double)e.x + (double)e.y;
-        sd += (double)e.z + (double)e.w;
+    const int per = (nch + 31) / 32;
+    const int c0 = lane * per, c1 = min(nch, c0 + per);
+    float4 q[kPerLane], e[kPerLane];
+    const bool held = per <= kPerLane;
+    double st = 0.0, sd = 0.0;
+    if (held) {
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int c = c0 + i;
+            q[i] = c < c1 ? sub[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+            e[i] = c < c1 ? sex[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            st += (double)e[i].x + (double)e[i].y;
+            sd += (double)e[i].z + (double)e[i].w;
+        }
+    } else {
+        for (int c = c0; c < c1; ++c) {
+            const float4 x = sex[c];
+            st += (double)x.x + (double)x.y;
+            sd += (double)x.z + (double)x.w;
+        }
     }
     st = warp_sum_d(st);
     sd = warp_sum_d(sd);
-    if (lane == 0) { red_d[warp] = st; }
-    __syncthreads();
-    if (tid == 0) { double t = 0; for (int i = 0; i < kWarps; ++i) t += red_d[i]; s_tot[0] = t; }
-    __syncthreads();
-    if (lane == 0) { red_d[warp] = sd; }
-    __syncthreads();
-    if (tid == 0) { double t = 0; for (int i = 0; i < kWarps; ++i) t += red_d[i]; s_tot[1] = t; }
-    __syncthreads();
-    const double kt = resid ? 1.0 / ((double)si.rho_t * s_tot[0]) : 1.0;
-    const double kd = resid ? 1.0 / ((double)si.rho_d * s_tot[1]) : 0.0;
-    // chunk masses: contiguous blocks of chunks per thread
-    const int per = (nch + kThreads - 1) / kThreads;
-    const int c0 = tid * per, c1 = min(nch, c0 + per);
-    for (int c = c0; c < c1; ++c) {
-        const float4 q = sub[c];
-        zr += resid ? fmax(0.0, kt * (double)q.x - kd * (double)q.y) : (double)q.z;
-        zw += (double)q.z;
+    const double kt = resid ? 1.0 / ((double)si.rho_t * st) : 1.0;
+    const double kd = resid ? 1.0 / ((double)si.rho_d * sd) : 0.0;
+    auto mass_r = [&](const float4 &x) {
+        return resid ? fmax(0.0, kt * (double)x.x - kd * (double)x.y) : (double)x.z;
+    };
+    double zr = 0.0, zw = 0.0;
+    if (held) {
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i)
+            if (c0 + i < c1) {
+                zr += mass_r(q[i]);
+                zw += (double)q[i].z;
+            }
+    } else {
+        for (int c = c0; c < c1; ++c) {
+            const float4 x = sub[c];
+            zr += mass_r(x);
+            zw += (double)x.z;
+        }
     }
-    // totals
-    double tr = warp_sum_d(zr), tw = warp_sum_d(zw);
-    __syncthreads();
-    if (lane == 0) red_d[warp] = tr;
-    __syncthreads();
-    if (tid == 0) { double t = 0; for (int i = 0; i < kWarps; ++i) t += red_d[i]; s_tot[2] = t; }
-    __syncthreads();
-    if (lane == 0) red_d[warp] = tw;
-    __syncthreads();
-    if (tid == 0) { double t = 0; for (int i = 0; i < kWarps; ++i) t += red_d[i]; s_tot[3] = t; s_chunk = INT_MAX; s_tok = INT_MAX; }
-    __syncthreads();
-    const bool use_w = !resid || !(s_tot[2] > 0.0);  // bonus, or residual with zero mass
-    const double Z = use_w ? s_tot[3] : s_tot[2];
-    const double theta = si.u * Z;
-    // exclusive prefix of this thread's block
+    const double Zr = warp_sum_d(zr), Zw = warp_sum_d(zw);
+    const bool use_w = !resid || !(Zr > 0.0);  // bonus, or residual with zero mass: sample p
+    const double theta = si.u * (use_w ? Zw : Zr);
     const double mine = use_w ? zw : zr;
     double incl = mine;
 #pragma unroll
@@ -573,101 +783,105 @@ __global__ void __launch_bounds__(kThreads) sv_find(Params P) {
         const double u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
         if (lane >= o) incl += u;
     }
-    __syncthreads();
-    if (lane == 31) red_d[warp] = incl;
-    __syncthreads();
-    double off = 0.0;
-    for (int i = 0; i < warp; ++i) off += red_d[i];
-    double base = off + incl - mine;
-    int my_c = INT_MAX;
+    double base = incl - mine;
+    int my_c = INT_MAX, my_last = -1;
     double my_base = 0.0;
-    if (base <= theta && base + mine > theta) {
-        for (int c = c0; c < c1; ++c) {
-            const float4 q = sub[c];
-            const double v = use_w ? (double)q.z : (resid ? fmax(0.0, kt * (double)q.x - kd * (double)q.y) : (double)q.z);
+    const bool mine_crosses = base <= theta && base + mine > theta;
+    auto visit = [&](int c, const float4 &x) {
+        const double v = use_w ? (double)x.z : mass_r(x);
+        if (v > 0.0) my_last = c;
+        if (mine_crosses && my_c == INT_MAX) {
             if (base + v > theta) {
                 my_c = c;
                 my_base = base;
-                break;
             }
             base += v;
         }
-        if (my_c != INT_MAX) atomicMin(&s_chunk, my_c);
-    }
-    __syncthreads();
-    if (my_c != INT_MAX && my_c == s_chunk) s_base = my_base;
-    __syncthreads();
-    int ch = s_chunk;
-    double th_local;
-    if (ch == INT_MAX) {
-        // rounding left no crossing: the last chunk with positive mass
-        ch = nch - 1;
-        for (int c = nch - 1; c >= 0; --c) {
-            const float4 q = sub[c];
-            const double v = use_w ? (double)q.z : fmax(0.0, kt * (double)q.x - kd * (double)q.y);
-            if (v > 0.0) { ch = c; break; }
-        }
-        th_local = INFINITY;
+    };
+    if (held) {
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i)
+            if (c0 + i < c1) visit(c0 + i, q[i]);
     } else {
-        th_local = theta - s_base;
+        for (int c = c0; c < c1; ++c) visit(c, sub[c]);
     }
-    if (warp == 0) {
-        const char *rowt = row_ptr(P, b, si.slot_t, ESZ);
-        const char *rowd = resid ? row_ptr(P, b, si.slot_d, ESZ) : rowt;
-        const long long e0 = (long long)ch * CE;
-        const uint32_t ni = Fmt<DT>::kNegInfWord;
-        const float2 m2 = make_float2(si.m_t, si.m_d);
-        const float2 chi2 = make_float2(si.c_hi, si.c_hi), clo2 = make_float2(si.c_lo, si.c_lo);
-        const float2 rho2 = make_float2(si.rho_t, si.rho_d);
-        const float dkt = (float)(kt - 1.0), dkd = (float)(kd - 1.0);
-        double run = 0.0;
-        int found = INT_MAX, last_pos = -1;
-        for (int i = 0; i < kVecPerLane && found == INT_MAX; ++i) {
-            const long long q0 = e0 + (long long)(i * 32 + lane) * EPV;
-            const uint4 vt = load_vec<DT, VEC>(rowt, q0, P.V);
-            const uint4 vd = (resid && !use_w) ? load_vec<DT, VEC>(rowd, q0, P.V) : make_uint4(ni, ni, ni, ni);
-            float w[EPV];
+    const int ch_found = warp_min_int(my_c);
+    int ch;
+    double th_local;  // remaining mass inside the chosen chunk
+    if (ch_found != INT_MAX) {
+        ch = ch_found;
+        const int owner = __ffs(__ballot_sync(0xFFFFFFFFu, my_c == ch_found)) - 1;
+        th_local = theta - __shfl_sync(0xFFFFFFFFu, my_base, owner);
+    } else {
+        // rounding left no crossing: the last chunk with positive mass
+        int last = my_last;
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-                float2 ee, ab;
-                pair_weights<DT>(elem<DT>(vt, e), elem<DT>(vd, e), m2, chi2, clo2,
-                                 (resid && !use_w) ? rho2 : make_float2(si.rho_t, 0.f), ee, ab);
-                float wv;
-                if (use_w) wv = ab.x;
-                else wv = ab.x > ab.y ? fmaxf(__fsub_rn(__fmaf_rn(ab.x, dkt, ab.x), __fmaf_rn(ab.y, dkd, ab.y)), 0.f) : 0.f;
-                w[e] = wv;
-                if (wv > 0.f && q0 + e < P.V) last_pos = (int)(q0 + e);
-            }
-            float vs = w[0];
-#pragma unroll
-            for (int e = 1; e < EPV; ++e) vs = __fadd_rn(vs, w[e]);
-            float inc = vs;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float u = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-                if (lane >= o) inc = __fadd_rn(inc, u);
-            }
-            const double lo_edge = run + (double)(inc - vs);
-            int tok = INT_MAX;
-            if (lo_edge <= th_local && lo_edge + (double)vs > th_local) {
-                float ps = 0.f;
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) {
-                    ps = e == 0 ? w[0] : __fadd_rn(ps, w[e]);
-                    if (tok == INT_MAX && lo_edge + (double)ps > th_local) tok = (int)(q0 + e);
-                }
-            }
-            found = warp_min_int(tok);
-            run += (double)__shfl_sync(0xFFFFFFFFu, inc, 31);
-        }
-        if (found == INT_MAX) {
-            int lp = last_pos;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xFFFFFFFFu, lp, o));
-            found = lp >= 0 ? lp : (int)e0;
-        }
-        if (lane == 0) P.out_tokens[(size_t)b * (P.K + 1) + si.a] = found;
+        for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xFFFFFFFFu, last, o));
+        ch = last >= 0 ? last : nch - 1;
+        th_local = INFINITY;
     }
+    const char *rowt = row_ptr(P, b, si.slot_t, ESZ);
+    const char *rowd = resid ? row_ptr(P, b, si.slot_d, ESZ) : rowt;
+    const long long e0 = (long long)ch * CE;
+    const uint32_t ni = Fmt<DT>::kNegInfWord;
+    const bool two = resid && !use_w;
+    uint4 vt[kVecPerLane], vd[kVecPerLane];
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+        const long long q0 = e0 + (long long)(i * 32 + lane) * EPV;
+        vt[i] = load_vec<DT, VEC>(rowt, q0, P.V);
+        vd[i] = two ? load_vec<DT, VEC>(rowd, q0, P.V) : make_uint4(ni, ni, ni, ni);
+    }
+    const float2 m2 = make_float2(si.m_t, si.m_d);
+    const float2 chi2 = make_float2(si.c_hi, si.c_hi), clo2 = make_float2(si.c_lo, si.c_lo);
+    const float2 rho2 = two ? make_float2(si.rho_t, si.rho_d) : make_float2(si.rho_t, 0.f);
+    const float dkt = (float)(kt - 1.0), dkd = (float)(kd - 1.0);
+    double run = 0.0;  // mass of the chunk's earlier vectors
+    int found = INT_MAX, last_pos = -1;
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+        if (found != INT_MAX) break;
+        const long long q0 = e0 + (long long)(i * 32 + lane) * EPV;
+        float w[EPV];
+#pragma unroll
+        for (int k = 0; k < EPV; ++k) {
+            const float2 ee = weight2(make_float2(elem<DT>(vt[i], k), elem<DT>(vd[i], k)), m2, chi2, clo2);
+            const float2 ab = mul2(ee, rho2);
+            float wv;
+            if (use_w) wv = ab.x;
+            else wv = ab.x > ab.y ? fmaxf(__fsub_rn(__fmaf_rn(ab.x, dkt, ab.x), __fmaf_rn(ab.y, dkd, ab.y)), 0.f) : 0.f;
+            w[k] = wv;
+            if (wv > 0.f && q0 + k < P.V) last_pos = (int)(q0 + k);
+        }
+        float vs = w[0];
+#pragma unroll
+        for (int k = 1; k < EPV; ++k) vs = __fadd_rn(vs, w[k]);
+        float inc = vs;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc = __fadd_rn(inc, u);
+        }
+        const double lo_edge = run + (double)__fsub_rn(inc, vs);
+        int tok = INT_MAX;
+        if (lo_edge <= th_local && lo_edge + (double)vs > th_local) {
+            float ps = 0.f;
+#pragma unroll
+            for (int k = 0; k < EPV; ++k) {
+                ps = k == 0 ? w[0] : __fadd_rn(ps, w[k]);
+                if (tok == INT_MAX && lo_edge + (double)ps > th_local) tok = (int)(q0 + k);
+            }
+        }
+        found = warp_min_int(tok);
+        run += (double)__shfl_sync(0xFFFFFFFFu, inc, 31);
+    }
+    if (found == INT_MAX) {
+        int lp = last_pos;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xFFFFFFFFu, lp, o));
+        found = lp >= 0 ? lp : (int)e0;
+    }
+    if (lane == 0) P.out_tokens[(size_t)b * (P.K + 1) + si.a] = found;
 }
 
 // ------------------------------------------------------------------ schedule
@@ -689,7 +903,7 @@ __global__ void sv_schedule(const float *__restrict__ mp, float thr, int B, int 
 // ------------------------------------------------------------------ host side
 
 struct Layout {
-    size_t req, row_count, rows, part, samp, sub, sexact, total;
+    size_t req, row_count, rows, part, samp, sub, sexact, samp_list, samp_count, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -723,6 +937,8 @@ static Layout layout(int B, int K, int V, spec_dtype_t dt) {
     L.samp = off; off = align256(off + sizeof(SampInfo) * (size_t)B);
     L.sub = off; off = align256(off + sizeof(float4) * (size_t)B * nchunk);
     L.sexact = off; off = align256(off + sizeof(float4) * (size_t)B * nchunk);
+    L.samp_list = off; off = align256(off + sizeof(int) * (size_t)B);
+    L.samp_count = off; off = align256(off + sizeof(int));
     L.total = off;
     return L;
 }
@@ -736,19 +952,22 @@ struct DevInfo {
 
 static DevInfo g_dev[64];
 constexpr size_t kP1Smem = sizeof(P1Shared);
+constexpr size_t kSSmem = sizeof(SShared);
 
 template <int DT, bool VEC>
 static bool setup_kernels(DevInfo &d) {
-    const size_t smem = VEC ? kP1Smem : 0;
-    if (VEC && cudaFuncSetAttribute(sv_pass1<DT, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem) != cudaSuccess)
+    const size_t smem1 = VEC ? kP1Smem : 0, smem2 = VEC ? kSSmem : 0;
+    if (VEC && (cudaFuncSetAttribute(sv_pass1<DT, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem1) != cudaSuccess ||
+                cudaFuncSetAttribute(sv_sample<DT, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem2) != cudaSuccess))
         return false;
     int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sv_pass1<DT, VEC>, kP1Warps * 32, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sv_pass1<DT, VEC>, kP1Warps * 32, smem1) !=
         cudaSuccess)
         return false;
     d.occ_p1[DT][VEC] = o > 0 ? o : 1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sv_sample<DT, VEC>, kThreads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sv_sample<DT, VEC>, kSWarps * 32, smem2) !=
         cudaSuccess)
         return false;
     d.occ_sample[DT][VEC] = o > 0 ? o : 1;
@@ -775,20 +994,43 @@ static const DevInfo *dev_info() {
 static cudaEvent_t g_prof_start = nullptr, g_prof_end = nullptr;
 constexpr int kKernelsPerVerify = 5;
 
+// Launch that may begin while the previous kernel of the stream is still
+// running (programmatic dependent launch): the kernel does its independent
+// set-up, then griddepcontrol.wait blocks until the previous kernel has
+// completed and its writes are visible.
+static void launch_dependent(void (*kernel)(Params), int grid, int block, size_t smem,
+                             cudaStream_t s, const Params &P) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, P);
+}
+
 template <int DT, bool VEC>
 static void launch_all(const Params &P, const DevInfo &d, cudaStream_t s) {
+    // sv_prep is an ordinary launch: it starts only after all earlier work of
+    // the stream, so the workspace of a previous call is free again.
     sv_prep<<<1, kPrepThreads, 0, s>>>(P);
-    const int g1 = d.sms * d.occ_p1[DT][VEC];
     if (g_prof_start) cudaEventRecord(g_prof_start, s);
-    sv_pass1<DT, VEC><<<g1, kP1Warps * 32, VEC ? kP1Smem : 0, s>>>(P);
+    launch_dependent(sv_pass1<DT, VEC>, d.sms * d.occ_p1[DT][VEC], kP1Warps * 32,
+                     VEC ? kP1Smem : 0, s, P);
     if (g_prof_end) cudaEventRecord(g_prof_end, s);
-    sv_decide<DT><<<P.B, kThreads, 0, s>>>(P);
-    const long long warps_needed = (long long)P.B * P.nchunk;
+    launch_dependent(sv_decide<DT>, P.B, kThreads, 0, s, P);
+    // the sampled requests are known only on the device: enough warps for all
+    // of them, at most one full wave
     long long g2 = (long long)d.sms * d.occ_sample[DT][VEC];
-    const long long g2_need = (warps_needed + kWarps - 1) / kWarps;
+    const long long g2_need = ((long long)P.B * P.nchunk + kSWarps - 1) / kSWarps;
     if (g2 > g2_need) g2 = g2_need;
-    sv_sample<DT, VEC><<<(int)g2, kThreads, 0, s>>>(P);
-    sv_find<DT, VEC><<<P.B, kThreads, 0, s>>>(P);
+    launch_dependent(sv_sample<DT, VEC>, (int)g2, kSWarps * 32, VEC ? kSSmem : 0, s, P);
+    launch_dependent(sv_find<DT, VEC>, (P.B + kFindWarps - 1) / kFindWarps, kFindWarps * 32, 0, s,
+                     P);
 }
 
 static spec_status_t verify_impl(const void *target_logits, const void *draft_logits,
@@ -838,6 +1080,8 @@ static spec_status_t verify_impl(const void *target_logits, const void *draft_lo
     P.samp = reinterpret_cast<SampInfo *>(ws + L.samp);
     P.sub = reinterpret_cast<float4 *>(ws + L.sub);
     P.sexact = reinterpret_cast<float4 *>(ws + L.sexact);
+    P.samp_list = reinterpret_cast<int *>(ws + L.samp_list);
+    P.samp_count = reinterpret_cast<int *>(ws + L.samp_count);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == SPEC_DTYPE_BF16) {
         if (vec) launch_all<kBF16, true>(P, *d, s);

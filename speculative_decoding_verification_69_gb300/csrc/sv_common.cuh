@@ -356,6 +356,47 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
+// ------------------------------------------------------------------ packed helpers
+
+__device__ __forceinline__ void mbar_arrive(unsigned long long *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// acc += (2^((lo(w) - m) c), 2^((hi(w) - m) c)) for the two bfloat16 of w.
+__device__ __forceinline__ void bf16x2_exp_acc(uint32_t w, unsigned long long m2,
+                                               unsigned long long c2, unsigned long long &acc) {
+    asm("{\n\t.reg .b32 a, b;\n\t.reg .b64 z;\n\t"
+        "shl.b32 a, %1, 16;\n\tand.b32 b, %1, 0xFFFF0000;\n\tmov.b64 z, {a, b};\n\t"
+        "sub.rn.f32x2 z, z, %2;\n\tmul.rn.f32x2 z, z, %3;\n\t"
+        "mov.b64 {a, b}, z;\n\tex2.approx.ftz.f32 a, a;\n\tex2.approx.ftz.f32 b, b;\n\t"
+        "mov.b64 z, {a, b};\n\tadd.rn.f32x2 %0, %0, z;\n\t}"
+        : "+l"(acc)
+        : "r"(w), "l"(m2), "l"(c2));
+}
+
+// Same for two float32 logits.
+__device__ __forceinline__ void f32x2_exp_acc(uint32_t w0, uint32_t w1, unsigned long long m2,
+                                              unsigned long long c2, unsigned long long &acc) {
+    asm("{\n\t.reg .b32 a, b;\n\t.reg .b64 z;\n\t"
+        "mov.b64 z, {%1, %2};\n\t"
+        "sub.rn.f32x2 z, z, %3;\n\tmul.rn.f32x2 z, z, %4;\n\t"
+        "mov.b64 {a, b}, z;\n\tex2.approx.ftz.f32 a, a;\n\tex2.approx.ftz.f32 b, b;\n\t"
+        "mov.b64 z, {a, b};\n\tadd.rn.f32x2 %0, %0, z;\n\t}"
+        : "+l"(acc)
+        : "r"(w0), "r"(w1), "l"(m2), "l"(c2));
+}
+
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Programmatic dependent launch: wait for the previous kernel's results /
+// allow the next kernel to be scheduled.  No-ops without the launch attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // ------------------------------------------------------------------ Philox4x32-10
 
 // Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, SC'11): each round
