@@ -34,16 +34,17 @@
 namespace sv {
 
 constexpr double kLog2E = 1.4426950408889634074;
+constexpr float kLog2EHi = 0x1.715476p+0f;   // log2(e) rounded to float
+constexpr float kLog2ELo = 0x1.4ae0c0p-26f;  // log2(e) - kLog2EHi (to ~1e-16)
+constexpr float kLn2F = 0.693147182f;
 
 struct ReqInfo {
     int L;        // effective verify length
     int greedy;   // 1: temperature 0 path
-    float c;      // log2(e)/T rounded to float (statistics pass)
-    float c_hi;   // two-float log2(e)/T, c_hi rounded toward zero (sampler)
+    float c;      // log2(e)/T as a float (statistics pass)
+    float c_hi;   // two-float log2(e)/T, c_hi rounded toward zero (sampler, acceptance)
     float c_lo;   // >= FLT_MIN
-    float pad;
-    double cd;    // log2(e)/T in double
-    double inv_t; // 1/T in double
+    float T;      // temperature as given
 };
 
 struct SampInfo {
@@ -138,20 +139,24 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
             ReqInfo ri;
             ri.L = L;
             ri.greedy = greedy;
+            ri.T = T;
             if (!greedy) {
-                double c = kLog2E / (double)T;
-                float chi = __double2float_rz(c);
-                float clo = __double2float_rn(c - (double)chi);
-                if (!(clo >= FLT_MIN)) clo = FLT_MIN;
-                ri.c = __double2float_rn(c);
+                // log2(e)/T as q + ql: q = fl(hi/T), its exact remainder, then the low part
+                const float q = __fdiv_rn(kLog2EHi, T);
+                const float rem = __fmaf_rn(-q, T, kLog2EHi);
+                float ql = __fdiv_rn(__fadd_rn(rem, kLog2ELo), T);
+                float chi = q;
+                if (ql < 0.f) {  // keep the high part at or below the value, the low part positive
+                    chi = __int_as_float(__float_as_int(q) - 1);
+                    ql = __fadd_rn(ql, __fsub_rn(q, chi));
+                }
+                if (!(ql >= FLT_MIN)) ql = FLT_MIN;
+                ri.c = q;
                 ri.c_hi = chi;
-                ri.c_lo = clo;
-                ri.cd = c;
-                ri.inv_t = 1.0 / (double)T;
+                ri.c_lo = ql;
             } else {
-                ri.c = 0.f; ri.c_hi = 0.f; ri.c_lo = 0.f; ri.cd = 0.0; ri.inv_t = 0.0;
+                ri.c = 0.f; ri.c_hi = 0.f; ri.c_lo = 0.f;
             }
-            ri.pad = 0.f;
             P.req[b] = ri;
             cval = ri.c;
             if (st && P.dev_status) atomicOr(P.dev_status, st);
@@ -385,10 +390,44 @@ __global__ void __launch_bounds__(kP1Warps * 32) sv_pass1(Params P) {
 
 // ------------------------------------------------------------------ 3. decide
 
-constexpr int kPerLane = 4;  // chunk records held in registers per lane (128 per warp)
+constexpr int kPerLane = 4;      // chunk records held in registers per lane (128 per warp)
+constexpr int kRowsPerWarp = 3;  // rows whose chunk records one warp loads at once
 
-// Row statistics from its chunk partials (one warp; loads issued up front):
-// {max, S (sampled rows), lowest argmax bits (greedy rows), -}.
+// Row statistics from one block of up to 32 * kPerLane chunk records held by
+// the warp: {max, S (sampled rows), lowest argmax bits (greedy rows)}.
+__device__ __forceinline__ void reduce_block(const float4 (&q)[kPerLane], bool greedy, float c,
+                                             float &m, float &S, int &amax) {
+    float mr = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) mr = fmaxf(mr, q[i].x);
+    mr = warp_max(mr);
+    if (greedy) {
+        int ar = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i)
+            if (q[i].x == mr) ar = min(ar, __float_as_int(q[i].z));
+        ar = warp_min_int(ar);
+        if (mr > m || (mr == m && ar < amax)) amax = ar;
+        m = fmaxf(m, mr);
+    } else {
+        const float mn = fmaxf(m, mr);
+        float Sr = 0.f;
+        if (mn > -INFINITY) {
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i)
+                if (q[i].x > -INFINITY) Sr += q[i].y * ex2((q[i].x - mn) * c);
+            if (m > -INFINITY) S *= ex2((m - mn) * c);
+        }
+        S += warp_sum(Sr);
+        m = mn;
+    }
+}
+
+__device__ __forceinline__ float4 part_filler() {
+    return make_float4(-INFINITY, 0.f, __int_as_float(INT_MAX), 0.f);
+}
+
+// Row statistics of any chunk count (one warp, blocks of 32 * kPerLane).
 __device__ __forceinline__ float4 combine_row(const Params &P, int b, int slot, bool greedy,
                                               float c, int lane) {
     const float4 *pp = P.part + ((size_t)b * P.nslot + slot) * P.nchunk;
@@ -400,35 +439,34 @@ __device__ __forceinline__ float4 combine_row(const Params &P, int b, int slot, 
 #pragma unroll
         for (int i = 0; i < kPerLane; ++i) {
             const int ci = base + i * 32 + lane;
-            q[i] = ci < n ? pp[ci] : make_float4(-INFINITY, 0.f, __int_as_float(INT_MAX), 0.f);
+            q[i] = ci < n ? pp[ci] : part_filler();
         }
-        float mr = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i) mr = fmaxf(mr, q[i].x);
-        mr = warp_max(mr);
-        if (greedy) {
-            int ar = INT_MAX;
-#pragma unroll
-            for (int i = 0; i < kPerLane; ++i)
-                if (q[i].x == mr) ar = min(ar, __float_as_int(q[i].z));
-            ar = warp_min_int(ar);
-            if (mr > m || (mr == m && ar < amax)) amax = ar;
-            m = fmaxf(m, mr);
-        } else {
-            const float mn = fmaxf(m, mr);
-            float Sr = 0.f;
-            if (mn > -INFINITY) {
-#pragma unroll
-                for (int i = 0; i < kPerLane; ++i)
-                    if (q[i].x > -INFINITY) Sr += q[i].y * ex2((q[i].x - mn) * c);
-                if (m > -INFINITY) S *= ex2((m - mn) * c);
-            }
-            S += warp_sum(Sr);
-            m = mn;
-        }
+        reduce_block(q, greedy, c, m, S, amax);
     }
-    if (greedy) return make_float4(m, 0.f, __int_as_float(amax), 0.f);
-    return make_float4(m, S, __int_as_float(-1), 0.f);
+    return make_float4(m, S, __int_as_float(amax), 0.f);
+}
+
+__device__ __forceinline__ int slot_of_row(int r, int L, int K) {
+    return r <= L ? r : K + 1 + (r - L - 1);
+}
+
+// Acceptance test u * q(x) < p(x) of one position, as u < p/q with
+// p/q = 2^(((g - m) - (g' - m')) c) * S'/S; the exponent is formed in
+// two-float arithmetic so that the ratio carries only the float error of the
+// row sums and of ex2.
+__device__ __forceinline__ bool accept_position(float u, float g, float m_t, float S_t, float gd,
+                                                float m_d, float S_d, float c_hi, float c_lo) {
+    if (!(S_t > 0.f) || g == -INFINITY) return false;  // p = 0
+    if (!(S_d > 0.f) || gd == -INFINITY) return true;   // q = 0 < p
+    if (u == 0.f) return true;                          // 0 < p
+    const FF dt = two_sum(g, -m_t), dd = two_sum(gd, -m_d);
+    const FF D = ff_add(dt, FF{-dd.hi, -dd.lo});
+    const float th = __fmul_rn(D.hi, c_hi);
+    if (th > 128.f) return true;    // ratio above 2^127 > u
+    if (th < -160.f) return false;  // ratio below 2^-159 < 2^-24 <= u
+    const float tl = __fadd_rn(__fmaf_rn(D.hi, c_hi, -th), __fmaf_rn(D.hi, c_lo, __fmul_rn(D.lo, c_hi)));
+    const float r = __fmul_rn(__fmul_rn(ex2(th), __fmaf_rn(tl, kLn2F, 1.f)), __fdiv_rn(S_d, S_t));
+    return u < r;
 }
 
 template <int DT>
@@ -444,44 +482,80 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
     const int L = rq.L;
     const bool greedy = rq.greedy != 0;
     int x = 0;
-    float g = 0.f, gd = 0.f;
+    float g = 0.f, gd = 0.f, u = 0.f;
     if (warp == 0 && lane < L) {
         x = P.tokens[(size_t)b * K + lane];
         if (!greedy) {
             g = load_logit(row_ptr(P, b, lane, Fmt<DT>::kESZ), DT, x);
             gd = load_logit(row_ptr(P, b, K + 1 + lane, Fmt<DT>::kESZ), DT, x);
+            u = uniform_accept_f(P.seed, (uint32_t)b, (uint32_t)lane);
         }
     }
     pdl_wait();  // chunk partials come from sv_pass1
     pdl_trigger();
     const int nrows = greedy ? L + 1 : 2 * L + 1;
-    for (int r = warp; r < nrows; r += kWarps) {
-        const int slot = r <= L ? r : K + 1 + (r - L - 1);
-        const float4 rs = combine_row(P, b, slot, greedy, rq.c, lane);
-        if (lane == 0) {
-            s_m[slot] = rs.x;
-            s_S[slot] = rs.y;
-            if (slot <= K) s_amax[slot] = __float_as_int(rs.z);
+    if (P.nchunk <= 32 * kPerLane) {
+        // each warp loads the records of up to kRowsPerWarp rows, then reduces them
+        for (int r0 = warp; r0 < nrows; r0 += kWarps * kRowsPerWarp) {
+            float4 q[kRowsPerWarp][kPerLane];
+#pragma unroll
+            for (int j = 0; j < kRowsPerWarp; ++j) {
+                const int r = r0 + j * kWarps;
+                const float4 *pp =
+                    P.part + ((size_t)b * P.nslot + slot_of_row(r < nrows ? r : 0, L, K)) * P.nchunk;
+#pragma unroll
+                for (int i = 0; i < kPerLane; ++i) {
+                    const int ci = i * 32 + lane;
+                    q[j][i] = (r < nrows && ci < P.nchunk) ? pp[ci] : part_filler();
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kRowsPerWarp; ++j) {
+                const int r = r0 + j * kWarps;
+                if (r < nrows) {
+                    float m = -INFINITY, S = 0.f;
+                    int amax = INT_MAX;
+                    reduce_block(q[j], greedy, rq.c, m, S, amax);
+                    const int slot = slot_of_row(r, L, K);
+                    if (lane == 0) {
+                        s_m[slot] = m;
+                        s_S[slot] = S;
+                        if (slot <= K) s_amax[slot] = amax;
+                    }
+                }
+            }
+        }
+    } else {
+        for (int r = warp; r < nrows; r += kWarps) {
+            const int slot = slot_of_row(r, L, K);
+            const float4 rs = combine_row(P, b, slot, greedy, rq.c, lane);
+            if (lane == 0) {
+                s_m[slot] = rs.x;
+                s_S[slot] = rs.y;
+                if (slot <= K) s_amax[slot] = __float_as_int(rs.z);
+            }
         }
     }
     __syncthreads();
     if (warp == 0) {
         bool acc = true;
-        double p = NAN, q = NAN;
         if (lane < L) {
-            if (greedy) {
+            if (greedy)
                 acc = (x == s_amax[lane]);
-            } else {
-                const float St = s_S[lane], Sd = s_S[K + 1 + lane];
-                p = St > 0.f ? exp2(((double)g - (double)s_m[lane]) * rq.cd) / (double)St : 0.0;
-                q = Sd > 0.f ? exp2(((double)gd - (double)s_m[K + 1 + lane]) * rq.cd) / (double)Sd : 0.0;
-                const double u = uniform_accept(P.seed, (uint32_t)b, (uint32_t)lane);
-                acc = u * q < p;
-            }
+            else
+                acc = accept_position(u, g, s_m[lane], s_S[lane], gd, s_m[K + 1 + lane],
+                                      s_S[K + 1 + lane], rq.c_hi, rq.c_lo);
         }
         if (P.dbg_probs && lane < K) {
-            P.dbg_probs[((size_t)b * K + lane) * 2 + 0] = (!greedy && lane < L) ? p : NAN;
-            P.dbg_probs[((size_t)b * K + lane) * 2 + 1] = (!greedy && lane < L) ? q : NAN;
+            double p = NAN, q = NAN;
+            if (!greedy && lane < L) {
+                const double cd = kLog2E / (double)rq.T;
+                const float St = s_S[lane], Sd = s_S[K + 1 + lane];
+                p = St > 0.f ? exp2(((double)g - (double)s_m[lane]) * cd) / (double)St : 0.0;
+                q = Sd > 0.f ? exp2(((double)gd - (double)s_m[K + 1 + lane]) * cd) / (double)Sd : 0.0;
+            }
+            P.dbg_probs[((size_t)b * K + lane) * 2 + 0] = p;
+            P.dbg_probs[((size_t)b * K + lane) * 2 + 1] = q;
         }
         const unsigned rej = ~__ballot_sync(0xFFFFFFFFu, acc);
         const int a = rej ? min(__ffs(rej) - 1, L) : L;
@@ -509,9 +583,9 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
             si.m_d = 0.f;
             si.rho_d = 0.f;
             if (si.mode == 1) {
-                si.rho_t = 1.f / s_S[a];
+                si.rho_t = __frcp_rn(s_S[a]);
                 si.m_d = s_m[K + 1 + a];
-                si.rho_d = 1.f / s_S[K + 1 + a];
+                si.rho_d = __frcp_rn(s_S[K + 1 + a]);
             }
             si.c_hi = rq.c_hi;
             si.c_lo = rq.c_lo;
@@ -527,7 +601,7 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
         for (int sl = tid; sl < nslot; sl += kThreads) {
             double m = NAN, ls = NAN;
             if (!greedy && (sl <= L || (sl >= K + 1 && sl - K - 1 < L))) {
-                m = (double)s_m[sl] * rq.inv_t;
+                m = (double)s_m[sl] / (double)rq.T;
                 ls = log((double)s_S[sl]);
             }
             P.dbg_rows[((size_t)b * nslot + sl) * 2 + 0] = m;
@@ -541,21 +615,23 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
 // Masses of one 4 KiB chunk of the sampled row (pair).  Per element pair
 // (target z, draft z'): e = 2^((z - m) c), e' = 2^((z' - m') c) with the row
 // maxima and the two-float c; a = e * rho, b = e' * rho' with rho = 1/S from
-// the statistics pass.  A = sum of a over {a > b}, B = sum of b over {a > b},
-// W = sum of a, and the exact sums of e and e' (Fast2Sum).  The residual mass
-// of a chunk is then kappa A - kappa' B, kappa = 1 / (rho * sum e).
+// the statistics pass.  Over {a > b}: D = sum of (a - b) and Bm = sum of b;
+// and the exact sums of e and e' (Fast2Sum).  With kappa = 1 / (rho * sum e)
+// = 1 + delta, the chunk's residual mass is
+//   kappa A - kappa' Bm = D + delta (D + Bm) - delta' Bm,   A = D + Bm;
+// the bonus draw (from p) uses the exact sums of e.
 template <int DT>
 __device__ __forceinline__ void sample_masses(const uint4 (&vt)[kVecPerLane],
                                               const uint4 (&vd)[kVecPerLane], int nvec,
-                                              const SampInfo &si, float &A, float &Bs, float &W,
-                                              FF &st, FF &sd, int lane) {
+                                              const SampInfo &si, float &D, float &Bm, FF &st,
+                                              FF &sd, int lane) {
     constexpr int EPV = Fmt<DT>::kEPV;
     const float2 m2 = make_float2(si.m_t, si.m_d);
     const float2 chi2 = make_float2(si.c_hi, si.c_hi), clo2 = make_float2(si.c_lo, si.c_lo);
     const float2 rho2 = make_float2(si.rho_t, si.rho_d);
     BiasAcc2 acc;
     acc.init(1.0f);
-    A = 0.f; Bs = 0.f; W = 0.f;
+    D = 0.f; Bm = 0.f;
 #pragma unroll
     for (int i = 0; i < kVecPerLane; ++i) {
         if (i * 32 + lane < nvec) {
@@ -564,23 +640,21 @@ __device__ __forceinline__ void sample_masses(const uint4 (&vt)[kVecPerLane],
                 const float2 ee = weight2(make_float2(elem<DT>(vt[i], e), elem<DT>(vd[i], e)), m2, chi2, clo2);
                 const float2 ab = mul2(ee, rho2);
                 acc.add(ee);
-                W = __fadd_rn(W, ab.x);
                 if (ab.x > ab.y) {
-                    A = __fadd_rn(A, ab.x);
-                    Bs = __fadd_rn(Bs, ab.y);
+                    D = __fadd_rn(D, __fsub_rn(ab.x, ab.y));
+                    Bm = __fadd_rn(Bm, ab.y);
                 }
             }
         }
     }
-    A = warp_sum(A);
-    Bs = warp_sum(Bs);
-    W = warp_sum(W);
+    D = warp_sum(D);
+    Bm = warp_sum(Bm);
     st = warp_sum_ff(ff_add(FF{__fsub_rn(acc.h.x, 1.0f), acc.l.x}, FF{0.f, 0.f}));
     sd = warp_sum_ff(ff_add(FF{__fsub_rn(acc.h.y, 1.0f), acc.l.y}, FF{0.f, 0.f}));
 }
 
 constexpr int kSWarps = 4;   // warps per CTA of the sampler pass
-constexpr int kSStages = 3;  // stages per warp; a stage holds a target and a draft chunk
+constexpr int kSStages = 2;  // stages per warp; a stage holds a target and a draft chunk
 
 struct SShared {
     uint4 buf[kSWarps][kSStages][2 * kChunkBytes / 16];
@@ -589,8 +663,10 @@ struct SShared {
     unsigned long long bar[kSWarps][kSStages];
 };
 
-// Items = (sampled request, 4 KiB chunk) over the list sv_decide built; item k
-// of a warp is first + k * total_warps.  Same per-warp ring as sv_pass1.
+// Items = (sampled request, 4 KiB chunk) over the list sv_decide built, in
+// request-major order; warp w takes the contiguous range
+// [w n / W, (w + 1) n / W), so it changes request (and reloads the request's
+// SampInfo) at most a few times.  Same per-warp ring as sv_pass1.
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kSWarps * 32) sv_sample(Params P) {
     constexpr int EPV = Fmt<DT>::kEPV;
@@ -607,39 +683,46 @@ __global__ void __launch_bounds__(kSWarps * 32) sv_sample(Params P) {
     __syncwarp();
     pdl_wait();  // the sampled-request list and SampInfo come from sv_decide
     pdl_trigger();
-    const uint32_t nitems = (uint32_t)(*P.samp_count) * (uint32_t)P.nchunk;
-    const uint32_t first = blockIdx.x * kSWarps + warp;
-    const uint32_t stride = gridDim.x * kSWarps;
-    const uint32_t nk = nitems > first ? (nitems - first + stride - 1) / stride : 0u;
+    const uint64_t nitems = (uint64_t)(*P.samp_count) * (uint64_t)P.nchunk;
+    const uint64_t nw = (uint64_t)gridDim.x * kSWarps;
+    const uint64_t gw = (uint64_t)blockIdx.x * kSWarps + warp;
+    const uint32_t k_begin = (uint32_t)(nitems * gw / nw);
+    const uint32_t nk = (uint32_t)(nitems * (gw + 1) / nw) - k_begin;
     const uint32_t ni = Fmt<DT>::kNegInfWord;
     const uint4 neg_inf = make_uint4(ni, ni, ni, ni);
 
-    auto item_of = [&](uint32_t k, int &b, uint32_t &c) {
-        const uint32_t item = first + k * stride;
-        const uint32_t li = item / (uint32_t)P.nchunk;
-        c = item - li * (uint32_t)P.nchunk;
-        b = P.samp_list[li];
+    // request metadata of the current item (lane 0 only uses these in the ring)
+    int cur_li = -1, cur_b = 0;
+    SampInfo cur_si;
+    auto item_of = [&](uint32_t k, uint32_t &c) {
+        const uint32_t item = k_begin + k;
+        const int li = (int)(item / (uint32_t)P.nchunk);
+        c = item - (uint32_t)li * (uint32_t)P.nchunk;
+        if (li != cur_li) {
+            cur_li = li;
+            cur_b = P.samp_list[li];
+            cur_si = P.samp[cur_b];
+        }
     };
     auto issue = [&](uint32_t k) {
         if (lane == 0) {
-            int b;
             uint32_t c;
-            item_of(k, b, c);
-            const SampInfo si = P.samp[b];
+            item_of(k, c);
             const int s = (int)(k % kSStages);
             const uint32_t e0 = c * CE;
             const uint32_t bytes = min((uint32_t)CE, (uint32_t)P.V - e0) * ESZ;
-            sh.info[warp][s] = si;
-            sh.item_b[warp][s] = b;
+            sh.info[warp][s] = cur_si;
+            sh.item_b[warp][s] = cur_b;
             sh.item_c[warp][s] = (int)c;
             sh.item_nvec[warp][s] = (int)(bytes / 16);
             fence_proxy_async();
             uint64_t *fb = reinterpret_cast<uint64_t *>(&bar[s]);
-            mbar_expect_tx(fb, si.mode == 1 ? 2u * bytes : bytes);
-            bulk_g2s(sh.buf[warp][s], row_ptr(P, b, si.slot_t, ESZ) + (size_t)e0 * ESZ, bytes, fb);
-            if (si.mode == 1)
+            const bool two = cur_si.mode == 1;
+            mbar_expect_tx(fb, two ? 2u * bytes : bytes);
+            bulk_g2s(sh.buf[warp][s], row_ptr(P, cur_b, cur_si.slot_t, ESZ) + (size_t)e0 * ESZ, bytes, fb);
+            if (two)
                 bulk_g2s(sh.buf[warp][s] + kChunkBytes / 16,
-                         row_ptr(P, b, si.slot_d, ESZ) + (size_t)e0 * ESZ, bytes, fb);
+                         row_ptr(P, cur_b, cur_si.slot_d, ESZ) + (size_t)e0 * ESZ, bytes, fb);
         }
         __syncwarp();
     };
@@ -673,9 +756,10 @@ __global__ void __launch_bounds__(kSWarps * 32) sv_sample(Params P) {
             if (k + kSStages < nk) issue(k + kSStages);
         } else {
             uint32_t cu;
-            item_of(k, b, cu);
+            item_of(k, cu);  // every lane keeps its own copy here
             c = (int)cu;
-            si = P.samp[b];
+            b = cur_b;
+            si = cur_si;
             const long long e0 = (long long)c * CE;
             nvec = (int)((min((long long)CE, (long long)P.V - e0) + EPV - 1) / EPV);
             const bool resid = si.mode == 1;
@@ -688,11 +772,11 @@ __global__ void __launch_bounds__(kSWarps * 32) sv_sample(Params P) {
                 vd[i] = resid ? load_vec<DT, false>(rowd, q, P.V) : neg_inf;
             }
         }
-        float A, Bs, W;
+        float Dm, Bm;
         FF st, sd;
-        sample_masses<DT>(vt, vd, nvec, si, A, Bs, W, st, sd, lane);
+        sample_masses<DT>(vt, vd, nvec, si, Dm, Bm, st, sd, lane);
         if (lane == 0) {
-            P.sub[(size_t)b * P.nchunk + c] = make_float4(A, Bs, W, 0.f);
+            P.sub[(size_t)b * P.nchunk + c] = make_float4(Dm, Bm, 0.f, 0.f);
             P.sexact[(size_t)b * P.nchunk + c] = make_float4(st.hi, st.lo, sd.hi, sd.lo);
         }
     }
@@ -708,9 +792,17 @@ __global__ void __launch_bounds__(kSWarps * 32) sv_sample(Params P) {
 
 constexpr int kFindWarps = 8;  // one warp per sampled request
 
-// Token of one sampled request (one warp): exact normalisers, prefix over the
-// chunk masses (each lane owns a contiguous block of chunks, loaded at once),
-// then the chosen chunk's vectors (loaded at once) scanned in order.
+// kappa - 1 for kappa = 1 / (rho * S), S a two-float sum close to 1/rho.
+__device__ __forceinline__ float kappa_minus_one(float rho, FF S) {
+    const float xh = __fmul_rn(rho, S.hi);
+    const float xl = __fmaf_rn(rho, S.lo, __fmaf_rn(rho, S.hi, -xh));
+    return __fdiv_rn(__fsub_rn(__fsub_rn(1.f, xh), xl), xh);
+}
+
+// Token of one sampled request (one warp), in float and two-float arithmetic
+// (fp64 has a long dependent latency on this part): exact normalisers, chunk
+// masses, a two-float prefix over the lanes (each lane owns a contiguous block
+// of chunks), then the chosen chunk's vectors scanned in order.
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
     constexpr int EPV = Fmt<DT>::kEPV;
@@ -729,9 +821,9 @@ __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
     const float4 *sex = P.sexact + (size_t)b * nch;
     const int per = (nch + 31) / 32;
     const int c0 = lane * per, c1 = min(nch, c0 + per);
-    float4 q[kPerLane], e[kPerLane];
     const bool held = per <= kPerLane;
-    double st = 0.0, sd = 0.0;
+    float4 q[kPerLane], e[kPerLane];
+    FF st{0.f, 0.f}, sd{0.f, 0.f};
     if (held) {
 #pragma unroll
         for (int i = 0; i < kPerLane; ++i) {
@@ -741,77 +833,81 @@ __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
         }
 #pragma unroll
         for (int i = 0; i < kPerLane; ++i) {
-            st += (double)e[i].x + (double)e[i].y;
-            sd += (double)e[i].z + (double)e[i].w;
+            st = ff_add(st, FF{e[i].x, e[i].y});
+            sd = ff_add(sd, FF{e[i].z, e[i].w});
         }
     } else {
         for (int c = c0; c < c1; ++c) {
             const float4 x = sex[c];
-            st += (double)x.x + (double)x.y;
-            sd += (double)x.z + (double)x.w;
+            st = ff_add(st, FF{x.x, x.y});
+            sd = ff_add(sd, FF{x.z, x.w});
         }
     }
-    st = warp_sum_d(st);
-    sd = warp_sum_d(sd);
-    const double kt = resid ? 1.0 / ((double)si.rho_t * st) : 1.0;
-    const double kd = resid ? 1.0 / ((double)si.rho_d * sd) : 0.0;
+    st = warp_sum_ff(st);
+    const float dlt = resid ? kappa_minus_one(si.rho_t, st) : 0.f;
+    float dld = 0.f;
+    if (resid) dld = kappa_minus_one(si.rho_d, warp_sum_ff(sd));
+    // residual mass D + delta (D + Bm) - delta' Bm; mass of p: rho * (exact sum of e)
     auto mass_r = [&](const float4 &x) {
-        return resid ? fmax(0.0, kt * (double)x.x - kd * (double)x.y) : (double)x.z;
+        return fmaxf(0.f, __fadd_rn(x.x, __fmaf_rn(dlt, __fadd_rn(x.x, x.y), -__fmul_rn(dld, x.y))));
     };
-    double zr = 0.0, zw = 0.0;
+    auto mass_w = [&](const float4 &y) { return __fmaf_rn(si.rho_t, y.x, __fmul_rn(si.rho_t, y.y)); };
+    float zr = 0.f, zw = 0.f;
     if (held) {
 #pragma unroll
         for (int i = 0; i < kPerLane; ++i)
             if (c0 + i < c1) {
-                zr += mass_r(q[i]);
-                zw += (double)q[i].z;
+                if (resid) zr = __fadd_rn(zr, mass_r(q[i]));
+                zw = __fadd_rn(zw, mass_w(e[i]));
             }
     } else {
         for (int c = c0; c < c1; ++c) {
-            const float4 x = sub[c];
-            zr += mass_r(x);
-            zw += (double)x.z;
+            if (resid) zr = __fadd_rn(zr, mass_r(sub[c]));
+            zw = __fadd_rn(zw, mass_w(sex[c]));
         }
     }
-    const double Zr = warp_sum_d(zr), Zw = warp_sum_d(zw);
-    const bool use_w = !resid || !(Zr > 0.0);  // bonus, or residual with zero mass: sample p
-    const double theta = si.u * (use_w ? Zw : Zr);
-    const double mine = use_w ? zw : zr;
-    double incl = mine;
+    const bool use_w = !resid || !(warp_sum(zr) > 0.f);  // bonus, or no residual mass: sample p
+    const float mine = use_w ? zw : zr;
+    // two-float inclusive prefix over the lanes, then theta = u * Z
+    FF incl{mine, 0.f};
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const double u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += u;
+        const FF t{__shfl_up_sync(0xFFFFFFFFu, incl.hi, o), __shfl_up_sync(0xFFFFFFFFu, incl.lo, o)};
+        if (lane >= o) incl = ff_add(incl, t);
     }
-    double base = incl - mine;
+    const FF Z{__shfl_sync(0xFFFFFFFFu, incl.hi, 31), __shfl_sync(0xFFFFFFFFu, incl.lo, 31)};
+    const double theta = si.u * ((double)Z.hi + (double)Z.lo);
+    // remaining mass at the start of this lane's block
+    const FF excl = ff_add(incl, FF{-mine, 0.f});
+    float rem = (float)(theta - ((double)excl.hi + (double)excl.lo));
+    const bool mine_crosses = rem >= 0.f && rem < mine;
     int my_c = INT_MAX, my_last = -1;
-    double my_base = 0.0;
-    const bool mine_crosses = base <= theta && base + mine > theta;
-    auto visit = [&](int c, const float4 &x) {
-        const double v = use_w ? (double)x.z : mass_r(x);
-        if (v > 0.0) my_last = c;
+    float my_rem = 0.f;
+    auto visit = [&](int c, const float4 &x, const float4 &y) {
+        const float v = use_w ? mass_w(y) : mass_r(x);
+        if (v > 0.f) my_last = c;
         if (mine_crosses && my_c == INT_MAX) {
-            if (base + v > theta) {
+            if (v > rem) {
                 my_c = c;
-                my_base = base;
+                my_rem = rem;
             }
-            base += v;
+            rem = __fsub_rn(rem, v);
         }
     };
     if (held) {
 #pragma unroll
         for (int i = 0; i < kPerLane; ++i)
-            if (c0 + i < c1) visit(c0 + i, q[i]);
+            if (c0 + i < c1) visit(c0 + i, q[i], e[i]);
     } else {
-        for (int c = c0; c < c1; ++c) visit(c, sub[c]);
+        for (int c = c0; c < c1; ++c) visit(c, sub[c], sex[c]);
     }
     const int ch_found = warp_min_int(my_c);
     int ch;
-    double th_local;  // remaining mass inside the chosen chunk
+    float th_local;  // remaining mass inside the chosen chunk
     if (ch_found != INT_MAX) {
         ch = ch_found;
         const int owner = __ffs(__ballot_sync(0xFFFFFFFFu, my_c == ch_found)) - 1;
-        th_local = theta - __shfl_sync(0xFFFFFFFFu, my_base, owner);
+        th_local = __shfl_sync(0xFFFFFFFFu, my_rem, owner);
     } else {
         // rounding left no crossing: the last chunk with positive mass
         int last = my_last;
@@ -835,8 +931,7 @@ __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
     const float2 m2 = make_float2(si.m_t, si.m_d);
     const float2 chi2 = make_float2(si.c_hi, si.c_hi), clo2 = make_float2(si.c_lo, si.c_lo);
     const float2 rho2 = two ? make_float2(si.rho_t, si.rho_d) : make_float2(si.rho_t, 0.f);
-    const float dkt = (float)(kt - 1.0), dkd = (float)(kd - 1.0);
-    double run = 0.0;  // mass of the chunk's earlier vectors
+    float run = 0.f;  // mass of the chunk's earlier vectors
     int found = INT_MAX, last_pos = -1;
 #pragma unroll
     for (int i = 0; i < kVecPerLane; ++i) {
@@ -848,8 +943,10 @@ __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
             const float2 ee = weight2(make_float2(elem<DT>(vt[i], k), elem<DT>(vd[i], k)), m2, chi2, clo2);
             const float2 ab = mul2(ee, rho2);
             float wv;
-            if (use_w) wv = ab.x;
-            else wv = ab.x > ab.y ? fmaxf(__fsub_rn(__fmaf_rn(ab.x, dkt, ab.x), __fmaf_rn(ab.y, dkd, ab.y)), 0.f) : 0.f;
+            if (!two) wv = ab.x;
+            else wv = ab.x > ab.y ? fmaxf(0.f, __fadd_rn(__fsub_rn(ab.x, ab.y),
+                                                        __fmaf_rn(dlt, ab.x, -__fmul_rn(dld, ab.y))))
+                                  : 0.f;
             w[k] = wv;
             if (wv > 0.f && q0 + k < P.V) last_pos = (int)(q0 + k);
         }
@@ -862,18 +959,18 @@ __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
             const float u = __shfl_up_sync(0xFFFFFFFFu, inc, o);
             if (lane >= o) inc = __fadd_rn(inc, u);
         }
-        const double lo_edge = run + (double)__fsub_rn(inc, vs);
+        const float lo_edge = __fadd_rn(run, __fsub_rn(inc, vs));
         int tok = INT_MAX;
-        if (lo_edge <= th_local && lo_edge + (double)vs > th_local) {
+        if (lo_edge <= th_local && __fadd_rn(lo_edge, vs) > th_local) {
             float ps = 0.f;
 #pragma unroll
             for (int k = 0; k < EPV; ++k) {
                 ps = k == 0 ? w[0] : __fadd_rn(ps, w[k]);
-                if (tok == INT_MAX && lo_edge + (double)ps > th_local) tok = (int)(q0 + k);
+                if (tok == INT_MAX && __fadd_rn(lo_edge, ps) > th_local) tok = (int)(q0 + k);
             }
         }
         found = warp_min_int(tok);
-        run += (double)__shfl_sync(0xFFFFFFFFu, inc, 31);
+        run = __fadd_rn(run, __shfl_sync(0xFFFFFFFFu, inc, 31));
     }
     if (found == INT_MAX) {
         int lp = last_pos;

@@ -172,6 +172,14 @@ __device__ __forceinline__ FF ff_add(FF a, FF b) {
     return FF{hi, lo};
 }
 
+// a + b as an unevaluated two-float sum (Knuth's TwoSum: no ordering needed).
+__device__ __forceinline__ FF two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return FF{s, e};
+}
+
 __device__ __forceinline__ FF ff_shfl_xor(FF a, int m) {
     return FF{__shfl_xor_sync(0xFFFFFFFFu, a.hi, m), __shfl_xor_sync(0xFFFFFFFFu, a.lo, m)};
 }
@@ -420,6 +428,12 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 __device__ __forceinline__ double uniform_accept(unsigned long long seed, uint32_t b, uint32_t k) {
     uint4 w = philox4x32_10(make_uint4(b, k, 0u, 0u), (uint32_t)seed, (uint32_t)(seed >> 32));
     return (double)(w.x >> 8) * 0x1p-24;
+}
+
+// The same acceptance uniform as a float: a 24-bit value, so exact.
+__device__ __forceinline__ float uniform_accept_f(unsigned long long seed, uint32_t b, uint32_t k) {
+    uint4 w = philox4x32_10(make_uint4(b, k, 0u, 0u), (uint32_t)seed, (uint32_t)(seed >> 32));
+    return (float)(w.x >> 8) * 0x1p-24f;
 }
 
 // Sampling uniform (draw 1): 53 bits of (w0:w1) -> [0,1).
