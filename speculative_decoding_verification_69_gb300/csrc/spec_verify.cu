@@ -48,7 +48,7 @@ struct ReqInfo {
 };
 
 struct SampInfo {
-    int mode;    // 0 none (greedy), 1 residual at row a, 2 bonus at row L
+    int mode;    // 1 residual at row a, 2 bonus at row L
     int slot_t;  // target row slot to sample from
     int slot_d;  // draft row slot (mode 1)
     int a;       // emitted position
@@ -57,9 +57,10 @@ struct SampInfo {
     float rho_t; // 1/S of the target row (mode 1; 1 for the bonus)
     float rho_d; // 1/S of the draft row (mode 1)
     float c_hi, c_lo;
-    int pad0, pad1;
+    int b;       // request
+    int pad0;
     double u;    // sampling uniform
-    double pad2;
+    double pad1;
 };
 
 struct Params {
@@ -80,11 +81,10 @@ struct Params {
     int *row_count;
     int4 *rows;        // (b, slot, greedy, log2(e)/T float bits) of every needed row, request-major
     float4 *part;      // [B, nslot, nchunk]: statistics-pass partials
-    SampInfo *samp;    // [B]
     float4 *sub;       // [B, nchunk]: sampler chunk masses A, B, W
     float4 *sexact;    // [B, nchunk]: exact sums of e (hi, lo) and e' (hi, lo)
-    int *samp_list;    // [B] sampled requests (order of decision)
-    int *samp_count;   // number of entries in samp_list
+    SampInfo *samp_list; // [B] one record per sampled request (order of decision)
+    int *samp_count;     // number of records in samp_list
 };
 
 __device__ __forceinline__ const char *row_ptr(const Params &P, int b, int slot, int esz) {
@@ -589,11 +589,11 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
             }
             si.c_hi = rq.c_hi;
             si.c_lo = rq.c_lo;
-            si.pad0 = si.pad1 = 0;
+            si.b = b;
+            si.pad0 = 0;
             si.u = uniform_sample(P.seed, (uint32_t)b, (uint32_t)a);
-            si.pad2 = 0.0;
-            P.samp[b] = si;
-            P.samp_list[atomicAdd(P.samp_count, 1)] = b;  // order is irrelevant to the results
+            si.pad1 = 0.0;
+            P.samp_list[atomicAdd(P.samp_count, 1)] = si;  // order is irrelevant to the results
         }
     }
     if (P.dbg_rows) {
@@ -700,8 +700,8 @@ __global__ void __launch_bounds__(kSWarps * 32) sv_sample(Params P) {
         c = item - (uint32_t)li * (uint32_t)P.nchunk;
         if (li != cur_li) {
             cur_li = li;
-            cur_b = P.samp_list[li];
-            cur_si = P.samp[cur_b];
+            cur_si = P.samp_list[li];
+            cur_b = cur_si.b;
         }
     };
     auto issue = [&](uint32_t k) {
@@ -813,8 +813,8 @@ __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
     pdl_trigger();
     const int li = blockIdx.x * kFindWarps + warp;
     if (li >= *P.samp_count) return;
-    const int b = P.samp_list[li];
-    const SampInfo si = P.samp[b];
+    const SampInfo si = P.samp_list[li];
+    const int b = si.b;
     const bool resid = si.mode == 1;
     const int nch = P.nchunk;
     const float4 *sub = P.sub + (size_t)b * nch;
@@ -1000,7 +1000,7 @@ __global__ void sv_schedule(const float *__restrict__ mp, float thr, int B, int 
 // ------------------------------------------------------------------ host side
 
 struct Layout {
-    size_t req, row_count, rows, part, samp, sub, sexact, samp_list, samp_count, total;
+    size_t req, row_count, rows, part, sub, sexact, samp_list, samp_count, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -1031,10 +1031,9 @@ static Layout layout(int B, int K, int V, spec_dtype_t dt) {
     L.row_count = off; off = align256(off + sizeof(int));
     L.rows = off; off = align256(off + sizeof(int4) * (size_t)B * nslot);
     L.part = off; off = align256(off + sizeof(float4) * (size_t)B * nslot * nchunk);
-    L.samp = off; off = align256(off + sizeof(SampInfo) * (size_t)B);
     L.sub = off; off = align256(off + sizeof(float4) * (size_t)B * nchunk);
     L.sexact = off; off = align256(off + sizeof(float4) * (size_t)B * nchunk);
-    L.samp_list = off; off = align256(off + sizeof(int) * (size_t)B);
+    L.samp_list = off; off = align256(off + sizeof(SampInfo) * (size_t)B);
     L.samp_count = off; off = align256(off + sizeof(int));
     L.total = off;
     return L;
@@ -1174,10 +1173,9 @@ static spec_status_t verify_impl(const void *target_logits, const void *draft_lo
     P.row_count = reinterpret_cast<int *>(ws + L.row_count);
     P.rows = reinterpret_cast<int4 *>(ws + L.rows);
     P.part = reinterpret_cast<float4 *>(ws + L.part);
-    P.samp = reinterpret_cast<SampInfo *>(ws + L.samp);
     P.sub = reinterpret_cast<float4 *>(ws + L.sub);
     P.sexact = reinterpret_cast<float4 *>(ws + L.sexact);
-    P.samp_list = reinterpret_cast<int *>(ws + L.samp_list);
+    P.samp_list = reinterpret_cast<SampInfo *>(ws + L.samp_list);
     P.samp_count = reinterpret_cast<int *>(ws + L.samp_count);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == SPEC_DTYPE_BF16) {
