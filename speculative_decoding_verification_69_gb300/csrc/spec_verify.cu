@@ -70,7 +70,7 @@ struct Params {
     const int32_t *verify_len;
     const float *temperature;
     unsigned long long seed;
-    int B, K, V, nchunk, nslot;
+    int B, K, V, nchunk, npart, nslot;
     int32_t *out_tokens;
     int32_t *accept_len;
     uint32_t *dev_status;
@@ -80,7 +80,7 @@ struct Params {
     ReqInfo *req;
     int *row_count;
     int4 *rows;        // (b, slot, greedy, log2(e)/T float bits) of every needed row, request-major
-    float4 *part;      // [B, nslot, nchunk]: statistics-pass partials
+    float4 *part;      // [B, nslot, npart]: statistics-pass partials (one per 8 KiB item)
     float4 *sub;       // [B, nchunk]: sampler chunk masses A, B, W
     float4 *sexact;    // [B, nchunk]: exact sums of e (hi, lo) and e' (hi, lo)
     SampInfo *samp_list; // [B] one record per sampled request (order of decision)
@@ -191,8 +191,14 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
 
 // ------------------------------------------------------------------ 2. statistics pass
 
-constexpr int kP1Warps = 8;  // warps per CTA; every warp runs its own copy pipeline
-constexpr int kStages = 3;   // bulk-copy stages per warp
+constexpr int kP1Warps = 4;          // warps per CTA (two CTAs per SM); each runs its own copy ring
+constexpr int kStages = 3;           // bulk-copy stages per warp
+constexpr int kP1ItemBytes = 8192;   // logits per item (one bulk copy, one partial)
+constexpr int kSubVecs = 256;        // 16-byte vectors per 4 KiB sub-block (8 per lane)
+constexpr int kP1Vecs = kP1ItemBytes / 16;
+template <int DT> __host__ __device__ constexpr int p1_item_elems() {
+    return kP1ItemBytes / Fmt<DT>::kESZ;
+}
 
 // What the issuing lane learned about a stage's item (the consumer reads it
 // from shared memory instead of global metadata).
@@ -204,84 +210,144 @@ struct StageDesc {
 };
 
 struct P1Shared {
-    uint4 buf[kP1Warps][kStages][kChunkBytes / 16];
+    uint4 buf[kP1Warps][kStages][kP1Vecs];
     StageDesc desc[kP1Warps][kStages];
     unsigned long long bar[kP1Warps][kStages];
 };
 
-// Chunk partial of one 4 KiB item held in registers (lane's vector i is vector
-// i*32 + lane of the chunk): greedy rows {max, -, lowest argmax, -}; sampled
-// rows {max, sum 2^((z - max) c), -1, -}.
-template <int DT>
-__device__ __forceinline__ float4 chunk_partial(const uint4 (&v)[kVecPerLane], int nvec, bool greedy,
-                                                float c, int e0, int lane) {
-    constexpr int EPV = Fmt<DT>::kEPV;
+// Lane maximum of 8 vectors (vectors at or past nvec - q0 excluded unless FULL).
+template <int DT, bool FULL>
+__device__ __forceinline__ float lane_max8(const uint4 (&v)[8], int lim, int lane) {
     float lm = -INFINITY;
     if (DT == kBF16) {
         uint32_t run = 0xFF80FF80u;
 #pragma unroll
-        for (int i = 0; i < kVecPerLane; ++i)
-            if (i * 32 + lane < nvec)
+        for (int i = 0; i < 8; ++i)
+            if (FULL || i * 32 + lane < lim)
                 run = bf16x2_max(run, bf16x2_max(bf16x2_max(v[i].x, v[i].y), bf16x2_max(v[i].z, v[i].w)));
         lm = fmaxf(__uint_as_float(run << 16), __uint_as_float(run & 0xFFFF0000u));
     } else {
 #pragma unroll
-        for (int i = 0; i < kVecPerLane; ++i)
-            if (i * 32 + lane < nvec) lm = fmaxf(lm, vec_max<DT>(v[i]));
+        for (int i = 0; i < 8; ++i)
+            if (FULL || i * 32 + lane < lim) lm = fmaxf(lm, vec_max<DT>(v[i]));
     }
-    const float m = warp_max(lm);
+    return lm;
+}
+
+// Sum of 2^((z - m) c) over the lane's elements of 8 vectors.
+template <int DT, bool FULL>
+__device__ __forceinline__ float lane_expsum8(const uint4 (&v)[8], int lim, float m, float c,
+                                              int lane) {
+    const unsigned long long m2 = f2u(make_float2(m, m)), c2 = f2u(make_float2(c, c));
+    unsigned long long a0 = 0ull, a1 = 0ull;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (FULL || i * 32 + lane < lim) {
+            if (DT == kBF16) {
+                bf16x2_exp_acc(v[i].x, m2, c2, a0);
+                bf16x2_exp_acc(v[i].y, m2, c2, a1);
+                bf16x2_exp_acc(v[i].z, m2, c2, a0);
+                bf16x2_exp_acc(v[i].w, m2, c2, a1);
+            } else {
+                f32x2_exp_acc(v[i].x, v[i].y, m2, c2, a0);
+                f32x2_exp_acc(v[i].z, v[i].w, m2, c2, a1);
+            }
+        }
+    }
+    const float2 t = add2(u2f(a0), u2f(a1));
+    return t.x + t.y;
+}
+
+// Offset (in elements from the sub-block start) of the lane's first element
+// equal to x, or INT_MAX.  Compares raw bit patterns (x is one of the
+// elements), with +0 and -0 treated as equal as floats compare them.
+template <int DT, bool FULL>
+__device__ __forceinline__ int first_equal8(const uint4 (&v)[8], int lim, float x, int lane) {
+    constexpr int EPV = Fmt<DT>::kEPV;
+    int off = INT_MAX;
+    if (DT == kBF16) {
+        const uint32_t key = __float_as_uint(x) >> 16;
+        const uint32_t msk = (key & 0x7FFFu) == 0 ? 0x7FFF7FFFu : 0xFFFFFFFFu;
+        const uint32_t key2 = (key | (key << 16)) & msk;
+#pragma unroll
+        for (int i = 7; i >= 0; --i) {  // the last hit written is the lowest index
+            if (FULL || i * 32 + lane < lim) {
+                const uint32_t m0 = __vcmpeq2(v[i].x & msk, key2), m1 = __vcmpeq2(v[i].y & msk, key2);
+                const uint32_t m2 = __vcmpeq2(v[i].z & msk, key2), m3 = __vcmpeq2(v[i].w & msk, key2);
+                const uint32_t bits = (m0 & 1u) | ((m0 >> 15) & 2u) | ((m1 & 1u) << 2) | ((m1 >> 13) & 8u) |
+                                      ((m2 & 1u) << 4) | ((m2 >> 11) & 32u) | ((m3 & 1u) << 6) |
+                                      ((m3 >> 9) & 128u);
+                if (bits) off = (i * 32 + lane) * EPV + (__ffs(bits) - 1);
+            }
+        }
+    } else {
+        const uint32_t key = __float_as_uint(x);
+        const uint32_t msk = (key & 0x7FFFFFFFu) == 0 ? 0x7FFFFFFFu : 0xFFFFFFFFu;
+        const uint32_t k2 = key & msk;
+#pragma unroll
+        for (int i = 7; i >= 0; --i) {
+            if (FULL || i * 32 + lane < lim) {
+                const uint32_t bits = ((v[i].x & msk) == k2 ? 1u : 0u) | ((v[i].y & msk) == k2 ? 2u : 0u) |
+                                      ((v[i].z & msk) == k2 ? 4u : 0u) | ((v[i].w & msk) == k2 ? 8u : 0u);
+                if (bits) off = (i * 32 + lane) * EPV + (__ffs(bits) - 1);
+            }
+        }
+    }
+    return off;
+}
+
+// Lane-local running statistics over the 4 KiB sub-blocks of one item: sampled
+// rows keep (max, sum 2^((z - max) c)) rescaled when the max grows; greedy rows
+// keep (max, lowest index of it).  The lane's elements come in increasing index
+// order (vector i * 32 + lane of each sub-block, sub-blocks in order).
+struct LaneStat {
+    float m, s;
+    int idx;
+};
+
+template <int DT, bool FULL>
+__device__ __forceinline__ void lane_update(LaneStat &st, const uint4 (&v)[8], int lim, bool greedy,
+                                            float c, int e_base, int lane) {
+    const float lm = lane_max8<DT, FULL>(v, lim, lane);
     if (greedy) {
-        int idx = INT_MAX;
-        if (lm == m) {
-#pragma unroll
-            for (int i = 0; i < kVecPerLane; ++i) {
-                if (i * 32 + lane < nvec) {
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e)
-                        if (idx == INT_MAX && elem<DT>(v[i], e) == m) idx = e0 + (i * 32 + lane) * EPV + e;
-                }
-            }
+        if (lm > st.m || (st.idx == INT_MAX && lm == st.m && lim > 0)) {  // also an all -inf start
+            st.m = lm;
+            const int j = first_equal8<DT, FULL>(v, lim, lm, lane);
+            st.idx = j == INT_MAX ? INT_MAX : e_base + j;
         }
-        return make_float4(m, 0.f, __int_as_float(warp_min_int(idx)), 0.f);
+        return;
     }
-    float s = 0.f;
-    if (m > -INFINITY) {
-        const unsigned long long m2 = f2u(make_float2(m, m)), c2 = f2u(make_float2(c, c));
-        unsigned long long a0 = 0ull, a1 = 0ull;
-#pragma unroll
-        for (int i = 0; i < kVecPerLane; ++i) {
-            if (i * 32 + lane < nvec) {
-                if (DT == kBF16) {
-                    bf16x2_exp_acc(v[i].x, m2, c2, a0);
-                    bf16x2_exp_acc(v[i].y, m2, c2, a1);
-                    bf16x2_exp_acc(v[i].z, m2, c2, a0);
-                    bf16x2_exp_acc(v[i].w, m2, c2, a1);
-                } else {
-                    f32x2_exp_acc(v[i].x, v[i].y, m2, c2, a0);
-                    f32x2_exp_acc(v[i].z, v[i].w, m2, c2, a1);
-                }
-            }
-        }
-        const float2 t = add2(u2f(a0), u2f(a1));
-        s = t.x + t.y;
+    if (lm > st.m) {
+        if (st.m > -INFINITY) st.s *= ex2((st.m - lm) * c);
+        st.m = lm;
     }
+    if (st.m > -INFINITY) st.s += lane_expsum8<DT, FULL>(v, lim, st.m, c, lane);
+}
+
+// Warp-wide partial of an item from the lanes' statistics: greedy rows
+// {max, -, lowest argmax, -}; sampled rows {max, sum 2^((z - max) c), -1, -}.
+__device__ __forceinline__ float4 warp_partial(const LaneStat &st, bool greedy, float c) {
+    const float m = warp_max(st.m);
+    if (greedy) return make_float4(m, 0.f, __int_as_float(warp_min_int(st.m == m ? st.idx : INT_MAX)), 0.f);
+    const float s = (st.m > -INFINITY) ? st.s * ex2((st.m - m) * c) : 0.f;
     return make_float4(m, warp_sum(s), __int_as_float(-1), 0.f);
 }
 
-// One item = 4 KiB of one needed logit row; item k of a warp is
-// first + k * total_warps (request-major order across the grid).  Each warp
-// keeps kStages bulk copies in flight into its own shared-memory ring; the row
-// metadata of 32 items at a time is gathered across the lanes, so neither the
-// issue nor the consumption of an item waits on a global load.
+// One item = 8 KiB of one needed logit row (one partial per item); item k of
+// a warp is first + k * total_warps (request-major order across the grid).
+// Each warp keeps kStages bulk copies in flight into its own shared-memory
+// ring and reads each stage in 4 KiB sub-blocks; the row metadata of 32 items
+// at a time is gathered across the lanes, so neither the issue nor the
+// consumption of an item waits on a global load.
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kP1Warps * 32) sv_pass1(Params P) {
+__global__ void __launch_bounds__(kP1Warps * 32, 1) sv_pass1(Params P) {
     constexpr int EPV = Fmt<DT>::kEPV;
     constexpr int ESZ = Fmt<DT>::kESZ;
-    constexpr int CE = chunk_elems<DT>();
+    constexpr int CE = p1_item_elems<DT>();
     extern __shared__ __align__(128) unsigned char smem_raw[];
     P1Shared &sh = *reinterpret_cast<P1Shared *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint4(*buf)[kChunkBytes / 16] = sh.buf[warp];
+    uint4(*buf)[kP1Vecs] = sh.buf[warp];
     StageDesc *desc = sh.desc[warp];
     unsigned long long *bar = sh.bar[warp];
     if (VEC && lane == 0) {
@@ -291,7 +357,7 @@ __global__ void __launch_bounds__(kP1Warps * 32) sv_pass1(Params P) {
     __syncwarp();
     pdl_wait();  // the row list comes from sv_prep
     pdl_trigger();
-    const uint32_t nitems = (uint32_t)(*P.row_count) * (uint32_t)P.nchunk;
+    const uint32_t nitems = (uint32_t)(*P.row_count) * (uint32_t)P.npart;
     const uint32_t first = blockIdx.x * kP1Warps + warp;
     const uint32_t stride = gridDim.x * kP1Warps;
     const uint32_t ni = Fmt<DT>::kNegInfWord;
@@ -306,8 +372,8 @@ __global__ void __launch_bounds__(kP1Warps * 32) sv_pass1(Params P) {
             mk0 = k & ~31u;
             const uint32_t item = first + (mk0 + (uint32_t)lane) * stride;
             if (item < nitems) {
-                const uint32_t ri = item / (uint32_t)P.nchunk;
-                mc = item - ri * (uint32_t)P.nchunk;
+                const uint32_t ri = item / (uint32_t)P.npart;
+                mc = item - ri * (uint32_t)P.npart;
                 mrow = P.rows[ri];
             }
         }
@@ -318,7 +384,7 @@ __global__ void __launch_bounds__(kP1Warps * 32) sv_pass1(Params P) {
         r.w = __shfl_sync(0xFFFFFFFFu, mrow.w, j);
         c = __shfl_sync(0xFFFFFFFFu, mc, j);
     };
-    auto nitems_of_warp = (nitems > first) ? (nitems - first + stride - 1) / stride : 0u;
+    const uint32_t nk = (nitems > first) ? (nitems - first + stride - 1) / stride : 0u;
 
     // issue item k of this warp into stage k % kStages
     auto issue = [&](uint32_t k) {
@@ -341,13 +407,12 @@ __global__ void __launch_bounds__(kP1Warps * 32) sv_pass1(Params P) {
         __syncwarp();
     };
 
-    if (VEC) {
-        for (uint32_t k = 0; k < (uint32_t)kStages && k < nitems_of_warp; ++k) issue(k);
-    }
+    if (VEC)
+        for (uint32_t k = 0; k < (uint32_t)kStages && k < nk; ++k) issue(k);
     uint32_t k = 0;
     bool failed = false;
-    for (; k < nitems_of_warp; ++k) {
-        uint4 v[kVecPerLane];
+    for (; k < nk; ++k) {
+        LaneStat st{-INFINITY, 0.f, INT_MAX};
         StageDesc d;
         if (VEC) {
             const int s = (int)(k % kStages);
@@ -357,32 +422,52 @@ __global__ void __launch_bounds__(kP1Warps * 32) sv_pass1(Params P) {
                 break;
             }
             d = desc[s];
+            const bool greedy = d.greedy != 0;
+            const int e0 = d.c * CE;
+            if (d.nvec == kP1Vecs) {
 #pragma unroll
-            for (int i = 0; i < kVecPerLane; ++i) {
-                const int q = i * 32 + lane;
-                v[i] = q < d.nvec ? buf[s][q] : neg_inf;
+                for (int sb = 0; sb < kP1Vecs / kSubVecs; ++sb) {
+                    uint4 v[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[i] = buf[s][sb * kSubVecs + i * 32 + lane];
+                    lane_update<DT, true>(st, v, kSubVecs, greedy, d.cval, e0 + sb * kSubVecs * EPV, lane);
+                }
+            } else {
+                for (int sb = 0; sb * kSubVecs < d.nvec; ++sb) {
+                    uint4 v[8];
+                    const int lim = d.nvec - sb * kSubVecs;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        v[i] = i * 32 + lane < lim ? buf[s][sb * kSubVecs + i * 32 + lane] : neg_inf;
+                    lane_update<DT, false>(st, v, lim, greedy, d.cval, e0 + sb * kSubVecs * EPV, lane);
+                }
             }
             __syncwarp();
-            if (k + kStages < nitems_of_warp) issue(k + kStages);
+            if (k + kStages < nk) issue(k + kStages);
         } else {
             int4 r;
             uint32_t c;
             meta(k, r, c);
             d.b = r.x; d.slot = r.y; d.c = (int)c; d.cval = __int_as_float(r.w); d.greedy = r.z;
-            const uint32_t e0 = c * CE;
-            d.nvec = (int)((min((uint32_t)CE, (uint32_t)P.V - e0) + EPV - 1) / EPV);
+            const int e0 = (int)(c * CE);
+            const int nvec = (int)((min((uint32_t)CE, (uint32_t)P.V - (uint32_t)e0) + EPV - 1) / EPV);
             const char *row = row_ptr(P, r.x, r.y, ESZ);
+            for (int sb = 0; sb * kSubVecs < nvec; ++sb) {
+                uint4 v[8];
+                const int lim = nvec - sb * kSubVecs;
 #pragma unroll
-            for (int i = 0; i < kVecPerLane; ++i)
-                v[i] = load_vec<DT, false>(row, (long long)e0 + (long long)(i * 32 + lane) * EPV, P.V);
+                for (int i = 0; i < 8; ++i)
+                    v[i] = load_vec<DT, false>(row, (long long)e0 + (long long)(sb * kSubVecs + i * 32 + lane) * EPV, P.V);
+                lane_update<DT, false>(st, v, lim, d.greedy != 0, d.cval, e0 + sb * kSubVecs * EPV, lane);
+            }
         }
-        const float4 out = chunk_partial<DT>(v, d.nvec, d.greedy != 0, d.cval, d.c * CE, lane);
-        if (lane == 0) P.part[((size_t)d.b * P.nslot + d.slot) * P.nchunk + d.c] = out;
+        const float4 out = warp_partial(st, d.greedy != 0, d.cval);
+        if (lane == 0) P.part[((size_t)d.b * P.nslot + d.slot) * P.npart + d.c] = out;
     }
     if (VEC && failed) {
         // report, then let every copy this warp still has in flight land
         if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
-        for (uint32_t kk = k; kk < k + kStages && kk < nitems_of_warp; ++kk)
+        for (uint32_t kk = k; kk < k + kStages && kk < nk; ++kk)
             mbar_wait_bounded(reinterpret_cast<uint64_t *>(&bar[kk % kStages]), (kk / kStages) & 1u,
                               kWaitLimitNs);
     }
@@ -430,8 +515,8 @@ __device__ __forceinline__ float4 part_filler() {
 // Row statistics of any chunk count (one warp, blocks of 32 * kPerLane).
 __device__ __forceinline__ float4 combine_row(const Params &P, int b, int slot, bool greedy,
                                               float c, int lane) {
-    const float4 *pp = P.part + ((size_t)b * P.nslot + slot) * P.nchunk;
-    const int n = P.nchunk;
+    const float4 *pp = P.part + ((size_t)b * P.nslot + slot) * P.npart;
+    const int n = P.npart;
     float m = -INFINITY, S = 0.f;
     int amax = INT_MAX;
     for (int base = 0; base < n; base += 32 * kPerLane) {
@@ -494,7 +579,7 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
     pdl_wait();  // chunk partials come from sv_pass1
     pdl_trigger();
     const int nrows = greedy ? L + 1 : 2 * L + 1;
-    if (P.nchunk <= 32 * kPerLane) {
+    if (P.npart <= 32 * kPerLane) {
         // each warp loads the records of up to kRowsPerWarp rows, then reduces them
         for (int r0 = warp; r0 < nrows; r0 += kWarps * kRowsPerWarp) {
             float4 q[kRowsPerWarp][kPerLane];
@@ -502,11 +587,11 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
             for (int j = 0; j < kRowsPerWarp; ++j) {
                 const int r = r0 + j * kWarps;
                 const float4 *pp =
-                    P.part + ((size_t)b * P.nslot + slot_of_row(r < nrows ? r : 0, L, K)) * P.nchunk;
+                    P.part + ((size_t)b * P.nslot + slot_of_row(r < nrows ? r : 0, L, K)) * P.npart;
 #pragma unroll
                 for (int i = 0; i < kPerLane; ++i) {
                     const int ci = i * 32 + lane;
-                    q[j][i] = (r < nrows && ci < P.nchunk) ? pp[ci] : part_filler();
+                    q[j][i] = (r < nrows && ci < P.npart) ? pp[ci] : part_filler();
                 }
             }
 #pragma unroll
@@ -1017,6 +1102,11 @@ static size_t nchunk_for(int V, spec_dtype_t dt) {
     return (size_t)((V + chunk_elems_for(dt) - 1) / chunk_elems_for(dt));
 }
 
+static size_t npart_for(int V, spec_dtype_t dt) {
+    const int pe = dt == SPEC_DTYPE_BF16 ? p1_item_elems<kBF16>() : p1_item_elems<kF32>();
+    return (size_t)((V + pe - 1) / pe);
+}
+
 // Work items are indexed with 32-bit integers.
 static bool items_fit(int B, int K, int V, spec_dtype_t dt) {
     return (size_t)B * (size_t)(2 * K + 1) * nchunk_for(V, dt) < ((size_t)1 << 31);
@@ -1030,7 +1120,7 @@ static Layout layout(int B, int K, int V, spec_dtype_t dt) {
     L.req = off; off = align256(off + sizeof(ReqInfo) * (size_t)B);
     L.row_count = off; off = align256(off + sizeof(int));
     L.rows = off; off = align256(off + sizeof(int4) * (size_t)B * nslot);
-    L.part = off; off = align256(off + sizeof(float4) * (size_t)B * nslot * nchunk);
+    L.part = off; off = align256(off + sizeof(float4) * (size_t)B * nslot * npart_for(V, dt));
     L.sub = off; off = align256(off + sizeof(float4) * (size_t)B * nchunk);
     L.sexact = off; off = align256(off + sizeof(float4) * (size_t)B * nchunk);
     L.samp_list = off; off = align256(off + sizeof(SampInfo) * (size_t)B);
@@ -1162,6 +1252,7 @@ static spec_status_t verify_impl(const void *target_logits, const void *draft_lo
     P.K = K;
     P.V = V;
     P.nchunk = (int)nchunk_for(V, dtype);
+    P.npart = (int)npart_for(V, dtype);
     P.nslot = 2 * K + 1;
     P.out_tokens = out_tokens;
     P.accept_len = accept_len;
