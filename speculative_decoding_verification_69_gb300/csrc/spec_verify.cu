@@ -54,8 +54,8 @@ struct SampInfo {
     int a;       // emitted position
     float m_t;   // max logit of the target row
     float m_d;   // max logit of the draft row (mode 1)
-    float rho_t; // 1/S of the target row (mode 1; 1 for the bonus)
-    float rho_d; // 1/S of the draft row (mode 1)
+    float l_t;   // log2(1/S) of the target row (mode 1; 0 for the bonus)
+    float l_d;   // log2(1/S) of the draft row (mode 1)
     float c_hi, c_lo;
     int b;       // request
     int pad0;
@@ -664,13 +664,13 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
             si.slot_t = a;
             si.slot_d = K + 1 + a;
             si.m_t = s_m[a];
-            si.rho_t = 1.f;
+            si.l_t = 0.f;
             si.m_d = 0.f;
-            si.rho_d = 0.f;
-            if (si.mode == 1) {
-                si.rho_t = __frcp_rn(s_S[a]);
+            si.l_d = 0.f;
+            if (si.mode == 1) {  // any constant factor cancels against the exact sums
+                si.l_t = -__log2f(s_S[a]);
                 si.m_d = s_m[K + 1 + a];
-                si.rho_d = __frcp_rn(s_S[K + 1 + a]);
+                si.l_d = -__log2f(s_S[K + 1 + a]);
             }
             si.c_hi = rq.c_hi;
             si.c_lo = rq.c_lo;
@@ -698,33 +698,31 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
 // ------------------------------------------------------------------ 4. sampler pass
 
 // Masses of one 4 KiB chunk of the sampled row (pair).  Per element pair
-// (target z, draft z'): e = 2^((z - m) c), e' = 2^((z' - m') c) with the row
-// maxima and the two-float c; a = e * rho, b = e' * rho' with rho = 1/S from
-// the statistics pass.  Over {a > b}: D = sum of (a - b) and Bm = sum of b;
-// and the exact sums of e and e' (Fast2Sum).  With kappa = 1 / (rho * sum e)
-// = 1 + delta, the chunk's residual mass is
-//   kappa A - kappa' Bm = D + delta (D + Bm) - delta' Bm,   A = D + Bm;
-// the bonus draw (from p) uses the exact sums of e.
+// (target z, draft z'): a = 2^((z - m) c + l), b = 2^((z' - m') c + l') with
+// the row maxima, the two-float c and l = log2(1/S) from the statistics pass.
+// Over {a > b}: D = sum of (a - b) and Bm = sum of b (warp totals).  The
+// element weights are also added exactly (Fast2Sum against a biased
+// accumulator) into `acc`, whose totals over the whole row give the exact
+// normalisers sum a, sum b.  With kappa = 1 / (sum a) = 1 + delta, a chunk's
+// residual mass is kappa A - kappa' Bm = D + delta (D + Bm) - delta' Bm,
+// A = D + Bm; for the bonus (b = 0) D is the chunk's mass of p.
 template <int DT>
 __device__ __forceinline__ void sample_masses(const uint4 (&vt)[kVecPerLane],
                                               const uint4 (&vd)[kVecPerLane], int nvec,
-                                              const SampInfo &si, float &D, float &Bm, FF &st,
-                                              FF &sd, int lane) {
+                                              const SampInfo &si, float &D, float &Bm,
+                                              BiasAcc2 &acc, int lane) {
     constexpr int EPV = Fmt<DT>::kEPV;
     const float2 m2 = make_float2(si.m_t, si.m_d);
     const float2 chi2 = make_float2(si.c_hi, si.c_hi), clo2 = make_float2(si.c_lo, si.c_lo);
-    const float2 rho2 = make_float2(si.rho_t, si.rho_d);
-    BiasAcc2 acc;
-    acc.init(1.0f);
+    const float2 l2 = make_float2(si.l_t, si.l_d);
     D = 0.f; Bm = 0.f;
 #pragma unroll
     for (int i = 0; i < kVecPerLane; ++i) {
         if (i * 32 + lane < nvec) {
 #pragma unroll
             for (int e = 0; e < EPV; ++e) {
-                const float2 ee = weight2(make_float2(elem<DT>(vt[i], e), elem<DT>(vd[i], e)), m2, chi2, clo2);
-                const float2 ab = mul2(ee, rho2);
-                acc.add(ee);
+                const float2 ab = weight2l(make_float2(elem<DT>(vt[i], e), elem<DT>(vd[i], e)), m2, chi2, clo2, l2);
+                acc.add(ab);
                 if (ab.x > ab.y) {
                     D = __fadd_rn(D, __fsub_rn(ab.x, ab.y));
                     Bm = __fadd_rn(Bm, ab.y);
@@ -734,8 +732,6 @@ __device__ __forceinline__ void sample_masses(const uint4 (&vt)[kVecPerLane],
     }
     D = warp_sum(D);
     Bm = warp_sum(Bm);
-    st = warp_sum_ff(ff_add(FF{__fsub_rn(acc.h.x, 1.0f), acc.l.x}, FF{0.f, 0.f}));
-    sd = warp_sum_ff(ff_add(FF{__fsub_rn(acc.h.y, 1.0f), acc.l.y}, FF{0.f, 0.f}));
 }
 
 constexpr int kSWarps = 4;   // warps per CTA of the sampler pass
@@ -751,7 +747,9 @@ struct SShared {
 // Items = (sampled request, 4 KiB chunk) over the list sv_decide built, in
 // request-major order; warp w takes the contiguous range
 // [w n / W, (w + 1) n / W), so it changes request (and reloads the request's
-// SampInfo) at most a few times.  Same per-warp ring as sv_pass1.
+// SampInfo) at most a few times.  Per item it writes the chunk's {D, Bm}; the
+// exact sums are written once per (warp, request) segment, at the segment's
+// last chunk, with zeros at the others.  Same per-warp ring as sv_pass1.
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kSWarps * 32) sv_sample(Params P) {
     constexpr int EPV = Fmt<DT>::kEPV;
@@ -813,6 +811,7 @@ __global__ void __launch_bounds__(kSWarps * 32) sv_sample(Params P) {
     };
     if (VEC)
         for (uint32_t k = 0; k < (uint32_t)kSStages && k < nk; ++k) issue(k);
+    FF seg_t{0.f, 0.f}, seg_d{0.f, 0.f};  // exact sums of the current request segment
     uint32_t k = 0;
     bool failed = false;
     for (; k < nk; ++k) {
@@ -858,11 +857,24 @@ __global__ void __launch_bounds__(kSWarps * 32) sv_sample(Params P) {
             }
         }
         float Dm, Bm;
-        FF st, sd;
-        sample_masses<DT>(vt, vd, nvec, si, Dm, Bm, st, sd, lane);
+        BiasAcc2 acc;
+        acc.init(1.0f);
+        sample_masses<DT>(vt, vd, nvec, si, Dm, Bm, acc, lane);
+        // fold the item's exact sums into the lane's two-float totals of this
+        // request segment; the warp reduces them once, at the segment's end
+        seg_t = ff_add(seg_t, FF{__fsub_rn(acc.h.x, 1.0f), acc.l.x});
+        seg_d = ff_add(seg_d, FF{__fsub_rn(acc.h.y, 1.0f), acc.l.y});
+        const bool seg_end = c == P.nchunk - 1 || k + 1 == nk;
+        float4 ex = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (seg_end) {
+            const FF st = warp_sum_ff(seg_t), sd = warp_sum_ff(seg_d);
+            ex = make_float4(st.hi, st.lo, sd.hi, sd.lo);
+            seg_t = FF{0.f, 0.f};
+            seg_d = FF{0.f, 0.f};
+        }
         if (lane == 0) {
             P.sub[(size_t)b * P.nchunk + c] = make_float4(Dm, Bm, 0.f, 0.f);
-            P.sexact[(size_t)b * P.nchunk + c] = make_float4(st.hi, st.lo, sd.hi, sd.lo);
+            P.sexact[(size_t)b * P.nchunk + c] = ex;  // nonzero only at a segment's last chunk
         }
     }
     if (VEC && failed) {
@@ -877,17 +889,27 @@ __global__ void __launch_bounds__(kSWarps * 32) sv_sample(Params P) {
 
 constexpr int kFindWarps = 8;  // one warp per sampled request
 
-// kappa - 1 for kappa = 1 / (rho * S), S a two-float sum close to 1/rho.
-__device__ __forceinline__ float kappa_minus_one(float rho, FF S) {
-    const float xh = __fmul_rn(rho, S.hi);
-    const float xl = __fmaf_rn(rho, S.lo, __fmaf_rn(rho, S.hi, -xh));
-    return __fdiv_rn(__fsub_rn(__fsub_rn(1.f, xh), xl), xh);
+// kappa - 1 for kappa = 1 / S, S a two-float sum close to 1.
+__device__ __forceinline__ float kappa_minus_one(FF S) {
+    return __fdiv_rn(__fsub_rn(__fsub_rn(1.f, S.hi), S.lo), S.hi);
+}
+
+// Scaled weights of one lane's 8 vectors of a chunk (lane-contiguous layout:
+// vectors 8 * lane .. 8 * lane + 7), and the draw's weight of each element:
+// the residual max(0, kappa a - kappa' b) or, from p, a.
+template <int DT>
+__device__ __forceinline__ float draw_weight(float2 ab, bool two, float dlt, float dld) {
+    if (!two) return ab.x;
+    return ab.x > ab.y ? fmaxf(0.f, __fadd_rn(__fsub_rn(ab.x, ab.y), __fmaf_rn(dlt, ab.x, -__fmul_rn(dld, ab.y))))
+                       : 0.f;
 }
 
 // Token of one sampled request (one warp), in float and two-float arithmetic
-// (fp64 has a long dependent latency on this part): exact normalisers, chunk
-// masses, a two-float prefix over the lanes (each lane owns a contiguous block
-// of chunks), then the chosen chunk's vectors scanned in order.
+// (fp64 has a long dependent latency on this part): exact normalisers from the
+// segment sums, chunk masses, a two-float prefix over the lanes (each lane owns
+// a contiguous block of chunks), then the chosen chunk (each lane owns 64
+// contiguous elements): one scan of the lane totals and an in-order walk in
+// the crossing lane.
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
     constexpr int EPV = Fmt<DT>::kEPV;
@@ -902,57 +924,73 @@ __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
     const int b = si.b;
     const bool resid = si.mode == 1;
     const int nch = P.nchunk;
-    const float4 *sub = P.sub + (size_t)b * nch;
+    float4 *sub = P.sub + (size_t)b * nch;
     const float4 *sex = P.sexact + (size_t)b * nch;
     const int per = (nch + 31) / 32;
     const int c0 = lane * per, c1 = min(nch, c0 + per);
     const bool held = per <= kPerLane;
-    float4 q[kPerLane], e[kPerLane];
-    FF st{0.f, 0.f}, sd{0.f, 0.f};
+    const char *rowt = row_ptr(P, b, si.slot_t, ESZ);
+    const char *rowd = resid ? row_ptr(P, b, si.slot_d, ESZ) : rowt;
+    const float2 m2 = make_float2(si.m_t, si.m_d);
+    const float2 chi2 = make_float2(si.c_hi, si.c_hi), clo2 = make_float2(si.c_lo, si.c_lo);
+    const uint32_t ni = Fmt<DT>::kNegInfWord;
+    const uint4 neg_inf = make_uint4(ni, ni, ni, ni);
+
+    float4 q[kPerLane];
+    float dlt = 0.f, dld = 0.f;
     if (held) {
 #pragma unroll
-        for (int i = 0; i < kPerLane; ++i) {
-            const int c = c0 + i;
-            q[i] = c < c1 ? sub[c] : make_float4(0.f, 0.f, 0.f, 0.f);
-            e[i] = c < c1 ? sex[c] : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i) {
-            st = ff_add(st, FF{e[i].x, e[i].y});
-            sd = ff_add(sd, FF{e[i].z, e[i].w});
-        }
-    } else {
+        for (int i = 0; i < kPerLane; ++i) q[i] = c0 + i < c1 ? sub[c0 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (resid) {  // exact normalisers: sums over the segment records
+        FF st{0.f, 0.f}, sd{0.f, 0.f};
         for (int c = c0; c < c1; ++c) {
             const float4 x = sex[c];
             st = ff_add(st, FF{x.x, x.y});
             sd = ff_add(sd, FF{x.z, x.w});
         }
+        dlt = kappa_minus_one(warp_sum_ff(st));
+        dld = kappa_minus_one(warp_sum_ff(sd));
     }
-    st = warp_sum_ff(st);
-    const float dlt = resid ? kappa_minus_one(si.rho_t, st) : 0.f;
-    float dld = 0.f;
-    if (resid) dld = kappa_minus_one(si.rho_d, warp_sum_ff(sd));
-    // residual mass D + delta (D + Bm) - delta' Bm; mass of p: rho * (exact sum of e)
+    // residual mass D + delta (D + Bm) - delta' Bm; the mass of p is D (bonus)
     auto mass_r = [&](const float4 &x) {
         return fmaxf(0.f, __fadd_rn(x.x, __fmaf_rn(dlt, __fadd_rn(x.x, x.y), -__fmul_rn(dld, x.y))));
     };
-    auto mass_w = [&](const float4 &y) { return __fmaf_rn(si.rho_t, y.x, __fmul_rn(si.rho_t, y.y)); };
-    float zr = 0.f, zw = 0.f;
+    bool use_w = !resid;
+    float mine = 0.f;
     if (held) {
 #pragma unroll
         for (int i = 0; i < kPerLane; ++i)
-            if (c0 + i < c1) {
-                if (resid) zr = __fadd_rn(zr, mass_r(q[i]));
-                zw = __fadd_rn(zw, mass_w(e[i]));
-            }
+            if (c0 + i < c1) mine = __fadd_rn(mine, use_w ? q[i].x : mass_r(q[i]));
     } else {
-        for (int c = c0; c < c1; ++c) {
-            if (resid) zr = __fadd_rn(zr, mass_r(sub[c]));
-            zw = __fadd_rn(zw, mass_w(sex[c]));
-        }
+        for (int c = c0; c < c1; ++c) mine = __fadd_rn(mine, use_w ? sub[c].x : mass_r(sub[c]));
     }
-    const bool use_w = !resid || !(warp_sum(zr) > 0.f);  // bonus, or no residual mass: sample p
-    const float mine = use_w ? zw : zr;
+    if (resid && !(warp_sum(mine) > 0.f)) {
+        // no residual mass (p = q up to rounding): draw from p.  Rare: the
+        // chunk masses of p are formed here, one chunk at a time.
+        use_w = true;
+        mine = 0.f;
+        const float2 l2 = make_float2(si.l_t, 0.f);
+        for (int c = 0; c < nch; ++c) {
+            float w = 0.f;
+#pragma unroll
+            for (int i = 0; i < kVecPerLane; ++i) {
+                const uint4 v = load_vec<DT, VEC>(rowt, (long long)c * CE + (long long)(i * 32 + lane) * EPV, P.V);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e)
+                    w = __fadd_rn(w, weight2l(make_float2(elem<DT>(v, e), -INFINITY), m2, chi2, clo2, l2).x);
+            }
+            w = warp_sum(w);
+            if (lane == 0) sub[c].x = w;  // this warp alone reads request b's records
+        }
+        __syncwarp();
+        __threadfence_block();
+        if (held) {
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i) q[i] = c0 + i < c1 ? sub[c0 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int c = c0; c < c1; ++c) mine = __fadd_rn(mine, sub[c].x);
+    }
     // two-float inclusive prefix over the lanes, then theta = u * Z
     FF incl{mine, 0.f};
 #pragma unroll
@@ -962,14 +1000,13 @@ __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
     }
     const FF Z{__shfl_sync(0xFFFFFFFFu, incl.hi, 31), __shfl_sync(0xFFFFFFFFu, incl.lo, 31)};
     const double theta = si.u * ((double)Z.hi + (double)Z.lo);
-    // remaining mass at the start of this lane's block
     const FF excl = ff_add(incl, FF{-mine, 0.f});
-    float rem = (float)(theta - ((double)excl.hi + (double)excl.lo));
+    float rem = (float)(theta - ((double)excl.hi + (double)excl.lo));  // mass left at this block
     const bool mine_crosses = rem >= 0.f && rem < mine;
     int my_c = INT_MAX, my_last = -1;
     float my_rem = 0.f;
-    auto visit = [&](int c, const float4 &x, const float4 &y) {
-        const float v = use_w ? mass_w(y) : mass_r(x);
+    auto visit = [&](int c, const float4 &x) {
+        const float v = use_w ? x.x : mass_r(x);
         if (v > 0.f) my_last = c;
         if (mine_crosses && my_c == INT_MAX) {
             if (v > rem) {
@@ -982,86 +1019,89 @@ __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
     if (held) {
 #pragma unroll
         for (int i = 0; i < kPerLane; ++i)
-            if (c0 + i < c1) visit(c0 + i, q[i], e[i]);
+            if (c0 + i < c1) visit(c0 + i, q[i]);
     } else {
-        for (int c = c0; c < c1; ++c) visit(c, sub[c], sex[c]);
+        for (int c = c0; c < c1; ++c) visit(c, sub[c]);
     }
     const int ch_found = warp_min_int(my_c);
     int ch;
-    float th_local;  // remaining mass inside the chosen chunk
+    float th;  // mass left inside the chosen chunk
     if (ch_found != INT_MAX) {
         ch = ch_found;
         const int owner = __ffs(__ballot_sync(0xFFFFFFFFu, my_c == ch_found)) - 1;
-        th_local = __shfl_sync(0xFFFFFFFFu, my_rem, owner);
+        th = __shfl_sync(0xFFFFFFFFu, my_rem, owner);
     } else {
         // rounding left no crossing: the last chunk with positive mass
         int last = my_last;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xFFFFFFFFu, last, o));
         ch = last >= 0 ? last : nch - 1;
-        th_local = INFINITY;
+        th = INFINITY;
     }
-    const char *rowt = row_ptr(P, b, si.slot_t, ESZ);
-    const char *rowd = resid ? row_ptr(P, b, si.slot_d, ESZ) : rowt;
-    const long long e0 = (long long)ch * CE;
-    const uint32_t ni = Fmt<DT>::kNegInfWord;
+    // the chosen chunk, lane-contiguous: lane owns vectors 8 * lane .. 8 * lane + 7
     const bool two = resid && !use_w;
-    uint4 vt[kVecPerLane], vd[kVecPerLane];
+    const float2 l2 = two ? make_float2(si.l_t, si.l_d) : make_float2(si.l_t, 0.f);
+    const long long e0 = (long long)ch * CE + (long long)lane * 8 * EPV;
+    uint4 vt[8], vd[8];
 #pragma unroll
-    for (int i = 0; i < kVecPerLane; ++i) {
-        const long long q0 = e0 + (long long)(i * 32 + lane) * EPV;
-        vt[i] = load_vec<DT, VEC>(rowt, q0, P.V);
-        vd[i] = two ? load_vec<DT, VEC>(rowd, q0, P.V) : make_uint4(ni, ni, ni, ni);
+    for (int i = 0; i < 8; ++i) {
+        vt[i] = load_vec<DT, VEC>(rowt, e0 + (long long)i * EPV, P.V);
+        vd[i] = two ? load_vec<DT, VEC>(rowd, e0 + (long long)i * EPV, P.V) : neg_inf;
     }
-    const float2 m2 = make_float2(si.m_t, si.m_d);
-    const float2 chi2 = make_float2(si.c_hi, si.c_hi), clo2 = make_float2(si.c_lo, si.c_lo);
-    const float2 rho2 = two ? make_float2(si.rho_t, si.rho_d) : make_float2(si.rho_t, 0.f);
-    float run = 0.f;  // mass of the chunk's earlier vectors
-    int found = INT_MAX, last_pos = -1;
+    float vs[8];
+    float tot = 0.f;
+    int last_pos = -1;
 #pragma unroll
-    for (int i = 0; i < kVecPerLane; ++i) {
-        if (found != INT_MAX) break;
-        const long long q0 = e0 + (long long)(i * 32 + lane) * EPV;
-        float w[EPV];
+    for (int i = 0; i < 8; ++i) {
+        float acc = 0.f;
 #pragma unroll
-        for (int k = 0; k < EPV; ++k) {
-            const float2 ee = weight2(make_float2(elem<DT>(vt[i], k), elem<DT>(vd[i], k)), m2, chi2, clo2);
-            const float2 ab = mul2(ee, rho2);
-            float wv;
-            if (!two) wv = ab.x;
-            else wv = ab.x > ab.y ? fmaxf(0.f, __fadd_rn(__fsub_rn(ab.x, ab.y),
-                                                        __fmaf_rn(dlt, ab.x, -__fmul_rn(dld, ab.y))))
-                                  : 0.f;
-            w[k] = wv;
-            if (wv > 0.f && q0 + k < P.V) last_pos = (int)(q0 + k);
+        for (int e = 0; e < EPV; ++e) {
+            const float w = draw_weight<DT>(
+                weight2l(make_float2(elem<DT>(vt[i], e), elem<DT>(vd[i], e)), m2, chi2, clo2, l2), two, dlt, dld);
+            acc = __fadd_rn(acc, w);
+            if (w > 0.f && e0 + i * EPV + e < P.V) last_pos = (int)(e0 + i * EPV + e);
         }
-        float vs = w[0];
+        vs[i] = acc;
+        tot = __fadd_rn(tot, acc);
+    }
+    float inc = tot;
 #pragma unroll
-        for (int k = 1; k < EPV; ++k) vs = __fadd_rn(vs, w[k]);
-        float inc = vs;
+    for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc = __fadd_rn(inc, u);
+    }
+    const float lo = __fsub_rn(inc, tot);
+    int tok = INT_MAX;
+    if (lo <= th && __fadd_rn(lo, tot) > th) {  // the crossing lane walks its elements in order
+        float acc_lo = lo;
+        bool done = false;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float u = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-            if (lane >= o) inc = __fadd_rn(inc, u);
-        }
-        const float lo_edge = __fadd_rn(run, __fsub_rn(inc, vs));
-        int tok = INT_MAX;
-        if (lo_edge <= th_local && __fadd_rn(lo_edge, vs) > th_local) {
-            float ps = 0.f;
+        for (int i = 0; i < 8; ++i) {
+            if (!done && __fadd_rn(acc_lo, vs[i]) > th) {
+                float ps = acc_lo;
+                int lastp = -1;
 #pragma unroll
-            for (int k = 0; k < EPV; ++k) {
-                ps = k == 0 ? w[0] : __fadd_rn(ps, w[k]);
-                if (tok == INT_MAX && __fadd_rn(lo_edge, ps) > th_local) tok = (int)(q0 + k);
+                for (int e = 0; e < EPV; ++e) {
+                    const float w = draw_weight<DT>(
+                        weight2l(make_float2(elem<DT>(vt[i], e), elem<DT>(vd[i], e)), m2, chi2, clo2, l2), two,
+                        dlt, dld);
+                    ps = __fadd_rn(ps, w);
+                    if (w > 0.f) lastp = (int)(e0 + i * EPV + e);
+                    if (tok == INT_MAX && ps > th) tok = (int)(e0 + i * EPV + e);
+                }
+                if (tok == INT_MAX) tok = lastp;  // rounding inside the vector: its last positive element
+                done = true;
             }
+            if (!done) acc_lo = __fadd_rn(acc_lo, vs[i]);
         }
-        found = warp_min_int(tok);
-        run = __fadd_rn(run, __shfl_sync(0xFFFFFFFFu, inc, 31));
+        if (tok < 0) tok = INT_MAX;
     }
+    int found = warp_min_int(tok);
     if (found == INT_MAX) {
         int lp = last_pos;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xFFFFFFFFu, lp, o));
-        found = lp >= 0 ? lp : (int)e0;
+        found = lp >= 0 ? lp : (int)((long long)ch * CE);
     }
     if (lane == 0) P.out_tokens[(size_t)b * (P.K + 1) + si.a] = found;
 }

@@ -156,6 +156,13 @@ __device__ __forceinline__ float2 weight2(float2 z, float2 m2, float2 chi2, floa
     return make_float2(ex2(t.x), ex2(t.y));
 }
 
+// Scaled weights of an element pair: 2^((z - m) * c + l), c = c_hi + c_lo.
+__device__ __forceinline__ float2 weight2l(float2 z, float2 m2, float2 chi2, float2 clo2, float2 l2) {
+    float2 d = sub2(z, m2);
+    float2 t = fma2(d, chi2, fma2(d, clo2, l2));
+    return make_float2(ex2(t.x), ex2(t.y));
+}
+
 // ------------------------------------------------------------------ two-float
 
 struct FF {
