@@ -196,16 +196,21 @@ def sum_over_ranks(x, world):
 
 # ---------------------------------------------------------------- CPU oracle
 
-def oracle_sample(inp, max_seconds=12.0, min_requests=2):
+def host_arrays(inp):
+    """Host copies of one workload's inputs in the oracle's layout (made once)."""
+    return dict(t=workloads.to_numpy_logits(inp["target"]), d=workloads.to_numpy_logits(inp["draft"]),
+                tok=inp["tokens"].cpu().numpy(),
+                vl=inp["verify_len"].cpu().numpy() if inp["verify_len"] is not None else None,
+                T=inp["temperature"].cpu().numpy())
+
+
+def oracle_sample(inp, max_seconds=12.0, min_requests=2, host=None):
     """Time the CPU oracle on a bounded sample of the workload's requests (all
     host cores, rows-parallel over requests).  Returns (positions/s, cores,
     sample description, seconds)."""
     import oracle
-    h_t = workloads.to_numpy_logits(inp["target"])
-    h_d = workloads.to_numpy_logits(inp["draft"])
-    tok = inp["tokens"].cpu().numpy()
-    vl = inp["verify_len"].cpu().numpy() if inp["verify_len"] is not None else None
-    T = inp["temperature"].cpu().numpy()
+    host = host or host_arrays(inp)
+    h_t, h_d, tok, vl, T = host["t"], host["d"], host["tok"], host["vl"], host["T"]
     B, K = tok.shape
     cores = oracle.cpu_count()
     nthreads = min(cores, B)
@@ -411,11 +416,12 @@ def run_reference(args, world, rank, local):
         vl = oracle.schedule_len(inp["draft_maxprob"].cpu().numpy(), inp["threshold"])
         inp["verify_len"] = torch.from_numpy(vl)
     budget = min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup))
+    host = host_arrays(inp)
     for _ in range(args.warmup):
-        oracle_sample(inp, max_seconds=budget)
+        oracle_sample(inp, max_seconds=budget, host=host)
     vals, secs = [], []
     for _ in range(args.steps):
-        pps, cores, sample, dt, _ = oracle_sample(inp, max_seconds=budget)
+        pps, cores, sample, dt, _ = oracle_sample(inp, max_seconds=budget, host=host)
         vals.append(pps)
         secs.append(dt)
     value = statistics.median(vals)
