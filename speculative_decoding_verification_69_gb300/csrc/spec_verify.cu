@@ -734,8 +734,9 @@ __device__ __forceinline__ void sample_masses(const uint4 (&vt)[kVecPerLane],
     Bm = warp_sum(Bm);
 }
 
-constexpr int kSWarps = 4;   // warps per CTA of the sampler pass
-constexpr int kSStages = 2;  // stages per warp; a stage holds a target and a draft chunk
+constexpr int kSWarps = 2;      // warps per CTA of the sampler pass
+constexpr int kSStages = 1;     // stages per warp; a stage holds a target and a draft chunk
+constexpr int kSMinBlocks = 1;  // CTAs per SM the register budget is cut for
 
 struct SShared {
     uint4 buf[kSWarps][kSStages][2 * kChunkBytes / 16];
@@ -751,7 +752,7 @@ struct SShared {
 // exact sums are written once per (warp, request) segment, at the segment's
 // last chunk, with zeros at the others.  Same per-warp ring as sv_pass1.
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kSWarps * 32) sv_sample(Params P) {
+__global__ void __launch_bounds__(kSWarps * 32, kSMinBlocks) sv_sample(Params P) {
     constexpr int EPV = Fmt<DT>::kEPV;
     constexpr int ESZ = Fmt<DT>::kESZ;
     constexpr int CE = chunk_elems<DT>();
