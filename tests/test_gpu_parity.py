@@ -223,6 +223,19 @@ def test_ties_lowest_index():
     assert (gpu["accept_len"][1::2] == K).all()
 
 
+@pytest.mark.parametrize("B", [1024, 1100])
+def test_large_batches(B):
+    """Batches larger than the per-request kernel's 1024 threads (its scan
+    carries across blocks): ragged, mixed batches checked in full against the
+    oracle."""
+    K, V = 3, 640
+    g = torch.Generator().manual_seed(11)
+    L = torch.randint(0, K + 1, (B,), generator=g).tolist()
+    T = [0.0 if b % 3 == 0 else 0.6 + 0.001 * b for b in range(B)]
+    inp = _rand_inputs(B, K, V, torch.bfloat16, seed=1100, T=T, L=L)
+    _check_all(inp, list(range(B)), debug=False)
+
+
 def test_deterministic_and_seed_sensitive():
     inp = workloads.make_inputs(1, B=8)
     a = gpu_run(inp)
