@@ -46,6 +46,31 @@ import workloads  # noqa: E402
 
 HBM_NOMINAL_GBS = 8000.0
 FALLBACK_PEAK_GBS = 6800.0
+def early_exit_bytes(temperature, verify_len, accept_len, K, V, esize, W):
+    """Logit bytes the two-wave path reads: per request, wave [0, W) lists
+    target rows 0..min(L, W-1) (0..L when L <= W) and, when sampled, draft rows
+    0..min(L, W)-1; a request still open after it (L > W, no rejection below W)
+    reads the rest of its rows."""
+    t = temperature.detach().float().cpu()
+    L = verify_len.detach().cpu().long().clamp(0, K)
+    a = accept_len.detach().cpu().long()
+    sampled = (t > 0) & torch.isfinite(t) & (t >= torch.finfo(torch.float32).tiny)
+
+    def rows(k0, k1):
+        t1 = torch.where(L <= k1, L, torch.full_like(L, k1 - 1))
+        nt = (t1 - k0 + 1).clamp(min=0)
+        nd = torch.where(sampled, (torch.minimum(L, torch.full_like(L, k1)) - k0).clamp(min=0),
+                         torch.zeros_like(L))
+        return nt + nd
+
+    if W >= K:
+        n = rows(0, K)
+    else:
+        open_ = (L > W) & (a >= W)
+        n = rows(0, W) + torch.where(open_, rows(W, K), torch.zeros_like(L))
+    return int(n.sum().item()) * V * esize
+
+
 def logit_copies(alg_bytes, l2_bytes):
     """Copies of the logits to cycle through so that >= 2x L2 is read between
     two uses of one copy."""
@@ -64,12 +89,21 @@ def measured_peak():
 
 
 def kernel_source_hash():
-    h = hashlib.sha256()
+    """Hash of the sources the dominant kernel (sv_pass1) is built and launched
+    from: the common device header, spec_verify.cu up to the decision kernel
+    (parameters, the per-request kernel, the statistics pass) and the host
+    launch sequence."""
     d = os.path.join(ROOT, "speculative_decoding_verification_69_gb300", "csrc")
-    for fn in sorted(os.listdir(d)):
-        with open(os.path.join(d, fn), "rb") as f:
-            h.update(fn.encode())
-            h.update(f.read())
+    with open(os.path.join(d, "sv_common.cuh"), "rb") as f:
+        common = f.read()
+    with open(os.path.join(d, "spec_verify.cu"), "rb") as f:
+        src = f.read()
+    head = src[:src.index(b"// ------------------------------------------------------------------ 3. decide")]
+    a = src.index(b"static void launch_all(")
+    launch = src[a:src.index(b"\n}\n", a)]
+    h = hashlib.sha256()
+    for part in (common, head, launch):
+        h.update(part)
     return h.hexdigest()[:16]
 
 
@@ -273,12 +307,14 @@ def run_ours(args, world, rank, local):
     copies = [(inp["target"], inp["draft"])] + [
         (inp["target"].clone(), inp["draft"].clone()) for _ in range(ncopies - 1)]
 
+    ee = args.early_exit
+
     def step(i):
         tgt, drf = copies[i % ncopies]
         if scheduled:
             sv.schedule_len(inp["draft_maxprob"], inp["threshold"], out=vlen)
         verifier(tgt, drf, inp["tokens"], vlen, inp["temperature"],
-                 inp["seed"], out_tokens=out_tokens, accept_len=accept_len)
+                 inp["seed"], out_tokens=out_tokens, accept_len=accept_len, early_exit=ee)
 
     for i in range(args.warmup):
         step(i)
@@ -309,9 +345,11 @@ def run_ours(args, world, rank, local):
     t_wall1 = time.perf_counter()
     # timed region 2: the same steps with CUDA events bracketing the dominant
     # kernel on its stream (roofline); the events end the programmatic launch
-    # overlap on both sides of it, so these steps run slower
+    # overlap on both sides of it, so these steps run slower.  (Early exit runs
+    # the statistics pass once per wave: its roofline is taken over the step.)
     for i in range(args.steps):
-        sv.profile_events(*kev[i])
+        if not ee:
+            sv.profile_events(*kev[i])
         ev_k[i][0].record(stream)
         step(args.warmup + args.steps + i)
         ev_k[i][1].record(stream)
@@ -330,6 +368,10 @@ def run_ours(args, world, rank, local):
     all_pos = sum_over_ranks(positions * args.steps, world)
     value = all_pos / total_s_max
     kern_avg_s = sum(kern_ms) / len(kern_ms) / 1e3
+    read_bytes = alg_bytes
+    if ee:  # logit bytes the two waves actually read, from each request's outcome
+        read_bytes = early_exit_bytes(inp["temperature"], vlen, accept_len, K, V, esz, ee)
+        kern_avg_s = total_s / args.steps
 
     # end to end through the public API: pinned host inputs -> device -> verify -> host
     host = {k: inp[k].cpu().pin_memory() for k in ("target", "draft", "tokens", "temperature")}
@@ -369,8 +411,8 @@ def run_ours(args, world, rank, local):
     e2e_value = all_pos / e2e_s
 
     peak, peak_kind = measured_peak()
-    achieved = alg_bytes / kern_avg_s / 1e9
-    traffic, _ = recorded_traffic("c%d" % cfg)
+    achieved = read_bytes / kern_avg_s / 1e9
+    traffic, _ = recorded_traffic("c%d" % cfg) if not ee else (None, None)
     launches = (sv.kernels_per_verify() + (1 if scheduled else 0)) * args.steps  # timed region 1
 
     result = {
@@ -401,10 +443,12 @@ def run_ours(args, world, rank, local):
                        "second (events bracket it, %.4f ms per step there)"
                        % (sum(step_k_ms) / len(step_k_ms))),
             "parallelism": "replicas" if world > 1 else "single GPU",
+            "mode": ("early exit, first wave %d positions (%d logit bytes read per step)"
+                     % (ee, read_bytes)) if ee else "single pass",
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "sv_pass1",
+            "kernel": "whole step (logit bytes read)" if ee else "sv_pass1",
             "achieved": achieved,
             "peak": peak,
             "peak_source": peak_kind,
@@ -412,7 +456,7 @@ def run_ours(args, world, rank, local):
             "frac": achieved / peak,
             "frac_of_8TBps": achieved / HBM_NOMINAL_GBS,
             "traffic": traffic,
-            "algorithmic_bytes_per_launch": alg_bytes,
+            "algorithmic_bytes_per_launch": read_bytes,
             "kernel_ms": kern_avg_s * 1e3,
         },
         "e2e": {"value": e2e_value, "unit": "positions/s", "h2d_bytes_per_step": h2d,
@@ -478,6 +522,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--early-exit", type=int, default=0,
+                    help="verify positions [0, W) first, then the rest for open requests")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -70,7 +70,8 @@ typedef enum {
 #define SPEC_MAX_V 0x40000000  /* largest supported vocabulary V (2^30) */
 
 /*
- * Workspace size in bytes that spec_verify / spec_verify_debug need for the
+ * Workspace size in bytes that spec_verify / spec_verify_debug /
+ * spec_verify_early_exit need for the
  * given problem (0 on invalid sizes).  The workspace is scratch device memory
  * owned by the caller; it must be 256-byte aligned, need not be initialised,
  * and must not be shared by calls that may run concurrently.
@@ -145,6 +146,26 @@ spec_status_t spec_verify_debug(const void *target_logits, const void *draft_log
                                 int32_t *accept_len, void *workspace, size_t workspace_bytes,
                                 uint32_t *dev_status, double *row_stats, double *probs,
                                 void *stream);
+
+/*
+ * spec_verify_early_exit -- spec_verify with the positions verified in two
+ * waves, [0, first_wave) and then [first_wave, K): a request whose first
+ * rejection falls in the first wave (or whose verify length is at most
+ * first_wave) needs no logit row of the second.  The outputs are bit-identical
+ * to spec_verify's; the rows after a rejection are never read ("speculative
+ * decoding от черновика до проверки" (braintools.ru), "Как это работает",
+ * step 3: the drafts are checked left to right and the first mismatch ends the
+ * step).  first_wave >= 1 (first_wave >= K is one wave, the spec_verify
+ * path); otherwise SPEC_ERR_INVALID_ARG.  The workspace is the one
+ * spec_verify_workspace_bytes gives.  Same contract as spec_verify otherwise;
+ * it launches 8 kernels (5 with one wave).
+ */
+spec_status_t spec_verify_early_exit(const void *target_logits, const void *draft_logits,
+                                     spec_dtype_t dtype, const int32_t *draft_tokens,
+                                     const int32_t *verify_len, const float *temperature,
+                                     uint64_t seed, int B, int K, int V, int first_wave,
+                                     int32_t *out_tokens, int32_t *accept_len, void *workspace,
+                                     size_t workspace_bytes, uint32_t *dev_status, void *stream);
 
 /*
  * spec_schedule_len -- confidence-scheduled verify length (DSpark, iitog.ru):

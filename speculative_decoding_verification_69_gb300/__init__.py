@@ -55,6 +55,8 @@ def load_library():
     L.spec_verify_debug.restype = ctypes.c_int
     L.spec_schedule_len.argtypes = [f32p, ctypes.c_float, ctypes.c_int, ctypes.c_int, i32p, vp]
     L.spec_schedule_len.restype = ctypes.c_int
+    L.spec_verify_early_exit.argtypes = common[:10] + [ctypes.c_int] + common[10:] + [vp]
+    L.spec_verify_early_exit.restype = ctypes.c_int
     L.spec_verify_noalloc.argtypes = common[:12] + [u32p, vp]
     L.spec_verify_noalloc.restype = ctypes.c_int
     L.spec_profile_events.argtypes = [vp, vp]
@@ -69,7 +71,8 @@ def load_library():
 
 def exported_symbols():
     return ["spec_verify_workspace_bytes", "spec_verify", "spec_verify_debug",
-            "spec_schedule_len", "spec_verify_noalloc", "spec_profile_events",
+            "spec_verify_early_exit", "spec_schedule_len", "spec_verify_noalloc",
+            "spec_profile_events",
             "spec_verify_kernel_count", "spec_status_str"]
 
 
@@ -171,7 +174,11 @@ class Verifier:
         return self._ws, n
 
     def __call__(self, target, draft, tokens, verify_len, temperature, seed, *, out_tokens=None,
-                 accept_len=None, dev_status=None, stream=None, row_stats=None, probs=None):
+                 accept_len=None, dev_status=None, stream=None, row_stats=None, probs=None,
+                 early_exit=0):
+        """early_exit = W >= 1 verifies positions [0, W) first and reads the
+        remaining rows only for requests still open (spec_verify_early_exit);
+        0 is the single-pass spec_verify."""
         L = load_library()
         B, K, V = _prepare(target, draft, tokens, verify_len, temperature)
         dev = target.device
@@ -183,7 +190,11 @@ class Verifier:
         args = [_ptr(target), _ptr(draft), _dtype_code(target), _ptr(tokens), _ptr(verify_len),
                 _ptr(temperature), int(seed) & 0xFFFFFFFFFFFFFFFF, B, K, V, _ptr(out_tokens),
                 _ptr(accept_len), _ptr(ws), ws.numel(), _ptr(dev_status)]
-        if row_stats is not None or probs is not None:
+        if early_exit:
+            if row_stats is not None or probs is not None:
+                raise ValueError("early_exit has no debug outputs")
+            st = L.spec_verify_early_exit(*args[:10], int(early_exit), *args[10:], _stream(stream))
+        elif row_stats is not None or probs is not None:
             st = L.spec_verify_debug(*args, _ptr(row_stats), _ptr(probs), _stream(stream))
         else:
             st = L.spec_verify(*args, _stream(stream))

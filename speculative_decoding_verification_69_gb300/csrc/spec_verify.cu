@@ -71,6 +71,8 @@ struct Params {
     const float *temperature;
     unsigned long long seed;
     int B, K, V, nchunk, npart, nslot;
+    int k0, k1;        // positions this wave verifies: [k0, k1) (one wave [0, K) unless early exit)
+    int *ee_done;      // [B] request finished in an earlier wave (early exit), else null
     int32_t *out_tokens;
     int32_t *accept_len;
     uint32_t *dev_status;
@@ -103,6 +105,20 @@ __device__ __forceinline__ float load_logit(const char *row, int dt, int x) {
 
 // ------------------------------------------------------------------ 1. prep
 
+// Rows a request needs in the wave of positions [k0, k1): target rows k0..t1
+// (t1 = L when L <= k1, the bonus / last row, else k1 - 1) and, when sampled,
+// draft rows k0..min(k1, L) - 1.  Returns the count; row r has slot
+// wave_slot(r, ...).  With one wave [0, K) this is every row of the request.
+__device__ __forceinline__ int wave_rows(int L, bool greedy, int k0, int k1, int &nt) {
+    const int t1 = L <= k1 ? L : k1 - 1;
+    nt = max(t1 - k0 + 1, 0);
+    const int nd = greedy ? 0 : max(min(k1, L) - k0, 0);
+    return nt + nd;
+}
+__device__ __forceinline__ int wave_slot(int r, int nt, int k0, int K) {
+    return r < nt ? k0 + r : K + 1 + k0 + (r - nt);
+}
+
 constexpr int kPrepThreads = 1024;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded wait: 2 s
 
@@ -112,15 +128,22 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     if (tid == 0) {
         carry_s = 0;
-        *P.samp_count = 0;
+        if (P.k0 == 0) *P.samp_count = 0;
     }
     __syncthreads();
     pdl_trigger();
+    const bool first_wave = P.k0 == 0;
     for (int base = 0; base < P.B; base += kPrepThreads) {
         const int b = base + tid;
-        int n = 0, L = 0, greedy = 1;
+        int n = 0, L = 0, greedy = 1, nt = 0;
         float cval = 0.f;
-        if (b < P.B) {
+        if (b < P.B && !first_wave) {  // a later wave: the records exist, finished requests drop out
+            const ReqInfo ri = P.req[b];
+            L = ri.L;
+            greedy = ri.greedy;
+            cval = ri.c;
+            n = P.ee_done[b] ? 0 : wave_rows(L, greedy != 0, P.k0, P.k1, nt);
+        } else if (b < P.B) {
             uint32_t st = 0;
             L = P.verify_len ? P.verify_len[b] : P.K;
             const float T = P.temperature[b];
@@ -160,7 +183,8 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
             P.req[b] = ri;
             cval = ri.c;
             if (st && P.dev_status) atomicOr(P.dev_status, st);
-            n = L + 1 + (greedy ? 0 : L);
+            if (P.ee_done) P.ee_done[b] = 0;
+            n = wave_rows(L, greedy != 0, P.k0, P.k1, nt);
         }
         // block exclusive scan of n
         int incl = n;
@@ -177,10 +201,8 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
         for (int i = 0; i < kPrepThreads / 32; ++i) block_tot += warp_tot[i];
         const int off = carry_s + woff + incl - n;
         if (b < P.B) {
-            for (int r = 0; r < n; ++r) {
-                int slot = r <= L ? r : (P.K + 1 + (r - L - 1));
-                P.rows[off + r] = make_int4(b, slot, greedy, __float_as_int(cval));
-            }
+            for (int r = 0; r < n; ++r)
+                P.rows[off + r] = make_int4(b, wave_slot(r, nt, P.k0, P.K), greedy, __float_as_int(cval));
         }
         __syncthreads();
         if (tid == 0) carry_s += block_tot;
@@ -531,9 +553,6 @@ __device__ __forceinline__ float4 combine_row(const Params &P, int b, int slot, 
     return make_float4(m, S, __int_as_float(amax), 0.f);
 }
 
-__device__ __forceinline__ int slot_of_row(int r, int L, int K) {
-    return r <= L ? r : K + 1 + (r - L - 1);
-}
 
 // Acceptance test u * q(x) < p(x) of one position, as u < p/q with
 // p/q = 2^(((g - m) - (g' - m')) c) * S'/S; the exponent is formed in
@@ -578,7 +597,11 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
     }
     pdl_wait();  // chunk partials come from sv_pass1
     pdl_trigger();
-    const int nrows = greedy ? L + 1 : 2 * L + 1;
+    if (P.ee_done && P.ee_done[b]) return;  // finished in an earlier wave (uniform over the CTA)
+    // the rows of this wave: positions [k0, e) and, when L <= k1, the row L
+    const int k0 = P.k0, e = min(P.k1, L);
+    int nt;
+    const int nrows = wave_rows(L, greedy, k0, P.k1, nt);
     if (P.npart <= 32 * kPerLane) {
         // each warp loads the records of up to kRowsPerWarp rows, then reduces them
         for (int r0 = warp; r0 < nrows; r0 += kWarps * kRowsPerWarp) {
@@ -587,7 +610,7 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
             for (int j = 0; j < kRowsPerWarp; ++j) {
                 const int r = r0 + j * kWarps;
                 const float4 *pp =
-                    P.part + ((size_t)b * P.nslot + slot_of_row(r < nrows ? r : 0, L, K)) * P.npart;
+                    P.part + ((size_t)b * P.nslot + wave_slot(r < nrows ? r : 0, nt, k0, K)) * P.npart;
 #pragma unroll
                 for (int i = 0; i < kPerLane; ++i) {
                     const int ci = i * 32 + lane;
@@ -601,7 +624,7 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
                     float m = -INFINITY, S = 0.f;
                     int amax = INT_MAX;
                     reduce_block(q[j], greedy, rq.c, m, S, amax);
-                    const int slot = slot_of_row(r, L, K);
+                    const int slot = wave_slot(r, nt, k0, K);
                     if (lane == 0) {
                         s_m[slot] = m;
                         s_S[slot] = S;
@@ -612,7 +635,7 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
         }
     } else {
         for (int r = warp; r < nrows; r += kWarps) {
-            const int slot = slot_of_row(r, L, K);
+            const int slot = wave_slot(r, nt, k0, K);
             const float4 rs = combine_row(P, b, slot, greedy, rq.c, lane);
             if (lane == 0) {
                 s_m[slot] = rs.x;
@@ -623,8 +646,8 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
     }
     __syncthreads();
     if (warp == 0) {
-        bool acc = true;
-        if (lane < L) {
+        bool acc = true;  // positions before k0 were accepted in earlier waves
+        if (lane >= k0 && lane < e) {
             if (greedy)
                 acc = (x == s_amax[lane]);
             else
@@ -643,11 +666,15 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
             P.dbg_probs[((size_t)b * K + lane) * 2 + 1] = q;
         }
         const unsigned rej = ~__ballot_sync(0xFFFFFFFFu, acc);
-        const int a = rej ? min(__ffs(rej) - 1, L) : L;
+        // first rejection; with none, the request ends at L if this wave
+        // reaches it, else it stays open for the next wave (-1)
+        const int a = rej ? min(__ffs(rej) - 1, L) : (L <= P.k1 ? L : -1);
         if (lane == 0) s_a = a;
     }
     __syncthreads();
     const int a = s_a;
+    if (a < 0) return;  // uniform over the CTA
+    if (P.ee_done && threadIdx.x == 0) P.ee_done[b] = 1;
     int32_t *out = P.out_tokens + (size_t)b * (K + 1);
     for (int k = tid; k <= K; k += kThreads) {
         int v = -1;
@@ -1126,7 +1153,7 @@ __global__ void sv_schedule(const float *__restrict__ mp, float thr, int B, int 
 // ------------------------------------------------------------------ host side
 
 struct Layout {
-    size_t req, row_count, rows, part, sub, sexact, samp_list, samp_count, total;
+    size_t req, row_count, rows, part, sub, sexact, samp_list, samp_count, ee_done, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -1166,6 +1193,7 @@ static Layout layout(int B, int K, int V, spec_dtype_t dt) {
     L.sexact = off; off = align256(off + sizeof(float4) * (size_t)B * nchunk);
     L.samp_list = off; off = align256(off + sizeof(SampInfo) * (size_t)B);
     L.samp_count = off; off = align256(off + sizeof(int));
+    L.ee_done = off; off = align256(off + sizeof(int) * (size_t)B);
     L.total = off;
     return L;
 }
@@ -1260,14 +1288,40 @@ static void launch_all(const Params &P, const DevInfo &d, cudaStream_t s) {
                      P);
 }
 
+// Early exit: the positions in two waves, [0, W) then [W, K).  A wave lists
+// the rows its still-open requests need, streams them and decides; a request
+// whose first rejection (or whose L) falls in the first wave needs no row of
+// the second.  Each wave's sv_prep is an ordinary launch, so it starts after
+// the previous wave's decisions.  The sampler and inverse CDF run once.
+template <int DT, bool VEC>
+static void launch_waves(const Params &P0, const DevInfo &d, cudaStream_t s, int W) {
+    Params P = P0;
+    const int nw = (W > 0 && W < P.K) ? 2 : 1;
+    for (int w = 0; w < nw; ++w) {
+        P.k0 = w == 0 ? 0 : W;
+        P.k1 = (w == 0 && nw == 2) ? W : P.K;
+        sv_prep<<<1, kPrepThreads, 0, s>>>(P);
+        launch_dependent(sv_pass1<DT, VEC>, d.sms * d.occ_p1[DT][VEC], kP1Warps * 32,
+                         VEC ? kP1Smem : 0, s, P);
+        launch_dependent(sv_decide<DT>, P.B, kThreads, 0, s, P);
+    }
+    long long g2 = (long long)d.sms * d.occ_sample[DT][VEC];
+    const long long g2_need = ((long long)P.B * P.nchunk + kSWarps - 1) / kSWarps;
+    if (g2 > g2_need) g2 = g2_need;
+    launch_dependent(sv_sample<DT, VEC>, (int)g2, kSWarps * 32, VEC ? kSSmem : 0, s, P);
+    launch_dependent(sv_find<DT, VEC>, (P.B + kFindWarps - 1) / kFindWarps, kFindWarps * 32, 0, s,
+                     P);
+}
+
 static spec_status_t verify_impl(const void *target_logits, const void *draft_logits,
                                  spec_dtype_t dtype, const int32_t *draft_tokens,
                                  const int32_t *verify_len, const float *temperature,
                                  uint64_t seed, int B, int K, int V, int32_t *out_tokens,
                                  int32_t *accept_len, void *workspace, size_t workspace_bytes,
                                  uint32_t *dev_status, double *row_stats, double *probs,
-                                 void *stream) {
+                                 void *stream, int first_wave = 0) {
     if (!sizes_ok(B, K, V)) return SPEC_ERR_INVALID_ARG;
+    if (first_wave < 0) return SPEC_ERR_INVALID_ARG;
     if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
     if (!items_fit(B, K, V, dtype)) return SPEC_ERR_UNSUPPORTED;
     if (!target_logits || !draft_logits || !draft_tokens || !temperature || !out_tokens ||
@@ -1309,8 +1363,22 @@ static spec_status_t verify_impl(const void *target_logits, const void *draft_lo
     P.sexact = reinterpret_cast<float4 *>(ws + L.sexact);
     P.samp_list = reinterpret_cast<SampInfo *>(ws + L.samp_list);
     P.samp_count = reinterpret_cast<int *>(ws + L.samp_count);
+    P.k0 = 0;
+    P.k1 = K;
+    P.ee_done = nullptr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (dtype == SPEC_DTYPE_BF16) {
+    if (first_wave > 0) {
+        P.ee_done = reinterpret_cast<int *>(ws + L.ee_done);
+        P.dbg_rows = nullptr;
+        P.dbg_probs = nullptr;
+        if (dtype == SPEC_DTYPE_BF16) {
+            if (vec) launch_waves<kBF16, true>(P, *d, s, first_wave);
+            else launch_waves<kBF16, false>(P, *d, s, first_wave);
+        } else {
+            if (vec) launch_waves<kF32, true>(P, *d, s, first_wave);
+            else launch_waves<kF32, false>(P, *d, s, first_wave);
+        }
+    } else if (dtype == SPEC_DTYPE_BF16) {
         if (vec) launch_all<kBF16, true>(P, *d, s);
         else launch_all<kBF16, false>(P, *d, s);
     } else {
@@ -1351,6 +1419,18 @@ spec_status_t spec_verify_debug(const void *target_logits, const void *draft_log
     return sv::verify_impl(target_logits, draft_logits, dtype, draft_tokens, verify_len,
                            temperature, seed, B, K, V, out_tokens, accept_len, workspace,
                            workspace_bytes, dev_status, row_stats, probs, stream);
+}
+
+spec_status_t spec_verify_early_exit(const void *target_logits, const void *draft_logits,
+                                     spec_dtype_t dtype, const int32_t *draft_tokens,
+                                     const int32_t *verify_len, const float *temperature,
+                                     uint64_t seed, int B, int K, int V, int first_wave,
+                                     int32_t *out_tokens, int32_t *accept_len, void *workspace,
+                                     size_t workspace_bytes, uint32_t *dev_status, void *stream) {
+    if (first_wave < 1) return SPEC_ERR_INVALID_ARG;
+    return sv::verify_impl(target_logits, draft_logits, dtype, draft_tokens, verify_len,
+                           temperature, seed, B, K, V, out_tokens, accept_len, workspace,
+                           workspace_bytes, dev_status, nullptr, nullptr, stream, first_wave);
 }
 
 spec_status_t spec_schedule_len(const float *draft_maxprob, float threshold, int B, int K,

@@ -82,3 +82,13 @@ def test_host_validation_without_gpu(lib):
     assert lib.spec_schedule_len(fake, 0.3, 4, 40, i32, None) == 1
     assert lib.spec_status_str(0) == b"ok"
     assert b"workspace" in lib.spec_status_str(4)
+
+    def call_ee(W, **kw):
+        a = dict(base, **kw)
+        return lib.spec_verify_early_exit(a["t"], a["d"], a["dt"], a["tok"], a["vl"], a["T"],
+                                          a["seed"], a["B"], a["K"], a["V"], W, a["o"], a["a"],
+                                          a["ws"], a["wsb"], a["st"], None)
+
+    assert call_ee(0) == 1 and call_ee(-3) == 1              # first wave must be >= 1
+    assert call_ee(2, B=0) == 1 and call_ee(2, t=None) == 1
+    assert call_ee(2, ws=None) == 4

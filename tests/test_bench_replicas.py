@@ -72,3 +72,17 @@ def test_logit_copies_cover_twice_l2():
         assert n >= 2
         assert (n - 1) * alg >= 2 * l2      # bytes read between two uses of a copy
         assert n == 2 or (n - 2) * alg < 2 * l2  # and no more copies than needed
+
+
+def test_early_exit_bytes():
+    import torch
+    T = torch.tensor([1.0, 0.0, 0.7, 0.5])          # sampled, greedy, sampled, sampled
+    L = torch.tensor([4, 4, 1, 4], dtype=torch.int32)
+    a = torch.tensor([3, 4, 1, 0], dtype=torch.int32)
+    K, V, s = 4, 10, 2
+    # one wave: each needed row once
+    assert bench.early_exit_bytes(T, L, a, K, V, s, K) == workloads.algorithmic_bytes(T, L, V, s)
+    # W = 2: wave 1 target 0..1 (+ draft 0..1 when sampled); request 2 (L = 1) ends in it
+    # with target 0..1 and draft 0; requests 0 and 1 stay open (a >= 2) and read target
+    # 2..4 (+ draft 2..3): 4 + 5, 2 + 3, 3, 4 rows
+    assert bench.early_exit_bytes(T, L, a, K, V, s, 2) == (9 + 5 + 3 + 4) * V * s
