@@ -63,6 +63,9 @@ def lib():
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, i32p, i32p, f64p, f64p, u32p]
         L.svo_schedule_len.argtypes = [f32p, ctypes.c_float, ctypes.c_int, ctypes.c_int, i32p]
+        L.svo_schedule_budget.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_longlong, i32p]
+        L.svo_draft_confidence.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, f32p, f64p]
         _lib = L
     return _lib
 
@@ -228,6 +231,28 @@ def schedule_len(draft_maxprob, threshold):
     out = np.empty(B, dtype=np.int32)
     lib().svo_schedule_len(_ptr(mp, ctypes.c_float), float(np.float32(threshold)), B, K,
                            _ptr(out, ctypes.c_int32))
+    return out
+
+
+def schedule_budget(draft_maxprob, budget):
+    """Load-aware schedule: the `budget` positions with the largest prefix
+    survival probabilities (ties to the lower request, then position)."""
+    mp = np.ascontiguousarray(draft_maxprob, dtype=np.float32)
+    B, K = mp.shape
+    out = np.empty(B, dtype=np.int32)
+    lib().svo_schedule_budget(_ptr(mp, ctypes.c_float), B, K, int(budget), _ptr(out, ctypes.c_int32))
+    return out
+
+
+def draft_confidence(draft, temperature):
+    """max_v q_k(v) of every draft row [B, K, V] at the request's temperature
+    (1 for greedy requests), in float64."""
+    draft = np.ascontiguousarray(draft)
+    B, K, V = draft.shape
+    T = np.ascontiguousarray(temperature, dtype=np.float32)
+    out = np.empty((B, K), dtype=np.float64)
+    lib().svo_draft_confidence(draft.ctypes.data, dtype_code(draft), B, K, V,
+                               _ptr(T, ctypes.c_float), _ptr(out, ctypes.c_double))
     return out
 
 

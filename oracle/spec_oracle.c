@@ -27,7 +27,7 @@
  *   chosen per request from the estimated survival probability of the draft
  *   prefix.
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   - the same per-request temperature T divides both target and draft logits;
  *   - T <= 0, T not finite, or T below the smallest normal float => greedy;
  *   - acceptance test "u * q(x) < p(x)" with u in [0,1) on a 2^-24 grid;
@@ -389,11 +389,78 @@ void svo_row_intermediates(const void *row, int dtype, int V, float T, int x, do
     if (x >= 0 && x < V) *px = exp(svo_logit(row, dtype, x) / (double)T - mm) / S;
 }
 
+/* ------------------------------------------------------------- confidence */
+
+/* Draft confidence of one position: the largest probability of the draft
+ * distribution q at the request's temperature, max_v q(v) = 1 / sum_v exp(z_v/T
+ * - max z/T).  A greedy request's q is a point mass: 1. */
+void svo_draft_confidence(const void *draft, int dtype, int B, int K, int V,
+                          const float *temperature, double *out) {
+    const size_t esz = dtype == SVO_BF16 ? 2 : (dtype == SVO_F64 ? 8 : 4);
+    for (int b = 0; b < B; ++b) {
+        for (int k = 0; k < K; ++k) {
+            const char *row = (const char *)draft + ((size_t)b * K + k) * (size_t)V * esz;
+            double m, S;
+            if (svo_is_greedy(temperature[b])) {
+                out[(size_t)b * K + k] = 1.0;
+                continue;
+            }
+            svo_row_softmax(row, dtype, V, (double)temperature[b], NULL, &m, &S);
+            out[(size_t)b * K + k] = 1.0 / S;
+        }
+    }
+}
+
 /* ------------------------------------------------------------- schedule */
 
 /* Confidence-scheduled verify length (DSpark): the number of leading draft
  * positions whose running float32 product of draft max-probabilities stays at
  * or above the threshold.  Each product is rounded to float32 on its own. */
+/* Survival probability of draft prefix k of request b: the running float32
+ * product c_0 * ... * c_k of the draft max-probabilities, each product rounded
+ * on its own, with every c clamped to [0, 1] (NaN counts as 0). */
+static void svo_survival(const float *maxprob, int B, int K, float *s) {
+    for (int b = 0; b < B; ++b) {
+        volatile float prod = 1.0f;
+        for (int k = 0; k < K; ++k) {
+            float c = maxprob[(size_t)b * K + k];
+            if (!(c >= 0.0f)) c = 0.0f;
+            if (c > 1.0f) c = 1.0f;
+            volatile float cv = c;
+            prod = prod * cv;
+            s[(size_t)b * K + k] = prod;
+        }
+    }
+}
+
+static const float *g_sort_s;
+static int svo_cmp_survival(const void *x, const void *y) {
+    const int i = *(const int *)x, j = *(const int *)y;
+    if (g_sort_s[i] != g_sort_s[j]) return g_sort_s[i] > g_sort_s[j] ? -1 : 1;
+    return i < j ? -1 : (i > j ? 1 : 0);
+}
+
+/* Load-aware schedule (DSpark: the verify length follows both the prefix's
+ * survival probability and the engine's current load): given a budget of
+ * positions the engine verifies this step, keep the `budget` positions (b, k)
+ * with the largest survival probabilities, ties to the lower b then the lower
+ * k.  Survival never grows along a request, so the kept set is a prefix of
+ * every request; verify_len[b] is its length. */
+void svo_schedule_budget(const float *maxprob, int B, int K, long long budget, int32_t *out) {
+    const size_t n = (size_t)B * K;
+    float *s = (float *)malloc(n * sizeof(float));
+    int *idx = (int *)malloc(n * sizeof(int));
+    svo_survival(maxprob, B, K, s);
+    for (size_t i = 0; i < n; ++i) idx[i] = (int)i;
+    g_sort_s = s;
+    qsort(idx, n, sizeof(int), svo_cmp_survival);
+    for (int b = 0; b < B; ++b) out[b] = 0;
+    const size_t take = budget <= 0 ? 0 : ((size_t)budget < n ? (size_t)budget : n);
+    for (size_t i = 0; i < take; ++i) out[idx[i] / K] += 1;
+    free(s);
+    free(idx);
+}
+
 void svo_schedule_len(const float *maxprob, float threshold, int B, int K, int32_t *out) {
     for (int b = 0; b < B; ++b) {
         volatile float prod = 1.0f;

@@ -428,3 +428,52 @@ def test_length_clamp_and_bad_tokens(oracle):
     for b in range(4):
         a = res["accept_len"][b]
         assert all(v == -1 for v in res["out_tokens"][b, a + 1:])
+
+
+# ---------------------------------------------------------------- load-aware schedule, confidence
+
+def test_schedule_budget_hand_cases(oracle):
+    """"DSpark ... верификацией по уверенности" (iitog.ru), "Ключевые факты": the
+    verify length follows the prefix's survival probability and the engine's load.
+    Survival of (b, k) is the running product of the draft max-probabilities; a
+    budget of N positions keeps the N most likely to survive."""
+    import numpy as np
+    mp = np.array([[0.9, 0.8, 0.5], [0.95, 0.1, 1.0]], np.float32)
+    # survival: request 0: 0.9, 0.72, 0.36; request 1: 0.95, 0.095, 0.095
+    assert oracle.schedule_budget(mp, 3).tolist() == [2, 1]
+    assert oracle.schedule_budget(mp, 4).tolist() == [3, 1]
+    assert oracle.schedule_budget(mp, 5).tolist() == [3, 2]   # tie 0.095: lower k first
+    assert oracle.schedule_budget(mp, 0).tolist() == [0, 0]
+    assert oracle.schedule_budget(mp, 100).tolist() == [3, 3]
+    ones = np.ones((2, 4), np.float32)                        # all survival 1: lower b first
+    assert oracle.schedule_budget(ones, 5).tolist() == [4, 1]
+    odd = np.array([[np.nan, 0.5], [1.5, 0.5]], np.float32)   # NaN -> 0, 1.5 -> 1
+    assert oracle.schedule_budget(odd, 1).tolist() == [0, 1]
+    assert oracle.schedule_budget(odd, 3).tolist() == [1, 2]
+
+
+def test_schedule_budget_matches_threshold_rule(oracle):
+    """With the budget set to the number of positions whose survival reaches a
+    threshold, the kept set is exactly the threshold schedule's (the separately
+    pinned confidence-scheduled verify length)."""
+    import numpy as np
+    rng = np.random.default_rng(5)
+    for trial in range(20):
+        mp = rng.uniform(0.05, 1.0, size=(64, 12)).astype(np.float32)
+        tau = float(rng.uniform(0.05, 0.6))
+        L = oracle.schedule_len(mp, tau)
+        assert oracle.schedule_budget(mp, int(L.sum())).tolist() == L.tolist()
+
+
+def test_draft_confidence_hand_values(oracle):
+    """max_v q(v) at temperature T: a uniform row gives 1/V; logits (ln 3, 0) give
+    3/4; halving T squares the odds (9/10); a greedy request's q is a point mass."""
+    import numpy as np
+    d = np.zeros((2, 2, 4), np.float64)
+    d[0, 1] = [np.log(3.0), 0.0, -np.inf, -np.inf]
+    d[1, 0] = [np.log(3.0), 0.0, -np.inf, -np.inf]
+    c = oracle.draft_confidence(d, np.array([1.0, 0.5], np.float32))
+    assert np.allclose(c[0], [0.25, 0.75], rtol=1e-14)
+    assert abs(c[1, 0] - 0.9) < 1e-14 and abs(c[1, 1] - 0.25) < 1e-14
+    g = oracle.draft_confidence(d, np.array([0.0, float("nan")], np.float32))
+    assert (g == 1.0).all()
