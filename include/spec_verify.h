@@ -168,6 +168,41 @@ spec_status_t spec_verify_early_exit(const void *target_logits, const void *draf
                                      size_t workspace_bytes, uint32_t *dev_status, void *stream);
 
 /*
+ * spec_draft_confidence -- the draft's confidence at every position, as the
+ * confidence-scheduled verification of "DSpark: ... верификацией по
+ * уверенности" (iitog.ru), "Ключевые факты", uses it: maxprob[b, k] =
+ * max_v q_k(v) with q_k = softmax(draft_logits[b, k] / T_b), that is
+ * 1 / sum_v exp((z_v - max z) / T_b); 1 for greedy requests (T_b not a
+ * positive normal float: q is a point mass).  One pass over the draft rows of
+ * the sampled requests.
+ *   draft_logits [B, K, V] bf16/fp32 device (16-byte aligned), temperature [B]
+ *   float32 device, maxprob [B, K] float32 device (written), relative accuracy
+ *   ~1e-6.  The workspace is the one spec_verify_workspace_bytes gives for the
+ *   same B, K, V.  Errors as spec_verify.
+ */
+spec_status_t spec_draft_confidence(const void *draft_logits, spec_dtype_t dtype,
+                                    const float *temperature, int B, int K, int V,
+                                    float *maxprob, void *workspace, size_t workspace_bytes,
+                                    void *stream);
+
+/*
+ * spec_schedule_budget -- the load-aware side of the same schedule: the
+ * verify length follows the prefix's survival probability and the engine's
+ * current load.  Given the number of positions the engine verifies this step
+ * (budget, from its load), keep the budget positions (b, k) with the largest
+ * survival s[b, k] = c[b, 0] * ... * c[b, k] (c = draft_maxprob clamped to
+ * [0, 1], NaN as 0; float32 products left to right, each rounded to nearest),
+ * ties to the lower b, then the lower k.  Survival never grows along a
+ * request, so the kept positions are a prefix of every request:
+ * verify_len[b] is its length (budget <= 0: all 0; budget >= B*K: all K).
+ *   draft_maxprob [B, K] float32 device, verify_len [B] int32 device (written).
+ *   1 <= B < 2^24, 1 <= K <= SPEC_MAX_K, B * K <= 2^22 (else
+ *   SPEC_ERR_UNSUPPORTED).  Bit-exact with a sort of the survival values.
+ */
+spec_status_t spec_schedule_budget(const float *draft_maxprob, int B, int K, long long budget,
+                                   int32_t *verify_len, void *stream);
+
+/*
  * spec_schedule_len -- confidence-scheduled verify length (DSpark, iitog.ru):
  *   verify_len[b] = number of leading positions k whose running product
  *   prod_{j<=k} draft_maxprob[b, j] stays >= threshold, the product taken left

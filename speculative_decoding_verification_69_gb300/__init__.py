@@ -57,6 +57,11 @@ def load_library():
     L.spec_schedule_len.restype = ctypes.c_int
     L.spec_verify_early_exit.argtypes = common[:10] + [ctypes.c_int] + common[10:] + [vp]
     L.spec_verify_early_exit.restype = ctypes.c_int
+    L.spec_draft_confidence.argtypes = [vp, ctypes.c_int, f32p, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, f32p, vp, ctypes.c_size_t, vp]
+    L.spec_draft_confidence.restype = ctypes.c_int
+    L.spec_schedule_budget.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_longlong, i32p, vp]
+    L.spec_schedule_budget.restype = ctypes.c_int
     L.spec_verify_noalloc.argtypes = common[:12] + [u32p, vp]
     L.spec_verify_noalloc.restype = ctypes.c_int
     L.spec_profile_events.argtypes = [vp, vp]
@@ -71,7 +76,8 @@ def load_library():
 
 def exported_symbols():
     return ["spec_verify_workspace_bytes", "spec_verify", "spec_verify_debug",
-            "spec_verify_early_exit", "spec_schedule_len", "spec_verify_noalloc",
+            "spec_verify_early_exit", "spec_draft_confidence", "spec_schedule_budget",
+            "spec_schedule_len", "spec_verify_noalloc",
             "spec_profile_events",
             "spec_verify_kernel_count", "spec_status_str"]
 
@@ -202,7 +208,45 @@ class Verifier:
         return out_tokens, accept_len
 
 
+def draft_confidence(draft, temperature, *, out=None, stream=None, verifier=None):
+    """max_v q_k(v) of every draft row [B, K, V] at the request's temperature
+    (1 for greedy requests): float32 [B, K] on the device."""
+    L = load_library()
+    if draft.dim() != 3 or not draft.is_cuda or not draft.is_contiguous():
+        raise ValueError("draft must be a contiguous CUDA tensor [B, K, V]")
+    B, K, V = draft.shape
+    if temperature.shape != (B,) or temperature.dtype != torch.float32 or not temperature.is_cuda:
+        raise ValueError("temperature must be float32 [B] on the device")
+    if out is None:
+        out = torch.empty((B, K), dtype=torch.float32, device=draft.device)
+    v = verifier or _default_verifier()
+    ws, n = v.workspace(B, K, V, draft.dtype, draft.device)
+    _check(L.spec_draft_confidence(_ptr(draft), _dtype_code(draft), _ptr(temperature), B, K, V,
+                                   _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def schedule_budget(draft_maxprob, budget, *, out=None, stream=None):
+    """Verify lengths keeping the `budget` positions with the largest prefix
+    survival probabilities: int32 [B] on the device."""
+    L = load_library()
+    B, K = draft_maxprob.shape
+    if draft_maxprob.dtype != torch.float32 or not draft_maxprob.is_cuda or not draft_maxprob.is_contiguous():
+        raise ValueError("draft_maxprob must be a contiguous float32 CUDA tensor [B, K]")
+    if out is None:
+        out = torch.empty((B,), dtype=torch.int32, device=draft_maxprob.device)
+    _check(L.spec_schedule_budget(_ptr(draft_maxprob), B, K, int(budget), _ptr(out), _stream(stream)))
+    return out
+
+
 _default = None
+
+
+def _default_verifier():
+    global _default
+    if _default is None:
+        _default = Verifier()
+    return _default
 
 
 def verify(target, draft, tokens, verify_len, temperature, seed, **kw):

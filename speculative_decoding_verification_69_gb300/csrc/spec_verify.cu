@@ -1150,6 +1150,146 @@ __global__ void sv_schedule(const float *__restrict__ mp, float thr, int B, int 
     out[b] = L;
 }
 
+// ------------------------------------------------------------------ draft confidence
+
+// Rows of the draft-confidence pass: every draft row of every sampled request
+// (a greedy request's draft distribution is a point mass).
+__global__ void __launch_bounds__(kPrepThreads) sv_conf_rows(Params P) {
+    __shared__ int warp_tot[kPrepThreads / 32];
+    __shared__ int carry_s;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    if (tid == 0) carry_s = 0;
+    __syncthreads();
+    pdl_trigger();
+    for (int base = 0; base < P.B; base += kPrepThreads) {
+        const int b = base + tid;
+        int n = 0;
+        float cval = 0.f;
+        if (b < P.B) {
+            const float T = P.temperature[b];
+            if (isfinite(T) && T >= FLT_MIN) {
+                n = P.K;
+                cval = __fdiv_rn(kLog2EHi, T);
+            }
+        }
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) warp_tot[w] = incl;
+        __syncthreads();
+        int woff = 0, block_tot = 0;
+        for (int i = 0; i < kPrepThreads / 32; ++i) {
+            if (i < w) woff += warp_tot[i];
+            block_tot += warp_tot[i];
+        }
+        const int off = carry_s + woff + incl - n;
+        for (int r = 0; r < n; ++r) P.rows[off + r] = make_int4(b, P.K + 1 + r, 0, __float_as_int(cval));
+        __syncthreads();
+        if (tid == 0) carry_s += block_tot;
+        __syncthreads();
+    }
+    if (tid == 0) *P.row_count = carry_s;
+}
+
+// max_v q(v) = 1 / sum_v 2^((z_v - m) log2(e)/T) of draft row (b, k), one warp
+// per row from the statistics pass's partials; 1 for greedy requests.
+__global__ void __launch_bounds__(kThreads) sv_conf_out(Params P, float *maxprob) {
+    pdl_wait();  // partials come from sv_pass1
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (row >= (long long)P.B * P.K) return;
+    const int b = (int)(row / P.K), k = (int)(row - (long long)b * P.K);
+    const float T = P.temperature[b];
+    float out = 1.0f;
+    if (isfinite(T) && T >= FLT_MIN) {
+        const float4 rs = combine_row(P, b, P.K + 1 + k, false, __fdiv_rn(kLog2EHi, T), lane);
+        out = __frcp_rn(rs.y);
+    }
+    if (lane == 0) maxprob[row] = out;
+}
+
+// ------------------------------------------------------------------ load-aware schedule
+
+constexpr int kBudgetThreads = 1024;
+constexpr long long kBudgetMaxN = 1 << 22;  // positions B * K one CTA selects from
+
+// Survival key of position (b, k): the float bits of the running product of
+// clamped max-probabilities (non-negative, so ordered as integers) above the
+// complemented flat index, so that larger keys survive more and ties go to the
+// lower (b, k).  All keys differ.
+__device__ __forceinline__ unsigned long long survival_key(float s, long long i) {
+    return ((unsigned long long)__float_as_uint(s) << 32) | (0xFFFFFFFFull - (unsigned long long)i);
+}
+__device__ __forceinline__ float clamp_prob(float c) {
+    if (!(c >= 0.0f)) c = 0.0f;  // NaN too
+    return c > 1.0f ? 1.0f : c;
+}
+
+// One CTA: the budget-th largest survival key by an 8-pass byte radix select
+// (keys recomputed each pass), then each request's verify length = the number
+// of its positions at or above that key (a prefix, since survival never grows
+// along a request).
+__global__ void __launch_bounds__(kBudgetThreads) sv_schedule_budget(const float *__restrict__ mp,
+                                                                    int B, int K, long long budget,
+                                                                    int32_t *__restrict__ out) {
+    __shared__ unsigned hist[256];
+    __shared__ unsigned long long s_prefix;
+    __shared__ long long s_rem;
+    const int tid = threadIdx.x;
+    const long long n = (long long)B * K;
+    if (budget <= 0 || budget >= n) {
+        for (int b = tid; b < B; b += kBudgetThreads) out[b] = budget <= 0 ? 0 : K;
+        return;
+    }
+    if (tid == 0) {
+        s_prefix = 0ull;
+        s_rem = budget;  // rank still to place (1-based) among the matching keys
+    }
+    unsigned long long mask = 0ull;
+    for (int pass = 7; pass >= 0; --pass) {
+        for (int i = tid; i < 256; i += kBudgetThreads) hist[i] = 0u;
+        __syncthreads();
+        const unsigned long long prefix = s_prefix;
+        const int sh = pass * 8;
+        for (int b = tid; b < B; b += kBudgetThreads) {
+            float s = 1.0f;
+            for (int k = 0; k < K; ++k) {
+                s = __fmul_rn(s, clamp_prob(mp[(size_t)b * K + k]));
+                const unsigned long long key = survival_key(s, (long long)b * K + k);
+                if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & 0xFFu], 1u);
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            long long rem = s_rem;
+            int d = 255;
+            for (; d > 0; --d) {
+                if ((long long)hist[d] >= rem) break;
+                rem -= hist[d];
+            }
+            s_rem = rem;
+            s_prefix = prefix | ((unsigned long long)d << sh);
+        }
+        mask |= 0xFFull << sh;
+        __syncthreads();
+    }
+    const unsigned long long tau = s_prefix;  // the budget-th largest key
+    for (int b = tid; b < B; b += kBudgetThreads) {
+        float s = 1.0f;
+        int L = 0;
+        for (int k = 0; k < K; ++k) {
+            s = __fmul_rn(s, clamp_prob(mp[(size_t)b * K + k]));
+            if (survival_key(s, (long long)b * K + k) >= tau) L = k + 1;
+            else break;
+        }
+        out[b] = L;
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 struct Layout {
@@ -1431,6 +1571,72 @@ spec_status_t spec_verify_early_exit(const void *target_logits, const void *draf
     return sv::verify_impl(target_logits, draft_logits, dtype, draft_tokens, verify_len,
                            temperature, seed, B, K, V, out_tokens, accept_len, workspace,
                            workspace_bytes, dev_status, nullptr, nullptr, stream, first_wave);
+}
+
+spec_status_t spec_draft_confidence(const void *draft_logits, spec_dtype_t dtype,
+                                    const float *temperature, int B, int K, int V,
+                                    float *maxprob, void *workspace, size_t workspace_bytes,
+                                    void *stream) {
+    if (!sv::sizes_ok(B, K, V)) return SPEC_ERR_INVALID_ARG;
+    if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
+    if (!sv::items_fit(B, K, V, dtype)) return SPEC_ERR_UNSUPPORTED;
+    if (!draft_logits || !temperature || !maxprob) return SPEC_ERR_INVALID_ARG;
+    if ((uintptr_t)draft_logits & 15u) return SPEC_ERR_INVALID_ARG;
+    const sv::Layout L = sv::layout(B, K, V, dtype);
+    if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u))
+        return SPEC_ERR_WORKSPACE;
+    const sv::DevInfo *d = sv::dev_info();
+    if (!d) return SPEC_ERR_CUDA;
+    const int esz = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+    const bool vec = ((size_t)V * (size_t)esz) % 16u == 0;
+    sv::Params P{};
+    P.tgt = static_cast<const char *>(draft_logits);  // only draft rows are listed
+    P.drf = static_cast<const char *>(draft_logits);
+    P.temperature = temperature;
+    P.B = B;
+    P.K = K;
+    P.V = V;
+    P.nchunk = (int)sv::nchunk_for(V, dtype);
+    P.npart = (int)sv::npart_for(V, dtype);
+    P.nslot = 2 * K + 1;
+    P.k0 = 0;
+    P.k1 = K;
+    char *ws = static_cast<char *>(workspace);
+    P.row_count = reinterpret_cast<int *>(ws + L.row_count);
+    P.rows = reinterpret_cast<int4 *>(ws + L.rows);
+    P.part = reinterpret_cast<float4 *>(ws + L.part);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    sv::sv_conf_rows<<<1, sv::kPrepThreads, 0, s>>>(P);
+    const int g1 = d->sms * d->occ_p1[dtype == SPEC_DTYPE_BF16 ? sv::kBF16 : sv::kF32][vec ? 1 : 0];
+    if (dtype == SPEC_DTYPE_BF16) {
+        if (vec) sv::launch_dependent(sv::sv_pass1<sv::kBF16, true>, g1, sv::kP1Warps * 32, sv::kP1Smem, s, P);
+        else sv::launch_dependent(sv::sv_pass1<sv::kBF16, false>, g1, sv::kP1Warps * 32, 0, s, P);
+    } else {
+        if (vec) sv::launch_dependent(sv::sv_pass1<sv::kF32, true>, g1, sv::kP1Warps * 32, sv::kP1Smem, s, P);
+        else sv::launch_dependent(sv::sv_pass1<sv::kF32, false>, g1, sv::kP1Warps * 32, 0, s, P);
+    }
+    const long long rows = (long long)B * K;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((rows + sv::kWarps - 1) / sv::kWarps));
+    cfg.blockDim = dim3(sv::kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, sv::sv_conf_out, P, maxprob);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status_t spec_schedule_budget(const float *draft_maxprob, int B, int K, long long budget,
+                                   int32_t *verify_len, void *stream) {
+    if (B < 1 || B >= (1 << 24) || K < 1 || K > SPEC_MAX_K) return SPEC_ERR_INVALID_ARG;
+    if (!draft_maxprob || !verify_len) return SPEC_ERR_INVALID_ARG;
+    if ((long long)B * K > sv::kBudgetMaxN) return SPEC_ERR_UNSUPPORTED;
+    sv::sv_schedule_budget<<<1, sv::kBudgetThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        draft_maxprob, B, K, budget, verify_len);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 spec_status_t spec_schedule_len(const float *draft_maxprob, float threshold, int B, int K,
