@@ -308,10 +308,22 @@ def run_ours(args, world, rank, local):
         (inp["target"].clone(), inp["draft"].clone()) for _ in range(ncopies - 1)]
 
     ee = args.early_exit
+    chain = args.chain
+    conf = torch.empty((B, K), dtype=torch.float32, device=dev)
+    if chain:  # confidences, budgeted schedule and verification, all on the device
+        vlen = torch.empty((B,), dtype=torch.int32, device=dev)
+        sv.draft_confidence(inp["draft"], inp["temperature"], out=conf, verifier=verifier)
+        sv.schedule_budget(conf, chain * B, out=vlen)
+        torch.cuda.synchronize()
+        positions = workloads.verified_positions(vlen)
+        alg_bytes = workloads.algorithmic_bytes(inp["temperature"], vlen, V, esz)
 
     def step(i):
         tgt, drf = copies[i % ncopies]
-        if scheduled:
+        if chain:
+            sv.draft_confidence(drf, inp["temperature"], out=conf, verifier=verifier)
+            sv.schedule_budget(conf, chain * B, out=vlen)
+        elif scheduled:
             sv.schedule_len(inp["draft_maxprob"], inp["threshold"], out=vlen)
         verifier(tgt, drf, inp["tokens"], vlen, inp["temperature"],
                  inp["seed"], out_tokens=out_tokens, accept_len=accept_len, early_exit=ee)
@@ -413,7 +425,7 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_peak()
     achieved = read_bytes / kern_avg_s / 1e9
     traffic, _ = recorded_traffic("c%d" % cfg) if not ee else (None, None)
-    launches = (sv.kernels_per_verify() + (1 if scheduled else 0)) * args.steps  # timed region 1
+    launches = (sv.kernels_per_verify() + (4 if chain else (1 if scheduled else 0))) * args.steps  # timed region 1
 
     result = {
         "metric": "verified draft positions/s",
@@ -443,8 +455,10 @@ def run_ours(args, world, rank, local):
                        "second (events bracket it, %.4f ms per step there)"
                        % (sum(step_k_ms) / len(step_k_ms))),
             "parallelism": "replicas" if world > 1 else "single GPU",
-            "mode": ("early exit, first wave %d positions (%d logit bytes read per step)"
-                     % (ee, read_bytes)) if ee else "single pass",
+            "mode": (("early exit, first wave %d positions (%d logit bytes read per step)"
+                      % (ee, read_bytes)) if ee else "single pass") + (
+                     ("; confidences from the draft logits (%d more bytes read), budget of %d "
+                      "positions per request" % (B * K * V * esz, chain)) if chain else ""),
         },
         "roofline": {
             "bound": "hbm",
@@ -522,6 +536,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--chain", type=int, default=0,
+                    help="per step: draft confidences, a budget of N positions per request, "
+                         "then verification (N = the value given)")
     ap.add_argument("--early-exit", type=int, default=0,
                     help="verify positions [0, W) first, then the rest for open requests")
     args = ap.parse_args(argv)
