@@ -121,6 +121,9 @@ __device__ __forceinline__ int wave_slot(int r, int nt, int k0, int K) {
 
 constexpr int kPrepThreads = 1024;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded wait: 2 s
+// Limit of the waits for bulk copies (diagnostics may lower it; the waits that
+// drain a warp's copies after a give-up always use kWaitLimitNs).
+__constant__ unsigned long long c_wait_ns = kWaitLimitNs;
 
 __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
     __shared__ int warp_tot[kPrepThreads / 32];
@@ -438,8 +441,9 @@ __global__ void __launch_bounds__(kP1Warps * 32, 1) sv_pass1(Params P) {
         StageDesc d;
         if (VEC) {
             const int s = (int)(k % kStages);
-            if (!mbar_wait_bounded(reinterpret_cast<uint64_t *>(&bar[s]), (k / kStages) & 1u,
-                                   kWaitLimitNs)) {
+            const bool ok = mbar_wait_bounded(reinterpret_cast<uint64_t *>(&bar[s]), (k / kStages) & 1u,
+                                              c_wait_ns);
+            if (!__all_sync(0xFFFFFFFFu, ok)) {  // the warp gives up together
                 failed = true;
                 break;
             }
@@ -848,8 +852,9 @@ __global__ void __launch_bounds__(kSWarps * 32, kSMinBlocks) sv_sample(Params P)
         int b, c, nvec;
         if (VEC) {
             const int s = (int)(k % kSStages);
-            if (!mbar_wait_bounded(reinterpret_cast<uint64_t *>(&bar[s]), (k / kSStages) & 1u,
-                                   kWaitLimitNs)) {
+            const bool ok = mbar_wait_bounded(reinterpret_cast<uint64_t *>(&bar[s]),
+                                              (k / kSStages) & 1u, c_wait_ns);
+            if (!__all_sync(0xFFFFFFFFu, ok)) {  // the warp gives up together
                 failed = true;
                 break;
             }
@@ -1690,6 +1695,11 @@ void spec_profile_events(void *ev_start, void *ev_end) {
 }
 
 int spec_verify_kernel_count(void) { return sv::kKernelsPerVerify; }
+
+spec_status_t spec_debug_set_wait_limit(unsigned long long limit_ns) {
+    const unsigned long long v = limit_ns == ~0ull ? sv::kWaitLimitNs : limit_ns;
+    return cudaMemcpyToSymbol(sv::c_wait_ns, &v, sizeof v) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
 
 const char *spec_status_str(spec_status_t status) {
     switch (status) {
