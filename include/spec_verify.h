@@ -258,15 +258,15 @@ spec_status_t spec_verify_noalloc(const void *target_logits, const void *draft_l
                                   int32_t *accept_len, uint32_t *dev_status, void *stream);
 
 /*
- * spec_debug_set_wait_limit -- diagnostics only: the time limit, in
- * nanoseconds, of the device waits for bulk copies in later calls on the
- * current device (default 2 s).  0 makes every such wait that is not already
- * satisfied give up at once, so a call reports SPEC_DEV_TIMEOUT (its outputs are
- * then undefined but in range; the waits that let a warp's copies land before
- * it exits keep the 2 s limit).  ~0ull restores the default.  No counterpart
- * on the pages: it exercises the failure path of the bounded waits.
+ * spec_debug_force_wait_timeout -- diagnostics only: while enabled (1), every
+ * warp of the bulk-copy kernels in later spec_verify calls (any device) first
+ * waits on a barrier nothing completes; that bounded wait runs out after 1 ms
+ * and the warp gives up as on a real timeout: SPEC_DEV_TIMEOUT in the status
+ * word, its copies in flight drained (with the 2 s limit), its items skipped
+ * (outputs then undefined but in range).  0 turns it off.  No counterpart on
+ * the pages: it exercises the failure path of the bounded waits.
  */
-spec_status_t spec_debug_set_wait_limit(unsigned long long limit_ns);
+spec_status_t spec_debug_force_wait_timeout(int enable);
 
 /* Static description of a status code. */
 const char *spec_status_str(spec_status_t status);

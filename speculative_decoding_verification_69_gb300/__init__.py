@@ -68,8 +68,8 @@ def load_library():
     L.spec_profile_events.restype = None
     L.spec_verify_kernel_count.argtypes = []
     L.spec_verify_kernel_count.restype = ctypes.c_int
-    L.spec_debug_set_wait_limit.argtypes = [ctypes.c_ulonglong]
-    L.spec_debug_set_wait_limit.restype = ctypes.c_int
+    L.spec_debug_force_wait_timeout.argtypes = [ctypes.c_int]
+    L.spec_debug_force_wait_timeout.restype = ctypes.c_int
     L.spec_status_str.argtypes = [ctypes.c_int]
     L.spec_status_str.restype = ctypes.c_char_p
     _lib = L
@@ -80,7 +80,7 @@ def exported_symbols():
     return ["spec_verify_workspace_bytes", "spec_verify", "spec_verify_debug",
             "spec_verify_early_exit", "spec_draft_confidence", "spec_schedule_budget",
             "spec_schedule_len", "spec_verify_noalloc",
-            "spec_profile_events", "spec_debug_set_wait_limit",
+            "spec_profile_events", "spec_debug_force_wait_timeout",
             "spec_verify_kernel_count", "spec_status_str"]
 
 
@@ -117,9 +117,9 @@ def profile_events(start=None, end=None):
         L.spec_profile_events(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(end.cuda_event))
 
 
-def set_wait_limit(ns=None):
-    """Diagnostics: limit of the device waits for bulk copies (None: the default)."""
-    _check(load_library().spec_debug_set_wait_limit(0xFFFFFFFFFFFFFFFF if ns is None else int(ns)))
+def force_wait_timeout(enable: bool):
+    """Diagnostics: make the bounded waits of later calls run out (see the header)."""
+    _check(load_library().spec_debug_force_wait_timeout(1 if enable else 0))
 
 
 def kernels_per_verify() -> int:

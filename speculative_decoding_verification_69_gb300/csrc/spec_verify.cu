@@ -121,9 +121,17 @@ __device__ __forceinline__ int wave_slot(int r, int nt, int k0, int K) {
 
 constexpr int kPrepThreads = 1024;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded wait: 2 s
-// Limit of the waits for bulk copies (diagnostics may lower it; the waits that
-// drain a warp's copies after a give-up always use kWaitLimitNs).
-__constant__ unsigned long long c_wait_ns = kWaitLimitNs;
+// Diagnostics: the DIAG instantiations of the bulk-copy kernels (launched only
+// while the switch is on) make every warp first wait on a barrier nothing
+// completes; that wait runs out after kDiagWaitNs and the warp gives up as on
+// a real timeout (status bit, its copies drained, no items).
+static bool g_diag_timeout = false;
+constexpr unsigned long long kDiagWaitNs = 1000000ull;  // 1 ms
+
+// The diagnostic wait of one warp: true when the warp must give up.
+__device__ __forceinline__ bool diag_wait_runs_out(uint64_t *never) {
+    return !__all_sync(0xFFFFFFFFu, mbar_wait_bounded(never, 0u, kDiagWaitNs));
+}
 
 __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
     __shared__ int warp_tot[kPrepThreads / 32];
@@ -238,6 +246,7 @@ struct P1Shared {
     uint4 buf[kP1Warps][kStages][kP1Vecs];
     StageDesc desc[kP1Warps][kStages];
     unsigned long long bar[kP1Warps][kStages];
+    unsigned long long never[kP1Warps];  // diagnostics: a barrier nothing completes
 };
 
 // Lane maximum of 8 vectors (vectors at or past nvec - q0 excluded unless FULL).
@@ -364,7 +373,7 @@ __device__ __forceinline__ float4 warp_partial(const LaneStat &st, bool greedy, 
 // ring and reads each stage in 4 KiB sub-blocks; the row metadata of 32 items
 // at a time is gathered across the lanes, so neither the issue nor the
 // consumption of an item waits on a global load.
-template <int DT, bool VEC>
+template <int DT, bool VEC, bool DIAG = false>
 __global__ void __launch_bounds__(kP1Warps * 32, 1) sv_pass1(Params P) {
     constexpr int EPV = Fmt<DT>::kEPV;
     constexpr int ESZ = Fmt<DT>::kESZ;
@@ -377,6 +386,7 @@ __global__ void __launch_bounds__(kP1Warps * 32, 1) sv_pass1(Params P) {
     unsigned long long *bar = sh.bar[warp];
     if (VEC && lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(reinterpret_cast<uint64_t *>(&bar[s]), 1);
+        mbar_init(reinterpret_cast<uint64_t *>(&sh.never[warp]), 1);
         fence_mbar_init();
     }
     __syncwarp();
@@ -436,13 +446,14 @@ __global__ void __launch_bounds__(kP1Warps * 32, 1) sv_pass1(Params P) {
         for (uint32_t k = 0; k < (uint32_t)kStages && k < nk; ++k) issue(k);
     uint32_t k = 0;
     bool failed = false;
-    for (; k < nk; ++k) {
+    if (VEC && DIAG) failed = diag_wait_runs_out(reinterpret_cast<uint64_t *>(&sh.never[warp]));
+    if (!failed) for (; k < nk; ++k) {
         LaneStat st{-INFINITY, 0.f, INT_MAX};
         StageDesc d;
         if (VEC) {
             const int s = (int)(k % kStages);
             const bool ok = mbar_wait_bounded(reinterpret_cast<uint64_t *>(&bar[s]), (k / kStages) & 1u,
-                                              c_wait_ns);
+                                              kWaitLimitNs);
             if (!__all_sync(0xFFFFFFFFu, ok)) {  // the warp gives up together
                 failed = true;
                 break;
@@ -767,13 +778,14 @@ __device__ __forceinline__ void sample_masses(const uint4 (&vt)[kVecPerLane],
 
 constexpr int kSWarps = 2;      // warps per CTA of the sampler pass
 constexpr int kSStages = 1;     // stages per warp; a stage holds a target and a draft chunk
-constexpr int kSMinBlocks = 1;  // CTAs per SM the register budget is cut for
+constexpr int kSMinBlocks = 8;  // CTAs per SM the register budget is cut for (16 warps)
 
 struct SShared {
     uint4 buf[kSWarps][kSStages][2 * kChunkBytes / 16];
     SampInfo info[kSWarps][kSStages];
     int item_b[kSWarps][kSStages], item_c[kSWarps][kSStages], item_nvec[kSWarps][kSStages];
     unsigned long long bar[kSWarps][kSStages];
+    unsigned long long never[kSWarps];  // diagnostics: a barrier nothing completes
 };
 
 // Items = (sampled request, 4 KiB chunk) over the list sv_decide built, in
@@ -782,7 +794,7 @@ struct SShared {
 // SampInfo) at most a few times.  Per item it writes the chunk's {D, Bm}; the
 // exact sums are written once per (warp, request) segment, at the segment's
 // last chunk, with zeros at the others.  Same per-warp ring as sv_pass1.
-template <int DT, bool VEC>
+template <int DT, bool VEC, bool DIAG = false>
 __global__ void __launch_bounds__(kSWarps * 32, kSMinBlocks) sv_sample(Params P) {
     constexpr int EPV = Fmt<DT>::kEPV;
     constexpr int ESZ = Fmt<DT>::kESZ;
@@ -793,6 +805,7 @@ __global__ void __launch_bounds__(kSWarps * 32, kSMinBlocks) sv_sample(Params P)
     unsigned long long *bar = sh.bar[warp];
     if (VEC && lane == 0) {
         for (int s = 0; s < kSStages; ++s) mbar_init(reinterpret_cast<uint64_t *>(&bar[s]), 1);
+        mbar_init(reinterpret_cast<uint64_t *>(&sh.never[warp]), 1);
         fence_mbar_init();
     }
     __syncwarp();
@@ -846,14 +859,15 @@ __global__ void __launch_bounds__(kSWarps * 32, kSMinBlocks) sv_sample(Params P)
     FF seg_t{0.f, 0.f}, seg_d{0.f, 0.f};  // exact sums of the current request segment
     uint32_t k = 0;
     bool failed = false;
-    for (; k < nk; ++k) {
+    if (VEC && DIAG) failed = diag_wait_runs_out(reinterpret_cast<uint64_t *>(&sh.never[warp]));
+    if (!failed) for (; k < nk; ++k) {
         uint4 vt[kVecPerLane], vd[kVecPerLane];
         SampInfo si;
         int b, c, nvec;
         if (VEC) {
             const int s = (int)(k % kSStages);
             const bool ok = mbar_wait_bounded(reinterpret_cast<uint64_t *>(&bar[s]),
-                                              (k / kSStages) & 1u, c_wait_ns);
+                                              (k / kSStages) & 1u, kWaitLimitNs);
             if (!__all_sync(0xFFFFFFFFu, ok)) {  // the warp gives up together
                 failed = true;
                 break;
@@ -1360,7 +1374,11 @@ static bool setup_kernels(DevInfo &d) {
     if (VEC && (cudaFuncSetAttribute(sv_pass1<DT, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)smem1) != cudaSuccess ||
                 cudaFuncSetAttribute(sv_sample<DT, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem2) != cudaSuccess))
+                                     (int)smem2) != cudaSuccess ||
+                cudaFuncSetAttribute(sv_pass1<DT, VEC, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1) != cudaSuccess ||
+                cudaFuncSetAttribute(sv_sample<DT, VEC, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2) != cudaSuccess))
         return false;
     int o = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sv_pass1<DT, VEC>, kP1Warps * 32, smem1) !=
@@ -1419,8 +1437,8 @@ static void launch_all(const Params &P, const DevInfo &d, cudaStream_t s) {
     // the stream, so the workspace of a previous call is free again.
     sv_prep<<<1, kPrepThreads, 0, s>>>(P);
     if (g_prof_start) cudaEventRecord(g_prof_start, s);
-    launch_dependent(sv_pass1<DT, VEC>, d.sms * d.occ_p1[DT][VEC], kP1Warps * 32,
-                     VEC ? kP1Smem : 0, s, P);
+    launch_dependent(g_diag_timeout ? sv_pass1<DT, VEC, true> : sv_pass1<DT, VEC>,
+                     d.sms * d.occ_p1[DT][VEC], kP1Warps * 32, VEC ? kP1Smem : 0, s, P);
     if (g_prof_end) cudaEventRecord(g_prof_end, s);
     launch_dependent(sv_decide<DT>, P.B, kThreads, 0, s, P);
     // the sampled requests are known only on the device: enough warps for all
@@ -1428,7 +1446,8 @@ static void launch_all(const Params &P, const DevInfo &d, cudaStream_t s) {
     long long g2 = (long long)d.sms * d.occ_sample[DT][VEC];
     const long long g2_need = ((long long)P.B * P.nchunk + kSWarps - 1) / kSWarps;
     if (g2 > g2_need) g2 = g2_need;
-    launch_dependent(sv_sample<DT, VEC>, (int)g2, kSWarps * 32, VEC ? kSSmem : 0, s, P);
+    launch_dependent(g_diag_timeout ? sv_sample<DT, VEC, true> : sv_sample<DT, VEC>, (int)g2,
+                     kSWarps * 32, VEC ? kSSmem : 0, s, P);
     launch_dependent(sv_find<DT, VEC>, (P.B + kFindWarps - 1) / kFindWarps, kFindWarps * 32, 0, s,
                      P);
 }
@@ -1696,9 +1715,9 @@ void spec_profile_events(void *ev_start, void *ev_end) {
 
 int spec_verify_kernel_count(void) { return sv::kKernelsPerVerify; }
 
-spec_status_t spec_debug_set_wait_limit(unsigned long long limit_ns) {
-    const unsigned long long v = limit_ns == ~0ull ? sv::kWaitLimitNs : limit_ns;
-    return cudaMemcpyToSymbol(sv::c_wait_ns, &v, sizeof v) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+spec_status_t spec_debug_force_wait_timeout(int enable) {
+    sv::g_diag_timeout = enable != 0;
+    return SPEC_OK;
 }
 
 const char *spec_status_str(spec_status_t status) {

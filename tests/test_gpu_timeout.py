@@ -1,8 +1,9 @@
-"""Failure path of the bounded device waits, without a GPU fault: with the wait
-limit at 0 every wait for a bulk copy that has not landed gives up at once; the
-call must report SPEC_DEV_TIMEOUT in the status word (the warps still let their
-copies land before exiting), and the next call with the default limit must be
-correct again (the context stays usable)."""
+"""Failure path of the bounded device waits, without a GPU fault: with the
+diagnostic switch on, every warp of the bulk-copy kernels waits on a barrier
+nothing completes; the wait runs out and the warp gives up as on a real
+timeout.  The call must report SPEC_DEV_TIMEOUT in the status word (the warps
+still let their copies land before exiting), and the next call must be correct
+again (the context stays usable)."""
 import numpy as np
 import pytest
 import torch
@@ -20,12 +21,12 @@ def test_wait_timeout_is_reported_and_recoverable():
     inp = workloads.make_inputs(1, rep=17, B=16)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     try:
-        sv.set_wait_limit(0)
+        sv.force_wait_timeout(True)
         out, acc = sv.verify(inp["target"], inp["draft"], inp["tokens"], inp["verify_len"],
                              inp["temperature"], inp["seed"], dev_status=st)
         torch.cuda.synchronize()
     finally:
-        sv.set_wait_limit(None)
+        sv.force_wait_timeout(False)
     assert int(st.item()) & sv.DEV_TIMEOUT
     acc = acc.cpu().numpy()
     assert ((acc >= 0) & (acc <= 8)).all()          # undefined but in range
@@ -35,3 +36,27 @@ def test_wait_timeout_is_reported_and_recoverable():
     h = host_inputs(inp)
     ng, ns, nu, nsamp, nflag = compare(gpu, oracle_run(h, idx), h, idx)
     assert ng == 0 and nu == 0
+
+
+@pytest.mark.parametrize("cfg,ee", [(1, 0), (4, 0), (2, 4)])
+def test_poisoned_workspace_and_outputs(cfg, ee):
+    """Every workspace byte set to 0xFF (NaN floats, -1 ints) and the outputs
+    pre-filled with garbage: the results must equal a clean run's, and every
+    output element must be written (no read of an unwritten workspace byte,
+    no output slot left over)."""
+    import speculative_decoding_verification_69_gb300 as sv
+    inp = workloads.make_inputs(cfg, rep=23, B=64)
+    B, K = inp["tokens"].shape
+    clean = sv.Verifier()
+    o1, a1 = clean(inp["target"], inp["draft"], inp["tokens"], inp["verify_len"],
+                   inp["temperature"], inp["seed"], early_exit=ee)
+    v = sv.Verifier()
+    ws, n = v.workspace(B, K, inp["target"].shape[2], inp["target"].dtype, inp["target"].device)
+    ws.fill_(0xFF)
+    o2 = torch.full((B, K + 1), 123456, dtype=torch.int32, device="cuda")
+    a2 = torch.full((B,), -99, dtype=torch.int32, device="cuda")
+    v(inp["target"], inp["draft"], inp["tokens"], inp["verify_len"], inp["temperature"],
+      inp["seed"], out_tokens=o2, accept_len=a2, early_exit=ee)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(a1, a2)
+    assert (o2 != 123456).all() and (a2 >= 0).all()
