@@ -63,6 +63,9 @@ def lib():
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, i32p, i32p, f64p, f64p, u32p]
         L.svo_schedule_len.argtypes = [f32p, ctypes.c_float, ctypes.c_int, ctypes.c_int, i32p]
+        L.svo_verify_tree_greedy.argtypes = [vp, ctypes.c_int, i32p, i32p, ctypes.c_int, ctypes.c_int,
+                                             i32p, i32p]
+        L.svo_verify_tree_greedy.restype = ctypes.c_int
         L.svo_schedule_budget.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_longlong, i32p]
         L.svo_draft_confidence.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, f32p, f64p]
@@ -232,6 +235,22 @@ def schedule_len(draft_maxprob, threshold):
     lib().svo_schedule_len(_ptr(mp, ctypes.c_float), float(np.float32(threshold)), B, K,
                            _ptr(out, ctypes.c_int32))
     return out
+
+
+def verify_tree_greedy(target, parent, token):
+    """Greedy verification of one candidate tree: target [N, V] (row n predicts
+    the token after node n), parent [N] (parent[0] ignored), token [N].
+    Returns (out_tokens [N], out_nodes [N], accepted)."""
+    target = np.ascontiguousarray(target)
+    N, V = target.shape
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    token = np.ascontiguousarray(token, dtype=np.int32)
+    ot = np.empty(N, dtype=np.int32)
+    on = np.empty(N, dtype=np.int32)
+    a = lib().svo_verify_tree_greedy(target.ctypes.data, dtype_code(target), _ptr(parent, ctypes.c_int32),
+                                     _ptr(token, ctypes.c_int32), N, V, _ptr(ot, ctypes.c_int32),
+                                     _ptr(on, ctypes.c_int32))
+    return ot, on, a
 
 
 def schedule_budget(draft_maxprob, budget):

@@ -389,6 +389,44 @@ void svo_row_intermediates(const void *row, int dtype, int V, float T, int x, do
     if (x >= 0 && x < V) *px = exp(svo_logit(row, dtype, x) / (double)T - mm) / S;
 }
 
+/* ------------------------------------------------------------- tree (greedy) */
+
+/* Greedy verification of a candidate tree ("speculative decoding от черновика до
+ * проверки" (braintools.ru), Medusa / EAGLE-2 passages: the drafts form a tree of
+ * candidates that the target checks in one pass; "Почему ответ не портится?": at
+ * temperature 0 a draft token is kept when it equals the target's argmax).
+ * Node 0 is the root (the last committed token); node n >= 1 carries token[n]
+ * and parent[n] < n.  Row n of the target logits predicts the token after node
+ * n.  Walk from the root: t = argmax of the current node's row (lowest index);
+ * the next node is the lowest-index child carrying t; without one, t is the
+ * emitted token.  Writes the path's tokens (accepted, then the emitted one) and
+ * node indices, -1 after; returns the number of accepted nodes.  A node whose
+ * parent is not an earlier node belongs to no path. */
+int svo_verify_tree_greedy(const void *target, int dtype, const int32_t *parent,
+                           const int32_t *token, int N, int V, int32_t *out_tokens,
+                           int32_t *out_nodes) {
+    const size_t esz = dtype == SVO_BF16 ? 2 : (dtype == SVO_F64 ? 8 : 4);
+    for (int i = 0; i < N; ++i) {
+        out_tokens[i] = -1;
+        out_nodes[i] = -1;
+    }
+    int cur = 0, depth = 0;
+    for (;;) {
+        const int t = svo_row_argmax((const char *)target + (size_t)cur * V * esz, dtype, V);
+        int next = -1;
+        for (int c = cur + 1; c < N; ++c)
+            if (parent[c] == cur && token[c] == t) {
+                next = c;
+                break;
+            }
+        out_tokens[depth] = t;  /* accepted, or emitted when no child carries it */
+        if (next < 0) return depth;  /* a path has at most N - 1 accepted nodes */
+        out_nodes[depth] = next;
+        cur = next;
+        ++depth;
+    }
+}
+
 /* ------------------------------------------------------------- confidence */
 
 /* Draft confidence of one position: the largest probability of the draft

@@ -477,3 +477,68 @@ def test_draft_confidence_hand_values(oracle):
     assert abs(c[1, 0] - 0.9) < 1e-14 and abs(c[1, 1] - 0.25) < 1e-14
     g = oracle.draft_confidence(d, np.array([0.0, float("nan")], np.float32))
     assert (g == 1.0).all()
+
+
+# ---------------------------------------------------------------- tree verification (greedy)
+
+def test_tree_greedy_hand_case(oracle):
+    """Root argmax 2 -> node 2 (the child carrying 2); node 2's argmax 1 has no
+    child: one accepted node, then token 1.  Siblings carrying the same token:
+    the lowest-index node is taken."""
+    import numpy as np
+    t = np.zeros((5, 6))
+    t[0, 2] = 1; t[1, 3] = 1; t[2, 1] = 1; t[3, 4] = 1; t[4, 5] = 1
+    ot, on, a = oracle.verify_tree_greedy(t, [-1, 0, 0, 1, 2], [0, 3, 2, 3, 1])
+    assert a == 2 and ot.tolist() == [2, 1, 5, -1, -1] and on.tolist() == [2, 4, -1, -1, -1]
+    ot, on, a = oracle.verify_tree_greedy(t, [-1, 0, 0, 0, 2], [0, 2, 2, 3, 1])  # nodes 1, 2 both carry 2
+    assert a == 1 and on.tolist()[:1] == [1] and ot.tolist()[:2] == [2, 3]
+
+
+def test_tree_greedy_chain_is_linear_verification(oracle):
+    """A chain tree (parent[n] = n - 1) is the linear draft: same accepted count
+    and tokens as the (separately pinned) greedy verification of K = N - 1
+    drafts on the same target rows."""
+    import numpy as np
+    rng = np.random.default_rng(8)
+    for trial in range(40):
+        N, V = int(rng.integers(1, 10)), int(rng.integers(2, 7))
+        tgt = rng.integers(-2, 3, size=(N, V)).astype(np.float64)
+        tok = rng.integers(0, V, size=N).astype(np.int32)
+        for n in range(1, N):  # make some drafts right
+            if rng.random() < 0.6:
+                tok[n] = int(np.argmax(tgt[n - 1]))
+        ot, on, a = oracle.verify_tree_greedy(tgt, np.arange(-1, N - 1), tok)
+        K = N - 1
+        if K == 0:
+            assert a == 0 and ot[0] == int(np.argmax(tgt[0]))
+            continue
+        r = oracle.verify(tgt[None], np.zeros((1, K, V)), tok[None, 1:], None,
+                          np.zeros(1, np.float32), 1)
+        assert a == r["accept_len"][0]
+        assert ot.tolist() == r["out_tokens"][0].tolist()
+
+
+def test_tree_greedy_matches_valid_set(oracle):
+    """Brute force on random trees: a node is valid when its parent is valid, its
+    token is the argmax of the parent's row and no lower-index sibling carries
+    that token; the valid nodes form one chain and the accepted count is the
+    depth of its deepest node."""
+    import numpy as np
+    rng = np.random.default_rng(9)
+    for trial in range(200):
+        N, V = int(rng.integers(1, 12)), int(rng.integers(2, 5))
+        tgt = rng.integers(-1, 2, size=(N, V)).astype(np.float32)
+        parent = np.array([-1] + [int(rng.integers(0, n)) for n in range(1, N)], np.int32)
+        tok = rng.integers(0, V, size=N).astype(np.int32)
+        am = [int(np.argmax(tgt[n])) for n in range(N)]
+        valid, depth = {0}, {0: 0}
+        for v in range(1, N):
+            u = parent[v]
+            first = min(c for c in range(1, N) if parent[c] == u and tok[c] == tok[v])
+            if u in valid and tok[v] == am[u] and first == v:
+                valid.add(v)
+                depth[v] = depth[u] + 1
+        deepest = max(valid, key=lambda v: depth[v])
+        ot, on, a = oracle.verify_tree_greedy(tgt, parent, tok)
+        assert a == depth[deepest]
+        assert ot[a] == am[deepest]
