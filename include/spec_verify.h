@@ -63,10 +63,12 @@ typedef enum {
 #define SPEC_DEV_BAD_TOKEN 1u /* a draft token outside [0, V): that request's verify
                                  length is cut to the first such position */
 #define SPEC_DEV_BAD_LEN 2u   /* verify_len outside [0, K]: clamped */
+#define SPEC_DEV_BAD_TREE    8u   /* a tree node whose parent is not an earlier node */
 #define SPEC_DEV_TIMEOUT 4u   /* a bounded device-side wait gave up; outputs of the
                                  affected request are undefined */
 
 #define SPEC_MAX_K 32          /* largest supported draft length K */
+#define SPEC_MAX_TREE 64       /* largest candidate tree (nodes, root included) */
 #define SPEC_MAX_V 0x40000000  /* largest supported vocabulary V (2^30) */
 
 /*
@@ -166,6 +168,33 @@ spec_status_t spec_verify_early_exit(const void *target_logits, const void *draf
                                      uint64_t seed, int B, int K, int V, int first_wave,
                                      int32_t *out_tokens, int32_t *accept_len, void *workspace,
                                      size_t workspace_bytes, uint32_t *dev_status, void *stream);
+
+/*
+ * spec_verify_tree_greedy -- greedy verification of a candidate tree
+ * ("speculative decoding от черновика до проверки" (braintools.ru), the Medusa
+ * and EAGLE-2 passages: the draft is a tree of candidates the target checks in
+ * one pass with tree attention; "Почему ответ не портится?": at temperature 0
+ * a draft token is kept when it equals the target's argmax).
+ *   Node 0 of each request is the root (the last committed token); node n >= 1
+ *   carries node_tokens[b, n] and parent[b, n] < n.  target_logits [B, N, V]
+ *   bf16/fp32 device, row n = the target's logits after node n's token (from
+ *   tree attention).  Walk from the root: t = argmax of the current node's row
+ *   (lowest index on ties); the next node is the lowest-index child carrying t;
+ *   without one, t is emitted and the walk ends.
+ *   Outputs (device int32): out_tokens [B, N] = the accepted tokens then the
+ *   emitted one, -1 after; out_nodes [B, N] = the accepted node indices, -1
+ *   after; accept_len [B] = the number of accepted nodes.
+ *   1 <= N <= SPEC_MAX_TREE.  A node whose parent is not an earlier node
+ *   belongs to no path (SPEC_DEV_BAD_TREE).  The workspace is
+ *   spec_tree_workspace_bytes(B, N, V, dtype) bytes.  Errors as spec_verify.
+ *   Sampled (T > 0) tree verification is not provided.
+ */
+size_t spec_tree_workspace_bytes(int B, int N, int V, spec_dtype_t dtype);
+spec_status_t spec_verify_tree_greedy(const void *target_logits, spec_dtype_t dtype,
+                                      const int32_t *parent, const int32_t *node_tokens, int B,
+                                      int N, int V, int32_t *out_tokens, int32_t *out_nodes,
+                                      int32_t *accept_len, void *workspace, size_t workspace_bytes,
+                                      uint32_t *dev_status, void *stream);
 
 /*
  * spec_draft_confidence -- the draft's confidence at every position, as the

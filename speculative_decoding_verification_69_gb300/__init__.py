@@ -19,7 +19,7 @@ from . import _build
 
 SPEC_OK = 0
 DTYPE_F32, DTYPE_BF16 = 0, 1
-DEV_BAD_TOKEN, DEV_BAD_LEN, DEV_TIMEOUT = 1, 2, 4
+DEV_BAD_TOKEN, DEV_BAD_LEN, DEV_TIMEOUT, DEV_BAD_TREE = 1, 2, 4, 8
 MAX_K = 32
 
 _lib = None
@@ -60,6 +60,11 @@ def load_library():
     L.spec_draft_confidence.argtypes = [vp, ctypes.c_int, f32p, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_int, f32p, vp, ctypes.c_size_t, vp]
     L.spec_draft_confidence.restype = ctypes.c_int
+    L.spec_tree_workspace_bytes.argtypes = [ctypes.c_int] * 4
+    L.spec_tree_workspace_bytes.restype = ctypes.c_size_t
+    L.spec_verify_tree_greedy.argtypes = [vp, ctypes.c_int, i32p, i32p, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, i32p, i32p, i32p, vp, ctypes.c_size_t, u32p, vp]
+    L.spec_verify_tree_greedy.restype = ctypes.c_int
     L.spec_schedule_budget.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_longlong, i32p, vp]
     L.spec_schedule_budget.restype = ctypes.c_int
     L.spec_verify_noalloc.argtypes = common[:12] + [u32p, vp]
@@ -78,7 +83,8 @@ def load_library():
 
 def exported_symbols():
     return ["spec_verify_workspace_bytes", "spec_verify", "spec_verify_debug",
-            "spec_verify_early_exit", "spec_draft_confidence", "spec_schedule_budget",
+            "spec_verify_early_exit", "spec_tree_workspace_bytes", "spec_verify_tree_greedy",
+            "spec_draft_confidence", "spec_schedule_budget",
             "spec_schedule_len", "spec_verify_noalloc",
             "spec_profile_events", "spec_debug_force_wait_timeout",
             "spec_verify_kernel_count", "spec_status_str"]
@@ -231,6 +237,29 @@ def draft_confidence(draft, temperature, *, out=None, stream=None, verifier=None
     _check(L.spec_draft_confidence(_ptr(draft), _dtype_code(draft), _ptr(temperature), B, K, V,
                                    _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
     return out
+
+
+def verify_tree_greedy(target, parent, node_tokens, *, dev_status=None, stream=None):
+    """Greedy verification of candidate trees: target [B, N, V] (row n: logits
+    after node n), parent / node_tokens int32 [B, N].  Returns (out_tokens
+    [B, N], out_nodes [B, N], accept_len [B]) on the device."""
+    L = load_library()
+    if target.dim() != 3 or not target.is_cuda or not target.is_contiguous():
+        raise ValueError("target must be a contiguous CUDA tensor [B, N, V]")
+    B, N, V = target.shape
+    for t in (parent, node_tokens):
+        if t.shape != (B, N) or t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("parent and node_tokens must be contiguous int32 CUDA tensors [B, N]")
+    dev = target.device
+    out = torch.empty((B, N), dtype=torch.int32, device=dev)
+    nodes = torch.empty((B, N), dtype=torch.int32, device=dev)
+    acc = torch.empty((B,), dtype=torch.int32, device=dev)
+    n = int(L.spec_tree_workspace_bytes(B, N, V, _dtype_code(target)))
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+    _check(L.spec_verify_tree_greedy(_ptr(target), _dtype_code(target), _ptr(parent),
+                                     _ptr(node_tokens), B, N, V, _ptr(out), _ptr(nodes), _ptr(acc),
+                                     _ptr(ws), ws.numel(), _ptr(dev_status), _stream(stream)))
+    return out, nodes, acc
 
 
 def schedule_budget(draft_maxprob, budget, *, out=None, stream=None):

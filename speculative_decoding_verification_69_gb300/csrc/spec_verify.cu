@@ -1231,6 +1231,70 @@ __global__ void __launch_bounds__(kThreads) sv_conf_out(Params P, float *maxprob
     if (lane == 0) maxprob[row] = out;
 }
 
+// ------------------------------------------------------------------ tree verification (greedy)
+
+// Rows of a greedy tree verification: every node row of every request (the
+// target logits [B, N, V] sit where the target rows 0..K of a K = N - 1 call
+// would).
+__global__ void sv_tree_rows(Params P) {
+    pdl_trigger();
+    const int n = P.K + 1;
+    const long long total = (long long)P.B * n;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x)
+        P.rows[i] = make_int4((int)(i / n), (int)(i % n), 1, 0);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *P.row_count = (int)total;
+}
+
+// Per request: the argmax of every node row from the statistics pass's
+// partials, then the walk from the root -- t = argmax of the current node, the
+// next node is the lowest-index child carrying t, else t is emitted.  A node
+// whose parent is not an earlier node belongs to no path (SPEC_DEV_BAD_TREE).
+__global__ void __launch_bounds__(kThreads) sv_tree_decide(Params P, const int32_t *parent,
+                                                          const int32_t *token,
+                                                          int32_t *out_nodes) {
+    __shared__ int s_amax[SPEC_MAX_TREE];
+    __shared__ int s_par[SPEC_MAX_TREE], s_tok[SPEC_MAX_TREE];
+    const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int N = P.K + 1;
+    for (int i = tid; i < N; i += kThreads) {
+        s_par[i] = parent[(size_t)b * N + i];
+        s_tok[i] = token[(size_t)b * N + i];
+    }
+    pdl_wait();  // partials come from sv_pass1
+    pdl_trigger();
+    for (int n = warp; n < N; n += kWarps) {
+        const float4 rs = combine_row(P, b, n, true, 0.f, lane);
+        if (lane == 0) s_amax[n] = __float_as_int(rs.z);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int32_t *out = P.out_tokens + (size_t)b * N;
+        int32_t *nodes = out_nodes + (size_t)b * N;
+        bool bad = false;
+        for (int c = 1; c < N; ++c) bad |= s_par[c] < 0 || s_par[c] >= c;
+        int cur = 0, depth = 0;
+        for (;;) {
+            const int t = s_amax[cur];
+            int next = -1;
+            for (int c = cur + 1; c < N; ++c)
+                if (s_par[c] == cur && s_tok[c] == t) {
+                    next = c;
+                    break;
+                }
+            out[depth] = t;
+            if (next < 0) break;
+            nodes[depth] = next;
+            cur = next;
+            ++depth;
+        }
+        for (int i = depth + 1; i < N; ++i) out[i] = -1;
+        for (int i = depth; i < N; ++i) nodes[i] = -1;
+        P.accept_len[b] = depth;
+        if (bad && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_BAD_TREE);
+    }
+}
+
 // ------------------------------------------------------------------ load-aware schedule
 
 constexpr int kBudgetThreads = 1024;
@@ -1650,6 +1714,74 @@ spec_status_t spec_draft_confidence(const void *draft_logits, spec_dtype_t dtype
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaLaunchKernelEx(&cfg, sv::sv_conf_out, P, maxprob);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+size_t spec_tree_workspace_bytes(int B, int N, int V, spec_dtype_t dtype) {
+    if (N < 1 || N > SPEC_MAX_TREE || B < 1 || B >= (1 << 24) || V < 2 || V > SPEC_MAX_V) return 0;
+    if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return 0;
+    return sv::layout(B, N - 1 > 0 ? N - 1 : 1, V, dtype).total;
+}
+
+spec_status_t spec_verify_tree_greedy(const void *target_logits, spec_dtype_t dtype,
+                                      const int32_t *parent, const int32_t *node_tokens, int B,
+                                      int N, int V, int32_t *out_tokens, int32_t *out_nodes,
+                                      int32_t *accept_len, void *workspace, size_t workspace_bytes,
+                                      uint32_t *dev_status, void *stream) {
+    if (N < 1 || N > SPEC_MAX_TREE || B < 1 || B >= (1 << 24) || V < 2 || V > SPEC_MAX_V)
+        return SPEC_ERR_INVALID_ARG;
+    const int K = N - 1 > 0 ? N - 1 : 1;  // the workspace layout of K = N - 1 holds N target rows
+    if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
+    if (!sv::items_fit(B, K, V, dtype)) return SPEC_ERR_UNSUPPORTED;
+    if (!target_logits || !parent || !node_tokens || !out_tokens || !out_nodes || !accept_len)
+        return SPEC_ERR_INVALID_ARG;
+    if ((uintptr_t)target_logits & 15u) return SPEC_ERR_INVALID_ARG;
+    const sv::Layout L = sv::layout(B, K, V, dtype);
+    if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u))
+        return SPEC_ERR_WORKSPACE;
+    const sv::DevInfo *d = sv::dev_info();
+    if (!d) return SPEC_ERR_CUDA;
+    const int esz = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+    const bool vec = ((size_t)V * (size_t)esz) % 16u == 0;
+    sv::Params P{};
+    P.tgt = static_cast<const char *>(target_logits);
+    P.drf = static_cast<const char *>(target_logits);  // no draft rows are listed
+    P.B = B;
+    P.K = N - 1;  // row n of the tree is target slot n
+    P.V = V;
+    P.nchunk = (int)sv::nchunk_for(V, dtype);
+    P.npart = (int)sv::npart_for(V, dtype);
+    P.nslot = 2 * K + 1;
+    P.k0 = 0;
+    P.k1 = P.K;
+    P.out_tokens = out_tokens;
+    P.accept_len = accept_len;
+    P.dev_status = dev_status;
+    char *ws = static_cast<char *>(workspace);
+    P.row_count = reinterpret_cast<int *>(ws + L.row_count);
+    P.rows = reinterpret_cast<int4 *>(ws + L.rows);
+    P.part = reinterpret_cast<float4 *>(ws + L.part);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const long long rows = (long long)B * N;
+    sv::sv_tree_rows<<<(unsigned)((rows + 255) / 256 < 1024 ? (rows + 255) / 256 : 1024), 256, 0, s>>>(P);
+    const int g1 = d->sms * d->occ_p1[dtype == SPEC_DTYPE_BF16 ? sv::kBF16 : sv::kF32][vec ? 1 : 0];
+    if (dtype == SPEC_DTYPE_BF16) {
+        if (vec) sv::launch_dependent(sv::sv_pass1<sv::kBF16, true>, g1, sv::kP1Warps * 32, sv::kP1Smem, s, P);
+        else sv::launch_dependent(sv::sv_pass1<sv::kBF16, false>, g1, sv::kP1Warps * 32, 0, s, P);
+    } else {
+        if (vec) sv::launch_dependent(sv::sv_pass1<sv::kF32, true>, g1, sv::kP1Warps * 32, sv::kP1Smem, s, P);
+        else sv::launch_dependent(sv::sv_pass1<sv::kF32, false>, g1, sv::kP1Warps * 32, 0, s, P);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)B);
+    cfg.blockDim = dim3(sv::kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, sv::sv_tree_decide, P, parent, node_tokens, out_nodes);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
