@@ -282,6 +282,77 @@ def prepare(cfg, rank, device):
     return inp
 
 
+def run_tree(args, world, rank, local):
+    """Greedy candidate-tree verification: B requests of N-node trees whose
+    node rows are the workload's target logits (N = --tree); half the nodes
+    carry their parent's argmax, so paths go deep.  Positions = candidate
+    nodes verified (N - 1 per request)."""
+    import numpy as np
+    import speculative_decoding_verification_69_gb300 as sv
+    sv.load_library()
+    dev = torch.device("cuda", local)
+    N = args.tree
+    inp = workloads.make_inputs(args.config, rep=rank, device=dev, K=N - 1)
+    tgt = inp["target"]
+    B, _, V = tgt.shape
+    esz = tgt.element_size()
+    rng = np.random.default_rng(workloads.seed_for(args.config, rank))
+    am = tgt.float().argmax(dim=-1).cpu().numpy() if N > 1 else np.zeros((B, 1), np.int64)
+    parent = np.full((B, N), -1, np.int32)
+    tok = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for n in range(1, N):
+            p = int(rng.integers(0, n))
+            parent[b, n] = p
+            tok[b, n] = am[b, p] if rng.random() < 0.5 else int(rng.integers(0, V))
+    parent = torch.from_numpy(parent).to(dev)
+    tok = torch.from_numpy(tok).to(dev)
+    alg_bytes = B * N * V * esz
+    l2_bytes = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    ncopies = logit_copies(alg_bytes, l2_bytes)
+    copies = [tgt] + [tgt.clone() for _ in range(ncopies - 1)]
+    stream = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        sv.verify_tree_greedy(copies[i % ncopies], parent, tok)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    clocks.start()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        sv.verify_tree_greedy(copies[(args.warmup + i) % ncopies], parent, tok)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.perf_counter()
+    clocks.mark(t0, t1 + 0.05)
+    clk = clocks.stop()
+    total_s = sum(a.elapsed_time(b) for a, b in ev) / 1e3
+    total_s_max = max_over_ranks(total_s, world)
+    positions = sum_over_ranks(B * (N - 1) * args.steps, world)
+    peak, peak_kind = measured_peak()
+    step_s = total_s_max / args.steps
+    return {
+        "metric": "verified draft positions/s", "value": positions / total_s_max,
+        "unit": "positions/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if tgt.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded logits and trees; no datasets or trained weights)",
+        "config": {"workload": workloads.NAMES[args.config] + " target rows as %d-node trees" % N,
+                   "B": B, "N": N, "V": V, "mode": "greedy tree verification",
+                   "logit_bytes_per_step": alg_bytes,
+                   "logits_GBps": alg_bytes / step_s / 1e9,
+                   "l2": "inputs larger than L2: %d copies cycled; no flush" % ncopies},
+        "roofline": {"bound": "hbm", "kernel": "whole step", "achieved": alg_bytes / step_s / 1e9,
+                     "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
+                     "frac": alg_bytes / step_s / 1e9 / peak, "traffic": None},
+        "e2e": None, "gpu_launches": 3 * args.steps, "clocks": clk,
+    }
+
+
 def run_ours(args, world, rank, local):
     import speculative_decoding_verification_69_gb300 as sv
     sv.load_library()
@@ -539,6 +610,8 @@ def main(argv=None):
     ap.add_argument("--chain", type=int, default=0,
                     help="per step: draft confidences, a budget of N positions per request, "
                          "then verification (N = the value given)")
+    ap.add_argument("--tree", type=int, default=0,
+                    help="greedy verification of N-node candidate trees instead of chains")
     ap.add_argument("--early-exit", type=int, default=0,
                     help="verify positions [0, W) first, then the rest for open requests")
     args = ap.parse_args(argv)
@@ -554,7 +627,7 @@ def main(argv=None):
             print(json.dumps(run_reference(args, world, 0, local)), flush=True)
         return 0
     world, rank, local = dist_setup(args.gpus)
-    res = run_ours(args, world, rank, local)
+    res = run_tree(args, world, rank, local) if args.tree else run_ours(args, world, rank, local)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
