@@ -7,7 +7,7 @@
 //                 sampled) -- all drafts are scored from one target pass and
 //                 checked together ("speculative decoding от черновика до
 //                 проверки" (braintools.ru), "Как это работает", steps 2-3).
-//   2. sv_pass1   the logit stream: every needed row is read once, 4 KiB per
+//   2. sv_pass1   the logit stream: every needed row is read once, 8 KiB per
 //                 warp item through a per-warp ring of bulk copies into shared
 //                 memory; per item the exact max and either the lowest-index
 //                 argmax (greedy) or the sum of 2^((z - m) log2(e)/T).
@@ -20,8 +20,12 @@
 //                 residual masses of max(0, p - q) (after a rejection) or of p
 //                 (bonus), with exact normalisers.
 //   5. sv_find    per request: inverse CDF over chunks, then over the chosen
-//                 chunk's vectors and elements.
-// spec_schedule_len is one more small kernel (sv_schedule).
+//                 chunk's elements.
+// spec_verify_early_exit runs kernels 1-3 once per wave of positions, then 4-5.
+// spec_verify_tree_greedy, spec_draft_confidence, spec_schedule_len and
+// spec_schedule_budget reuse the statistics pass or are small kernels of
+// their own (sv_tree_rows / sv_tree_decide, sv_conf_rows / sv_conf_out,
+// sv_schedule, sv_schedule_budget).
 #include "spec_verify.h"
 #include "sv_common.cuh"
 
