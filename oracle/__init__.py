@@ -66,6 +66,12 @@ def lib():
         L.svo_verify_tree_greedy.argtypes = [vp, ctypes.c_int, i32p, i32p, ctypes.c_int, ctypes.c_int,
                                              i32p, i32p]
         L.svo_verify_tree_greedy.restype = ctypes.c_int
+        L.svo_verify_tree_u.argtypes = [vp, vp, ctypes.c_int, i32p, i32p, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_float, f64p, f64p, i32p, i32p, f64p, vp]
+        L.svo_verify_tree_u.restype = ctypes.c_int
+        L.svo_verify_tree_sampled.argtypes = [vp, vp, ctypes.c_int, i32p, i32p, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, f32p, ctypes.c_uint64,
+                                              i32p, i32p, i32p, f64p, f64p]
         L.svo_schedule_budget.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_longlong, i32p]
         L.svo_draft_confidence.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, f32p, f64p]
@@ -251,6 +257,59 @@ def verify_tree_greedy(target, parent, token):
                                      _ptr(token, ctypes.c_int32), N, V, _ptr(ot, ctypes.c_int32),
                                      _ptr(on, ctypes.c_int32))
     return ot, on, a
+
+
+def verify_tree_u(target, draft, parent, token, T, u_acc, u_s):
+    """Sampled verification of one candidate tree with explicit uniforms:
+    target, draft [N, V] (row n: the target / draft distribution after node n),
+    parent, token [N], u_acc [N] (entry c: the uniform of candidate node c;
+    entry 0 unused) and u_s [N] (entry n: the sampling uniform when node n emits)
+    or scalars.  Returns (out_tokens [N], out_nodes [N], accepted)."""
+    target = np.ascontiguousarray(target)
+    N, V = target.shape
+    draft = np.ascontiguousarray(draft, dtype=target.dtype)
+    assert draft.shape == (N, V)
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    token = np.ascontiguousarray(token, dtype=np.int32)
+    u_acc = np.ascontiguousarray(np.broadcast_to(np.asarray(u_acc, dtype=np.float64), (N,)))
+    u_s = np.ascontiguousarray(np.broadcast_to(np.asarray(u_s, dtype=np.float64), (N,)))
+    ot = np.empty(N, dtype=np.int32)
+    on = np.empty(N, dtype=np.int32)
+    work = np.empty(3 * V, dtype=np.float64)
+    a = lib().svo_verify_tree_u(target.ctypes.data, draft.ctypes.data, dtype_code(target),
+                                _ptr(parent, ctypes.c_int32), _ptr(token, ctypes.c_int32), N, V,
+                                float(T), _ptr(u_acc, ctypes.c_double), _ptr(u_s, ctypes.c_double),
+                                _ptr(ot, ctypes.c_int32), _ptr(on, ctypes.c_int32),
+                                _ptr(work, ctypes.c_double), None)
+    return ot, on, a
+
+
+def verify_tree(target, draft, parent, token, temperature, seed):
+    """A batch of candidate trees with the oracle's own Philox (greedy rows take
+    the greedy walk): target, draft [B, N, V]; parent, token [B, N];
+    temperature [B].  Returns dict(out_tokens, out_nodes [B, N], accept_len,
+    accept_margin, cdf_margin [B])."""
+    target = np.ascontiguousarray(target)
+    B, N, V = target.shape
+    draft = np.ascontiguousarray(draft)
+    assert draft.dtype == target.dtype and draft.shape == (B, N, V)
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    token = np.ascontiguousarray(token, dtype=np.int32)
+    assert parent.shape == (B, N) and token.shape == (B, N)
+    temperature = np.ascontiguousarray(temperature, dtype=np.float32)
+    ot = np.empty((B, N), dtype=np.int32)
+    on = np.empty((B, N), dtype=np.int32)
+    al = np.empty(B, dtype=np.int32)
+    am = np.empty(B, dtype=np.float64)
+    cm = np.empty(B, dtype=np.float64)
+    rc = lib().svo_verify_tree_sampled(
+        target.ctypes.data, draft.ctypes.data, dtype_code(target), _ptr(parent, ctypes.c_int32),
+        _ptr(token, ctypes.c_int32), B, N, V, _ptr(temperature, ctypes.c_float),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(ot, ctypes.c_int32), _ptr(on, ctypes.c_int32),
+        _ptr(al, ctypes.c_int32), _ptr(am, ctypes.c_double), _ptr(cm, ctypes.c_double))
+    if rc != 0:
+        raise RuntimeError("oracle tree verification failed (%d)" % rc)
+    return dict(out_tokens=ot, out_nodes=on, accept_len=al, accept_margin=am, cdf_margin=cm)
 
 
 def schedule_budget(draft_maxprob, budget):

@@ -41,7 +41,10 @@
  *     position k cuts the verify length to k;
  *   - schedule: L = number of leading positions whose float32 running product
  *     of draft max-probabilities stays >= threshold (left to right, every
- *     product rounded to float32, no fused multiply-add).
+ *     product rounded to float32, no fused multiply-add);
+ *   - candidate trees: the functions of the two tree sections state their
+ *     readings (the greedy walk; sibling candidates checked in index order
+ *     against successively updated residuals).
  *
  * Random numbers: Philox4x32-10 as published by Salmon, Moraes, Dror and Shaw,
  * "Parallel random numbers: as easy as 1, 2, 3" (SC'11), written here from the
@@ -425,6 +428,134 @@ int svo_verify_tree_greedy(const void *target, int dtype, const int32_t *parent,
         cur = next;
         ++depth;
     }
+}
+
+/* ------------------------------------------------------------- tree (sampled) */
+
+/* Sampled verification of a candidate tree.  The pages give the acceptance rule
+ * for one candidate per position ("Спекулятивный декодинг в проде"
+ * (kiosknews.app), "Правило проверки") and let the drafts form a tree (the
+ * Medusa and EAGLE-2 passages of the braintools.ru page); several children of
+ * one node are checked against successively updated residuals, the
+ * multi-candidate form of the same rule (reading):
+ *   at node u the weights r start as p_u (target row u at T) with normaliser
+ *   Z = 1; each child c of u, in index order, proposes x = token[c] (a token
+ *   outside [0, V) is no candidate) and is accepted iff u_acc[c] * q_u(x) <
+ *   r(x) / Z (q_u = draft row u at T); a rejection replaces r by
+ *   max(0, r / Z - q_u) and Z by its sum (when that sum is 0, r = p_u and
+ *   Z = 1 again).  An accepted child becomes the current node; when no child is
+ *   accepted the emitted token is the inverse CDF of r at u_s[u].
+ * With one child per node this is the linear rule step for step: the first
+ * residual is max(0, p - q) and a node without candidates samples p.  Each
+ * child's proposal drawn independently from q_u keeps the emitted token's law
+ * equal to p_u.  Greedy T: the greedy tree walk.  work holds 3 * V doubles.
+ * Writes the path (tokens, node indices, -1 after) and returns the number of
+ * accepted nodes; diag receives the smallest |u_acc - (r(x)/Z)/q_u(x)| over the
+ * evaluated candidates and the inverse CDF's margin. */
+int svo_verify_tree_u(const void *target, const void *draft, int dtype, const int32_t *parent,
+                      const int32_t *token, int N, int V, float T, const double *u_acc,
+                      const double *u_s, int32_t *out_tokens, int32_t *out_nodes, double *work,
+                      svo_diag *diag) {
+    svo_diag d = {INFINITY, INFINITY, 0u};
+    if (svo_is_greedy(T)) {
+        int a = svo_verify_tree_greedy(target, dtype, parent, token, N, V, out_tokens, out_nodes);
+        if (diag) *diag = d;
+        return a;
+    }
+    for (int i = 0; i < N; ++i) {
+        out_tokens[i] = -1;
+        out_nodes[i] = -1;
+    }
+    const double Td = (double)T;
+    double *p = work, *q = work + V, *r = work + 2 * (size_t)V;
+    int cur = 0, depth = 0;
+    for (;;) {
+        svo_row_softmax(svo_row(target, dtype, (size_t)cur, V), dtype, V, Td, p, NULL, NULL);
+        memcpy(r, p, (size_t)V * sizeof(double));
+        double Z = 1.0;
+        int have_q = 0, next = -1;
+        for (int c = cur + 1; c < N; ++c) {
+            if (parent[c] != cur) continue;
+            const int x = token[c];
+            if (x < 0 || x >= V) continue;
+            if (!have_q) {
+                svo_row_softmax(svo_row(draft, dtype, (size_t)cur, V), dtype, V, Td, q, NULL, NULL);
+                have_q = 1;
+            }
+            const double rx = r[x] / Z;
+            if (q[x] > 0.0) {
+                double gap = fabs(u_acc[c] - rx / q[x]);
+                if (gap < d.accept_margin) d.accept_margin = gap;
+            }
+            if (svo_accept(rx, q[x], u_acc[c])) {
+                next = c;
+                break;
+            }
+            double Zn = 0.0;
+            for (int v = 0; v < V; ++v) {
+                double w = r[v] / Z - q[v];
+                r[v] = w > 0.0 ? w : 0.0;
+                Zn += r[v];
+            }
+            if (Zn == 0.0) {
+                memcpy(r, p, (size_t)V * sizeof(double));
+                Zn = 1.0;
+            }
+            Z = Zn;
+        }
+        if (next < 0) {
+            out_tokens[depth] = svo_inverse_cdf(r, V, u_s[cur], &d.cdf_margin);
+            break;
+        }
+        out_tokens[depth] = token[next];
+        out_nodes[depth] = next;
+        cur = next;
+        ++depth;
+    }
+    if (diag) *diag = d;
+    return depth;
+}
+
+/* A batch of sampled trees with the oracle's own Philox: candidate node c >= 1
+ * of request b takes the acceptance uniform of position c - 1 and node u's
+ * emitted token the sampling uniform of position u, so a chain tree draws the
+ * same numbers as the linear verification.  target and draft [B, N, V];
+ * parent, token [B, N]; outputs [B, N] and per-request accepted counts and
+ * margins. */
+int svo_verify_tree_sampled(const void *target, const void *draft, int dtype,
+                            const int32_t *parent, const int32_t *token, int B, int N, int V,
+                            const float *temperature, uint64_t seed, int32_t *out_tokens,
+                            int32_t *out_nodes, int32_t *accepted, double *accept_margin,
+                            double *cdf_margin) {
+    const size_t esz = svo_esize(dtype);
+    double *work = (double *)malloc(3 * (size_t)V * sizeof(double));
+    double *ua = (double *)malloc((size_t)N * sizeof(double));
+    double *us = (double *)malloc((size_t)N * sizeof(double));
+    if (!work || !ua || !us) {
+        free(work);
+        free(ua);
+        free(us);
+        return -1;
+    }
+    for (int b = 0; b < B; ++b) {
+        ua[0] = 0.0;
+        for (int n = 0; n < N; ++n) {
+            if (n > 0) ua[n] = svo_u_accept(seed, (uint32_t)b, (uint32_t)(n - 1));
+            us[n] = svo_u_sample(seed, (uint32_t)b, (uint32_t)n);
+        }
+        const size_t off = (size_t)b * N;
+        svo_diag d;
+        accepted[b] = svo_verify_tree_u((const char *)target + off * V * esz,
+                                        (const char *)draft + off * V * esz, dtype, parent + off,
+                                        token + off, N, V, temperature[b], ua, us,
+                                        out_tokens + off, out_nodes + off, work, &d);
+        accept_margin[b] = d.accept_margin;
+        cdf_margin[b] = d.cdf_margin;
+    }
+    free(work);
+    free(ua);
+    free(us);
+    return 0;
 }
 
 /* ------------------------------------------------------------- confidence */

@@ -542,3 +542,235 @@ def test_tree_greedy_matches_valid_set(oracle):
         ot, on, a = oracle.verify_tree_greedy(tgt, parent, tok)
         assert a == depth[deepest]
         assert ot[a] == am[deepest]
+
+
+# ---------------------------------------------------------------- tree verification (sampled)
+
+def test_tree_sampled_chain_is_linear_verification(oracle):
+    """A chain tree (parent[n] = n - 1) is the linear draft: with one child per
+    node the multi-candidate rule is the pages' rule ('Правило проверки',
+    kiosknews.app) step for step, and the Philox keys of node c (acceptance of
+    position c - 1, sampling at position c) are the linear ones, so the
+    (separately pinned) linear verification gives the same tokens and counts,
+    including invalid tokens, which cut the chain."""
+    rng = np.random.default_rng(12)
+    for trial in range(60):
+        B, N, V = int(rng.integers(1, 5)), int(rng.integers(1, 9)), int(rng.integers(2, 40))
+        T = rng.choice([1.0, 0.6, 1.7, 0.0], size=B).astype(np.float32)
+        tgt = rng.normal(size=(B, N, V)) * 1.5
+        drf = tgt + rng.normal(size=(B, N, V)) * 0.7   # drafts near the target: long chains
+        tok = np.zeros((B, N), np.int32)
+        for b in range(B):
+            for n in range(1, N):
+                z = drf[b, n - 1] / max(float(T[b]), 0.5)
+                e = np.exp(z - z.max())
+                tok[b, n] = rng.choice(V, p=e / e.sum())
+        if trial % 7 == 3 and N > 2:
+            tok[0, N // 2] = V + 3                     # cuts the chain
+        parent = np.tile(np.arange(-1, N - 1, dtype=np.int32), (B, 1))
+        seed = int(rng.integers(1, 2**62))
+        r = oracle.verify_tree(tgt, drf, parent, tok, T, seed)
+        if N == 1:
+            assert (r["accept_len"] == 0).all()
+            continue
+        lin = oracle.verify(tgt, drf[:, :N - 1], tok[:, 1:], None, T, seed)
+        assert np.array_equal(r["accept_len"], lin["accept_len"]), trial
+        assert np.array_equal(r["out_tokens"], lin["out_tokens"]), trial
+        a = r["accept_len"]
+        for b in range(B):
+            assert r["out_nodes"][b, :a[b]].tolist() == list(range(1, a[b] + 1))
+
+
+def _tree_law(run, parent, tok, N, V, one=1.0 - 2.0**-40):
+    """Exact law of the emitted tokens of one tree walk, integrating every
+    acceptance and sampling uniform by bisection on the oracle's own decisions
+    (each monotone in its uniform).  run(ua, us) -> (out_tokens, out_nodes, a).
+    Returns {emitted tuple: probability}."""
+    law = {}
+
+    def explore(ua, cur, depth, prob, prefix):
+        reach = prob
+        ua = list(ua)
+        for c in [c for c in range(cur + 1, N) if parent[c] == cur]:
+            if reach == 0.0:
+                break
+
+            def accepted(u, c=c):
+                w = list(ua)
+                w[c] = u
+                _, on, a = run(w, [0.5] * N)
+                return a > depth and on[depth] == c
+            t = 1.0 if accepted(one) else (_bisect(accepted) if accepted(0.0) else 0.0)
+            if t > 0.0:
+                w = list(ua)
+                w[c] = 0.0
+                explore(w, c, depth + 1, reach * t, prefix + (int(tok[c]),))
+            ua[c] = one
+            reach *= 1.0 - t
+        if reach == 0.0:
+            return
+        prev = 0.0
+        for v in range(V):
+            def at_most(u):
+                us = [0.5] * N
+                us[cur] = u
+                return run(ua, us)[0][depth] <= v
+            if v == V - 1:
+                bnd = 1.0
+            elif not at_most(0.0):
+                bnd = 0.0
+            else:
+                bnd = _bisect(at_most)
+            pv = max(0.0, bnd - prev)
+            prev = max(prev, bnd)
+            if pv > 0.0:
+                e = prefix + (v,)
+                law[e] = law.get(e, 0.0) + reach * pv
+
+    explore([0.0] * N, 0, 0, 1.0, ())
+    return law
+
+
+def _tree_from_tables(P, Q, parent, tok, T, K):
+    """Node rows of a tree whose node n follows the token prefix of its path:
+    target row log P(.|prefix)*T, draft row log Q(.|prefix)*T (zeros where the
+    prefix is longer than the tables)."""
+    N = len(parent)
+    V = len(P[()])
+    pre = [()] * N
+    for n in range(1, N):
+        pre[n] = pre[parent[n]] + (int(tok[n]),)
+    tgt = np.stack([np.log(P[pre[n]]) * T for n in range(N)])
+    drf = np.stack([np.log(Q[pre[n]]) * T if len(pre[n]) < K else np.zeros(V) for n in range(N)])
+    return tgt, drf, pre
+
+
+def _tree_lossless_worst(oracle, P, Q, parent, V, K, T):
+    """Largest error of the tree walk's law against the target law, over every
+    token assignment of the candidates (each child drawn independently from
+    its parent's draft distribution), every continuation filled in by target
+    sampling up to K + 1 tokens."""
+    T = float(np.float32(T))
+    N = len(parent)
+    agg = {}
+    for assign in itertools.product(range(V), repeat=N - 1):
+        tok = np.array((0,) + assign, np.int32)
+        tgt, drf, pre = _tree_from_tables(P, Q, parent, tok, T, K)
+        w = 1.0
+        for n in range(1, N):
+            w *= Q[pre[parent[n]]][tok[n]]
+        law = _tree_law(lambda ua, us: oracle.verify_tree_u(tgt, drf, parent, tok, T, ua, us),
+                        parent, tok, N, V)
+        for e, pr in law.items():
+            agg[e] = agg.get(e, 0.0) + w * pr
+    assert abs(sum(agg.values()) - 1.0) < 1e-12
+    worst = 0.0
+    for s in itertools.product(range(V), repeat=K + 1):
+        want = 1.0
+        for j in range(K + 1):
+            want *= P[s[:j]][s[j]]
+        got = 0.0
+        for n in range(1, K + 2):
+            if s[:n] in agg:
+                cont = 1.0
+                for j in range(n, K + 1):
+                    cont *= P[s[:j]][s[j]]
+                got += agg[s[:n]] * cont
+        worst = max(worst, abs(got - want))
+    return worst
+
+
+TREE_SHAPES = {
+    # parents of nodes 1..N-1 (node 0 is the root)
+    "three_siblings": ([-1, 0, 0, 0], 4, 1),
+    "two_levels": ([-1, 0, 0, 1, 1, 2], 3, 2),
+}
+
+
+@pytest.mark.parametrize("shape,T,seed", [("three_siblings", 1.0, 1), ("three_siblings", 0.7, 2),
+                                          ("two_levels", 1.0, 3), ("two_levels", 1.4, 4)])
+def test_tree_sampled_lossless_exact_enumeration(oracle, shape, T, seed):
+    """'Утверждение 1' (kiosknews.app) for trees: whatever the draft, when every
+    child is drawn independently from its parent's draft distribution the
+    emitted tokens follow the target law exactly.  Enumerates every token
+    assignment of the candidates and integrates every uniform; siblings share
+    a draft row, so this checks the residual updates between them, and the
+    two-level tree checks that the walk reads the accepted node's rows."""
+    parent, V, K = TREE_SHAPES[shape]
+    rng = np.random.default_rng(seed)
+    P, Q = _tables(rng, V, K)
+    worst = _tree_lossless_worst(oracle, P, Q, np.array(parent, np.int32), V, K, T)
+    assert worst < 1e-12, worst
+
+
+TREE_MUTANTS = {
+    # siblings tested against p again instead of the updated residual
+    "tree_no_residual_update": ("double w = r[v] / Z - q[v];", "double w = r[v] / Z;"),
+    # the residual's normaliser left out of the acceptance test
+    "tree_unnormalised": ("const double rx = r[x] / Z;", "const double rx = r[x];"),
+    # rows of the node at the path's depth instead of the current node
+    "tree_row_by_depth": (
+        "svo_row_softmax(svo_row(target, dtype, (size_t)cur, V), dtype, V, Td, p, NULL, NULL);",
+        "svo_row_softmax(svo_row(target, dtype, (size_t)depth, V), dtype, V, Td, p, NULL, NULL);"),
+    # the emitted token sampled from p after rejected siblings
+    "tree_sample_p": ("out_tokens[depth] = svo_inverse_cdf(r, V, u_s[cur], &d.cdf_margin);",
+                      "out_tokens[depth] = svo_inverse_cdf(p, V, u_s[cur], &d.cdf_margin);"),
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(TREE_MUTANTS))
+def test_tree_enumeration_catches_planted_mistakes(oracle, mutant, tmp_path):
+    """The tree enumeration is sensitive: a copy of the oracle with one planted
+    mistake in the tree walk breaks the lossless identity on one of the shapes."""
+    import ctypes
+    import subprocess
+    import oracle.build as ob
+    src = open(ob.SRC).read()
+    old, new = TREE_MUTANTS[mutant]
+    assert src.count(old) == 1, mutant
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(old, new))
+    so = str(tmp_path / "libmutant.so")
+    subprocess.check_call(["gcc", *ob.CFLAGS, str(path), "-o", so, "-lm", "-lpthread"])
+    good = oracle.lib()
+    mut = ctypes.CDLL(so)
+    mut.svo_verify_tree_u.argtypes = good.svo_verify_tree_u.argtypes
+    mut.svo_verify_tree_u.restype = good.svo_verify_tree_u.restype
+    oracle._lib = mut
+    try:
+        worst = 0.0
+        for shape, seed in (("three_siblings", 1), ("two_levels", 3)):
+            parent, V, K = TREE_SHAPES[shape]
+            P, Q = _tables(np.random.default_rng(seed), V, K)
+            try:
+                worst = max(worst, _tree_lossless_worst(oracle, P, Q, np.array(parent, np.int32),
+                                                        V, K, 1.0))
+            except AssertionError:
+                worst = 1.0   # the law does not even sum to 1
+            if worst > 1e-4:
+                break
+    finally:
+        oracle._lib = good
+    assert worst > 1e-4, mutant
+
+
+def test_tree_sampled_hand_case(oracle):
+    """Two siblings carrying tokens 0 and 1 under p = (0.5, 0.5, 0), q = (0.75,
+    0.25, 0): the first is accepted iff u < p/q = 2/3; after its rejection the
+    residual is max(0, p - q) = (0, 0.25, 0), normalised (0, 1, 0), so the
+    second (token 1, q = 0.25) is always accepted."""
+    T = 1.0
+    tgt = np.log(np.array([[0.5, 0.5, 1e-300], [1.0, 1.0, 1.0], [1.0, 1.0, 1.0]]))
+    drf = np.log(np.array([[0.75, 0.25, 1e-300], [1.0, 1.0, 1.0], [1.0, 1.0, 1.0]]))
+    parent = [-1, 0, 0]
+    tok = [0, 0, 1]
+    ot, on, a = oracle.verify_tree_u(tgt, drf, parent, tok, T, [0, 0.66, 0.0], 0.5)
+    assert a == 1 and on[0] == 1 and ot[0] == 0
+    ot, on, a = oracle.verify_tree_u(tgt, drf, parent, tok, T, [0, 0.67, 0.999], 0.5)
+    assert a == 1 and on[0] == 2 and ot[0] == 1
+    # leaf row 2 uniform: the emitted token after node 2 follows u_s of node 2
+    ot, on, a = oracle.verify_tree_u(tgt, drf, parent, tok, T, [0, 0.67, 0.0], [0.5, 0.5, 0.9])
+    assert ot[:2].tolist() == [1, 2] and ot[2] == -1
+    # a token outside [0, V) is no candidate: the second sibling is tested first
+    ot, on, a = oracle.verify_tree_u(tgt, drf, parent, [0, 7, 1], T, [0, 0.0, 0.4], 0.5)
+    assert a == 1 and on[0] == 2
