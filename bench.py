@@ -283,37 +283,69 @@ def prepare(cfg, rank, device):
 
 
 def run_tree(args, world, rank, local):
-    """Greedy candidate-tree verification: B requests of N-node trees whose
-    node rows are the workload's target logits (N = --tree); half the nodes
-    carry their parent's argmax, so paths go deep.  Positions = candidate
-    nodes verified (N - 1 per request)."""
+    """Candidate-tree verification: B requests of N-node trees (N = --tree) at
+    the workload's vocabulary.  Greedy: the node rows are the workload's
+    target logits and half the nodes carry their parent's argmax, so paths go
+    deep.  Sampled (--tree-sampled): seeded trees whose tokens are drawn from
+    their parent's draft row, target and draft rows as in the workload, at its
+    temperature (c4: a quarter of the requests greedy).  Positions =
+    candidate nodes verified (N - 1 per request)."""
     import numpy as np
     import speculative_decoding_verification_69_gb300 as sv
     sv.load_library()
     dev = torch.device("cuda", local)
     N = args.tree
-    inp = workloads.make_inputs(args.config, rep=rank, device=dev, K=N - 1)
-    tgt = inp["target"]
-    B, _, V = tgt.shape
-    esz = tgt.element_size()
-    rng = np.random.default_rng(workloads.seed_for(args.config, rank))
-    am = tgt.float().argmax(dim=-1).cpu().numpy() if N > 1 else np.zeros((B, 1), np.int64)
-    parent = np.full((B, N), -1, np.int32)
-    tok = np.zeros((B, N), np.int32)
-    for b in range(B):
-        for n in range(1, N):
-            p = int(rng.integers(0, n))
-            parent[b, n] = p
-            tok[b, n] = am[b, p] if rng.random() < 0.5 else int(rng.integers(0, V))
-    parent = torch.from_numpy(parent).to(dev)
-    tok = torch.from_numpy(tok).to(dev)
-    alg_bytes = B * N * V * esz
+    c = workloads.CONFIGS[args.config]
+    if args.tree_sampled:
+        T = c["T"] if isinstance(c["T"], float) else 1.0
+        noise = c["noise"] if isinstance(c["noise"], float) else 0.5
+        inp = workloads.make_tree_inputs(c["B"], N, c["V"], c["dtype"],
+                                         seed=workloads.seed_for(args.config, rank), T=T,
+                                         sigma=c["sigma"], noise=noise,
+                                         n_greedy=c.get("n_greedy", 0), device=dev)
+        tgt, drf = inp["target"], inp["draft"]
+        parent, tok, temp, seed = inp["parent"], inp["tokens"], inp["temperature"], inp["seed"]
+        B, _, V = tgt.shape
+        esz = tgt.element_size()
+    else:
+        inp = workloads.make_inputs(args.config, rep=rank, device=dev, K=N - 1)
+        tgt = inp["target"]
+        B, _, V = tgt.shape
+        esz = tgt.element_size()
+        rng = np.random.default_rng(workloads.seed_for(args.config, rank))
+        am = tgt.float().argmax(dim=-1).cpu().numpy() if N > 1 else np.zeros((B, 1), np.int64)
+        parent = np.full((B, N), -1, np.int32)
+        tok = np.zeros((B, N), np.int32)
+        for b in range(B):
+            for n in range(1, N):
+                p = int(rng.integers(0, n))
+                parent[b, n] = p
+                tok[b, n] = am[b, p] if rng.random() < 0.5 else int(rng.integers(0, V))
+        parent = torch.from_numpy(parent).to(dev)
+        tok = torch.from_numpy(tok).to(dev)
+        drf = None
+    if drf is None:
+        alg_bytes = B * N * V * esz
+    else:  # every target row, and the draft rows of sampled requests, once
+        n_samp = int((temp > 0).sum().item())
+        alg_bytes = (B * N + n_samp * (N - 1)) * V * esz
     l2_bytes = int(torch.cuda.get_device_properties(dev).L2_cache_size)
     ncopies = logit_copies(alg_bytes, l2_bytes)
-    copies = [tgt] + [tgt.clone() for _ in range(ncopies - 1)]
+    copies = [(tgt, drf)] + [(tgt.clone(), None if drf is None else drf.clone())
+                             for _ in range(ncopies - 1)]
+    ws = torch.empty(max(int(sv.load_library().spec_tree_workspace_bytes(B, N, V, sv._dtype_code(tgt))), 256),
+                     dtype=torch.uint8, device=dev)
+
+    def step(i):
+        t, d = copies[i % ncopies]
+        if d is None:
+            sv.verify_tree_greedy(t, parent, tok)
+        else:
+            sv.verify_tree(t, d, parent, tok, temp, seed, workspace=ws)
+
     stream = torch.cuda.current_stream()
     for i in range(args.warmup):
-        sv.verify_tree_greedy(copies[i % ncopies], parent, tok)
+        step(i)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
@@ -323,7 +355,7 @@ def run_tree(args, world, rank, local):
     t0 = time.perf_counter()
     for i in range(args.steps):
         ev[i][0].record(stream)
-        sv.verify_tree_greedy(copies[(args.warmup + i) % ncopies], parent, tok)
+        step(args.warmup + i)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -341,8 +373,12 @@ def run_tree(args, world, rank, local):
         "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if tgt.dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded logits and trees; no datasets or trained weights)",
-        "config": {"workload": workloads.NAMES[args.config] + " target rows as %d-node trees" % N,
-                   "B": B, "N": N, "V": V, "mode": "greedy tree verification",
+        "config": {"workload": workloads.NAMES[args.config] + (
+                       " target rows as %d-node trees" % N if drf is None else
+                       " shapes, %d-node sampled trees (tokens drawn from the parent's draft row)" % N),
+                   "B": B, "N": N, "V": V,
+                   "mode": "greedy tree verification" if drf is None else
+                   "tree verification (sampled requests: multi-candidate residual walk)",
                    "logit_bytes_per_step": alg_bytes,
                    "logits_GBps": alg_bytes / step_s / 1e9,
                    "l2": "inputs larger than L2: %d copies cycled; no flush" % ncopies},
@@ -612,6 +648,8 @@ def main(argv=None):
                          "then verification (N = the value given)")
     ap.add_argument("--tree", type=int, default=0,
                     help="greedy verification of N-node candidate trees instead of chains")
+    ap.add_argument("--tree-sampled", action="store_true",
+                    help="with --tree: sampled trees (draft rows, the workload's temperature)")
     ap.add_argument("--early-exit", type=int, default=0,
                     help="verify positions [0, W) first, then the rest for open requests")
     args = ap.parse_args(argv)

@@ -187,7 +187,7 @@ spec_status_t spec_verify_early_exit(const void *target_logits, const void *draf
  *   1 <= N <= SPEC_MAX_TREE.  A node whose parent is not an earlier node
  *   belongs to no path (SPEC_DEV_BAD_TREE).  The workspace is
  *   spec_tree_workspace_bytes(B, N, V, dtype) bytes.  Errors as spec_verify.
- *   Sampled (T > 0) tree verification is not provided.
+ *   Sampled (T > 0) requests: spec_verify_tree.
  */
 size_t spec_tree_workspace_bytes(int B, int N, int V, spec_dtype_t dtype);
 spec_status_t spec_verify_tree_greedy(const void *target_logits, spec_dtype_t dtype,
@@ -195,6 +195,40 @@ spec_status_t spec_verify_tree_greedy(const void *target_logits, spec_dtype_t dt
                                       int N, int V, int32_t *out_tokens, int32_t *out_nodes,
                                       int32_t *accept_len, void *workspace, size_t workspace_bytes,
                                       uint32_t *dev_status, void *stream);
+
+/*
+ * spec_verify_tree -- verification of candidate trees at each request's
+ * temperature: greedy requests (T not a positive normal float) take the walk
+ * of spec_verify_tree_greedy; sampled requests apply the acceptance rule of
+ * "Спекулятивный декодинг в проде" (kiosknews.app), "Правило проверки", to
+ * every candidate of the tree, siblings in index order against successively
+ * updated residuals (the multi-candidate form of the rule):
+ *   at node u the weights r start as p_u = softmax(target row u / T); child c
+ *   (token x; a token outside [0, V) is no candidate) is accepted iff
+ *   u_acc * q_u(x) < r(x) / Z, q_u = softmax(draft row u / T); a rejection
+ *   sets r = max(0, r / Z - q_u) with Z its sum (zero mass: r = p_u again).
+ *   An accepted child becomes the current node; with none accepted the
+ *   emitted token is the inverse CDF of r (smallest v whose inclusive prefix
+ *   exceeds u_s * Z) and the walk ends.  With one child per node this is
+ *   spec_verify's rule step for step; with the siblings of node u drawn
+ *   independently from q_u the emitted tokens follow the target exactly.
+ *   Uniforms: candidate node c uses the acceptance uniform of position c - 1
+ *   and node u's emitted token the sampling uniform of position u (Philox keys
+ *   as spec_verify), so a chain tree draws spec_verify's numbers.
+ *   target_logits [B, N, V], draft_logits [B, N-1, V] (row n: the draft's
+ *   logits after node n; the last node has no children; may be NULL when
+ *   N = 1), both bf16/fp32 device and 16-byte aligned; parent, node_tokens
+ *   [B, N] int32; temperature [B] float32 device.  Outputs as
+ *   spec_verify_tree_greedy; the workspace is spec_tree_workspace_bytes.
+ *   Each sampled request costs one pass over its vocabulary per rejected
+ *   candidate, run by one CTA.  Errors as spec_verify.
+ */
+spec_status_t spec_verify_tree(const void *target_logits, const void *draft_logits,
+                               spec_dtype_t dtype, const int32_t *parent,
+                               const int32_t *node_tokens, const float *temperature, uint64_t seed,
+                               int B, int N, int V, int32_t *out_tokens, int32_t *out_nodes,
+                               int32_t *accept_len, void *workspace, size_t workspace_bytes,
+                               uint32_t *dev_status, void *stream);
 
 /*
  * spec_draft_confidence -- the draft's confidence at every position, as the

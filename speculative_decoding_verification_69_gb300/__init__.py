@@ -65,6 +65,10 @@ def load_library():
     L.spec_verify_tree_greedy.argtypes = [vp, ctypes.c_int, i32p, i32p, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, i32p, i32p, i32p, vp, ctypes.c_size_t, u32p, vp]
     L.spec_verify_tree_greedy.restype = ctypes.c_int
+    L.spec_verify_tree.argtypes = [vp, vp, ctypes.c_int, i32p, i32p, f32p, ctypes.c_uint64,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, i32p, i32p, vp,
+                                   ctypes.c_size_t, u32p, vp]
+    L.spec_verify_tree.restype = ctypes.c_int
     L.spec_schedule_budget.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_longlong, i32p, vp]
     L.spec_schedule_budget.restype = ctypes.c_int
     L.spec_verify_noalloc.argtypes = common[:12] + [u32p, vp]
@@ -84,6 +88,7 @@ def load_library():
 def exported_symbols():
     return ["spec_verify_workspace_bytes", "spec_verify", "spec_verify_debug",
             "spec_verify_early_exit", "spec_tree_workspace_bytes", "spec_verify_tree_greedy",
+            "spec_verify_tree",
             "spec_draft_confidence", "spec_schedule_budget",
             "spec_schedule_len", "spec_verify_noalloc",
             "spec_profile_events", "spec_debug_force_wait_timeout",
@@ -259,6 +264,43 @@ def verify_tree_greedy(target, parent, node_tokens, *, dev_status=None, stream=N
     _check(L.spec_verify_tree_greedy(_ptr(target), _dtype_code(target), _ptr(parent),
                                      _ptr(node_tokens), B, N, V, _ptr(out), _ptr(nodes), _ptr(acc),
                                      _ptr(ws), ws.numel(), _ptr(dev_status), _stream(stream)))
+    return out, nodes, acc
+
+
+def verify_tree(target, draft, parent, node_tokens, temperature, seed, *, dev_status=None,
+                workspace=None, stream=None):
+    """Verification of candidate trees at each request's temperature (greedy
+    requests take the greedy walk; sampled ones check siblings against
+    successively updated residuals): target [B, N, V], draft [B, N-1, V] (row
+    n: the draft's logits after node n; None when N = 1), parent / node_tokens
+    int32 [B, N], temperature float32 [B].  Returns (out_tokens [B, N],
+    out_nodes [B, N], accept_len [B]) on the device."""
+    L = load_library()
+    if target.dim() != 3 or not target.is_cuda or not target.is_contiguous():
+        raise ValueError("target must be a contiguous CUDA tensor [B, N, V]")
+    B, N, V = target.shape
+    if N > 1:
+        if (draft is None or draft.shape != (B, N - 1, V) or draft.dtype != target.dtype
+                or not draft.is_cuda or not draft.is_contiguous()):
+            raise ValueError("draft must be a contiguous CUDA tensor [B, N-1, V] of target's dtype")
+    for t in (parent, node_tokens):
+        if t.shape != (B, N) or t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("parent and node_tokens must be contiguous int32 CUDA tensors [B, N]")
+    if (temperature.shape != (B,) or temperature.dtype != torch.float32 or not temperature.is_cuda
+            or not temperature.is_contiguous()):
+        raise ValueError("temperature must be a contiguous float32 CUDA tensor [B]")
+    dev = target.device
+    out = torch.empty((B, N), dtype=torch.int32, device=dev)
+    nodes = torch.empty((B, N), dtype=torch.int32, device=dev)
+    acc = torch.empty((B,), dtype=torch.int32, device=dev)
+    n = int(L.spec_tree_workspace_bytes(B, N, V, _dtype_code(target)))
+    if workspace is None or workspace.numel() < n:
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+    _check(L.spec_verify_tree(_ptr(target), _ptr(draft) if N > 1 else None, _dtype_code(target),
+                              _ptr(parent), _ptr(node_tokens), _ptr(temperature),
+                              int(seed) & 0xFFFFFFFFFFFFFFFF, B, N, V, _ptr(out), _ptr(nodes),
+                              _ptr(acc), _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                              _stream(stream)))
     return out, nodes, acc
 
 

@@ -123,6 +123,25 @@ __device__ __forceinline__ int wave_slot(int r, int nt, int k0, int K) {
     return r < nt ? k0 + r : K + 1 + k0 + (r - nt);
 }
 
+// log2(e)/T of a sampled request: c = fl(log2(e)/T) (the statistics pass's
+// factor) and the same value as c_hi + c_lo: c_hi = fl(hi/T), its exact
+// remainder, then the low part, with the high part kept at or below the value
+// and the low part positive.
+__device__ __forceinline__ void temp_coeffs(float T, float &c, float &c_hi, float &c_lo) {
+    const float q = __fdiv_rn(kLog2EHi, T);
+    const float rem = __fmaf_rn(-q, T, kLog2EHi);
+    float ql = __fdiv_rn(__fadd_rn(rem, kLog2ELo), T);
+    float chi = q;
+    if (ql < 0.f) {
+        chi = __int_as_float(__float_as_int(q) - 1);
+        ql = __fadd_rn(ql, __fsub_rn(q, chi));
+    }
+    if (!(ql >= FLT_MIN)) ql = FLT_MIN;
+    c = q;
+    c_hi = chi;
+    c_lo = ql;
+}
+
 constexpr int kPrepThreads = 1024;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded wait: 2 s
 // Diagnostics: the DIAG instantiations of the bulk-copy kernels (launched only
@@ -179,19 +198,7 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
             ri.greedy = greedy;
             ri.T = T;
             if (!greedy) {
-                // log2(e)/T as q + ql: q = fl(hi/T), its exact remainder, then the low part
-                const float q = __fdiv_rn(kLog2EHi, T);
-                const float rem = __fmaf_rn(-q, T, kLog2EHi);
-                float ql = __fdiv_rn(__fadd_rn(rem, kLog2ELo), T);
-                float chi = q;
-                if (ql < 0.f) {  // keep the high part at or below the value, the low part positive
-                    chi = __int_as_float(__float_as_int(q) - 1);
-                    ql = __fadd_rn(ql, __fsub_rn(q, chi));
-                }
-                if (!(ql >= FLT_MIN)) ql = FLT_MIN;
-                ri.c = q;
-                ri.c_hi = chi;
-                ri.c_lo = ql;
+                temp_coeffs(T, ri.c, ri.c_hi, ri.c_lo);
             } else {
                 ri.c = 0.f; ri.c_hi = 0.f; ri.c_lo = 0.f;
             }
@@ -1250,6 +1257,40 @@ __global__ void sv_tree_rows(Params P) {
     if (blockIdx.x == 0 && threadIdx.x == 0) *P.row_count = (int)total;
 }
 
+// A node whose parent is not an earlier node belongs to no path; such a tree
+// raises SPEC_DEV_BAD_TREE.
+__device__ __forceinline__ void flag_bad_tree(const Params &P, int N, const int *s_par) {
+    bool bad = false;
+    for (int c = 1; c < N; ++c) bad |= s_par[c] < 0 || s_par[c] >= c;
+    if (bad && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_BAD_TREE);
+}
+
+// One thread: the greedy walk of request b from the argmax of every node row.
+__device__ void greedy_tree_walk(const Params &P, int b, int N, const int *s_amax,
+                                 const int *s_par, const int *s_tok, int32_t *out_nodes) {
+    int32_t *out = P.out_tokens + (size_t)b * N;
+    int32_t *nodes = out_nodes + (size_t)b * N;
+    int cur = 0, depth = 0;
+    for (;;) {
+        const int t = s_amax[cur];
+        int next = -1;
+        for (int c = cur + 1; c < N; ++c)
+            if (s_par[c] == cur && s_tok[c] == t) {
+                next = c;
+                break;
+            }
+        out[depth] = t;
+        if (next < 0) break;
+        nodes[depth] = next;
+        cur = next;
+        ++depth;
+    }
+    for (int i = depth + 1; i < N; ++i) out[i] = -1;
+    for (int i = depth; i < N; ++i) nodes[i] = -1;
+    P.accept_len[b] = depth;
+    flag_bad_tree(P, N, s_par);
+}
+
 // Per request: the argmax of every node row from the statistics pass's
 // partials, then the walk from the root -- t = argmax of the current node, the
 // next node is the lowest-index child carrying t, else t is emitted.  A node
@@ -1272,30 +1313,548 @@ __global__ void __launch_bounds__(kThreads) sv_tree_decide(Params P, const int32
         if (lane == 0) s_amax[n] = __float_as_int(rs.z);
     }
     __syncthreads();
-    if (tid == 0) {
-        int32_t *out = P.out_tokens + (size_t)b * N;
-        int32_t *nodes = out_nodes + (size_t)b * N;
-        bool bad = false;
-        for (int c = 1; c < N; ++c) bad |= s_par[c] < 0 || s_par[c] >= c;
-        int cur = 0, depth = 0;
-        for (;;) {
-            const int t = s_amax[cur];
-            int next = -1;
-            for (int c = cur + 1; c < N; ++c)
-                if (s_par[c] == cur && s_tok[c] == t) {
-                    next = c;
-                    break;
+    if (tid == 0) greedy_tree_walk(P, b, N, s_amax, s_par, s_tok, out_nodes);
+}
+
+// ------------------------------------------------------------------ tree verification (sampled)
+
+// Rows of a tree verification with sampled requests: every node row of the
+// target (slots 0..N-1) and, for sampled requests, the draft rows 0..N-2
+// (slots N..2N-2; draft row n is the distribution node n's children were drawn
+// from, and the last node has no children).  Request-major, one CTA.
+__global__ void __launch_bounds__(kPrepThreads) sv_tree_rows_s(Params P) {
+    __shared__ int warp_tot[kPrepThreads / 32];
+    __shared__ int carry_s;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int N = P.K + 1;
+    if (tid == 0) carry_s = 0;
+    __syncthreads();
+    pdl_trigger();
+    for (int base = 0; base < P.B; base += kPrepThreads) {
+        const int b = base + tid;
+        int n = 0, greedy = 1;
+        float cval = 0.f;
+        if (b < P.B) {
+            const float T = P.temperature[b];
+            greedy = !(isfinite(T) && T >= FLT_MIN);
+            if (!greedy) cval = __fdiv_rn(kLog2EHi, T);
+            n = greedy ? N : 2 * N - 1;
+        }
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) warp_tot[w] = incl;
+        __syncthreads();
+        int woff = 0, block_tot = 0;
+        for (int i = 0; i < kPrepThreads / 32; ++i) {
+            if (i < w) woff += warp_tot[i];
+            block_tot += warp_tot[i];
+        }
+        const int off = carry_s + woff + incl - n;
+        for (int r = 0; r < n; ++r)
+            P.rows[off + r] = make_int4(b, r, greedy, __float_as_int(cval));
+        __syncthreads();
+        if (tid == 0) carry_s += block_tot;
+        __syncthreads();
+    }
+    if (tid == 0) *P.row_count = carry_s;
+}
+
+constexpr int kTreeThreads = 512;
+constexpr int kTreeWarps = kTreeThreads / 32;
+constexpr int kTreeStep = 256;     // elements a warp covers per step: 8 per lane
+constexpr int kTreeGroups = 256;   // recorded masses per warp (groups of steps)
+constexpr float kTreeBias = 2.0f;  // every summed weight is at most ~1
+
+// The weight 2^((z - m) c + l) of one element: the scalar twin of weight2l
+// (the same operations in the same order, so the same value).
+__device__ __forceinline__ float weight1l(float z, float m, float chi, float clo, float l) {
+    const float d = __fsub_rn(z, m);
+    return ex2(__fmaf_rn(d, chi, __fmaf_rn(d, clo, l)));
+}
+
+// The residual weight of an element after J >= 1 rejected siblings.  a and b
+// are the element's target and draft weights (close to normalised); the exact
+// normalisers are 1 + dt and 1 + dd, so p = a + dt a and q = b + dd b.
+// r_1 = max(0, p - q), formed as (a - b) + (dt a - dd b) to keep its rounding
+// relative to itself; r_j = max(0, r_(j-1) / Z_(j-1) - q).  After a residual of
+// zero mass at rejection `start` the weights restart from p.
+__device__ __forceinline__ float tree_resid(float a, float b, float dt, float dd, int J, int start,
+                                            const float *zinv) {
+    const float q = __fmaf_rn(dd, b, b);
+    float r;
+    int j;
+    if (start == 0) {
+        r = fmaxf(__fadd_rn(__fsub_rn(a, b), __fmaf_rn(dt, a, -__fmul_rn(dd, b))), 0.f);
+        j = 2;
+    } else {
+        r = __fmaf_rn(dt, a, a);
+        j = start + 1;
+    }
+    for (; j <= J; ++j) r = fmaxf(__fmaf_rn(r, zinv[j - 1], -q), 0.f);
+    return r;
+}
+
+// Elements [e0, e0 + 8) of a row as 4 pairs (-inf past V).
+template <int DT, bool VEC> struct Eight {
+    uint4 v0, v1;
+    __device__ __forceinline__ void load(const char *row, long long e0, int V) {
+        v0 = load_vec<DT, VEC>(row, e0, V);
+        if (DT == kF32) v1 = load_vec<DT, VEC>(row, e0 + 4, V);
+    }
+    __device__ __forceinline__ float2 pair(int i) const {
+        if (DT == kBF16) return make_float2(elem<DT>(v0, 2 * i), elem<DT>(v0, 2 * i + 1));
+        return i < 2 ? make_float2(elem<DT>(v0, 2 * i), elem<DT>(v0, 2 * i + 1))
+                     : make_float2(elem<DT>(v1, 2 * i - 4), elem<DT>(v1, 2 * i - 3));
+    }
+};
+
+// Per-node constants of the sampled walk.
+struct TreeNodeC {
+    float2 mt, lt, md, ld, chi, clo;  // row max and log2(1/S) of the target and draft rows, c
+    float dt, dd;                     // exact normalisers - 1 (after the first rejection)
+    int J, start;                     // rejections so far; restart point of the residual
+};
+
+// Weights a pass sums: the target weights a; the parts of the first residual
+// (sum a, sum b, sum over a > b of (a - b), sum over a > b of b); the residual
+// after J rejections.
+enum { kTreeModeP = 0, kTreeModeFirst = 1, kTreeModeResid = 2 };
+
+// The 8 weights of a lane at e0 in a pass of mode P or Resid.
+template <int DT, bool VEC>
+__device__ __forceinline__ void tree_weights8(const Eight<DT, VEC> &zt, const Eight<DT, VEC> &zd,
+                                              const TreeNodeC &nc, int mode, const float *zinv,
+                                              float w[8]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 a = weight2l(zt.pair(i), nc.mt, nc.chi, nc.clo, nc.lt);
+        if (mode == kTreeModeP) {
+            w[2 * i] = a.x;
+            w[2 * i + 1] = a.y;
+        } else {
+            const float2 bq = weight2l(zd.pair(i), nc.md, nc.chi, nc.clo, nc.ld);
+            w[2 * i] = tree_resid(a.x, bq.x, nc.dt, nc.dd, nc.J, nc.start, zinv);
+            w[2 * i + 1] = tree_resid(a.y, bq.y, nc.dt, nc.dd, nc.J, nc.start, zinv);
+        }
+    }
+}
+
+// Steps of warp w: [s0, s1) of kTreeStep elements; recorded masses cover
+// groups of gsz consecutive steps.
+struct TreeSplit {
+    int s0, s1, gsz;
+    __device__ __forceinline__ TreeSplit(int V, int w) {
+        const int nsteps = (V + kTreeStep - 1) / kTreeStep;
+        const int spw = (nsteps + kTreeWarps - 1) / kTreeWarps;
+        s0 = min(nsteps, w * spw);
+        s1 = min(nsteps, s0 + spw);
+        gsz = (spw + kTreeGroups - 1) / kTreeGroups;
+    }
+};
+
+// One pass of the CTA over the vocabulary.  Warp w covers its contiguous steps,
+// lane l the 8 elements at 8 l of each step, kU steps' loads in flight.  Writes
+// the warp's sums (as doubles) to red[w]; with `record`, also the mass of each
+// group of steps to mass[w * kTreeGroups + g] and the warp's total as their sum.
+template <int DT, bool VEC>
+__device__ void tree_pass(const char *rowt, const char *rowd, int V, const TreeNodeC &nc, int mode,
+                          bool record, const float *zinv, double (*red)[4], float *mass, int warp,
+                          int lane) {
+    constexpr int kU = DT == kBF16 ? 4 : 2;
+    const TreeSplit sp(V, warp);
+    BiasAcc2 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i].init(kTreeBias);
+    float gs = 0.f;   // this lane's part of the current group
+    double mw = 0.0;  // the warp's recorded total (lane 0)
+    for (int st0 = sp.s0; st0 < sp.s1; st0 += kU) {
+        Eight<DT, VEC> zt[kU], zd[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const long long e0 = (long long)(st0 + u) * kTreeStep + lane * 8;
+            if (st0 + u < sp.s1) {
+                zt[u].load(rowt, e0, V);
+                if (mode != kTreeModeP) zd[u].load(rowd, e0, V);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (st0 + u >= sp.s1) break;
+            if (mode == kTreeModeFirst) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 a = weight2l(zt[u].pair(i), nc.mt, nc.chi, nc.clo, nc.lt);
+                    const float2 bq = weight2l(zd[u].pair(i), nc.md, nc.chi, nc.clo, nc.ld);
+                    acc[0].add(a);
+                    acc[1].add(bq);
+                    const bool gx = a.x > bq.x, gy = a.y > bq.y;
+                    acc[2].add(make_float2(gx ? __fsub_rn(a.x, bq.x) : 0.f, gy ? __fsub_rn(a.y, bq.y) : 0.f));
+                    acc[3].add(make_float2(gx ? bq.x : 0.f, gy ? bq.y : 0.f));
                 }
-            out[depth] = t;
-            if (next < 0) break;
-            nodes[depth] = next;
+                continue;
+            }
+            float w[8];
+            tree_weights8<DT, VEC>(zt[u], zd[u], nc, mode, zinv, w);
+            if (record) {
+                float ls = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ls = __fadd_rn(ls, w[i]);
+                gs = __fadd_rn(gs, ls);
+                const int k = st0 + u - sp.s0;
+                if ((k + 1) % sp.gsz == 0 || st0 + u + 1 == sp.s1) {
+                    const float gm = warp_sum(gs);
+                    if (lane == 0) {
+                        mass[warp * kTreeGroups + k / sp.gsz] = gm;
+                        mw += (double)gm;
+                    }
+                    gs = 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[0].add(make_float2(w[2 * i], w[2 * i + 1]));
+            }
+        }
+    }
+    if (record) {
+        if (lane == 0) red[warp][0] = mw;
+        return;
+    }
+    const int nsum = mode == kTreeModeFirst ? 4 : 1;
+    for (int i = 0; i < nsum; ++i) {
+        const FF t = warp_sum_ff(acc[i].total());
+        if (lane == 0) red[warp][i] = ff_to_double(t);
+    }
+}
+
+// The emitted token, by one warp: the inverse CDF of the weights of the last
+// recording pass at thr, inside warp W's steps (base = the mass of the warps
+// before W): the group whose prefix crosses thr, then the step, then the
+// element.  Rounding that leaves the crossing outside takes the last positive
+// weight met.
+template <int DT, bool VEC>
+__device__ int tree_find(const char *rowt, const char *rowd, int V, const TreeNodeC &nc, int mode,
+                         const float *zinv, const float *mass, int W, double base, double thr,
+                         int lane) {
+    const TreeSplit sp(V, W);
+    const int ng = (sp.s1 - sp.s0 + sp.gsz - 1) / sp.gsz;
+    // the group: lane l sums groups [8 l, 8 l + 8) of W
+    constexpr int kPer = kTreeGroups / 32;
+    double ls = 0.0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int g = lane * kPer + i;
+        if (g < ng) ls += (double)mass[W * kTreeGroups + g];
+    }
+    double incl = ls;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    unsigned cross = __ballot_sync(0xFFFFFFFFu, base + incl > thr && ls > 0.0);
+    int g = -1;
+    double gbase = 0.0;
+    if (lane == (cross ? __ffs(cross) - 1 : 31)) {
+        double c = base + incl - ls;
+        int last = -1;
+        double last_base = 0.0;
+        for (int i = 0; i < kPer; ++i) {
+            const int gi = lane * kPer + i;
+            if (gi >= ng) break;
+            const double m = (double)mass[W * kTreeGroups + gi];
+            if (m > 0.0) {
+                last = gi;
+                last_base = c;
+            }
+            if (m > 0.0 && c + m > thr) {
+                g = gi;
+                gbase = c;
+                break;
+            }
+            c += m;
+        }
+        if (g < 0) {
+            g = last;
+            gbase = last_base;
+        }
+    }
+    const int src = cross ? __ffs(cross) - 1 : 31;
+    g = __shfl_sync(0xFFFFFFFFu, g, src);
+    gbase = __shfl_sync(0xFFFFFFFFu, gbase, src);
+    if (g < 0) {  // no mass among the lanes' blocks: the last group with mass
+        const unsigned has = __ballot_sync(0xFFFFFFFFu, ls > 0.0);
+        if (!has) return -1;
+        const int L = 31 - __clz(has);
+        int gl = -1;
+        double bl = 0.0;
+        if (lane == L) {
+            double c = base + incl - ls;
+            for (int i = 0; i < kPer; ++i) {
+                const int gi = lane * kPer + i;
+                if (gi >= ng) break;
+                const double m = (double)mass[W * kTreeGroups + gi];
+                if (m > 0.0) {
+                    gl = gi;
+                    bl = c;
+                }
+                c += m;
+            }
+        }
+        g = __shfl_sync(0xFFFFFFFFu, gl, L);
+        gbase = __shfl_sync(0xFFFFFFFFu, bl, L);
+    }
+    // the steps of group g, in order
+    const int st_a = sp.s0 + g * sp.gsz, st_b = min(sp.s1, st_a + sp.gsz);
+    double b0 = gbase;
+    int last_pos = -1;
+    for (int st = st_a; st < st_b; ++st) {
+        const long long e0 = (long long)st * kTreeStep + lane * 8;
+        Eight<DT, VEC> zt, zd;
+        zt.load(rowt, e0, V);
+        if (mode != kTreeModeP) zd.load(rowd, e0, V);
+        float w[8];
+        tree_weights8<DT, VEC>(zt, zd, nc, mode, zinv, w);
+        double s8 = 0.0;
+        int lp = -1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            s8 += (double)w[i];
+            if (w[i] > 0.f) lp = (int)e0 + i;
+        }
+        double in8 = s8;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double v = __shfl_up_sync(0xFFFFFFFFu, in8, o);
+            if (lane >= o) in8 += v;
+        }
+        const unsigned cr = __ballot_sync(0xFFFFFFFFu, b0 + in8 > thr && s8 > 0.0);
+        const int lp_max = __reduce_max_sync(0xFFFFFFFFu, (unsigned)(lp + 1)) - 1;
+        if (cr) {
+            const int L = __ffs(cr) - 1;
+            int tok = -1;
+            if (lane == L) {
+                double c = b0 + in8 - s8;
+                for (int i = 0; i < 8 && tok < 0; ++i) {
+                    c += (double)w[i];
+                    if (w[i] > 0.f && c > thr) tok = (int)e0 + i;
+                }
+                if (tok < 0) tok = lp;
+            }
+            return __shfl_sync(0xFFFFFFFFu, tok, L);
+        }
+        if (lp_max >= 0) last_pos = lp_max;
+        b0 += __shfl_sync(0xFFFFFFFFu, in8, 31);
+    }
+    return last_pos;
+}
+
+// Sampled verification of candidate trees, one CTA per request (greedy
+// requests take the greedy walk).  At node u the first child is checked with
+// the linear acceptance test; every rejection followed by another candidate
+// updates the residual with one pass over the vocabulary (its mass Z_J),
+// against which the next sibling is checked: accept iff
+// u_acc * q(x) * Z_J < r_J(x).  When no child is accepted a recording pass over
+// the current weights (p, or the last residual) and an inverse CDF give the
+// emitted token.  Candidate node c takes the acceptance uniform of position
+// c - 1, node u's emitted token the sampling uniform of position u.
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const int32_t *parent,
+                                                               const int32_t *token,
+                                                               int32_t *out_nodes) {
+    __shared__ int s_par[SPEC_MAX_TREE], s_tok[SPEC_MAX_TREE], s_amax[SPEC_MAX_TREE];
+    __shared__ float s_m[2 * SPEC_MAX_TREE], s_S[2 * SPEC_MAX_TREE];
+    __shared__ float s_zinv[SPEC_MAX_TREE];
+    __shared__ float s_mass[kTreeWarps * kTreeGroups];
+    __shared__ double s_red[kTreeWarps][4];
+    __shared__ float s_dt, s_dd;
+    __shared__ double s_Z, s_base, s_thr;
+    __shared__ int s_start, s_acc, s_W, s_emit, s_again;
+    constexpr int ESZ = Fmt<DT>::kESZ;
+    const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int N = P.K + 1, K = P.K, V = P.V;
+    for (int i = tid; i < N; i += kTreeThreads) {
+        s_par[i] = parent[(size_t)b * N + i];
+        s_tok[i] = token[(size_t)b * N + i];
+    }
+    const float T = P.temperature[b];
+    const bool greedy = !(isfinite(T) && T >= FLT_MIN);
+    float c = 0.f, chi = 0.f, clo = 0.f;
+    if (!greedy) temp_coeffs(T, c, chi, clo);
+    pdl_wait();  // partials come from sv_pass1
+    pdl_trigger();
+    const int nrows = greedy ? N : 2 * N - 1;
+    for (int r = warp; r < nrows; r += kTreeWarps) {
+        const float4 rs = combine_row(P, b, r, greedy, c, lane);
+        if (lane == 0) {
+            s_m[r] = rs.x;
+            s_S[r] = rs.y;
+            if (r < N) s_amax[r] = __float_as_int(rs.z);
+        }
+    }
+    __syncthreads();
+    if (greedy) {
+        if (tid == 0) greedy_tree_walk(P, b, N, s_amax, s_par, s_tok, out_nodes);
+        return;
+    }
+    int32_t *out = P.out_tokens + (size_t)b * N;
+    int32_t *nodes = out_nodes + (size_t)b * N;
+    if (tid == 0) flag_bad_tree(P, N, s_par);
+    int cur = 0, depth = 0;
+    for (;;) {
+        const char *rowt = row_ptr(P, b, cur, ESZ);
+        const bool inner = cur < N - 1;  // only such a node can have children (and a draft row)
+        const char *rowd = inner ? row_ptr(P, b, K + 1 + cur, ESZ) : rowt;
+        TreeNodeC nc;
+        nc.chi = make_float2(chi, chi);
+        nc.clo = make_float2(clo, clo);
+        const float mt = s_m[cur], St = s_S[cur];
+        const float md = inner ? s_m[K + 1 + cur] : 0.f, Sd = inner ? s_S[K + 1 + cur] : 1.f;
+        const float lt = -log2f(St), ld = -log2f(Sd);
+        nc.mt = make_float2(mt, mt);
+        nc.lt = make_float2(lt, lt);
+        nc.md = make_float2(md, md);
+        nc.ld = make_float2(ld, ld);
+        nc.dt = nc.dd = 0.f;
+        nc.J = 0;
+        nc.start = 0;
+        int next = -1;
+        for (int ch = cur + 1; ch < N; ++ch) {
+            if (s_par[ch] != cur) continue;
+            const int x = s_tok[ch];
+            if (x < 0 || x >= V) continue;
+            if (tid == 0) {
+                const float u = uniform_accept_f(P.seed, (uint32_t)b, (uint32_t)(ch - 1));
+                const float g = load_logit(rowt, DT, x), gd = load_logit(rowd, DT, x);
+                bool acc;
+                if (nc.J == 0) {
+                    acc = accept_position(u, g, mt, St, gd, md, Sd, chi, clo);
+                } else {
+                    const float a = weight1l(g, mt, chi, clo, lt), bq = weight1l(gd, md, chi, clo, ld);
+                    const float rx = tree_resid(a, bq, nc.dt, nc.dd, nc.J, nc.start, s_zinv);
+                    const float qx = __fmaf_rn(nc.dd, bq, bq);
+                    acc = (double)u * (double)qx * s_Z < (double)rx;
+                }
+                s_acc = acc;
+            }
+            __syncthreads();
+            if (s_acc) {
+                next = ch;
+                break;
+            }
+            ++nc.J;
+            bool more = false;  // another candidate follows: the residual's mass is needed
+            for (int c2 = ch + 1; c2 < N && !more; ++c2)
+                more = s_par[c2] == cur && s_tok[c2] >= 0 && s_tok[c2] < V;
+            if (!more && nc.J > 1) break;  // the recording pass below needs no mass
+            const int mode = nc.J == 1 ? kTreeModeFirst : kTreeModeResid;
+            tree_pass<DT, VEC>(rowt, rowd, V, nc, mode, false, s_zinv, s_red, s_mass, warp, lane);
+            __syncthreads();
+            if (tid == 0) {
+                double Z = 0.0;
+                if (mode == kTreeModeFirst) {
+                    double SA = 0.0, SB = 0.0;
+                    for (int w = 0; w < kTreeWarps; ++w) {
+                        SA += s_red[w][0];
+                        SB += s_red[w][1];
+                    }
+                    const double dt = 1.0 / SA - 1.0, dd = 1.0 / SB - 1.0;
+                    s_dt = (float)dt;
+                    s_dd = (float)dd;
+                    for (int w = 0; w < kTreeWarps; ++w) {  // sum over a > b of (p - q)
+                        const double D = s_red[w][2], Pb = s_red[w][3];
+                        Z += D + dt * (D + Pb) - dd * Pb;
+                    }
+                } else {
+                    for (int w = 0; w < kTreeWarps; ++w) Z += s_red[w][0];
+                }
+                if (Z > 0.0) {
+                    s_zinv[nc.J] = (float)(1.0 / Z);
+                    s_start = nc.start;
+                } else {  // no residual mass: the weights restart from p
+                    s_zinv[nc.J] = 1.f;
+                    Z = 1.0;
+                    s_start = nc.J;
+                }
+                s_Z = Z;
+            }
+            __syncthreads();
+            if (mode == kTreeModeFirst) {
+                nc.dt = s_dt;
+                nc.dd = s_dd;
+            }
+            nc.start = s_start;
+            if (!more) break;
+        }
+        if (next >= 0) {
+            if (tid == 0) {
+                out[depth] = s_tok[next];
+                nodes[depth] = next;
+            }
             cur = next;
             ++depth;
+            __syncthreads();  // s_acc / s_zinv are rewritten at the next node
+            continue;
         }
-        for (int i = depth + 1; i < N; ++i) out[i] = -1;
-        for (int i = depth; i < N; ++i) nodes[i] = -1;
-        P.accept_len[b] = depth;
-        if (bad && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_BAD_TREE);
+        // no child accepted: the emitted token from the current weights
+        const int mode = nc.J == 0 ? kTreeModeP : kTreeModeResid;
+        for (;;) {
+            tree_pass<DT, VEC>(rowt, rowd, V, nc, mode, true, s_zinv, s_red, s_mass, warp, lane);
+            __syncthreads();
+            if (tid == 0) {
+                double Z = 0.0;
+                for (int w = 0; w < kTreeWarps; ++w) Z += s_red[w][0];
+                s_again = 0;
+                if (!(Z > 0.0) && nc.J > 0 && nc.start != nc.J) {  // no residual mass: p
+                    s_zinv[nc.J] = 1.f;
+                    s_start = nc.J;
+                    s_again = 1;
+                }
+                const double thr = uniform_sample(P.seed, (uint32_t)b, (uint32_t)cur) * Z;
+                int W = -1;
+                double base = 0.0, run = 0.0, lbase = 0.0;
+                int lastw = -1;
+                for (int w = 0; w < kTreeWarps; ++w) {
+                    const double m = s_red[w][0];
+                    if (m > 0.0) {
+                        if (W < 0 && run + m > thr) {
+                            W = w;
+                            base = run;
+                        }
+                        lastw = w;
+                        lbase = run;
+                    }
+                    run += m;
+                }
+                if (W < 0) {  // rounding: the last warp with mass
+                    W = lastw;
+                    base = lbase;
+                }
+                s_W = W;
+                s_base = base;
+                s_thr = thr;
+                s_emit = V - 1;  // no mass at all
+            }
+            __syncthreads();
+            if (!s_again) break;
+            nc.start = s_start;
+        }
+        if (s_W >= 0 && warp == 0) {
+            const int tok = tree_find<DT, VEC>(rowt, rowd, V, nc, mode, s_zinv, s_mass, s_W, s_base,
+                                               s_thr, lane);
+            if (lane == 0 && tok >= 0) s_emit = tok;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            out[depth] = s_emit;
+            for (int i = depth + 1; i < N; ++i) out[i] = -1;
+            for (int i = depth; i < N; ++i) nodes[i] = -1;
+            P.accept_len[b] = depth;
+        }
+        return;
     }
 }
 
@@ -1786,6 +2345,74 @@ spec_status_t spec_verify_tree_greedy(const void *target_logits, spec_dtype_t dt
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaLaunchKernelEx(&cfg, sv::sv_tree_decide, P, parent, node_tokens, out_nodes);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status_t spec_verify_tree(const void *target_logits, const void *draft_logits,
+                               spec_dtype_t dtype, const int32_t *parent,
+                               const int32_t *node_tokens, const float *temperature, uint64_t seed,
+                               int B, int N, int V, int32_t *out_tokens, int32_t *out_nodes,
+                               int32_t *accept_len, void *workspace, size_t workspace_bytes,
+                               uint32_t *dev_status, void *stream) {
+    if (N < 1 || N > SPEC_MAX_TREE || B < 1 || B >= (1 << 24) || V < 2 || V > SPEC_MAX_V)
+        return SPEC_ERR_INVALID_ARG;
+    const int K = N - 1 > 0 ? N - 1 : 1;  // the workspace layout of K = N - 1
+    if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
+    if (!sv::items_fit(B, K, V, dtype)) return SPEC_ERR_UNSUPPORTED;
+    if (!target_logits || (N > 1 && !draft_logits) || !parent || !node_tokens || !temperature ||
+        !out_tokens || !out_nodes || !accept_len)
+        return SPEC_ERR_INVALID_ARG;
+    if (((uintptr_t)target_logits & 15u) || ((uintptr_t)draft_logits & 15u)) return SPEC_ERR_INVALID_ARG;
+    const sv::Layout L = sv::layout(B, K, V, dtype);
+    if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u))
+        return SPEC_ERR_WORKSPACE;
+    const sv::DevInfo *d = sv::dev_info();
+    if (!d) return SPEC_ERR_CUDA;
+    const int esz = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+    const bool vec = ((size_t)V * (size_t)esz) % 16u == 0;
+    sv::Params P{};
+    P.tgt = static_cast<const char *>(target_logits);
+    P.drf = static_cast<const char *>(N > 1 ? draft_logits : target_logits);
+    P.temperature = temperature;
+    P.seed = seed;
+    P.B = B;
+    P.K = N - 1;  // target slots 0..N-1 are the node rows, draft slots N..2N-2 the draft rows
+    P.V = V;
+    P.nchunk = (int)sv::nchunk_for(V, dtype);
+    P.npart = (int)sv::npart_for(V, dtype);
+    P.nslot = 2 * K + 1;
+    P.k0 = 0;
+    P.k1 = P.K;
+    P.out_tokens = out_tokens;
+    P.accept_len = accept_len;
+    P.dev_status = dev_status;
+    char *ws = static_cast<char *>(workspace);
+    P.row_count = reinterpret_cast<int *>(ws + L.row_count);
+    P.rows = reinterpret_cast<int4 *>(ws + L.rows);
+    P.part = reinterpret_cast<float4 *>(ws + L.part);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    sv::sv_tree_rows_s<<<1, sv::kPrepThreads, 0, s>>>(P);
+    const int g1 = d->sms * d->occ_p1[dtype == SPEC_DTYPE_BF16 ? sv::kBF16 : sv::kF32][vec ? 1 : 0];
+    void (*walk)(sv::Params, const int32_t *, const int32_t *, int32_t *);
+    if (dtype == SPEC_DTYPE_BF16) {
+        if (vec) sv::launch_dependent(sv::sv_pass1<sv::kBF16, true>, g1, sv::kP1Warps * 32, sv::kP1Smem, s, P);
+        else sv::launch_dependent(sv::sv_pass1<sv::kBF16, false>, g1, sv::kP1Warps * 32, 0, s, P);
+        walk = vec ? sv::sv_tree_walk<sv::kBF16, true> : sv::sv_tree_walk<sv::kBF16, false>;
+    } else {
+        if (vec) sv::launch_dependent(sv::sv_pass1<sv::kF32, true>, g1, sv::kP1Warps * 32, sv::kP1Smem, s, P);
+        else sv::launch_dependent(sv::sv_pass1<sv::kF32, false>, g1, sv::kP1Warps * 32, 0, s, P);
+        walk = vec ? sv::sv_tree_walk<sv::kF32, true> : sv::sv_tree_walk<sv::kF32, false>;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)B);
+    cfg.blockDim = dim3(sv::kTreeThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, walk, P, parent, node_tokens, out_nodes);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -83,3 +83,123 @@ def test_invalid_parents_flagged(sv):
     for b in range(4):
         ot, on, a = oracle.verify_tree_greedy(h_t[b], parent[b].cpu().numpy(), tok[b].cpu().numpy())
         assert acc[b].item() == a and np.array_equal(out[b].cpu().numpy(), ot)
+
+
+# ---------------------------------------------------------------- sampled trees
+
+# Near-tie window of the sampled tree walk: the residual after a rejection is
+# formed from float weights whose exp2 carries ~2^-22 relative error, so its
+# normalised CDF is known to ~1e-6 / Z; a request may differ from the oracle
+# only when the oracle's uniform lies within this distance of a decision
+# boundary.
+TREE_NEAR_TIE = 1e-5
+
+
+def _oracle_tree(inp):
+    """Oracle results for the whole batch (Philox keys use the request index).
+    The draft rows are padded to N with zeros: the last node has no children,
+    so the oracle never reads that row."""
+    t = workloads.to_numpy_logits(inp["target"])
+    B, N, V = t.shape
+    d = workloads.to_numpy_logits(inp["draft"]) if N > 1 else np.zeros((B, 0, V), t.dtype)
+    d = np.concatenate([d, np.zeros((B, 1, V), d.dtype)], axis=1)
+    return oracle.verify_tree(t, d, inp["parent"].cpu().numpy(), inp["tokens"].cpu().numpy(),
+                              inp["temperature"].cpu().numpy(), inp["seed"])
+
+
+def _compare_tree(sv, inp, max_flag_frac=0.1):
+    """GPU against the oracle: every request equal unless the oracle flags a
+    near tie; returns the GPU outputs and the device status."""
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, nodes, acc = sv.verify_tree(inp["target"], inp["draft"], inp["parent"], inp["tokens"],
+                                     inp["temperature"], inp["seed"], dev_status=st)
+    torch.cuda.synchronize()
+    out, nodes, acc = out.cpu().numpy(), nodes.cpu().numpy(), acc.cpu().numpy()
+    r = _oracle_tree(inp)
+    same = ((acc == r["accept_len"]) & (out == r["out_tokens"]).all(axis=1)
+            & (nodes == r["out_nodes"]).all(axis=1))
+    flagged = (r["accept_margin"] < TREE_NEAR_TIE) | (r["cdf_margin"] < TREE_NEAR_TIE)
+    bad = np.flatnonzero(~same & ~flagged)
+    assert bad.size == 0, (bad, acc[bad], r["accept_len"][bad])
+    assert flagged.sum() <= max_flag_frac * len(acc) + 1, flagged.sum()
+    return out, nodes, acc, int(st.item())
+
+
+@pytest.mark.parametrize("B,N,V,dtype,T", [
+    (48, 1, 1000, torch.bfloat16, 1.0), (48, 2, 1000, torch.bfloat16, 1.0),
+    (32, 9, 3000, torch.float32, 0.8), (16, 16, 4096 + 8, torch.bfloat16, 1.3),
+    (8, 33, 1001, torch.bfloat16, 1.0), (6, 17, 151936, torch.bfloat16, 1.0),
+    (12, 64, 2048, torch.bfloat16, 0.7), (8, 12, 999, torch.float32, 1.0),
+])
+def test_sampled_trees_against_oracle(sv, B, N, V, dtype, T):
+    inp = workloads.make_tree_inputs(B, N, V, dtype, seed=B * 1000 + N + V, T=T,
+                                     n_greedy=B // 8)
+    out, nodes, acc, st = _compare_tree(sv, inp)
+    assert st == 0
+    if N > 3:
+        assert acc.max() >= 2  # some paths go past the first level
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 4])
+def test_sampled_chain_trees_equal_linear(sv, cfg):
+    """A chain tree is the linear draft, with the same rows, tokens and Philox
+    keys: the tree walk gives spec_verify's outputs, except where the oracle
+    flags a near tie (the two paths form the residual differently)."""
+    inp = workloads.make_inputs(cfg, rep=9, B=64)
+    B, K1, V = inp["target"].shape
+    out_l, acc_l = sv.verify(inp["target"], inp["draft"], inp["tokens"], inp["verify_len"],
+                             inp["temperature"], inp["seed"])
+    parent = torch.arange(-1, K1 - 1, dtype=torch.int32, device="cuda").expand(B, K1).contiguous()
+    tok = torch.cat([torch.zeros((B, 1), dtype=torch.int32, device="cuda"), inp["tokens"]], dim=1)
+    out_t, nodes, acc_t = sv.verify_tree(inp["target"], inp["draft"], parent, tok.contiguous(),
+                                         inp["temperature"], inp["seed"])
+    torch.cuda.synchronize()
+    diff = torch.nonzero((acc_t != acc_l) | (out_t != out_l).any(dim=1)).flatten().tolist()
+    assert len(diff) <= B // 10, diff
+    if diff:
+        h_t = workloads.to_numpy_logits(inp["target"])
+        h_d = workloads.to_numpy_logits(inp["draft"])
+        r = oracle.verify(h_t, h_d, inp["tokens"].cpu().numpy(), None,
+                          inp["temperature"].cpu().numpy(), inp["seed"])
+        for b in diff:
+            assert min(r["accept_margin"][b], r["cdf_margin"][b]) < TREE_NEAR_TIE, b
+    a = acc_t.cpu().numpy()
+    n = nodes.cpu().numpy()
+    for b in range(B):
+        assert n[b, :a[b]].tolist() == list(range(1, a[b] + 1))
+
+
+def test_sampled_edge_cases(sv):
+    """Invalid tokens (no candidate), invalid parents (no path through them,
+    SPEC_DEV_BAD_TREE), a node whose children all carry tokens with zero draft
+    mass, and duplicated sibling tokens."""
+    inp = workloads.make_tree_inputs(8, 10, 700, torch.bfloat16, seed=77, T=1.0)
+    tok, par = inp["tokens"].clone(), inp["parent"].clone()
+    tok[0, 1:4] = torch.tensor([-5, 700, 10 ** 6], dtype=torch.int32)
+    par[1, 4] = 7          # not an earlier node
+    par[2, 5] = -3
+    par[3, 1:] = 0         # nine siblings under the root
+    tok[3, 1:] = tok[3, 1]  # all carrying the same token
+    dr = inp["draft"].clone()
+    dr[4, 0, :] = float("-inf")
+    dr[4, 0, 5] = 0.0      # the root's draft is a point mass on token 5
+    par[4, 1:4] = 0
+    tok[4, 1:4] = torch.tensor([5, 6, 5], dtype=torch.int32)
+    inp.update(tokens=tok.contiguous(), parent=par.contiguous(), draft=dr.contiguous())
+    out, nodes, acc, st = _compare_tree(sv, inp, max_flag_frac=0.3)
+    assert st & sv.DEV_BAD_TREE
+
+
+def test_greedy_requests_take_the_greedy_walk(sv):
+    inp = workloads.make_tree_inputs(16, 12, 2000, torch.bfloat16, seed=5, n_greedy=16)
+    out, nodes, acc = sv.verify_tree(inp["target"], inp["draft"], inp["parent"], inp["tokens"],
+                                     inp["temperature"], inp["seed"])
+    out_g, nodes_g, acc_g = sv.verify_tree_greedy(inp["target"], inp["parent"], inp["tokens"])
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_g) and torch.equal(nodes, nodes_g) and torch.equal(acc, acc_g)
+
+
+def test_sampled_tree_mismatch_rate(sv):
+    """Many small requests: no unflagged mismatch and few flagged ones."""
+    inp = workloads.make_tree_inputs(2048, 8, 512, torch.bfloat16, seed=31, T=1.0)
+    _compare_tree(sv, inp, max_flag_frac=0.02)

@@ -124,6 +124,46 @@ def make_inputs(cfg: int, rep: int = 0, device="cuda", B=None, V=None, K=None, g
     return out
 
 
+def make_tree_inputs(B, N, V, dtype=torch.bfloat16, seed=0, T=1.0, sigma=2.5, noise=0.7,
+                     chain_prob=0.5, n_greedy=0, device="cuda"):
+    """Seeded candidate trees: target [B, N, V] ~ N(0, sigma); draft [B, N-1, V] =
+    target rows + N(0, noise); node n >= 1 hangs under node n - 1 with
+    probability chain_prob, else under a uniformly drawn earlier node; its
+    token is a multinomial draw from softmax(draft row of its parent / T)
+    (independently for siblings), the argmax of that row for greedy requests.
+    The first n_greedy requests are greedy (T = 0).  Returns dict(target,
+    draft, parent, tokens, temperature, seed)."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev).manual_seed(int(seed))
+    target = (torch.randn((B, N, V), generator=g, device=dev) * sigma).to(dtype)
+    draft = (target[:, :max(N - 1, 0)].float()
+             + torch.randn((B, max(N - 1, 0), V), generator=g, device=dev) * noise).to(dtype)
+    gc = torch.Generator().manual_seed(int(seed) + 1)
+    parent = torch.full((B, N), -1, dtype=torch.int64)
+    for n in range(1, N):
+        chain = torch.rand((B,), generator=gc) < chain_prob
+        anyp = torch.randint(0, n, (B,), generator=gc)
+        parent[:, n] = torch.where(chain, torch.full((B,), n - 1), anyp)
+    temp = torch.full((B,), float(T), dtype=torch.float32, device=dev)
+    temp[:n_greedy] = 0.0
+    tokens = torch.zeros((B, N), dtype=torch.int64, device=dev)
+    if N > 1:
+        par = parent[:, 1:].to(dev)
+        chunk = max(1, (1 << 26) // ((N - 1) * V))
+        for b0 in range(0, B, chunk):
+            b1 = min(B, b0 + chunk)
+            rows = torch.gather(draft[b0:b1], 1,
+                                par[b0:b1].view(b1 - b0, N - 1, 1).expand(-1, -1, V)).float()
+            tb = temp[b0:b1].view(-1, 1, 1)
+            sampled = tb > 0
+            probs = torch.softmax(rows / torch.where(sampled, tb, torch.ones_like(tb)), dim=-1)
+            draws = torch.multinomial(probs.view(-1, V), 1, generator=g).view(b1 - b0, N - 1)
+            tokens[b0:b1, 1:] = torch.where(sampled.view(-1, 1), draws, rows.argmax(dim=-1))
+    return dict(target=target.contiguous(), draft=draft.contiguous(),
+                parent=parent.to(torch.int32).to(dev).contiguous(),
+                tokens=tokens.to(torch.int32).contiguous(), temperature=temp, seed=int(seed) * 7 + 3)
+
+
 def algorithmic_bytes(temperature, verify_len, V, esize):
     """Bytes the step must read, each needed row once: (2L+1) rows of V logits
     for a sampled request, (L+1) for a greedy one."""
