@@ -1376,26 +1376,17 @@ __device__ __forceinline__ float weight1l(float z, float m, float chi, float clo
     return ex2(__fmaf_rn(d, chi, __fmaf_rn(d, clo, l)));
 }
 
-// The residual weight of an element after J >= 1 rejected siblings.  a and b
-// are the element's target and draft weights (close to normalised); the exact
-// normalisers are 1 + dt and 1 + dd, so p = a + dt a and q = b + dd b.
-// r_1 = max(0, p - q), formed as (a - b) + (dt a - dd b) to keep its rounding
-// relative to itself; r_j = max(0, r_(j-1) / Z_(j-1) - q).  After a residual of
-// zero mass at rejection `start` the weights restart from p.
-__device__ __forceinline__ float tree_resid(float a, float b, float dt, float dd, int J, int start,
-                                            const float *zinv) {
-    const float q = __fmaf_rn(dd, b, b);
-    float r;
-    int j;
-    if (start == 0) {
-        r = fmaxf(__fadd_rn(__fsub_rn(a, b), __fmaf_rn(dt, a, -__fmul_rn(dd, b))), 0.f);
-        j = 2;
-    } else {
-        r = __fmaf_rn(dt, a, a);
-        j = start + 1;
-    }
-    for (; j <= J; ++j) r = fmaxf(__fmaf_rn(r, zinv[j - 1], -q), 0.f);
-    return r;
+// Residual after j rejected siblings, in closed form.  With p, q the target
+// and draft distributions, r_1 = max(0, p - q) and r_(j+1) = max(0, r_j / Z_j
+// - q) give r_j = c_j max(0, p - t_j q) for a scale c_j and the threshold
+// t_1 = 1, t_(j+1) = t_j + sum_v max(0, p - t_j q): the scale cancels in the
+// acceptance test and the inverse CDF, so only the threshold is carried.  In
+// the weights a, b (p = a / A, q = b / B with A, B their exact sums) the
+// residual is proportional to max(0, a - s b), s = t A / B, and
+// s_1 = A / B, s_(j+1) = s_j + S_j / B with S_j = sum_v max(0, a - s_j b).
+// s = 0 stands for the weights p themselves (a restart after zero mass).
+__device__ __forceinline__ float resid_weight(float a, float b, float s) {
+    return fmaxf(__fmaf_rn(-s, b, a), 0.f);
 }
 
 // Elements [e0, e0 + 8) of a row as 4 pairs (-inf past V).
@@ -1415,20 +1406,18 @@ template <int DT, bool VEC> struct Eight {
 // Per-node constants of the sampled walk.
 struct TreeNodeC {
     float2 mt, lt, md, ld, chi, clo;  // row max and log2(1/S) of the target and draft rows, c
-    float dt, dd;                     // exact normalisers - 1 (after the first rejection)
-    int J, start;                     // rejections so far; restart point of the residual
+    float s;                          // residual threshold (0: the weights p)
 };
 
 // Weights a pass sums: the target weights a; the parts of the first residual
 // (sum a, sum b, sum over a > b of (a - b), sum over a > b of b); the residual
-// after J rejections.
-enum { kTreeModeP = 0, kTreeModeFirst = 1, kTreeModeResid = 2 };
+// max(0, a - s b).
+enum { kTreeModeP = 0, kTreeModeFirst = 1, kTreeModeThr = 2 };
 
-// The 8 weights of a lane at e0 in a pass of mode P or Resid.
+// The 8 weights of a lane in a pass of mode P or Thr.
 template <int DT, bool VEC>
 __device__ __forceinline__ void tree_weights8(const Eight<DT, VEC> &zt, const Eight<DT, VEC> &zd,
-                                              const TreeNodeC &nc, int mode, const float *zinv,
-                                              float w[8]) {
+                                              const TreeNodeC &nc, int mode, float w[8]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const float2 a = weight2l(zt.pair(i), nc.mt, nc.chi, nc.clo, nc.lt);
@@ -1437,35 +1426,63 @@ __device__ __forceinline__ void tree_weights8(const Eight<DT, VEC> &zt, const Ei
             w[2 * i + 1] = a.y;
         } else {
             const float2 bq = weight2l(zd.pair(i), nc.md, nc.chi, nc.clo, nc.ld);
-            w[2 * i] = tree_resid(a.x, bq.x, nc.dt, nc.dd, nc.J, nc.start, zinv);
-            w[2 * i + 1] = tree_resid(a.y, bq.y, nc.dt, nc.dd, nc.J, nc.start, zinv);
+            w[2 * i] = resid_weight(a.x, bq.x, nc.s);
+            w[2 * i + 1] = resid_weight(a.y, bq.y, nc.s);
         }
     }
 }
 
-// Steps of warp w: [s0, s1) of kTreeStep elements; recorded masses cover
-// groups of gsz consecutive steps.
+// The CTAs of a cluster share one request: CTA `rank` of `cs` covers a
+// contiguous slice of the steps of kTreeStep elements, and its warp w the
+// steps [s0, s1) of that slice; recorded masses cover groups of gsz
+// consecutive steps.
 struct TreeSplit {
     int s0, s1, gsz;
-    __device__ __forceinline__ TreeSplit(int V, int w) {
+    __device__ __forceinline__ TreeSplit(int V, int rank, int cs, int w) {
         const int nsteps = (V + kTreeStep - 1) / kTreeStep;
-        const int spw = (nsteps + kTreeWarps - 1) / kTreeWarps;
-        s0 = min(nsteps, w * spw);
-        s1 = min(nsteps, s0 + spw);
-        gsz = (spw + kTreeGroups - 1) / kTreeGroups;
+        const int spc = (nsteps + cs - 1) / cs;
+        const int c0 = min(nsteps, rank * spc), c1 = min(nsteps, c0 + spc);
+        const int spw = (c1 - c0 + kTreeWarps - 1) / kTreeWarps;
+        s0 = min(c1, c0 + w * spw);
+        s1 = min(c1, s0 + spw);
+        gsz = max(1, (spw + kTreeGroups - 1) / kTreeGroups);
     }
 };
 
-// One pass of the CTA over the vocabulary.  Warp w covers its contiguous steps,
+// Cluster primitives: this CTA's rank and the cluster's size, a barrier of all
+// threads of the cluster (release / acquire), and a double read from the
+// shared memory of CTA `rank` at the address of `local` in this CTA.
+__device__ __forceinline__ int cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return (int)r;
+}
+__device__ __forceinline__ int cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return (int)r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ double ld_cluster_f64(const double *local, int rank) {
+    uint32_t ra;
+    double v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(ra) : "memory");
+    return v;
+}
+
+// One pass of the CTA over its slice of the vocabulary.  Warp w covers its contiguous steps,
 // lane l the 8 elements at 8 l of each step, kU steps' loads in flight.  Writes
 // the warp's sums (as doubles) to red[w]; with `record`, also the mass of each
 // group of steps to mass[w * kTreeGroups + g] and the warp's total as their sum.
 template <int DT, bool VEC>
-__device__ void tree_pass(const char *rowt, const char *rowd, int V, const TreeNodeC &nc, int mode,
-                          bool record, const float *zinv, double (*red)[4], float *mass, int warp,
-                          int lane) {
+__device__ void tree_pass(const char *rowt, const char *rowd, int V, int rank, int cs,
+                          const TreeNodeC &nc, int mode, bool record, double (*red)[4], float *mass,
+                          int warp, int lane) {
     constexpr int kU = DT == kBF16 ? 4 : 2;
-    const TreeSplit sp(V, warp);
+    const TreeSplit sp(V, rank, cs, warp);
     BiasAcc2 acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i].init(kTreeBias);
@@ -1483,39 +1500,41 @@ __device__ void tree_pass(const char *rowt, const char *rowd, int V, const TreeN
         }
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-            if (st0 + u >= sp.s1) break;
-            if (mode == kTreeModeFirst) {
+            if (st0 + u < sp.s1) {
+                if (mode == kTreeModeFirst) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 a = weight2l(zt[u].pair(i), nc.mt, nc.chi, nc.clo, nc.lt);
-                    const float2 bq = weight2l(zd[u].pair(i), nc.md, nc.chi, nc.clo, nc.ld);
-                    acc[0].add(a);
-                    acc[1].add(bq);
-                    const bool gx = a.x > bq.x, gy = a.y > bq.y;
-                    acc[2].add(make_float2(gx ? __fsub_rn(a.x, bq.x) : 0.f, gy ? __fsub_rn(a.y, bq.y) : 0.f));
-                    acc[3].add(make_float2(gx ? bq.x : 0.f, gy ? bq.y : 0.f));
-                }
-                continue;
-            }
-            float w[8];
-            tree_weights8<DT, VEC>(zt[u], zd[u], nc, mode, zinv, w);
-            if (record) {
-                float ls = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) ls = __fadd_rn(ls, w[i]);
-                gs = __fadd_rn(gs, ls);
-                const int k = st0 + u - sp.s0;
-                if ((k + 1) % sp.gsz == 0 || st0 + u + 1 == sp.s1) {
-                    const float gm = warp_sum(gs);
-                    if (lane == 0) {
-                        mass[warp * kTreeGroups + k / sp.gsz] = gm;
-                        mw += (double)gm;
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 a = weight2l(zt[u].pair(i), nc.mt, nc.chi, nc.clo, nc.lt);
+                        const float2 bq = weight2l(zd[u].pair(i), nc.md, nc.chi, nc.clo, nc.ld);
+                        acc[0].add(a);
+                        acc[1].add(bq);
+                        const bool gx = a.x > bq.x, gy = a.y > bq.y;
+                        acc[2].add(make_float2(gx ? __fsub_rn(a.x, bq.x) : 0.f,
+                                               gy ? __fsub_rn(a.y, bq.y) : 0.f));
+                        acc[3].add(make_float2(gx ? bq.x : 0.f, gy ? bq.y : 0.f));
                     }
-                    gs = 0.f;
-                }
-            } else {
+                } else {
+                    float w[8];
+                    tree_weights8<DT, VEC>(zt[u], zd[u], nc, mode, w);
+                    if (record) {
+                        float ls = 0.f;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) acc[0].add(make_float2(w[2 * i], w[2 * i + 1]));
+                        for (int i = 0; i < 8; ++i) ls = __fadd_rn(ls, w[i]);
+                        gs = __fadd_rn(gs, ls);
+                        const int k = st0 + u - sp.s0;
+                        if ((k + 1) % sp.gsz == 0 || st0 + u + 1 == sp.s1) {
+                            const float gm = warp_sum(gs);
+                            if (lane == 0) {
+                                mass[warp * kTreeGroups + k / sp.gsz] = gm;
+                                mw += (double)gm;
+                            }
+                            gs = 0.f;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[0].add(make_float2(w[2 * i], w[2 * i + 1]));
+                    }
+                }
             }
         }
     }
@@ -1536,18 +1555,19 @@ __device__ void tree_pass(const char *rowt, const char *rowd, int V, const TreeN
 // element.  Rounding that leaves the crossing outside takes the last positive
 // weight met.
 template <int DT, bool VEC>
-__device__ int tree_find(const char *rowt, const char *rowd, int V, const TreeNodeC &nc, int mode,
-                         const float *zinv, const float *mass, int W, double base, double thr,
-                         int lane) {
-    const TreeSplit sp(V, W);
+__device__ int tree_find(const char *rowt, const char *rowd, int V, int rank, int cs,
+                         const TreeNodeC &nc, int mode, const float *mass, int W, double base,
+                         double thr, int lane) {
+    const TreeSplit sp(V, rank, cs, W);
     const int ng = (sp.s1 - sp.s0 + sp.gsz - 1) / sp.gsz;
-    // the group: lane l sums groups [8 l, 8 l + 8) of W
-    constexpr int kPer = kTreeGroups / 32;
+    constexpr int kPer = kTreeGroups / 32;  // lane l holds groups [kPer l, kPer (l + 1))
+    float gm[kPer];
     double ls = 0.0;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
         const int g = lane * kPer + i;
-        if (g < ng) ls += (double)mass[W * kTreeGroups + g];
+        gm[i] = g < ng ? mass[W * kTreeGroups + g] : 0.f;
+        ls += (double)gm[i];
     }
     double incl = ls;
 #pragma unroll
@@ -1555,58 +1575,26 @@ __device__ int tree_find(const char *rowt, const char *rowd, int V, const TreeNo
         const double v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
         if (lane >= o) incl += v;
     }
-    unsigned cross = __ballot_sync(0xFFFFFFFFu, base + incl > thr && ls > 0.0);
+    const unsigned cross = __ballot_sync(0xFFFFFFFFu, base + incl > thr && ls > 0.0);
+    const unsigned has = __ballot_sync(0xFFFFFFFFu, ls > 0.0);
+    if (!has) return -1;
+    // the crossing lane, else (rounding) the last lane with mass
+    const int src = cross ? __ffs(cross) - 1 : 31 - __clz(has);
     int g = -1;
     double gbase = 0.0;
-    if (lane == (cross ? __ffs(cross) - 1 : 31)) {
+    if (lane == src) {
         double c = base + incl - ls;
-        int last = -1;
-        double last_base = 0.0;
+#pragma unroll
         for (int i = 0; i < kPer; ++i) {
-            const int gi = lane * kPer + i;
-            if (gi >= ng) break;
-            const double m = (double)mass[W * kTreeGroups + gi];
-            if (m > 0.0) {
-                last = gi;
-                last_base = c;
-            }
-            if (m > 0.0 && c + m > thr) {
-                g = gi;
+            if (gm[i] > 0.f && (g < 0 || c <= thr)) {
+                g = lane * kPer + i;
                 gbase = c;
-                break;
             }
-            c += m;
-        }
-        if (g < 0) {
-            g = last;
-            gbase = last_base;
+            c += (double)gm[i];
         }
     }
-    const int src = cross ? __ffs(cross) - 1 : 31;
     g = __shfl_sync(0xFFFFFFFFu, g, src);
     gbase = __shfl_sync(0xFFFFFFFFu, gbase, src);
-    if (g < 0) {  // no mass among the lanes' blocks: the last group with mass
-        const unsigned has = __ballot_sync(0xFFFFFFFFu, ls > 0.0);
-        if (!has) return -1;
-        const int L = 31 - __clz(has);
-        int gl = -1;
-        double bl = 0.0;
-        if (lane == L) {
-            double c = base + incl - ls;
-            for (int i = 0; i < kPer; ++i) {
-                const int gi = lane * kPer + i;
-                if (gi >= ng) break;
-                const double m = (double)mass[W * kTreeGroups + gi];
-                if (m > 0.0) {
-                    gl = gi;
-                    bl = c;
-                }
-                c += m;
-            }
-        }
-        g = __shfl_sync(0xFFFFFFFFu, gl, L);
-        gbase = __shfl_sync(0xFFFFFFFFu, bl, L);
-    }
     // the steps of group g, in order
     const int st_a = sp.s0 + g * sp.gsz, st_b = min(sp.s1, st_a + sp.gsz);
     double b0 = gbase;
@@ -1617,7 +1605,7 @@ __device__ int tree_find(const char *rowt, const char *rowd, int V, const TreeNo
         zt.load(rowt, e0, V);
         if (mode != kTreeModeP) zd.load(rowd, e0, V);
         float w[8];
-        tree_weights8<DT, VEC>(zt, zd, nc, mode, zinv, w);
+        tree_weights8<DT, VEC>(zt, zd, nc, mode, w);
         double s8 = 0.0;
         int lp = -1;
 #pragma unroll
@@ -1632,7 +1620,7 @@ __device__ int tree_find(const char *rowt, const char *rowd, int V, const TreeNo
             if (lane >= o) in8 += v;
         }
         const unsigned cr = __ballot_sync(0xFFFFFFFFu, b0 + in8 > thr && s8 > 0.0);
-        const int lp_max = __reduce_max_sync(0xFFFFFFFFu, (unsigned)(lp + 1)) - 1;
+        const int lp_max = (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)(lp + 1)) - 1;
         if (cr) {
             const int L = __ffs(cr) - 1;
             int tok = -1;
@@ -1652,36 +1640,57 @@ __device__ int tree_find(const char *rowt, const char *rowd, int V, const TreeNo
     return last_pos;
 }
 
-// Sampled verification of candidate trees, one CTA per request (greedy
-// requests take the greedy walk).  At node u the first child is checked with
-// the linear acceptance test; every rejection followed by another candidate
-// updates the residual with one pass over the vocabulary (its mass Z_J),
+// Sampled verification of candidate trees by a cluster of CTAs per request
+// (greedy requests take the greedy walk).  At node u the first child is
+// checked with the linear acceptance test; after j rejections the residual is
+// max(0, a - s_j b) (see resid_weight), and a rejection followed by another
+// candidate costs one pass over the vocabulary for the residual's mass S_j,
 // against which the next sibling is checked: accept iff
-// u_acc * q(x) * Z_J < r_J(x).  When no child is accepted a recording pass over
-// the current weights (p, or the last residual) and an inverse CDF give the
+// u_acc * b(x) * S_j < B * max(0, a(x) - s_j b(x)).  When no child is accepted
+// a recording pass over the current weights and an inverse CDF give the
 // emitted token.  Candidate node c takes the acceptance uniform of position
 // c - 1, node u's emitted token the sampling uniform of position u.
+// Each CTA of the cluster passes over its slice of the vocabulary; the sums
+// are exchanged through distributed shared memory and added in rank order by
+// every CTA, so all CTAs take the same decisions and meet the same cluster
+// barriers.
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const int32_t *parent,
                                                                const int32_t *token,
                                                                int32_t *out_nodes) {
     __shared__ int s_par[SPEC_MAX_TREE], s_tok[SPEC_MAX_TREE], s_amax[SPEC_MAX_TREE];
     __shared__ float s_m[2 * SPEC_MAX_TREE], s_S[2 * SPEC_MAX_TREE];
-    __shared__ float s_zinv[SPEC_MAX_TREE];
+    __shared__ float s_u[SPEC_MAX_TREE], s_g[SPEC_MAX_TREE], s_gd[SPEC_MAX_TREE];
+    __shared__ double s_us[SPEC_MAX_TREE];
     __shared__ float s_mass[kTreeWarps * kTreeGroups];
     __shared__ double s_red[kTreeWarps][4];
-    __shared__ float s_dt, s_dd;
-    __shared__ double s_Z, s_base, s_thr;
-    __shared__ int s_start, s_acc, s_W, s_emit, s_again;
+    __shared__ double s_slot[2][4];   // this CTA's sums, read by the cluster (two buffers)
+    __shared__ double s_sum;          // S_j of the current residual
+    __shared__ double s_SA, s_SB;     // exact sums of a and b at the node
+    __shared__ double s_base, s_thr;
+    __shared__ float s_s;
+    __shared__ int s_acc, s_R, s_W, s_emit, s_again;
     constexpr int ESZ = Fmt<DT>::kESZ;
-    const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cs = cluster_size(), rank = cluster_rank();
+    const int b = blockIdx.x / cs, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int N = P.K + 1, K = P.K, V = P.V;
-    for (int i = tid; i < N; i += kTreeThreads) {
-        s_par[i] = parent[(size_t)b * N + i];
-        s_tok[i] = token[(size_t)b * N + i];
-    }
     const float T = P.temperature[b];
     const bool greedy = !(isfinite(T) && T >= FLT_MIN);
+    // inputs only (nothing from the statistics pass): tree, uniforms, candidate logits
+    for (int i = tid; i < N; i += kTreeThreads) {
+        const int pa = parent[(size_t)b * N + i], x = token[(size_t)b * N + i];
+        s_par[i] = pa;
+        s_tok[i] = x;
+        if (!greedy) {
+            s_us[i] = uniform_sample(P.seed, (uint32_t)b, (uint32_t)i);
+            if (i > 0) {
+                s_u[i] = uniform_accept_f(P.seed, (uint32_t)b, (uint32_t)(i - 1));
+                const bool ok = pa >= 0 && pa < i && x >= 0 && x < V;
+                s_g[i] = ok ? load_logit(row_ptr(P, b, pa, ESZ), DT, x) : 0.f;
+                s_gd[i] = ok ? load_logit(row_ptr(P, b, K + 1 + pa, ESZ), DT, x) : 0.f;
+            }
+        }
+    }
     float c = 0.f, chi = 0.f, clo = 0.f;
     if (!greedy) temp_coeffs(T, c, chi, clo);
     pdl_wait();  // partials come from sv_pass1
@@ -1696,13 +1705,14 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
         }
     }
     __syncthreads();
-    if (greedy) {
-        if (tid == 0) greedy_tree_walk(P, b, N, s_amax, s_par, s_tok, out_nodes);
+    if (greedy) {  // no cluster exchange: rank 0 walks, the others leave
+        if (tid == 0 && rank == 0) greedy_tree_walk(P, b, N, s_amax, s_par, s_tok, out_nodes);
         return;
     }
     int32_t *out = P.out_tokens + (size_t)b * N;
     int32_t *nodes = out_nodes + (size_t)b * N;
-    if (tid == 0) flag_bad_tree(P, N, s_par);
+    if (tid == 0 && rank == 0) flag_bad_tree(P, N, s_par);
+    int par = 0;  // slot buffer of the next exchange
     int cur = 0, depth = 0;
     for (;;) {
         const char *rowt = row_ptr(P, b, cur, ESZ);
@@ -1718,25 +1728,21 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
         nc.lt = make_float2(lt, lt);
         nc.md = make_float2(md, md);
         nc.ld = make_float2(ld, ld);
-        nc.dt = nc.dd = 0.f;
-        nc.J = 0;
-        nc.start = 0;
-        int next = -1;
+        nc.s = 0.f;
+        int J = 0, next = -1;
         for (int ch = cur + 1; ch < N; ++ch) {
             if (s_par[ch] != cur) continue;
             const int x = s_tok[ch];
             if (x < 0 || x >= V) continue;
             if (tid == 0) {
-                const float u = uniform_accept_f(P.seed, (uint32_t)b, (uint32_t)(ch - 1));
-                const float g = load_logit(rowt, DT, x), gd = load_logit(rowd, DT, x);
+                const float u = s_u[ch], g = s_g[ch], gd = s_gd[ch];
                 bool acc;
-                if (nc.J == 0) {
+                if (J == 0) {
                     acc = accept_position(u, g, mt, St, gd, md, Sd, chi, clo);
                 } else {
                     const float a = weight1l(g, mt, chi, clo, lt), bq = weight1l(gd, md, chi, clo, ld);
-                    const float rx = tree_resid(a, bq, nc.dt, nc.dd, nc.J, nc.start, s_zinv);
-                    const float qx = __fmaf_rn(nc.dd, bq, bq);
-                    acc = (double)u * (double)qx * s_Z < (double)rx;
+                    const float w = nc.s > 0.f ? resid_weight(a, bq, nc.s) : a;
+                    acc = (double)u * (double)bq * s_sum < (double)w * s_SB;
                 }
                 s_acc = acc;
             }
@@ -1745,115 +1751,154 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
                 next = ch;
                 break;
             }
-            ++nc.J;
+            ++J;
             bool more = false;  // another candidate follows: the residual's mass is needed
             for (int c2 = ch + 1; c2 < N && !more; ++c2)
                 more = s_par[c2] == cur && s_tok[c2] >= 0 && s_tok[c2] < V;
-            if (!more && nc.J > 1) break;  // the recording pass below needs no mass
-            const int mode = nc.J == 1 ? kTreeModeFirst : kTreeModeResid;
-            tree_pass<DT, VEC>(rowt, rowd, V, nc, mode, false, s_zinv, s_red, s_mass, warp, lane);
+            if (J > 1) {  // the threshold after this rejection
+                if (tid == 0) s_s = nc.s > 0.f ? (float)((double)nc.s + s_sum / s_SB) : (float)(s_SA / s_SB);
+                __syncthreads();
+                nc.s = s_s;
+                if (!more) break;  // the recording pass below needs no mass
+            }
+            const int mode = J == 1 ? kTreeModeFirst : kTreeModeThr;
+            tree_pass<DT, VEC>(rowt, rowd, V, rank, cs, nc, mode, false, s_red, s_mass, warp, lane);
             __syncthreads();
+            const int nsum = mode == kTreeModeFirst ? 4 : 1;
+            if (tid == 0)
+                for (int i = 0; i < nsum; ++i) {
+                    double v = 0.0;
+                    for (int w = 0; w < kTreeWarps; ++w) v += s_red[w][i];
+                    s_slot[par][i] = v;
+                }
+            cluster_sync_all();
             if (tid == 0) {
-                double Z = 0.0;
+                double tot[4] = {0.0, 0.0, 0.0, 0.0};
+                for (int r = 0; r < cs; ++r)
+                    for (int i = 0; i < nsum; ++i) tot[i] += ld_cluster_f64(&s_slot[par][i], r);
+                double S;
                 if (mode == kTreeModeFirst) {
-                    double SA = 0.0, SB = 0.0;
-                    for (int w = 0; w < kTreeWarps; ++w) {
-                        SA += s_red[w][0];
-                        SB += s_red[w][1];
-                    }
-                    const double dt = 1.0 / SA - 1.0, dd = 1.0 / SB - 1.0;
-                    s_dt = (float)dt;
-                    s_dd = (float)dd;
-                    for (int w = 0; w < kTreeWarps; ++w) {  // sum over a > b of (p - q)
-                        const double D = s_red[w][2], Pb = s_red[w][3];
-                        Z += D + dt * (D + Pb) - dd * Pb;
-                    }
+                    s_SA = tot[0];
+                    s_SB = tot[1];
+                    const float s1 = (float)(tot[0] / tot[1]);
+                    S = tot[2] + (1.0 - (double)s1) * tot[3];  // sum over a > b of (a - s_1 b)
+                    s_s = s1;
                 } else {
-                    for (int w = 0; w < kTreeWarps; ++w) Z += s_red[w][0];
+                    S = tot[0];
+                    s_s = nc.s;
                 }
-                if (Z > 0.0) {
-                    s_zinv[nc.J] = (float)(1.0 / Z);
-                    s_start = nc.start;
-                } else {  // no residual mass: the weights restart from p
-                    s_zinv[nc.J] = 1.f;
-                    Z = 1.0;
-                    s_start = nc.J;
+                if (!(S > 0.0)) {  // no residual mass: the weights restart from p
+                    s_s = 0.f;
+                    S = s_SA;
                 }
-                s_Z = Z;
+                s_sum = S;
             }
+            par ^= 1;
             __syncthreads();
-            if (mode == kTreeModeFirst) {
-                nc.dt = s_dt;
-                nc.dd = s_dd;
-            }
-            nc.start = s_start;
+            nc.s = s_s;
             if (!more) break;
         }
         if (next >= 0) {
-            if (tid == 0) {
+            if (tid == 0 && rank == 0) {
                 out[depth] = s_tok[next];
                 nodes[depth] = next;
             }
             cur = next;
             ++depth;
-            __syncthreads();  // s_acc / s_zinv are rewritten at the next node
+            __syncthreads();  // s_acc and the sums are rewritten at the next node
             continue;
         }
         // no child accepted: the emitted token from the current weights
-        const int mode = nc.J == 0 ? kTreeModeP : kTreeModeResid;
         for (;;) {
-            tree_pass<DT, VEC>(rowt, rowd, V, nc, mode, true, s_zinv, s_red, s_mass, warp, lane);
+            const int mode = nc.s > 0.f ? kTreeModeThr : kTreeModeP;
+            tree_pass<DT, VEC>(rowt, rowd, V, rank, cs, nc, mode, true, s_red, s_mass, warp, lane);
             __syncthreads();
             if (tid == 0) {
+                double v = 0.0;
+                for (int w = 0; w < kTreeWarps; ++w) v += s_red[w][0];
+                s_slot[par][0] = v;
+            }
+            cluster_sync_all();
+            if (tid == 0) {
+                double Mr[8];
                 double Z = 0.0;
-                for (int w = 0; w < kTreeWarps; ++w) Z += s_red[w][0];
+                for (int r = 0; r < cs; ++r) {
+                    Mr[r] = ld_cluster_f64(&s_slot[par][0], r);
+                    Z += Mr[r];
+                }
                 s_again = 0;
-                if (!(Z > 0.0) && nc.J > 0 && nc.start != nc.J) {  // no residual mass: p
-                    s_zinv[nc.J] = 1.f;
-                    s_start = nc.J;
+                if (!(Z > 0.0) && mode == kTreeModeThr) {  // no residual mass: p
+                    s_s = 0.f;
                     s_again = 1;
                 }
-                const double thr = uniform_sample(P.seed, (uint32_t)b, (uint32_t)cur) * Z;
-                int W = -1;
+                const double thr = s_us[cur] * Z;
+                // the CTA whose slice holds the crossing (rounding: the last with mass)
+                int R = -1, lastr = -1;
                 double base = 0.0, run = 0.0, lbase = 0.0;
-                int lastw = -1;
-                for (int w = 0; w < kTreeWarps; ++w) {
-                    const double m = s_red[w][0];
-                    if (m > 0.0) {
-                        if (W < 0 && run + m > thr) {
-                            W = w;
+                for (int r = 0; r < cs; ++r) {
+                    if (Mr[r] > 0.0) {
+                        if (R < 0 && run + Mr[r] > thr) {
+                            R = r;
                             base = run;
                         }
-                        lastw = w;
+                        lastr = r;
                         lbase = run;
                     }
-                    run += m;
+                    run += Mr[r];
                 }
-                if (W < 0) {  // rounding: the last warp with mass
-                    W = lastw;
+                if (R < 0) {
+                    R = lastr;
                     base = lbase;
                 }
+                // inside it, the warp
+                int W = -1;
+                if (R == rank) {
+                    int lastw = -1;
+                    double wb = base, lwb = base;
+                    run = base;
+                    for (int w = 0; w < kTreeWarps; ++w) {
+                        const double m = s_red[w][0];
+                        if (m > 0.0) {
+                            if (W < 0 && run + m > thr) {
+                                W = w;
+                                wb = run;
+                            }
+                            lastw = w;
+                            lwb = run;
+                        }
+                        run += m;
+                    }
+                    if (W < 0) {
+                        W = lastw;
+                        wb = lwb;
+                    }
+                    base = wb;
+                }
+                s_R = R < 0 ? 0 : R;
                 s_W = W;
                 s_base = base;
                 s_thr = thr;
                 s_emit = V - 1;  // no mass at all
             }
+            par ^= 1;
             __syncthreads();
             if (!s_again) break;
-            nc.start = s_start;
+            nc.s = s_s;
         }
-        if (s_W >= 0 && warp == 0) {
-            const int tok = tree_find<DT, VEC>(rowt, rowd, V, nc, mode, s_zinv, s_mass, s_W, s_base,
+        const int mode = nc.s > 0.f ? kTreeModeThr : kTreeModeP;
+        if (rank == s_R && s_W >= 0 && warp == 0) {
+            const int tok = tree_find<DT, VEC>(rowt, rowd, V, rank, cs, nc, mode, s_mass, s_W, s_base,
                                                s_thr, lane);
             if (lane == 0 && tok >= 0) s_emit = tok;
         }
         __syncthreads();
-        if (tid == 0) {
-            out[depth] = s_emit;
+        if (tid == 0 && rank == s_R) out[depth] = s_emit;
+        if (tid == 0 && rank == 0) {
             for (int i = depth + 1; i < N; ++i) out[i] = -1;
             for (int i = depth; i < N; ++i) nodes[i] = -1;
             P.accept_len[b] = depth;
         }
+        cluster_sync_all();  // no CTA leaves while another may read its slots
         return;
     }
 }
@@ -2403,15 +2448,22 @@ spec_status_t spec_verify_tree(const void *target_logits, const void *draft_logi
         else sv::launch_dependent(sv::sv_pass1<sv::kF32, false>, g1, sv::kP1Warps * 32, 0, s, P);
         walk = vec ? sv::sv_tree_walk<sv::kF32, true> : sv::sv_tree_walk<sv::kF32, false>;
     }
+    // a cluster of cs CTAs (one per SM) per request while the batch leaves SMs free
+    int cs = 1;
+    while (cs < 8 && (long long)B * cs * 2 <= d->sms) cs *= 2;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)B);
+    cfg.gridDim = dim3((unsigned)((long long)B * cs));
     cfg.blockDim = dim3(sv::kTreeThreads);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaLaunchKernelEx(&cfg, walk, P, parent, node_tokens, out_nodes);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
