@@ -22,10 +22,13 @@
 //   5. sv_find    per request: inverse CDF over chunks, then over the chosen
 //                 chunk's elements.
 // spec_verify_early_exit runs kernels 1-3 once per wave of positions, then 4-5.
-// spec_verify_tree_greedy, spec_draft_confidence, spec_schedule_len and
-// spec_schedule_budget reuse the statistics pass or are small kernels of
-// their own (sv_tree_rows / sv_tree_decide, sv_conf_rows / sv_conf_out,
-// sv_schedule, sv_schedule_budget).
+// spec_verify_tree_greedy, spec_verify_tree, spec_draft_confidence,
+// spec_schedule_len and spec_schedule_budget reuse the statistics pass or are
+// small kernels of their own (sv_tree_rows / sv_tree_decide, sv_tree_rows_s /
+// sv_tree_walk, sv_conf_rows / sv_conf_out, sv_schedule, sv_schedule_budget).
+// sv_tree_walk runs a cluster of CTAs per request: sibling candidates are
+// checked against residuals kept in closed form (a threshold on
+// max(0, a - s b)), one pass over the vocabulary per rejection.
 #include "spec_verify.h"
 #include "sv_common.cuh"
 
