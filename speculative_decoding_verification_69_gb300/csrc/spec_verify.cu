@@ -1476,6 +1476,49 @@ __device__ __forceinline__ double ld_cluster_f64(const double *local, int rank) 
     return v;
 }
 
+// Warp 0 of a CTA: the sums red[w][i] (i < n) of its warps into slot[i], added
+// by a fixed shuffle tree.
+__device__ __forceinline__ void warp_sums_to_slot(const double (*red)[4], double *slot, int n,
+                                                  int lane) {
+    for (int i = 0; i < n; ++i) {
+        const double v = warp_sum_d(lane < kTreeWarps ? red[lane][i] : 0.0);
+        if (lane == 0) slot[i] = v;
+    }
+}
+
+// Warp 0: the cluster totals of slot[0..n) (n <= 4, cs <= 8).  Lane 4 r + i
+// reads slot[i] of CTA r; a fixed shuffle tree adds over r, so every CTA
+// obtains the same bits.  Every lane receives tot[0..n).
+__device__ __forceinline__ void cluster_totals(const double *slot, int n, int cs, int lane,
+                                               double tot[4]) {
+    const int r = lane >> 2, i = lane & 3;
+    double v = (r < cs && i < n) ? ld_cluster_f64(&slot[i], r) : 0.0;
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) tot[k] = __shfl_sync(0xFFFFFFFFu, v, k);
+}
+
+// Warp 0: the first of n masses (lane j holds m, 0 past n) whose inclusive
+// prefix from base exceeds thr, and the mass before it; rounding that leaves
+// no crossing takes the last positive mass.  Returns -1 when all are 0.
+__device__ __forceinline__ int crossing_lane(double m, double base, double thr, int lane,
+                                             double &before) {
+    double incl = m;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const unsigned cross = __ballot_sync(0xFFFFFFFFu, m > 0.0 && base + incl > thr);
+    const unsigned has = __ballot_sync(0xFFFFFFFFu, m > 0.0);
+    if (!has) return -1;
+    const int j = cross ? __ffs(cross) - 1 : 31 - __clz(has);
+    before = base + __shfl_sync(0xFFFFFFFFu, incl - m, j);
+    return j;
+}
+
 // One pass of the CTA over its slice of the vocabulary.  Warp w covers its contiguous steps,
 // lane l the 8 elements at 8 l of each step, kU steps' loads in flight.  Writes
 // the warp's sums (as doubles) to red[w]; with `record`, also the mass of each
@@ -1484,15 +1527,14 @@ template <int DT, bool VEC>
 __device__ void tree_pass(const char *rowt, const char *rowd, int V, int rank, int cs,
                           const TreeNodeC &nc, int mode, bool record, double (*red)[4], float *mass,
                           int warp, int lane) {
-    constexpr int kU = DT == kBF16 ? 4 : 2;
+    constexpr int kU = DT == kBF16 ? 2 : 1;  // steps per batch; two batches in flight
     const TreeSplit sp(V, rank, cs, warp);
     BiasAcc2 acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i].init(kTreeBias);
     float gs = 0.f;   // this lane's part of the current group
     double mw = 0.0;  // the warp's recorded total (lane 0)
-    for (int st0 = sp.s0; st0 < sp.s1; st0 += kU) {
-        Eight<DT, VEC> zt[kU], zd[kU];
+    auto load = [&](Eight<DT, VEC> (&zt)[kU], Eight<DT, VEC> (&zd)[kU], int st0) {
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const long long e0 = (long long)(st0 + u) * kTreeStep + lane * 8;
@@ -1501,45 +1543,56 @@ __device__ void tree_pass(const char *rowt, const char *rowd, int V, int rank, i
                 if (mode != kTreeModeP) zd[u].load(rowd, e0, V);
             }
         }
+    };
+    auto consume = [&](const Eight<DT, VEC> (&zt)[kU], const Eight<DT, VEC> (&zd)[kU], int st0) {
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-            if (st0 + u < sp.s1) {
-                if (mode == kTreeModeFirst) {
+            if (st0 + u >= sp.s1) break;
+            if (mode == kTreeModeFirst) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 a = weight2l(zt[u].pair(i), nc.mt, nc.chi, nc.clo, nc.lt);
-                        const float2 bq = weight2l(zd[u].pair(i), nc.md, nc.chi, nc.clo, nc.ld);
-                        acc[0].add(a);
-                        acc[1].add(bq);
-                        const bool gx = a.x > bq.x, gy = a.y > bq.y;
-                        acc[2].add(make_float2(gx ? __fsub_rn(a.x, bq.x) : 0.f,
-                                               gy ? __fsub_rn(a.y, bq.y) : 0.f));
-                        acc[3].add(make_float2(gx ? bq.x : 0.f, gy ? bq.y : 0.f));
+                for (int i = 0; i < 4; ++i) {
+                    const float2 a = weight2l(zt[u].pair(i), nc.mt, nc.chi, nc.clo, nc.lt);
+                    const float2 bq = weight2l(zd[u].pair(i), nc.md, nc.chi, nc.clo, nc.ld);
+                    acc[0].add(a);
+                    acc[1].add(bq);
+                    const bool gx = a.x > bq.x, gy = a.y > bq.y;
+                    acc[2].add(make_float2(gx ? __fsub_rn(a.x, bq.x) : 0.f,
+                                           gy ? __fsub_rn(a.y, bq.y) : 0.f));
+                    acc[3].add(make_float2(gx ? bq.x : 0.f, gy ? bq.y : 0.f));
+                }
+            } else {
+                float w[8];
+                tree_weights8<DT, VEC>(zt[u], zd[u], nc, mode, w);
+                if (record) {
+                    float ls = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) ls = __fadd_rn(ls, w[i]);
+                    gs = __fadd_rn(gs, ls);
+                    const int k = st0 + u - sp.s0;
+                    if ((k + 1) % sp.gsz == 0 || st0 + u + 1 == sp.s1) {
+                        const float gm = warp_sum(gs);
+                        if (lane == 0) {
+                            mass[warp * kTreeGroups + k / sp.gsz] = gm;
+                            mw += (double)gm;
+                        }
+                        gs = 0.f;
                     }
                 } else {
-                    float w[8];
-                    tree_weights8<DT, VEC>(zt[u], zd[u], nc, mode, w);
-                    if (record) {
-                        float ls = 0.f;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) ls = __fadd_rn(ls, w[i]);
-                        gs = __fadd_rn(gs, ls);
-                        const int k = st0 + u - sp.s0;
-                        if ((k + 1) % sp.gsz == 0 || st0 + u + 1 == sp.s1) {
-                            const float gm = warp_sum(gs);
-                            if (lane == 0) {
-                                mass[warp * kTreeGroups + k / sp.gsz] = gm;
-                                mw += (double)gm;
-                            }
-                            gs = 0.f;
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) acc[0].add(make_float2(w[2 * i], w[2 * i + 1]));
-                    }
+                    for (int i = 0; i < 4; ++i) acc[0].add(make_float2(w[2 * i], w[2 * i + 1]));
                 }
             }
         }
+    };
+    // batch A holds steps [st0, st0 + kU), batch B the next kU: one is loading
+    // while the other is consumed
+    Eight<DT, VEC> ta[kU], da[kU], tb[kU], db[kU];
+    load(ta, da, sp.s0);
+    for (int st0 = sp.s0; st0 < sp.s1; st0 += 2 * kU) {
+        load(tb, db, st0 + kU);
+        consume(ta, da, st0);
+        load(ta, da, st0 + 2 * kU);
+        consume(tb, db, st0 + kU);
     }
     if (record) {
         if (lane == 0) red[warp][0] = mw;
@@ -1564,14 +1617,16 @@ __device__ int tree_find(const char *rowt, const char *rowd, int V, int rank, in
     const TreeSplit sp(V, rank, cs, W);
     const int ng = (sp.s1 - sp.s0 + sp.gsz - 1) / sp.gsz;
     constexpr int kPer = kTreeGroups / 32;  // lane l holds groups [kPer l, kPer (l + 1))
+    static_assert(kPer == 8, "the lane sum below adds 8 group masses");
     float gm[kPer];
-    double ls = 0.0;
+    double t8[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
         const int g = lane * kPer + i;
         gm[i] = g < ng ? mass[W * kTreeGroups + g] : 0.f;
-        ls += (double)gm[i];
+        t8[i] = (double)gm[i];
     }
+    const double ls = ((t8[0] + t8[1]) + (t8[2] + t8[3])) + ((t8[4] + t8[5]) + (t8[6] + t8[7]));
     double incl = ls;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -1609,13 +1664,12 @@ __device__ int tree_find(const char *rowt, const char *rowd, int V, int rank, in
         if (mode != kTreeModeP) zd.load(rowd, e0, V);
         float w[8];
         tree_weights8<DT, VEC>(zt, zd, nc, mode, w);
-        double s8 = 0.0;
         int lp = -1;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            s8 += (double)w[i];
+        for (int i = 0; i < 8; ++i)
             if (w[i] > 0.f) lp = (int)e0 + i;
-        }
+        const double s8 = (((double)w[0] + (double)w[1]) + ((double)w[2] + (double)w[3])) +
+                          (((double)w[4] + (double)w[5]) + ((double)w[6] + (double)w[7]));
         double in8 = s8;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -1768,17 +1822,11 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
             tree_pass<DT, VEC>(rowt, rowd, V, rank, cs, nc, mode, false, s_red, s_mass, warp, lane);
             __syncthreads();
             const int nsum = mode == kTreeModeFirst ? 4 : 1;
-            if (tid == 0)
-                for (int i = 0; i < nsum; ++i) {
-                    double v = 0.0;
-                    for (int w = 0; w < kTreeWarps; ++w) v += s_red[w][i];
-                    s_slot[par][i] = v;
-                }
+            if (warp == 0) warp_sums_to_slot(s_red, s_slot[par], nsum, lane);
             cluster_sync_all();
+            double tot[4];
+            if (warp == 0) cluster_totals(s_slot[par], nsum, cs, lane, tot);
             if (tid == 0) {
-                double tot[4] = {0.0, 0.0, 0.0, 0.0};
-                for (int r = 0; r < cs; ++r)
-                    for (int i = 0; i < nsum; ++i) tot[i] += ld_cluster_f64(&s_slot[par][i], r);
                 double S;
                 if (mode == kTreeModeFirst) {
                     s_SA = tot[0];
@@ -1816,72 +1864,34 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
             const int mode = nc.s > 0.f ? kTreeModeThr : kTreeModeP;
             tree_pass<DT, VEC>(rowt, rowd, V, rank, cs, nc, mode, true, s_red, s_mass, warp, lane);
             __syncthreads();
-            if (tid == 0) {
-                double v = 0.0;
-                for (int w = 0; w < kTreeWarps; ++w) v += s_red[w][0];
-                s_slot[par][0] = v;
-            }
+            if (warp == 0) warp_sums_to_slot(s_red, s_slot[par], 1, lane);
             cluster_sync_all();
-            if (tid == 0) {
-                double Mr[8];
-                double Z = 0.0;
-                for (int r = 0; r < cs; ++r) {
-                    Mr[r] = ld_cluster_f64(&s_slot[par][0], r);
-                    Z += Mr[r];
-                }
-                s_again = 0;
-                if (!(Z > 0.0) && mode == kTreeModeThr) {  // no residual mass: p
-                    s_s = 0.f;
-                    s_again = 1;
-                }
+            if (warp == 0) {
+                // the masses of the cluster's CTAs, their total, the threshold
+                const double Mr = lane < cs ? ld_cluster_f64(&s_slot[par][0], lane) : 0.0;
+                const double Z = warp_sum_d(Mr);
                 const double thr = s_us[cur] * Z;
-                // the CTA whose slice holds the crossing (rounding: the last with mass)
-                int R = -1, lastr = -1;
-                double base = 0.0, run = 0.0, lbase = 0.0;
-                for (int r = 0; r < cs; ++r) {
-                    if (Mr[r] > 0.0) {
-                        if (R < 0 && run + Mr[r] > thr) {
-                            R = r;
-                            base = run;
-                        }
-                        lastr = r;
-                        lbase = run;
-                    }
-                    run += Mr[r];
-                }
-                if (R < 0) {
-                    R = lastr;
-                    base = lbase;
-                }
-                // inside it, the warp
+                // the CTA whose slice holds the crossing, then (in it) the warp
+                double base = 0.0;
+                const int R = crossing_lane(Mr, 0.0, thr, lane, base);
                 int W = -1;
                 if (R == rank) {
-                    int lastw = -1;
-                    double wb = base, lwb = base;
-                    run = base;
-                    for (int w = 0; w < kTreeWarps; ++w) {
-                        const double m = s_red[w][0];
-                        if (m > 0.0) {
-                            if (W < 0 && run + m > thr) {
-                                W = w;
-                                wb = run;
-                            }
-                            lastw = w;
-                            lwb = run;
-                        }
-                        run += m;
-                    }
-                    if (W < 0) {
-                        W = lastw;
-                        wb = lwb;
-                    }
+                    double wb = base;
+                    W = crossing_lane(lane < kTreeWarps ? s_red[lane][0] : 0.0, base, thr, lane, wb);
                     base = wb;
                 }
-                s_R = R < 0 ? 0 : R;
-                s_W = W;
-                s_base = base;
-                s_thr = thr;
-                s_emit = V - 1;  // no mass at all
+                if (lane == 0) {
+                    s_again = 0;
+                    if (!(Z > 0.0) && mode == kTreeModeThr) {  // no residual mass: p
+                        s_s = 0.f;
+                        s_again = 1;
+                    }
+                    s_R = R < 0 ? 0 : R;
+                    s_W = W;
+                    s_base = base;
+                    s_thr = thr;
+                    s_emit = V - 1;  // no mass at all
+                }
             }
             par ^= 1;
             __syncthreads();

@@ -203,3 +203,33 @@ def test_sampled_tree_mismatch_rate(sv):
     """Many small requests: no unflagged mismatch and few flagged ones."""
     inp = workloads.make_tree_inputs(2048, 8, 512, torch.bfloat16, seed=31, T=1.0)
     _compare_tree(sv, inp, max_flag_frac=0.02)
+
+
+def test_sampled_tree_first_token_law(sv):
+    """'Утверждение 1' (kiosknews.app) through the GPU path: with three
+    siblings drafted independently from the root's draft row, the first
+    emitted token of 200 000 requests (one set of logits, Philox keyed by the
+    request) follows the target distribution p of the root row (chi-square);
+    a copy whose siblings all carry the draft's most likely token does not."""
+    scipy_stats = pytest.importorskip("scipy.stats")
+    B, N, V, T = 200000, 4, 12, 1.0
+    g = torch.Generator(device="cuda").manual_seed(99)
+    trow = torch.randn((N, V), generator=g, device="cuda") * 1.5
+    drow = (trow[:N - 1] + torch.randn((N - 1, V), generator=g, device="cuda") * 1.0)
+    tgt = trow.expand(B, N, V).contiguous()
+    drf = drow.expand(B, N - 1, V).contiguous()
+    parent = torch.tensor([-1, 0, 0, 0], dtype=torch.int32, device="cuda").expand(B, N).contiguous()
+    q0 = torch.softmax(drow[0] / T, dim=-1)
+    draws = torch.multinomial(q0.expand(B, V), N - 1, replacement=True, generator=g)
+    tok = torch.cat([torch.zeros((B, 1), dtype=torch.int64, device="cuda"), draws], 1)
+    temp = torch.full((B,), T, device="cuda")
+    p = oracle.row_softmax(trow[0].cpu().numpy().astype(np.float32), T)[0]
+    for tokens, lossless in ((tok, True), (torch.where(tok > 0, torch.full_like(tok, int(q0.argmax())), tok), False)):
+        out, nodes, acc = sv.verify_tree(tgt, drf, parent, tokens.to(torch.int32).contiguous(), temp, 1234)
+        first = out[:, 0].long().cpu().numpy()
+        counts = np.bincount(first, minlength=V)
+        _, pval = scipy_stats.chisquare(counts, p * B)
+        if lossless:
+            assert pval > 1e-4, (pval, counts, p * B)
+        else:
+            assert pval < 1e-6, pval
