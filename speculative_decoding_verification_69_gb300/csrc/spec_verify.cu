@@ -1371,6 +1371,7 @@ constexpr int kTreeWarps = kTreeThreads / 32;
 constexpr int kTreeStep = 256;     // elements a warp covers per step: 8 per lane
 constexpr int kTreeGroups = 256;   // recorded masses per warp (groups of steps)
 constexpr float kTreeBias = 2.0f;  // every summed weight is at most ~1
+constexpr int kTreeStageMax = 192 * 1024;  // dynamic shared memory for a staged slice (two rows)
 
 // The weight 2^((z - m) c + l) of one element: the scalar twin of weight2l
 // (the same operations in the same order, so the same value).
@@ -1398,6 +1399,17 @@ template <int DT, bool VEC> struct Eight {
     __device__ __forceinline__ void load(const char *row, long long e0, int V) {
         v0 = load_vec<DT, VEC>(row, e0, V);
         if (DT == kF32) v1 = load_vec<DT, VEC>(row, e0 + 4, V);
+    }
+    // the same elements from a staged copy in shared memory (stage = the
+    // element at index 0 of the copy, i0 = e0's index there; V a multiple of
+    // the 16-byte vector, so each vector lies wholly before or past V)
+    __device__ __forceinline__ void load_staged(const char *stage, int i0, long long e0, int V) {
+        const uint32_t ni = Fmt<DT>::kNegInfWord;
+        const uint4 neg = make_uint4(ni, ni, ni, ni);
+        v0 = e0 < V ? *reinterpret_cast<const uint4 *>(stage + (size_t)i0 * Fmt<DT>::kESZ) : neg;
+        if (DT == kF32)
+            v1 = e0 + 4 < V ? *reinterpret_cast<const uint4 *>(stage + (size_t)(i0 + 4) * Fmt<DT>::kESZ)
+                            : neg;
     }
     __device__ __forceinline__ float2 pair(int i) const {
         if (DT == kBF16) return make_float2(elem<DT>(v0, 2 * i), elem<DT>(v0, 2 * i + 1));
@@ -1440,11 +1452,12 @@ __device__ __forceinline__ void tree_weights8(const Eight<DT, VEC> &zt, const Ei
 // steps [s0, s1) of that slice; recorded masses cover groups of gsz
 // consecutive steps.
 struct TreeSplit {
-    int s0, s1, gsz;
+    int c0, s0, s1, gsz;
     __device__ __forceinline__ TreeSplit(int V, int rank, int cs, int w) {
         const int nsteps = (V + kTreeStep - 1) / kTreeStep;
         const int spc = (nsteps + cs - 1) / cs;
-        const int c0 = min(nsteps, rank * spc), c1 = min(nsteps, c0 + spc);
+        c0 = min(nsteps, rank * spc);
+        const int c1 = min(nsteps, c0 + spc);
         const int spw = (c1 - c0 + kTreeWarps - 1) / kTreeWarps;
         s0 = min(c1, c0 + w * spw);
         s1 = min(c1, s0 + spw);
@@ -1524,9 +1537,9 @@ __device__ __forceinline__ int crossing_lane(double m, double base, double thr, 
 // the warp's sums (as doubles) to red[w]; with `record`, also the mass of each
 // group of steps to mass[w * kTreeGroups + g] and the warp's total as their sum.
 template <int DT, bool VEC>
-__device__ void tree_pass(const char *rowt, const char *rowd, int V, int rank, int cs,
-                          const TreeNodeC &nc, int mode, bool record, double (*red)[4], float *mass,
-                          int warp, int lane) {
+__device__ void tree_pass(const char *rowt, const char *rowd, const char *stt, const char *std_,
+                          int V, int rank, int cs, const TreeNodeC &nc, int mode, bool record,
+                          double (*red)[4], float *mass, int warp, int lane) {
     constexpr int kU = DT == kBF16 ? 2 : 1;  // steps per batch; two batches in flight
     const TreeSplit sp(V, rank, cs, warp);
     BiasAcc2 acc[4];
@@ -1539,8 +1552,14 @@ __device__ void tree_pass(const char *rowt, const char *rowd, int V, int rank, i
         for (int u = 0; u < kU; ++u) {
             const long long e0 = (long long)(st0 + u) * kTreeStep + lane * 8;
             if (st0 + u < sp.s1) {
-                zt[u].load(rowt, e0, V);
-                if (mode != kTreeModeP) zd[u].load(rowd, e0, V);
+                if (stt) {  // staged slice of this CTA
+                    const int i0 = (st0 + u - sp.c0) * kTreeStep + lane * 8;
+                    zt[u].load_staged(stt, i0, e0, V);
+                    if (mode != kTreeModeP) zd[u].load_staged(std_, i0, e0, V);
+                } else {
+                    zt[u].load(rowt, e0, V);
+                    if (mode != kTreeModeP) zd[u].load(rowd, e0, V);
+                }
             }
         }
     };
@@ -1611,9 +1630,9 @@ __device__ void tree_pass(const char *rowt, const char *rowd, int V, int rank, i
 // element.  Rounding that leaves the crossing outside takes the last positive
 // weight met.
 template <int DT, bool VEC>
-__device__ int tree_find(const char *rowt, const char *rowd, int V, int rank, int cs,
-                         const TreeNodeC &nc, int mode, const float *mass, int W, double base,
-                         double thr, int lane) {
+__device__ int tree_find(const char *rowt, const char *rowd, const char *stt, const char *std_,
+                         int V, int rank, int cs, const TreeNodeC &nc, int mode, const float *mass,
+                         int W, double base, double thr, int lane) {
     const TreeSplit sp(V, rank, cs, W);
     const int ng = (sp.s1 - sp.s0 + sp.gsz - 1) / sp.gsz;
     constexpr int kPer = kTreeGroups / 32;  // lane l holds groups [kPer l, kPer (l + 1))
@@ -1660,8 +1679,14 @@ __device__ int tree_find(const char *rowt, const char *rowd, int V, int rank, in
     for (int st = st_a; st < st_b; ++st) {
         const long long e0 = (long long)st * kTreeStep + lane * 8;
         Eight<DT, VEC> zt, zd;
-        zt.load(rowt, e0, V);
-        if (mode != kTreeModeP) zd.load(rowd, e0, V);
+        if (stt) {
+            const int i0 = (st - sp.c0) * kTreeStep + lane * 8;
+            zt.load_staged(stt, i0, e0, V);
+            if (mode != kTreeModeP) zd.load_staged(std_, i0, e0, V);
+        } else {
+            zt.load(rowt, e0, V);
+            if (mode != kTreeModeP) zd.load(rowd, e0, V);
+        }
         float w[8];
         tree_weights8<DT, VEC>(zt, zd, nc, mode, w);
         int lp = -1;
@@ -1714,7 +1739,13 @@ __device__ int tree_find(const char *rowt, const char *rowd, int V, int rank, in
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const int32_t *parent,
                                                                const int32_t *token,
-                                                               int32_t *out_nodes) {
+                                                               int32_t *out_nodes,
+                                                               int stage_row_bytes) {
+    // stage_row_bytes > 0: this CTA's slice of a node's target and draft rows is
+    // copied into dynamic shared memory at the node's first rejection, and the
+    // node's later passes read it there
+    extern __shared__ __align__(128) unsigned char s_stage[];
+    __shared__ uint64_t s_tbar[kTreeWarps];
     __shared__ int s_par[SPEC_MAX_TREE], s_tok[SPEC_MAX_TREE], s_amax[SPEC_MAX_TREE];
     __shared__ float s_m[2 * SPEC_MAX_TREE], s_S[2 * SPEC_MAX_TREE];
     __shared__ float s_u[SPEC_MAX_TREE], s_g[SPEC_MAX_TREE], s_gd[SPEC_MAX_TREE];
@@ -1750,6 +1781,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
     }
     float c = 0.f, chi = 0.f, clo = 0.f;
     if (!greedy) temp_coeffs(T, c, chi, clo);
+    if (lane == 0) mbar_init(&s_tbar[warp], 1);
+    fence_mbar_init();
     pdl_wait();  // partials come from sv_pass1
     pdl_trigger();
     const int nrows = greedy ? N : 2 * N - 1;
@@ -1770,6 +1803,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
     int32_t *nodes = out_nodes + (size_t)b * N;
     if (tid == 0 && rank == 0) flag_bad_tree(P, N, s_par);
     int par = 0;  // slot buffer of the next exchange
+    uint32_t stagings = 0;  // copies into the staging buffer so far (phase of s_tbar)
     int cur = 0, depth = 0;
     for (;;) {
         const char *rowt = row_ptr(P, b, cur, ESZ);
@@ -1786,6 +1820,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
         nc.md = make_float2(md, md);
         nc.ld = make_float2(ld, ld);
         nc.s = 0.f;
+        bool staged = false;  // this node's slice is in shared memory
         int J = 0, next = -1;
         for (int ch = cur + 1; ch < N; ++ch) {
             if (s_par[ch] != cur) continue;
@@ -1818,8 +1853,32 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
                 nc.s = s_s;
                 if (!more) break;  // the recording pass below needs no mass
             }
+            if (J == 1 && stage_row_bytes > 0) {  // every warp copies its own steps, then waits
+                const TreeSplit sp(V, rank, cs, warp);
+                fence_proxy_async();  // earlier reads of the buffer come first
+                __syncwarp();
+                if (lane == 0) {
+                    const long long ea = (long long)sp.s0 * kTreeStep;
+                    const long long eb = min((long long)sp.s1 * kTreeStep, (long long)V);
+                    const uint32_t bytes = eb > ea ? (uint32_t)((eb - ea) * ESZ) : 0u;
+                    unsigned char *dt = s_stage + (size_t)(sp.s0 - sp.c0) * kTreeStep * ESZ;
+                    mbar_expect_tx(&s_tbar[warp], 2u * bytes);
+                    if (bytes) {
+                        bulk_g2s(dt, rowt + ea * ESZ, bytes, &s_tbar[warp]);
+                        bulk_g2s(dt + stage_row_bytes, rowd + ea * ESZ, bytes, &s_tbar[warp]);
+                    }
+                }
+                __syncwarp();
+                const bool ok = mbar_wait_bounded(&s_tbar[warp], stagings & 1u, kWaitLimitNs);
+                if (!__all_sync(0xFFFFFFFFu, ok) && lane == 0 && P.dev_status)
+                    atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
+                ++stagings;
+                staged = true;
+            }
+            const char *stt = staged ? (const char *)s_stage : nullptr;
+            const char *std_ = staged ? (const char *)s_stage + stage_row_bytes : nullptr;
             const int mode = J == 1 ? kTreeModeFirst : kTreeModeThr;
-            tree_pass<DT, VEC>(rowt, rowd, V, rank, cs, nc, mode, false, s_red, s_mass, warp, lane);
+            tree_pass<DT, VEC>(rowt, rowd, stt, std_, V, rank, cs, nc, mode, false, s_red, s_mass, warp, lane);
             __syncthreads();
             const int nsum = mode == kTreeModeFirst ? 4 : 1;
             if (warp == 0) warp_sums_to_slot(s_red, s_slot[par], nsum, lane);
@@ -1860,9 +1919,11 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
             continue;
         }
         // no child accepted: the emitted token from the current weights
+        const char *stt = staged ? (const char *)s_stage : nullptr;
+        const char *std_ = staged ? (const char *)s_stage + stage_row_bytes : nullptr;
         for (;;) {
             const int mode = nc.s > 0.f ? kTreeModeThr : kTreeModeP;
-            tree_pass<DT, VEC>(rowt, rowd, V, rank, cs, nc, mode, true, s_red, s_mass, warp, lane);
+            tree_pass<DT, VEC>(rowt, rowd, stt, std_, V, rank, cs, nc, mode, true, s_red, s_mass, warp, lane);
             __syncthreads();
             if (warp == 0) warp_sums_to_slot(s_red, s_slot[par], 1, lane);
             cluster_sync_all();
@@ -1900,8 +1961,10 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
         }
         const int mode = nc.s > 0.f ? kTreeModeThr : kTreeModeP;
         if (rank == s_R && s_W >= 0 && warp == 0) {
-            const int tok = tree_find<DT, VEC>(rowt, rowd, V, rank, cs, nc, mode, s_mass, s_W, s_base,
-                                               s_thr, lane);
+            if (staged)  // warp W's copy completed before its pass: acquire it here
+                mbar_wait_bounded(&s_tbar[s_W], (stagings - 1u) & 1u, kWaitLimitNs);
+            const int tok = tree_find<DT, VEC>(rowt, rowd, stt, std_, V, rank, cs, nc, mode, s_mass,
+                                               s_W, s_base, s_thr, lane);
             if (lane == 0 && tok >= 0) s_emit = tok;
         }
         __syncthreads();
@@ -2451,7 +2514,7 @@ spec_status_t spec_verify_tree(const void *target_logits, const void *draft_logi
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     sv::sv_tree_rows_s<<<1, sv::kPrepThreads, 0, s>>>(P);
     const int g1 = d->sms * d->occ_p1[dtype == SPEC_DTYPE_BF16 ? sv::kBF16 : sv::kF32][vec ? 1 : 0];
-    void (*walk)(sv::Params, const int32_t *, const int32_t *, int32_t *);
+    void (*walk)(sv::Params, const int32_t *, const int32_t *, int32_t *, int);
     if (dtype == SPEC_DTYPE_BF16) {
         if (vec) sv::launch_dependent(sv::sv_pass1<sv::kBF16, true>, g1, sv::kP1Warps * 32, sv::kP1Smem, s, P);
         else sv::launch_dependent(sv::sv_pass1<sv::kBF16, false>, g1, sv::kP1Warps * 32, 0, s, P);
@@ -2477,7 +2540,20 @@ spec_status_t spec_verify_tree(const void *target_logits, const void *draft_logi
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaLaunchKernelEx(&cfg, walk, P, parent, node_tokens, out_nodes);
+    // the slice of a node's two rows each CTA stages in shared memory, when it fits
+    const long long nsteps = ((long long)V + sv::kTreeStep - 1) / sv::kTreeStep;
+    const long long row_bytes = (nsteps + cs - 1) / cs * sv::kTreeStep * esz;
+    const int stage = vec && 2 * row_bytes <= sv::kTreeStageMax ? (int)row_bytes : 0;
+    static bool smem_set[2][2] = {{false, false}, {false, false}};
+    bool &set = smem_set[dtype == SPEC_DTYPE_BF16 ? 1 : 0][vec ? 1 : 0];
+    if (!set) {
+        if (cudaFuncSetAttribute(walk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sv::kTreeStageMax) != cudaSuccess)
+            return SPEC_ERR_CUDA;
+        set = true;
+    }
+    cfg.dynamicSmemBytes = stage ? (size_t)(2 * row_bytes) : 0;
+    cudaLaunchKernelEx(&cfg, walk, P, parent, node_tokens, out_nodes, stage);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -130,6 +130,7 @@ def _compare_tree(sv, inp, max_flag_frac=0.1):
     (32, 9, 3000, torch.float32, 0.8), (16, 16, 4096 + 8, torch.bfloat16, 1.3),
     (8, 33, 1001, torch.bfloat16, 1.0), (6, 17, 151936, torch.bfloat16, 1.0),
     (12, 64, 2048, torch.bfloat16, 0.7), (8, 12, 999, torch.float32, 1.0),
+    (10, 10, 4100, torch.float32, 1.0),  # staged fp32 rows whose last vector is half past V
 ])
 def test_sampled_trees_against_oracle(sv, B, N, V, dtype, T):
     inp = workloads.make_tree_inputs(B, N, V, dtype, seed=B * 1000 + N + V, T=T,
