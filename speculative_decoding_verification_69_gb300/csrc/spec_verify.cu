@@ -1755,6 +1755,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
     __shared__ double s_slot[2][4];   // this CTA's sums, read by the cluster (two buffers)
     __shared__ double s_sum;          // S_j of the current residual
     __shared__ double s_SA, s_SB;     // exact sums of a and b at the node
+    __shared__ double s_iSB;          // 1 / s_SB
+    __shared__ int s_cand[SPEC_MAX_TREE], s_ncand;  // the current node's candidates, in order
     __shared__ double s_base, s_thr;
     __shared__ float s_s;
     __shared__ int s_acc, s_R, s_W, s_emit, s_again;
@@ -1821,11 +1823,22 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
         nc.ld = make_float2(ld, ld);
         nc.s = 0.f;
         bool staged = false;  // this node's slice is in shared memory
+        if (warp == 0) {  // the children of cur with a token in [0, V), in index order
+            int n = 0;
+            for (int base = cur + 1; base < N; base += 32) {
+                const int ch = base + lane;
+                const bool ok = ch < N && s_par[ch] == cur && s_tok[ch] >= 0 && s_tok[ch] < V;
+                const unsigned m = __ballot_sync(0xFFFFFFFFu, ok);
+                if (ok) s_cand[n + __popc(m & ((1u << lane) - 1u))] = ch;
+                n += __popc(m);
+            }
+            if (lane == 0) s_ncand = n;
+        }
+        __syncthreads();
+        const int ncand = s_ncand;
         int J = 0, next = -1;
-        for (int ch = cur + 1; ch < N; ++ch) {
-            if (s_par[ch] != cur) continue;
-            const int x = s_tok[ch];
-            if (x < 0 || x >= V) continue;
+        for (int k = 0; k < ncand; ++k) {
+            const int ch = s_cand[k];
             if (tid == 0) {
                 const float u = s_u[ch], g = s_g[ch], gd = s_gd[ch];
                 bool acc;
@@ -1844,11 +1857,9 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
                 break;
             }
             ++J;
-            bool more = false;  // another candidate follows: the residual's mass is needed
-            for (int c2 = ch + 1; c2 < N && !more; ++c2)
-                more = s_par[c2] == cur && s_tok[c2] >= 0 && s_tok[c2] < V;
+            const bool more = k + 1 < ncand;  // another candidate follows: the residual's mass is needed
             if (J > 1) {  // the threshold after this rejection
-                if (tid == 0) s_s = nc.s > 0.f ? (float)((double)nc.s + s_sum / s_SB) : (float)(s_SA / s_SB);
+                if (tid == 0) s_s = nc.s > 0.f ? (float)((double)nc.s + s_sum * s_iSB) : (float)(s_SA * s_iSB);
                 __syncthreads();
                 nc.s = s_s;
                 if (!more) break;  // the recording pass below needs no mass
@@ -1890,7 +1901,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
                 if (mode == kTreeModeFirst) {
                     s_SA = tot[0];
                     s_SB = tot[1];
-                    const float s1 = (float)(tot[0] / tot[1]);
+                    s_iSB = 1.0 / tot[1];
+                    const float s1 = (float)(tot[0] * s_iSB);
                     S = tot[2] + (1.0 - (double)s1) * tot[3];  // sum over a > b of (a - s_1 b)
                     s_s = s1;
                 } else {
