@@ -92,3 +92,33 @@ def test_host_validation_without_gpu(lib):
     assert call_ee(0) == 1 and call_ee(-3) == 1              # first wave must be >= 1
     assert call_ee(2, B=0) == 1 and call_ee(2, t=None) == 1
     assert call_ee(2, ws=None) == 4
+
+
+def test_tree_host_validation_without_gpu(lib):
+    """The tree entry points reject bad sizes, null pointers, misaligned logits
+    and small workspaces on the host, before any CUDA call."""
+    fake = ctypes.c_void_p(0x10000)
+    ws = ctypes.c_void_p(0x10000)
+    assert lib.spec_tree_workspace_bytes(2, 0, 100, 1) == 0
+    assert lib.spec_tree_workspace_bytes(2, 65, 100, 1) == 0
+    assert lib.spec_tree_workspace_bytes(2, 64, 100, 1) > 0
+    base = dict(t=fake, d=fake, dt=1, par=fake, tok=fake, T=fake, seed=1, B=2, N=5, V=100,
+                o=fake, n=fake, a=fake, ws=ws, wsb=1 << 30, st=None)
+
+    def call(**kw):
+        x = dict(base, **kw)
+        return lib.spec_verify_tree(x["t"], x["d"], x["dt"], x["par"], x["tok"], x["T"], x["seed"],
+                                    x["B"], x["N"], x["V"], x["o"], x["n"], x["a"], x["ws"],
+                                    x["wsb"], x["st"], None)
+
+    assert call(N=0) == 1 and call(N=65) == 1 and call(B=0) == 1 and call(V=1) == 1
+    assert call(dt=7) == 2
+    assert call(t=None) == 1 and call(d=None) == 1 and call(par=None) == 1
+    assert call(tok=None) == 1 and call(T=None) == 1
+    assert call(o=None) == 1 and call(n=None) == 1 and call(a=None) == 1
+    assert call(d=ctypes.c_void_p(0x10008)) == 1          # draft logits not 16-byte aligned
+    assert call(ws=None) == 4 and call(wsb=16) == 4
+    greedy = lib.spec_verify_tree_greedy
+    assert greedy(fake, 1, fake, fake, 2, 0, 100, fake, fake, fake, ws, 1 << 30, None, None) == 1
+    assert greedy(None, 1, fake, fake, 2, 5, 100, fake, fake, fake, ws, 1 << 30, None, None) == 1
+    assert greedy(fake, 1, fake, fake, 2, 5, 100, fake, fake, fake, None, 1 << 30, None, None) == 4
