@@ -1733,9 +1733,9 @@ __device__ int tree_find(const char *rowt, const char *rowd, const char *stt, co
 // emitted token.  Candidate node c takes the acceptance uniform of position
 // c - 1, node u's emitted token the sampling uniform of position u.
 // Each CTA of the cluster passes over its slice of the vocabulary; the sums
-// are exchanged through distributed shared memory and added in rank order by
-// every CTA, so all CTAs take the same decisions and meet the same cluster
-// barriers.
+// are exchanged through distributed shared memory and added by the same fixed
+// shuffle tree in every CTA, so all CTAs take the same decisions and meet the
+// same cluster barriers.
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const int32_t *parent,
                                                                const int32_t *token,
