@@ -234,3 +234,30 @@ def test_sampled_tree_first_token_law(sv):
             assert pval > 1e-4, (pval, counts, p * B)
         else:
             assert pval < 1e-6, pval
+
+
+@pytest.mark.parametrize("cfg,N,n_check", [(1, 16, 32), (4, 9, 48)])
+def test_sampled_trees_at_bench_workloads(sv, cfg, N, n_check):
+    """The sampled-tree workloads the benchmark times (same generator, seed and
+    launch configuration: clusters with staged slices at c1, one CTA per
+    request at c4 with its quarter of greedy requests), against the oracle on
+    the first n_check requests."""
+    c = workloads.CONFIGS[cfg]
+    T = c["T"] if isinstance(c["T"], float) else 1.0
+    noise = c["noise"] if isinstance(c["noise"], float) else 0.5
+    inp = workloads.make_tree_inputs(c["B"], N, c["V"], c["dtype"], seed=workloads.seed_for(cfg, 0),
+                                     T=T, sigma=c["sigma"], noise=noise,
+                                     n_greedy=c.get("n_greedy", 0))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, nodes, acc = sv.verify_tree(inp["target"], inp["draft"], inp["parent"], inp["tokens"],
+                                     inp["temperature"], inp["seed"], dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    sub = {k: (v[:n_check] if torch.is_tensor(v) else v) for k, v in inp.items()}
+    r = _oracle_tree(sub)
+    out, nodes, acc = out[:n_check].cpu().numpy(), nodes[:n_check].cpu().numpy(), acc[:n_check].cpu().numpy()
+    same = ((acc == r["accept_len"]) & (out == r["out_tokens"]).all(axis=1)
+            & (nodes == r["out_nodes"]).all(axis=1))
+    flagged = (r["accept_margin"] < TREE_NEAR_TIE) | (r["cdf_margin"] < TREE_NEAR_TIE)
+    assert not (~same & ~flagged).any(), np.flatnonzero(~same & ~flagged)
+    assert flagged.sum() <= max(2, n_check // 10)
