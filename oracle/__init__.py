@@ -70,7 +70,8 @@ def lib():
                                         ctypes.c_float, f64p, f64p, i32p, i32p, f64p, vp]
         L.svo_verify_tree_u.restype = ctypes.c_int
         L.svo_verify_tree_sampled.argtypes = [vp, vp, ctypes.c_int, i32p, i32p, ctypes.c_int,
-                                              ctypes.c_int, ctypes.c_int, f32p, ctypes.c_uint64,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, f32p,
+                                              ctypes.c_uint64,
                                               i32p, i32p, i32p, f64p, f64p]
         L.svo_schedule_budget.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_longlong, i32p]
         L.svo_draft_confidence.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -284,11 +285,11 @@ def verify_tree_u(target, draft, parent, token, T, u_acc, u_s):
     return ot, on, a
 
 
-def verify_tree(target, draft, parent, token, temperature, seed):
+def verify_tree(target, draft, parent, token, temperature, seed, b0=0):
     """A batch of candidate trees with the oracle's own Philox (greedy rows take
     the greedy walk): target, draft [B, N, V]; parent, token [B, N];
-    temperature [B].  Returns dict(out_tokens, out_nodes [B, N], accept_len,
-    accept_margin, cdf_margin [B])."""
+    temperature [B]; row b is request b0 + b (its Philox index).  Returns
+    dict(out_tokens, out_nodes [B, N], accept_len, accept_margin, cdf_margin [B])."""
     target = np.ascontiguousarray(target)
     B, N, V = target.shape
     draft = np.ascontiguousarray(draft)
@@ -304,7 +305,7 @@ def verify_tree(target, draft, parent, token, temperature, seed):
     cm = np.empty(B, dtype=np.float64)
     rc = lib().svo_verify_tree_sampled(
         target.ctypes.data, draft.ctypes.data, dtype_code(target), _ptr(parent, ctypes.c_int32),
-        _ptr(token, ctypes.c_int32), B, N, V, _ptr(temperature, ctypes.c_float),
+        _ptr(token, ctypes.c_int32), int(b0), B, N, V, _ptr(temperature, ctypes.c_float),
         int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(ot, ctypes.c_int32), _ptr(on, ctypes.c_int32),
         _ptr(al, ctypes.c_int32), _ptr(am, ctypes.c_double), _ptr(cm, ctypes.c_double))
     if rc != 0:

@@ -521,10 +521,11 @@ int svo_verify_tree_u(const void *target, const void *draft, int dtype, const in
  * emitted token the sampling uniform of position u, so a chain tree draws the
  * same numbers as the linear verification.  target and draft [B, N, V];
  * parent, token [B, N]; outputs [B, N] and per-request accepted counts and
- * margins. */
+ * margins.  Row b of the arrays is request b0 + b of the batch (its Philox
+ * index). */
 int svo_verify_tree_sampled(const void *target, const void *draft, int dtype,
-                            const int32_t *parent, const int32_t *token, int B, int N, int V,
-                            const float *temperature, uint64_t seed, int32_t *out_tokens,
+                            const int32_t *parent, const int32_t *token, int b0, int B, int N,
+                            int V, const float *temperature, uint64_t seed, int32_t *out_tokens,
                             int32_t *out_nodes, int32_t *accepted, double *accept_margin,
                             double *cdf_margin) {
     const size_t esz = svo_esize(dtype);
@@ -540,8 +541,8 @@ int svo_verify_tree_sampled(const void *target, const void *draft, int dtype,
     for (int b = 0; b < B; ++b) {
         ua[0] = 0.0;
         for (int n = 0; n < N; ++n) {
-            if (n > 0) ua[n] = svo_u_accept(seed, (uint32_t)b, (uint32_t)(n - 1));
-            us[n] = svo_u_sample(seed, (uint32_t)b, (uint32_t)n);
+            if (n > 0) ua[n] = svo_u_accept(seed, (uint32_t)(b0 + b), (uint32_t)(n - 1));
+            us[n] = svo_u_sample(seed, (uint32_t)(b0 + b), (uint32_t)n);
         }
         const size_t off = (size_t)b * N;
         svo_diag d;

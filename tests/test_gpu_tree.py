@@ -95,16 +95,16 @@ def test_invalid_parents_flagged(sv):
 TREE_NEAR_TIE = 1e-5
 
 
-def _oracle_tree(inp):
-    """Oracle results for the whole batch (Philox keys use the request index).
-    The draft rows are padded to N with zeros: the last node has no children,
-    so the oracle never reads that row."""
+def _oracle_tree(inp, b0=0):
+    """Oracle results for the batch (Philox keys use the request index, the
+    first row being request b0).  The draft rows are padded to N with zeros:
+    the last node has no children, so the oracle never reads that row."""
     t = workloads.to_numpy_logits(inp["target"])
     B, N, V = t.shape
     d = workloads.to_numpy_logits(inp["draft"]) if N > 1 else np.zeros((B, 0, V), t.dtype)
     d = np.concatenate([d, np.zeros((B, 1, V), d.dtype)], axis=1)
     return oracle.verify_tree(t, d, inp["parent"].cpu().numpy(), inp["tokens"].cpu().numpy(),
-                              inp["temperature"].cpu().numpy(), inp["seed"])
+                              inp["temperature"].cpu().numpy(), inp["seed"], b0=b0)
 
 
 def _compare_tree(sv, inp, max_flag_frac=0.1):
@@ -236,12 +236,12 @@ def test_sampled_tree_first_token_law(sv):
             assert pval < 1e-6, pval
 
 
-@pytest.mark.parametrize("cfg,N,n_check", [(1, 16, 32), (4, 9, 48)])
-def test_sampled_trees_at_bench_workloads(sv, cfg, N, n_check):
+@pytest.mark.parametrize("cfg,N,b0,n_check", [(1, 16, 0, 32), (4, 9, 112, 48)])
+def test_sampled_trees_at_bench_workloads(sv, cfg, N, b0, n_check):
     """The sampled-tree workloads the benchmark times (same generator, seed and
     launch configuration: clusters with staged slices at c1, one CTA per
     request at c4 with its quarter of greedy requests), against the oracle on
-    the first n_check requests."""
+    requests [b0, b0 + n_check) (c4: greedy requests 112-127, sampled after)."""
     c = workloads.CONFIGS[cfg]
     T = c["T"] if isinstance(c["T"], float) else 1.0
     noise = c["noise"] if isinstance(c["noise"], float) else 0.5
@@ -253,9 +253,10 @@ def test_sampled_trees_at_bench_workloads(sv, cfg, N, n_check):
                                      inp["temperature"], inp["seed"], dev_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    sub = {k: (v[:n_check] if torch.is_tensor(v) else v) for k, v in inp.items()}
-    r = _oracle_tree(sub)
-    out, nodes, acc = out[:n_check].cpu().numpy(), nodes[:n_check].cpu().numpy(), acc[:n_check].cpu().numpy()
+    sl = slice(b0, b0 + n_check)
+    sub = {k: (v[sl] if torch.is_tensor(v) else v) for k, v in inp.items()}
+    r = _oracle_tree(sub, b0=b0)
+    out, nodes, acc = out[sl].cpu().numpy(), nodes[sl].cpu().numpy(), acc[sl].cpu().numpy()
     same = ((acc == r["accept_len"]) & (out == r["out_tokens"]).all(axis=1)
             & (nodes == r["out_nodes"]).all(axis=1))
     flagged = (r["accept_margin"] < TREE_NEAR_TIE) | (r["cdf_margin"] < TREE_NEAR_TIE)

@@ -774,3 +774,19 @@ def test_tree_sampled_hand_case(oracle):
     # a token outside [0, V) is no candidate: the second sibling is tested first
     ot, on, a = oracle.verify_tree_u(tgt, drf, parent, [0, 7, 1], T, [0, 0.0, 0.4], 0.5)
     assert a == 1 and on[0] == 2
+
+
+def test_tree_batch_offset_keeps_philox_index(oracle):
+    """Row b of a sliced batch with b0 is request b0 + b: the slice reproduces
+    the full batch's results for those requests."""
+    rng = np.random.default_rng(21)
+    B, N, V = 7, 6, 30
+    tgt = rng.normal(size=(B, N, V))
+    drf = tgt + rng.normal(size=(B, N, V)) * 0.8
+    parent = np.array([[-1] + [int(rng.integers(0, n)) for n in range(1, N)] for _ in range(B)], np.int32)
+    tok = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    T = np.full(B, 1.0, np.float32)
+    full = oracle.verify_tree(tgt, drf, parent, tok, T, 99)
+    part = oracle.verify_tree(tgt[3:6], drf[3:6], parent[3:6], tok[3:6], T[3:6], 99, b0=3)
+    for k in ("out_tokens", "out_nodes", "accept_len"):
+        assert np.array_equal(full[k][3:6], part[k])
