@@ -261,4 +261,6 @@ def test_sampled_trees_at_bench_workloads(sv, cfg, N, b0, n_check):
             & (nodes == r["out_nodes"]).all(axis=1))
     flagged = (r["accept_margin"] < TREE_NEAR_TIE) | (r["cdf_margin"] < TREE_NEAR_TIE)
     assert not (~same & ~flagged).any(), np.flatnonzero(~same & ~flagged)
-    assert flagged.sum() <= max(2, n_check // 10)
+    # at V >= 128k the CDF window flags many rows (much of the mass sits in
+    # tokens of tiny probability), so the gate counts actual mismatches
+    assert (~same).sum() <= 1, np.flatnonzero(~same)
