@@ -326,8 +326,11 @@ spec_status_t spec_verify_noalloc(const void *target_logits, const void *draft_l
  * waits on a barrier nothing completes; that bounded wait runs out after 1 ms
  * and the warp gives up as on a real timeout: SPEC_DEV_TIMEOUT in the status
  * word, its copies in flight drained (with the 2 s limit), its items skipped
- * (outputs then undefined but in range).  0 turns it off.  No counterpart on
- * the pages: it exercises the failure path of the bounded waits.
+ * (outputs then undefined but in range).  In spec_verify_tree calls, each
+ * staging of node rows in the sampled walk first waits on such a barrier,
+ * reports SPEC_DEV_TIMEOUT and then waits for its copies as usual (outputs
+ * unchanged).  0 turns it off.  No counterpart on the pages: it exercises the
+ * failure path of the bounded waits.
  */
 spec_status_t spec_debug_force_wait_timeout(int enable);
 

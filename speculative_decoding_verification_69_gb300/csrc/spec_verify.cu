@@ -1740,12 +1740,15 @@ template <int DT, bool VEC>
 __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const int32_t *parent,
                                                                const int32_t *token,
                                                                int32_t *out_nodes,
-                                                               int stage_row_bytes) {
+                                                               int stage_row_bytes, int diag) {
     // stage_row_bytes > 0: this CTA's slice of a node's target and draft rows is
     // copied into dynamic shared memory at the node's first rejection, and the
-    // node's later passes read it there
+    // node's later passes read it there.  diag: before each staging wait, every
+    // warp first waits on a barrier nothing completes, gives up after
+    // kDiagWaitNs and reports SPEC_DEV_TIMEOUT as on a real timeout (the real
+    // wait follows, so the results are unchanged).
     extern __shared__ __align__(128) unsigned char s_stage[];
-    __shared__ uint64_t s_tbar[kTreeWarps];
+    __shared__ uint64_t s_tbar[kTreeWarps], s_never;
     __shared__ int s_par[SPEC_MAX_TREE], s_tok[SPEC_MAX_TREE], s_amax[SPEC_MAX_TREE];
     __shared__ float s_m[2 * SPEC_MAX_TREE], s_S[2 * SPEC_MAX_TREE];
     __shared__ float s_u[SPEC_MAX_TREE], s_g[SPEC_MAX_TREE], s_gd[SPEC_MAX_TREE];
@@ -1784,6 +1787,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
     float c = 0.f, chi = 0.f, clo = 0.f;
     if (!greedy) temp_coeffs(T, c, chi, clo);
     if (lane == 0) mbar_init(&s_tbar[warp], 1);
+    if (tid == 0) mbar_init(&s_never, 1);
     fence_mbar_init();
     pdl_wait();  // partials come from sv_pass1
     pdl_trigger();
@@ -1880,6 +1884,9 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
                     }
                 }
                 __syncwarp();
+                if (diag && !__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&s_never, 0u, kDiagWaitNs)) &&
+                    lane == 0 && P.dev_status)
+                    atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
                 const bool ok = mbar_wait_bounded(&s_tbar[warp], stagings & 1u, kWaitLimitNs);
                 if (!__all_sync(0xFFFFFFFFu, ok) && lane == 0 && P.dev_status)
                     atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
@@ -2526,7 +2533,7 @@ spec_status_t spec_verify_tree(const void *target_logits, const void *draft_logi
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     sv::sv_tree_rows_s<<<1, sv::kPrepThreads, 0, s>>>(P);
     const int g1 = d->sms * d->occ_p1[dtype == SPEC_DTYPE_BF16 ? sv::kBF16 : sv::kF32][vec ? 1 : 0];
-    void (*walk)(sv::Params, const int32_t *, const int32_t *, int32_t *, int);
+    void (*walk)(sv::Params, const int32_t *, const int32_t *, int32_t *, int, int);
     if (dtype == SPEC_DTYPE_BF16) {
         if (vec) sv::launch_dependent(sv::sv_pass1<sv::kBF16, true>, g1, sv::kP1Warps * 32, sv::kP1Smem, s, P);
         else sv::launch_dependent(sv::sv_pass1<sv::kBF16, false>, g1, sv::kP1Warps * 32, 0, s, P);
@@ -2565,7 +2572,8 @@ spec_status_t spec_verify_tree(const void *target_logits, const void *draft_logi
         set = true;
     }
     cfg.dynamicSmemBytes = stage ? (size_t)(2 * row_bytes) : 0;
-    cudaLaunchKernelEx(&cfg, walk, P, parent, node_tokens, out_nodes, stage);
+    cudaLaunchKernelEx(&cfg, walk, P, parent, node_tokens, out_nodes, stage,
+                       sv::g_diag_timeout ? 1 : 0);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

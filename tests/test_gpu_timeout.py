@@ -60,3 +60,27 @@ def test_poisoned_workspace_and_outputs(cfg, ee):
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(a1, a2)
     assert (o2 != 123456).all() and (a2 >= 0).all()
+
+
+def test_tree_walk_wait_timeout_is_reported():
+    """The sampled tree walk's staging wait: with the diagnostic switch on, each
+    warp first gives up on a barrier nothing completes and reports
+    SPEC_DEV_TIMEOUT, then waits for its copies, so the outputs equal a clean
+    run's; the next call reports nothing."""
+    import speculative_decoding_verification_69_gb300 as sv
+    inp = workloads.make_tree_inputs(32, 16, 151936, torch.bfloat16, seed=41, T=1.0)
+    args = (inp["target"], inp["draft"], inp["parent"], inp["tokens"], inp["temperature"],
+            inp["seed"])
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    try:
+        sv.force_wait_timeout(True)
+        o1, n1, a1 = sv.verify_tree(*args, dev_status=st)
+        torch.cuda.synchronize()
+    finally:
+        sv.force_wait_timeout(False)
+    assert int(st.item()) & sv.DEV_TIMEOUT
+    st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o2, n2, a2 = sv.verify_tree(*args, dev_status=st2)
+    torch.cuda.synchronize()
+    assert int(st2.item()) == 0
+    assert torch.equal(o1, o2) and torch.equal(n1, n2) and torch.equal(a1, a2)
