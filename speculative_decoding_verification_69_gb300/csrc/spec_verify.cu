@@ -1373,11 +1373,20 @@ constexpr int kTreeGroups = 256;   // recorded masses per warp (groups of steps)
 constexpr float kTreeBias = 2.0f;  // every summed weight is at most ~1
 constexpr int kTreeStageMax = 192 * 1024;  // dynamic shared memory for a staged slice (two rows)
 
-// The weight 2^((z - m) c + l) of one element: the scalar twin of weight2l
-// (the same operations in the same order, so the same value).
-__device__ __forceinline__ float weight1l(float z, float m, float chi, float clo, float l) {
-    const float d = __fsub_rn(z, m);
-    return ex2(__fmaf_rn(d, chi, __fmaf_rn(d, clo, l)));
+// The weight 2^(z c + base) of one element, base = l - m c for a row with
+// max m and log2(1/S) = l: one FMA per element.  The rounding of base scales
+// every weight of the row alike, which the exact normalisers (the sums of the
+// same weights) remove.  wpair is the twin for an element pair (the same
+// operations, so the same values).
+__device__ __forceinline__ float weight1b(float z, float c, float base) {
+    return ex2(__fmaf_rn(z, c, base));
+}
+__device__ __forceinline__ float2 wpair(float2 z, float2 c2, float2 base2) {
+    const float2 t = fma2(z, c2, base2);
+    return make_float2(ex2(t.x), ex2(t.y));
+}
+__device__ __forceinline__ float row_base(float m, float c, float l) {
+    return __fmaf_rn(-m, c, l);
 }
 
 // Residual after j rejected siblings, in closed form.  With p, q the target
@@ -1420,7 +1429,7 @@ template <int DT, bool VEC> struct Eight {
 
 // Per-node constants of the sampled walk.
 struct TreeNodeC {
-    float2 mt, lt, md, ld, chi, clo;  // row max and log2(1/S) of the target and draft rows, c
+    float2 bt, bd, c2;  // weight bases of the target and draft rows (row_base), log2(e)/T
     float s;                          // residual threshold (0: the weights p)
 };
 
@@ -1435,12 +1444,12 @@ __device__ __forceinline__ void tree_weights8(const Eight<DT, VEC> &zt, const Ei
                                               const TreeNodeC &nc, int mode, float w[8]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float2 a = weight2l(zt.pair(i), nc.mt, nc.chi, nc.clo, nc.lt);
+        const float2 a = wpair(zt.pair(i), nc.c2, nc.bt);
         if (mode == kTreeModeP) {
             w[2 * i] = a.x;
             w[2 * i + 1] = a.y;
         } else {
-            const float2 bq = weight2l(zd.pair(i), nc.md, nc.chi, nc.clo, nc.ld);
+            const float2 bq = wpair(zd.pair(i), nc.c2, nc.bd);
             w[2 * i] = resid_weight(a.x, bq.x, nc.s);
             w[2 * i + 1] = resid_weight(a.y, bq.y, nc.s);
         }
@@ -1570,8 +1579,8 @@ __device__ void tree_pass(const char *rowt, const char *rowd, const char *stt, c
             if (mode == kTreeModeFirst) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float2 a = weight2l(zt[u].pair(i), nc.mt, nc.chi, nc.clo, nc.lt);
-                    const float2 bq = weight2l(zd[u].pair(i), nc.md, nc.chi, nc.clo, nc.ld);
+                    const float2 a = wpair(zt[u].pair(i), nc.c2, nc.bt);
+                    const float2 bq = wpair(zd[u].pair(i), nc.c2, nc.bd);
                     acc[0].add(a);
                     acc[1].add(bq);
                     const bool gx = a.x > bq.x, gy = a.y > bq.y;
@@ -1816,15 +1825,13 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
         const bool inner = cur < N - 1;  // only such a node can have children (and a draft row)
         const char *rowd = inner ? row_ptr(P, b, K + 1 + cur, ESZ) : rowt;
         TreeNodeC nc;
-        nc.chi = make_float2(chi, chi);
-        nc.clo = make_float2(clo, clo);
+        nc.c2 = make_float2(c, c);
         const float mt = s_m[cur], St = s_S[cur];
         const float md = inner ? s_m[K + 1 + cur] : 0.f, Sd = inner ? s_S[K + 1 + cur] : 1.f;
         const float lt = -log2f(St), ld = -log2f(Sd);
-        nc.mt = make_float2(mt, mt);
-        nc.lt = make_float2(lt, lt);
-        nc.md = make_float2(md, md);
-        nc.ld = make_float2(ld, ld);
+        const float bt = row_base(mt, c, lt), bd = row_base(md, c, ld);
+        nc.bt = make_float2(bt, bt);
+        nc.bd = make_float2(bd, bd);
         nc.s = 0.f;
         bool staged = false;  // this node's slice is in shared memory
         if (warp == 0) {  // the children of cur with a token in [0, V), in index order
@@ -1849,7 +1856,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
                 if (J == 0) {
                     acc = accept_position(u, g, mt, St, gd, md, Sd, chi, clo);
                 } else {
-                    const float a = weight1l(g, mt, chi, clo, lt), bq = weight1l(gd, md, chi, clo, ld);
+                    const float a = weight1b(g, c, bt), bq = weight1b(gd, c, bd);
                     const float w = nc.s > 0.f ? resid_weight(a, bq, nc.s) : a;
                     acc = (double)u * (double)bq * s_sum < (double)w * s_SB;
                 }
