@@ -324,6 +324,7 @@ def run_tree(args, world, rank, local):
         parent = torch.from_numpy(parent).to(dev)
         tok = torch.from_numpy(tok).to(dev)
         drf = None
+        temp, seed = None, 0  # greedy walk: no temperatures, no uniforms
     if drf is None:
         alg_bytes = B * N * V * esz
     else:  # every target row, and the draft rows of sampled requests, once
@@ -367,7 +368,7 @@ def run_tree(args, world, rank, local):
     positions = sum_over_ranks(B * (N - 1) * args.steps, world)
     peak, peak_kind = measured_peak()
     step_s = total_s_max / args.steps
-    return {
+    res = {
         "metric": "verified draft positions/s", "value": positions / total_s_max,
         "unit": "positions/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -385,8 +386,107 @@ def run_tree(args, world, rank, local):
         "roofline": {"bound": "hbm", "kernel": "whole step", "achieved": alg_bytes / step_s / 1e9,
                      "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
                      "frac": alg_bytes / step_s / 1e9 / peak, "traffic": None},
-        "e2e": None, "gpu_launches": 3 * args.steps, "clocks": clk,
+        "e2e": tree_e2e(args, world, sv, dev, tgt, drf, parent, tok, temp, seed, N),
+        "gpu_launches": 3 * args.steps, "clocks": clk,
     }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pps, cores, sample, dt = tree_oracle_sample(tgt, drf, parent, tok, temp, seed,
+                                                    args.cpu_seconds)
+        res["cpu_baseline"] = {"value": pps, "unit": "positions/s", "cores": cores,
+                               "kind": "oracle", "sample": sample, "seconds": dt}
+    return res
+
+
+def tree_e2e(args, world, sv, dev, tgt, drf, parent, tok, temp, seed, N):
+    """The tree metric through the public API with the step's inputs copied
+    from pinned host memory and the outputs read back, every step."""
+    B = tgt.shape[0]
+    host = {"t": tgt.cpu().pin_memory(), "p": parent.cpu().pin_memory(), "k": tok.cpu().pin_memory()}
+    if drf is not None:
+        host["d"] = drf.cpu().pin_memory()
+        host["T"] = temp.cpu().pin_memory()
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    h_out = torch.empty((B, N), dtype=torch.int32).pin_memory()
+    h_nodes = torch.empty((B, N), dtype=torch.int32).pin_memory()
+    h_acc = torch.empty((B,), dtype=torch.int32).pin_memory()
+    ws = torch.empty(max(int(sv.load_library().spec_tree_workspace_bytes(B, N, tgt.shape[2],
+                                                                          sv._dtype_code(tgt))), 256),
+                     dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        for k, v in host.items():
+            dbuf[k].copy_(v, non_blocking=True)
+        if drf is None:
+            o, n, a = sv.verify_tree_greedy(dbuf["t"], dbuf["p"], dbuf["k"])
+        else:
+            o, n, a = sv.verify_tree(dbuf["t"], dbuf["d"], dbuf["p"], dbuf["k"], dbuf["T"], seed,
+                                     workspace=ws)
+        h_out.copy_(o, non_blocking=True)
+        h_nodes.copy_(n, non_blocking=True)
+        h_acc.copy_(a, non_blocking=True)
+
+    steps = max(1, min(args.steps, 50))
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier(world)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        e2e_step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / 1e3, world)
+    positions = sum_over_ranks(B * (N - 1) * steps, world)
+    return {"value": positions / e2e_s, "unit": "positions/s",
+            "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
+            "d2h_bytes_per_step": (h_out.numel() + h_nodes.numel() + h_acc.numel()) * 4,
+            "steps": steps}
+
+
+def tree_oracle_sample(tgt, drf, parent, tok, temp, seed, max_seconds):
+    """Time the CPU oracle's tree verification on a bounded sample of the
+    workload's requests, one host thread per core (the oracle's C code runs
+    outside the interpreter lock), requests split across the threads."""
+    import numpy as np
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    B, N, V = tgt.shape
+    t = workloads.to_numpy_logits(tgt)
+    par, tk = parent.cpu().numpy(), tok.cpu().numpy()
+    if drf is not None:
+        d = workloads.to_numpy_logits(drf)
+        d = np.concatenate([d, np.zeros((B, 1, V), d.dtype)], axis=1)  # the last node has no children
+        T = temp.cpu().numpy()
+
+    def run(b0, b1):
+        if drf is None:
+            for b in range(b0, b1):
+                oracle.verify_tree_greedy(t[b], par[b], tk[b])
+        else:
+            oracle.verify_tree(t[b0:b1], d[b0:b1], par[b0:b1], tk[b0:b1], T[b0:b1], seed, b0=b0)
+
+    cores = oracle.cpu_count()
+    t0 = time.perf_counter()
+    run(0, 1)
+    t_one = max(time.perf_counter() - t0, 1e-6)
+    nthreads = min(cores, B)
+    n = B if t_one * B / nthreads <= max_seconds else int(min(B, max(nthreads, max_seconds * nthreads / t_one)))
+    nthreads = min(nthreads, n)
+    bounds = [(i * n // nthreads, (i + 1) * n // nthreads) for i in range(nthreads)]
+    reps, dt = 0, 0.0
+    with ThreadPoolExecutor(max_workers=nthreads) as ex:
+        while reps == 0 or dt < max_seconds:
+            t0 = time.perf_counter()
+            list(ex.map(lambda r: run(*r), bounds))
+            dt += time.perf_counter() - t0
+            reps += 1
+    pos = n * (N - 1) * reps
+    return (pos / dt, nthreads, "requests 0..%d of %d x %d passes (%d candidate nodes), %d threads"
+            % (n - 1, B, reps, pos, nthreads), dt)
 
 
 def run_ours(args, world, rank, local):
