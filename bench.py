@@ -4,8 +4,9 @@
 
 One step = one pass of the whole hot path over one batch of synthetic inputs
 already resident in HBM: spec_schedule_len (for the confidence-scheduled
-workload c3) and spec_verify.  Default workload: c1 (B=32, K=8, V=151936,
-bf16).  L2: every workload reads more logits per step than L2 holds, and the
+workload c3) and spec_verify.  Default workload: c4 (B=512, K=8, V=201088,
+bf16, a quarter of the requests greedy, the others T ~ U(0, 1.2]); --config
+picks c1-c3.  L2: every workload reads more logits per step than L2 holds, and the
 timed steps cycle round-robin through several device copies of the logits, so
 that at least twice the L2 size is read between two uses of the same copy:
 each step starts L2-cold without a flush write (whose dirty lines would be
@@ -37,6 +38,7 @@ import sys
 import threading
 import time
 
+import numpy as np
 import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -157,7 +159,12 @@ class ClockSampler:
     def mark(self, t0, t1):
         self.window = (t0, t1)
 
-    def stop(self):
+    def stop(self, timed=None, label=None):
+        """Median SM clock, max clock and active throttle reasons over the
+        marked window (the whole stretch of GPU work: warm-up, timed loops and
+        the end-to-end loop, so that short timed regions still get samples);
+        `timed` = (t0, t1) of the timed region, whose sample count is also
+        given."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -170,9 +177,12 @@ class ClockSampler:
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         lo, hi = self.window
+        n_timed = 0
         for ts, ln in self.lines:
             if ts < lo or ts > hi:
                 continue
+            if timed and timed[0] <= ts <= timed[1]:
+                n_timed += 1
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -186,8 +196,13 @@ class ClockSampler:
                     reasons.add(n)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        res = {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if label:
+            res["window"] = label
+        if timed:
+            res["timed_region_samples"] = n_timed
+        return res
 
 
 def dist_setup(n_gpus):
@@ -272,6 +287,43 @@ def oracle_sample(inp, max_seconds=12.0, min_requests=2, host=None):
             % (n - 1, B, reps, pos, nthreads), dt, r)
 
 
+def oracle_single_thread(inp, host, max_seconds=4.0):
+    """The oracle on one host thread: requests one at a time from the start of
+    the batch until the time budget is spent (at least one)."""
+    import oracle
+    B, K = host["tok"].shape
+    vl = host["vl"]
+    pos, dt, b = 0, 0.0, 0
+    while b == 0 or (dt < max_seconds and b < B):
+        t0 = time.perf_counter()
+        oracle.verify(host["t"], host["d"], host["tok"], vl, host["T"], inp["seed"], b0=b,
+                      b1=b + 1, nthreads=1)
+        dt += time.perf_counter() - t0
+        pos += int(min(max(int(vl[b]), 0), K)) if vl is not None else K
+        b += 1
+    return pos / max(dt, 1e-9), "requests 0..%d, one at a time, 1 thread (%d positions, %.2f s)" % (
+        b - 1, pos, dt)
+
+
+def parity_counts(o_host, a_host, r, T, window=1e-6):
+    """GPU outputs of the timed steps against the oracle on the requests the CPU
+    baseline verified: exact agreement, and the oracle's near-tie flags (its
+    uniform within `window` of an acceptance ratio or a normalised CDF
+    boundary)."""
+    import numpy as np
+    import oracle
+    n = len(r["accept_len"])
+    same = (a_host[:n] == r["accept_len"]) & np.all(o_host[:n] == r["out_tokens"], axis=1)
+    greedy = np.array([oracle.is_greedy(float(t)) for t in T[:n]])
+    flagged = (r["accept_margin"] < window) | (r["cdf_margin"] < window)
+    samp = ~greedy
+    return {"requests": int(n), "greedy": int(greedy.sum()), "sampled": int(samp.sum()),
+            "greedy_mismatch": int((~same & greedy).sum()),
+            "sampled_mismatch": int((~same & samp).sum()),
+            "unflagged_mismatch": int((~same & samp & ~flagged).sum()),
+            "near_tie_flagged": int((flagged & samp).sum()), "window": window}
+
+
 # ---------------------------------------------------------------- GPU arm
 
 def prepare(cfg, rank, device):
@@ -345,14 +397,15 @@ def run_tree(args, world, rank, local):
             sv.verify_tree(t, d, parent, tok, temp, seed, workspace=ws)
 
     stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_gpu0 = time.perf_counter()
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    clocks = ClockSampler(local)
     barrier(world)
-    clocks.start()
     t0 = time.perf_counter()
     for i in range(args.steps):
         ev[i][0].record(stream)
@@ -361,8 +414,6 @@ def run_tree(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     t1 = time.perf_counter()
-    clocks.mark(t0, t1 + 0.05)
-    clk = clocks.stop()
     total_s = sum(a.elapsed_time(b) for a, b in ev) / 1e3
     total_s_max = max_over_ranks(total_s, world)
     positions = sum_over_ranks(B * (N - 1) * args.steps, world)
@@ -387,8 +438,11 @@ def run_tree(args, world, rank, local):
                      "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
                      "frac": alg_bytes / step_s / 1e9 / peak, "traffic": None},
         "e2e": tree_e2e(args, world, sv, dev, tgt, drf, parent, tok, temp, seed, N),
-        "gpu_launches": 3 * args.steps, "clocks": clk,
+        "gpu_launches": 3 * args.steps,
     }
+    clocks.mark(t_gpu0, time.perf_counter() + 0.05)
+    res["clocks"] = clocks.stop(timed=(t0, t1),
+                                label="warm-up, the timed loop and the end-to-end loop")
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         pps, cores, sample, dt = tree_oracle_sample(tgt, drf, parent, tok, temp, seed,
                                                     args.cpu_seconds)
@@ -535,6 +589,9 @@ def run_ours(args, world, rank, local):
         verifier(tgt, drf, inp["tokens"], vlen, inp["temperature"],
                  inp["seed"], out_tokens=out_tokens, accept_len=accept_len, early_exit=ee)
 
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_gpu0 = time.perf_counter()
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
@@ -549,10 +606,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(args.steps)]
-    clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
-    clocks.start()
     t_wall0 = time.perf_counter()
     # timed region 1: the steps as a caller runs them (value, ms_per_step)
     for i in range(args.steps):
@@ -577,8 +632,6 @@ def run_ours(args, world, rank, local):
     barrier(world)
     t_wall2 = time.perf_counter()
     t_wall = t_wall1 - t_wall0
-    clocks.mark(t_wall0, t_wall2 + 0.05)
-    clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     kern_ms = [a.elapsed_time(b) for a, b in kev]
     step_k_ms = [a.elapsed_time(b) for a, b in ev_k]
@@ -591,6 +644,11 @@ def run_ours(args, world, rank, local):
     if ee:  # logit bytes the two waves actually read, from each request's outcome
         read_bytes = early_exit_bytes(inp["temperature"], vlen, accept_len, K, V, esz, ee)
         kern_avg_s = total_s / args.steps
+
+    # outcome of the timed steps (each step verifies the same batch)
+    o_host = out_tokens.cpu().numpy()
+    a_host = accept_len.cpu().numpy()
+    accept_hist = [int(x) for x in np.bincount(a_host, minlength=K + 1)]
 
     # end to end through the public API: pinned host inputs -> device -> verify -> host
     host = {k: inp[k].cpu().pin_memory() for k in ("target", "draft", "tokens", "temperature")}
@@ -614,20 +672,25 @@ def run_ours(args, world, rank, local):
         h_out.copy_(o, non_blocking=True)
         h_acc.copy_(a, non_blocking=True)
 
+    e2e_steps = max(1, min(args.steps, 100))  # each copies the whole batch over the host link
     for _ in range(max(1, args.warmup)):
         e2e_step()
     torch.cuda.synchronize()
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+              for _ in range(e2e_steps)]
     barrier(world)
-    for i in range(args.steps):
+    for i in range(e2e_steps):
         e2e_ev[i][0].record(stream)
         e2e_step()
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     e2e_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev) / 1e3, world)
-    e2e_value = all_pos / e2e_s
+    e2e_value = sum_over_ranks(positions * e2e_steps, world) / e2e_s
+    t_gpu1 = time.perf_counter()
+    clocks.mark(t_gpu0, t_gpu1 + 0.05)
+    clk = clocks.stop(timed=(t_wall0, t_wall2),
+                      label="warm-up, both timed loops and the end-to-end loop")
 
     peak, peak_kind = measured_peak()
     achieved = read_bytes / kern_avg_s / 1e9
@@ -681,15 +744,23 @@ def run_ours(args, world, rank, local):
             "kernel_ms": kern_avg_s * 1e3,
         },
         "e2e": {"value": e2e_value, "unit": "positions/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": launches,
         "clocks": clk,
         "wall_s": t_wall,
+        "accept_len_hist": accept_hist,
+        "emitted_tokens_per_step": int(a_host.sum()) + B,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        pps, cores, sample, dt, _ = oracle_sample(inp, max_seconds=args.cpu_seconds)
+        oinp = dict(inp, verify_len=vlen)  # the lengths the GPU verified
+        host_o = host_arrays(oinp)
+        pps, cores, sample, dt, r = oracle_sample(oinp, max_seconds=args.cpu_seconds, host=host_o)
+        pps1, sample1 = oracle_single_thread(oinp, host_o, max_seconds=min(4.0, args.cpu_seconds))
         result["cpu_baseline"] = {"value": pps, "unit": "positions/s", "cores": cores,
-                                  "kind": "oracle", "sample": sample, "seconds": dt}
+                                  "kind": "oracle", "sample": sample, "seconds": dt,
+                                  "single_thread": {"value": pps1, "unit": "positions/s",
+                                                    "sample": sample1}}
+        result["parity_sample"] = parity_counts(o_host, a_host, r, host_o["T"])
     return result
 
 
@@ -739,7 +810,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--config", type=int, default=4, choices=[0, 1, 2, 3, 4])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -221,7 +221,10 @@ spec_status_t spec_verify_tree_greedy(const void *target_logits, spec_dtype_t dt
  *   [B, N] int32; temperature [B] float32 device.  Outputs as
  *   spec_verify_tree_greedy; the workspace is spec_tree_workspace_bytes.
  *   Each sampled request costs one pass over its vocabulary per rejected
- *   candidate, run by one CTA.  Errors as spec_verify.
+ *   candidate, run by a thread-block cluster of up to 8 CTAs (as many as the
+ *   batch leaves SMs free; one CTA each at large batches).  After a staging
+ *   wait runs out (SPEC_DEV_TIMEOUT) the request's outputs are undefined but
+ *   in range.  Errors as spec_verify.
  */
 spec_status_t spec_verify_tree(const void *target_logits, const void *draft_logits,
                                spec_dtype_t dtype, const int32_t *parent,

@@ -1772,6 +1772,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
     __shared__ double s_base, s_thr;
     __shared__ float s_s;
     __shared__ int s_acc, s_R, s_W, s_emit, s_again;
+    __shared__ int s_nostage;  // a staging wait ran out: no more staging in this request
     constexpr int ESZ = Fmt<DT>::kESZ;
     const int cs = cluster_size(), rank = cluster_rank();
     const int b = blockIdx.x / cs, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1796,7 +1797,10 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
     float c = 0.f, chi = 0.f, clo = 0.f;
     if (!greedy) temp_coeffs(T, c, chi, clo);
     if (lane == 0) mbar_init(&s_tbar[warp], 1);
-    if (tid == 0) mbar_init(&s_never, 1);
+    if (tid == 0) {
+        mbar_init(&s_never, 1);
+        s_nostage = 0;
+    }
     fence_mbar_init();
     pdl_wait();  // partials come from sv_pass1
     pdl_trigger();
@@ -1833,7 +1837,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
         nc.bt = make_float2(bt, bt);
         nc.bd = make_float2(bd, bd);
         nc.s = 0.f;
-        bool staged = false;  // this node's slice is in shared memory
+        bool staged = false;  // this node's slice is in shared memory (this warp's steps)
         if (warp == 0) {  // the children of cur with a token in [0, V), in index order
             int n = 0;
             for (int base = cur + 1; base < N; base += 32) {
@@ -1875,7 +1879,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
                 nc.s = s_s;
                 if (!more) break;  // the recording pass below needs no mass
             }
-            if (J == 1 && stage_row_bytes > 0) {  // every warp copies its own steps, then waits
+            if (J == 1 && stage_row_bytes > 0 && !s_nostage) {  // every warp copies its own steps, then waits
                 const TreeSplit sp(V, rank, cs, warp);
                 fence_proxy_async();  // earlier reads of the buffer come first
                 __syncwarp();
@@ -1895,10 +1899,17 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
                     lane == 0 && P.dev_status)
                     atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
                 const bool ok = mbar_wait_bounded(&s_tbar[warp], stagings & 1u, kWaitLimitNs);
-                if (!__all_sync(0xFFFFFFFFu, ok) && lane == 0 && P.dev_status)
-                    atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
-                ++stagings;
                 staged = true;
+                if (!__all_sync(0xFFFFFFFFu, ok)) {
+                    // give up on staging: report, let this warp's copies land
+                    // (bounded), read global memory from here on (the barrier's
+                    // phase is no longer known, so the request stages no more)
+                    if (lane == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_TIMEOUT);
+                    mbar_wait_bounded(&s_tbar[warp], stagings & 1u, kWaitLimitNs);
+                    if (lane == 0) s_nostage = 1;
+                    staged = false;
+                }
+                ++stagings;
             }
             const char *stt = staged ? (const char *)s_stage : nullptr;
             const char *std_ = staged ? (const char *)s_stage + stage_row_bytes : nullptr;
@@ -1917,7 +1928,13 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
                     s_SB = tot[1];
                     s_iSB = 1.0 / tot[1];
                     const float s1 = (float)(tot[0] * s_iSB);
-                    S = tot[2] + (1.0 - (double)s1) * tot[3];  // sum over a > b of (a - s_1 b)
+                    // sum over a > b of (a - s_1 b): the residual max(0, a - s_1 b)
+                    // summed over a > b instead of a > s_1 b.  The two supports
+                    // differ only where a lies between b and s_1 b; with
+                    // |s_1 - 1| ~ 1e-6 (both weight sets are normalised to ~1)
+                    // the mass differs by at most |s_1 - 1| times the draft mass
+                    // of those near ties, far below the acceptance window.
+                    S = tot[2] + (1.0 - (double)s1) * tot[3];
                     s_s = s1;
                 } else {
                     S = tot[0];
@@ -1944,7 +1961,9 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
             __syncthreads();  // s_acc and the sums are rewritten at the next node
             continue;
         }
-        // no child accepted: the emitted token from the current weights
+        // no child accepted: the emitted token from the current weights (a warp
+        // whose staging gave up reads global memory; tree_find below reads
+        // another warp's steps, so it takes the staged copy only if no warp gave up)
         const char *stt = staged ? (const char *)s_stage : nullptr;
         const char *std_ = staged ? (const char *)s_stage + stage_row_bytes : nullptr;
         for (;;) {
@@ -1987,10 +2006,12 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
         }
         const int mode = nc.s > 0.f ? kTreeModeThr : kTreeModeP;
         if (rank == s_R && s_W >= 0 && warp == 0) {
-            if (staged)  // warp W's copy completed before its pass: acquire it here
+            const bool use_stage = staged && !s_nostage;
+            if (use_stage)  // warp W's copy completed before its pass: acquire it here
                 mbar_wait_bounded(&s_tbar[s_W], (stagings - 1u) & 1u, kWaitLimitNs);
-            const int tok = tree_find<DT, VEC>(rowt, rowd, stt, std_, V, rank, cs, nc, mode, s_mass,
-                                               s_W, s_base, s_thr, lane);
+            const int tok = tree_find<DT, VEC>(rowt, rowd, use_stage ? stt : nullptr,
+                                               use_stage ? std_ : nullptr, V, rank, cs, nc, mode,
+                                               s_mass, s_W, s_base, s_thr, lane);
             if (lane == 0 && tok >= 0) s_emit = tok;
         }
         __syncthreads();
@@ -2135,6 +2156,7 @@ struct DevInfo {
     int sms = 0;
     int occ_p1[2][2] = {{0, 0}, {0, 0}};
     int occ_sample[2][2] = {{0, 0}, {0, 0}};
+    bool walk_smem[2][2] = {{false, false}, {false, false}};  // tree walk's shared-memory limit raised
     bool ok = false;
 };
 
@@ -2166,7 +2188,7 @@ static bool setup_kernels(DevInfo &d) {
     return true;
 }
 
-static const DevInfo *dev_info() {
+static DevInfo *dev_info() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     DevInfo &d = g_dev[dev];
@@ -2270,7 +2292,7 @@ static spec_status_t verify_impl(const void *target_logits, const void *draft_lo
     const Layout L = layout(B, K, V, dtype);
     if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u))
         return SPEC_ERR_WORKSPACE;
-    const DevInfo *d = dev_info();
+    DevInfo *d = dev_info();
     if (!d) return SPEC_ERR_CUDA;
     const int esz = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
     const bool vec = ((size_t)V * (size_t)esz) % 16u == 0;
@@ -2383,7 +2405,7 @@ spec_status_t spec_draft_confidence(const void *draft_logits, spec_dtype_t dtype
     const sv::Layout L = sv::layout(B, K, V, dtype);
     if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u))
         return SPEC_ERR_WORKSPACE;
-    const sv::DevInfo *d = sv::dev_info();
+    sv::DevInfo *d = sv::dev_info();
     if (!d) return SPEC_ERR_CUDA;
     const int esz = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
     const bool vec = ((size_t)V * (size_t)esz) % 16u == 0;
@@ -2449,7 +2471,7 @@ spec_status_t spec_verify_tree_greedy(const void *target_logits, spec_dtype_t dt
     const sv::Layout L = sv::layout(B, K, V, dtype);
     if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u))
         return SPEC_ERR_WORKSPACE;
-    const sv::DevInfo *d = sv::dev_info();
+    sv::DevInfo *d = sv::dev_info();
     if (!d) return SPEC_ERR_CUDA;
     const int esz = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
     const bool vec = ((size_t)V * (size_t)esz) % 16u == 0;
@@ -2513,7 +2535,7 @@ spec_status_t spec_verify_tree(const void *target_logits, const void *draft_logi
     const sv::Layout L = sv::layout(B, K, V, dtype);
     if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u))
         return SPEC_ERR_WORKSPACE;
-    const sv::DevInfo *d = sv::dev_info();
+    sv::DevInfo *d = sv::dev_info();
     if (!d) return SPEC_ERR_CUDA;
     const int esz = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
     const bool vec = ((size_t)V * (size_t)esz) % 16u == 0;
@@ -2570,8 +2592,8 @@ spec_status_t spec_verify_tree(const void *target_logits, const void *draft_logi
     const long long nsteps = ((long long)V + sv::kTreeStep - 1) / sv::kTreeStep;
     const long long row_bytes = (nsteps + cs - 1) / cs * sv::kTreeStep * esz;
     const int stage = vec && 2 * row_bytes <= sv::kTreeStageMax ? (int)row_bytes : 0;
-    static bool smem_set[2][2] = {{false, false}, {false, false}};
-    bool &set = smem_set[dtype == SPEC_DTYPE_BF16 ? 1 : 0][vec ? 1 : 0];
+    // the attribute applies to the current device only: raised once per device
+    bool &set = d->walk_smem[dtype == SPEC_DTYPE_BF16 ? 1 : 0][vec ? 1 : 0];
     if (!set) {
         if (cudaFuncSetAttribute(walk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)sv::kTreeStageMax) != cudaSuccess)
@@ -2579,8 +2601,9 @@ spec_status_t spec_verify_tree(const void *target_logits, const void *draft_logi
         set = true;
     }
     cfg.dynamicSmemBytes = stage ? (size_t)(2 * row_bytes) : 0;
-    cudaLaunchKernelEx(&cfg, walk, P, parent, node_tokens, out_nodes, stage,
-                       sv::g_diag_timeout ? 1 : 0);
+    if (cudaLaunchKernelEx(&cfg, walk, P, parent, node_tokens, out_nodes, stage,
+                           sv::g_diag_timeout ? 1 : 0) != cudaSuccess)
+        return SPEC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
