@@ -571,23 +571,36 @@ def run_ours(args, world, rank, local):
     ee = args.early_exit
     chain = args.chain
     conf = torch.empty((B, K), dtype=torch.float32, device=dev)
-    if chain:  # confidences, budgeted schedule and verification, all on the device
+    fused = chain or (scheduled and not ee)  # one spec_verify_scheduled call per step
+    if chain:
+        # confidences from the draft rows (read once; their statistics serve the
+        # step too), a budget of `chain` positions per request, verification
         vlen = torch.empty((B,), dtype=torch.int32, device=dev)
-        sv.draft_confidence(inp["draft"], inp["temperature"], out=conf, verifier=verifier)
-        sv.schedule_budget(conf, chain * B, out=vlen)
+        sv.verify_scheduled(inp["target"], inp["draft"], inp["tokens"], inp["temperature"],
+                            inp["seed"], budget=chain * B, maxprob_out=conf, verify_len_out=vlen,
+                            out_tokens=out_tokens, accept_len=accept_len, verifier=verifier)
         torch.cuda.synchronize()
         positions = workloads.verified_positions(vlen)
-        alg_bytes = workloads.algorithmic_bytes(inp["temperature"], vlen, V, esz)
+        t_ = inp["temperature"].float().cpu()
+        n_samp = int(((t_ > 0) & torch.isfinite(t_) & (t_ >= torch.finfo(torch.float32).tiny)).sum())
+        alg_bytes = (n_samp * K + int((vlen.cpu().long() + 1).sum())) * V * esz
 
     def step(i):
         tgt, drf = copies[i % ncopies]
         if chain:
-            sv.draft_confidence(drf, inp["temperature"], out=conf, verifier=verifier)
-            sv.schedule_budget(conf, chain * B, out=vlen)
-        elif scheduled:
-            sv.schedule_len(inp["draft_maxprob"], inp["threshold"], out=vlen)
-        verifier(tgt, drf, inp["tokens"], vlen, inp["temperature"],
-                 inp["seed"], out_tokens=out_tokens, accept_len=accept_len, early_exit=ee)
+            sv.verify_scheduled(tgt, drf, inp["tokens"], inp["temperature"], inp["seed"],
+                                budget=chain * B, maxprob_out=conf, verify_len_out=vlen,
+                                out_tokens=out_tokens, accept_len=accept_len, verifier=verifier)
+        elif fused:  # the threshold schedule formed inside the step's first kernel
+            sv.verify_scheduled(tgt, drf, inp["tokens"], inp["temperature"], inp["seed"],
+                                threshold=inp["threshold"], draft_maxprob=inp["draft_maxprob"],
+                                verify_len_out=vlen, out_tokens=out_tokens, accept_len=accept_len,
+                                verifier=verifier)
+        else:
+            if scheduled:
+                sv.schedule_len(inp["draft_maxprob"], inp["threshold"], out=vlen)
+            verifier(tgt, drf, inp["tokens"], vlen, inp["temperature"],
+                     inp["seed"], out_tokens=out_tokens, accept_len=accept_len, early_exit=ee)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -622,7 +635,7 @@ def run_ours(args, world, rank, local):
     # overlap on both sides of it, so these steps run slower.  (Early exit runs
     # the statistics pass once per wave: its roofline is taken over the step.)
     for i in range(args.steps):
-        if not ee:
+        if not ee and not chain:
             sv.profile_events(*kev[i])
         ev_k[i][0].record(stream)
         step(args.warmup + args.steps + i)
@@ -643,6 +656,8 @@ def run_ours(args, world, rank, local):
     read_bytes = alg_bytes
     if ee:  # logit bytes the two waves actually read, from each request's outcome
         read_bytes = early_exit_bytes(inp["temperature"], vlen, accept_len, K, V, esz, ee)
+        kern_avg_s = total_s / args.steps
+    if chain:  # two statistics passes (draft rows, then target rows): the step's rate
         kern_avg_s = total_s / args.steps
 
     # outcome of the timed steps (each step verifies the same batch)
@@ -665,10 +680,21 @@ def run_ours(args, world, rank, local):
     def e2e_step():
         for k, v in host.items():
             dbuf[k].copy_(v, non_blocking=True)
-        vl = sv.schedule_len(dbuf["draft_maxprob"], inp["threshold"], out=vlen) if scheduled \
-            else dbuf.get("verify_len")
-        o, a = verifier(dbuf["target"], dbuf["draft"], dbuf["tokens"], vl, dbuf["temperature"],
-                        inp["seed"], out_tokens=out_tokens, accept_len=accept_len)
+        if chain:
+            o, a, _, _ = sv.verify_scheduled(
+                dbuf["target"], dbuf["draft"], dbuf["tokens"], dbuf["temperature"], inp["seed"],
+                budget=chain * B, maxprob_out=conf, verify_len_out=vlen, out_tokens=out_tokens,
+                accept_len=accept_len, verifier=verifier)
+        elif scheduled:
+            o, a, _, _ = sv.verify_scheduled(
+                dbuf["target"], dbuf["draft"], dbuf["tokens"], dbuf["temperature"], inp["seed"],
+                threshold=inp["threshold"], draft_maxprob=dbuf["draft_maxprob"],
+                verify_len_out=vlen, out_tokens=out_tokens, accept_len=accept_len,
+                verifier=verifier)
+        else:
+            o, a = verifier(dbuf["target"], dbuf["draft"], dbuf["tokens"], dbuf.get("verify_len"),
+                            dbuf["temperature"], inp["seed"], out_tokens=out_tokens,
+                            accept_len=accept_len)
         h_out.copy_(o, non_blocking=True)
         h_acc.copy_(a, non_blocking=True)
 
@@ -695,7 +721,15 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_peak()
     achieved = read_bytes / kern_avg_s / 1e9
     traffic, _ = recorded_traffic("c%d" % cfg) if not ee else (None, None)
-    launches = (sv.kernels_per_verify() + (4 if chain else (1 if scheduled else 0))) * args.steps  # timed region 1
+    if chain:
+        per_step = sv.kernels_per_scheduled(True, True)
+    elif fused:
+        per_step = sv.kernels_per_scheduled(False, False)
+    elif ee:
+        per_step = (8 if ee < K else 5) + (1 if scheduled else 0)
+    else:
+        per_step = sv.kernels_per_verify()
+    launches = per_step * args.steps  # timed region 1
 
     result = {
         "metric": "verified draft positions/s",
@@ -727,12 +761,15 @@ def run_ours(args, world, rank, local):
             "parallelism": "replicas" if world > 1 else "single GPU",
             "mode": (("early exit, first wave %d positions (%d logit bytes read per step)"
                       % (ee, read_bytes)) if ee else "single pass") + (
-                     ("; confidences from the draft logits (%d more bytes read), budget of %d "
-                      "positions per request" % (B * K * V * esz, chain)) if chain else ""),
+                     ("; one call: confidences from the draft rows (read once, their "
+                      "statistics reused by the step), a budget of %d positions per request, "
+                      "verification" % chain) if chain else
+                     ("; one call: threshold schedule formed in the step's first kernel"
+                      if fused else "")),
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "whole step (logit bytes read)" if ee else "sv_pass1",
+            "kernel": "whole step (logit bytes read)" if (ee or chain) else "sv_pass1",
             "achieved": achieved,
             "peak": peak,
             "peak_source": peak_kind,

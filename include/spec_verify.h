@@ -282,6 +282,48 @@ spec_status_t spec_schedule_len(const float *draft_maxprob, float threshold, int
                                 int32_t *verify_len, void *stream);
 
 /*
+ * spec_verify_scheduled -- confidence-scheduled verification in one call: the
+ * draft's confidences, the verify lengths they give, and the verification
+ * step, with every draft row read once.  "DSpark: ... верификацией по
+ * уверенности" (iitog.ru), "Ключевые факты": the verify length of each request
+ * follows the estimated survival of its draft prefix and the engine's load;
+ * "Спекулятивный декодинг в проде" (kiosknews.app), "6. DSpark", "Грабли":
+ * the scheduler cuts the draft where the drafter is unsure, and doing that
+ * trimming on the GPU was the missing piece.
+ *   draft_maxprob [B, K] float32 device, or NULL.  NULL: the confidences are
+ *       computed from the draft rows, max_v q_k(v) as spec_draft_confidence
+ *       gives them (1 for greedy requests), by one statistics pass over the
+ *       sampled requests' draft rows whose per-row partials the step then reuses
+ *       (its own statistics pass reads target rows only).  Given: they are
+ *       used as they are and the step reads the draft rows it needs itself.
+ *   mode SPEC_SCHED_THRESHOLD: verify_len[b] is the spec_schedule_len rule at
+ *       `threshold` (formed per request inside the step's first kernel);
+ *       SPEC_SCHED_BUDGET: the spec_schedule_budget rule with `budget`
+ *       positions (B * K <= 2^22, else SPEC_ERR_UNSUPPORTED).
+ *   maxprob_out [B, K] float32 device, nullable: receives the computed
+ *       confidences (written only when draft_maxprob is NULL).
+ *   verify_len_out [B] int32 device, nullable: receives the scheduled lengths
+ *       (before the draft-token check of spec_verify, which may cut them).
+ *   Everything else as spec_verify (the same workspace size).  The outputs
+ *   are bit-identical to spec_draft_confidence (when draft_maxprob is NULL),
+ *   then spec_schedule_len / spec_schedule_budget, then spec_verify on the
+ *   same inputs.  Launches 5 kernels (threshold, confidences given), plus 3
+ *   for the confidences and 1 for a budget.
+ */
+typedef enum {
+    SPEC_SCHED_THRESHOLD = 0, /* survival product >= threshold */
+    SPEC_SCHED_BUDGET = 1     /* the `budget` positions of highest survival */
+} spec_sched_mode_t;
+spec_status_t spec_verify_scheduled(const void *target_logits, const void *draft_logits,
+                                    spec_dtype_t dtype, const int32_t *draft_tokens,
+                                    const float *temperature, uint64_t seed, int B, int K, int V,
+                                    const float *draft_maxprob, spec_sched_mode_t mode,
+                                    float threshold, long long budget, float *maxprob_out,
+                                    int32_t *verify_len_out, int32_t *out_tokens,
+                                    int32_t *accept_len, void *workspace, size_t workspace_bytes,
+                                    uint32_t *dev_status, void *stream);
+
+/*
  * spec_profile_events -- measurement hook.  When both events are non-NULL
  * (cudaEvent_t values passed as void*), every later spec_verify /
  * spec_verify_debug call records ev_start immediately before and ev_end

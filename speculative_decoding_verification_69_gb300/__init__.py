@@ -71,6 +71,11 @@ def load_library():
     L.spec_verify_tree.restype = ctypes.c_int
     L.spec_schedule_budget.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_longlong, i32p, vp]
     L.spec_schedule_budget.restype = ctypes.c_int
+    L.spec_verify_scheduled.argtypes = [vp, vp, ctypes.c_int, i32p, f32p, ctypes.c_uint64,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, f32p, ctypes.c_int,
+                                        ctypes.c_float, ctypes.c_longlong, f32p, i32p, i32p, i32p,
+                                        vp, ctypes.c_size_t, u32p, vp]
+    L.spec_verify_scheduled.restype = ctypes.c_int
     L.spec_verify_noalloc.argtypes = common[:12] + [u32p, vp]
     L.spec_verify_noalloc.restype = ctypes.c_int
     L.spec_profile_events.argtypes = [vp, vp]
@@ -89,7 +94,7 @@ def exported_symbols():
     return ["spec_verify_workspace_bytes", "spec_verify", "spec_verify_debug",
             "spec_verify_early_exit", "spec_tree_workspace_bytes", "spec_verify_tree_greedy",
             "spec_verify_tree",
-            "spec_draft_confidence", "spec_schedule_budget",
+            "spec_draft_confidence", "spec_schedule_budget", "spec_verify_scheduled",
             "spec_schedule_len", "spec_verify_noalloc",
             "spec_profile_events", "spec_debug_force_wait_timeout",
             "spec_verify_kernel_count", "spec_status_str"]
@@ -315,6 +320,53 @@ def schedule_budget(draft_maxprob, budget, *, out=None, stream=None):
         out = torch.empty((B,), dtype=torch.int32, device=draft_maxprob.device)
     _check(L.spec_schedule_budget(_ptr(draft_maxprob), B, K, int(budget), _ptr(out), _stream(stream)))
     return out
+
+
+SCHED_THRESHOLD, SCHED_BUDGET = 0, 1
+
+
+def verify_scheduled(target, draft, tokens, temperature, seed, *, threshold=None, budget=None,
+                     draft_maxprob=None, maxprob_out=None, verify_len_out=None, out_tokens=None,
+                     accept_len=None, dev_status=None, verifier=None, stream=None):
+    """Confidence-scheduled verification in one call (spec_verify_scheduled):
+    exactly one of threshold (survival product >= threshold) or budget (the
+    `budget` positions of highest survival).  With draft_maxprob None the
+    confidences are computed from the draft rows, whose statistics the step
+    then reuses.  Returns (out_tokens [B, K+1], accept_len [B], verify_len [B],
+    maxprob [B, K] or None) on the device."""
+    L = load_library()
+    if (threshold is None) == (budget is None):
+        raise ValueError("give exactly one of threshold or budget")
+    B, K, V = _prepare(target, draft, tokens, None, temperature)
+    dev = target.device
+    if draft_maxprob is not None and (draft_maxprob.shape != (B, K) or draft_maxprob.dtype != torch.float32
+                                      or not draft_maxprob.is_cuda or not draft_maxprob.is_contiguous()):
+        raise ValueError("draft_maxprob must be a contiguous float32 CUDA tensor [B, K]")
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if accept_len is None:
+        accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    if verify_len_out is None:
+        verify_len_out = torch.empty((B,), dtype=torch.int32, device=dev)
+    if draft_maxprob is None and maxprob_out is None:
+        maxprob_out = torch.empty((B, K), dtype=torch.float32, device=dev)
+    v = verifier or _default_verifier()
+    ws, n = v.workspace(B, K, V, target.dtype, dev)
+    mode = SCHED_THRESHOLD if threshold is not None else SCHED_BUDGET
+    _check(L.spec_verify_scheduled(_ptr(target), _ptr(draft), _dtype_code(target), _ptr(tokens),
+                                   _ptr(temperature), int(seed) & 0xFFFFFFFFFFFFFFFF, B, K, V,
+                                   _ptr(draft_maxprob), mode,
+                                   float(threshold) if threshold is not None else 0.0,
+                                   int(budget) if budget is not None else 0,
+                                   _ptr(maxprob_out) if draft_maxprob is None else None,
+                                   _ptr(verify_len_out), _ptr(out_tokens), _ptr(accept_len),
+                                   _ptr(ws), ws.numel(), _ptr(dev_status), _stream(stream)))
+    return out_tokens, accept_len, verify_len_out, (maxprob_out if draft_maxprob is None else None)
+
+
+def kernels_per_scheduled(confidence: bool, budget: bool) -> int:
+    """Kernels one spec_verify_scheduled call launches."""
+    return kernels_per_verify() + (3 if confidence else 0) + (1 if budget else 0)
 
 
 _default = None

@@ -94,6 +94,13 @@ struct Params {
     float4 *sexact;    // [B, nchunk]: exact sums of e (hi, lo) and e' (hi, lo)
     SampInfo *samp_list; // [B] one record per sampled request (order of decision)
     int *samp_count;     // number of records in samp_list
+    // confidence-scheduled verification (spec_verify_scheduled)
+    const float *sched_mp;  // [B, K] draft max-probabilities: sv_prep takes L from the
+                            // threshold schedule of these (verify_len unused), or null
+    float sched_thr;        // the schedule's threshold
+    int32_t *vlen_out;      // [B] the scheduled lengths, written by sv_prep (nullable)
+    int draft_ready;        // the draft rows' partials are already in `part` (a confidence
+                            // pass over the same rows at the same T): list target rows only
 };
 
 __device__ __forceinline__ const char *row_ptr(const Params &P, int b, int slot, int esz) {
@@ -182,7 +189,19 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
             n = P.ee_done[b] ? 0 : wave_rows(L, greedy != 0, P.k0, P.k1, nt);
         } else if (b < P.B) {
             uint32_t st = 0;
-            L = P.verify_len ? P.verify_len[b] : P.K;
+            if (P.sched_mp) {  // threshold schedule: fp32 running product, left to right
+                const float *mp = P.sched_mp + (size_t)b * P.K;
+                float prod = 1.0f;
+                L = 0;
+                for (int k = 0; k < P.K; ++k) {
+                    prod = __fmul_rn(prod, mp[k]);
+                    if (prod >= P.sched_thr) L = k + 1;
+                    else break;
+                }
+                if (P.vlen_out) P.vlen_out[b] = L;
+            } else {
+                L = P.verify_len ? P.verify_len[b] : P.K;
+            }
             const float T = P.temperature[b];
             if (L < 0) { L = 0; st |= SPEC_DEV_BAD_LEN; }
             if (L > P.K) { L = P.K; st |= SPEC_DEV_BAD_LEN; }
@@ -210,6 +229,7 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
             if (st && P.dev_status) atomicOr(P.dev_status, st);
             if (P.ee_done) P.ee_done[b] = 0;
             n = wave_rows(L, greedy != 0, P.k0, P.k1, nt);
+            if (P.draft_ready) n = nt;  // draft partials exist: target rows only
         }
         // block exclusive scan of n
         int incl = n;
@@ -2107,7 +2127,7 @@ __global__ void __launch_bounds__(kBudgetThreads) sv_schedule_budget(const float
 // ------------------------------------------------------------------ host side
 
 struct Layout {
-    size_t req, row_count, rows, part, sub, sexact, samp_list, samp_count, ee_done, total;
+    size_t req, row_count, rows, part, sub, sexact, samp_list, samp_count, ee_done, mp, vlen, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -2148,6 +2168,8 @@ static Layout layout(int B, int K, int V, spec_dtype_t dt) {
     L.samp_list = off; off = align256(off + sizeof(SampInfo) * (size_t)B);
     L.samp_count = off; off = align256(off + sizeof(int));
     L.ee_done = off; off = align256(off + sizeof(int) * (size_t)B);
+    L.mp = off; off = align256(off + sizeof(float) * (size_t)B * (size_t)K);
+    L.vlen = off; off = align256(off + sizeof(int) * (size_t)B);
     L.total = off;
     return L;
 }
@@ -2273,15 +2295,15 @@ static void launch_waves(const Params &P0, const DevInfo &d, cudaStream_t s, int
                      P);
 }
 
-static spec_status_t verify_impl(const void *target_logits, const void *draft_logits,
+// Host-side checks of the step's arguments and the Params they give (the
+// workspace cut into its regions).  Nothing is launched.
+static spec_status_t step_params(Params &P, const void *target_logits, const void *draft_logits,
                                  spec_dtype_t dtype, const int32_t *draft_tokens,
                                  const int32_t *verify_len, const float *temperature,
                                  uint64_t seed, int B, int K, int V, int32_t *out_tokens,
                                  int32_t *accept_len, void *workspace, size_t workspace_bytes,
-                                 uint32_t *dev_status, double *row_stats, double *probs,
-                                 void *stream, int first_wave = 0) {
+                                 uint32_t *dev_status, Layout &L) {
     if (!sizes_ok(B, K, V)) return SPEC_ERR_INVALID_ARG;
-    if (first_wave < 0) return SPEC_ERR_INVALID_ARG;
     if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
     if (!items_fit(B, K, V, dtype)) return SPEC_ERR_UNSUPPORTED;
     if (!target_logits || !draft_logits || !draft_tokens || !temperature || !out_tokens ||
@@ -2289,14 +2311,10 @@ static spec_status_t verify_impl(const void *target_logits, const void *draft_lo
         return SPEC_ERR_INVALID_ARG;
     if (((uintptr_t)target_logits & 15u) || ((uintptr_t)draft_logits & 15u))
         return SPEC_ERR_INVALID_ARG;
-    const Layout L = layout(B, K, V, dtype);
+    L = layout(B, K, V, dtype);
     if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u))
         return SPEC_ERR_WORKSPACE;
-    DevInfo *d = dev_info();
-    if (!d) return SPEC_ERR_CUDA;
-    const int esz = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
-    const bool vec = ((size_t)V * (size_t)esz) % 16u == 0;
-    Params P{};
+    P = Params{};
     P.tgt = static_cast<const char *>(target_logits);
     P.drf = static_cast<const char *>(draft_logits);
     P.tokens = draft_tokens;
@@ -2312,8 +2330,6 @@ static spec_status_t verify_impl(const void *target_logits, const void *draft_lo
     P.out_tokens = out_tokens;
     P.accept_len = accept_len;
     P.dev_status = dev_status;
-    P.dbg_rows = row_stats;
-    P.dbg_probs = probs;
     char *ws = static_cast<char *>(workspace);
     P.req = reinterpret_cast<ReqInfo *>(ws + L.req);
     P.row_count = reinterpret_cast<int *>(ws + L.row_count);
@@ -2326,9 +2342,47 @@ static spec_status_t verify_impl(const void *target_logits, const void *draft_lo
     P.k0 = 0;
     P.k1 = K;
     P.ee_done = nullptr;
+    return SPEC_OK;
+}
+
+static bool vec_rows(int V, spec_dtype_t dtype) {
+    return ((size_t)V * (size_t)(dtype == SPEC_DTYPE_BF16 ? 2 : 4)) % 16u == 0;
+}
+
+// The five kernels of one step, for the logits' dtype and row alignment.
+static void launch_step(const Params &P, const DevInfo &d, cudaStream_t s, spec_dtype_t dtype,
+                        bool vec) {
+    if (dtype == SPEC_DTYPE_BF16) {
+        if (vec) launch_all<kBF16, true>(P, d, s);
+        else launch_all<kBF16, false>(P, d, s);
+    } else {
+        if (vec) launch_all<kF32, true>(P, d, s);
+        else launch_all<kF32, false>(P, d, s);
+    }
+}
+
+static spec_status_t verify_impl(const void *target_logits, const void *draft_logits,
+                                 spec_dtype_t dtype, const int32_t *draft_tokens,
+                                 const int32_t *verify_len, const float *temperature,
+                                 uint64_t seed, int B, int K, int V, int32_t *out_tokens,
+                                 int32_t *accept_len, void *workspace, size_t workspace_bytes,
+                                 uint32_t *dev_status, double *row_stats, double *probs,
+                                 void *stream, int first_wave = 0) {
+    if (first_wave < 0) return SPEC_ERR_INVALID_ARG;
+    Params P;
+    Layout L;
+    const spec_status_t st = step_params(P, target_logits, draft_logits, dtype, draft_tokens,
+                                         verify_len, temperature, seed, B, K, V, out_tokens,
+                                         accept_len, workspace, workspace_bytes, dev_status, L);
+    if (st != SPEC_OK) return st;
+    DevInfo *d = dev_info();
+    if (!d) return SPEC_ERR_CUDA;
+    const bool vec = vec_rows(V, dtype);
+    P.dbg_rows = row_stats;
+    P.dbg_probs = probs;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (first_wave > 0) {
-        P.ee_done = reinterpret_cast<int *>(ws + L.ee_done);
+        P.ee_done = reinterpret_cast<int *>(static_cast<char *>(workspace) + L.ee_done);
         P.dbg_rows = nullptr;
         P.dbg_probs = nullptr;
         if (dtype == SPEC_DTYPE_BF16) {
@@ -2338,14 +2392,37 @@ static spec_status_t verify_impl(const void *target_logits, const void *draft_lo
             if (vec) launch_waves<kF32, true>(P, *d, s, first_wave);
             else launch_waves<kF32, false>(P, *d, s, first_wave);
         }
-    } else if (dtype == SPEC_DTYPE_BF16) {
-        if (vec) launch_all<kBF16, true>(P, *d, s);
-        else launch_all<kBF16, false>(P, *d, s);
     } else {
-        if (vec) launch_all<kF32, true>(P, *d, s);
-        else launch_all<kF32, false>(P, *d, s);
+        launch_step(P, *d, s, dtype, vec);
     }
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+// Confidence pass of the draft rows: every draft row of every sampled request
+// through the statistics pass (its partials stay in the workspace, in the
+// slots the step's decision kernel reads), then max_v q per row.
+static void launch_confidence(const Params &P, const DevInfo &d, cudaStream_t s,
+                              spec_dtype_t dtype, bool vec, float *maxprob) {
+    sv_conf_rows<<<1, kPrepThreads, 0, s>>>(P);
+    const int g1 = d.sms * d.occ_p1[dtype == SPEC_DTYPE_BF16 ? kBF16 : kF32][vec ? 1 : 0];
+    if (dtype == SPEC_DTYPE_BF16) {
+        if (vec) launch_dependent(sv_pass1<kBF16, true>, g1, kP1Warps * 32, kP1Smem, s, P);
+        else launch_dependent(sv_pass1<kBF16, false>, g1, kP1Warps * 32, 0, s, P);
+    } else {
+        if (vec) launch_dependent(sv_pass1<kF32, true>, g1, kP1Warps * 32, kP1Smem, s, P);
+        else launch_dependent(sv_pass1<kF32, false>, g1, kP1Warps * 32, 0, s, P);
+    }
+    const long long rows = (long long)P.B * P.K;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((rows + kWarps - 1) / kWarps));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, sv_conf_out, P, maxprob);
 }
 
 } // namespace sv
@@ -2407,8 +2484,6 @@ spec_status_t spec_draft_confidence(const void *draft_logits, spec_dtype_t dtype
         return SPEC_ERR_WORKSPACE;
     sv::DevInfo *d = sv::dev_info();
     if (!d) return SPEC_ERR_CUDA;
-    const int esz = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
-    const bool vec = ((size_t)V * (size_t)esz) % 16u == 0;
     sv::Params P{};
     P.tgt = static_cast<const char *>(draft_logits);  // only draft rows are listed
     P.drf = static_cast<const char *>(draft_logits);
@@ -2425,27 +2500,49 @@ spec_status_t spec_draft_confidence(const void *draft_logits, spec_dtype_t dtype
     P.row_count = reinterpret_cast<int *>(ws + L.row_count);
     P.rows = reinterpret_cast<int4 *>(ws + L.rows);
     P.part = reinterpret_cast<float4 *>(ws + L.part);
+    sv::launch_confidence(P, *d, static_cast<cudaStream_t>(stream), dtype, sv::vec_rows(V, dtype),
+                          maxprob);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status_t spec_verify_scheduled(const void *target_logits, const void *draft_logits,
+                                    spec_dtype_t dtype, const int32_t *draft_tokens,
+                                    const float *temperature, uint64_t seed, int B, int K, int V,
+                                    const float *draft_maxprob, spec_sched_mode_t mode,
+                                    float threshold, long long budget, float *maxprob_out,
+                                    int32_t *verify_len_out, int32_t *out_tokens,
+                                    int32_t *accept_len, void *workspace, size_t workspace_bytes,
+                                    uint32_t *dev_status, void *stream) {
+    if (mode != SPEC_SCHED_THRESHOLD && mode != SPEC_SCHED_BUDGET) return SPEC_ERR_INVALID_ARG;
+    sv::Params P;
+    sv::Layout L;
+    const spec_status_t st = sv::step_params(P, target_logits, draft_logits, dtype, draft_tokens,
+                                             nullptr, temperature, seed, B, K, V, out_tokens,
+                                             accept_len, workspace, workspace_bytes, dev_status, L);
+    if (st != SPEC_OK) return st;
+    if (mode == SPEC_SCHED_BUDGET && (long long)B * K > sv::kBudgetMaxN) return SPEC_ERR_UNSUPPORTED;
+    sv::DevInfo *d = sv::dev_info();
+    if (!d) return SPEC_ERR_CUDA;
+    const bool vec = sv::vec_rows(V, dtype);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    sv::sv_conf_rows<<<1, sv::kPrepThreads, 0, s>>>(P);
-    const int g1 = d->sms * d->occ_p1[dtype == SPEC_DTYPE_BF16 ? sv::kBF16 : sv::kF32][vec ? 1 : 0];
-    if (dtype == SPEC_DTYPE_BF16) {
-        if (vec) sv::launch_dependent(sv::sv_pass1<sv::kBF16, true>, g1, sv::kP1Warps * 32, sv::kP1Smem, s, P);
-        else sv::launch_dependent(sv::sv_pass1<sv::kBF16, false>, g1, sv::kP1Warps * 32, 0, s, P);
-    } else {
-        if (vec) sv::launch_dependent(sv::sv_pass1<sv::kF32, true>, g1, sv::kP1Warps * 32, sv::kP1Smem, s, P);
-        else sv::launch_dependent(sv::sv_pass1<sv::kF32, false>, g1, sv::kP1Warps * 32, 0, s, P);
+    char *ws = static_cast<char *>(workspace);
+    const float *mp = draft_maxprob;
+    if (!mp) {  // confidences from the draft rows; their statistics serve the step too
+        float *out = maxprob_out ? maxprob_out : reinterpret_cast<float *>(ws + L.mp);
+        sv::launch_confidence(P, *d, s, dtype, vec, out);
+        mp = out;
+        P.draft_ready = 1;
     }
-    const long long rows = (long long)B * K;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((rows + sv::kWarps - 1) / sv::kWarps));
-    cfg.blockDim = dim3(sv::kThreads);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaLaunchKernelEx(&cfg, sv::sv_conf_out, P, maxprob);
+    if (mode == SPEC_SCHED_THRESHOLD) {  // sv_prep takes each length from the product itself
+        P.sched_mp = mp;
+        P.sched_thr = threshold;
+        P.vlen_out = verify_len_out;
+    } else {
+        int32_t *vl = verify_len_out ? verify_len_out : reinterpret_cast<int32_t *>(ws + L.vlen);
+        sv::sv_schedule_budget<<<1, sv::kBudgetThreads, 0, s>>>(mp, B, K, budget, vl);
+        P.verify_len = vl;
+    }
+    sv::launch_step(P, *d, s, dtype, vec);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

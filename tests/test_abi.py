@@ -122,3 +122,33 @@ def test_tree_host_validation_without_gpu(lib):
     assert greedy(fake, 1, fake, fake, 2, 0, 100, fake, fake, fake, ws, 1 << 30, None, None) == 1
     assert greedy(None, 1, fake, fake, 2, 5, 100, fake, fake, fake, ws, 1 << 30, None, None) == 1
     assert greedy(fake, 1, fake, fake, 2, 5, 100, fake, fake, fake, None, 1 << 30, None, None) == 4
+
+
+def test_scheduled_host_validation_without_gpu(lib):
+    """spec_verify_scheduled rejects an unknown schedule mode, the step's bad
+    sizes, null pointers and workspaces, and a budget over too many positions,
+    on the host before any CUDA call."""
+    fake = ctypes.c_void_p(0x10000)
+    base = dict(t=fake, d=fake, dt=1, tok=fake, T=fake, seed=1, B=2, K=4, V=100, mp=None, mode=0,
+                thr=0.3, budget=4, mpo=None, vlo=None, o=fake, a=fake, ws=fake, wsb=1 << 40,
+                st=None)
+
+    def call(**kw):
+        x = dict(base, **kw)
+        return lib.spec_verify_scheduled(x["t"], x["d"], x["dt"], x["tok"], x["T"], x["seed"],
+                                         x["B"], x["K"], x["V"], x["mp"], x["mode"], x["thr"],
+                                         x["budget"], x["mpo"], x["vlo"], x["o"], x["a"], x["ws"],
+                                         x["wsb"], x["st"], None)
+
+    assert call(mode=2) == 1 and call(mode=-1) == 1
+    assert call(B=0) == 1 and call(K=33) == 1 and call(V=1) == 1
+    assert call(dt=3) == 2
+    assert call(t=None) == 1 and call(d=None) == 1 and call(tok=None) == 1 and call(T=None) == 1
+    assert call(o=None) == 1 and call(a=None) == 1
+    assert call(d=ctypes.c_void_p(0x10004)) == 1              # draft logits not 16-byte aligned
+    assert call(ws=None) == 4 and call(wsb=64) == 4
+    assert call(mode=1, B=1 << 20, K=8) == 2                  # budget over more than 2^22 positions
+    # the workspace covers the schedule's own buffers: it grows with B * K
+    n1 = lib.spec_verify_workspace_bytes(8, 4, 100, 1)
+    n2 = lib.spec_verify_workspace_bytes(8, 8, 100, 1)
+    assert n2 > n1

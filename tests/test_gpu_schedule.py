@@ -91,3 +91,71 @@ def test_confidence_budget_verify_chain(sv):
                          inp["seed"])
     torch.cuda.synchronize()
     assert (acc.cpu() <= vl.cpu()).all()
+
+
+def _unfused(sv, inp, threshold=None, budget=None, given=None):
+    """The chain as separate calls: confidences (unless given), the schedule,
+    then spec_verify."""
+    conf = given if given is not None else sv.draft_confidence(inp["draft"], inp["temperature"])
+    if threshold is not None:
+        vl = sv.schedule_len(conf, threshold)
+    else:
+        vl = sv.schedule_budget(conf, budget)
+    out, acc = sv.verify(inp["target"], inp["draft"], inp["tokens"], vl, inp["temperature"],
+                         inp["seed"])
+    torch.cuda.synchronize()
+    return out.clone(), acc.clone(), vl.clone(), conf.clone()
+
+
+@pytest.mark.parametrize("cfg,B", [(3, 256), (4, 128), (2, 64), (0, 1)])
+@pytest.mark.parametrize("sched", ["threshold", "budget"])
+@pytest.mark.parametrize("computed", [True, False])
+def test_verify_scheduled_equals_separate_calls(sv, cfg, B, sched, computed):
+    """spec_verify_scheduled (one call; with computed confidences the draft rows
+    are read once and their statistics reused by the step) gives bit-identical
+    tokens, accept lengths, verify lengths and confidences to the separate
+    calls on the same inputs."""
+    inp = workloads.make_inputs(cfg, rep=5, B=B)
+    K = inp["tokens"].shape[1]
+    if "draft_maxprob" not in inp:
+        inp["draft_maxprob"] = sv.draft_confidence(inp["draft"], inp["temperature"])
+    kw = dict(threshold=0.3) if sched == "threshold" else dict(budget=max(1, (K * B) // 3))
+    given = None if computed else inp["draft_maxprob"]
+    ref_out, ref_acc, ref_vl, ref_conf = _unfused(sv, inp, given=given, **kw)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, acc, vl, conf = sv.verify_scheduled(inp["target"], inp["draft"], inp["tokens"],
+                                             inp["temperature"], inp["seed"], draft_maxprob=given,
+                                             dev_status=st, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(vl, ref_vl)
+    assert torch.equal(acc, ref_acc)
+    assert torch.equal(out, ref_out)
+    if computed:
+        assert torch.equal(conf, ref_conf)
+    else:
+        assert conf is None
+    assert int(st.item()) == 0
+    if cfg == 3 or sched == "budget" and B > 1:
+        assert len(set(vl.cpu().tolist())) > 1  # ragged lengths
+
+
+def test_verify_scheduled_against_oracle(sv):
+    """The fused call's outputs against the oracle, with the oracle's own
+    confidences and threshold schedule: lengths bit-exact, tokens equal
+    except oracle-flagged near ties (c3 shapes, 64 requests)."""
+    from gpu_helpers import compare, host_inputs, oracle_run
+    inp = workloads.make_inputs(3, rep=6, B=64)
+    out, acc, vl, conf = sv.verify_scheduled(inp["target"], inp["draft"], inp["tokens"],
+                                             inp["temperature"], inp["seed"], threshold=0.3)
+    torch.cuda.synchronize()
+    ref_conf = oracle.draft_confidence(workloads.to_numpy_logits(inp["draft"]),
+                                       inp["temperature"].cpu().numpy())
+    assert np.allclose(conf.cpu().numpy(), ref_conf, rtol=1e-5, atol=0.0)
+    ref_vl = oracle.schedule_len(conf.cpu().numpy(), 0.3)
+    assert np.array_equal(vl.cpu().numpy(), ref_vl)
+    h = host_inputs(inp, verify_len=vl)
+    idx = list(range(64))
+    orc = oracle_run(h, idx)
+    gpu = dict(out_tokens=out.cpu().numpy(), accept_len=acc.cpu().numpy())
+    ng, ns, nu, nsamp, nflag = compare(gpu, orc, h, idx)
+    assert ng == 0 and nu == 0 and ns <= 1
