@@ -67,11 +67,11 @@ def lib():
                                              i32p, i32p]
         L.svo_verify_tree_greedy.restype = ctypes.c_int
         L.svo_verify_tree_u.argtypes = [vp, vp, ctypes.c_int, i32p, i32p, ctypes.c_int, ctypes.c_int,
-                                        ctypes.c_float, f64p, f64p, i32p, i32p, f64p, vp]
+                                        ctypes.c_float, ctypes.c_int, f64p, f64p, i32p, i32p, f64p, vp]
         L.svo_verify_tree_u.restype = ctypes.c_int
         L.svo_verify_tree_sampled.argtypes = [vp, vp, ctypes.c_int, i32p, i32p, ctypes.c_int,
                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, f32p,
-                                              ctypes.c_uint64,
+                                              ctypes.c_uint64, ctypes.c_int,
                                               i32p, i32p, i32p, f64p, f64p]
         L.svo_schedule_budget.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_longlong, i32p]
         L.svo_draft_confidence.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -260,12 +260,15 @@ def verify_tree_greedy(target, parent, token):
     return ot, on, a
 
 
-def verify_tree_u(target, draft, parent, token, T, u_acc, u_s):
+def verify_tree_u(target, draft, parent, token, T, u_acc, u_s, distinct=False):
     """Sampled verification of one candidate tree with explicit uniforms:
     target, draft [N, V] (row n: the target / draft distribution after node n),
     parent, token [N], u_acc [N] (entry c: the uniform of candidate node c;
     entry 0 unused) and u_s [N] (entry n: the sampling uniform when node n emits)
-    or scalars.  Returns (out_tokens [N], out_nodes [N], accepted)."""
+    or scalars.  distinct: the siblings were drawn without replacement from
+    their parent's draft row (each child's draft law excludes the tokens of
+    the siblings rejected before it).  Returns (out_tokens [N], out_nodes [N],
+    accepted)."""
     target = np.ascontiguousarray(target)
     N, V = target.shape
     draft = np.ascontiguousarray(draft, dtype=target.dtype)
@@ -279,17 +282,19 @@ def verify_tree_u(target, draft, parent, token, T, u_acc, u_s):
     work = np.empty(3 * V, dtype=np.float64)
     a = lib().svo_verify_tree_u(target.ctypes.data, draft.ctypes.data, dtype_code(target),
                                 _ptr(parent, ctypes.c_int32), _ptr(token, ctypes.c_int32), N, V,
-                                float(T), _ptr(u_acc, ctypes.c_double), _ptr(u_s, ctypes.c_double),
+                                float(T), 1 if distinct else 0, _ptr(u_acc, ctypes.c_double),
+                                _ptr(u_s, ctypes.c_double),
                                 _ptr(ot, ctypes.c_int32), _ptr(on, ctypes.c_int32),
                                 _ptr(work, ctypes.c_double), None)
     return ot, on, a
 
 
-def verify_tree(target, draft, parent, token, temperature, seed, b0=0):
+def verify_tree(target, draft, parent, token, temperature, seed, b0=0, distinct=False):
     """A batch of candidate trees with the oracle's own Philox (greedy rows take
     the greedy walk): target, draft [B, N, V]; parent, token [B, N];
-    temperature [B]; row b is request b0 + b (its Philox index).  Returns
-    dict(out_tokens, out_nodes [B, N], accept_len, accept_margin, cdf_margin [B])."""
+    temperature [B]; row b is request b0 + b (its Philox index); distinct as
+    verify_tree_u.  Returns dict(out_tokens, out_nodes [B, N], accept_len,
+    accept_margin, cdf_margin [B])."""
     target = np.ascontiguousarray(target)
     B, N, V = target.shape
     draft = np.ascontiguousarray(draft)
@@ -306,7 +311,8 @@ def verify_tree(target, draft, parent, token, temperature, seed, b0=0):
     rc = lib().svo_verify_tree_sampled(
         target.ctypes.data, draft.ctypes.data, dtype_code(target), _ptr(parent, ctypes.c_int32),
         _ptr(token, ctypes.c_int32), int(b0), B, N, V, _ptr(temperature, ctypes.c_float),
-        int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(ot, ctypes.c_int32), _ptr(on, ctypes.c_int32),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, 1 if distinct else 0, _ptr(ot, ctypes.c_int32),
+        _ptr(on, ctypes.c_int32),
         _ptr(al, ctypes.c_int32), _ptr(am, ctypes.c_double), _ptr(cm, ctypes.c_double))
     if rc != 0:
         raise RuntimeError("oracle tree verification failed (%d)" % rc)

@@ -449,13 +449,25 @@ int svo_verify_tree_greedy(const void *target, int dtype, const int32_t *parent,
  * residual is max(0, p - q) and a node without candidates samples p.  Each
  * child's proposal drawn independently from q_u keeps the emitted token's law
  * equal to p_u.  Greedy T: the greedy tree walk.  work holds 3 * V doubles.
+ *
+ * distinct != 0: the siblings of a node are distinct tokens, drawn one after
+ * another WITHOUT replacement from q_u (the top-k candidates per position of
+ * the EAGLE and DFlash 2 passages: "Спекулятивное декодирование в vLLM и
+ * SGLang" (alesha.pro), EAGLE-3 tree flags; kiosknews.app, "7. DFlash 2", 16
+ * candidates per position).  Each child's draft law is then q_u without the
+ * tokens of the siblings checked before it, renormalised (reading): after a
+ * rejected sibling with token x, q(x) is set to 0 and q is divided by its
+ * remaining mass 1 - q(x) before the next sibling is checked, and the residual
+ * update uses that q.  A sibling repeating a rejected sibling's token, or one
+ * met when q has no mass left, could not have been drawn: no candidate.
+ *
  * Writes the path (tokens, node indices, -1 after) and returns the number of
  * accepted nodes; diag receives the smallest |u_acc - (r(x)/Z)/q_u(x)| over the
  * evaluated candidates and the inverse CDF's margin. */
 int svo_verify_tree_u(const void *target, const void *draft, int dtype, const int32_t *parent,
-                      const int32_t *token, int N, int V, float T, const double *u_acc,
-                      const double *u_s, int32_t *out_tokens, int32_t *out_nodes, double *work,
-                      svo_diag *diag) {
+                      const int32_t *token, int N, int V, float T, int distinct,
+                      const double *u_acc, const double *u_s, int32_t *out_tokens,
+                      int32_t *out_nodes, double *work, svo_diag *diag) {
     svo_diag d = {INFINITY, INFINITY, 0u};
     if (svo_is_greedy(T)) {
         int a = svo_verify_tree_greedy(target, dtype, parent, token, N, V, out_tokens, out_nodes);
@@ -474,10 +486,17 @@ int svo_verify_tree_u(const void *target, const void *draft, int dtype, const in
         memcpy(r, p, (size_t)V * sizeof(double));
         double Z = 1.0;
         int have_q = 0, next = -1;
+        int q_empty = 0;  /* distinct: q has no mass left */
         for (int c = cur + 1; c < N; ++c) {
             if (parent[c] != cur) continue;
             const int x = token[c];
             if (x < 0 || x >= V) continue;
+            if (distinct) {  /* a token no draw without replacement could give */
+                int dup = 0;
+                for (int i = cur + 1; i < c; ++i)
+                    if (parent[i] == cur && token[i] == x) dup = 1;
+                if (dup || q_empty) continue;
+            }
             if (!have_q) {
                 svo_row_softmax(svo_row(draft, dtype, (size_t)cur, V), dtype, V, Td, q, NULL, NULL);
                 have_q = 1;
@@ -502,6 +521,15 @@ int svo_verify_tree_u(const void *target, const void *draft, int dtype, const in
                 Zn = 1.0;
             }
             Z = Zn;
+            if (distinct) {  /* the next sibling is drawn from q without x */
+                const double rest = 1.0 - q[x];
+                q[x] = 0.0;
+                if (rest > 0.0) {
+                    for (int v = 0; v < V; ++v) q[v] = q[v] / rest;
+                } else {
+                    q_empty = 1;
+                }
+            }
         }
         if (next < 0) {
             out_tokens[depth] = svo_inverse_cdf(r, V, u_s[cur], &d.cdf_margin);
@@ -525,9 +553,9 @@ int svo_verify_tree_u(const void *target, const void *draft, int dtype, const in
  * index). */
 int svo_verify_tree_sampled(const void *target, const void *draft, int dtype,
                             const int32_t *parent, const int32_t *token, int b0, int B, int N,
-                            int V, const float *temperature, uint64_t seed, int32_t *out_tokens,
-                            int32_t *out_nodes, int32_t *accepted, double *accept_margin,
-                            double *cdf_margin) {
+                            int V, const float *temperature, uint64_t seed, int distinct,
+                            int32_t *out_tokens, int32_t *out_nodes, int32_t *accepted,
+                            double *accept_margin, double *cdf_margin) {
     const size_t esz = svo_esize(dtype);
     double *work = (double *)malloc(3 * (size_t)V * sizeof(double));
     double *ua = (double *)malloc((size_t)N * sizeof(double));
@@ -548,7 +576,7 @@ int svo_verify_tree_sampled(const void *target, const void *draft, int dtype,
         svo_diag d;
         accepted[b] = svo_verify_tree_u((const char *)target + off * V * esz,
                                         (const char *)draft + off * V * esz, dtype, parent + off,
-                                        token + off, N, V, temperature[b], ua, us,
+                                        token + off, N, V, temperature[b], distinct, ua, us,
                                         out_tokens + off, out_nodes + off, work, &d);
         accept_margin[b] = d.accept_margin;
         cdf_margin[b] = d.cdf_margin;

@@ -645,21 +645,42 @@ def _tree_from_tables(P, Q, parent, tok, T, K):
     return tgt, drf, pre
 
 
-def _tree_lossless_worst(oracle, P, Q, parent, V, K, T):
+def _assignment_weight(Q, pre, parent, tok, distinct):
+    """Probability of one token assignment of the candidates: each child drawn
+    from its parent's draft distribution, independently, or (distinct) the
+    siblings one after another in index order without replacement (a child's
+    law is the draft law without its earlier siblings' tokens, renormalised)."""
+    N = len(parent)
+    w = 1.0
+    for n in range(1, N):
+        q = Q[pre[parent[n]]]
+        if not distinct:
+            w *= q[tok[n]]
+            continue
+        used = [int(tok[m]) for m in range(1, n) if parent[m] == parent[n]]
+        if int(tok[n]) in used:
+            return 0.0
+        w *= q[tok[n]] / (1.0 - sum(q[u] for u in used))
+    return w
+
+
+def _tree_lossless_worst(oracle, P, Q, parent, V, K, T, distinct=False):
     """Largest error of the tree walk's law against the target law, over every
-    token assignment of the candidates (each child drawn independently from
-    its parent's draft distribution), every continuation filled in by target
-    sampling up to K + 1 tokens."""
+    token assignment of the candidates (each child drawn from its parent's
+    draft distribution, independently or, with distinct, siblings without
+    replacement), every continuation filled in by target sampling up to K + 1
+    tokens."""
     T = float(np.float32(T))
     N = len(parent)
     agg = {}
     for assign in itertools.product(range(V), repeat=N - 1):
         tok = np.array((0,) + assign, np.int32)
         tgt, drf, pre = _tree_from_tables(P, Q, parent, tok, T, K)
-        w = 1.0
-        for n in range(1, N):
-            w *= Q[pre[parent[n]]][tok[n]]
-        law = _tree_law(lambda ua, us: oracle.verify_tree_u(tgt, drf, parent, tok, T, ua, us),
+        w = _assignment_weight(Q, pre, parent, tok, distinct)
+        if w == 0.0:
+            continue
+        law = _tree_law(lambda ua, us: oracle.verify_tree_u(tgt, drf, parent, tok, T, ua, us,
+                                                            distinct=distinct),
                         parent, tok, N, V)
         for e, pr in law.items():
             agg[e] = agg.get(e, 0.0) + w * pr
@@ -790,3 +811,156 @@ def test_tree_batch_offset_keeps_philox_index(oracle):
     part = oracle.verify_tree(tgt[3:6], drf[3:6], parent[3:6], tok[3:6], T[3:6], 99, b0=3)
     for k in ("out_tokens", "out_nodes", "accept_len"):
         assert np.array_equal(full[k][3:6], part[k])
+
+
+# ---------------------------------------------------------------- distinct siblings
+
+DISTINCT_SHAPES = {
+    "three_siblings": ([-1, 0, 0, 0], 4, 1),
+    "two_levels": ([-1, 0, 0, 1, 1, 2], 3, 2),
+    "four_of_four": ([-1, 0, 0, 0, 0], 4, 1),   # the siblings use up the whole vocabulary
+}
+
+
+@pytest.mark.parametrize("shape,T,seed", [("three_siblings", 1.0, 5), ("three_siblings", 0.6, 6),
+                                          ("two_levels", 1.0, 7), ("two_levels", 1.3, 8),
+                                          ("four_of_four", 1.0, 9)])
+def test_tree_distinct_lossless_exact_enumeration(oracle, shape, T, seed):
+    """'Утверждение 1' (kiosknews.app) for top-k style candidates: siblings are
+    distinct tokens drawn one after another without replacement from their
+    parent's draft distribution (the EAGLE top-k and DFlash 2 candidates of
+    alesha.pro and kiosknews.app, '7. DFlash 2').  With each child's draft law
+    taken as q without the rejected siblings' tokens, renormalised, the emitted
+    tokens follow the target law exactly: every ordered distinct assignment of
+    the candidates, weighted by its draw probability, and every uniform
+    integrated."""
+    parent, V, K = DISTINCT_SHAPES[shape]
+    rng = np.random.default_rng(seed)
+    P, Q = _tables(rng, V, K)
+    worst = _tree_lossless_worst(oracle, P, Q, np.array(parent, np.int32), V, K, T, distinct=True)
+    assert worst < 1e-12, worst
+
+
+def test_tree_independent_rule_is_not_lossless_for_distinct_draws(oracle):
+    """The independent-siblings rule applied to siblings drawn without
+    replacement misses the target law: the two rules are not interchangeable,
+    so the enumeration above tests something."""
+    parent, V, K = DISTINCT_SHAPES["three_siblings"]
+    P, Q = _tables(np.random.default_rng(5), V, K)
+    par = np.array(parent, np.int32)
+    T = 1.0
+    agg = {}
+    for assign in itertools.product(range(V), repeat=len(parent) - 1):
+        tok = np.array((0,) + assign, np.int32)
+        tgt, drf, pre = _tree_from_tables(P, Q, par, tok, T, K)
+        w = _assignment_weight(Q, pre, par, tok, True)
+        if w == 0.0:
+            continue
+        law = _tree_law(lambda ua, us: oracle.verify_tree_u(tgt, drf, par, tok, T, ua, us),
+                        par, tok, len(parent), V)
+        for e, pr in law.items():
+            agg[e] = agg.get(e, 0.0) + w * pr
+    first = np.zeros(V)
+    for e, pr in agg.items():
+        first[e[0]] += pr
+    assert np.abs(first - P[()]).max() > 1e-3
+
+
+def test_tree_distinct_hand_case(oracle):
+    """p = (0.2, 0.5, 0.3), q = (0.6, 0.2, 0.2), siblings carrying tokens 0 then
+    2.  The first is accepted iff u < p/q = 1/3.  After its rejection the
+    residual is max(0, p - q) = (0, 0.3, 0.1), normalised (0, 0.75, 0.25), and
+    the second sibling's draft law is q without token 0, renormalised:
+    (0, 0.5, 0.5).  So it is accepted iff u * 0.5 < 0.25, u < 1/2 (under the
+    independent rule, u * 0.2 < 0.25 always holds).  After its rejection the
+    residual is max(0, (0, 0.75, 0.25) - (0, 0.5, 0.5)) = (0, 0.25, 0): token 1
+    for every sampling uniform."""
+    T = 1.0
+    tgt = np.log(np.array([[0.2, 0.5, 0.3]] + [[1.0, 1.0, 1.0]] * 2))
+    drf = np.log(np.array([[0.6, 0.2, 0.2]] + [[1.0, 1.0, 1.0]] * 2))
+    parent, tok = [-1, 0, 0], [0, 0, 2]
+    # first sibling accepted below 1/3
+    ot, on, a = oracle.verify_tree_u(tgt, drf, parent, tok, T, [0, 0.33, 0.9], 0.5, distinct=True)
+    assert a == 1 and on[0] == 1
+    # second sibling: accepted below 1/2, rejected above
+    ot, on, a = oracle.verify_tree_u(tgt, drf, parent, tok, T, [0, 0.34, 0.49], 0.5, distinct=True)
+    assert a == 1 and on[0] == 2 and ot[0] == 2
+    for us in (0.0, 0.5, 0.999):
+        ot, on, a = oracle.verify_tree_u(tgt, drf, parent, tok, T, [0, 0.34, 0.51], us,
+                                         distinct=True)
+        assert a == 0 and ot[0] == 1, us
+    # the independent rule accepts the second sibling at the same uniforms
+    ot, on, a = oracle.verify_tree_u(tgt, drf, parent, tok, T, [0, 0.34, 0.51], 0.5)
+    assert a == 1 and on[0] == 2
+    # a sibling repeating a rejected sibling's token is no candidate
+    tgt4 = np.concatenate([tgt, tgt[1:2]])
+    drf4 = np.concatenate([drf, drf[1:2]])
+    ot, on, a = oracle.verify_tree_u(tgt4, drf4, [-1, 0, 0, 0], [0, 0, 0, 2], T,
+                                     [0, 0.34, 0.0, 0.49], 0.5, distinct=True)
+    assert a == 1 and on[0] == 3
+
+
+def test_tree_distinct_chain_equals_independent(oracle):
+    """With one child per node no sibling is ever rejected before another is
+    checked, so the distinct rule is the independent one (and the linear
+    verification) on chains."""
+    rng = np.random.default_rng(31)
+    for trial in range(20):
+        B, N, V = 3, int(rng.integers(2, 8)), int(rng.integers(3, 30))
+        T = np.array([1.0, 0.7, 0.0], np.float32)
+        tgt = rng.normal(size=(B, N, V)) * 1.5
+        drf = tgt + rng.normal(size=(B, N, V)) * 0.7
+        tok = rng.integers(0, V, size=(B, N)).astype(np.int32)
+        parent = np.tile(np.arange(-1, N - 1, dtype=np.int32), (B, 1))
+        a = oracle.verify_tree(tgt, drf, parent, tok, T, 17 + trial)
+        b = oracle.verify_tree(tgt, drf, parent, tok, T, 17 + trial, distinct=True)
+        for k in ("out_tokens", "out_nodes", "accept_len"):
+            assert np.array_equal(a[k], b[k]), (trial, k)
+
+
+# (Leaving the rejected token's mass in q while renormalising the rest is no
+# mistake: after a rejection r(x) = 0, and x is never checked again, so q(x)
+# takes part in nothing.)
+DISTINCT_MUTANTS = {
+    # the renormalisation inverted: multiplied by the remaining mass
+    "distinct_renormalise_inverted": ("for (int v = 0; v < V; ++v) q[v] = q[v] / rest;",
+                                      "for (int v = 0; v < V; ++v) q[v] = q[v] * rest;"),
+    # q not renormalised after the rejected token is removed
+    "distinct_no_renormalise": ("for (int v = 0; v < V; ++v) q[v] = q[v] / rest;",
+                                "for (int v = 0; v < V; ++v) q[v] = q[v];"),
+    # siblings checked as if drawn independently
+    "distinct_as_independent": ("if (distinct) {  /* the next sibling is drawn from q without x */",
+                                "if (0) {"),
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(DISTINCT_MUTANTS))
+def test_tree_distinct_enumeration_catches_planted_mistakes(oracle, mutant, tmp_path):
+    """A copy of the oracle with one planted mistake in the without-replacement
+    update breaks the distinct enumeration."""
+    import ctypes
+    import subprocess
+    import oracle.build as ob
+    src = open(ob.SRC).read()
+    old, new = DISTINCT_MUTANTS[mutant]
+    assert src.count(old) == 1, mutant
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(old, new))
+    so = str(tmp_path / "libmutant.so")
+    subprocess.check_call(["gcc", *ob.CFLAGS, str(path), "-o", so, "-lm", "-lpthread"])
+    good = oracle.lib()
+    mut = ctypes.CDLL(so)
+    mut.svo_verify_tree_u.argtypes = good.svo_verify_tree_u.argtypes
+    mut.svo_verify_tree_u.restype = good.svo_verify_tree_u.restype
+    oracle._lib = mut
+    try:
+        parent, V, K = DISTINCT_SHAPES["three_siblings"]
+        P, Q = _tables(np.random.default_rng(5), V, K)
+        try:
+            worst = _tree_lossless_worst(oracle, P, Q, np.array(parent, np.int32), V, K, 1.0,
+                                         distinct=True)
+        except AssertionError:
+            worst = 1.0   # the law does not even sum to 1
+    finally:
+        oracle._lib = good
+    assert worst > 1e-4, mutant
