@@ -354,7 +354,8 @@ def run_tree(args, world, rank, local):
         inp = workloads.make_tree_inputs(c["B"], N, c["V"], c["dtype"],
                                          seed=workloads.seed_for(args.config, rank), T=T,
                                          sigma=c["sigma"], noise=noise,
-                                         n_greedy=c.get("n_greedy", 0), device=dev)
+                                         n_greedy=c.get("n_greedy", 0), device=dev,
+                                         distinct=args.distinct)
         tgt, drf = inp["target"], inp["draft"]
         parent, tok, temp, seed = inp["parent"], inp["tokens"], inp["temperature"], inp["seed"]
         B, _, V = tgt.shape
@@ -394,7 +395,7 @@ def run_tree(args, world, rank, local):
         if d is None:
             sv.verify_tree_greedy(t, parent, tok)
         else:
-            sv.verify_tree(t, d, parent, tok, temp, seed, workspace=ws)
+            sv.verify_tree(t, d, parent, tok, temp, seed, workspace=ws, distinct=args.distinct)
 
     stream = torch.cuda.current_stream()
     clocks = ClockSampler(local)
@@ -427,17 +428,19 @@ def run_tree(args, world, rank, local):
         "data": "synthetic (seeded logits and trees; no datasets or trained weights)",
         "config": {"workload": workloads.NAMES[args.config] + (
                        " target rows as %d-node trees" % N if drf is None else
-                       " shapes, %d-node sampled trees (tokens drawn from the parent's draft row)" % N),
+                       " shapes, %d-node sampled trees (tokens drawn from the parent's draft row%s)"
+                       % (N, ", siblings without replacement" if args.distinct else "")),
                    "B": B, "N": N, "V": V,
                    "mode": "greedy tree verification" if drf is None else
-                   "tree verification (sampled requests: multi-candidate residual walk)",
+                   "tree verification (sampled requests: multi-candidate residual walk%s)"
+                   % (", distinct siblings" if args.distinct else ""),
                    "logit_bytes_per_step": alg_bytes,
                    "logits_GBps": alg_bytes / step_s / 1e9,
                    "l2": "inputs larger than L2: %d copies cycled; no flush" % ncopies},
         "roofline": {"bound": "hbm", "kernel": "whole step", "achieved": alg_bytes / step_s / 1e9,
                      "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
                      "frac": alg_bytes / step_s / 1e9 / peak, "traffic": None},
-        "e2e": tree_e2e(args, world, sv, dev, tgt, drf, parent, tok, temp, seed, N),
+        "e2e": tree_e2e(args, world, sv, dev, tgt, drf, parent, tok, temp, seed, N, args.distinct),
         "gpu_launches": 3 * args.steps,
     }
     clocks.mark(t_gpu0, time.perf_counter() + 0.05)
@@ -445,13 +448,13 @@ def run_tree(args, world, rank, local):
                                 label="warm-up, the timed loop and the end-to-end loop")
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         pps, cores, sample, dt = tree_oracle_sample(tgt, drf, parent, tok, temp, seed,
-                                                    args.cpu_seconds)
+                                                    args.cpu_seconds, args.distinct)
         res["cpu_baseline"] = {"value": pps, "unit": "positions/s", "cores": cores,
                                "kind": "oracle", "sample": sample, "seconds": dt}
     return res
 
 
-def tree_e2e(args, world, sv, dev, tgt, drf, parent, tok, temp, seed, N):
+def tree_e2e(args, world, sv, dev, tgt, drf, parent, tok, temp, seed, N, distinct=False):
     """The tree metric through the public API with the step's inputs copied
     from pinned host memory and the outputs read back, every step."""
     B = tgt.shape[0]
@@ -474,7 +477,7 @@ def tree_e2e(args, world, sv, dev, tgt, drf, parent, tok, temp, seed, N):
             o, n, a = sv.verify_tree_greedy(dbuf["t"], dbuf["p"], dbuf["k"])
         else:
             o, n, a = sv.verify_tree(dbuf["t"], dbuf["d"], dbuf["p"], dbuf["k"], dbuf["T"], seed,
-                                     workspace=ws)
+                                     workspace=ws, distinct=distinct)
         h_out.copy_(o, non_blocking=True)
         h_nodes.copy_(n, non_blocking=True)
         h_acc.copy_(a, non_blocking=True)
@@ -501,7 +504,7 @@ def tree_e2e(args, world, sv, dev, tgt, drf, parent, tok, temp, seed, N):
             "steps": steps}
 
 
-def tree_oracle_sample(tgt, drf, parent, tok, temp, seed, max_seconds):
+def tree_oracle_sample(tgt, drf, parent, tok, temp, seed, max_seconds, distinct=False):
     """Time the CPU oracle's tree verification on a bounded sample of the
     workload's requests, one host thread per core (the oracle's C code runs
     outside the interpreter lock), requests split across the threads."""
@@ -521,7 +524,8 @@ def tree_oracle_sample(tgt, drf, parent, tok, temp, seed, max_seconds):
             for b in range(b0, b1):
                 oracle.verify_tree_greedy(t[b], par[b], tk[b])
         else:
-            oracle.verify_tree(t[b0:b1], d[b0:b1], par[b0:b1], tk[b0:b1], T[b0:b1], seed, b0=b0)
+            oracle.verify_tree(t[b0:b1], d[b0:b1], par[b0:b1], tk[b0:b1], T[b0:b1], seed, b0=b0,
+                               distinct=distinct)
 
     cores = oracle.cpu_count()
     t0 = time.perf_counter()
@@ -858,6 +862,9 @@ def main(argv=None):
                     help="greedy verification of N-node candidate trees instead of chains")
     ap.add_argument("--tree-sampled", action="store_true",
                     help="with --tree: sampled trees (draft rows, the workload's temperature)")
+    ap.add_argument("--distinct", action="store_true",
+                    help="with --tree-sampled: siblings drawn without replacement (top-k style), "
+                         "verified by spec_verify_tree_distinct")
     ap.add_argument("--early-exit", type=int, default=0,
                     help="verify positions [0, W) first, then the rest for open requests")
     args = ap.parse_args(argv)

@@ -234,6 +234,30 @@ spec_status_t spec_verify_tree(const void *target_logits, const void *draft_logi
                                uint32_t *dev_status, void *stream);
 
 /*
+ * spec_verify_tree_distinct -- spec_verify_tree for trees whose siblings are
+ * DISTINCT tokens drawn one after another without replacement from their
+ * parent's draft distribution q_u: the several candidates per position of
+ * "Спекулятивное декодирование в vLLM и SGLang: MTP, EAGLE-3 и n-gram в 2026"
+ * (alesha.pro; the EAGLE top-k tree of candidates) and of "Спекулятивный
+ * декодинг в проде" (kiosknews.app), "7. DFlash 2" (16 candidates per
+ * position).  The sibling checked after rejected siblings carrying tokens X
+ * was drawn from q_u without X, renormalised by its remaining mass 1 - q_u(X);
+ * the acceptance test and the residual update use that law (the residual keeps
+ * the closed form of spec_verify_tree, its threshold step divided by the
+ * remaining mass).  A sibling repeating a rejected sibling's token, or checked
+ * when q_u has no mass left, could not have been drawn and is no candidate.
+ * With the siblings drawn that way the emitted tokens follow the target
+ * exactly.  Arguments, outputs, errors and workspace as spec_verify_tree;
+ * chains give spec_verify_tree's (and spec_verify's) outputs.
+ */
+spec_status_t spec_verify_tree_distinct(const void *target_logits, const void *draft_logits,
+                                        spec_dtype_t dtype, const int32_t *parent,
+                                        const int32_t *node_tokens, const float *temperature,
+                                        uint64_t seed, int B, int N, int V, int32_t *out_tokens,
+                                        int32_t *out_nodes, int32_t *accept_len, void *workspace,
+                                        size_t workspace_bytes, uint32_t *dev_status, void *stream);
+
+/*
  * spec_draft_confidence -- the draft's confidence at every position, as the
  * confidence-scheduled verification of "DSpark: ... верификацией по
  * уверенности" (iitog.ru), "Ключевые факты", uses it: maxprob[b, k] =

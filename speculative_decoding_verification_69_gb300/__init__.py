@@ -69,6 +69,8 @@ def load_library():
                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, i32p, i32p, vp,
                                    ctypes.c_size_t, u32p, vp]
     L.spec_verify_tree.restype = ctypes.c_int
+    L.spec_verify_tree_distinct.argtypes = L.spec_verify_tree.argtypes
+    L.spec_verify_tree_distinct.restype = ctypes.c_int
     L.spec_schedule_budget.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_longlong, i32p, vp]
     L.spec_schedule_budget.restype = ctypes.c_int
     L.spec_verify_scheduled.argtypes = [vp, vp, ctypes.c_int, i32p, f32p, ctypes.c_uint64,
@@ -93,7 +95,7 @@ def load_library():
 def exported_symbols():
     return ["spec_verify_workspace_bytes", "spec_verify", "spec_verify_debug",
             "spec_verify_early_exit", "spec_tree_workspace_bytes", "spec_verify_tree_greedy",
-            "spec_verify_tree",
+            "spec_verify_tree", "spec_verify_tree_distinct",
             "spec_draft_confidence", "spec_schedule_budget", "spec_verify_scheduled",
             "spec_schedule_len", "spec_verify_noalloc",
             "spec_profile_events", "spec_debug_force_wait_timeout",
@@ -273,13 +275,15 @@ def verify_tree_greedy(target, parent, node_tokens, *, dev_status=None, stream=N
 
 
 def verify_tree(target, draft, parent, node_tokens, temperature, seed, *, dev_status=None,
-                workspace=None, stream=None):
+                workspace=None, stream=None, distinct=False):
     """Verification of candidate trees at each request's temperature (greedy
     requests take the greedy walk; sampled ones check siblings against
     successively updated residuals): target [B, N, V], draft [B, N-1, V] (row
     n: the draft's logits after node n; None when N = 1), parent / node_tokens
-    int32 [B, N], temperature float32 [B].  Returns (out_tokens [B, N],
-    out_nodes [B, N], accept_len [B]) on the device."""
+    int32 [B, N], temperature float32 [B].  distinct: the siblings are distinct
+    tokens drawn without replacement from their parent's draft row
+    (spec_verify_tree_distinct).  Returns (out_tokens [B, N], out_nodes [B, N],
+    accept_len [B]) on the device."""
     L = load_library()
     if target.dim() != 3 or not target.is_cuda or not target.is_contiguous():
         raise ValueError("target must be a contiguous CUDA tensor [B, N, V]")
@@ -301,7 +305,8 @@ def verify_tree(target, draft, parent, node_tokens, temperature, seed, *, dev_st
     n = int(L.spec_tree_workspace_bytes(B, N, V, _dtype_code(target)))
     if workspace is None or workspace.numel() < n:
         workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
-    _check(L.spec_verify_tree(_ptr(target), _ptr(draft) if N > 1 else None, _dtype_code(target),
+    fn = L.spec_verify_tree_distinct if distinct else L.spec_verify_tree
+    _check(fn(_ptr(target), _ptr(draft) if N > 1 else None, _dtype_code(target),
                               _ptr(parent), _ptr(node_tokens), _ptr(temperature),
                               int(seed) & 0xFFFFFFFFFFFFFFFF, B, N, V, _ptr(out), _ptr(nodes),
                               _ptr(acc), _ptr(workspace), workspace.numel(), _ptr(dev_status),

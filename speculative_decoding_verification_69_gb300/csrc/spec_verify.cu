@@ -1761,6 +1761,14 @@ __device__ int tree_find(const char *rowt, const char *rowd, const char *stt, co
 // a recording pass over the current weights and an inverse CDF give the
 // emitted token.  Candidate node c takes the acceptance uniform of position
 // c - 1, node u's emitted token the sampling uniform of position u.
+// distinct: the siblings were drawn without replacement from q_u, so the
+// draft law of the sibling after j rejections is q without the rejected
+// tokens, divided by their remaining mass 1 - Q_j.  The residual keeps the
+// same closed form with the threshold step divided by that mass, and the test
+// is scaled by it: with R_j = B - sum of b over the rejected tokens (= B (1 -
+// Q_j)), accept iff u_acc * b(x) * S_j < R_j * max(0, a(x) - s_j b(x)), and
+// s_(j+1) = s_j + S_j / R_j (s_j = A / R_(j-1) after a restart from p).  A
+// sibling repeating a rejected token, or met when R_j <= 0, is no candidate.
 // Each CTA of the cluster passes over its slice of the vocabulary; the sums
 // are exchanged through distributed shared memory and added by the same fixed
 // shuffle tree in every CTA, so all CTAs take the same decisions and meet the
@@ -1769,7 +1777,8 @@ template <int DT, bool VEC>
 __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const int32_t *parent,
                                                                const int32_t *token,
                                                                int32_t *out_nodes,
-                                                               int stage_row_bytes, int diag) {
+                                                               int stage_row_bytes, int diag,
+                                                               int distinct) {
     // stage_row_bytes > 0: this CTA's slice of a node's target and draft rows is
     // copied into dynamic shared memory at the node's first rejection, and the
     // node's later passes read it there.  diag: before each staging wait, every
@@ -1793,6 +1802,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
     __shared__ float s_s;
     __shared__ int s_acc, s_R, s_W, s_emit, s_again;
     __shared__ int s_nostage;  // a staging wait ran out: no more staging in this request
+    __shared__ double s_brej;  // distinct: sum of b over the rejected siblings' tokens at the node
+    __shared__ int s_rejtok[SPEC_MAX_TREE], s_nrej;  // distinct: those tokens
     constexpr int ESZ = Fmt<DT>::kESZ;
     const int cs = cluster_size(), rank = cluster_rank();
     const int b = blockIdx.x / cs, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1869,6 +1880,10 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
             }
             if (lane == 0) s_ncand = n;
         }
+        if (tid == 0) {
+            s_brej = 0.0;
+            s_nrej = 0;
+        }
         __syncthreads();
         const int ncand = s_ncand;
         int J = 0, next = -1;
@@ -1876,29 +1891,53 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
             const int ch = s_cand[k];
             if (tid == 0) {
                 const float u = s_u[ch], g = s_g[ch], gd = s_gd[ch];
-                bool acc;
-                if (J == 0) {
+                int acc;  // 1 accepted, 0 rejected, -1 no candidate
+                bool skip = false;
+                if (distinct && J > 0) {  // a draw without replacement could not give it
+                    const int x = s_tok[ch];
+                    for (int i = 0; i < s_nrej; ++i) skip |= s_rejtok[i] == x;
+                    skip |= !(s_SB - s_brej > 0.0);
+                }
+                if (skip) {
+                    acc = -1;
+                } else if (J == 0) {
                     acc = accept_position(u, g, mt, St, gd, md, Sd, chi, clo);
                 } else {
                     const float a = weight1b(g, c, bt), bq = weight1b(gd, c, bd);
                     const float w = nc.s > 0.f ? resid_weight(a, bq, nc.s) : a;
-                    acc = (double)u * (double)bq * s_sum < (double)w * s_SB;
+                    acc = (double)u * (double)bq * s_sum < (double)w * (distinct ? s_SB - s_brej : s_SB);
                 }
                 s_acc = acc;
             }
             __syncthreads();
-            if (s_acc) {
+            const int verdict = s_acc;
+            if (verdict < 0) {
+                __syncthreads();  // s_acc is rewritten for the next candidate
+                continue;
+            }
+            if (verdict) {
                 next = ch;
                 break;
             }
             ++J;
             const bool more = k + 1 < ncand;  // another candidate follows: the residual's mass is needed
             if (J > 1) {  // the threshold after this rejection
-                if (tid == 0) s_s = nc.s > 0.f ? (float)((double)nc.s + s_sum * s_iSB) : (float)(s_SA * s_iSB);
+                if (tid == 0) {
+                    if (!distinct) {
+                        s_s = nc.s > 0.f ? (float)((double)nc.s + s_sum * s_iSB) : (float)(s_SA * s_iSB);
+                    } else {  // the remaining draft mass before this rejection
+                        const double R = s_SB - s_brej;
+                        s_s = nc.s > 0.f ? (float)((double)nc.s + s_sum / R) : (float)(s_SA / R);
+                    }
+                }
                 __syncthreads();
                 nc.s = s_s;
-                if (!more) break;  // the recording pass below needs no mass
             }
+            if (distinct && tid == 0) {  // this sibling's token leaves the draft law
+                s_rejtok[s_nrej++] = s_tok[ch];
+                s_brej += (double)weight1b(s_gd[ch], c, bd);
+            }
+            if (J > 1 && !more) break;  // the recording pass below needs no mass
             if (J == 1 && stage_row_bytes > 0 && !s_nostage) {  // every warp copies its own steps, then waits
                 const TreeSplit sp(V, rank, cs, warp);
                 fence_proxy_async();  // earlier reads of the buffer come first
@@ -2614,12 +2653,13 @@ spec_status_t spec_verify_tree_greedy(const void *target_logits, spec_dtype_t dt
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
-spec_status_t spec_verify_tree(const void *target_logits, const void *draft_logits,
-                               spec_dtype_t dtype, const int32_t *parent,
-                               const int32_t *node_tokens, const float *temperature, uint64_t seed,
-                               int B, int N, int V, int32_t *out_tokens, int32_t *out_nodes,
-                               int32_t *accept_len, void *workspace, size_t workspace_bytes,
-                               uint32_t *dev_status, void *stream) {
+static spec_status_t verify_tree_impl(const void *target_logits, const void *draft_logits,
+                                      spec_dtype_t dtype, const int32_t *parent,
+                                      const int32_t *node_tokens, const float *temperature,
+                                      uint64_t seed, int B, int N, int V, int32_t *out_tokens,
+                                      int32_t *out_nodes, int32_t *accept_len, void *workspace,
+                                      size_t workspace_bytes, uint32_t *dev_status, void *stream,
+                                      int distinct) {
     if (N < 1 || N > SPEC_MAX_TREE || B < 1 || B >= (1 << 24) || V < 2 || V > SPEC_MAX_V)
         return SPEC_ERR_INVALID_ARG;
     const int K = N - 1 > 0 ? N - 1 : 1;  // the workspace layout of K = N - 1
@@ -2659,7 +2699,7 @@ spec_status_t spec_verify_tree(const void *target_logits, const void *draft_logi
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     sv::sv_tree_rows_s<<<1, sv::kPrepThreads, 0, s>>>(P);
     const int g1 = d->sms * d->occ_p1[dtype == SPEC_DTYPE_BF16 ? sv::kBF16 : sv::kF32][vec ? 1 : 0];
-    void (*walk)(sv::Params, const int32_t *, const int32_t *, int32_t *, int, int);
+    void (*walk)(sv::Params, const int32_t *, const int32_t *, int32_t *, int, int, int);
     if (dtype == SPEC_DTYPE_BF16) {
         if (vec) sv::launch_dependent(sv::sv_pass1<sv::kBF16, true>, g1, sv::kP1Warps * 32, sv::kP1Smem, s, P);
         else sv::launch_dependent(sv::sv_pass1<sv::kBF16, false>, g1, sv::kP1Warps * 32, 0, s, P);
@@ -2699,9 +2739,31 @@ spec_status_t spec_verify_tree(const void *target_logits, const void *draft_logi
     }
     cfg.dynamicSmemBytes = stage ? (size_t)(2 * row_bytes) : 0;
     if (cudaLaunchKernelEx(&cfg, walk, P, parent, node_tokens, out_nodes, stage,
-                           sv::g_diag_timeout ? 1 : 0) != cudaSuccess)
+                           sv::g_diag_timeout ? 1 : 0, distinct) != cudaSuccess)
         return SPEC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status_t spec_verify_tree(const void *target_logits, const void *draft_logits,
+                               spec_dtype_t dtype, const int32_t *parent,
+                               const int32_t *node_tokens, const float *temperature, uint64_t seed,
+                               int B, int N, int V, int32_t *out_tokens, int32_t *out_nodes,
+                               int32_t *accept_len, void *workspace, size_t workspace_bytes,
+                               uint32_t *dev_status, void *stream) {
+    return verify_tree_impl(target_logits, draft_logits, dtype, parent, node_tokens, temperature,
+                            seed, B, N, V, out_tokens, out_nodes, accept_len, workspace,
+                            workspace_bytes, dev_status, stream, 0);
+}
+
+spec_status_t spec_verify_tree_distinct(const void *target_logits, const void *draft_logits,
+                                        spec_dtype_t dtype, const int32_t *parent,
+                                        const int32_t *node_tokens, const float *temperature,
+                                        uint64_t seed, int B, int N, int V, int32_t *out_tokens,
+                                        int32_t *out_nodes, int32_t *accept_len, void *workspace,
+                                        size_t workspace_bytes, uint32_t *dev_status, void *stream) {
+    return verify_tree_impl(target_logits, draft_logits, dtype, parent, node_tokens, temperature,
+                            seed, B, N, V, out_tokens, out_nodes, accept_len, workspace,
+                            workspace_bytes, dev_status, stream, 1);
 }
 
 spec_status_t spec_schedule_budget(const float *draft_maxprob, int B, int K, long long budget,

@@ -95,7 +95,7 @@ def test_invalid_parents_flagged(sv):
 TREE_NEAR_TIE = 1e-5
 
 
-def _oracle_tree(inp, b0=0):
+def _oracle_tree(inp, b0=0, distinct=False):
     """Oracle results for the batch (Philox keys use the request index, the
     first row being request b0).  The draft rows are padded to N with zeros:
     the last node has no children, so the oracle never reads that row."""
@@ -104,18 +104,20 @@ def _oracle_tree(inp, b0=0):
     d = workloads.to_numpy_logits(inp["draft"]) if N > 1 else np.zeros((B, 0, V), t.dtype)
     d = np.concatenate([d, np.zeros((B, 1, V), d.dtype)], axis=1)
     return oracle.verify_tree(t, d, inp["parent"].cpu().numpy(), inp["tokens"].cpu().numpy(),
-                              inp["temperature"].cpu().numpy(), inp["seed"], b0=b0)
+                              inp["temperature"].cpu().numpy(), inp["seed"], b0=b0,
+                              distinct=distinct)
 
 
-def _compare_tree(sv, inp, max_flag_frac=0.1):
+def _compare_tree(sv, inp, max_flag_frac=0.1, distinct=False):
     """GPU against the oracle: every request equal unless the oracle flags a
     near tie; returns the GPU outputs and the device status."""
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     out, nodes, acc = sv.verify_tree(inp["target"], inp["draft"], inp["parent"], inp["tokens"],
-                                     inp["temperature"], inp["seed"], dev_status=st)
+                                     inp["temperature"], inp["seed"], dev_status=st,
+                                     distinct=distinct)
     torch.cuda.synchronize()
     out, nodes, acc = out.cpu().numpy(), nodes.cpu().numpy(), acc.cpu().numpy()
-    r = _oracle_tree(inp)
+    r = _oracle_tree(inp, distinct=distinct)
     same = ((acc == r["accept_len"]) & (out == r["out_tokens"]).all(axis=1)
             & (nodes == r["out_nodes"]).all(axis=1))
     flagged = (r["accept_margin"] < TREE_NEAR_TIE) | (r["cdf_margin"] < TREE_NEAR_TIE)
@@ -266,3 +268,97 @@ def test_sampled_trees_at_bench_workloads(sv, cfg, N, b0, n_check):
     # at V >= 128k the CDF window flags many rows (much of the mass sits in
     # tokens of tiny probability), so the gate counts actual mismatches
     assert (~same).sum() <= 1, np.flatnonzero(~same)
+
+
+# ---------------------------------------------------------------- distinct siblings
+
+@pytest.mark.parametrize("B,N,V,dtype,T,sigma", [
+    (48, 4, 64, torch.bfloat16, 1.0, 3.0), (32, 9, 40, torch.float32, 0.7, 3.0),
+    (16, 16, 4096 + 8, torch.bfloat16, 1.3, 2.5), (8, 33, 1001, torch.bfloat16, 1.0, 4.0),
+    (6, 17, 151936, torch.bfloat16, 1.0, 2.5), (12, 64, 2048, torch.bfloat16, 0.7, 3.0),
+    (10, 10, 4100, torch.float32, 1.0, 3.0),
+])
+def test_distinct_trees_against_oracle(sv, B, N, V, dtype, T, sigma):
+    """Siblings drawn without replacement (top-k style candidates), checked
+    with spec_verify_tree_distinct against the oracle's distinct rule; small
+    vocabularies with peaked drafts make the rejected siblings' mass large."""
+    inp = workloads.make_tree_inputs(B, N, V, dtype, seed=B * 7000 + N + V, T=T, sigma=sigma,
+                                     noise=0.7, chain_prob=0.3, n_greedy=B // 8, distinct=True)
+    out, nodes, acc, st = _compare_tree(sv, inp, distinct=True)
+    assert st == 0
+    if N > 3:
+        assert acc.max() >= 2
+
+
+def test_distinct_rule_differs_from_independent(sv):
+    """On distinct draws with peaked drafts the two rules give different walks
+    for some requests (the flag changes the arithmetic), and each matches its
+    own oracle."""
+    inp = workloads.make_tree_inputs(256, 6, 32, torch.float32, seed=404, T=1.0, sigma=3.0,
+                                     noise=0.7, chain_prob=0.0, distinct=True)
+    a = _compare_tree(sv, inp, distinct=True)
+    b = _compare_tree(sv, inp, distinct=False)
+    assert (a[2] != b[2]).any() or (a[0] != b[0]).any()
+
+
+@pytest.mark.parametrize("cfg", [1, 4])
+def test_distinct_chains_equal_independent(sv, cfg):
+    """One child per node: nothing is ever removed from a draft row, so the
+    distinct walk is the independent one, bit for bit."""
+    inp = workloads.make_inputs(cfg, rep=9, B=32)
+    B, K1, V = inp["target"].shape
+    parent = torch.arange(-1, K1 - 1, dtype=torch.int32, device="cuda").expand(B, K1).contiguous()
+    tok = torch.cat([torch.zeros((B, 1), dtype=torch.int32, device="cuda"), inp["tokens"]], 1)
+    r1 = sv.verify_tree(inp["target"], inp["draft"], parent, tok.contiguous(), inp["temperature"],
+                        inp["seed"])
+    r2 = sv.verify_tree(inp["target"], inp["draft"], parent, tok.contiguous(), inp["temperature"],
+                        inp["seed"], distinct=True)
+    torch.cuda.synchronize()
+    for x, y in zip(r1, r2):
+        assert torch.equal(x, y)
+
+
+def test_distinct_duplicates_and_point_mass(sv):
+    """Inputs no draw without replacement gives: repeated sibling tokens (no
+    candidate after the first is rejected) and a point-mass draft (no mass
+    left after its token is rejected); GPU and oracle agree."""
+    inp = workloads.make_tree_inputs(8, 10, 700, torch.bfloat16, seed=78, T=1.0, distinct=True)
+    tok, par = inp["tokens"].clone(), inp["parent"].clone()
+    par[3, 1:] = 0
+    tok[3, 1:] = tok[3, 1]          # nine siblings, one token
+    dr = inp["draft"].clone()
+    dr[4, 0, :] = float("-inf")
+    dr[4, 0, 5] = 0.0               # the root's draft is a point mass on token 5
+    par[4, 1:4] = 0
+    tok[4, 1:4] = torch.tensor([5, 6, 7], dtype=torch.int32)
+    inp.update(tokens=tok.contiguous(), parent=par.contiguous(), draft=dr.contiguous())
+    _compare_tree(sv, inp, max_flag_frac=0.3, distinct=True)
+
+
+def test_distinct_tree_first_token_law(sv):
+    """'Утверждение 1' (kiosknews.app) for top-k style candidates through the
+    GPU path: three sibling tokens drawn without replacement from the root's
+    draft row, 200 000 requests; the first emitted token follows p
+    (chi-square).  The independent-siblings rule on the same draws does not."""
+    scipy_stats = pytest.importorskip("scipy.stats")
+    B, N, V, T = 200000, 4, 12, 1.0
+    g = torch.Generator(device="cuda").manual_seed(99)
+    trow = torch.randn((N, V), generator=g, device="cuda") * 1.5
+    drow = (trow[:N - 1] + torch.randn((N - 1, V), generator=g, device="cuda") * 1.0)
+    tgt = trow.expand(B, N, V).contiguous()
+    drf = drow.expand(B, N - 1, V).contiguous()
+    parent = torch.tensor([-1, 0, 0, 0], dtype=torch.int32, device="cuda").expand(B, N).contiguous()
+    q0 = torch.softmax(drow[0] / T, dim=-1)
+    draws = torch.multinomial(q0.expand(B, V), N - 1, replacement=False, generator=g)
+    tok = torch.cat([torch.zeros((B, 1), dtype=torch.int64, device="cuda"), draws], 1)
+    tok = tok.to(torch.int32).contiguous()
+    temp = torch.full((B,), T, device="cuda")
+    p = oracle.row_softmax(trow[0].cpu().numpy().astype(np.float32), T)[0]
+    for distinct in (True, False):
+        out, nodes, acc = sv.verify_tree(tgt, drf, parent, tok, temp, 1234, distinct=distinct)
+        counts = np.bincount(out[:, 0].long().cpu().numpy(), minlength=V)
+        _, pval = scipy_stats.chisquare(counts, p * B)
+        if distinct:
+            assert pval > 1e-4, (pval, counts, p * B)
+        else:
+            assert pval < 1e-6, pval

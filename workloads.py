@@ -125,14 +125,16 @@ def make_inputs(cfg: int, rep: int = 0, device="cuda", B=None, V=None, K=None, g
 
 
 def make_tree_inputs(B, N, V, dtype=torch.bfloat16, seed=0, T=1.0, sigma=2.5, noise=0.7,
-                     chain_prob=0.5, n_greedy=0, device="cuda"):
+                     chain_prob=0.5, n_greedy=0, device="cuda", distinct=False):
     """Seeded candidate trees: target [B, N, V] ~ N(0, sigma); draft [B, N-1, V] =
     target rows + N(0, noise); node n >= 1 hangs under node n - 1 with
     probability chain_prob, else under a uniformly drawn earlier node; its
     token is a multinomial draw from softmax(draft row of its parent / T)
     (independently for siblings), the argmax of that row for greedy requests.
-    The first n_greedy requests are greedy (T = 0).  Returns dict(target,
-    draft, parent, tokens, temperature, seed)."""
+    distinct: siblings are drawn one after another without replacement (a
+    node's draw excludes the tokens of its earlier siblings), the top-k style
+    candidates.  The first n_greedy requests are greedy (T = 0).  Returns
+    dict(target, draft, parent, tokens, temperature, seed)."""
     dev = torch.device(device)
     g = torch.Generator(device=dev).manual_seed(int(seed))
     target = (torch.randn((B, N, V), generator=g, device=dev) * sigma).to(dtype)
@@ -157,7 +159,19 @@ def make_tree_inputs(B, N, V, dtype=torch.bfloat16, seed=0, T=1.0, sigma=2.5, no
             tb = temp[b0:b1].view(-1, 1, 1)
             sampled = tb > 0
             probs = torch.softmax(rows / torch.where(sampled, tb, torch.ones_like(tb)), dim=-1)
-            draws = torch.multinomial(probs.view(-1, V), 1, generator=g).view(b1 - b0, N - 1)
+            if distinct:  # node by node, without the earlier siblings' tokens
+                par_c = parent[b0:b1, 1:]
+                draws = torch.zeros((b1 - b0, N - 1), dtype=torch.int64, device=dev)
+                for j in range(N - 1):
+                    pj = probs[:, j].clone()
+                    for i in range(j):
+                        same = (par_c[:, i] == par_c[:, j]).to(dev)
+                        pj[same, draws[same, i]] = 0.0
+                    empty = pj.sum(dim=-1) <= 0
+                    pj[empty] = 1.0  # no mass left (a tiny vocabulary): any token
+                    draws[:, j] = torch.multinomial(pj, 1, generator=g).view(-1)
+            else:
+                draws = torch.multinomial(probs.view(-1, V), 1, generator=g).view(b1 - b0, N - 1)
             tokens[b0:b1, 1:] = torch.where(sampled.view(-1, 1), draws, rows.argmax(dim=-1))
     return dict(target=target.contiguous(), draft=draft.contiguous(),
                 parent=parent.to(torch.int32).to(dev).contiguous(),
