@@ -284,7 +284,10 @@ def test_distinct_trees_against_oracle(sv, B, N, V, dtype, T, sigma):
     vocabularies with peaked drafts make the rejected siblings' mass large."""
     inp = workloads.make_tree_inputs(B, N, V, dtype, seed=B * 7000 + N + V, T=T, sigma=sigma,
                                      noise=0.7, chain_prob=0.3, n_greedy=B // 8, distinct=True)
-    out, nodes, acc, st = _compare_tree(sv, inp, distinct=True)
+    # at V >= 128k the CDF window flags many rows (much of the mass sits in
+    # tokens of tiny probability): mismatches are gated, the flags only counted
+    out, nodes, acc, st = _compare_tree(sv, inp, distinct=True,
+                                        max_flag_frac=0.5 if V > 100000 else 0.1)
     assert st == 0
     if N > 3:
         assert acc.max() >= 2
