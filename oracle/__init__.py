@@ -76,6 +76,8 @@ def lib():
         L.svo_schedule_budget.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_longlong, i32p]
         L.svo_draft_confidence.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, f32p, f64p]
+        L.svo_lm_logits.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, f64p]
+        L.svo_lm_logits.restype = None
         _lib = L
     return _lib
 
@@ -339,6 +341,21 @@ def draft_confidence(draft, temperature):
     lib().svo_draft_confidence(draft.ctypes.data, dtype_code(draft), B, K, V,
                                _ptr(T, ctypes.c_float), _ptr(out, ctypes.c_double))
     return out
+
+
+def lm_logits(hidden, weight):
+    """LM-head logits in float64: hidden [..., d] and weight [V, d] as bf16 bit
+    patterns (uint16); returns [..., V] float64, z = sum_j h_j w_vj in
+    ascending j."""
+    h = np.ascontiguousarray(hidden, dtype=np.uint16)
+    w = np.ascontiguousarray(weight, dtype=np.uint16)
+    d = h.shape[-1]
+    V = w.shape[0]
+    assert w.shape == (V, d)
+    M = h.size // d
+    z = np.empty((M, V), dtype=np.float64)
+    lib().svo_lm_logits(h.ctypes.data, w.ctypes.data, M, V, d, _ptr(z, ctypes.c_double))
+    return z.reshape(h.shape[:-1] + (V,))
 
 
 def cpu_count():

@@ -587,6 +587,33 @@ int svo_verify_tree_sampled(const void *target, const void *draft, int dtype,
     return 0;
 }
 
+/* ------------------------------------------------------------- LM head */
+
+/* Logits of the LM-head product ("speculative decoding от черновика до
+ * проверки" (braintools.ru), "Как это работает", step 2: the target scores the
+ * drafts in one pass, whose last step maps each hidden state to vocabulary
+ * logits): z[i][v] = sum_j h[i][j] * w[v][j] over j = 0..d-1 in ascending
+ * order, in double, from bf16 hidden states h [M, d] and weights w [V, d]
+ * (raw bit patterns).  Each product of two bf16 values is exact in double. */
+static double svo_bf16_value(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+void svo_lm_logits(const uint16_t *h, const uint16_t *w, int M, int V, int d, double *z) {
+    for (int i = 0; i < M; ++i) {
+        const uint16_t *hr = h + (size_t)i * d;
+        for (int v = 0; v < V; ++v) {
+            const uint16_t *wr = w + (size_t)v * d;
+            double s = 0.0;
+            for (int j = 0; j < d; ++j) s += svo_bf16_value(hr[j]) * svo_bf16_value(wr[j]);
+            z[(size_t)i * V + v] = s;
+        }
+    }
+}
+
 /* ------------------------------------------------------------- confidence */
 
 /* Draft confidence of one position: the largest probability of the draft

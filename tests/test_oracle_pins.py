@@ -964,3 +964,57 @@ def test_tree_distinct_enumeration_catches_planted_mistakes(oracle, mutant, tmp_
     finally:
         oracle._lib = good
     assert worst > 1e-4, mutant
+
+
+# ---------------------------------------------------------------- LM-head logits
+
+def _bf16_bits(x):
+    """float32 values that are exactly bf16 -> their uint16 bit patterns."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    b = x.view(np.uint32)
+    assert ((b & 0xFFFF) == 0).all()
+    return (b >> 16).astype(np.uint16)
+
+
+def test_lm_logits_unit_vectors(oracle):
+    """Hidden states that are unit vectors pick weight columns: z[i, v] =
+    w[v, j_i] exactly."""
+    rng = np.random.default_rng(40)
+    d, V = 16, 7
+    w = rng.normal(size=(V, d)).astype(np.float32)
+    w = (w.view(np.uint32) & 0xFFFF0000).view(np.float32)   # round toward zero to bf16
+    j = np.array([3, 0, 15, 7])
+    h = np.zeros((4, d), np.float32)
+    h[np.arange(4), j] = 1.0
+    z = oracle.lm_logits(_bf16_bits(h), _bf16_bits(w))
+    assert np.array_equal(z, w[:, j].T.astype(np.float64))
+
+
+def test_lm_logits_small_integers_exact(oracle):
+    """Small integer entries: every partial sum is an integer, so the result is
+    exact in any order; checked against Python's exact integer arithmetic."""
+    rng = np.random.default_rng(41)
+    M, V, d = 5, 9, 64
+    hi = rng.integers(-3, 4, size=(M, d))
+    wi = rng.integers(-3, 4, size=(V, d))
+    z = oracle.lm_logits(_bf16_bits(hi.astype(np.float32)), _bf16_bits(wi.astype(np.float32)))
+    want = [[sum(int(a) * int(b) for a, b in zip(hi[i], wi[v])) for v in range(V)] for i in range(M)]
+    assert np.array_equal(z, np.array(want, dtype=np.float64))
+
+
+def test_lm_logits_against_library_matmul(oracle):
+    """Random bf16 inputs against numpy's float64 matrix product of the same
+    values (an independent summation): equal to within double rounding."""
+    rng = np.random.default_rng(42)
+    M, V, d = 6, 50, 256
+    h = rng.normal(size=(M, d)).astype(np.float32)
+    w = rng.normal(size=(V, d)).astype(np.float32) * 0.05
+    h = (h.view(np.uint32) & 0xFFFF0000).view(np.float32)
+    w = (w.view(np.uint32) & 0xFFFF0000).view(np.float32)
+    z = oracle.lm_logits(_bf16_bits(h), _bf16_bits(w))
+    ref = h.astype(np.float64) @ w.astype(np.float64).T
+    scale = np.abs(h).astype(np.float64) @ np.abs(w).astype(np.float64).T
+    assert (np.abs(z - ref) <= 1e-14 * scale + 1e-300).all()
+    # the batch shape is kept
+    z3 = oracle.lm_logits(_bf16_bits(h).reshape(2, 3, d), _bf16_bits(w))
+    assert z3.shape == (2, 3, V) and np.array_equal(z3.reshape(M, V), z)
