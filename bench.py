@@ -547,6 +547,181 @@ def tree_oracle_sample(tgt, drf, parent, tok, temp, seed, max_seconds, distinct=
             % (n - 1, B, reps, pos, nthreads), dt)
 
 
+def lm_oracle_sample(inp, max_seconds):
+    """The oracle's LM-head step (float64 logits of each request's rows, then
+    its verification) on requests taken in order until the time budget is
+    spent (at least one): the rows of a request are split across host threads
+    (the C loops run outside the interpreter lock)."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    ht = workloads.bf16_bits(inp["hidden_target"])
+    hd = workloads.bf16_bits(inp["hidden_draft"])
+    w = workloads.bf16_bits(inp["w"])
+    tok = inp["tokens"].cpu().numpy()
+    T = inp["temperature"].cpu().numpy()
+    B, K1, d = ht.shape
+    K = K1 - 1
+    rows = [(0, k) for k in range(K + 1)] + [(1, k) for k in range(K)]
+    cores = oracle.cpu_count()
+    nthreads = min(cores, len(rows))
+    pos, dt, b = 0, 0.0, 0
+    with ThreadPoolExecutor(max_workers=nthreads) as ex:
+        while b == 0 or (dt < max_seconds and b < B):
+            t0 = time.perf_counter()
+            z = list(ex.map(lambda r: oracle.lm_logits((ht if r[0] == 0 else hd)[b, r[1]], w), rows))
+            zt = np.stack(z[:K + 1])[None]
+            zd = np.stack(z[K + 1:])[None]
+            oracle.verify(zt, zd, tok, None, T, inp["seed"], b0=b, b1=b + 1, broadcast_rows=True)
+            dt += time.perf_counter() - t0
+            pos += K
+            b += 1
+    return pos / dt, nthreads, ("requests 0..%d, each one's %d logit rows split over %d threads "
+                                "(%d positions, %.1f s)" % (b - 1, len(rows), nthreads, pos, dt)), dt
+
+
+def run_lmhead(args, world, rank, local):
+    """The verification step with the LM-head product fused: hidden states of
+    the K+1 target and K draft positions and the head's weights in, tokens
+    out; the logits live only in the GEMM's accumulators (and, for the rows
+    the sampler draws from, a recompute).  Hidden size of the workload's model
+    family; synthetic normal hidden states and weights."""
+    import speculative_decoding_verification_69_gb300 as sv
+    sv.load_library()
+    dev = torch.device("cuda", local)
+    cfg = args.config
+    c = workloads.CONFIGS[cfg]
+    B, K, V = c["B"], c["K"], c["V"]
+    d = workloads.LM_HIDDEN[cfg]
+    T = workloads.workload_temperatures(cfg, B, device=dev)
+    noise = c["noise"] if isinstance(c["noise"], float) else 0.5
+    inp = workloads.make_lmhead_inputs(B, K, V, d, seed=workloads.seed_for(cfg, rank), T=T,
+                                       sigma=c["sigma"], noise=noise, device=dev)
+    ws = torch.empty(sv.lmhead_workspace_bytes(B, K, V, d), dtype=torch.uint8, device=dev)
+    out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    # hidden states cycled through copies (the weights are the model's, resident)
+    ncopies = 2
+    copies = [(inp["hidden_target"], inp["hidden_draft"])] + [
+        (inp["hidden_target"].clone(), inp["hidden_draft"].clone()) for _ in range(ncopies - 1)]
+
+    def step(i, ht=None, hd=None):
+        if ht is None:
+            ht, hd = copies[i % ncopies]
+        sv.verify_lmhead(ht, hd, inp["w"], inp["w"], inp["tokens"], inp["verify_len"],
+                         inp["temperature"], inp["seed"], out_tokens=out_tokens,
+                         accept_len=accept_len, workspace=ws)
+
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_gpu0 = time.perf_counter()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, b in kev:
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(args.warmup + i)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.perf_counter()
+    for i in range(args.steps):  # the two statistics GEMMs bracketed by events
+        sv.profile_events(*kev[i])
+        step(args.warmup + args.steps + i)
+    sv.profile_events(None, None)
+    torch.cuda.synchronize()
+    t2 = time.perf_counter()
+    a_host = accept_len.cpu().numpy()
+    o_host = out_tokens.cpu().numpy()
+    total_s = sum(a.elapsed_time(b) for a, b in ev) / 1e3
+    total_s_max = max_over_ranks(total_s, world)
+    positions = B * K
+    gemm_s = sum(a.elapsed_time(b) for a, b in kev) / 1e3 / args.steps
+    flop_stats = 2.0 * (B * (2 * K + 1)) * d * V
+    # end to end: the step's hidden states, tokens and temperatures copied in
+    # from pinned host memory, the outputs read back
+    host = {k: inp[k].cpu().pin_memory() for k in ("hidden_target", "hidden_draft", "tokens",
+                                                   "temperature")}
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    h_out = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    h_acc = torch.empty((B,), dtype=torch.int32).pin_memory()
+
+    def e2e_step():
+        for k, v in host.items():
+            dbuf[k].copy_(v, non_blocking=True)
+        o, a = sv.verify_lmhead(dbuf["hidden_target"], dbuf["hidden_draft"], inp["w"], inp["w"],
+                                dbuf["tokens"], inp["verify_len"], dbuf["temperature"],
+                                inp["seed"], out_tokens=out_tokens, accept_len=accept_len,
+                                workspace=ws)
+        h_out.copy_(o, non_blocking=True)
+        h_acc.copy_(a, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 100))
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(e2e_steps)]
+    barrier(world)
+    for i in range(e2e_steps):
+        e2e_ev[i][0].record(stream)
+        e2e_step()
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev) / 1e3, world)
+    clocks.mark(t_gpu0, time.perf_counter() + 0.05)
+    clk = clocks.stop(timed=(t0, t2), label="warm-up, both timed loops and the end-to-end loop")
+    n_samp = int((inp["temperature"] > 0).sum().item())
+    peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, peak_kind = float(json.load(f)["bf16_tflops_sustained"]), "measured, sustained"
+    except Exception:
+        peak, peak_kind = 1700.0, "fallback, sustained"
+    achieved = flop_stats / gemm_s / 1e12
+    res = {
+        "metric": "verified draft positions/s", "value": sum_over_ranks(positions * args.steps, world) / total_s_max,
+        "unit": "positions/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_s_max * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded normal hidden states and LM-head weights; no trained weights)",
+        "config": {"workload": workloads.NAMES[cfg] + " shapes, LM head fused (d=%d)" % d,
+                   "B": B, "K": K, "V": V, "d": d,
+                   "mode": "LM-head product with the row statistics in its epilogue; the "
+                           "sampled requests' draw rows recomputed after the decisions",
+                   "flop_per_step": flop_stats + 2.0 * 2 * n_samp * d * V,
+                   "tflops_step": (flop_stats + 4.0 * n_samp * d * V) * args.steps / total_s / 1e12,
+                   "logit_bytes_never_written": B * (2 * K + 1) * V * 4,
+                   "l2": "weights %d bytes (larger than L2) stream once per step; hidden states "
+                         "cycled through %d copies" % (V * d * 2, ncopies)},
+        "roofline": {"bound": "tensor", "kernel": "lm_gemm<LmStatsEpi> (target and draft rows)",
+                     "achieved": achieved, "peak": peak, "peak_source": peak_kind,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "algorithmic_flop_per_launch_pair": flop_stats, "kernel_ms": gemm_s * 1e3},
+        "e2e": {"value": sum_over_ranks(positions * e2e_steps, world) / e2e_s, "unit": "positions/s",
+                "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
+                "d2h_bytes_per_step": (h_out.numel() + h_acc.numel()) * 4, "steps": e2e_steps},
+        "gpu_launches": 9 * args.steps, "clocks": clk,
+        "accept_len_hist": [int(x) for x in np.bincount(a_host, minlength=K + 1)],
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pps, cores, sample, dt = lm_oracle_sample(inp, args.cpu_seconds)
+        res["cpu_baseline"] = {"value": pps, "unit": "positions/s", "cores": cores,
+                               "kind": "oracle", "sample": sample, "seconds": dt}
+    return res
+
+
 def run_ours(args, world, rank, local):
     import speculative_decoding_verification_69_gb300 as sv
     sv.load_library()
@@ -865,6 +1040,9 @@ def main(argv=None):
     ap.add_argument("--distinct", action="store_true",
                     help="with --tree-sampled: siblings drawn without replacement (top-k style), "
                          "verified by spec_verify_tree_distinct")
+    ap.add_argument("--lmhead", action="store_true",
+                    help="hidden states and LM-head weights in: the product on the tensor cores "
+                         "with the row statistics in its epilogue (spec_verify_lmhead)")
     ap.add_argument("--early-exit", type=int, default=0,
                     help="verify positions [0, W) first, then the rest for open requests")
     args = ap.parse_args(argv)
@@ -880,7 +1058,12 @@ def main(argv=None):
             print(json.dumps(run_reference(args, world, 0, local)), flush=True)
         return 0
     world, rank, local = dist_setup(args.gpus)
-    res = run_tree(args, world, rank, local) if args.tree else run_ours(args, world, rank, local)
+    if args.tree:
+        res = run_tree(args, world, rank, local)
+    elif args.lmhead:
+        res = run_lmhead(args, world, rank, local)
+    else:
+        res = run_ours(args, world, rank, local)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -348,6 +348,43 @@ spec_status_t spec_verify_scheduled(const void *target_logits, const void *draft
                                     uint32_t *dev_status, void *stream);
 
 /*
+ * spec_verify_lmhead -- the verification step with its input side fused: the
+ * logits come from the LM-head product of the hidden states, computed on the
+ * tensor cores, and are consumed in that product's epilogue instead of being
+ * written to memory ("speculative decoding от черновика до проверки"
+ * (braintools.ru), "Как это работает", step 2: the target scores all drafts
+ * in one pass, whose last step is the vocabulary projection; the same page
+ * stresses that moving weights and activations through memory is the cost).
+ *   hidden_target [B, K+1, d]  bf16, row (b, k) = the target's last hidden
+ *                              state at position k; target logits row (b, k)
+ *                              = hidden_target[b, k] . w_target^T.
+ *   hidden_draft  [B, K, d]    bf16, the drafter's hidden states; draft logits
+ *                              row (b, k) = hidden_draft[b, k] . w_draft^T.
+ *   w_target, w_draft [V, d]   bf16 row-major LM-head weights (may be the same
+ *                              buffer, as when the drafter shares the target's
+ *                              head).  All four 16-byte aligned.
+ *   d                          hidden size, a multiple of 64, at most 65536.
+ *   V                          a multiple of 4.
+ *   The logits are the fp32 accumulations of the bf16 products (tensor-core
+ *   order); the step is then spec_verify's on those fp32 values: the same
+ *   rule, outputs, uniforms, status bits and errors.  Every target row and
+ *   every draft row is multiplied (the verify lengths and greedy requests do
+ *   not shrink the product); the few rows the sampler draws from (one or two
+ *   per sampled request) are multiplied again after the decisions, into the
+ *   workspace.  row_stats / probs: as spec_verify_debug (nullable).
+ *   workspace: spec_lmhead_workspace_bytes(B, K, V, d) bytes, 256-byte
+ *   aligned (it holds 8 B V bytes of recomputed rows).  Launches 9 kernels.
+ */
+size_t spec_lmhead_workspace_bytes(int B, int K, int V, int d);
+spec_status_t spec_verify_lmhead(const void *hidden_target, const void *hidden_draft,
+                                 const void *w_target, const void *w_draft, int d,
+                                 const int32_t *draft_tokens, const int32_t *verify_len,
+                                 const float *temperature, uint64_t seed, int B, int K, int V,
+                                 int32_t *out_tokens, int32_t *accept_len, void *workspace,
+                                 size_t workspace_bytes, uint32_t *dev_status, double *row_stats,
+                                 double *probs, void *stream);
+
+/*
  * spec_profile_events -- measurement hook.  When both events are non-NULL
  * (cudaEvent_t values passed as void*), every later spec_verify /
  * spec_verify_debug call records ev_start immediately before and ev_end

@@ -78,6 +78,12 @@ def load_library():
                                         ctypes.c_float, ctypes.c_longlong, f32p, i32p, i32p, i32p,
                                         vp, ctypes.c_size_t, u32p, vp]
     L.spec_verify_scheduled.restype = ctypes.c_int
+    L.spec_lmhead_workspace_bytes.argtypes = [ctypes.c_int] * 4
+    L.spec_lmhead_workspace_bytes.restype = ctypes.c_size_t
+    L.spec_verify_lmhead.argtypes = [vp, vp, vp, vp, ctypes.c_int, i32p, i32p, f32p, ctypes.c_uint64,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, i32p, vp,
+                                     ctypes.c_size_t, u32p, f64p, f64p, vp]
+    L.spec_verify_lmhead.restype = ctypes.c_int
     L.spec_verify_noalloc.argtypes = common[:12] + [u32p, vp]
     L.spec_verify_noalloc.restype = ctypes.c_int
     L.spec_profile_events.argtypes = [vp, vp]
@@ -97,6 +103,7 @@ def exported_symbols():
             "spec_verify_early_exit", "spec_tree_workspace_bytes", "spec_verify_tree_greedy",
             "spec_verify_tree", "spec_verify_tree_distinct",
             "spec_draft_confidence", "spec_schedule_budget", "spec_verify_scheduled",
+            "spec_lmhead_workspace_bytes", "spec_verify_lmhead",
             "spec_schedule_len", "spec_verify_noalloc",
             "spec_profile_events", "spec_debug_force_wait_timeout",
             "spec_verify_kernel_count", "spec_status_str"]
@@ -367,6 +374,60 @@ def verify_scheduled(target, draft, tokens, temperature, seed, *, threshold=None
                                    _ptr(verify_len_out), _ptr(out_tokens), _ptr(accept_len),
                                    _ptr(ws), ws.numel(), _ptr(dev_status), _stream(stream)))
     return out_tokens, accept_len, verify_len_out, (maxprob_out if draft_maxprob is None else None)
+
+
+def lmhead_workspace_bytes(B, K, V, d) -> int:
+    return int(load_library().spec_lmhead_workspace_bytes(B, K, V, d))
+
+
+def verify_lmhead(hidden_target, hidden_draft, w_target, w_draft, tokens, verify_len, temperature,
+                  seed, *, out_tokens=None, accept_len=None, dev_status=None, workspace=None,
+                  debug=False, stream=None):
+    """Verification with the LM-head product fused (spec_verify_lmhead):
+    hidden_target [B, K+1, d], hidden_draft [B, K, d], w_target / w_draft [V, d],
+    all bf16 CUDA tensors.  Returns (out_tokens, accept_len), plus (row_stats,
+    probs) with debug."""
+    L = load_library()
+    if hidden_target.dim() != 3:
+        raise ValueError("hidden_target must be [B, K+1, d]")
+    B, K1, d = hidden_target.shape
+    K = K1 - 1
+    V = w_target.shape[0]
+    for t, shape in ((hidden_target, (B, K + 1, d)), (hidden_draft, (B, K, d)),
+                     (w_target, (V, d)), (w_draft, (V, d))):
+        if (t.shape != shape or t.dtype != torch.bfloat16 or not t.is_cuda
+                or not t.is_contiguous()):
+            raise ValueError("hidden states and weights must be contiguous bf16 CUDA tensors "
+                             "[B, K+1, d], [B, K, d], [V, d], [V, d]")
+    if tokens.shape != (B, K) or tokens.dtype != torch.int32 or not tokens.is_cuda:
+        raise ValueError("tokens must be int32 [B, K] on the device")
+    if verify_len is not None and (verify_len.shape != (B,) or verify_len.dtype != torch.int32):
+        raise ValueError("verify_len must be int32 [B] or None")
+    if temperature.shape != (B,) or temperature.dtype != torch.float32 or not temperature.is_cuda:
+        raise ValueError("temperature must be float32 [B] on the device")
+    dev = hidden_target.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if accept_len is None:
+        accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    n = lmhead_workspace_bytes(B, K, V, d)
+    if n == 0:
+        raise SpecVerifyError("unsupported LM-head shape B=%d K=%d V=%d d=%d" % (B, K, V, d))
+    if workspace is None or workspace.numel() < n:
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    rs = pr = None
+    if debug:
+        rs = torch.full((B, 2 * K + 1, 2), float("nan"), dtype=torch.float64, device=dev)
+        pr = torch.full((B, K, 2), float("nan"), dtype=torch.float64, device=dev)
+    _check(L.spec_verify_lmhead(_ptr(hidden_target), _ptr(hidden_draft), _ptr(w_target),
+                                _ptr(w_draft), d, _ptr(tokens), _ptr(verify_len),
+                                _ptr(temperature), int(seed) & 0xFFFFFFFFFFFFFFFF, B, K, V,
+                                _ptr(out_tokens), _ptr(accept_len), _ptr(workspace),
+                                workspace.numel(), _ptr(dev_status), _ptr(rs), _ptr(pr),
+                                _stream(stream)))
+    if debug:
+        return out_tokens, accept_len, rs, pr
+    return out_tokens, accept_len
 
 
 def kernels_per_scheduled(confidence: bool, budget: bool) -> int:

@@ -31,7 +31,10 @@
 // max(0, a - s b)), one pass over the vocabulary per rejection.
 #include "spec_verify.h"
 #include "sv_common.cuh"
+#include "lm_gemm.cuh"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <cfloat>
 #include <climits>
@@ -101,12 +104,24 @@ struct Params {
     int32_t *vlen_out;      // [B] the scheduled lengths, written by sv_prep (nullable)
     int draft_ready;        // the draft rows' partials are already in `part` (a confidence
                             // pass over the same rows at the same T): list target rows only
+    // LM-head path (spec_verify_lmhead): the logits exist only inside the GEMM
+    const float *gz;        // [B, nslot] logit of each row at its draft token, or null
+    const char *samp_t;     // [B, V] fp32: row li = the target row sampled by list entry li
+    const char *samp_d;     // [B, V] fp32: row li = its draft row (residual draws)
 };
 
 __device__ __forceinline__ const char *row_ptr(const Params &P, int b, int slot, int esz) {
     if (slot <= P.K)
         return P.tgt + ((size_t)b * (size_t)(P.K + 1) + (size_t)slot) * (size_t)P.V * esz;
     return P.drf + ((size_t)b * (size_t)P.K + (size_t)(slot - P.K - 1)) * (size_t)P.V * esz;
+}
+
+// Row of a sampled request's draw: list entry li's recomputed row on the
+// LM-head path, else the request's logit row.
+__device__ __forceinline__ const char *samp_row(const Params &P, int li, int b, int slot, int esz,
+                                                bool draft) {
+    if (P.samp_t) return (draft ? P.samp_d : P.samp_t) + (size_t)li * (size_t)P.V * esz;
+    return row_ptr(P, b, slot, esz);
 }
 
 __device__ __forceinline__ float load_logit(const char *row, int dt, int x) {
@@ -639,13 +654,19 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
     if (warp == 0 && lane < L) {
         x = P.tokens[(size_t)b * K + lane];
         if (!greedy) {
-            g = load_logit(row_ptr(P, b, lane, Fmt<DT>::kESZ), DT, x);
-            gd = load_logit(row_ptr(P, b, K + 1 + lane, Fmt<DT>::kESZ), DT, x);
+            if (!P.gz) {
+                g = load_logit(row_ptr(P, b, lane, Fmt<DT>::kESZ), DT, x);
+                gd = load_logit(row_ptr(P, b, K + 1 + lane, Fmt<DT>::kESZ), DT, x);
+            }
             u = uniform_accept_f(P.seed, (uint32_t)b, (uint32_t)lane);
         }
     }
     pdl_wait();  // chunk partials come from sv_pass1
     pdl_trigger();
+    if (P.gz && warp == 0 && lane < L && !greedy) {  // written by the LM-head GEMM's epilogue
+        g = P.gz[(size_t)b * P.nslot + lane];
+        gd = P.gz[(size_t)b * P.nslot + K + 1 + lane];
+    }
     if (P.ee_done && P.ee_done[b]) return;  // finished in an earlier wave (uniform over the CTA)
     // the rows of this wave: positions [k0, e) and, when L <= k1, the row L
     const int k0 = P.k0, e = min(P.k1, L);
@@ -881,10 +902,11 @@ __global__ void __launch_bounds__(kSWarps * 32, kSMinBlocks) sv_sample(Params P)
             uint64_t *fb = reinterpret_cast<uint64_t *>(&bar[s]);
             const bool two = cur_si.mode == 1;
             mbar_expect_tx(fb, two ? 2u * bytes : bytes);
-            bulk_g2s(sh.buf[warp][s], row_ptr(P, cur_b, cur_si.slot_t, ESZ) + (size_t)e0 * ESZ, bytes, fb);
+            bulk_g2s(sh.buf[warp][s], samp_row(P, cur_li, cur_b, cur_si.slot_t, ESZ, false) + (size_t)e0 * ESZ,
+                     bytes, fb);
             if (two)
                 bulk_g2s(sh.buf[warp][s] + kChunkBytes / 16,
-                         row_ptr(P, cur_b, cur_si.slot_d, ESZ) + (size_t)e0 * ESZ, bytes, fb);
+                         samp_row(P, cur_li, cur_b, cur_si.slot_d, ESZ, true) + (size_t)e0 * ESZ, bytes, fb);
         }
         __syncwarp();
     };
@@ -928,8 +950,8 @@ __global__ void __launch_bounds__(kSWarps * 32, kSMinBlocks) sv_sample(Params P)
             const long long e0 = (long long)c * CE;
             nvec = (int)((min((long long)CE, (long long)P.V - e0) + EPV - 1) / EPV);
             const bool resid = si.mode == 1;
-            const char *rowt = row_ptr(P, b, si.slot_t, ESZ);
-            const char *rowd = resid ? row_ptr(P, b, si.slot_d, ESZ) : rowt;
+            const char *rowt = samp_row(P, cur_li, b, si.slot_t, ESZ, false);
+            const char *rowd = resid ? samp_row(P, cur_li, b, si.slot_d, ESZ, true) : rowt;
 #pragma unroll
             for (int i = 0; i < kVecPerLane; ++i) {
                 const long long q = e0 + (long long)(i * 32 + lane) * EPV;
@@ -1010,8 +1032,8 @@ __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
     const int per = (nch + 31) / 32;
     const int c0 = lane * per, c1 = min(nch, c0 + per);
     const bool held = per <= kPerLane;
-    const char *rowt = row_ptr(P, b, si.slot_t, ESZ);
-    const char *rowd = resid ? row_ptr(P, b, si.slot_d, ESZ) : rowt;
+    const char *rowt = samp_row(P, li, b, si.slot_t, ESZ, false);
+    const char *rowd = resid ? samp_row(P, li, b, si.slot_d, ESZ, true) : rowt;
     const float2 m2 = make_float2(si.m_t, si.m_d);
     const float2 chi2 = make_float2(si.c_hi, si.c_hi), clo2 = make_float2(si.c_lo, si.c_lo);
     const uint32_t ni = Fmt<DT>::kNegInfWord;
@@ -2163,6 +2185,144 @@ __global__ void __launch_bounds__(kBudgetThreads) sv_schedule_budget(const float
     }
 }
 
+// ------------------------------------------------------------------ LM head (epilogues)
+
+// Statistics epilogue of the LM-head GEMM: the same per-row statistics the
+// streaming pass produces, taken from the fp32 accumulators of a 128 x 256
+// tile instead of a logit row in memory ("speculative decoding от черновика до
+// проверки" (braintools.ru), "Как это работает", step 2: the target scores
+// all drafts in one pass, whose last step is this product).  Row r of the
+// product is slot slot0 + r % rows_per_req of request r / rows_per_req; per
+// (row, tile) one partial {max, sum 2^((z - max) log2(e)/T), -1} (sampled
+// request) or {max, 0, lowest index of the max} (greedy request), and the
+// logit at the row's draft token when the tile holds it.
+struct LmStatsEpi {
+    float4 *part;
+    float *gz;
+    const int32_t *tokens;
+    const float *temperature;
+    int npart, nslot, K, rows_per_req, slot0, tok_off;
+    __device__ __forceinline__ void row(int r, bool valid, int n0, int V, uint32_t taddr) const {
+        int b = 0, slot = 0, x = -1;
+        bool greedy = true;
+        float c = 0.f;
+        if (valid) {
+            b = r / rows_per_req;
+            slot = slot0 + (r - b * rows_per_req);
+            const int tk = slot - tok_off;  // the draft token this row scores, if any
+            if (tk >= 0 && tk < K) x = tokens[(size_t)b * K + tk];
+            const float T = temperature[b];
+            greedy = !(isfinite(T) && T >= FLT_MIN);
+            if (!greedy) c = __fdiv_rn(kLog2EHi, T);  // the statistics pass's factor
+        }
+        float m = -INFINITY, s = 0.f, g = 0.f;
+        int am = INT_MAX;
+        bool have_g = false;
+        const unsigned long long c2 = f2u(make_float2(c, c));
+#pragma unroll 1
+        for (int j = 0; j < kLmBN / 32; ++j) {
+            float v[32];
+            __syncwarp();
+            tmem_ld32(taddr + (uint32_t)(j * 32), v);
+            const int nb = n0 + j * 32;
+            if (nb + 32 > V) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (nb + i >= V) v[i] = -INFINITY;
+            }
+            if (x >= nb && x < nb + 32) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (x - nb == i) g = v[i];
+                have_g = true;
+            }
+            float cm = v[0];
+#pragma unroll
+            for (int i = 1; i < 32; ++i) cm = fmaxf(cm, v[i]);
+            if (greedy) {
+                if (cm > m) {  // chunks come in increasing index order
+                    int idx = 31;
+#pragma unroll
+                    for (int i = 31; i >= 0; --i)
+                        if (v[i] == cm) idx = i;
+                    m = cm;
+                    am = nb + idx;
+                }
+            } else if (cm > -INFINITY) {
+                if (cm > m) {
+                    if (m > -INFINITY) s *= ex2((m - cm) * c);
+                    m = cm;
+                }
+                const unsigned long long m2 = f2u(make_float2(m, m));
+                unsigned long long a0 = 0ull, a1 = 0ull;
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    f32x2_exp_acc(__float_as_uint(v[i]), __float_as_uint(v[i + 1]), m2, c2, a0);
+                    f32x2_exp_acc(__float_as_uint(v[i + 2]), __float_as_uint(v[i + 3]), m2, c2, a1);
+                }
+                const float2 t = add2(u2f(a0), u2f(a1));
+                s += t.x + t.y;
+            }
+        }
+        if (valid) {
+            part[((size_t)b * nslot + slot) * npart + n0 / kLmBN] =
+                greedy ? make_float4(m, 0.f, __int_as_float(am), 0.f)
+                       : make_float4(m, s, __int_as_float(-1), 0.f);
+            if (have_g) gz[(size_t)b * nslot + slot] = g;
+        }
+    }
+};
+
+// Store epilogue: the rows themselves (fp32), for the few rows the sampler
+// draws from, recomputed after the decisions.
+struct LmStoreEpi {
+    float *out;  // [rows, V]
+    __device__ __forceinline__ void row(int r, bool valid, int n0, int V, uint32_t taddr) const {
+        float *o = out + (size_t)r * (size_t)V;
+#pragma unroll 1
+        for (int j = 0; j < kLmBN / 32; ++j) {
+            float v[32];
+            __syncwarp();
+            tmem_ld32(taddr + (uint32_t)(j * 32), v);
+            const int nb = n0 + j * 32;
+            if (!valid) continue;
+            if (nb + 32 <= V && (V & 3) == 0) {
+                float4 *o4 = reinterpret_cast<float4 *>(o + nb);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    o4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            } else {
+                for (int i = 0; i < 32; ++i)
+                    if (nb + i < V) o[nb + i] = v[i];
+            }
+        }
+    }
+};
+
+// The hidden states of each sampled request's draw rows, packed by its entry
+// in the sampled-request list (target row a or L; draft row a for a residual
+// draw, zeros for a bonus draw), for the recompute of those rows.
+__global__ void __launch_bounds__(256) lm_gather(Params P, const uint16_t *ht, const uint16_t *hd,
+                                                  int d, uint16_t *hct, uint16_t *hcd) {
+    pdl_wait();  // the list comes from sv_decide
+    pdl_trigger();
+    const int li = blockIdx.x;
+    if (li >= *P.samp_count) return;
+    const SampInfo si = P.samp_list[li];
+    const int K = P.K, nv = d / 8;
+    const uint4 *st = reinterpret_cast<const uint4 *>(ht + ((size_t)si.b * (K + 1) + si.slot_t) * d);
+    uint4 *dt = reinterpret_cast<uint4 *>(hct + (size_t)li * d);
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) dt[i] = st[i];
+    uint4 *dd = reinterpret_cast<uint4 *>(hcd + (size_t)li * d);
+    if (si.mode == 1) {
+        const uint4 *sd =
+            reinterpret_cast<const uint4 *>(hd + ((size_t)si.b * K + (si.slot_d - K - 1)) * d);
+        for (int i = threadIdx.x; i < nv; i += blockDim.x) dd[i] = sd[i];
+    } else {
+        for (int i = threadIdx.x; i < nv; i += blockDim.x) dd[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 struct Layout {
@@ -2218,6 +2378,7 @@ struct DevInfo {
     int occ_p1[2][2] = {{0, 0}, {0, 0}};
     int occ_sample[2][2] = {{0, 0}, {0, 0}};
     bool walk_smem[2][2] = {{false, false}, {false, false}};  // tree walk's shared-memory limit raised
+    bool lm_ready = false;  // LM-head GEMM's shared-memory limit raised
     bool ok = false;
 };
 
@@ -2464,6 +2625,94 @@ static void launch_confidence(const Params &P, const DevInfo &d, cudaStream_t s,
     cudaLaunchKernelEx(&cfg, sv_conf_out, P, maxprob);
 }
 
+// ------------------------------------------------------------------ LM head (host)
+
+static size_t npart_lm(int V) { return (size_t)((V + kLmBN - 1) / kLmBN); }
+
+struct LmLayout {
+    size_t req, row_count, rows, part, sub, sexact, samp_list, samp_count, gz, hct, hcd, ct, cd, total;
+};
+
+static LmLayout layout_lm(int B, int K, int V, int d) {
+    LmLayout L{};
+    const size_t nslot = (size_t)(2 * K + 1), nchunk = nchunk_for(V, SPEC_DTYPE_F32);
+    size_t off = 0;
+    L.req = off; off = align256(off + sizeof(ReqInfo) * (size_t)B);
+    L.row_count = off; off = align256(off + sizeof(int));
+    L.rows = off; off = align256(off + sizeof(int4) * (size_t)B * nslot);
+    L.part = off; off = align256(off + sizeof(float4) * (size_t)B * nslot * npart_lm(V));
+    L.sub = off; off = align256(off + sizeof(float4) * (size_t)B * nchunk);
+    L.sexact = off; off = align256(off + sizeof(float4) * (size_t)B * nchunk);
+    L.samp_list = off; off = align256(off + sizeof(SampInfo) * (size_t)B);
+    L.samp_count = off; off = align256(off + sizeof(int));
+    L.gz = off; off = align256(off + sizeof(float) * (size_t)B * nslot);
+    L.hct = off; off = align256(off + 2 * (size_t)B * (size_t)d);
+    L.hcd = off; off = align256(off + 2 * (size_t)B * (size_t)d);
+    L.ct = off; off = align256(off + 4 * (size_t)B * (size_t)V);
+    L.cd = off; off = align256(off + 4 * (size_t)B * (size_t)V);
+    L.total = off;
+    return L;
+}
+
+static bool lm_sizes_ok(int B, int K, int V, int d) {
+    return sizes_ok(B, K, V) && d >= kLmBK && d % kLmBK == 0 && d <= (1 << 16) &&
+           (size_t)B * (size_t)(K + 1) < ((size_t)1 << 31) && (V % 4) == 0 &&
+           (size_t)B * (size_t)(2 * K + 1) * nchunk_for(V, SPEC_DTYPE_F32) < ((size_t)1 << 31);
+}
+
+// A 2D tensor map over a row-major bf16 matrix [rows, cols] with boxes of
+// 64 columns (128 bytes, the swizzle span) by box_rows rows, 128-byte swizzle,
+// out-of-range elements read as zero.
+static bool make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return false;
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kLmBK, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <class Epi>
+static cudaError_t launch_lm_gemm(const CUtensorMap &tA, const CUtensorMap &tB, int M_max,
+                                  const int *M_dev, int V, int d, const Epi &epi, uint32_t *status,
+                                  const DevInfo &dv, cudaStream_t s) {
+    const long long tiles = ((long long)(M_max + kLmBM - 1) / kLmBM) * ((V + kLmBN - 1) / kLmBN);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(tiles < dv.sms ? (tiles > 0 ? tiles : 1) : dv.sms));
+    cfg.blockDim = dim3(kLmThreads);
+    cfg.dynamicSmemBytes = kLmSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, lm_gemm<Epi>, tA, tB, M_max, M_dev, V, d, epi, status);
+}
+
+static bool lm_setup(DevInfo &d) {
+    if (d.lm_ready) return true;
+    if (cudaFuncSetAttribute(lm_gemm<LmStatsEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kLmSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(lm_gemm<LmStoreEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kLmSmem) != cudaSuccess)
+        return false;
+    d.lm_ready = true;
+    return true;
+}
+
 } // namespace sv
 
 extern "C" {
@@ -2582,6 +2831,126 @@ spec_status_t spec_verify_scheduled(const void *target_logits, const void *draft
         P.verify_len = vl;
     }
     sv::launch_step(P, *d, s, dtype, vec);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+size_t spec_lmhead_workspace_bytes(int B, int K, int V, int d) {
+    if (!sv::lm_sizes_ok(B, K, V, d)) return 0;
+    return sv::layout_lm(B, K, V, d).total;
+}
+
+spec_status_t spec_verify_lmhead(const void *hidden_target, const void *hidden_draft,
+                                 const void *w_target, const void *w_draft, int d,
+                                 const int32_t *draft_tokens, const int32_t *verify_len,
+                                 const float *temperature, uint64_t seed, int B, int K, int V,
+                                 int32_t *out_tokens, int32_t *accept_len, void *workspace,
+                                 size_t workspace_bytes, uint32_t *dev_status, double *row_stats,
+                                 double *probs, void *stream) {
+    if (!sv::lm_sizes_ok(B, K, V, d)) return SPEC_ERR_INVALID_ARG;
+    if (!hidden_target || !hidden_draft || !w_target || !w_draft || !draft_tokens ||
+        !temperature || !out_tokens || !accept_len)
+        return SPEC_ERR_INVALID_ARG;
+    if (((uintptr_t)hidden_target & 15u) || ((uintptr_t)hidden_draft & 15u) ||
+        ((uintptr_t)w_target & 15u) || ((uintptr_t)w_draft & 15u))
+        return SPEC_ERR_INVALID_ARG;
+    const sv::LmLayout L = sv::layout_lm(B, K, V, d);
+    if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u))
+        return SPEC_ERR_WORKSPACE;
+    sv::DevInfo *dv = sv::dev_info();
+    if (!dv || !sv::lm_setup(*dv)) return SPEC_ERR_CUDA;
+    char *ws = static_cast<char *>(workspace);
+    CUtensorMap tHt, tHd, tWt, tWd, tCt, tCd;
+    if (!sv::make_tmap_bf16(&tHt, hidden_target, (uint64_t)B * (K + 1), (uint64_t)d, sv::kLmBM) ||
+        !sv::make_tmap_bf16(&tHd, hidden_draft, (uint64_t)B * K, (uint64_t)d, sv::kLmBM) ||
+        !sv::make_tmap_bf16(&tWt, w_target, (uint64_t)V, (uint64_t)d, sv::kLmBN) ||
+        !sv::make_tmap_bf16(&tWd, w_draft, (uint64_t)V, (uint64_t)d, sv::kLmBN) ||
+        !sv::make_tmap_bf16(&tCt, ws + L.hct, (uint64_t)B, (uint64_t)d, sv::kLmBM) ||
+        !sv::make_tmap_bf16(&tCd, ws + L.hcd, (uint64_t)B, (uint64_t)d, sv::kLmBM))
+        return SPEC_ERR_CUDA;
+    sv::Params P{};
+    P.tgt = ws + L.ct;  // no logit row is read in place on this path
+    P.drf = ws + L.cd;
+    P.tokens = draft_tokens;
+    P.verify_len = verify_len;
+    P.temperature = temperature;
+    P.seed = seed;
+    P.B = B;
+    P.K = K;
+    P.V = V;
+    P.nchunk = (int)sv::nchunk_for(V, SPEC_DTYPE_F32);
+    P.npart = (int)sv::npart_lm(V);
+    P.nslot = 2 * K + 1;
+    P.out_tokens = out_tokens;
+    P.accept_len = accept_len;
+    P.dev_status = dev_status;
+    P.dbg_rows = row_stats;
+    P.dbg_probs = probs;
+    P.req = reinterpret_cast<sv::ReqInfo *>(ws + L.req);
+    P.row_count = reinterpret_cast<int *>(ws + L.row_count);
+    P.rows = reinterpret_cast<int4 *>(ws + L.rows);
+    P.part = reinterpret_cast<float4 *>(ws + L.part);
+    P.sub = reinterpret_cast<float4 *>(ws + L.sub);
+    P.sexact = reinterpret_cast<float4 *>(ws + L.sexact);
+    P.samp_list = reinterpret_cast<sv::SampInfo *>(ws + L.samp_list);
+    P.samp_count = reinterpret_cast<int *>(ws + L.samp_count);
+    P.k0 = 0;
+    P.k1 = K;
+    P.gz = reinterpret_cast<const float *>(ws + L.gz);
+    P.samp_t = ws + L.ct;
+    P.samp_d = ws + L.cd;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // 1. per-request set-up (lengths, greedy / sampled, the sampled-request count)
+    sv::sv_prep<<<1, sv::kPrepThreads, 0, s>>>(P);
+    // 2. the products of the target and draft rows; their epilogues leave the
+    //    row statistics (and the logit at each draft token) in the workspace
+    sv::LmStatsEpi et{P.part, reinterpret_cast<float *>(ws + L.gz), draft_tokens, temperature,
+                      P.npart, P.nslot, K, K + 1, 0, 0};
+    sv::LmStatsEpi ed = et;
+    ed.rows_per_req = K;
+    ed.slot0 = K + 1;
+    ed.tok_off = K + 1;
+    if (sv::g_prof_start) cudaEventRecord(sv::g_prof_start, s);
+    if (sv::launch_lm_gemm(tHt, tWt, B * (K + 1), nullptr, V, d, et, dev_status, *dv, s) != cudaSuccess ||
+        sv::launch_lm_gemm(tHd, tWd, B * K, nullptr, V, d, ed, dev_status, *dv, s) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    if (sv::g_prof_end) cudaEventRecord(sv::g_prof_end, s);
+    // 3. decisions; 4. the rows the sampled requests draw from, recomputed
+    sv::launch_dependent(sv::sv_decide<sv::kF32>, B, sv::kThreads, 0, s, P);
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)B);
+        cfg.blockDim = dim3(256);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, sv::lm_gather, P, static_cast<const uint16_t *>(hidden_target),
+                               static_cast<const uint16_t *>(hidden_draft), d,
+                               reinterpret_cast<uint16_t *>(ws + L.hct),
+                               reinterpret_cast<uint16_t *>(ws + L.hcd)) != cudaSuccess)
+            return SPEC_ERR_CUDA;
+    }
+    sv::LmStoreEpi st{reinterpret_cast<float *>(ws + L.ct)};
+    sv::LmStoreEpi sd{reinterpret_cast<float *>(ws + L.cd)};
+    if (sv::launch_lm_gemm(tCt, tWt, B, P.samp_count, V, d, st, dev_status, *dv, s) != cudaSuccess ||
+        sv::launch_lm_gemm(tCd, tWd, B, P.samp_count, V, d, sd, dev_status, *dv, s) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    // 5. residual / bonus masses and the inverse CDF over the recomputed rows
+    const bool vec = sv::vec_rows(V, SPEC_DTYPE_F32);
+    long long g2 = (long long)dv->sms * dv->occ_sample[sv::kF32][vec ? 1 : 0];
+    const long long g2_need = ((long long)B * P.nchunk + sv::kSWarps - 1) / sv::kSWarps;
+    if (g2 > g2_need) g2 = g2_need;
+    if (vec) {
+        sv::launch_dependent(sv::sv_sample<sv::kF32, true>, (int)g2, sv::kSWarps * 32, sv::kSSmem, s, P);
+        sv::launch_dependent(sv::sv_find<sv::kF32, true>, (B + sv::kFindWarps - 1) / sv::kFindWarps,
+                             sv::kFindWarps * 32, 0, s, P);
+    } else {
+        sv::launch_dependent(sv::sv_sample<sv::kF32, false>, (int)g2, sv::kSWarps * 32, 0, s, P);
+        sv::launch_dependent(sv::sv_find<sv::kF32, false>, (B + sv::kFindWarps - 1) / sv::kFindWarps,
+                             sv::kFindWarps * 32, 0, s, P);
+    }
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -1,0 +1,189 @@
+"""The LM-head path (spec_verify_lmhead) against the oracle: logits H W^T in
+float64 from the same bf16 hidden states and weights, then the oracle's
+verification of those logits.
+
+With small-integer inputs every partial sum of a logit is exact in float32, so
+the tensor-core product equals the float64 one and the step is held to the
+bars of the logits path: greedy bit-exact, sampled requests equal unless the
+oracle flags a near tie (at most one such difference).  With random inputs the
+float32 accumulation differs from the float64 product by rounding: the row
+statistics agree within 1e-5 relative, and greedy argmaxes are bit-exact
+wherever the top-two gap exceeds the accumulation bound."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_helpers import NEAR_TIE, REL_TOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sv():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import speculative_decoding_verification_69_gb300 as m
+    m.load_library()
+    return m
+
+
+def _oracle_logits(inp, b_idx=None):
+    """float64 logits of the target and draft rows (requests b_idx, or all)."""
+    ht, hd = inp["hidden_target"], inp["hidden_draft"]
+    if b_idx is not None:
+        ht, hd = ht[b_idx], hd[b_idx]
+    w = workloads.bf16_bits(inp["w"])
+    return oracle.lm_logits(workloads.bf16_bits(ht), w), oracle.lm_logits(workloads.bf16_bits(hd), w)
+
+
+def _run(sv, inp, debug=False):
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r = sv.verify_lmhead(inp["hidden_target"], inp["hidden_draft"], inp["w"], inp["w"],
+                         inp["tokens"], inp["verify_len"], inp["temperature"], inp["seed"],
+                         dev_status=st, debug=debug)
+    torch.cuda.synchronize()
+    return [x.cpu().numpy() for x in r] + [int(st.item())]
+
+
+def _compare(out, acc, r, T, idx=None):
+    """(greedy mismatches, sampled mismatches, unflagged sampled mismatches)."""
+    idx = range(len(acc)) if idx is None else idx
+    ng = ns = nu = 0
+    for i, b in enumerate(idx):
+        same = acc[b] == r["accept_len"][i] and np.array_equal(out[b], r["out_tokens"][i])
+        if same:
+            continue
+        if oracle.is_greedy(T[b]):
+            ng += 1
+        else:
+            ns += 1
+            if min(r["accept_margin"][i], r["cdf_margin"][i]) >= NEAR_TIE:
+                nu += 1
+    return ng, ns, nu
+
+
+@pytest.mark.parametrize("B,K,V,d,T,n_greedy", [
+    (8, 4, 1000, 64, 1.0, 2),       # one m tile, a ragged vocabulary tile
+    (16, 8, 4096, 128, 0.8, 4),     # 144 rows: two m tiles, the second ragged
+    (64, 8, 3000, 128, 1.0, 16),    # 576 rows: 4.5 m tiles
+    (6, 3, 2052, 192, 1.3, 0),      # 2052 = 8 tiles of 256 + 4
+    (3, 2, 32000, 256, 1.0, 1),     # many vocabulary tiles per row
+    (40, 16, 1024, 64, 0.7, 8),     # K = 16
+])
+def test_lmhead_exact_products_against_oracle(sv, B, K, V, d, T, n_greedy):
+    inp = workloads.make_lmhead_inputs(B, K, V, d, seed=B * 100 + K + V + d, T=T,
+                                       n_greedy=n_greedy, exact=True)
+    out, acc, st = _run(sv, inp)
+    assert st == 0
+    zt, zd = _oracle_logits(inp)
+    Tn = inp["temperature"].cpu().numpy()
+    r = oracle.verify(zt, zd, inp["tokens"].cpu().numpy(), inp["verify_len"].cpu().numpy(), Tn,
+                      inp["seed"])
+    ng, ns, nu = _compare(out, acc, r, Tn)
+    assert ng == 0 and nu == 0 and ns <= 1, (ng, ns, nu)
+    assert acc.max() >= 1  # some drafts are accepted
+
+
+def test_lmhead_ragged_lengths_and_bad_tokens(sv):
+    """Verify lengths below K, out of range (clamped) and draft tokens outside
+    [0, V) (the length is cut): the status bits and outputs of spec_verify's
+    rule, against the oracle."""
+    B, K, V, d = 12, 6, 1500, 64
+    inp = workloads.make_lmhead_inputs(B, K, V, d, seed=77, exact=True, n_greedy=3)
+    vl = torch.tensor([6, 0, 3, 9, -2, 6, 1, 5, 6, 2, 4, 6], dtype=torch.int32, device="cuda")
+    tok = inp["tokens"].clone()
+    tok[5, 2] = V + 7
+    tok[8, 0] = -1
+    inp.update(verify_len=vl, tokens=tok.contiguous())
+    out, acc, st = _run(sv, inp)
+    assert st & sv.DEV_BAD_LEN and st & sv.DEV_BAD_TOKEN
+    zt, zd = _oracle_logits(inp)
+    Tn = inp["temperature"].cpu().numpy()
+    r = oracle.verify(zt, zd, tok.cpu().numpy(), vl.cpu().numpy(), Tn, inp["seed"])
+    ng, ns, nu = _compare(out, acc, r, Tn)
+    assert ng == 0 and nu == 0 and ns <= 1
+
+
+def _accumulation_bound(h, w):
+    """Per logit, a bound on |fp32 tensor-core sum - exact sum|: at most
+    d/16 + 16 roundings of a float32 sum, each below 2^-24 of the sum of
+    |h_j w_vj| (h [M, d], w [V, d] as float64)."""
+    d = h.shape[1]
+    return (d / 16 + 16) * 2.0 ** -24 * (np.abs(h) @ np.abs(w).T)
+
+
+@pytest.mark.parametrize("B,K,V,d", [(12, 4, 8192, 512), (4, 8, 32000, 1024)])
+def test_lmhead_random_products_row_statistics(sv, B, K, V, d):
+    """Random normal inputs: row max, log-sum and p(x), q(x) within 1e-5
+    relative of the oracle's (on float64 logits); greedy requests bit-exact
+    wherever every row's top-two gap exceeds the accumulation bound; sampled
+    outputs within the valid range."""
+    inp = workloads.make_lmhead_inputs(B, K, V, d, seed=B + V + d, T=1.0, n_greedy=B // 2)
+    out, acc, rs, pr, st = _run(sv, inp, debug=True)
+    assert st == 0
+    zt, zd = _oracle_logits(inp)
+    Tn = inp["temperature"].cpu().numpy()
+    tok = inp["tokens"].cpu().numpy()
+    worst = 0.0
+    for b in range(B):
+        if oracle.is_greedy(Tn[b]):
+            continue
+        for k in range(K + 1):
+            rows = [(k, zt[b, k])] + ([(K + 1 + k, zd[b, k])] if k < K else [])
+            for slot, row in rows:
+                x = int(tok[b, k]) if k < K else -1
+                m, ls, px = oracle.row_intermediates(row, Tn[b], x)
+                gm, gls = rs[b, slot]
+                worst = max(worst, abs(gm - m) / max(abs(m), 1e-30), abs(gls - ls) / max(abs(ls), 1.0))
+                if k < K:
+                    gp = pr[b, k, 0 if slot <= K else 1]
+                    worst = max(worst, abs(gp - px) / max(abs(px), 1e-30))
+    assert worst < REL_TOL, worst
+    # greedy requests whose rows all have a clear top-two gap: bit-exact
+    w = workloads.bf16_bits(inp["w"]).astype(np.uint32) << 16
+    w = w.view(np.float32).astype(np.float64)
+    checked = 0
+    for b in range(B):
+        if not oracle.is_greedy(Tn[b]):
+            continue
+        h = (workloads.bf16_bits(inp["hidden_target"][b]).astype(np.uint32) << 16)
+        h = h.view(np.float32).astype(np.float64)
+        bound = _accumulation_bound(h, w)
+        clear = True
+        for k in range(K + 1):
+            o = np.argsort(-zt[b, k], kind="stable")
+            clear &= zt[b, k, o[0]] - zt[b, k, o[1]] > bound[k, o[0]] + bound[k, o[1]]
+        if not clear:
+            continue
+        ot = oracle.verify(zt[b:b + 1], zd[b:b + 1], tok, None, Tn, inp["seed"], b0=b, b1=b + 1,
+                           broadcast_rows=True)
+        assert acc[b] == ot["accept_len"][0] and np.array_equal(out[b], ot["out_tokens"][0]), b
+        checked += 1
+    assert checked >= 1
+    for b in range(B):
+        assert 0 <= acc[b] <= K and np.array_equal(out[b, :acc[b]], tok[b, :acc[b]])
+        assert 0 <= out[b, acc[b]] < V and (out[b, acc[b] + 1:] == -1).all()
+
+
+def test_lmhead_bench_shape_one_request(sv):
+    """The benchmark's shapes (B=32, K=8, V=151936, d=4096) with exact
+    products: the whole batch through the GPU path, the last request (its rows
+    in the last m tile) against the oracle, invariants on all."""
+    B, K, V, d = 32, 8, 151936, 4096
+    inp = workloads.make_lmhead_inputs(B, K, V, d, seed=4242, T=1.0, exact=True, n_greedy=8)
+    out, acc, st = _run(sv, inp)
+    assert st == 0
+    b = B - 1
+    zt, zd = _oracle_logits(inp, slice(b, b + 1))
+    Tn = inp["temperature"].cpu().numpy()
+    tok = inp["tokens"].cpu().numpy()
+    # request b with its own Philox index: the oracle reads the one request's
+    # logits for request b of the full token / temperature arrays
+    r = oracle.verify(zt, zd, tok, None, Tn, inp["seed"], b0=b, b1=b + 1, broadcast_rows=True)
+    same = acc[b] == r["accept_len"][0] and np.array_equal(out[b], r["out_tokens"][0])
+    flagged = min(r["accept_margin"][0], r["cdf_margin"][0]) < NEAR_TIE
+    assert same or flagged
+    for i in range(B):
+        assert 0 <= acc[i] <= K and np.array_equal(out[i, :acc[i]], tok[i, :acc[i]])
+        assert 0 <= out[i, acc[i]] < V and (out[i, acc[i] + 1:] == -1).all()

@@ -25,6 +25,8 @@ Workloads (sigma is a standard deviation):
 Draft tokens: multinomial draws from softmax(draft/T) of the (rounded) draft logits;
 argmax of the draft for greedy requests.
 """
+import math
+
 import torch
 
 BASE_SEED = 20261202
@@ -200,3 +202,75 @@ def to_numpy_logits(t):
     return t.numpy()
 
 
+
+
+# LM-head inputs: hidden sizes of the model families the vocabularies belong to
+# (Qwen3-8B 4096, Llama-3.1-8B 4096, gpt-oss 2880).
+LM_HIDDEN = {0: 256, 1: 4096, 2: 4096, 3: 4096, 4: 2880}
+
+
+def make_lmhead_inputs(B, K, V, d, seed=0, T=1.0, sigma=2.5, noise=0.5, n_greedy=0, exact=False,
+                       device="cuda"):
+    """Seeded inputs of the LM-head path: hidden_target [B, K+1, d],
+    hidden_draft [B, K, d], one shared weight w [V, d] (the drafter uses the
+    target's head), all bf16, with logits of standard deviation ~sigma and
+    draft logits ~ target + N(0, noise).  exact: small-integer hidden states
+    and weights of +-2^-s, so every partial sum of a logit is exactly
+    representable in float32 (the product's result does not depend on the
+    summation order).  T: one temperature (the first n_greedy requests greedy)
+    or a [B] tensor of them.  Draft tokens are drawn from the draft logits'
+    softmax at each request's T (argmax for greedy requests).  Returns
+    dict(hidden_target, hidden_draft, w, tokens, temperature, verify_len,
+    seed)."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev).manual_seed(int(seed))
+    if exact:
+        s = max(0, round(math.log2(math.sqrt(4.0 * d / 3.0) / sigma)))
+        ht = torch.randint(-2, 3, (B, K + 1, d), generator=g, device=dev).float()
+        w = torch.randint(-1, 2, (V, d), generator=g, device=dev).float() * (2.0 ** -s)
+        flip = torch.rand((B, K, d), generator=g, device=dev) < 0.1
+        step = torch.randint(-1, 2, (B, K, d), generator=g, device=dev).float()
+        hd = ht[:, :K] + torch.where(flip, step, torch.zeros_like(step))
+    else:
+        ht = torch.randn((B, K + 1, d), generator=g, device=dev)
+        w = torch.randn((V, d), generator=g, device=dev) * (sigma / math.sqrt(d))
+        hd = ht[:, :K] + torch.randn((B, K, d), generator=g, device=dev) * (noise / sigma)
+    ht, hd, w = ht.to(torch.bfloat16), hd.to(torch.bfloat16), w.to(torch.bfloat16)
+    if torch.is_tensor(T):  # per-request temperatures given
+        temp = T.to(device=dev, dtype=torch.float32).clone()
+    else:
+        temp = torch.full((B,), float(T), dtype=torch.float32, device=dev)
+        temp[:n_greedy] = 0.0
+    tokens = torch.empty((B, K), dtype=torch.int64, device=dev)
+    chunk = max(1, (1 << 26) // (K * V))
+    wf = w.float()
+    for b0 in range(0, B, chunk):
+        b1 = min(B, b0 + chunk)
+        z = hd[b0:b1].float() @ wf.t()
+        tb = temp[b0:b1].view(-1, 1, 1)
+        sampled = tb > 0
+        probs = torch.softmax(z / torch.where(sampled, tb, torch.ones_like(tb)), dim=-1)
+        draws = torch.multinomial(probs.view(-1, V), 1, generator=g).view(b1 - b0, K)
+        tokens[b0:b1] = torch.where(sampled.view(-1, 1), draws, z.argmax(dim=-1))
+    return dict(hidden_target=ht.contiguous(), hidden_draft=hd.contiguous(), w=w.contiguous(),
+                tokens=tokens.to(torch.int32).contiguous(), temperature=temp,
+                verify_len=torch.full((B,), K, dtype=torch.int32, device=dev), seed=int(seed) * 5 + 1)
+
+
+def workload_temperatures(cfg, B, device="cuda"):
+    """The per-request temperatures of workload cfg, drawn as make_inputs
+    draws them (c4: a quarter greedy, the others U(0, t_max])."""
+    c = CONFIGS[cfg]
+    dev = torch.device(device)
+    if c["T"] != "mixed":
+        return torch.full((B,), float(c["T"]), dtype=torch.float32, device=dev)
+    g = torch.Generator(device=dev).manual_seed(seed_for(cfg, 0) + 17)
+    temp = c["t_max"] * (1.0 - torch.rand((B,), generator=g, device=dev))
+    n_greedy = max(0, min(B, round(c["n_greedy"] * B / c["B"])))
+    temp[torch.randperm(B, generator=g, device=dev)[:n_greedy]] = 0.0
+    return temp.contiguous()
+
+
+def bf16_bits(t):
+    """Host copy of a bf16 tensor as its uint16 bit patterns."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
