@@ -167,17 +167,21 @@ __device__ __forceinline__ bool lm_wait(uint64_t *bar, uint32_t parity, volatile
 
 // ------------------------------------------------------------------ the kernel
 
-// Rows M = min(M_max, *M_dev) when M_dev is given (a count only the device
-// knows), else M_max.  Epi::row(r, valid, n0, V, taddr) is called by every
-// epilogue thread for each finished tile, convergently per warp (tcgen05.ld
-// is warp-collective): row r of the tile's rows (valid = r < M), the tile's
-// first vocabulary entry n0, and the TMEM address of the row's 256 fp32
-// accumulators (column j at taddr + j).  Columns at or past V and rows past M
-// hold zeros (the TMA fills them): Epi masks them.
+// The rows come in two segments with their own tensor maps: rows [0, M0) of
+// tmA0, then rows [0, M1) of tmA1 (M1 = 0: one segment), each cut into row
+// tiles of its own.  M0 = min(M0, mult * *M_dev) when M_dev is given (a count
+// only the device knows).  Epi::row(seg, r, valid, n0, V, taddr) is called by
+// every epilogue thread for each finished tile, convergently per warp
+// (tcgen05.ld is warp-collective): row r of segment seg (valid = r below the
+// segment's row count), the tile's first vocabulary entry n0, and the TMEM
+// address of the row's 256 fp32 accumulators (column j at taddr + j).
+// Columns at or past V and rows past the segment's count hold zeros (the TMA
+// fills them): Epi masks them.
 template <class Epi>
 __global__ void __launch_bounds__(kLmThreads, 1)
-    lm_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-            int M_max, const int *M_dev, int V, int d, Epi epi, uint32_t *status) {
+    lm_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+            const __grid_constant__ CUtensorMap tmB, int M0, int M1, const int *M_dev, int mult,
+            int V, int d, Epi epi, uint32_t *status) {
     extern __shared__ uint8_t lm_raw[];
     LmShared &sh = *reinterpret_cast<LmShared *>((reinterpret_cast<uintptr_t>(lm_raw) + 1023) &
                                                   ~(uintptr_t)1023);
@@ -194,7 +198,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         mbar_init(&sh.done, 1);
         sh.abort = 0;
         fence_mbar_init();
-        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmA0);
+        if (M1 > 0) tma_prefetch_map(&tmA1);
         tma_prefetch_map(&tmB);
     }
     if (warp == 1) {
@@ -206,9 +211,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     tc_fence_after();
     pdl_wait();  // a device-side row count comes from the previous kernel
     const uint32_t tmem = sh.tmem_base;
-    int M = M_max;
-    if (M_dev) M = min(M, *M_dev);
-    const int m_tiles = (M + kLmBM - 1) / kLmBM;
+    if (M_dev) M0 = min(M0, mult * *M_dev);
+    const int mt0 = (M0 + kLmBM - 1) / kLmBM;
+    const int m_tiles = mt0 + (M1 + kLmBM - 1) / kLmBM;
     const int n_tiles = (V + kLmBN - 1) / kLmBN;
     const int k_blocks = d / kLmBK;
     const int num_tiles = m_tiles * n_tiles;
@@ -219,12 +224,15 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             uint32_t it = 0;
             for (int tile = blockIdx.x; tile < num_tiles && !*abort; tile += gridDim.x) {
                 const int m_blk = tile % m_tiles, n_blk = tile / m_tiles;
+                const bool seg1 = m_blk >= mt0;
+                const CUtensorMap *ta = seg1 ? &tmA1 : &tmA0;
+                const int row0 = (seg1 ? m_blk - mt0 : m_blk) * kLmBM;
                 for (int kb = 0; kb < k_blocks; ++kb, ++it) {
                     const int s = (int)(it % kLmStages);
                     const uint32_t fill = it / kLmStages;
                     if (fill > 0 && !lm_wait(&sh.empty[s], (fill - 1) & 1u, abort)) break;
                     mbar_expect_tx(&sh.full[s], kLmBytesA + kLmBytesB);
-                    tma_load_2d(sh.a[s], &tmA, kb * kLmBK, m_blk * kLmBM, &sh.full[s]);
+                    tma_load_2d(sh.a[s], ta, kb * kLmBK, row0, &sh.full[s]);
                     tma_load_2d(sh.b[s], &tmB, kb * kLmBK, n_blk * kLmBN, &sh.full[s]);
                 }
             }
@@ -274,8 +282,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             tc_fence_after();
             const int m_blk = tile % m_tiles, n_blk = tile / m_tiles;
-            const int r = m_blk * kLmBM + r_in;
-            epi.row(r, r < M, n_blk * kLmBN, V,
+            const int seg = m_blk >= mt0 ? 1 : 0;
+            const int r = (seg ? m_blk - mt0 : m_blk) * kLmBM + r_in;
+            epi.row(seg, r, r < (seg ? M1 : M0), n_blk * kLmBN, V,
                     tmem + ((uint32_t)(q * 32) << 16) + buf * kLmBN);
             tc_fence_before();
             __syncwarp();

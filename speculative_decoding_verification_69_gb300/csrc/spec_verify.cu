@@ -106,8 +106,9 @@ struct Params {
                             // pass over the same rows at the same T): list target rows only
     // LM-head path (spec_verify_lmhead): the logits exist only inside the GEMM
     const float *gz;        // [B, nslot] logit of each row at its draft token, or null
-    const char *samp_t;     // [B, V] fp32: row li = the target row sampled by list entry li
-    const char *samp_d;     // [B, V] fp32: row li = its draft row (residual draws)
+    const char *samp_t;     // fp32 rows: list entry li's target draw row at samp_t + li * samp_stride rows
+    const char *samp_d;     // and its draft row (residual draws) at samp_d + li * samp_stride rows
+    int samp_stride;
 };
 
 __device__ __forceinline__ const char *row_ptr(const Params &P, int b, int slot, int esz) {
@@ -120,7 +121,8 @@ __device__ __forceinline__ const char *row_ptr(const Params &P, int b, int slot,
 // LM-head path, else the request's logit row.
 __device__ __forceinline__ const char *samp_row(const Params &P, int li, int b, int slot, int esz,
                                                 bool draft) {
-    if (P.samp_t) return (draft ? P.samp_d : P.samp_t) + (size_t)li * (size_t)P.V * esz;
+    if (P.samp_t)
+        return (draft ? P.samp_d : P.samp_t) + (size_t)li * (size_t)P.samp_stride * (size_t)P.V * esz;
     return row_ptr(P, b, slot, esz);
 }
 
@@ -2201,15 +2203,18 @@ struct LmStatsEpi {
     float *gz;
     const int32_t *tokens;
     const float *temperature;
-    int npart, nslot, K, rows_per_req, slot0, tok_off;
-    __device__ __forceinline__ void row(int r, bool valid, int n0, int V, uint32_t taddr) const {
+    int npart, nslot, K;
+    int rows_per_req[2], slot0[2], tok_off[2];  // per row segment (target rows, draft rows)
+    __device__ __forceinline__ void row(int seg, int r, bool valid, int n0, int V,
+                                        uint32_t taddr) const {
         int b = 0, slot = 0, x = -1;
         bool greedy = true;
         float c = 0.f;
-        if (valid) {
-            b = r / rows_per_req;
-            slot = slot0 + (r - b * rows_per_req);
-            const int tk = slot - tok_off;  // the draft token this row scores, if any
+        if (valid) {  // (selects, not indexing: the functor stays in registers)
+            const int rpr = seg ? rows_per_req[1] : rows_per_req[0];
+            b = r / rpr;
+            slot = (seg ? slot0[1] : slot0[0]) + (r - b * rpr);
+            const int tk = slot - (seg ? tok_off[1] : tok_off[0]);  // the draft token this row scores
             if (tk >= 0 && tk < K) x = tokens[(size_t)b * K + tk];
             const float T = temperature[b];
             greedy = !(isfinite(T) && T >= FLT_MIN);
@@ -2230,10 +2235,18 @@ struct LmStatsEpi {
                 for (int i = 0; i < 32; ++i)
                     if (nb + i >= V) v[i] = -INFINITY;
             }
-            if (x >= nb && x < nb + 32) {
+            if (x >= nb && x < nb + 32) {  // a binary select tree, no indexed local copy of v
+                const int o = x - nb;
+                float t16[16], t8[8], t4[4], t2[2];
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (x - nb == i) g = v[i];
+                for (int i = 0; i < 16; ++i) t16[i] = (o & 1) ? v[2 * i + 1] : v[2 * i];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) t8[i] = (o & 2) ? t16[2 * i + 1] : t16[2 * i];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) t4[i] = (o & 4) ? t8[2 * i + 1] : t8[2 * i];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) t2[i] = (o & 8) ? t4[2 * i + 1] : t4[2 * i];
+                g = (o & 16) ? t2[1] : t2[0];
                 have_g = true;
             }
             float cm = v[0];
@@ -2276,9 +2289,10 @@ struct LmStatsEpi {
 // Store epilogue: the rows themselves (fp32), for the few rows the sampler
 // draws from, recomputed after the decisions.
 struct LmStoreEpi {
-    float *out;  // [rows, V]
-    __device__ __forceinline__ void row(int r, bool valid, int n0, int V, uint32_t taddr) const {
-        float *o = out + (size_t)r * (size_t)V;
+    float *out[2];  // [rows, V] per row segment
+    __device__ __forceinline__ void row(int seg, int r, bool valid, int n0, int V,
+                                        uint32_t taddr) const {
+        float *o = (seg ? out[1] : out[0]) + (size_t)r * (size_t)V;
 #pragma unroll 1
         for (int j = 0; j < kLmBN / 32; ++j) {
             float v[32];
@@ -2300,10 +2314,11 @@ struct LmStoreEpi {
 };
 
 // The hidden states of each sampled request's draw rows, packed by its entry
-// in the sampled-request list (target row a or L; draft row a for a residual
-// draw, zeros for a bonus draw), for the recompute of those rows.
+// li in the sampled-request list (target row a or L; draft row a for a
+// residual draw, zeros for a bonus draw), for the recompute of those rows:
+// target row at hct + li * stride rows, draft row at hcd + li * stride rows.
 __global__ void __launch_bounds__(256) lm_gather(Params P, const uint16_t *ht, const uint16_t *hd,
-                                                  int d, uint16_t *hct, uint16_t *hcd) {
+                                                  int d, uint16_t *hct, uint16_t *hcd, int stride) {
     pdl_wait();  // the list comes from sv_decide
     pdl_trigger();
     const int li = blockIdx.x;
@@ -2311,9 +2326,9 @@ __global__ void __launch_bounds__(256) lm_gather(Params P, const uint16_t *ht, c
     const SampInfo si = P.samp_list[li];
     const int K = P.K, nv = d / 8;
     const uint4 *st = reinterpret_cast<const uint4 *>(ht + ((size_t)si.b * (K + 1) + si.slot_t) * d);
-    uint4 *dt = reinterpret_cast<uint4 *>(hct + (size_t)li * d);
+    uint4 *dt = reinterpret_cast<uint4 *>(hct + (size_t)li * stride * d);
     for (int i = threadIdx.x; i < nv; i += blockDim.x) dt[i] = st[i];
-    uint4 *dd = reinterpret_cast<uint4 *>(hcd + (size_t)li * d);
+    uint4 *dd = reinterpret_cast<uint4 *>(hcd + (size_t)li * stride * d);
     if (si.mode == 1) {
         const uint4 *sd =
             reinterpret_cast<const uint4 *>(hd + ((size_t)si.b * K + (si.slot_d - K - 1)) * d);
@@ -2630,7 +2645,7 @@ static void launch_confidence(const Params &P, const DevInfo &d, cudaStream_t s,
 static size_t npart_lm(int V) { return (size_t)((V + kLmBN - 1) / kLmBN); }
 
 struct LmLayout {
-    size_t req, row_count, rows, part, sub, sexact, samp_list, samp_count, gz, hct, hcd, ct, cd, total;
+    size_t req, row_count, rows, part, sub, sexact, samp_list, samp_count, gz, hc, crow, total;
 };
 
 static LmLayout layout_lm(int B, int K, int V, int d) {
@@ -2646,10 +2661,8 @@ static LmLayout layout_lm(int B, int K, int V, int d) {
     L.samp_list = off; off = align256(off + sizeof(SampInfo) * (size_t)B);
     L.samp_count = off; off = align256(off + sizeof(int));
     L.gz = off; off = align256(off + sizeof(float) * (size_t)B * nslot);
-    L.hct = off; off = align256(off + 2 * (size_t)B * (size_t)d);
-    L.hcd = off; off = align256(off + 2 * (size_t)B * (size_t)d);
-    L.ct = off; off = align256(off + 4 * (size_t)B * (size_t)V);
-    L.cd = off; off = align256(off + 4 * (size_t)B * (size_t)V);
+    L.hc = off; off = align256(off + 2 * 2 * (size_t)B * (size_t)d);    // 2B hidden rows, bf16
+    L.crow = off; off = align256(off + 4 * 2 * (size_t)B * (size_t)V);  // 2B logit rows, fp32
     L.total = off;
     return L;
 }
@@ -2684,11 +2697,16 @@ static bool make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t rows, uin
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One product over up to two row segments (rows [0, M0) of tA0, rows [0, M1)
+// of tA1) against the weights of tB; M0 is capped on the device at
+// mult * *M_dev when M_dev is given.
 template <class Epi>
-static cudaError_t launch_lm_gemm(const CUtensorMap &tA, const CUtensorMap &tB, int M_max,
-                                  const int *M_dev, int V, int d, const Epi &epi, uint32_t *status,
+static cudaError_t launch_lm_gemm(const CUtensorMap &tA0, const CUtensorMap &tA1,
+                                  const CUtensorMap &tB, int M0, int M1, const int *M_dev,
+                                  int mult, int V, int d, const Epi &epi, uint32_t *status,
                                   const DevInfo &dv, cudaStream_t s) {
-    const long long tiles = ((long long)(M_max + kLmBM - 1) / kLmBM) * ((V + kLmBN - 1) / kLmBN);
+    const long long tiles = ((long long)(M0 + kLmBM - 1) / kLmBM + (M1 + kLmBM - 1) / kLmBM) *
+                            ((V + kLmBN - 1) / kLmBN);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(tiles < dv.sms ? (tiles > 0 ? tiles : 1) : dv.sms));
     cfg.blockDim = dim3(kLmThreads);
@@ -2699,7 +2717,8 @@ static cudaError_t launch_lm_gemm(const CUtensorMap &tA, const CUtensorMap &tB, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, lm_gemm<Epi>, tA, tB, M_max, M_dev, V, d, epi, status);
+    return cudaLaunchKernelEx(&cfg, lm_gemm<Epi>, tA0, tA1, tB, M0, M1, M_dev, mult, V, d, epi,
+                              status);
 }
 
 static bool lm_setup(DevInfo &d) {
@@ -2859,17 +2878,22 @@ spec_status_t spec_verify_lmhead(const void *hidden_target, const void *hidden_d
     sv::DevInfo *dv = sv::dev_info();
     if (!dv || !sv::lm_setup(*dv)) return SPEC_ERR_CUDA;
     char *ws = static_cast<char *>(workspace);
-    CUtensorMap tHt, tHd, tWt, tWd, tCt, tCd;
+    // the drafter shares the target's head: one product over both row sets
+    // (the weights stream once), and one recompute over interleaved rows
+    const bool shared = w_target == w_draft;
+    uint16_t *hc = reinterpret_cast<uint16_t *>(ws + L.hc);
+    float *crow = reinterpret_cast<float *>(ws + L.crow);
+    CUtensorMap tHt, tHd, tWt, tWd, tC0, tC1;
     if (!sv::make_tmap_bf16(&tHt, hidden_target, (uint64_t)B * (K + 1), (uint64_t)d, sv::kLmBM) ||
         !sv::make_tmap_bf16(&tHd, hidden_draft, (uint64_t)B * K, (uint64_t)d, sv::kLmBM) ||
         !sv::make_tmap_bf16(&tWt, w_target, (uint64_t)V, (uint64_t)d, sv::kLmBN) ||
         !sv::make_tmap_bf16(&tWd, w_draft, (uint64_t)V, (uint64_t)d, sv::kLmBN) ||
-        !sv::make_tmap_bf16(&tCt, ws + L.hct, (uint64_t)B, (uint64_t)d, sv::kLmBM) ||
-        !sv::make_tmap_bf16(&tCd, ws + L.hcd, (uint64_t)B, (uint64_t)d, sv::kLmBM))
+        !sv::make_tmap_bf16(&tC0, hc, (uint64_t)(shared ? 2 * B : B), (uint64_t)d, sv::kLmBM) ||
+        !sv::make_tmap_bf16(&tC1, hc + (size_t)B * d, (uint64_t)B, (uint64_t)d, sv::kLmBM))
         return SPEC_ERR_CUDA;
     sv::Params P{};
-    P.tgt = ws + L.ct;  // no logit row is read in place on this path
-    P.drf = ws + L.cd;
+    P.tgt = ws + L.crow;  // no logit row is read in place on this path
+    P.drf = ws + L.crow;
     P.tokens = draft_tokens;
     P.verify_len = verify_len;
     P.temperature = temperature;
@@ -2896,23 +2920,31 @@ spec_status_t spec_verify_lmhead(const void *hidden_target, const void *hidden_d
     P.k0 = 0;
     P.k1 = K;
     P.gz = reinterpret_cast<const float *>(ws + L.gz);
-    P.samp_t = ws + L.ct;
-    P.samp_d = ws + L.cd;
+    P.samp_t = reinterpret_cast<const char *>(crow);
+    P.samp_d = reinterpret_cast<const char *>(shared ? crow + V : crow + (size_t)B * V);
+    P.samp_stride = shared ? 2 : 1;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // 1. per-request set-up (lengths, greedy / sampled, the sampled-request count)
     sv::sv_prep<<<1, sv::kPrepThreads, 0, s>>>(P);
     // 2. the products of the target and draft rows; their epilogues leave the
     //    row statistics (and the logit at each draft token) in the workspace
-    sv::LmStatsEpi et{P.part, reinterpret_cast<float *>(ws + L.gz), draft_tokens, temperature,
-                      P.npart, P.nslot, K, K + 1, 0, 0};
-    sv::LmStatsEpi ed = et;
-    ed.rows_per_req = K;
-    ed.slot0 = K + 1;
-    ed.tok_off = K + 1;
+    sv::LmStatsEpi ep{P.part, reinterpret_cast<float *>(ws + L.gz), draft_tokens, temperature,
+                      P.npart, P.nslot, K, {K + 1, K}, {0, K + 1}, {0, K + 1}};
+    sv::LmStatsEpi ed = ep;  // the draft rows as segment 0 of a launch of their own
+    ed.rows_per_req[0] = K;
+    ed.slot0[0] = K + 1;
+    ed.tok_off[0] = K + 1;
     if (sv::g_prof_start) cudaEventRecord(sv::g_prof_start, s);
-    if (sv::launch_lm_gemm(tHt, tWt, B * (K + 1), nullptr, V, d, et, dev_status, *dv, s) != cudaSuccess ||
-        sv::launch_lm_gemm(tHd, tWd, B * K, nullptr, V, d, ed, dev_status, *dv, s) != cudaSuccess)
+    if (shared) {
+        if (sv::launch_lm_gemm(tHt, tHd, tWt, B * (K + 1), B * K, nullptr, 1, V, d, ep, dev_status,
+                               *dv, s) != cudaSuccess)
+            return SPEC_ERR_CUDA;
+    } else if (sv::launch_lm_gemm(tHt, tHt, tWt, B * (K + 1), 0, nullptr, 1, V, d, ep, dev_status,
+                                  *dv, s) != cudaSuccess ||
+               sv::launch_lm_gemm(tHd, tHd, tWd, B * K, 0, nullptr, 1, V, d, ed, dev_status, *dv,
+                                  s) != cudaSuccess) {
         return SPEC_ERR_CUDA;
+    }
     if (sv::g_prof_end) cudaEventRecord(sv::g_prof_end, s);
     // 3. decisions; 4. the rows the sampled requests draw from, recomputed
     sv::launch_dependent(sv::sv_decide<sv::kF32>, B, sv::kThreads, 0, s, P);
@@ -2927,16 +2959,23 @@ spec_status_t spec_verify_lmhead(const void *hidden_target, const void *hidden_d
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         if (cudaLaunchKernelEx(&cfg, sv::lm_gather, P, static_cast<const uint16_t *>(hidden_target),
-                               static_cast<const uint16_t *>(hidden_draft), d,
-                               reinterpret_cast<uint16_t *>(ws + L.hct),
-                               reinterpret_cast<uint16_t *>(ws + L.hcd)) != cudaSuccess)
+                               static_cast<const uint16_t *>(hidden_draft), d, hc,
+                               shared ? hc + d : hc + (size_t)B * d, shared ? 2 : 1) != cudaSuccess)
             return SPEC_ERR_CUDA;
     }
-    sv::LmStoreEpi st{reinterpret_cast<float *>(ws + L.ct)};
-    sv::LmStoreEpi sd{reinterpret_cast<float *>(ws + L.cd)};
-    if (sv::launch_lm_gemm(tCt, tWt, B, P.samp_count, V, d, st, dev_status, *dv, s) != cudaSuccess ||
-        sv::launch_lm_gemm(tCd, tWd, B, P.samp_count, V, d, sd, dev_status, *dv, s) != cudaSuccess)
-        return SPEC_ERR_CUDA;
+    if (shared) {  // rows 2 li (target) and 2 li + 1 (draft), 2 * count of them
+        sv::LmStoreEpi st{{crow, crow}};
+        if (sv::launch_lm_gemm(tC0, tC0, tWt, 2 * B, 0, P.samp_count, 2, V, d, st, dev_status, *dv,
+                               s) != cudaSuccess)
+            return SPEC_ERR_CUDA;
+    } else {
+        sv::LmStoreEpi st{{crow, crow}}, sd{{crow + (size_t)B * V, crow + (size_t)B * V}};
+        if (sv::launch_lm_gemm(tC0, tC0, tWt, B, 0, P.samp_count, 1, V, d, st, dev_status, *dv, s) !=
+                cudaSuccess ||
+            sv::launch_lm_gemm(tC1, tC1, tWd, B, 0, P.samp_count, 1, V, d, sd, dev_status, *dv, s) !=
+                cudaSuccess)
+            return SPEC_ERR_CUDA;
+    }
     // 5. residual / bonus masses and the inverse CDF over the recomputed rows
     const bool vec = sv::vec_rows(V, SPEC_DTYPE_F32);
     long long g2 = (long long)dv->sms * dv->occ_sample[sv::kF32][vec ? 1 : 0];

@@ -187,3 +187,29 @@ def test_lmhead_bench_shape_one_request(sv):
     for i in range(B):
         assert 0 <= acc[i] <= K and np.array_equal(out[i, :acc[i]], tok[i, :acc[i]])
         assert 0 <= out[i, acc[i]] < V and (out[i, acc[i] + 1:] == -1).all()
+
+
+@pytest.mark.parametrize("B,K,V,d", [(16, 8, 4096, 128), (40, 4, 2052, 64)])
+def test_lmhead_separate_draft_head(sv, B, K, V, d):
+    """A drafter with a head of its own (w_draft a different matrix): the
+    target and draft rows take separate products and separate recomputes;
+    exact products against the oracle with each head."""
+    inp = workloads.make_lmhead_inputs(B, K, V, d, seed=B * 3 + V, T=0.9, n_greedy=B // 4,
+                                       exact=True)
+    g = torch.Generator(device="cuda").manual_seed(B + d)
+    s = inp["w"].float().abs().max().item()  # the target head's step (2^-s)
+    wd = (torch.randint(-1, 2, (V, d), generator=g, device="cuda").float() * s).to(torch.bfloat16)
+    wd = torch.where(torch.rand((V, d), generator=g, device="cuda") < 0.8, inp["w"], wd).contiguous()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, acc = sv.verify_lmhead(inp["hidden_target"], inp["hidden_draft"], inp["w"], wd,
+                                inp["tokens"], inp["verify_len"], inp["temperature"], inp["seed"],
+                                dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    zt = oracle.lm_logits(workloads.bf16_bits(inp["hidden_target"]), workloads.bf16_bits(inp["w"]))
+    zd = oracle.lm_logits(workloads.bf16_bits(inp["hidden_draft"]), workloads.bf16_bits(wd))
+    Tn = inp["temperature"].cpu().numpy()
+    r = oracle.verify(zt, zd, inp["tokens"].cpu().numpy(), inp["verify_len"].cpu().numpy(), Tn,
+                      inp["seed"])
+    ng, ns, nu = _compare(out.cpu().numpy(), acc.cpu().numpy(), r, Tn)
+    assert ng == 0 and nu == 0 and ns <= 1, (ng, ns, nu)
