@@ -326,8 +326,8 @@ def parity_counts(o_host, a_host, r, T, window=1e-6):
 
 # ---------------------------------------------------------------- GPU arm
 
-def prepare(cfg, rank, device):
-    inp = workloads.make_inputs(cfg, rep=rank, device=device)
+def prepare(cfg, rank, device, batch=None):
+    inp = workloads.make_inputs(cfg, rep=rank, device=device, B=batch)
     if "draft_maxprob" in inp:
         import speculative_decoding_verification_69_gb300 as sv
         inp["verify_len"] = sv.schedule_len(inp["draft_maxprob"], inp["threshold"])
@@ -727,7 +727,7 @@ def run_ours(args, world, rank, local):
     sv.load_library()
     dev = torch.device("cuda", local)
     cfg = args.config
-    inp = prepare(cfg, rank, dev)
+    inp = prepare(cfg, rank, dev, args.batch)
     B, K1, V = inp["target"].shape
     K = K1 - 1
     esz = inp["target"].element_size()
@@ -924,7 +924,8 @@ def run_ours(args, world, rank, local):
         "dtype": "bf16" if inp["target"].dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded logits; no datasets or trained weights)",
         "config": {
-            "workload": workloads.NAMES[cfg],
+            "workload": workloads.NAMES[cfg] + ("" if args.batch is None else
+                                                " shapes with B=%d" % B),
             "B": B, "K": K, "V": V,
             "verified_positions_per_step": positions,
             "logit_bytes_per_step": alg_bytes,
@@ -1040,6 +1041,9 @@ def main(argv=None):
     ap.add_argument("--distinct", action="store_true",
                     help="with --tree-sampled: siblings drawn without replacement (top-k style), "
                          "verified by spec_verify_tree_distinct")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="requests per step instead of the workload's B (smaller cases of the same "
+                         "shapes, for profiler captures); the bench line then names the batch")
     ap.add_argument("--lmhead", action="store_true",
                     help="hidden states and LM-head weights in: the product on the tensor cores "
                          "with the row statistics in its epilogue (spec_verify_lmhead)")
