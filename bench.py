@@ -712,7 +712,7 @@ def run_lmhead(args, world, rank, local):
         "e2e": {"value": sum_over_ranks(positions * e2e_steps, world) / e2e_s, "unit": "positions/s",
                 "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
                 "d2h_bytes_per_step": (h_out.numel() + h_acc.numel()) * 4, "steps": e2e_steps},
-        "gpu_launches": 9 * args.steps, "clocks": clk,
+        "gpu_launches": 7 * args.steps, "clocks": clk,  # shared head: 7 kernels per call
         "accept_len_hist": [int(x) for x in np.bincount(a_host, minlength=K + 1)],
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

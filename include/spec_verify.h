@@ -373,7 +373,9 @@ spec_status_t spec_verify_scheduled(const void *target_logits, const void *draft
  *   per sampled request) are multiplied again after the decisions, into the
  *   workspace.  row_stats / probs: as spec_verify_debug (nullable).
  *   workspace: spec_lmhead_workspace_bytes(B, K, V, d) bytes, 256-byte
- *   aligned (it holds 8 B V bytes of recomputed rows).  Launches 9 kernels.
+ *   aligned (it holds 8 B V bytes of recomputed rows).  Launches 7 kernels when
+ *   w_target == w_draft (the target and draft rows share one product launch
+ *   and one recompute), 9 otherwise.
  */
 size_t spec_lmhead_workspace_bytes(int B, int K, int V, int d);
 spec_status_t spec_verify_lmhead(const void *hidden_target, const void *hidden_draft,

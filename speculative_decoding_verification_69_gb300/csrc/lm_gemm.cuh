@@ -149,15 +149,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Bounded wait that also gives up as soon as another role of the CTA has.
-__device__ __forceinline__ bool lm_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+// Bounded wait (limit_ns) that also gives up as soon as another role of the
+// CTA has.
+__device__ __forceinline__ bool lm_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                        unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort) return false;
-            if (global_ns() - t0 > kLmWaitNs) {
+            if (global_ns() - t0 > limit_ns) {
                 *abort = 1;
                 return false;
             }
@@ -176,12 +178,15 @@ __device__ __forceinline__ bool lm_wait(uint64_t *bar, uint32_t parity, volatile
 // segment's row count), the tile's first vocabulary entry n0, and the TMEM
 // address of the row's 256 fp32 accumulators (column j at taddr + j).
 // Columns at or past V and rows past the segment's count hold zeros (the TMA
-// fills them): Epi masks them.
+// fills them): Epi masks them.  diag (diagnostics only): the producer issues
+// no copy, so the first wait on a stage runs out after diag_ns and the CTA
+// gives up as on a real timeout.
 template <class Epi>
 __global__ void __launch_bounds__(kLmThreads, 1)
     lm_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
             const __grid_constant__ CUtensorMap tmB, int M0, int M1, const int *M_dev, int mult,
-            int V, int d, Epi epi, uint32_t *status) {
+            int V, int d, Epi epi, uint32_t *status, int diag, unsigned long long diag_ns) {
+    const unsigned long long limit_ns = diag ? diag_ns : kLmWaitNs;
     extern __shared__ uint8_t lm_raw[];
     LmShared &sh = *reinterpret_cast<LmShared *>((reinterpret_cast<uintptr_t>(lm_raw) + 1023) &
                                                   ~(uintptr_t)1023);
@@ -230,7 +235,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
                 for (int kb = 0; kb < k_blocks; ++kb, ++it) {
                     const int s = (int)(it % kLmStages);
                     const uint32_t fill = it / kLmStages;
-                    if (fill > 0 && !lm_wait(&sh.empty[s], (fill - 1) & 1u, abort)) break;
+                    if (fill > 0 && !lm_wait(&sh.empty[s], (fill - 1) & 1u, abort, limit_ns)) break;
+                    if (diag) break;  // nothing is copied: the consumers' waits run out
                     mbar_expect_tx(&sh.full[s], kLmBytesA + kLmBytesB);
                     tma_load_2d(sh.a[s], ta, kb * kLmBK, row0, &sh.full[s]);
                     tma_load_2d(sh.b[s], &tmB, kb * kLmBK, n_blk * kLmBN, &sh.full[s]);
@@ -247,13 +253,13 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             uint32_t it = 0, tcount = 0;
             for (int tile = blockIdx.x; tile < num_tiles && !*abort; tile += gridDim.x, ++tcount) {
                 const uint32_t buf = tcount & 1u, use = tcount >> 1;
-                if (use > 0 && !lm_wait(&sh.acc_empty[buf], (use - 1) & 1u, abort)) break;
+                if (use > 0 && !lm_wait(&sh.acc_empty[buf], (use - 1) & 1u, abort, limit_ns)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + buf * kLmBN;
                 bool ok = true;
                 for (int kb = 0; kb < k_blocks; ++kb, ++it) {
                     const int s = (int)(it % kLmStages);
-                    if (!lm_wait(&sh.full[s], (it / kLmStages) & 1u, abort)) {
+                    if (!lm_wait(&sh.full[s], (it / kLmStages) & 1u, abort, limit_ns)) {
                         ok = false;
                         break;
                     }
@@ -278,7 +284,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         uint32_t tcount = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tcount) {
             const uint32_t buf = tcount & 1u, use = tcount >> 1;
-            const bool ok = lm_wait(&sh.acc_full[buf], use & 1u, abort);
+            const bool ok = lm_wait(&sh.acc_full[buf], use & 1u, abort, limit_ns);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             tc_fence_after();
             const int m_blk = tile % m_tiles, n_blk = tile / m_tiles;

@@ -2718,7 +2718,7 @@ static cudaError_t launch_lm_gemm(const CUtensorMap &tA0, const CUtensorMap &tA1
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, lm_gemm<Epi>, tA0, tA1, tB, M0, M1, M_dev, mult, V, d, epi,
-                              status);
+                              status, g_diag_timeout ? 1 : 0, kDiagWaitNs);
 }
 
 static bool lm_setup(DevInfo &d) {

@@ -213,3 +213,31 @@ def test_lmhead_separate_draft_head(sv, B, K, V, d):
                       inp["seed"])
     ng, ns, nu = _compare(out.cpu().numpy(), acc.cpu().numpy(), r, Tn)
     assert ng == 0 and nu == 0 and ns <= 1, (ng, ns, nu)
+
+
+def test_lmhead_bounded_waits_run_out(sv):
+    """The product's failure path without a fault: under the diagnostic switch
+    the producer copies nothing, every CTA's bounded wait runs out (1 ms),
+    SPEC_DEV_TIMEOUT is reported, the TMEM is freed and the call returns; the
+    next call, with the switch off, is correct."""
+    B, K, V, d = 8, 4, 1000, 64
+    inp = workloads.make_lmhead_inputs(B, K, V, d, seed=515, exact=True, n_greedy=2)
+    ws = torch.zeros(sv.lmhead_workspace_bytes(B, K, V, d), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sv.force_wait_timeout(True)
+    try:
+        sv.verify_lmhead(inp["hidden_target"], inp["hidden_draft"], inp["w"], inp["w"],
+                         inp["tokens"], inp["verify_len"], inp["temperature"], inp["seed"],
+                         dev_status=st, workspace=ws)
+        torch.cuda.synchronize()
+    finally:
+        sv.force_wait_timeout(False)
+    assert int(st.item()) & sv.DEV_TIMEOUT
+    out, acc, st2 = _run(sv, inp)
+    assert st2 == 0
+    zt, zd = _oracle_logits(inp)
+    Tn = inp["temperature"].cpu().numpy()
+    r = oracle.verify(zt, zd, inp["tokens"].cpu().numpy(), inp["verify_len"].cpu().numpy(), Tn,
+                      inp["seed"])
+    ng, ns, nu = _compare(out, acc, r, Tn)
+    assert ng == 0 and nu == 0 and ns <= 1
