@@ -39,6 +39,24 @@ def test_uniform_mapping(oracle):
     assert abs(np.mean(us) - 0.5) < 0.03
 
 
+def test_uniform_mapping_from_known_answers(oracle):
+    """The acceptance uniform of (seed 0, request 0, position 0) is the first
+    known-answer vector's word 0 (counter and key all zero, read from the
+    golden fixture, not from the oracle's generator) shifted to 24 bits; the
+    acceptance uniforms lie on the 2^-24 grid and the sampling uniforms are
+    uniform on [0, 1) (Kolmogorov-Smirnov)."""
+    lhs, rhs = golden_lines("philox4x32_10_kat.txt")[0].split("->")
+    assert [int(x, 16) for x in lhs.split()] == [0] * 6
+    w0 = int(rhs.split()[0], 16)
+    assert oracle.u_accept(0, 0, 0) == (w0 >> 8) * 2.0 ** -24
+    ua = np.array([oracle.u_accept(99, b, k) for b in range(200) for k in range(8)])
+    assert np.all(ua * 2.0 ** 24 == np.floor(ua * 2.0 ** 24))
+    stats = pytest.importorskip("scipy.stats")
+    us = np.array([oracle.u_sample(2026, b, k) for b in range(4000) for k in range(5)])
+    assert stats.kstest(us, "uniform").pvalue > 1e-3
+    assert len(np.unique(us)) == us.size
+
+
 # ---------------------------------------------------------------- hand rule
 
 def _logp(p):
