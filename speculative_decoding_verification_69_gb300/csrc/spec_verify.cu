@@ -222,15 +222,10 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
             const float T = P.temperature[b];
             if (L < 0) { L = 0; st |= SPEC_DEV_BAD_LEN; }
             if (L > P.K) { L = P.K; st |= SPEC_DEV_BAD_LEN; }
-            // all token loads issued before any is checked
-            int tok[SPEC_MAX_K];
-#pragma unroll
-            for (int k = 0; k < SPEC_MAX_K; ++k) tok[k] = k < L ? P.tokens[(size_t)b * P.K + k] : 0;
-            int Lv = L;
-#pragma unroll
-            for (int k = SPEC_MAX_K - 1; k >= 0; --k)
-                if (k < L && (tok[k] < 0 || tok[k] >= P.V)) Lv = k;
-            if (Lv < L) { L = Lv; st |= SPEC_DEV_BAD_TOKEN; }
+            // (a draft token outside [0, V) cuts the length further; sv_decide
+            // applies that cut, so the rows listed here may include a few the
+            // step then ignores, and this kernel, which the statistics pass
+            // waits for, loads no tokens)
             greedy = !(isfinite(T) && T >= FLT_MIN);
             ReqInfo ri;
             ri.L = L;
@@ -649,12 +644,15 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
     __shared__ int s_a;
     // inputs and sv_prep's results (two kernels back) may be read before the wait
     const ReqInfo rq = P.req[b];
-    const int L = rq.L;
     const bool greedy = rq.greedy != 0;
-    int x = 0;
+    // the first draft token outside [0, V) cuts the verify length (every warp
+    // forms the cut itself from the tokens; the status bit from warp 0)
+    const int x = lane < rq.L ? P.tokens[(size_t)b * K + lane] : 0;
+    const unsigned bad = __ballot_sync(0xFFFFFFFFu, lane < rq.L && (x < 0 || x >= P.V));
+    const int L = bad ? __ffs(bad) - 1 : rq.L;
+    if (bad && tid == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_BAD_TOKEN);
     float g = 0.f, gd = 0.f, u = 0.f;
     if (warp == 0 && lane < L) {
-        x = P.tokens[(size_t)b * K + lane];
         if (!greedy) {
             if (!P.gz) {
                 g = load_logit(row_ptr(P, b, lane, Fmt<DT>::kESZ), DT, x);
@@ -739,8 +737,11 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
         }
         const unsigned rej = ~__ballot_sync(0xFFFFFFFFu, acc);
         // first rejection; with none, the request ends at L if this wave
-        // reaches it, else it stays open for the next wave (-1)
-        const int a = rej ? min(__ffs(rej) - 1, L) : (L <= P.k1 ? L : -1);
+        // listed target row L (the last row sv_prep listed is t1, from the
+        // length before the bad-token cut), else it stays open for the next
+        // wave (-1)
+        const int t1 = rq.L <= P.k1 ? rq.L : P.k1 - 1;
+        const int a = rej ? min(__ffs(rej) - 1, L) : (L <= t1 ? L : -1);
         if (lane == 0) s_a = a;
     }
     __syncthreads();

@@ -84,3 +84,36 @@ def test_tree_walk_wait_timeout_is_reported():
     torch.cuda.synchronize()
     assert int(st2.item()) == 0
     assert torch.equal(o1, o2) and torch.equal(n1, n2) and torch.equal(a1, a2)
+
+
+def test_bad_tokens_at_the_wave_boundary():
+    """Draft tokens outside [0, V) at positions W - 1, W and W + 1 of a
+    two-wave call (the cut is applied by the decision kernel, after the rows
+    were listed from the clamped lengths): a poisoned workspace gives the
+    outputs and status of a clean single-pass call, which match the oracle."""
+    import speculative_decoding_verification_69_gb300 as sv
+    inp = workloads.make_inputs(2, rep=29, B=48)
+    B, K = inp["tokens"].shape
+    V = inp["target"].shape[2]
+    W = 4
+    tok = inp["tokens"].clone()
+    for b in range(0, B, 4):
+        tok[b, W - 1 + (b // 4) % 3] = V + b  # W - 1, W or W + 1
+    inp["tokens"] = tok.contiguous()
+    st1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o1, a1 = sv.Verifier()(inp["target"], inp["draft"], inp["tokens"], inp["verify_len"],
+                           inp["temperature"], inp["seed"], dev_status=st1)
+    v = sv.Verifier()
+    ws, n = v.workspace(B, K, V, inp["target"].dtype, inp["target"].device)
+    ws.fill_(0xFF)
+    st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o2, a2 = v(inp["target"], inp["draft"], inp["tokens"], inp["verify_len"], inp["temperature"],
+               inp["seed"], early_exit=W, dev_status=st2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(a1, a2)
+    assert int(st1.item()) & sv.DEV_BAD_TOKEN and int(st2.item()) & sv.DEV_BAD_TOKEN
+    idx = list(range(B))
+    h = host_inputs(inp)
+    gpu = dict(out_tokens=o1.cpu().numpy(), accept_len=a1.cpu().numpy())
+    ng, ns, nu, nsamp, nflag = compare(gpu, oracle_run(h, idx), h, idx)
+    assert ng == 0 and nu == 0 and ns <= 1
