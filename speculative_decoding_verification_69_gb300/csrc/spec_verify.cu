@@ -652,6 +652,11 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
     const int L = bad ? __ffs(bad) - 1 : rq.L;
     if (bad && tid == 0 && P.dev_status) atomicOr(P.dev_status, SPEC_DEV_BAD_TOKEN);
     float g = 0.f, gd = 0.f, u = 0.f;
+    // the sampling uniform of every position the emitted token may take
+    // (lane k: position k), drawn before the wait
+    const double us_lane = (warp == 0 && !greedy && lane <= L) ? uniform_sample(P.seed, (uint32_t)b,
+                                                                               (uint32_t)lane)
+                                                              : 0.0;
     if (warp == 0 && lane < L) {
         if (!greedy) {
             if (!P.gz) {
@@ -747,6 +752,7 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
     __syncthreads();
     const int a = s_a;
     if (a < 0) return;  // uniform over the CTA
+    const double ua = __shfl_sync(0xFFFFFFFFu, us_lane, a & 31);  // position a's (a <= 31)
     if (P.ee_done && threadIdx.x == 0) P.ee_done[b] = 1;
     int32_t *out = P.out_tokens + (size_t)b * (K + 1);
     for (int k = tid; k <= K; k += kThreads) {
@@ -776,7 +782,7 @@ __global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
             si.c_lo = rq.c_lo;
             si.b = b;
             si.pad0 = 0;
-            si.u = uniform_sample(P.seed, (uint32_t)b, (uint32_t)a);
+            si.u = a < 32 ? ua : uniform_sample(P.seed, (uint32_t)b, (uint32_t)a);
             si.pad1 = 0.0;
             P.samp_list[atomicAdd(P.samp_count, 1)] = si;  // order is irrelevant to the results
         }
@@ -1022,11 +1028,15 @@ __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
     constexpr int ESZ = Fmt<DT>::kESZ;
     constexpr int CE = chunk_elems<DT>();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the sampled-request list is sv_decide's (two kernels back, complete once
+    // this kernel runs): read before the wait; the chunk masses come after it
+    const int li = blockIdx.x * kFindWarps + warp;
+    const bool active = li < *P.samp_count;
+    SampInfo si;
+    if (active) si = P.samp_list[li];
     pdl_wait();  // chunk masses come from sv_sample
     pdl_trigger();
-    const int li = blockIdx.x * kFindWarps + warp;
-    if (li >= *P.samp_count) return;
-    const SampInfo si = P.samp_list[li];
+    if (!active) return;
     const int b = si.b;
     const bool resid = si.mode == 1;
     const int nch = P.nchunk;
