@@ -1945,12 +1945,12 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
                 s_acc = acc;
             }
             __syncthreads();
-            const int verdict = s_acc;
-            if (verdict < 0) {
+            const int decision = s_acc;
+            if (decision < 0) {
                 __syncthreads();  // s_acc is rewritten for the next candidate
                 continue;
             }
-            if (verdict) {
+            if (decision) {
                 next = ch;
                 break;
             }
