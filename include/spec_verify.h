@@ -72,11 +72,11 @@ typedef enum {
 #define SPEC_MAX_V 0x40000000  /* largest supported vocabulary V (2^30) */
 
 /*
- * Workspace size in bytes that spec_verify / spec_verify_debug /
- * spec_verify_early_exit need for the
- * given problem (0 on invalid sizes).  The workspace is scratch device memory
- * owned by the caller; it must be 256-byte aligned, need not be initialised,
- * and must not be shared by calls that may run concurrently.
+ * Workspace size in bytes that spec_verify, spec_verify_debug,
+ * spec_verify_early_exit, spec_verify_scheduled and spec_draft_confidence
+ * need for the given problem (0 on invalid sizes).  The workspace is scratch
+ * device memory owned by the caller; it must be 256-byte aligned, need not be
+ * initialised, and must not be shared by calls that may run concurrently.
  */
 size_t spec_verify_workspace_bytes(int B, int K, int V, spec_dtype_t dtype);
 
