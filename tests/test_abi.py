@@ -152,3 +152,36 @@ def test_scheduled_host_validation_without_gpu(lib):
     n1 = lib.spec_verify_workspace_bytes(8, 4, 100, 1)
     n2 = lib.spec_verify_workspace_bytes(8, 8, 100, 1)
     assert n2 > n1
+
+
+def test_lmhead_host_validation_without_gpu(lib):
+    """spec_verify_lmhead rejects bad sizes (d not a multiple of 64, V not a
+    multiple of 4), null pointers, misaligned buffers and small workspaces on
+    the host, before any CUDA call; its workspace size follows B, V and d."""
+    fake = ctypes.c_void_p(0x10000)
+    assert lib.spec_lmhead_workspace_bytes(2, 4, 1000, 96) == 0      # d % 64
+    assert lib.spec_lmhead_workspace_bytes(2, 4, 1001, 64) == 0      # V % 4
+    assert lib.spec_lmhead_workspace_bytes(0, 4, 1000, 64) == 0
+    assert lib.spec_lmhead_workspace_bytes(2, 33, 1000, 64) == 0
+    n1 = lib.spec_lmhead_workspace_bytes(2, 4, 1000, 64)
+    n2 = lib.spec_lmhead_workspace_bytes(4, 4, 1000, 64)
+    n3 = lib.spec_lmhead_workspace_bytes(2, 4, 1000, 128)
+    assert 0 < n1 < n2 and n1 < n3 and n1 % 256 == 0
+    assert n1 >= 8 * 2 * 1000                                        # the recomputed rows
+    base = dict(ht=fake, hd=fake, wt=fake, wd=fake, d=64, tok=fake, vl=None, T=fake, seed=1, B=2,
+                K=4, V=1000, o=fake, a=fake, ws=fake, wsb=1 << 40, st=None, rs=None, pr=None)
+
+    def call(**kw):
+        x = dict(base, **kw)
+        return lib.spec_verify_lmhead(x["ht"], x["hd"], x["wt"], x["wd"], x["d"], x["tok"], x["vl"],
+                                      x["T"], x["seed"], x["B"], x["K"], x["V"], x["o"], x["a"],
+                                      x["ws"], x["wsb"], x["st"], x["rs"], x["pr"], None)
+
+    assert call(d=96) == 1 and call(d=0) == 1 and call(V=1001) == 1 and call(B=0) == 1
+    assert call(K=0) == 1 and call(K=33) == 1
+    for k in ("ht", "hd", "wt", "wd", "tok", "T", "o", "a"):
+        assert call(**{k: None}) == 1, k
+    for k in ("ht", "hd", "wt", "wd"):
+        assert call(**{k: ctypes.c_void_p(0x10008)}) == 1, k        # not 16-byte aligned
+    assert call(ws=None) == 4 and call(wsb=1024) == 4
+    assert call(ws=ctypes.c_void_p(0x10080)) == 4                    # not 256-byte aligned
