@@ -404,18 +404,11 @@ def run_tree(args, world, rank, local):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    barrier(world)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        step(args.warmup + i)
-        ev[i][1].record(stream)
+    graphs = [] if args.no_graph else capture_steps(step, ncopies, stream)
+    for g in graphs:
+        g.replay()
     torch.cuda.synchronize()
-    barrier(world)
-    t1 = time.perf_counter()
-    total_s = sum(a.elapsed_time(b) for a, b in ev) / 1e3
+    total_s, _, t0, t1 = timed_loop(args, world, stream, step, graphs, args.warmup)
     total_s_max = max_over_ranks(total_s, world)
     positions = sum_over_ranks(B * (N - 1) * args.steps, world)
     peak, peak_kind = measured_peak()
@@ -436,7 +429,10 @@ def run_tree(args, world, rank, local):
                    % (", distinct siblings" if args.distinct else ""),
                    "logit_bytes_per_step": alg_bytes,
                    "logits_GBps": alg_bytes / step_s / 1e9,
-                   "l2": "inputs larger than L2: %d copies cycled; no flush" % ncopies},
+                   "l2": "inputs larger than L2: %d copies cycled; no flush" % ncopies,
+                   "timing": ("%d steps, each a replay of the CUDA graph captured from its call, "
+                              "one pair of CUDA events around them" % args.steps) if graphs else
+                             ("%d plain calls, one pair of CUDA events around them" % args.steps)},
         "roofline": {"bound": "hbm", "kernel": "whole step", "achieved": alg_bytes / step_s / 1e9,
                      "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
                      "frac": alg_bytes / step_s / 1e9 / peak, "traffic": None},
@@ -618,24 +614,18 @@ def run_lmhead(args, world, rank, local):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    graphs = [] if args.no_graph else capture_steps(step, ncopies, stream)
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     for a, b in kev:
         a.record(stream)
         b.record(stream)
     torch.cuda.synchronize()
-    barrier(world)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        step(args.warmup + i)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    t1 = time.perf_counter()
-    for i in range(args.steps):  # the two statistics GEMMs bracketed by events
+    total_s, _, t0, t1 = timed_loop(args, world, stream, step, graphs, args.warmup)
+    for i in range(args.steps):  # the statistics GEMM bracketed by events (plain calls)
         sv.profile_events(*kev[i])
         step(args.warmup + args.steps + i)
     sv.profile_events(None, None)
@@ -643,7 +633,6 @@ def run_lmhead(args, world, rank, local):
     t2 = time.perf_counter()
     a_host = accept_len.cpu().numpy()
     o_host = out_tokens.cpu().numpy()
-    total_s = sum(a.elapsed_time(b) for a, b in ev) / 1e3
     total_s_max = max_over_ranks(total_s, world)
     positions = B * K
     gemm_s = sum(a.elapsed_time(b) for a, b in kev) / 1e3 / args.steps
@@ -704,7 +693,10 @@ def run_lmhead(args, world, rank, local):
                    "tflops_step": (flop_stats + 4.0 * n_samp * d * V) * args.steps / total_s / 1e12,
                    "logit_bytes_never_written": B * (2 * K + 1) * V * 4,
                    "l2": "weights %d bytes (larger than L2) stream once per step; hidden states "
-                         "cycled through %d copies" % (V * d * 2, ncopies)},
+                         "cycled through %d copies" % (V * d * 2, ncopies),
+                   "timing": ("%d steps, each a replay of the CUDA graph captured from its call, "
+                              "one pair of CUDA events around them" % args.steps) if graphs else
+                             ("%d plain calls, one pair of CUDA events around them" % args.steps)},
         "roofline": {"bound": "tensor", "kernel": "lm_gemm<LmStatsEpi> (target and draft rows)",
                      "achieved": achieved, "peak": peak, "peak_source": peak_kind,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
@@ -720,6 +712,46 @@ def run_lmhead(args, world, rank, local):
         res["cpu_baseline"] = {"value": pps, "unit": "positions/s", "cores": cores,
                                "kind": "oracle", "sample": sample, "seconds": dt}
     return res
+
+
+def capture_steps(step, n, stream):
+    """One CUDA graph per logit copy j (step j), captured on a side stream after
+    the warm-up; replaying graph i % n is step i.  The library's calls allocate
+    nothing and do not synchronise, so a step captures as it is enqueued."""
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    graphs = []
+    with torch.cuda.stream(side):
+        for j in range(n):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                step(j)
+            graphs.append(g)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    return graphs
+
+
+def timed_loop(args, world, stream, step, graphs, first):
+    """Timed region: exactly args.steps steps (graph replays, or plain calls
+    without graphs) bracketed by one pair of CUDA events on the launching
+    stream, with a barrier and a synchronisation on both sides.  Returns
+    (seconds on the device, wall seconds, wall start, wall end)."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for i in range(args.steps):
+        if graphs:
+            graphs[(first + i) % len(graphs)].replay()
+        else:
+            step(first + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.perf_counter()
+    return e0.elapsed_time(e1) / 1e3, t1 - t0, t0, t1
 
 
 def run_ours(args, world, rank, local):
@@ -788,8 +820,10 @@ def run_ours(args, world, rank, local):
         step(i)
     torch.cuda.synchronize()
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    graphs = [] if args.no_graph else capture_steps(step, ncopies, stream)
+    for g in graphs:  # the replays themselves warmed up once
+        g.replay()
+    torch.cuda.synchronize()
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     for a, b in kev:  # torch creates the CUDA event on first record
@@ -798,17 +832,9 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    t_wall0 = time.perf_counter()
-    # timed region 1: the steps as a caller runs them (value, ms_per_step)
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        step(args.warmup + i)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    t_wall1 = time.perf_counter()
+    # timed region 1: the steps back to back as a serving loop issues them
+    # (value, ms_per_step)
+    total_s, t_wall, t_wall0, t_wall1 = timed_loop(args, world, stream, step, graphs, args.warmup)
     # timed region 2: the same steps with CUDA events bracketing the dominant
     # kernel on its stream (roofline); the events end the programmatic launch
     # overlap on both sides of it, so these steps run slower.  (Early exit runs
@@ -823,11 +849,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     t_wall2 = time.perf_counter()
-    t_wall = t_wall1 - t_wall0
-    step_ms = [a.elapsed_time(b) for a, b in ev]
     kern_ms = [a.elapsed_time(b) for a, b in kev]
     step_k_ms = [a.elapsed_time(b) for a, b in ev_k]
-    total_s = sum(step_ms) / 1e3
     total_s_max = max_over_ranks(total_s, world)
     all_pos = sum_over_ranks(positions * args.steps, world)
     value = all_pos / total_s_max
@@ -929,15 +952,19 @@ def run_ours(args, world, rank, local):
             "B": B, "K": K, "V": V,
             "verified_positions_per_step": positions,
             "logit_bytes_per_step": alg_bytes,
-            "logits_GBps": alg_bytes * args.steps / total_s / 1e9,
-            "logits_frac_of_8TBps": alg_bytes * args.steps / total_s / 1e9 / HBM_NOMINAL_GBS,
+            # logit bytes the step read (early exit reads fewer rows than the single pass)
+            "logits_GBps": read_bytes * args.steps / total_s / 1e9,
+            "logits_frac_of_8TBps": read_bytes * args.steps / total_s / 1e9 / HBM_NOMINAL_GBS,
             "l2": ("inputs larger than L2: %d device copies of the logits cycled round-robin, "
                    "%d logit bytes read per step, L2 %d bytes; no flush" %
                    (ncopies, alg_bytes, l2_bytes)),
-            "timing": ("two timed loops of the same steps: value from the first (no events "
-                       "inside a step), the dominant kernel's CUDA-event duration from the "
-                       "second (events bracket it, %.4f ms per step there)"
-                       % (sum(step_k_ms) / len(step_k_ms))),
+            "timing": ("two timed loops of the same steps: value from the first (%s, one "
+                       "pair of CUDA events around the %d steps), the dominant kernel's "
+                       "CUDA-event duration from the second (plain calls, events bracket the "
+                       "kernel, %.4f ms per step there)"
+                       % ("each step replays the CUDA graph captured from that step's call"
+                          if graphs else "plain calls", args.steps,
+                          sum(step_k_ms) / len(step_k_ms))),
             "parallelism": "replicas" if world > 1 else "single GPU",
             "mode": (("early exit, first wave %d positions (%d logit bytes read per step)"
                       % (ee, read_bytes)) if ee else "single pass") + (
@@ -1041,6 +1068,9 @@ def main(argv=None):
     ap.add_argument("--distinct", action="store_true",
                     help="with --tree-sampled: siblings drawn without replacement (top-k style), "
                          "verified by spec_verify_tree_distinct")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time plain calls instead of replays of the CUDA graphs captured from "
+                         "them")
     ap.add_argument("--batch", type=int, default=None,
                     help="requests per step instead of the workload's B (smaller cases of the same "
                          "shapes, for profiler captures); the bench line then names the batch")
