@@ -159,3 +159,45 @@ def test_verify_scheduled_against_oracle(sv):
     gpu = dict(out_tokens=out.cpu().numpy(), accept_len=acc.cpu().numpy())
     ng, ns, nu, nsamp, nflag = compare(gpu, orc, h, idx)
     assert ng == 0 and nu == 0 and ns <= 1
+
+
+def test_bench_c3_scheduled_call_full_size(sv):
+    """The c3 step exactly as the benchmark times it (one spec_verify_scheduled
+    call, threshold 0.3 on the given confidences): lengths bit-exact with the
+    oracle's schedule, every one of the 256 requests against the oracle."""
+    from gpu_helpers import compare, host_inputs, oracle_run
+    inp = workloads.make_inputs(3)
+    out, acc, vl, _ = sv.verify_scheduled(inp["target"], inp["draft"], inp["tokens"],
+                                          inp["temperature"], inp["seed"], threshold=0.3,
+                                          draft_maxprob=inp["draft_maxprob"])
+    torch.cuda.synchronize()
+    ref_vl = oracle.schedule_len(inp["draft_maxprob"].cpu().numpy(), 0.3)
+    assert np.array_equal(vl.cpu().numpy(), ref_vl)
+    B = inp["tokens"].shape[0]
+    h = host_inputs(inp, verify_len=vl)
+    idx = list(range(B))
+    gpu = dict(out_tokens=out.cpu().numpy(), accept_len=acc.cpu().numpy())
+    ng, ns, nu, nsamp, nflag = compare(gpu, oracle_run(h, idx), h, idx)
+    assert ng == 0 and nu == 0 and ns <= 1, (ng, ns, nu, nsamp, nflag)
+
+
+def test_bench_chain_call_full_size(sv):
+    """The --chain step at c3 (confidences computed from the draft rows, a
+    budget of 5 positions per request): confidences within 1e-5 of the
+    oracle's, lengths equal to the oracle's budget schedule of the GPU's
+    confidences, all 256 requests against the oracle."""
+    from gpu_helpers import compare, host_inputs, oracle_run
+    inp = workloads.make_inputs(3)
+    B = inp["tokens"].shape[0]
+    out, acc, vl, conf = sv.verify_scheduled(inp["target"], inp["draft"], inp["tokens"],
+                                             inp["temperature"], inp["seed"], budget=5 * B)
+    torch.cuda.synchronize()
+    ref_conf = oracle.draft_confidence(workloads.to_numpy_logits(inp["draft"][:16]),
+                                       inp["temperature"][:16].cpu().numpy())
+    assert np.allclose(conf[:16].cpu().numpy(), ref_conf, rtol=1e-5, atol=0.0)
+    assert np.array_equal(vl.cpu().numpy(), oracle.schedule_budget(conf.cpu().numpy(), 5 * B))
+    h = host_inputs(inp, verify_len=vl)
+    idx = list(range(B))
+    gpu = dict(out_tokens=out.cpu().numpy(), accept_len=acc.cpu().numpy())
+    ng, ns, nu, nsamp, nflag = compare(gpu, oracle_run(h, idx), h, idx)
+    assert ng == 0 and nu == 0 and ns <= 1, (ng, ns, nu, nsamp, nflag)

@@ -240,8 +240,9 @@ def test_sampled_tree_first_token_law(sv):
             assert pval < 1e-6, pval
 
 
-@pytest.mark.parametrize("cfg,N,b0,n_check", [(1, 16, 0, 32), (4, 9, 112, 48)])
-def test_sampled_trees_at_bench_workloads(sv, cfg, N, b0, n_check):
+@pytest.mark.parametrize("cfg,N,b0,n_check,distinct", [(1, 16, 0, 32, False), (4, 9, 112, 48, False),
+                                                       (1, 16, 0, 32, True)])
+def test_sampled_trees_at_bench_workloads(sv, cfg, N, b0, n_check, distinct):
     """The sampled-tree workloads the benchmark times (same generator, seed and
     launch configuration: clusters with staged slices at c1, one CTA per
     request at c4 with its quarter of greedy requests), against the oracle on
@@ -251,15 +252,16 @@ def test_sampled_trees_at_bench_workloads(sv, cfg, N, b0, n_check):
     noise = c["noise"] if isinstance(c["noise"], float) else 0.5
     inp = workloads.make_tree_inputs(c["B"], N, c["V"], c["dtype"], seed=workloads.seed_for(cfg, 0),
                                      T=T, sigma=c["sigma"], noise=noise,
-                                     n_greedy=c.get("n_greedy", 0))
+                                     n_greedy=c.get("n_greedy", 0), distinct=distinct)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     out, nodes, acc = sv.verify_tree(inp["target"], inp["draft"], inp["parent"], inp["tokens"],
-                                     inp["temperature"], inp["seed"], dev_status=st)
+                                     inp["temperature"], inp["seed"], dev_status=st,
+                                     distinct=distinct)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     sl = slice(b0, b0 + n_check)
     sub = {k: (v[sl] if torch.is_tensor(v) else v) for k, v in inp.items()}
-    r = _oracle_tree(sub, b0=b0)
+    r = _oracle_tree(sub, b0=b0, distinct=distinct)
     out, nodes, acc = out[sl].cpu().numpy(), nodes[sl].cpu().numpy(), acc[sl].cpu().numpy()
     same = ((acc == r["accept_len"]) & (out == r["out_tokens"]).all(axis=1)
             & (nodes == r["out_nodes"]).all(axis=1))
