@@ -169,6 +169,28 @@ __device__ __forceinline__ void temp_coeffs(float T, float &c, float &c_hi, floa
     c_lo = ql;
 }
 
+// Threshold schedule of one request: the longest prefix whose fp32 running
+// product of draft max-probabilities, multiplied left to right, stays at or
+// above thr.  The row is loaded whole first (independent loads), then the
+// product runs on registers in the same order.
+__device__ __forceinline__ int schedule_threshold(const float *mp, int K, float thr) {
+    float v[SPEC_MAX_K];
+#pragma unroll
+    for (int k = 0; k < SPEC_MAX_K; ++k) v[k] = k < K ? __ldg(mp + k) : 0.f;
+    float prod = 1.0f;
+    int L = 0;
+    bool run = true;
+#pragma unroll
+    for (int k = 0; k < SPEC_MAX_K; ++k) {
+        if (run && k < K) {
+            prod = __fmul_rn(prod, v[k]);
+            if (prod >= thr) L = k + 1;
+            else run = false;
+        }
+    }
+    return L;
+}
+
 constexpr int kPrepThreads = 1024;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded wait: 2 s
 // Diagnostics: the DIAG instantiations of the bulk-copy kernels (launched only
@@ -207,14 +229,7 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
         } else if (b < P.B) {
             uint32_t st = 0;
             if (P.sched_mp) {  // threshold schedule: fp32 running product, left to right
-                const float *mp = P.sched_mp + (size_t)b * P.K;
-                float prod = 1.0f;
-                L = 0;
-                for (int k = 0; k < P.K; ++k) {
-                    prod = __fmul_rn(prod, mp[k]);
-                    if (prod >= P.sched_thr) L = k + 1;
-                    else break;
-                }
+                L = schedule_threshold(P.sched_mp + (size_t)b * P.K, P.K, P.sched_thr);
                 if (P.vlen_out) P.vlen_out[b] = L;
             } else {
                 L = P.verify_len ? P.verify_len[b] : P.K;
@@ -1228,14 +1243,7 @@ __global__ void sv_schedule(const float *__restrict__ mp, float thr, int B, int 
                             int32_t *__restrict__ out) {
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
-    float prod = 1.0f;
-    int L = 0;
-    for (int k = 0; k < K; ++k) {
-        prod = __fmul_rn(prod, mp[(size_t)b * K + k]);
-        if (prod >= thr) L = k + 1;
-        else break;
-    }
-    out[b] = L;
+    out[b] = schedule_threshold(mp + (size_t)b * K, K, thr);
 }
 
 // ------------------------------------------------------------------ draft confidence
