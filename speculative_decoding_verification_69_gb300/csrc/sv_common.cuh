@@ -148,14 +148,6 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Weights of an element pair: 2^((z - m) * c) with c = c_hi + c_lo.
-__device__ __forceinline__ float2 weight2(float2 z, float2 m2, float2 chi2, float2 clo2) {
-    float2 d = sub2(z, m2);
-    float2 lo = mul2(d, clo2);
-    float2 t = fma2(d, chi2, lo);
-    return make_float2(ex2(t.x), ex2(t.y));
-}
-
 // Scaled weights of an element pair: 2^((z - m) * c + l), c = c_hi + c_lo.
 __device__ __forceinline__ float2 weight2l(float2 z, float2 m2, float2 chi2, float2 clo2, float2 l2) {
     float2 d = sub2(z, m2);
@@ -191,12 +183,6 @@ __device__ __forceinline__ FF ff_shfl_xor(FF a, int m) {
     return FF{__shfl_xor_sync(0xFFFFFFFFu, a.hi, m), __shfl_xor_sync(0xFFFFFFFFu, a.lo, m)};
 }
 
-__device__ __forceinline__ FF ff_from_double(double x) {
-    float hi = __double2float_rn(x);
-    float lo = __double2float_rn(x - (double)hi);
-    return FF{hi, lo};
-}
-
 __device__ __forceinline__ double ff_to_double(FF a) { return (double)a.hi + (double)a.lo; }
 
 // Per-thread accumulator of non-negative terms <= bias: Fast2Sum against a
@@ -222,70 +208,6 @@ struct BiasAcc2 {
         return ff_add(a, b);
     }
 };
-
-// ------------------------------------------------------------------ CTA reductions
-
-// CTA-wide max; every thread gets the result.  `red` holds kWarps floats.
-__device__ __forceinline__ float cta_max(float v, float *red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
-    if (l == 0) red[w] = v;
-    __syncthreads();
-    float r = red[0];
-#pragma unroll
-    for (int i = 1; i < kWarps; ++i) r = fmaxf(r, red[i]);
-    return r;
-}
-
-// CTA-wide two-float sum; valid in every thread.  `red` holds 2*kWarps floats.
-__device__ __forceinline__ FF cta_sum_ff(FF v, float *red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = ff_add(v, ff_shfl_xor(v, o));
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
-    if (l == 0) {
-        red[2 * w] = v.hi;
-        red[2 * w + 1] = v.lo;
-    }
-    __syncthreads();
-    FF r{red[0], red[1]};
-#pragma unroll
-    for (int i = 1; i < kWarps; ++i) r = ff_add(r, FF{red[2 * i], red[2 * i + 1]});
-    return r;
-}
-
-// CTA-wide (max value, lowest index) pair; valid in every thread.
-__device__ __forceinline__ void cta_argmax(float &v, int &idx, float *redv, int *redi) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        float ov = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-        int oi = __shfl_xor_sync(0xFFFFFFFFu, idx, o);
-        if (ov > v || (ov == v && oi < idx)) {
-            v = ov;
-            idx = oi;
-        }
-    }
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
-    if (l == 0) {
-        redv[w] = v;
-        redi[w] = idx;
-    }
-    __syncthreads();
-    v = redv[0];
-    idx = redi[0];
-#pragma unroll
-    for (int i = 1; i < kWarps; ++i) {
-        float ov = redv[i];
-        int oi = redi[i];
-        if (ov > v || (ov == v && oi < idx)) {
-            v = ov;
-            idx = oi;
-        }
-    }
-}
 
 // ------------------------------------------------------------------ warp reductions
 
@@ -431,13 +353,8 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
     return c;
 }
 
-// Acceptance uniform (draw 0): 24 bits -> [0,1) exactly representable.
-__device__ __forceinline__ double uniform_accept(unsigned long long seed, uint32_t b, uint32_t k) {
-    uint4 w = philox4x32_10(make_uint4(b, k, 0u, 0u), (uint32_t)seed, (uint32_t)(seed >> 32));
-    return (double)(w.x >> 8) * 0x1p-24;
-}
-
-// The same acceptance uniform as a float: a 24-bit value, so exact.
+// Acceptance uniform (draw 0): the top 24 bits of word 0 -> [0,1), a float
+// (24 bits, so exact).
 __device__ __forceinline__ float uniform_accept_f(unsigned long long seed, uint32_t b, uint32_t k) {
     uint4 w = philox4x32_10(make_uint4(b, k, 0u, 0u), (uint32_t)seed, (uint32_t)(seed >> 32));
     return (float)(w.x >> 8) * 0x1p-24f;
