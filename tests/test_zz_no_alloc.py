@@ -64,3 +64,25 @@ def test_noalloc_matches_workspace_entry_two_calls():
         assert np.array_equal(out_n.cpu().numpy(), out_w.cpu().numpy())
         assert np.array_equal(acc_n.cpu().numpy(), acc_w.cpu().numpy())
         assert (acc_n.cpu().numpy() >= 0).all()
+
+
+@pytest.mark.gpu
+def test_noalloc_binding_matches_verify():
+    """The same entry point through the Python binding (argument marshalling
+    only), on the mixed greedy / sampled recipe of the B=512 workload shrunk to
+    64 requests: identical tokens and accept lengths, no status bit."""
+    assert torch.cuda.is_available(), "GPU test needs a CUDA device"
+    sv, L = _lib()
+    inp = workloads.make_inputs(4, rep=41, B=64)
+    B, K1, V = inp["target"].shape
+    assert L.spec_verify_workspace_bytes(B, K1 - 1, V, sv.DTYPE_BF16) <= sv.NOALLOC_SCRATCH_BYTES
+    args = (inp["target"], inp["draft"], inp["tokens"], inp["verify_len"], inp["temperature"],
+            inp["seed"])
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o1, a1 = sv.verify_noalloc(*args, dev_status=st)
+    o2, a2 = sv.verify(*args)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(o1, o2) and torch.equal(a1, a2)
+    t = inp["temperature"].cpu()
+    assert (t == 0).any() and (t > 0).any()  # both paths exercised
