@@ -1014,7 +1014,7 @@ __global__ void __launch_bounds__(kSWarps * 32, kSMinBlocks) sv_sample(Params P)
 
 // ------------------------------------------------------------------ 5. inverse CDF
 
-constexpr int kFindWarps = 8;  // one warp per sampled request
+constexpr int kFindWarps = 2;  // one warp per sampled request (small CTAs spread the draws over more SMs)
 
 // kappa - 1 for kappa = 1 / S, S a two-float sum close to 1.
 __device__ __forceinline__ float kappa_minus_one(FF S) {
