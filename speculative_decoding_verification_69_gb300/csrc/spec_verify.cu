@@ -649,8 +649,10 @@ __device__ __forceinline__ bool accept_position(float u, float g, float m_t, flo
     return u < r;
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kThreads) sv_decide(Params P) {
+// MINB: CTAs per SM the register budget is cut for (0: the compiler's own
+// budget; 4 when the batch would not fit one wave at that budget).
+template <int DT, int MINB = 0>
+__global__ void __launch_bounds__(kThreads, MINB) sv_decide(Params P) {
     const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int K = P.K;
     __shared__ float s_m[2 * SPEC_MAX_K + 1];
@@ -2411,6 +2413,7 @@ struct DevInfo {
     int sms = 0;
     int occ_p1[2][2] = {{0, 0}, {0, 0}};
     int occ_sample[2][2] = {{0, 0}, {0, 0}};
+    int occ_decide[2] = {0, 0};  // resident sv_decide CTAs per SM at the default register budget
     bool walk_smem[2][2] = {{false, false}, {false, false}};  // tree walk's shared-memory limit raised
     bool lm_ready = false;  // LM-head GEMM's shared-memory limit raised
     bool ok = false;
@@ -2441,7 +2444,18 @@ static bool setup_kernels(DevInfo &d) {
         cudaSuccess)
         return false;
     d.occ_sample[DT][VEC] = o > 0 ? o : 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, sv_decide<DT>, kThreads, 0) != cudaSuccess)
+        return false;
+    d.occ_decide[DT] = o > 0 ? o : 1;
     return true;
+}
+
+// The decision kernel for a batch: one CTA per request, all resident at once
+// when the default register budget allows it, else the build cut to 4 CTAs
+// per SM.
+template <int DT>
+static void (*decide_kernel(const DevInfo &d, int B))(Params) {
+    return (long long)B > (long long)d.occ_decide[DT] * d.sms ? sv_decide<DT, 4> : sv_decide<DT>;
 }
 
 static DevInfo *dev_info() {
@@ -2492,7 +2506,7 @@ static void launch_all(const Params &P, const DevInfo &d, cudaStream_t s) {
     launch_dependent(g_diag_timeout ? sv_pass1<DT, VEC, true> : sv_pass1<DT, VEC>,
                      d.sms * d.occ_p1[DT][VEC], kP1Warps * 32, VEC ? kP1Smem : 0, s, P);
     if (g_prof_end) cudaEventRecord(g_prof_end, s);
-    launch_dependent(sv_decide<DT>, P.B, kThreads, 0, s, P);
+    launch_dependent(decide_kernel<DT>(d, P.B), P.B, kThreads, 0, s, P);
     // the sampled requests are known only on the device: enough warps for all
     // of them, at most one full wave
     long long g2 = (long long)d.sms * d.occ_sample[DT][VEC];
@@ -2519,7 +2533,7 @@ static void launch_waves(const Params &P0, const DevInfo &d, cudaStream_t s, int
         sv_prep<<<1, kPrepThreads, 0, s>>>(P);
         launch_dependent(sv_pass1<DT, VEC>, d.sms * d.occ_p1[DT][VEC], kP1Warps * 32,
                          VEC ? kP1Smem : 0, s, P);
-        launch_dependent(sv_decide<DT>, P.B, kThreads, 0, s, P);
+        launch_dependent(decide_kernel<DT>(d, P.B), P.B, kThreads, 0, s, P);
     }
     long long g2 = (long long)d.sms * d.occ_sample[DT][VEC];
     const long long g2_need = ((long long)P.B * P.nchunk + kSWarps - 1) / kSWarps;
@@ -2966,7 +2980,7 @@ spec_status_t spec_verify_lmhead(const void *hidden_target, const void *hidden_d
     }
     if (sv::g_prof_end) cudaEventRecord(sv::g_prof_end, s);
     // 3. decisions; 4. the rows the sampled requests draw from, recomputed
-    sv::launch_dependent(sv::sv_decide<sv::kF32>, B, sv::kThreads, 0, s, P);
+    sv::launch_dependent(sv::decide_kernel<sv::kF32>(*dv, B), B, sv::kThreads, 0, s, P);
     {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)B);
