@@ -774,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, MINB) sv_decide(Params P) {
     int32_t *out = P.out_tokens + (size_t)b * (K + 1);
     for (int k = tid; k <= K; k += kThreads) {
         int v = -1;
-        if (k < a) v = P.tokens[(size_t)b * K + k];
+        if (k < a) v = x;  // thread k < a <= L is lane k of warp 0, which holds draft token k
         else if (k == a && greedy) v = s_amax[a];
         out[k] = v;
     }
