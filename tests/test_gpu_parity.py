@@ -172,6 +172,9 @@ def _rand_inputs(B, K, V, dtype, seed, T, L=None, device="cuda"):
     (2, 32, 3000, torch.bfloat16),      # K = SPEC_MAX_K
     (6, 4, 16384 + 8, torch.bfloat16),  # one full tile plus an 8-element tail tile
     (6, 4, 3 * 8192 + 4, torch.float32),
+    (2, 2, 600_000, torch.bfloat16),    # 147 statistics items per row (> 128: the looping
+                                        # combine), 293 sampler chunks (records not held)
+    (2, 2, 300_001, torch.float32),     # the same counts on the scalar path
 ])
 def test_shapes_sampled_and_greedy(B, K, V, dtype):
     for T in (0.9, 0.0):
