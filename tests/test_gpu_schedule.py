@@ -33,10 +33,12 @@ def test_draft_confidence_against_oracle(sv, cfg, n):
 
 
 def test_draft_confidence_shapes(sv):
-    """Odd vocabularies (vector path with bounds), fp32, -inf entries."""
+    """Odd vocabularies (vector path with bounds), fp32, -inf entries, and a
+    vocabulary past 128 statistics items per row (the looping combine)."""
     g = torch.Generator(device="cuda").manual_seed(21)
     for B, K, V, dt in [(3, 2, 1001, torch.bfloat16), (2, 5, 999, torch.float32),
-                        (4, 3, 16384 + 8, torch.bfloat16)]:
+                        (4, 3, 16384 + 8, torch.bfloat16),
+                        (2, 2, 600_000, torch.bfloat16)]:  # > 128 statistics items per row
         d = (torch.randn((B, K, V), generator=g, device="cuda") * 3.0).to(dt)
         d[0, 0, ::2] = float("-inf")
         T = torch.tensor([0.7, 1.3, 0.2, 2.0][:B], device="cuda")
