@@ -99,3 +99,16 @@ def test_repeated_calls_reuse_workspace(sv):
     for _ in range(2):
         assert np.array_equal(_run(sv, a, 3)[0], ra[0])
         assert np.array_equal(_run(sv, b, 3)[0], rb[0])
+
+
+def test_large_vocabulary_identical(sv):
+    """A 600K-element vocabulary (more than 128 statistics items per row, so
+    the decision combines each row in blocks, and 293 sampler chunks): the two
+    waves give the single pass's outputs bit for bit, greedy and sampled."""
+    inp = workloads.make_inputs(1, rep=11, B=8, K=4, V=600_000)
+    inp["temperature"][::3] = 0.0  # some greedy requests
+    ref = _run(sv, inp, 0)
+    for W in (1, 2, 3):
+        got = _run(sv, inp, W)
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1]), W
+        assert got[2] == ref[2] == 0
