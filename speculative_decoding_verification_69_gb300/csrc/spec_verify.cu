@@ -1016,7 +1016,9 @@ __global__ void __launch_bounds__(kSWarps * 32, kSMinBlocks) sv_sample(Params P)
 
 // ------------------------------------------------------------------ 5. inverse CDF
 
-constexpr int kFindWarps = 2;  // one warp per sampled request (small CTAs spread the draws over more SMs)
+constexpr int kFindWarps = 4;  // warps per sampled request (one CTA each)
+constexpr int kFindVecs = kChunkBytes / 16 / (kFindWarps * 32);  // chosen chunk's vectors per lane
+static_assert(kFindVecs * kFindWarps * 32 * 16 == kChunkBytes, "the CTA covers the chunk");
 
 // kappa - 1 for kappa = 1 / S, S a two-float sum close to 1.
 __device__ __forceinline__ float kappa_minus_one(FF S) {
@@ -1033,22 +1035,28 @@ __device__ __forceinline__ float draw_weight(float2 ab, bool two, float dlt, flo
                        : 0.f;
 }
 
-// Token of one sampled request (one warp), in float and two-float arithmetic
-// (fp64 has a long dependent latency on this part): exact normalisers from the
-// segment sums, chunk masses, a two-float prefix over the lanes (each lane owns
-// a contiguous block of chunks), then the chosen chunk (each lane owns 64
-// contiguous elements): one scan of the lane totals and an in-order walk in
-// the crossing lane.
+// Token of one sampled request (one CTA), in float and two-float arithmetic
+// (fp64 has a long dependent latency on this part).  Warp 0 picks the chunk:
+// exact normalisers from the segment sums, chunk masses, a two-float prefix
+// over the lanes (each lane owns a contiguous block of chunks).  Then every
+// warp takes a contiguous slice of the chosen chunk (each lane kFindVecs
+// contiguous vectors, lanes and warps in element order): the lane totals are
+// scanned within the warp, the warp totals added in warp order, and the
+// crossing lane walks its elements in order.
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
     constexpr int EPV = Fmt<DT>::kEPV;
     constexpr int ESZ = Fmt<DT>::kESZ;
     constexpr int CE = chunk_elems<DT>();
+    __shared__ int s_ch, s_two;
+    __shared__ float s_th, s_dlt, s_dld;
+    __shared__ float s_wt[kFindWarps];
+    __shared__ int s_tok[kFindWarps], s_last[kFindWarps];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // the sampled-request list is sv_decide's (two kernels back, complete once
     // this kernel runs): read before the wait; the chunk masses come after it
-    const int li = blockIdx.x * kFindWarps + warp;
-    const bool active = li < *P.samp_count;
+    const int li = blockIdx.x;
+    const bool active = li < *P.samp_count;  // uniform over the CTA
     SampInfo si;
     if (active) si = P.samp_list[li];
     pdl_wait();  // chunk masses come from sv_sample
@@ -1069,123 +1077,135 @@ __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
     const uint32_t ni = Fmt<DT>::kNegInfWord;
     const uint4 neg_inf = make_uint4(ni, ni, ni, ni);
 
-    float4 q[kPerLane];
-    float dlt = 0.f, dld = 0.f;
-    if (held) {
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i) q[i] = c0 + i < c1 ? sub[c0 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    if (resid) {  // exact normalisers: sums over the segment records
-        FF st{0.f, 0.f}, sd{0.f, 0.f};
-        for (int c = c0; c < c1; ++c) {
-            const float4 x = sex[c];
-            st = ff_add(st, FF{x.x, x.y});
-            sd = ff_add(sd, FF{x.z, x.w});
-        }
-        dlt = kappa_minus_one(warp_sum_ff(st));
-        dld = kappa_minus_one(warp_sum_ff(sd));
-    }
-    // residual mass D + delta (D + Bm) - delta' Bm; the mass of p is D (bonus)
-    auto mass_r = [&](const float4 &x) {
-        return fmaxf(0.f, __fadd_rn(x.x, __fmaf_rn(dlt, __fadd_rn(x.x, x.y), -__fmul_rn(dld, x.y))));
-    };
-    bool use_w = !resid;
-    float mine = 0.f;
-    if (held) {
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i)
-            if (c0 + i < c1) mine = __fadd_rn(mine, use_w ? q[i].x : mass_r(q[i]));
-    } else {
-        for (int c = c0; c < c1; ++c) mine = __fadd_rn(mine, use_w ? sub[c].x : mass_r(sub[c]));
-    }
-    if (resid && !(warp_sum(mine) > 0.f)) {
-        // no residual mass (p = q up to rounding): draw from p.  Rare: the
-        // chunk masses of p are formed here, one chunk at a time.
-        use_w = true;
-        mine = 0.f;
-        const float2 l2 = make_float2(si.l_t, 0.f);
-        for (int c = 0; c < nch; ++c) {
-            float w = 0.f;
-#pragma unroll
-            for (int i = 0; i < kVecPerLane; ++i) {
-                const uint4 v = load_vec<DT, VEC>(rowt, (long long)c * CE + (long long)(i * 32 + lane) * EPV, P.V);
-#pragma unroll
-                for (int e = 0; e < EPV; ++e)
-                    w = __fadd_rn(w, weight2l(make_float2(elem<DT>(v, e), -INFINITY), m2, chi2, clo2, l2).x);
-            }
-            w = warp_sum(w);
-            if (lane == 0) sub[c].x = w;  // this warp alone reads request b's records
-        }
-        __syncwarp();
-        __threadfence_block();
+    if (warp == 0) {  // the chunk
+        float4 q[kPerLane];
+        float dlt = 0.f, dld = 0.f;
         if (held) {
 #pragma unroll
             for (int i = 0; i < kPerLane; ++i) q[i] = c0 + i < c1 ? sub[c0 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        for (int c = c0; c < c1; ++c) mine = __fadd_rn(mine, sub[c].x);
-    }
-    // two-float inclusive prefix over the lanes, then theta = u * Z
-    FF incl{mine, 0.f};
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const FF t{__shfl_up_sync(0xFFFFFFFFu, incl.hi, o), __shfl_up_sync(0xFFFFFFFFu, incl.lo, o)};
-        if (lane >= o) incl = ff_add(incl, t);
-    }
-    const FF Z{__shfl_sync(0xFFFFFFFFu, incl.hi, 31), __shfl_sync(0xFFFFFFFFu, incl.lo, 31)};
-    const double theta = si.u * ((double)Z.hi + (double)Z.lo);
-    const FF excl = ff_add(incl, FF{-mine, 0.f});
-    float rem = (float)(theta - ((double)excl.hi + (double)excl.lo));  // mass left at this block
-    const bool mine_crosses = rem >= 0.f && rem < mine;
-    int my_c = INT_MAX, my_last = -1;
-    float my_rem = 0.f;
-    auto visit = [&](int c, const float4 &x) {
-        const float v = use_w ? x.x : mass_r(x);
-        if (v > 0.f) my_last = c;
-        if (mine_crosses && my_c == INT_MAX) {
-            if (v > rem) {
-                my_c = c;
-                my_rem = rem;
+        if (resid) {  // exact normalisers: sums over the segment records
+            FF st{0.f, 0.f}, sd{0.f, 0.f};
+            for (int c = c0; c < c1; ++c) {
+                const float4 x = sex[c];
+                st = ff_add(st, FF{x.x, x.y});
+                sd = ff_add(sd, FF{x.z, x.w});
             }
-            rem = __fsub_rn(rem, v);
+            dlt = kappa_minus_one(warp_sum_ff(st));
+            dld = kappa_minus_one(warp_sum_ff(sd));
         }
-    };
-    if (held) {
+        // residual mass D + delta (D + Bm) - delta' Bm; the mass of p is D (bonus)
+        auto mass_r = [&](const float4 &x) {
+            return fmaxf(0.f, __fadd_rn(x.x, __fmaf_rn(dlt, __fadd_rn(x.x, x.y), -__fmul_rn(dld, x.y))));
+        };
+        bool use_w = !resid;
+        float mine = 0.f;
+        if (held) {
 #pragma unroll
-        for (int i = 0; i < kPerLane; ++i)
-            if (c0 + i < c1) visit(c0 + i, q[i]);
-    } else {
-        for (int c = c0; c < c1; ++c) visit(c, sub[c]);
-    }
-    const int ch_found = warp_min_int(my_c);
-    int ch;
-    float th;  // mass left inside the chosen chunk
-    if (ch_found != INT_MAX) {
-        ch = ch_found;
-        const int owner = __ffs(__ballot_sync(0xFFFFFFFFu, my_c == ch_found)) - 1;
-        th = __shfl_sync(0xFFFFFFFFu, my_rem, owner);
-    } else {
-        // rounding left no crossing: the last chunk with positive mass
-        int last = my_last;
+            for (int i = 0; i < kPerLane; ++i)
+                if (c0 + i < c1) mine = __fadd_rn(mine, use_w ? q[i].x : mass_r(q[i]));
+        } else {
+            for (int c = c0; c < c1; ++c) mine = __fadd_rn(mine, use_w ? sub[c].x : mass_r(sub[c]));
+        }
+        if (resid && !(warp_sum(mine) > 0.f)) {
+            // no residual mass (p = q up to rounding): draw from p.  Rare: the
+            // chunk masses of p are formed here, one chunk at a time.
+            use_w = true;
+            mine = 0.f;
+            const float2 l2 = make_float2(si.l_t, 0.f);
+            for (int c = 0; c < nch; ++c) {
+                float w = 0.f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xFFFFFFFFu, last, o));
-        ch = last >= 0 ? last : nch - 1;
-        th = INFINITY;
+                for (int i = 0; i < kVecPerLane; ++i) {
+                    const uint4 v = load_vec<DT, VEC>(rowt, (long long)c * CE + (long long)(i * 32 + lane) * EPV, P.V);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e)
+                        w = __fadd_rn(w, weight2l(make_float2(elem<DT>(v, e), -INFINITY), m2, chi2, clo2, l2).x);
+                }
+                w = warp_sum(w);
+                if (lane == 0) sub[c].x = w;  // this warp alone reads request b's records
+            }
+            __syncwarp();
+            __threadfence_block();
+            if (held) {
+#pragma unroll
+                for (int i = 0; i < kPerLane; ++i) q[i] = c0 + i < c1 ? sub[c0 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            for (int c = c0; c < c1; ++c) mine = __fadd_rn(mine, sub[c].x);
+        }
+        // two-float inclusive prefix over the lanes, then theta = u * Z
+        FF incl{mine, 0.f};
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const FF t{__shfl_up_sync(0xFFFFFFFFu, incl.hi, o), __shfl_up_sync(0xFFFFFFFFu, incl.lo, o)};
+            if (lane >= o) incl = ff_add(incl, t);
+        }
+        const FF Z{__shfl_sync(0xFFFFFFFFu, incl.hi, 31), __shfl_sync(0xFFFFFFFFu, incl.lo, 31)};
+        const double theta = si.u * ((double)Z.hi + (double)Z.lo);
+        const FF excl = ff_add(incl, FF{-mine, 0.f});
+        float rem = (float)(theta - ((double)excl.hi + (double)excl.lo));  // mass left at this block
+        const bool mine_crosses = rem >= 0.f && rem < mine;
+        int my_c = INT_MAX, my_last = -1;
+        float my_rem = 0.f;
+        auto visit = [&](int c, const float4 &x) {
+            const float v = use_w ? x.x : mass_r(x);
+            if (v > 0.f) my_last = c;
+            if (mine_crosses && my_c == INT_MAX) {
+                if (v > rem) {
+                    my_c = c;
+                    my_rem = rem;
+                }
+                rem = __fsub_rn(rem, v);
+            }
+        };
+        if (held) {
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i)
+                if (c0 + i < c1) visit(c0 + i, q[i]);
+        } else {
+            for (int c = c0; c < c1; ++c) visit(c, sub[c]);
+        }
+        const int ch_found = warp_min_int(my_c);
+        int ch;
+        float th;  // mass left inside the chosen chunk
+        if (ch_found != INT_MAX) {
+            ch = ch_found;
+            const int owner = __ffs(__ballot_sync(0xFFFFFFFFu, my_c == ch_found)) - 1;
+            th = __shfl_sync(0xFFFFFFFFu, my_rem, owner);
+        } else {
+            // rounding left no crossing: the last chunk with positive mass
+            int last = my_last;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xFFFFFFFFu, last, o));
+            ch = last >= 0 ? last : nch - 1;
+            th = INFINITY;
+        }
+        if (lane == 0) {
+            s_ch = ch;
+            s_th = th;
+            s_two = resid && !use_w;
+            s_dlt = dlt;
+            s_dld = dld;
+        }
     }
-    // the chosen chunk, lane-contiguous: lane owns vectors 8 * lane .. 8 * lane + 7
-    const bool two = resid && !use_w;
+    __syncthreads();
+    // the chosen chunk: thread t owns vectors t * kFindVecs .. t * kFindVecs + kFindVecs - 1
+    const int ch = s_ch;
+    const float th = s_th, dlt = s_dlt, dld = s_dld;  // th: mass left inside the chunk
+    const bool two = s_two != 0;
     const float2 l2 = two ? make_float2(si.l_t, si.l_d) : make_float2(si.l_t, 0.f);
-    const long long e0 = (long long)ch * CE + (long long)lane * 8 * EPV;
-    uint4 vt[8], vd[8];
+    const long long e0 = (long long)ch * CE + (long long)threadIdx.x * kFindVecs * EPV;
+    uint4 vt[kFindVecs], vd[kFindVecs];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kFindVecs; ++i) {
         vt[i] = load_vec<DT, VEC>(rowt, e0 + (long long)i * EPV, P.V);
         vd[i] = two ? load_vec<DT, VEC>(rowd, e0 + (long long)i * EPV, P.V) : neg_inf;
     }
-    float vs[8];
+    float vs[kFindVecs];
     float tot = 0.f;
     int last_pos = -1;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kFindVecs; ++i) {
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
@@ -1203,13 +1223,17 @@ __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
         const float u = __shfl_up_sync(0xFFFFFFFFu, inc, o);
         if (lane >= o) inc = __fadd_rn(inc, u);
     }
-    const float lo = __fsub_rn(inc, tot);
+    if (lane == 31) s_wt[warp] = inc;
+    __syncthreads();
+    float woff = 0.f;  // the mass of the warps before this one, added in warp order
+    for (int j = 0; j < warp; ++j) woff = __fadd_rn(woff, s_wt[j]);
+    const float lo = __fadd_rn(woff, __fsub_rn(inc, tot));
     int tok = INT_MAX;
     if (lo <= th && __fadd_rn(lo, tot) > th) {  // the crossing lane walks its elements in order
         float acc_lo = lo;
         bool done = false;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kFindVecs; ++i) {
             if (!done && __fadd_rn(acc_lo, vs[i]) > th) {
                 float ps = acc_lo;
                 int lastp = -1;
@@ -1229,14 +1253,23 @@ __global__ void __launch_bounds__(kFindWarps * 32) sv_find(Params P) {
         }
         if (tok < 0) tok = INT_MAX;
     }
-    int found = warp_min_int(tok);
-    if (found == INT_MAX) {
-        int lp = last_pos;
+    tok = warp_min_int(tok);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xFFFFFFFFu, lp, o));
-        found = lp >= 0 ? lp : (int)((long long)ch * CE);
+    for (int o = 16; o > 0; o >>= 1) last_pos = max(last_pos, __shfl_xor_sync(0xFFFFFFFFu, last_pos, o));
+    if (lane == 0) {
+        s_tok[warp] = tok;
+        s_last[warp] = last_pos;
     }
-    if (lane == 0) P.out_tokens[(size_t)b * (P.K + 1) + si.a] = found;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int found = INT_MAX, lp = -1;
+        for (int j = 0; j < kFindWarps; ++j) {
+            found = min(found, s_tok[j]);
+            lp = max(lp, s_last[j]);
+        }
+        if (found == INT_MAX) found = lp >= 0 ? lp : (int)((long long)ch * CE);
+        P.out_tokens[(size_t)b * (P.K + 1) + si.a] = found;
+    }
 }
 
 // ------------------------------------------------------------------ schedule
@@ -2514,7 +2547,7 @@ static void launch_all(const Params &P, const DevInfo &d, cudaStream_t s) {
     if (g2 > g2_need) g2 = g2_need;
     launch_dependent(g_diag_timeout ? sv_sample<DT, VEC, true> : sv_sample<DT, VEC>, (int)g2,
                      kSWarps * 32, VEC ? kSSmem : 0, s, P);
-    launch_dependent(sv_find<DT, VEC>, (P.B + kFindWarps - 1) / kFindWarps, kFindWarps * 32, 0, s,
+    launch_dependent(sv_find<DT, VEC>, P.B, kFindWarps * 32, 0, s,
                      P);
 }
 
@@ -2539,7 +2572,7 @@ static void launch_waves(const Params &P0, const DevInfo &d, cudaStream_t s, int
     const long long g2_need = ((long long)P.B * P.nchunk + kSWarps - 1) / kSWarps;
     if (g2 > g2_need) g2 = g2_need;
     launch_dependent(sv_sample<DT, VEC>, (int)g2, kSWarps * 32, VEC ? kSSmem : 0, s, P);
-    launch_dependent(sv_find<DT, VEC>, (P.B + kFindWarps - 1) / kFindWarps, kFindWarps * 32, 0, s,
+    launch_dependent(sv_find<DT, VEC>, P.B, kFindWarps * 32, 0, s,
                      P);
 }
 
@@ -3016,11 +3049,11 @@ spec_status_t spec_verify_lmhead(const void *hidden_target, const void *hidden_d
     if (g2 > g2_need) g2 = g2_need;
     if (vec) {
         sv::launch_dependent(sv::sv_sample<sv::kF32, true>, (int)g2, sv::kSWarps * 32, sv::kSSmem, s, P);
-        sv::launch_dependent(sv::sv_find<sv::kF32, true>, (B + sv::kFindWarps - 1) / sv::kFindWarps,
+        sv::launch_dependent(sv::sv_find<sv::kF32, true>, B,
                              sv::kFindWarps * 32, 0, s, P);
     } else {
         sv::launch_dependent(sv::sv_sample<sv::kF32, false>, (int)g2, sv::kSWarps * 32, 0, s, P);
-        sv::launch_dependent(sv::sv_find<sv::kF32, false>, (B + sv::kFindWarps - 1) / sv::kFindWarps,
+        sv::launch_dependent(sv::sv_find<sv::kF32, false>, B,
                              sv::kFindWarps * 32, 0, s, P);
     }
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
