@@ -55,6 +55,7 @@ struct ReqInfo {
     float c_hi;   // two-float log2(e)/T, c_hi rounded toward zero (sampler, acceptance)
     float c_lo;   // >= FLT_MIN
     float T;      // temperature as given
+    int ord;      // sampled: the request's entry in samp_list (request order); greedy: -1
 };
 
 struct SampInfo {
@@ -95,8 +96,8 @@ struct Params {
     float4 *part;      // [B, nslot, npart]: statistics-pass partials (one per 8 KiB item)
     float4 *sub;       // [B, nchunk]: sampler chunk masses A, B, W
     float4 *sexact;    // [B, nchunk]: exact sums of e (hi, lo) and e' (hi, lo)
-    SampInfo *samp_list; // [B] one record per sampled request (order of decision)
-    int *samp_count;     // number of records in samp_list
+    SampInfo *samp_list; // [B] one record per sampled request, in request order
+    int *samp_count;     // number of sampled requests (records in samp_list), from sv_prep
     // confidence-scheduled verification (spec_verify_scheduled)
     const float *sched_mp;  // [B, K] draft max-probabilities: sv_prep takes L from the
                             // threshold schedule of these (verify_len unused), or null
@@ -192,6 +193,10 @@ __device__ __forceinline__ int schedule_threshold(const float *mp, int K, float 
 }
 
 constexpr int kPrepThreads = 1024;
+// Threads of the per-batch set-up kernel for B requests: one per request up to
+// kPrepThreads (each thread adds the warp totals before its own, so a block
+// no larger than the batch keeps that short).
+static inline int prep_threads(int B) { return B >= kPrepThreads ? kPrepThreads : ((B + 31) / 32) * 32; }
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bounded wait: 2 s
 // Diagnostics: the DIAG instantiations of the bulk-copy kernels (launched only
 // while the switch is on) make every warp first wait on a barrier nothing
@@ -206,22 +211,24 @@ __device__ __forceinline__ bool diag_wait_runs_out(uint64_t *never) {
 }
 
 __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
-    __shared__ int warp_tot[kPrepThreads / 32];
-    __shared__ int carry_s;
+    __shared__ int warp_tot[kPrepThreads / 32], warp_smp[kPrepThreads / 32];
+    __shared__ int carry_s, carry_o;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int nthr = blockDim.x, nw = nthr >> 5;  // a multiple of 32, at most kPrepThreads
     if (tid == 0) {
         carry_s = 0;
-        if (P.k0 == 0) *P.samp_count = 0;
+        carry_o = 0;
     }
     __syncthreads();
     pdl_trigger();
     const bool first_wave = P.k0 == 0;
-    for (int base = 0; base < P.B; base += kPrepThreads) {
+    for (int base = 0; base < P.B; base += nthr) {
         const int b = base + tid;
-        int n = 0, L = 0, greedy = 1, nt = 0;
+        int n = 0, L = 0, greedy = 1, nt = 0, smp = 0;
         float cval = 0.f;
+        ReqInfo ri;
         if (b < P.B && !first_wave) {  // a later wave: the records exist, finished requests drop out
-            const ReqInfo ri = P.req[b];
+            ri = P.req[b];
             L = ri.L;
             greedy = ri.greedy;
             cval = ri.c;
@@ -242,7 +249,7 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
             // step then ignores, and this kernel, which the statistics pass
             // waits for, loads no tokens)
             greedy = !(isfinite(T) && T >= FLT_MIN);
-            ReqInfo ri;
+            smp = greedy ? 0 : 1;
             ri.L = L;
             ri.greedy = greedy;
             ri.T = T;
@@ -251,36 +258,58 @@ __global__ void __launch_bounds__(kPrepThreads) sv_prep(Params P) {
             } else {
                 ri.c = 0.f; ri.c_hi = 0.f; ri.c_lo = 0.f;
             }
-            P.req[b] = ri;
             cval = ri.c;
             if (st && P.dev_status) atomicOr(P.dev_status, st);
             if (P.ee_done) P.ee_done[b] = 0;
             n = wave_rows(L, greedy != 0, P.k0, P.k1, nt);
             if (P.draft_ready) n = nt;  // draft partials exist: target rows only
         }
-        // block exclusive scan of n
-        int incl = n;
+        // block exclusive scans of n (row-list offsets) and, in the first
+        // wave, of the sampled flags (samp_list entries in request order)
+        int incl = n, incl_o = smp;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += v;
+            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            const int vo = __shfl_up_sync(0xFFFFFFFFu, incl_o, o);
+            if (lane >= o) {
+                incl += v;
+                incl_o += vo;
+            }
         }
-        if (lane == 31) warp_tot[w] = incl;
+        if (lane == 31) {
+            warp_tot[w] = incl;
+            warp_smp[w] = incl_o;
+        }
         __syncthreads();
-        int woff = 0;
-        for (int i = 0; i < w; ++i) woff += warp_tot[i];
-        int block_tot = 0;
-        for (int i = 0; i < kPrepThreads / 32; ++i) block_tot += warp_tot[i];
+        int woff = 0, woff_o = 0, block_tot = 0, block_o = 0;
+        for (int i = 0; i < nw; ++i) {
+            if (i < w) {
+                woff += warp_tot[i];
+                woff_o += warp_smp[i];
+            }
+            block_tot += warp_tot[i];
+            block_o += warp_smp[i];
+        }
         const int off = carry_s + woff + incl - n;
         if (b < P.B) {
+            if (first_wave) {
+                ri.ord = smp ? carry_o + woff_o + incl_o - smp : -1;
+                P.req[b] = ri;
+            }
             for (int r = 0; r < n; ++r)
                 P.rows[off + r] = make_int4(b, wave_slot(r, nt, P.k0, P.K), greedy, __float_as_int(cval));
         }
         __syncthreads();
-        if (tid == 0) carry_s += block_tot;
+        if (tid == 0) {
+            carry_s += block_tot;
+            carry_o += block_o;
+        }
         __syncthreads();
     }
-    if (tid == 0) *P.row_count = carry_s;
+    if (tid == 0) {
+        *P.row_count = carry_s;
+        if (first_wave) *P.samp_count = carry_o;
+    }
 }
 
 // ------------------------------------------------------------------ 2. statistics pass
@@ -801,7 +830,7 @@ __global__ void __launch_bounds__(kThreads, MINB) sv_decide(Params P) {
             si.pad0 = 0;
             si.u = a < 32 ? ua : uniform_sample(P.seed, (uint32_t)b, (uint32_t)a);
             si.pad1 = 0.0;
-            P.samp_list[atomicAdd(P.samp_count, 1)] = si;  // order is irrelevant to the results
+            P.samp_list[rq.ord] = si;
         }
     }
     if (P.dbg_rows) {
@@ -869,8 +898,8 @@ struct SShared {
     unsigned long long never[kSWarps];  // diagnostics: a barrier nothing completes
 };
 
-// Items = (sampled request, 4 KiB chunk) over the list sv_decide built, in
-// request-major order; warp w takes the contiguous range
+// Items = (sampled request, 4 KiB chunk) over the list sv_decide built (in
+// request order), request-major; warp w takes the contiguous range
 // [w n / W, (w + 1) n / W), so it changes request (and reloads the request's
 // SampInfo) at most a few times.  Per item it writes the chunk's {D, Bm}; the
 // exact sums are written once per (warp, request) segment, at the segment's
@@ -2534,7 +2563,7 @@ template <int DT, bool VEC>
 static void launch_all(const Params &P, const DevInfo &d, cudaStream_t s) {
     // sv_prep is an ordinary launch: it starts only after all earlier work of
     // the stream, so the workspace of a previous call is free again.
-    sv_prep<<<1, kPrepThreads, 0, s>>>(P);
+    sv_prep<<<1, prep_threads(P.B), 0, s>>>(P);
     if (g_prof_start) cudaEventRecord(g_prof_start, s);
     launch_dependent(g_diag_timeout ? sv_pass1<DT, VEC, true> : sv_pass1<DT, VEC>,
                      d.sms * d.occ_p1[DT][VEC], kP1Warps * 32, VEC ? kP1Smem : 0, s, P);
@@ -2563,7 +2592,7 @@ static void launch_waves(const Params &P0, const DevInfo &d, cudaStream_t s, int
     for (int w = 0; w < nw; ++w) {
         P.k0 = w == 0 ? 0 : W;
         P.k1 = (w == 0 && nw == 2) ? W : P.K;
-        sv_prep<<<1, kPrepThreads, 0, s>>>(P);
+        sv_prep<<<1, prep_threads(P.B), 0, s>>>(P);
         launch_dependent(sv_pass1<DT, VEC>, d.sms * d.occ_p1[DT][VEC], kP1Warps * 32,
                          VEC ? kP1Smem : 0, s, P);
         launch_dependent(decide_kernel<DT>(d, P.B), P.B, kThreads, 0, s, P);
@@ -2991,7 +3020,7 @@ spec_status_t spec_verify_lmhead(const void *hidden_target, const void *hidden_d
     P.samp_stride = shared ? 2 : 1;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // 1. per-request set-up (lengths, greedy / sampled, the sampled-request count)
-    sv::sv_prep<<<1, sv::kPrepThreads, 0, s>>>(P);
+    sv::sv_prep<<<1, sv::prep_threads(P.B), 0, s>>>(P);
     // 2. the products of the target and draft rows; their epilogues leave the
     //    row statistics (and the logit at each draft token) in the workspace
     sv::LmStatsEpi ep{P.part, reinterpret_cast<float *>(ws + L.gz), draft_tokens, temperature,
