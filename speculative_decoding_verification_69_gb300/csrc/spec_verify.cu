@@ -1498,7 +1498,7 @@ constexpr int kTreeWarps = kTreeThreads / 32;
 constexpr int kTreeStep = 256;     // elements a warp covers per step: 8 per lane
 constexpr int kTreeGroups = 256;   // recorded masses per warp (groups of steps)
 constexpr float kTreeBias = 2.0f;  // every summed weight is at most ~1
-constexpr int kTreeStageMax = 192 * 1024;  // dynamic shared memory for a staged slice (two rows)
+constexpr int kTreeStageMax = 176 * 1024;  // dynamic shared memory for a staged slice (two rows)
 
 // The weight 2^(z c + base) of one element, base = l - m c for a row with
 // max m and log2(1/S) = l: one FMA per element.  The rounding of base scales
@@ -1672,17 +1672,38 @@ __device__ __forceinline__ int crossing_lane(double m, double base, double thr, 
 // lane l the 8 elements at 8 l of each step, kU steps' loads in flight.  Writes
 // the warp's sums (as doubles) to red[w]; with `record`, also the mass of each
 // group of steps to mass[w * kTreeGroups + g] and the warp's total as their sum.
+// Mode First with `record` (the first residual's threshold is not known yet):
+// red[w] = {sum a, sum b (exact), sum over a > b of (a - b), of b}, the last
+// two also per group, in mass[] and mass2[].
 template <int DT, bool VEC>
 __device__ void tree_pass(const char *rowt, const char *rowd, const char *stt, const char *std_,
                           int V, int rank, int cs, const TreeNodeC &nc, int mode, bool record,
-                          double (*red)[4], float *mass, int warp, int lane) {
+                          double (*red)[4], float *mass, float *mass2, int warp, int lane) {
     constexpr int kU = DT == kBF16 ? 2 : 1;  // steps per batch; two batches in flight
     const TreeSplit sp(V, rank, cs, warp);
     BiasAcc2 acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i].init(kTreeBias);
-    float gs = 0.f;   // this lane's part of the current group
-    double mw = 0.0;  // the warp's recorded total (lane 0)
+    float gs = 0.f, gs2 = 0.f;  // this lane's parts of the current group
+    double mw = 0.0, mw2 = 0.0;  // the warp's recorded totals (lane 0)
+    // close the group of step st (the last of its group or of the warp's steps)
+    auto close_group = [&](int st, bool two) {
+        const int k = st - sp.s0;
+        if ((k + 1) % sp.gsz == 0 || st + 1 == sp.s1) {
+            const float gm = warp_sum(gs);
+            const float gm2 = two ? warp_sum(gs2) : 0.f;
+            if (lane == 0) {
+                mass[warp * kTreeGroups + k / sp.gsz] = gm;
+                mw += (double)gm;
+                if (two) {
+                    mass2[warp * kTreeGroups + k / sp.gsz] = gm2;
+                    mw2 += (double)gm2;
+                }
+            }
+            gs = 0.f;
+            gs2 = 0.f;
+        }
+    };
     auto load = [&](Eight<DT, VEC> (&zt)[kU], Eight<DT, VEC> (&zd)[kU], int st0) {
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
@@ -1704,6 +1725,7 @@ __device__ void tree_pass(const char *rowt, const char *rowd, const char *stt, c
         for (int u = 0; u < kU; ++u) {
             if (st0 + u >= sp.s1) break;
             if (mode == kTreeModeFirst) {
+                float ld = 0.f, lb = 0.f;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float2 a = wpair(zt[u].pair(i), nc.c2, nc.bt);
@@ -1711,9 +1733,21 @@ __device__ void tree_pass(const char *rowt, const char *rowd, const char *stt, c
                     acc[0].add(a);
                     acc[1].add(bq);
                     const bool gx = a.x > bq.x, gy = a.y > bq.y;
-                    acc[2].add(make_float2(gx ? __fsub_rn(a.x, bq.x) : 0.f,
-                                           gy ? __fsub_rn(a.y, bq.y) : 0.f));
-                    acc[3].add(make_float2(gx ? bq.x : 0.f, gy ? bq.y : 0.f));
+                    const float2 dd = make_float2(gx ? __fsub_rn(a.x, bq.x) : 0.f,
+                                                  gy ? __fsub_rn(a.y, bq.y) : 0.f);
+                    const float2 bb = make_float2(gx ? bq.x : 0.f, gy ? bq.y : 0.f);
+                    if (record) {
+                        ld = __fadd_rn(ld, __fadd_rn(dd.x, dd.y));
+                        lb = __fadd_rn(lb, __fadd_rn(bb.x, bb.y));
+                    } else {
+                        acc[2].add(dd);
+                        acc[3].add(bb);
+                    }
+                }
+                if (record) {
+                    gs = __fadd_rn(gs, ld);
+                    gs2 = __fadd_rn(gs2, lb);
+                    close_group(st0 + u, true);
                 }
             } else {
                 float w[8];
@@ -1723,15 +1757,7 @@ __device__ void tree_pass(const char *rowt, const char *rowd, const char *stt, c
 #pragma unroll
                     for (int i = 0; i < 8; ++i) ls = __fadd_rn(ls, w[i]);
                     gs = __fadd_rn(gs, ls);
-                    const int k = st0 + u - sp.s0;
-                    if ((k + 1) % sp.gsz == 0 || st0 + u + 1 == sp.s1) {
-                        const float gm = warp_sum(gs);
-                        if (lane == 0) {
-                            mass[warp * kTreeGroups + k / sp.gsz] = gm;
-                            mw += (double)gm;
-                        }
-                        gs = 0.f;
-                    }
+                    close_group(st0 + u, false);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) acc[0].add(make_float2(w[2 * i], w[2 * i + 1]));
@@ -1748,6 +1774,16 @@ __device__ void tree_pass(const char *rowt, const char *rowd, const char *stt, c
         consume(ta, da, st0);
         load(ta, da, st0 + 2 * kU);
         consume(tb, db, st0 + kU);
+    }
+    if (record && mode == kTreeModeFirst) {
+        const FF ta = warp_sum_ff(acc[0].total()), tb = warp_sum_ff(acc[1].total());
+        if (lane == 0) {
+            red[warp][0] = ff_to_double(ta);
+            red[warp][1] = ff_to_double(tb);
+            red[warp][2] = mw;
+            red[warp][3] = mw2;
+        }
+        return;
     }
     if (record) {
         if (lane == 0) red[warp][0] = mw;
@@ -1899,6 +1935,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
     __shared__ float s_u[SPEC_MAX_TREE], s_g[SPEC_MAX_TREE], s_gd[SPEC_MAX_TREE];
     __shared__ double s_us[SPEC_MAX_TREE];
     __shared__ float s_mass[kTreeWarps * kTreeGroups];
+    __shared__ float s_mass2[kTreeWarps * kTreeGroups];  // a merged first pass: sum of b per group
     __shared__ double s_red[kTreeWarps][4];
     __shared__ double s_slot[2][4];   // this CTA's sums, read by the cluster (two buffers)
     __shared__ double s_sum;          // S_j of the current residual
@@ -1976,6 +2013,9 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
         nc.bd = make_float2(bd, bd);
         nc.s = 0.f;
         bool staged = false;  // this node's slice is in shared memory (this warp's steps)
+        // the only candidate left was the first and it was rejected: the
+        // recording pass also forms the exact sums (one pass instead of two)
+        bool first_rec = false;
         if (warp == 0) {  // the children of cur with a token in [0, V), in index order
             int n = 0;
             for (int base = cur + 1; base < N; base += 32) {
@@ -2077,10 +2117,15 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
                 }
                 ++stagings;
             }
+            if (J == 1 && !more) {
+                first_rec = true;
+                break;
+            }
             const char *stt = staged ? (const char *)s_stage : nullptr;
             const char *std_ = staged ? (const char *)s_stage + stage_row_bytes : nullptr;
             const int mode = J == 1 ? kTreeModeFirst : kTreeModeThr;
-            tree_pass<DT, VEC>(rowt, rowd, stt, std_, V, rank, cs, nc, mode, false, s_red, s_mass, warp, lane);
+            tree_pass<DT, VEC>(rowt, rowd, stt, std_, V, rank, cs, nc, mode, false, s_red, s_mass, s_mass2,
+                               warp, lane);
             __syncthreads();
             const int nsum = mode == kTreeModeFirst ? 4 : 1;
             if (warp == 0) warp_sums_to_slot(s_red, s_slot[par], nsum, lane);
@@ -2133,14 +2178,39 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
         const char *stt = staged ? (const char *)s_stage : nullptr;
         const char *std_ = staged ? (const char *)s_stage + stage_row_bytes : nullptr;
         for (;;) {
-            const int mode = nc.s > 0.f ? kTreeModeThr : kTreeModeP;
-            tree_pass<DT, VEC>(rowt, rowd, stt, std_, V, rank, cs, nc, mode, true, s_red, s_mass, warp, lane);
+            const int mode = first_rec ? kTreeModeFirst : nc.s > 0.f ? kTreeModeThr : kTreeModeP;
+            tree_pass<DT, VEC>(rowt, rowd, stt, std_, V, rank, cs, nc, mode, true, s_red, s_mass, s_mass2,
+                               warp, lane);
             __syncthreads();
-            if (warp == 0) warp_sums_to_slot(s_red, s_slot[par], 1, lane);
+            if (warp == 0) warp_sums_to_slot(s_red, s_slot[par], first_rec ? 4 : 1, lane);
             cluster_sync_all();
+            double k1 = 0.0;  // merged first pass: 1 - s_1
+            if (first_rec) {
+                // s_1 = A / B from the exact sums, then the residual max(0, a - s_1 b)
+                // of each group and warp as D + (1 - s_1) Bm over a > b (the two
+                // supports differ only at near ties, as for the mass S_1 above)
+                double tot[4];
+                if (warp == 0) cluster_totals(s_slot[par], 4, cs, lane, tot);
+                if (tid == 0) {
+                    s_SA = tot[0];
+                    s_SB = tot[1];
+                    s_iSB = 1.0 / tot[1];
+                    s_s = (float)(tot[0] * s_iSB);
+                }
+                __syncthreads();
+                nc.s = s_s;
+                k1 = 1.0 - (double)nc.s;
+                for (int i = tid; i < kTreeWarps * kTreeGroups; i += kTreeThreads)
+                    s_mass[i] = fmaxf(0.f, (float)((double)s_mass[i] + k1 * (double)s_mass2[i]));
+                if (lane == 0) s_red[warp][0] = fmax(0.0, s_red[warp][2] + k1 * s_red[warp][3]);
+                __syncthreads();
+            }
             if (warp == 0) {
                 // the masses of the cluster's CTAs, their total, the threshold
-                const double Mr = lane < cs ? ld_cluster_f64(&s_slot[par][0], lane) : 0.0;
+                const double Mr = lane >= cs ? 0.0
+                                  : first_rec ? fmax(0.0, ld_cluster_f64(&s_slot[par][2], lane) +
+                                                              k1 * ld_cluster_f64(&s_slot[par][3], lane))
+                                              : ld_cluster_f64(&s_slot[par][0], lane);
                 const double Z = warp_sum_d(Mr);
                 const double thr = s_us[cur] * Z;
                 // the CTA whose slice holds the crossing, then (in it) the warp
@@ -2154,7 +2224,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
                 }
                 if (lane == 0) {
                     s_again = 0;
-                    if (!(Z > 0.0) && mode == kTreeModeThr) {  // no residual mass: p
+                    if (!(Z > 0.0) && mode != kTreeModeP) {  // no residual mass: p
                         s_s = 0.f;
                         s_again = 1;
                     }
@@ -2167,6 +2237,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sv_tree_walk(Params P, const 
             }
             par ^= 1;
             __syncthreads();
+            first_rec = false;
             if (!s_again) break;
             nc.s = s_s;
         }
