@@ -603,7 +603,10 @@ __global__ void __launch_bounds__(kP1Warps * 32, 1) sv_pass1(Params P) {
 // ------------------------------------------------------------------ 3. decide
 
 constexpr int kPerLane = 4;      // chunk records held in registers per lane (128 per warp)
-constexpr int kRowsPerWarp = 3;  // rows whose chunk records one warp loads at once
+// rows whose chunk records one warp loads at once: 5 (8 warps cover K = 16's
+// 33 rows in one round) at the compiler's register budget, 3 in the build cut
+// to 64 registers
+template <int MINB> __host__ __device__ constexpr int rows_per_warp() { return MINB >= 4 ? 3 : 5; }
 
 // Row statistics from one block of up to 32 * kPerLane chunk records held by
 // the warp: {max, S (sampled rows), lowest argmax bits (greedy rows)}.
@@ -724,11 +727,12 @@ __global__ void __launch_bounds__(kThreads, MINB) sv_decide(Params P) {
     int nt;
     const int nrows = wave_rows(L, greedy, k0, P.k1, nt);
     if (P.npart <= 32 * kPerLane) {
-        // each warp loads the records of up to kRowsPerWarp rows, then reduces them
-        for (int r0 = warp; r0 < nrows; r0 += kWarps * kRowsPerWarp) {
-            float4 q[kRowsPerWarp][kPerLane];
+        // each warp loads the records of up to RPW rows, then reduces them
+        constexpr int RPW = rows_per_warp<MINB>();
+        for (int r0 = warp; r0 < nrows; r0 += kWarps * RPW) {
+            float4 q[RPW][kPerLane];
 #pragma unroll
-            for (int j = 0; j < kRowsPerWarp; ++j) {
+            for (int j = 0; j < RPW; ++j) {
                 const int r = r0 + j * kWarps;
                 const float4 *pp =
                     P.part + ((size_t)b * P.nslot + wave_slot(r < nrows ? r : 0, nt, k0, K)) * P.npart;
@@ -739,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, MINB) sv_decide(Params P) {
                 }
             }
 #pragma unroll
-            for (int j = 0; j < kRowsPerWarp; ++j) {
+            for (int j = 0; j < RPW; ++j) {
                 const int r = r0 + j * kWarps;
                 if (r < nrows) {
                     float m = -INFINITY, S = 0.f;
