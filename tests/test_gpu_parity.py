@@ -238,11 +238,12 @@ def test_ties_lowest_index():
     assert (gpu["accept_len"][1::2] == K).all()
 
 
-@pytest.mark.parametrize("B", [1024, 1100])
+@pytest.mark.parametrize("B", [33, 1024, 1100, 2049])
 def test_large_batches(B):
-    """Batches larger than the per-request kernel's 1024 threads (its scan
-    carries across blocks): ragged, mixed batches checked in full against the
-    oracle."""
+    """Batches sized around the per-request kernel's block (one thread per
+    request up to 1024, so 33 requests run two warps, the last with one
+    request; above 1024 its scans carry across blocks): ragged, mixed batches
+    checked in full against the oracle."""
     K, V = 3, 640
     g = torch.Generator().manual_seed(11)
     L = torch.randint(0, K + 1, (B,), generator=g).tolist()
