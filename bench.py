@@ -878,8 +878,16 @@ def run_ours(args, world, rank, local):
     h_acc = torch.empty((B,), dtype=torch.int32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = h_out.numel() * 4 + h_acc.numel() * 4
+    # lengths known on the host: spec_verify_from_host copies only the rows the
+    # step reads (the schedules form the lengths on the device: whole tensors)
+    from_host = not (chain or scheduled or ee)
+    hv = sv.HostVerifier(dev) if from_host else None
 
     def e2e_step():
+        if from_host:
+            hv(host["target"], host["draft"], host["tokens"], host.get("verify_len"),
+               host["temperature"], inp["seed"], out_tokens=h_out, accept_len=h_acc)
+            return
         for k, v in host.items():
             dbuf[k].copy_(v, non_blocking=True)
         if chain:
@@ -900,10 +908,12 @@ def run_ours(args, world, rank, local):
         h_out.copy_(o, non_blocking=True)
         h_acc.copy_(a, non_blocking=True)
 
-    e2e_steps = max(1, min(args.steps, 100))  # each copies the whole batch over the host link
+    e2e_steps = max(1, min(args.steps, 100))  # each copies the batch over the host link
     for _ in range(max(1, args.warmup)):
         e2e_step()
     torch.cuda.synchronize()
+    if from_host:
+        h2d = hv.last_h2d_bytes  # the rows the step reads, plus tokens, lengths, temperatures
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(e2e_steps)]
     barrier(world)
@@ -988,7 +998,11 @@ def run_ours(args, world, rank, local):
             "kernel_ms": kern_avg_s * 1e3,
         },
         "e2e": {"value": e2e_value, "unit": "positions/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "path": ("spec_verify_from_host: pinned host inputs, the logit rows the step "
+                         "reads copied to the device, outputs copied back" if from_host else
+                         "pinned host tensors copied whole to the device, the call, outputs "
+                         "copied back")},
         "gpu_launches": launches,
         "clocks": clk,
         "wall_s": t_wall,

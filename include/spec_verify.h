@@ -429,6 +429,49 @@ spec_status_t spec_verify_noalloc(const void *target_logits, const void *draft_l
                                   int32_t *accept_len, uint32_t *dev_status, void *stream);
 
 /*
+ * spec_verify_from_host -- spec_verify for inputs held in host memory, with
+ * the copies over the host link limited to what the step reads.  The step of
+ * "Спекулятивный декодинг в проде" (kiosknews.app), "Правило проверки", reads
+ * for request b, with L_b its verify length clamped to [0, K], the target rows
+ * 0..L_b and, when the request is sampled, the draft rows 0..L_b-1; a greedy
+ * request reads no draft row.  The call, in stream order:
+ *   1. copies draft_tokens, verify_len (when given) and temperature to their
+ *      device buffers, and those rows of the logits to the same places of
+ *      target_dev / draft_dev (one copy per run of adjacent rows);
+ *   2. runs spec_verify on the device buffers;
+ *   3. copies out_tokens_dev and accept_len_dev to out_tokens_host and
+ *      accept_len_host.
+ *   *_host inputs          host memory with spec_verify's layouts; the
+ *                          greedy / sampled split and the clamp follow
+ *                          spec_verify's rules (T not a finite value >=
+ *                          FLT_MIN: greedy), read from verify_len_host and
+ *                          temperature_host during the call.  verify_len_host
+ *                          NULL: L_b = K (verify_len_dev is then unused).
+ *   target_dev, draft_dev  device [B, K+1, V] / [B, K, V] buffers, 16-byte
+ *                          aligned; rows the step does not read keep whatever
+ *                          they held.
+ *   draft_tokens_dev, verify_len_dev, temperature_dev, out_tokens_dev,
+ *   accept_len_dev         device buffers of spec_verify's shapes.
+ *   out_tokens_host, accept_len_host   host outputs [B, K+1], [B].
+ *   workspace, dev_status  as spec_verify.
+ *   h2d_bytes              nullable: the bytes copied host to device.
+ * Everything is asynchronous on `stream` and nothing is allocated: the host
+ * buffers must stay valid and unchanged until the stream has passed the
+ * call (pinned host memory lets the copies run asynchronously).  Errors as
+ * spec_verify, plus SPEC_ERR_INVALID_ARG for a missing buffer and
+ * SPEC_ERR_CUDA when a copy cannot be enqueued (copies already enqueued may
+ * then have run).
+ */
+spec_status_t spec_verify_from_host(
+    const void *target_host, const void *draft_host, spec_dtype_t dtype,
+    const int32_t *draft_tokens_host, const int32_t *verify_len_host,
+    const float *temperature_host, uint64_t seed, int B, int K, int V, void *target_dev,
+    void *draft_dev, int32_t *draft_tokens_dev, int32_t *verify_len_dev, float *temperature_dev,
+    int32_t *out_tokens_dev, int32_t *accept_len_dev, int32_t *out_tokens_host,
+    int32_t *accept_len_host, void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+    void *stream, size_t *h2d_bytes);
+
+/*
  * spec_debug_force_wait_timeout -- diagnostics only: while enabled (1), every
  * warp of the bulk-copy kernels in later spec_verify calls (any device) first
  * waits on a barrier nothing completes; that bounded wait runs out after 1 ms

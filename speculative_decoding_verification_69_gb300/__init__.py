@@ -86,6 +86,10 @@ def load_library():
     L.spec_verify_lmhead.restype = ctypes.c_int
     L.spec_verify_noalloc.argtypes = common[:12] + [u32p, vp]
     L.spec_verify_noalloc.restype = ctypes.c_int
+    L.spec_verify_from_host.argtypes = (common[:10] + [vp, vp, i32p, i32p, f32p, i32p, i32p, i32p, i32p,
+                                                       vp, ctypes.c_size_t, u32p, vp,
+                                                       ctypes.POINTER(ctypes.c_size_t)])
+    L.spec_verify_from_host.restype = ctypes.c_int
     L.spec_profile_events.argtypes = [vp, vp]
     L.spec_profile_events.restype = None
     L.spec_verify_kernel_count.argtypes = []
@@ -104,7 +108,7 @@ def exported_symbols():
             "spec_verify_tree", "spec_verify_tree_distinct",
             "spec_draft_confidence", "spec_schedule_budget", "spec_verify_scheduled",
             "spec_lmhead_workspace_bytes", "spec_verify_lmhead",
-            "spec_schedule_len", "spec_verify_noalloc",
+            "spec_schedule_len", "spec_verify_noalloc", "spec_verify_from_host",
             "spec_profile_events", "spec_debug_force_wait_timeout",
             "spec_verify_kernel_count", "spec_status_str"]
 
@@ -237,6 +241,74 @@ class Verifier:
         else:
             st = L.spec_verify(*args, _stream(stream))
         _check(st)
+        return out_tokens, accept_len
+
+
+class HostVerifier:
+    """spec_verify for inputs in host memory (spec_verify_from_host): owns the
+    device buffers and the workspace for the last shape it saw, copies only
+    the logit rows the step reads, and returns the outputs in host memory.
+    Host tensors should be pinned so the copies run asynchronously; the call
+    is asynchronous on `stream`, so synchronise before reading the outputs or
+    changing the inputs."""
+
+    def __init__(self, device=None):
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        self._key = None
+        self._d = None
+        self.last_h2d_bytes = 0
+
+    def _buffers(self, B, K, V, dtype):
+        key = (B, K, V, dtype)
+        if self._key != key:
+            dev = self.device
+            n = workspace_bytes(B, K, V, dtype)
+            self._d = dict(
+                target=torch.empty((B, K + 1, V), dtype=dtype, device=dev),
+                draft=torch.empty((B, K, V), dtype=dtype, device=dev),
+                tokens=torch.empty((B, K), dtype=torch.int32, device=dev),
+                verify_len=torch.empty((B,), dtype=torch.int32, device=dev),
+                temperature=torch.empty((B,), dtype=torch.float32, device=dev),
+                out_tokens=torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+                accept_len=torch.empty((B,), dtype=torch.int32, device=dev),
+                ws=torch.empty(max(n, 256), dtype=torch.uint8, device=dev))
+            self._key = key
+        return self._d
+
+    def __call__(self, target, draft, tokens, verify_len, temperature, seed, *, out_tokens=None,
+                 accept_len=None, dev_status=None, stream=None):
+        L = load_library()
+        if target.dim() != 3:
+            raise ValueError("target must be [B, K+1, V]")
+        B, K1, V = target.shape
+        K = K1 - 1
+        host = (target, draft, tokens, temperature) + ((verify_len,) if verify_len is not None else ())
+        for t in host:
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError("inputs must be contiguous host tensors")
+        if draft.shape != (B, K, V) or draft.dtype != target.dtype:
+            raise ValueError("draft must be [B, K, V] with the target's dtype")
+        if tokens.shape != (B, K) or tokens.dtype != torch.int32:
+            raise ValueError("tokens must be int32 [B, K]")
+        if verify_len is not None and (verify_len.shape != (B,) or verify_len.dtype != torch.int32):
+            raise ValueError("verify_len must be int32 [B] or None")
+        if temperature.shape != (B,) or temperature.dtype != torch.float32:
+            raise ValueError("temperature must be float32 [B]")
+        d = self._buffers(B, K, V, target.dtype)
+        if out_tokens is None:
+            out_tokens = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+        if accept_len is None:
+            accept_len = torch.empty((B,), dtype=torch.int32).pin_memory()
+        nbytes = ctypes.c_size_t(0)
+        with torch.cuda.device(self.device):
+            _check(L.spec_verify_from_host(
+                _ptr(target), _ptr(draft), _dtype_code(target), _ptr(tokens), _ptr(verify_len),
+                _ptr(temperature), int(seed) & 0xFFFFFFFFFFFFFFFF, B, K, V, _ptr(d["target"]),
+                _ptr(d["draft"]), _ptr(d["tokens"]), _ptr(d["verify_len"]), _ptr(d["temperature"]),
+                _ptr(d["out_tokens"]), _ptr(d["accept_len"]), _ptr(out_tokens), _ptr(accept_len),
+                _ptr(d["ws"]), d["ws"].numel(), _ptr(dev_status), _stream(stream),
+                ctypes.byref(nbytes)))
+        self.last_h2d_bytes = int(nbytes.value)
         return out_tokens, accept_len
 
 

@@ -2904,6 +2904,37 @@ static bool lm_setup(DevInfo &d) {
 
 } // namespace sv
 
+namespace sv {
+// Host-to-device copies of byte ranges, each merged into the previous one when
+// it continues it in both memories; `total` counts the bytes enqueued.
+struct H2DRuns {
+    cudaStream_t s = nullptr;
+    const char *src = nullptr;
+    char *dst = nullptr;
+    size_t n = 0, total = 0;
+    bool ok = true;
+    void add(const void *from, void *to, size_t bytes) {
+        const char *f = static_cast<const char *>(from);
+        char *t = static_cast<char *>(to);
+        if (!bytes) return;
+        if (n && f == src + n && t == dst + n) {
+            n += bytes;
+            return;
+        }
+        flush();
+        src = f;
+        dst = t;
+        n = bytes;
+    }
+    void flush() {
+        if (!n) return;
+        if (cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, s) != cudaSuccess) ok = false;
+        total += n;
+        n = 0;
+    }
+};
+}  // namespace sv
+
 extern "C" {
 
 size_t spec_verify_workspace_bytes(int B, int K, int V, spec_dtype_t dtype) {
@@ -3392,6 +3423,67 @@ spec_status_t spec_verify_noalloc(const void *target_logits, const void *draft_l
                            temperature, seed, B, K, V, out_tokens, accept_len,
                            g_noalloc_ptr[dev], (size_t)SPEC_NOALLOC_SCRATCH_BYTES, dev_status,
                            nullptr, nullptr, stream);
+}
+
+spec_status_t spec_verify_from_host(
+    const void *target_host, const void *draft_host, spec_dtype_t dtype,
+    const int32_t *draft_tokens_host, const int32_t *verify_len_host,
+    const float *temperature_host, uint64_t seed, int B, int K, int V, void *target_dev,
+    void *draft_dev, int32_t *draft_tokens_dev, int32_t *verify_len_dev, float *temperature_dev,
+    int32_t *out_tokens_dev, int32_t *accept_len_dev, int32_t *out_tokens_host,
+    int32_t *accept_len_host, void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+    void *stream, size_t *h2d_bytes) {
+    if (!target_host || !draft_host || !draft_tokens_host || !temperature_host || !draft_tokens_dev ||
+        !temperature_dev || !out_tokens_host || !accept_len_host || (verify_len_host && !verify_len_dev))
+        return SPEC_ERR_INVALID_ARG;
+    int32_t *vlen_dev = verify_len_host ? verify_len_dev : nullptr;
+    // every argument check of the step first: nothing is copied on an error
+    sv::Params P;
+    sv::Layout L;
+    const spec_status_t st = sv::step_params(P, target_dev, draft_dev, dtype, draft_tokens_dev,
+                                             vlen_dev, temperature_dev, seed, B, K, V, out_tokens_dev,
+                                             accept_len_dev, workspace, workspace_bytes, dev_status, L);
+    if (st != SPEC_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t row = (size_t)V * (dtype == SPEC_DTYPE_BF16 ? 2u : 4u);
+    sv::H2DRuns small, tgt, drf;
+    small.s = tgt.s = drf.s = s;
+    small.add(draft_tokens_host, draft_tokens_dev, (size_t)B * K * sizeof(int32_t));
+    small.flush();
+    if (verify_len_host) small.add(verify_len_host, verify_len_dev, (size_t)B * sizeof(int32_t));
+    small.flush();
+    small.add(temperature_host, temperature_dev, (size_t)B * sizeof(float));
+    small.flush();
+    const char *th = static_cast<const char *>(target_host), *dh = static_cast<const char *>(draft_host);
+    char *td = static_cast<char *>(target_dev), *dd = static_cast<char *>(draft_dev);
+    for (int b = 0; b < B; ++b) {
+        // the rows request b's step reads (the rules of sv_prep)
+        int Lb = verify_len_host ? verify_len_host[b] : K;
+        Lb = Lb < 0 ? 0 : (Lb > K ? K : Lb);
+        const float T = temperature_host[b];
+        const bool greedy = !(std::isfinite(T) && T >= FLT_MIN);
+        const size_t t0 = (size_t)b * (size_t)(K + 1) * row;
+        tgt.add(th + t0, td + t0, (size_t)(Lb + 1) * row);
+        if (!greedy) {
+            const size_t d0 = (size_t)b * (size_t)K * row;
+            drf.add(dh + d0, dd + d0, (size_t)Lb * row);
+        }
+    }
+    tgt.flush();
+    drf.flush();
+    if (!small.ok || !tgt.ok || !drf.ok) return SPEC_ERR_CUDA;
+    if (h2d_bytes) *h2d_bytes = small.total + tgt.total + drf.total;
+    const spec_status_t sv_st = sv::verify_impl(target_dev, draft_dev, dtype, draft_tokens_dev, vlen_dev,
+                                                temperature_dev, seed, B, K, V, out_tokens_dev,
+                                                accept_len_dev, workspace, workspace_bytes, dev_status,
+                                                nullptr, nullptr, stream);
+    if (sv_st != SPEC_OK) return sv_st;
+    if (cudaMemcpyAsync(out_tokens_host, out_tokens_dev, (size_t)B * (K + 1) * sizeof(int32_t),
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(accept_len_host, accept_len_dev, (size_t)B * sizeof(int32_t),
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
 }
 
 void spec_profile_events(void *ev_start, void *ev_end) {

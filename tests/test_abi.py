@@ -94,6 +94,29 @@ def test_host_validation_without_gpu(lib):
     assert call_ee(2, ws=None) == 4
 
 
+def test_from_host_validation_without_gpu(lib):
+    """spec_verify_from_host checks every argument before its first copy."""
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    base = dict(th=fake, dh=fake, dt=1, tokh=fake, vlh=None, Th=fake, seed=1, B=2, K=4, V=100,
+                td=fake, dd=fake, tokd=fake, vld=None, Td=fake, od=fake, ad=fake, oh=fake, ah=fake,
+                ws=ctypes.c_void_p(0x10000), wsb=1 << 30, st=None, nb=None)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return lib.spec_verify_from_host(
+            a["th"], a["dh"], a["dt"], a["tokh"], a["vlh"], a["Th"], a["seed"], a["B"], a["K"],
+            a["V"], a["td"], a["dd"], a["tokd"], a["vld"], a["Td"], a["od"], a["ad"], a["oh"],
+            a["ah"], a["ws"], a["wsb"], a["st"], None, a["nb"])
+
+    for k in ("th", "dh", "tokh", "Th", "td", "dd", "tokd", "Td", "od", "ad", "oh", "ah"):
+        assert call(**{k: None}) == 1, k
+    assert call(vlh=fake) == 1                            # host lengths without a device buffer
+    assert call(B=0) == 1 and call(K=33) == 1 and call(V=1) == 1
+    assert call(dt=5) == 2
+    assert call(td=ctypes.c_void_p(0x10008)) == 1         # device logits not 16-byte aligned
+    assert call(ws=None) == 4 and call(wsb=16) == 4
+
+
 def test_tree_host_validation_without_gpu(lib):
     """The tree entry points reject bad sizes, null pointers, misaligned logits
     and small workspaces on the host, before any CUDA call."""
