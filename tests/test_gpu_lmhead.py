@@ -244,3 +244,27 @@ def test_lmhead_bounded_waits_run_out(sv):
                       inp["seed"])
     ng, ns, nu = _compare(out, acc, r, Tn)
     assert ng == 0 and nu == 0 and ns <= 1
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_lmhead_random_exact_cases(sv, i):
+    """Seeded random shapes with exact products: B in [1, 48], K up to 16, V a
+    multiple of 4 from 4 to 20,000, d a multiple of 64 up to 512, mixed
+    temperatures and greedy shares; the logits path's bars against the
+    oracle."""
+    rng = np.random.default_rng(33_000 + i)
+    B = int(rng.integers(1, 49))
+    K = int(rng.choice([1, 2, 4, 8, 16]))
+    V = int(rng.choice([4, 100, 512, 1000, 2052, 4100, 20000]))
+    d = int(rng.choice([64, 128, 192, 320, 512]))
+    T = float(rng.choice([0.5, 1.0, 1.5]))
+    inp = workloads.make_lmhead_inputs(B, K, V, d, seed=40_000 + i, T=T,
+                                       n_greedy=int(rng.integers(0, B + 1)), exact=True)
+    out, acc, st = _run(sv, inp)
+    assert st == 0
+    zt, zd = _oracle_logits(inp)
+    Tn = inp["temperature"].cpu().numpy()
+    r = oracle.verify(zt, zd, inp["tokens"].cpu().numpy(), inp["verify_len"].cpu().numpy(), Tn,
+                      inp["seed"])
+    ng, ns, nu = _compare(out, acc, r, Tn)
+    assert ng == 0 and nu == 0 and ns <= 1, (i, ng, ns, nu)
