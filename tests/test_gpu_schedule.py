@@ -203,3 +203,31 @@ def test_bench_chain_call_full_size(sv):
     gpu = dict(out_tokens=out.cpu().numpy(), accept_len=acc.cpu().numpy())
     ng, ns, nu, nsamp, nflag = compare(gpu, oracle_run(h, idx), h, idx)
     assert ng == 0 and nu == 0 and ns <= 1, (ng, ns, nu, nsamp, nflag)
+
+
+@pytest.mark.parametrize("i", range(30))
+def test_verify_scheduled_random_cases(sv, i):
+    """Seeded random shapes (the fuzz test's generator) through the fused
+    scheduled call, threshold or budget, confidences computed or given:
+    bit-identical to the separate calls, and the lengths equal to the
+    oracle's schedule of the same confidences."""
+    from test_gpu_fuzz import _case
+    rng = np.random.default_rng(55_000 + i)
+    inp = _case(200 + i)
+    B, K = inp["tokens"].shape
+    sched = "threshold" if rng.random() < 0.5 else "budget"
+    kw = (dict(threshold=float(rng.choice([0.05, 0.3, 0.8]))) if sched == "threshold"
+          else dict(budget=int(rng.integers(0, B * K + 3))))
+    given = None
+    if rng.random() < 0.5:
+        given = torch.from_numpy(rng.uniform(0.0, 1.0, size=(B, K)).astype(np.float32)).cuda()
+    ref_out, ref_acc, ref_vl, ref_conf = _unfused(sv, inp, given=given, **kw)
+    out, acc, vl, conf = sv.verify_scheduled(inp["target"], inp["draft"], inp["tokens"],
+                                             inp["temperature"], inp["seed"], draft_maxprob=given,
+                                             **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(vl, ref_vl) and torch.equal(acc, ref_acc) and torch.equal(out, ref_out)
+    mp = (given if given is not None else conf).cpu().numpy()
+    want = (oracle.schedule_len(mp, kw["threshold"]) if sched == "threshold"
+            else oracle.schedule_budget(mp, kw["budget"]))
+    assert np.array_equal(vl.cpu().numpy(), want)
