@@ -878,12 +878,20 @@ def run_ours(args, world, rank, local):
     h_acc = torch.empty((B,), dtype=torch.int32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = h_out.numel() * 4 + h_acc.numel() * 4
-    # lengths known on the host: spec_verify_from_host copies only the rows the
-    # step reads (the schedules form the lengths on the device: whole tensors)
-    from_host = not (chain or scheduled or ee)
+    # spec_verify_from_host copies only the rows the step reads; with given
+    # confidences the scheduled variant forms the lengths on the device and
+    # reads them back first.  Computed confidences need every draft row, and
+    # early exit decides per wave: those copy whole tensors.
+    from_host = not (chain or ee)
     hv = sv.HostVerifier(dev) if from_host else None
+    h_vl = torch.empty((B,), dtype=torch.int32).pin_memory()
 
     def e2e_step():
+        if from_host and scheduled:
+            hv.scheduled(host["target"], host["draft"], host["tokens"], host["temperature"],
+                         inp["seed"], host["draft_maxprob"], threshold=inp["threshold"],
+                         out_tokens=h_out, accept_len=h_acc, verify_len_out=h_vl)
+            return
         if from_host:
             hv(host["target"], host["draft"], host["tokens"], host.get("verify_len"),
                host["temperature"], inp["seed"], out_tokens=h_out, accept_len=h_acc)
@@ -914,6 +922,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     if from_host:
         h2d = hv.last_h2d_bytes  # the rows the step reads, plus tokens, lengths, temperatures
+        if scheduled:
+            d2h += B * 4  # the scheduled lengths, read back before the rows are copied
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(e2e_steps)]
     barrier(world)
@@ -999,7 +1009,11 @@ def run_ours(args, world, rank, local):
         },
         "e2e": {"value": e2e_value, "unit": "positions/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "path": ("spec_verify_from_host: pinned host inputs, the logit rows the step "
+                "path": (("spec_verify_scheduled_from_host: pinned host inputs, the threshold "
+                          "schedule of the given confidences formed on the device and its "
+                          "lengths read back, the logit rows they need copied, outputs copied "
+                          "back") if from_host and scheduled else
+                         "spec_verify_from_host: pinned host inputs, the logit rows the step "
                          "reads copied to the device, outputs copied back" if from_host else
                          "pinned host tensors copied whole to the device, the call, outputs "
                          "copied back")},

@@ -472,6 +472,33 @@ spec_status_t spec_verify_from_host(
     void *stream, size_t *h2d_bytes);
 
 /*
+ * spec_verify_scheduled_from_host -- spec_verify_from_host for lengths set by
+ * a schedule of given draft confidences ("DSpark: спекулятивное
+ * декодирование с верификацией по уверенности…" (iitog.ru), "Ключевые
+ * факты"): the confidences go to the device, the schedule of mode (threshold:
+ * spec_schedule_len; budget: spec_schedule_budget) runs there and writes
+ * verify_len_dev, the lengths come back to verify_len_host, and the call
+ * WAITS for them (one cudaStreamSynchronize of `stream`) before it copies
+ * the logit rows those lengths need and runs the step as
+ * spec_verify_from_host does.  Only that wait is synchronous.
+ *   draft_maxprob_host [B, K] float32 host; maxprob_dev its device buffer.
+ *   verify_len_dev, verify_len_host  [B] int32 device / host (written).
+ *   Other arguments as spec_verify_from_host; h2d_bytes includes the
+ *   confidences.
+ * Errors as spec_verify_from_host and spec_verify_scheduled (mode, budget
+ * size).
+ */
+spec_status_t spec_verify_scheduled_from_host(
+    const void *target_host, const void *draft_host, spec_dtype_t dtype,
+    const int32_t *draft_tokens_host, const float *temperature_host,
+    const float *draft_maxprob_host, uint64_t seed, int B, int K, int V, spec_sched_mode_t mode,
+    float threshold, long long budget, void *target_dev, void *draft_dev,
+    int32_t *draft_tokens_dev, float *temperature_dev, float *maxprob_dev, int32_t *verify_len_dev,
+    int32_t *out_tokens_dev, int32_t *accept_len_dev, int32_t *out_tokens_host,
+    int32_t *accept_len_host, int32_t *verify_len_host, void *workspace, size_t workspace_bytes,
+    uint32_t *dev_status, void *stream, size_t *h2d_bytes);
+
+/*
  * spec_debug_force_wait_timeout -- diagnostics only: while enabled (1), every
  * warp of the bulk-copy kernels in later spec_verify calls (any device) first
  * waits on a barrier nothing completes; that bounded wait runs out after 1 ms

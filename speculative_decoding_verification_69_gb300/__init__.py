@@ -90,6 +90,12 @@ def load_library():
                                                        vp, ctypes.c_size_t, u32p, vp,
                                                        ctypes.POINTER(ctypes.c_size_t)])
     L.spec_verify_from_host.restype = ctypes.c_int
+    L.spec_verify_scheduled_from_host.argtypes = (
+        [vp, vp, ctypes.c_int, i32p, f32p, f32p, ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
+         ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_longlong, vp, vp, i32p, f32p, f32p,
+         i32p, i32p, i32p, i32p, i32p, i32p, vp, ctypes.c_size_t, u32p, vp,
+         ctypes.POINTER(ctypes.c_size_t)])
+    L.spec_verify_scheduled_from_host.restype = ctypes.c_int
     L.spec_profile_events.argtypes = [vp, vp]
     L.spec_profile_events.restype = None
     L.spec_verify_kernel_count.argtypes = []
@@ -109,6 +115,7 @@ def exported_symbols():
             "spec_draft_confidence", "spec_schedule_budget", "spec_verify_scheduled",
             "spec_lmhead_workspace_bytes", "spec_verify_lmhead",
             "spec_schedule_len", "spec_verify_noalloc", "spec_verify_from_host",
+            "spec_verify_scheduled_from_host",
             "spec_profile_events", "spec_debug_force_wait_timeout",
             "spec_verify_kernel_count", "spec_status_str"]
 
@@ -269,6 +276,7 @@ class HostVerifier:
                 tokens=torch.empty((B, K), dtype=torch.int32, device=dev),
                 verify_len=torch.empty((B,), dtype=torch.int32, device=dev),
                 temperature=torch.empty((B,), dtype=torch.float32, device=dev),
+                maxprob=torch.empty((B, K), dtype=torch.float32, device=dev),
                 out_tokens=torch.empty((B, K + 1), dtype=torch.int32, device=dev),
                 accept_len=torch.empty((B,), dtype=torch.int32, device=dev),
                 ws=torch.empty(max(n, 256), dtype=torch.uint8, device=dev))
@@ -310,6 +318,44 @@ class HostVerifier:
                 ctypes.byref(nbytes)))
         self.last_h2d_bytes = int(nbytes.value)
         return out_tokens, accept_len
+
+    def scheduled(self, target, draft, tokens, temperature, seed, draft_maxprob, *,
+                  threshold=None, budget=None, out_tokens=None, accept_len=None,
+                  verify_len_out=None, dev_status=None, stream=None):
+        """spec_verify_scheduled_from_host: lengths from the threshold or budget
+        schedule of the given host confidences, formed on the device and read
+        back (the call waits for them), then only the rows they need copied.
+        Returns (out_tokens, accept_len, verify_len) in host memory."""
+        L = load_library()
+        if (threshold is None) == (budget is None):
+            raise ValueError("give exactly one of threshold, budget")
+        B, K1, V = target.shape
+        K = K1 - 1
+        for t in (target, draft, tokens, temperature, draft_maxprob):
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError("inputs must be contiguous host tensors")
+        if draft_maxprob.shape != (B, K) or draft_maxprob.dtype != torch.float32:
+            raise ValueError("draft_maxprob must be float32 [B, K]")
+        d = self._buffers(B, K, V, target.dtype)
+        if out_tokens is None:
+            out_tokens = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+        if accept_len is None:
+            accept_len = torch.empty((B,), dtype=torch.int32).pin_memory()
+        if verify_len_out is None:
+            verify_len_out = torch.empty((B,), dtype=torch.int32).pin_memory()
+        mode = 0 if threshold is not None else 1
+        nbytes = ctypes.c_size_t(0)
+        with torch.cuda.device(self.device):
+            _check(L.spec_verify_scheduled_from_host(
+                _ptr(target), _ptr(draft), _dtype_code(target), _ptr(tokens), _ptr(temperature),
+                _ptr(draft_maxprob), int(seed) & 0xFFFFFFFFFFFFFFFF, B, K, V, mode,
+                float(threshold or 0.0), int(budget or 0), _ptr(d["target"]), _ptr(d["draft"]),
+                _ptr(d["tokens"]), _ptr(d["temperature"]), _ptr(d["maxprob"]),
+                _ptr(d["verify_len"]), _ptr(d["out_tokens"]), _ptr(d["accept_len"]),
+                _ptr(out_tokens), _ptr(accept_len), _ptr(verify_len_out), _ptr(d["ws"]),
+                d["ws"].numel(), _ptr(dev_status), _stream(stream), ctypes.byref(nbytes)))
+        self.last_h2d_bytes = int(nbytes.value)
+        return out_tokens, accept_len, verify_len_out
 
 
 def draft_confidence(draft, temperature, *, out=None, stream=None, verifier=None):

@@ -3486,6 +3486,54 @@ spec_status_t spec_verify_from_host(
     return SPEC_OK;
 }
 
+spec_status_t spec_verify_scheduled_from_host(
+    const void *target_host, const void *draft_host, spec_dtype_t dtype,
+    const int32_t *draft_tokens_host, const float *temperature_host,
+    const float *draft_maxprob_host, uint64_t seed, int B, int K, int V, spec_sched_mode_t mode,
+    float threshold, long long budget, void *target_dev, void *draft_dev,
+    int32_t *draft_tokens_dev, float *temperature_dev, float *maxprob_dev, int32_t *verify_len_dev,
+    int32_t *out_tokens_dev, int32_t *accept_len_dev, int32_t *out_tokens_host,
+    int32_t *accept_len_host, int32_t *verify_len_host, void *workspace, size_t workspace_bytes,
+    uint32_t *dev_status, void *stream, size_t *h2d_bytes) {
+    if (mode != SPEC_SCHED_THRESHOLD && mode != SPEC_SCHED_BUDGET) return SPEC_ERR_INVALID_ARG;
+    if (!draft_maxprob_host || !maxprob_dev || !verify_len_dev || !verify_len_host || !target_host ||
+        !draft_host || !draft_tokens_host || !temperature_host || !draft_tokens_dev ||
+        !temperature_dev || !out_tokens_host || !accept_len_host)
+        return SPEC_ERR_INVALID_ARG;
+    {  // every argument check of the step before the first copy
+        sv::Params P;
+        sv::Layout L;
+        const spec_status_t st = sv::step_params(P, target_dev, draft_dev, dtype, draft_tokens_dev,
+                                                 verify_len_dev, temperature_dev, seed, B, K, V,
+                                                 out_tokens_dev, accept_len_dev, workspace,
+                                                 workspace_bytes, dev_status, L);
+        if (st != SPEC_OK) return st;
+    }
+    if (mode == SPEC_SCHED_BUDGET && (long long)B * K > sv::kBudgetMaxN) return SPEC_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t mp_bytes = (size_t)B * K * sizeof(float);
+    if (cudaMemcpyAsync(maxprob_dev, draft_maxprob_host, mp_bytes, cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+        return SPEC_ERR_CUDA;
+    const spec_status_t ss = mode == SPEC_SCHED_THRESHOLD
+                                 ? spec_schedule_len(maxprob_dev, threshold, B, K, verify_len_dev, stream)
+                                 : spec_schedule_budget(maxprob_dev, B, K, budget, verify_len_dev, stream);
+    if (ss != SPEC_OK) return ss;
+    // the lengths decide which rows cross the host link: wait for them
+    if (cudaMemcpyAsync(verify_len_host, verify_len_dev, (size_t)B * sizeof(int32_t),
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    size_t n = 0;
+    const spec_status_t st = spec_verify_from_host(
+        target_host, draft_host, dtype, draft_tokens_host, verify_len_host, temperature_host, seed, B,
+        K, V, target_dev, draft_dev, draft_tokens_dev, verify_len_dev, temperature_dev, out_tokens_dev,
+        accept_len_dev, out_tokens_host, accept_len_host, workspace, workspace_bytes, dev_status,
+        stream, &n);
+    if (h2d_bytes) *h2d_bytes = n + mp_bytes;
+    return st;
+}
+
 void spec_profile_events(void *ev_start, void *ev_end) {
     if (ev_start && ev_end) {
         sv::g_prof_start = static_cast<cudaEvent_t>(ev_start);

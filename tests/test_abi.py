@@ -117,6 +117,31 @@ def test_from_host_validation_without_gpu(lib):
     assert call(ws=None) == 4 and call(wsb=16) == 4
 
 
+def test_scheduled_from_host_validation_without_gpu(lib):
+    """spec_verify_scheduled_from_host checks every argument before its first copy."""
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    base = dict(th=fake, dh=fake, dt=1, tokh=fake, Th=fake, mph=fake, seed=1, B=2, K=4, V=100,
+                mode=0, thr=0.3, budget=3, td=fake, dd=fake, tokd=fake, Td=fake, mpd=fake, vld=fake,
+                od=fake, ad=fake, oh=fake, ah=fake, vlh=fake, ws=ctypes.c_void_p(0x10000),
+                wsb=1 << 30, st=None, nb=None)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return lib.spec_verify_scheduled_from_host(
+            a["th"], a["dh"], a["dt"], a["tokh"], a["Th"], a["mph"], a["seed"], a["B"], a["K"],
+            a["V"], a["mode"], a["thr"], a["budget"], a["td"], a["dd"], a["tokd"], a["Td"],
+            a["mpd"], a["vld"], a["od"], a["ad"], a["oh"], a["ah"], a["vlh"], a["ws"], a["wsb"],
+            a["st"], None, a["nb"])
+
+    for k in ("th", "dh", "tokh", "Th", "mph", "td", "dd", "tokd", "Td", "mpd", "vld", "od", "ad",
+              "oh", "ah", "vlh"):
+        assert call(**{k: None}) == 1, k
+    assert call(mode=2) == 1
+    assert call(B=0) == 1 and call(K=33) == 1 and call(dt=5) == 2
+    assert call(ws=None) == 4
+    assert call(mode=1, B=200_000, K=32) == 2          # budget selection over more than 2^22 positions
+
+
 def test_tree_host_validation_without_gpu(lib):
     """The tree entry points reject bad sizes, null pointers, misaligned logits
     and small workspaces on the host, before any CUDA call."""

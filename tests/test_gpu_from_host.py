@@ -89,3 +89,40 @@ def test_no_lengths_and_scalar_rows(sv, dtype, V):
 def test_full_size_workload(sv):
     """B=32, K=8, V=151936 bf16 (every row of every request read)."""
     _compare(sv, workloads.make_inputs(1), poison=False)
+
+
+@pytest.mark.parametrize("cfg,B,sched", [(3, 64, "threshold"), (3, 64, "budget"), (4, 48, "threshold"),
+                                         (0, 1, "budget")])
+def test_scheduled_from_host(sv, cfg, B, sched):
+    """Lengths from the schedule of given confidences formed on the device and
+    read back, then only their rows copied: the outputs, lengths and status
+    equal spec_verify_scheduled's, with the unread device rows set to NaN, and
+    the bytes copied are the confidences, the listed rows and the small arrays."""
+    inp = workloads.make_inputs(cfg, rep=8, B=B)
+    K = inp["tokens"].shape[1]
+    if "draft_maxprob" not in inp:
+        inp["draft_maxprob"] = sv.draft_confidence(inp["draft"], inp["temperature"])
+    kw = dict(threshold=0.3) if sched == "threshold" else dict(budget=max(1, (K * B) // 3))
+    st_d = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o_d, a_d, vl_d, _ = sv.verify_scheduled(inp["target"], inp["draft"], inp["tokens"],
+                                            inp["temperature"], inp["seed"],
+                                            draft_maxprob=inp["draft_maxprob"], dev_status=st_d,
+                                            **kw)
+    torch.cuda.synchronize()
+    h = _host(inp)
+    mp_h = inp["draft_maxprob"].cpu().pin_memory()
+    hv = sv.HostVerifier()
+    hv.scheduled(h["target"], h["draft"], h["tokens"], h["temperature"], inp["seed"], mp_h, **kw)
+    torch.cuda.synchronize()
+    d = hv._buffers(B, K, inp["target"].shape[2], inp["target"].dtype)
+    d["target"].fill_(float("nan"))
+    d["draft"].fill_(float("nan"))
+    st_h = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o_h, a_h, vl_h = hv.scheduled(h["target"], h["draft"], h["tokens"], h["temperature"],
+                                  inp["seed"], mp_h, dev_status=st_h, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(vl_h, vl_d.cpu())
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(a_h, a_d.cpu())
+    assert int(st_h.item()) == int(st_d.item())
+    want = dict(inp, verify_len=vl_d)
+    assert hv.last_h2d_bytes == _expected_bytes(want) + B * K * 4
